@@ -1,0 +1,170 @@
+/*
+ * evo_attn.h — C ABI of the GB300 (sm_103a) memory-efficient biased
+ * Evoformer attention library (libevo_attn.so).
+ *
+ * What it computes.  For each batch b, row n and head h, with L queries and
+ * L keys of head dimension D:
+ *
+ *     O = softmax(Q Kᵀ · D^-1/2 + bias1 + bias2) · V
+ *
+ * with the key mask bias1 broadcast over heads and queries and the pair
+ * bias bias2 shared by all N rows.  Source: the web page "DeepSpeed4Science
+ * 技术指南：AI4Science 大模型长序列训练与 Evoformer 内存高效注意力内核实战"
+ * — §3.5 (the reference test scales Q·Kᵀ, adds the bias, applies softmax and
+ * multiplies by V), §3.6 (the layouts below and the four Evoformer usages),
+ * §3.7 (inputs fp16/bf16 on the device; bias1 shaped (B, N, 1, 1, L) and
+ * bias2 (B, 1, H, L, L); the forward saves an fp32 log-sum-exp for the
+ * backward; the backward forms delta first, then dQ, dK, dV and the bias
+ * gradients, accumulating bias gradients in fp32 before casting back).
+ *
+ * Layouts (all dense, row-major, no padding):
+ *     q, k, v, out, dout, dq, dk, dv : [B, N, L, H, D]   dtype
+ *     bias1 (key mask)               : [B, N, 1, 1, L]   dtype, nullable
+ *     bias2 (pair bias)              : [B, 1, H, L, L]   dtype, nullable
+ *     dbias2                         : [B, 1, H, L, L]   dtype
+ *     lse                            : [B, N, H, L]      float32, natural log
+ *
+ * Readings where the page is silent: the scale is D^-1/2 with D the true head
+ * dimension; lse is the natural log of the scaled, biased scores; a query row
+ * whose every key score is -inf (an fp16 -1e9 mask over all keys) has an
+ * empty softmax: its output row is 0, its lse is -inf and it contributes no
+ * gradient.
+ *
+ * Supported: B, N, H >= 1; 1 <= L <= 32768; D in {8, 16, 24, ..., 64};
+ * fp16 or bf16 with fp32 accumulation.  The page's own limits (forward
+ * sequence length > 16, backward head dimension <= 64) are relaxed to L >= 1
+ * and kept at D <= 64.
+ *
+ * Conventions for every entry point:
+ *  - Pointers named as device pointers must point to memory of the current
+ *    CUDA device; the caller owns all buffers.  The library keeps no
+ *    per-call state and allocates no device memory.
+ *  - Device buffers of the tensors above must be 16-byte aligned, except
+ *    bias1 (2-byte) and lse (4-byte); the backward workspace 256-byte.
+ *  - Outputs are overwritten, never accumulated into, and must not overlap
+ *    any input (EVO_ERR_ALIASING).
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *    default stream).  Argument errors are reported synchronously, before
+ *    anything is launched, and leave every buffer untouched.  A failed kernel
+ *    launch returns EVO_ERR_CUDA.
+ *  - Every device-side wait is bounded.  A wait that runs out sets a device
+ *    status word instead of hanging; evo_attn_device_status() reports it.
+ */
+#ifndef EVO_ATTN_H
+#define EVO_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define EVO_ATTN_ABI_VERSION 1
+
+/* Every entry point below is exported from libevo_attn.so; nothing else is. */
+#if defined(__GNUC__)
+#define EVO_API __attribute__((visibility("default")))
+#else
+#define EVO_API
+#endif
+
+typedef enum {
+  EVO_OK = 0,
+  EVO_ERR_NULL_POINTER = 1,        /* a required pointer is NULL                    */
+  EVO_ERR_BAD_SHAPE = 2,           /* B,N,H < 1, L outside [1, 32768], D not 8..64 step 8,
+                                      or an element count that overflows           */
+  EVO_ERR_BAD_DTYPE = 3,           /* dtype is neither EVO_F16 nor EVO_BF16         */
+  EVO_ERR_MISALIGNED = 4,          /* a pointer breaks the alignment rule above     */
+  EVO_ERR_WORKSPACE_TOO_SMALL = 5, /* workspace_bytes < evo_attn_bwd_workspace_bytes */
+  EVO_ERR_ARCH = 6,                /* current device is not compute capability 10.3 */
+  EVO_ERR_CUDA = 7,                /* a CUDA runtime/driver call or launch failed   */
+  EVO_ERR_DEVICE_TIMEOUT = 8,      /* a bounded device-side wait ran out            */
+  EVO_ERR_ALIASING = 9,            /* an output overlaps an input                   */
+  EVO_ERR_BAD_ARGUMENT = 10        /* any other invalid argument (e.g. dbias2 given
+                                      without bias2, or missing with bias2)         */
+} evo_status_t;
+
+typedef enum { EVO_F16 = 0, EVO_BF16 = 1 } evo_dtype_t;
+
+typedef struct {
+  int64_t B, N, L, H, D;
+} evo_shape_t;
+
+/* ABI version of the loaded library (EVO_ATTN_ABI_VERSION at build time). */
+EVO_API int evo_attn_abi_version(void);
+
+/* Static, NUL-terminated description of a status code. */
+EVO_API const char* evo_status_string(evo_status_t status);
+
+/*
+ * Forward (page §3.5-§3.7).  Device pointers:
+ *   q, k, v  [B,N,L,H,D] inputs; bias1 [B,N,1,1,L] or NULL; bias2 [B,1,H,L,L] or NULL;
+ *   out      [B,N,L,H,D] output O, rounded to nearest in dtype;
+ *   lse      [B,N,H,L]   fp32 output, natural-log log-sum-exp of each query row.
+ * The L×L score matrix never exists in device memory.
+ */
+EVO_API evo_status_t evo_attn_fwd(const void* q, const void* k, const void* v,
+                          const void* bias1, const void* bias2,
+                          void* out, float* lse,
+                          evo_shape_t shape, evo_dtype_t dtype, void* stream);
+
+/*
+ * Bytes of device workspace the backward needs for this problem (0 on a bad
+ * shape).  It holds the fp32 row terms delta [B,N,H,L], the fp32 dQ
+ * accumulator [B,N,L,H,D] and, when has_bias2 != 0, the fp32 per-group
+ * partial sums of the pair-bias gradient.  Depends only on its arguments.
+ */
+EVO_API size_t evo_attn_bwd_workspace_bytes(evo_shape_t shape, evo_dtype_t dtype, int has_bias2);
+
+/*
+ * Backward (page §3.7: delta first, then dQ/dK/dV and the bias gradient).
+ * Device pointers:
+ *   q, k, v, bias1, bias2 : the forward's inputs (bias1/bias2 nullable as there);
+ *   out, lse              : the forward's outputs;
+ *   dout                  : [B,N,L,H,D] gradient of the loss with respect to out;
+ *   dq, dk, dv            : [B,N,L,H,D] outputs;
+ *   dbias2                : [B,1,H,L,L] output, required iff bias2 != NULL.
+ *                           Summed over N in fp32 in a fixed order (two stages:
+ *                           per-group partials, then a fixed-order sum of the
+ *                           groups), so repeated calls give identical bytes;
+ *   workspace             : >= evo_attn_bwd_workspace_bytes(...) bytes, caller-owned,
+ *                           contents need not be initialised; clobbered.
+ * The gradient of bias1 is not produced by this version.
+ */
+EVO_API evo_status_t evo_attn_bwd(const void* q, const void* k, const void* v,
+                          const void* bias1, const void* bias2,
+                          const void* out, const float* lse, const void* dout,
+                          void* dq, void* dk, void* dv, void* dbias2,
+                          void* workspace, size_t workspace_bytes,
+                          evo_shape_t shape, evo_dtype_t dtype, void* stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the library's device status
+ * word on the current device: EVO_OK, or EVO_ERR_DEVICE_TIMEOUT if some
+ * kernel since the last call gave up on a bounded wait (its outputs are then
+ * undefined).  EVO_ERR_CUDA if the synchronisation itself failed.
+ */
+EVO_API evo_status_t evo_attn_device_status(void* stream);
+
+/*
+ * Upper bound, in nanoseconds, on every device-side wait of later launches
+ * (default 2e9).  Values below 1000 are raised to 1000.  Host-side setting,
+ * process-wide; meant for tests of the timeout path.
+ */
+EVO_API void evo_attn_set_wait_limit_ns(uint64_t ns);
+
+/*
+ * Self-test of the bounded-wait path: launches one block that waits on a
+ * shared-memory barrier nothing ever signals, with the wait limit given here
+ * (clamped to [1000 ns, 1e9 ns]).  The block gives up, records
+ * EVO_ERR_DEVICE_TIMEOUT in the status word and exits; read it with
+ * evo_attn_device_status().  Faults nothing and leaves the context usable.
+ */
+EVO_API evo_status_t evo_attn_selftest_wait_timeout(uint64_t limit_ns, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EVO_ATTN_H */

@@ -1,0 +1,390 @@
+// evo_host.cu — the C ABI of libevo_attn.so (declared in include/evo_attn.h):
+// argument validation, TMA tensor-map construction, workspace carving and
+// dispatch to the sm_103a kernels.  The operation is the one defined on the
+// web page "DeepSpeed4Science 技术指南：AI4Science 大模型长序列训练与 Evoformer
+// 内存高效注意力内核实战" §3.5-§3.7; §3.7 also fixes the validation this layer
+// performs (bias1 (B, N, 1, 1, L), bias2 (B, 1, H, L, L), fp16/bf16 inputs,
+// device-resident tensors, backward head dimension <= 64).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "evo_attn.h"
+#include "evo_internal.h"
+#include "evo_ptx.cuh"
+
+namespace evo {
+
+// Device status word: kernels record a bounded wait that ran out here.
+__device__ int g_evo_status = 0;
+
+static std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  std::once_flag once;
+  int cc_major = 0, cc_minor = 0, sms = 0;
+  int* status = nullptr;
+  cudaError_t err = cudaSuccess;
+};
+DeviceInfo g_dev[kMaxDevices];
+
+DeviceInfo* device_info(int* dev_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  DeviceInfo& d = g_dev[dev];
+  std::call_once(d.once, [&d, dev]() {
+    cudaError_t e = cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status), g_evo_status);
+    d.err = e;
+  });
+  if (dev_out) *dev_out = dev;
+  return &d;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }();
+  return fn;
+}
+
+bool encode(CUtensorMap* m, const void* base, bool bf16, int rank, const cuuint64_t* dims,
+            const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle swz) {
+  auto fn = tmap_encoder();
+  if (!fn) return false;
+  cuuint32_t es[5] = {1, 1, 1, 1, 1};
+  CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                  static_cast<cuuint32_t>(rank), const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int padded_dim(int64_t D) { return D <= 16 ? 16 : (D <= 32 ? 32 : 64); }
+
+// [B,N,L,H,D] viewed as 4-D (D, H, L, B*N); box (DP, 1, 128, 1), swizzle = 2*DP bytes.
+bool map_qkv(CUtensorMap* m, const void* p, const evo_shape_t& s, bool bf16) {
+  const int DP = padded_dim(s.D);
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(s.D), static_cast<cuuint64_t>(s.H), static_cast<cuuint64_t>(s.L),
+                        static_cast<cuuint64_t>(s.B * s.N)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(s.D * 2), static_cast<cuuint64_t>(s.H * s.D * 2),
+                           static_cast<cuuint64_t>(s.L * s.H * s.D * 2)};
+  cuuint32_t box[4] = {static_cast<cuuint32_t>(DP), 1, static_cast<cuuint32_t>(kTile), 1};
+  const CUtensorMapSwizzle swz = DP == 64   ? CU_TENSOR_MAP_SWIZZLE_128B
+                                 : DP == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                            : CU_TENSOR_MAP_SWIZZLE_32B;
+  return encode(m, p, bf16, 4, dims, strides, box, swz);
+}
+
+// [B,1,H,L,L] viewed as 3-D (key j, query i, B*H).
+bool map_bias2(CUtensorMap* m, const void* p, const evo_shape_t& s, bool bf16, int box_j, CUtensorMapSwizzle swz) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(s.L), static_cast<cuuint64_t>(s.L),
+                        static_cast<cuuint64_t>(s.B * s.H)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(s.L * 2), static_cast<cuuint64_t>(s.L * s.L * 2)};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(box_j), static_cast<cuuint32_t>(kTile), 1};
+  return encode(m, p, bf16, 3, dims, strides, box, swz);
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+struct Range {
+  const void* p;
+  size_t bytes;
+};
+bool overlap(const Range& a, const Range& b) {
+  if (!a.p || !b.p || !a.bytes || !b.bytes) return false;
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a.p), b0 = reinterpret_cast<uintptr_t>(b.p);
+  return a0 < b0 + b.bytes && b0 < a0 + a.bytes;
+}
+
+evo_status_t check_shape(const evo_shape_t& s) {
+  if (s.B < 1 || s.N < 1 || s.H < 1 || s.L < 1 || s.L > 32768) return EVO_ERR_BAD_SHAPE;
+  if (s.D < 8 || s.D > 64 || (s.D % 8) != 0) return EVO_ERR_BAD_SHAPE;
+  const int64_t lim = int64_t(1) << 31;
+  if (s.B > lim / s.N || s.B > lim / s.H) return EVO_ERR_BAD_SHAPE;  // TMA coordinates are int32
+  // element counts must stay far from size_t overflow: B*N*L*H*D and B*H*L*L below 2^44
+  const double e1 = double(s.B) * s.N * s.L * s.H * s.D, e2 = double(s.B) * s.H * s.L * s.L;
+  if (e1 >= 17592186044416.0 || e2 >= 17592186044416.0) return EVO_ERR_BAD_SHAPE;
+  if (double(s.B) * s.N * s.H * ((s.L + kTile - 1) / kTile) >= 9.0e18) return EVO_ERR_BAD_SHAPE;
+  return EVO_OK;
+}
+
+evo_status_t check_device(DeviceInfo** out) {
+  DeviceInfo* d = device_info(nullptr);
+  if (!d || d->err != cudaSuccess) return EVO_ERR_CUDA;
+  if (d->cc_major != 10 || d->cc_minor != 3) return EVO_ERR_ARCH;
+  *out = d;
+  return EVO_OK;
+}
+
+size_t qkv_bytes(const evo_shape_t& s) { return size_t(s.B) * s.N * s.L * s.H * s.D * 2; }
+size_t lse_bytes(const evo_shape_t& s) { return size_t(s.B) * s.N * s.H * s.L * 4; }
+size_t bias1_bytes(const evo_shape_t& s) { return size_t(s.B) * s.N * s.L * 2; }
+size_t bias2_bytes(const evo_shape_t& s) { return size_t(s.B) * s.H * s.L * s.L * 2; }
+size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// n-groups of the deterministic two-stage pair-bias gradient: enough
+// (b, h, q-tile, k-tile, group) blocks for two waves over 152 SMs.
+void bwd_groups(const evo_shape_t& s, int* groups, int* group_size) {
+  const int64_t QT = (s.L + kTile - 1) / kTile;
+  const int64_t tiles = s.B * s.H * QT * QT;
+  int64_t g = (304 + tiles - 1) / tiles;
+  if (g < 1) g = 1;
+  if (g > s.N) g = s.N;
+  int64_t gs = (s.N + g - 1) / g;
+  g = (s.N + gs - 1) / gs;
+  *groups = static_cast<int>(g);
+  *group_size = static_cast<int>(gs);
+}
+
+struct WsLayout {
+  size_t delta, dq_acc, db2, total;
+};
+WsLayout ws_layout(const evo_shape_t& s, bool has_bias2) {
+  WsLayout w{};
+  size_t off = 0;
+  w.delta = off;
+  off += round256(size_t(s.B) * s.N * s.H * s.L * 4);
+  w.dq_acc = off;
+  off += round256(size_t(s.B) * s.N * s.L * s.H * s.D * 4);
+  w.db2 = off;
+  if (has_bias2) {
+    int g = 0, gs = 0;
+    bwd_groups(s, &g, &gs);
+    off += round256(size_t(g) * s.B * s.H * s.L * s.L * 4);
+  }
+  w.total = off;
+  return w;
+}
+
+}  // namespace
+
+int num_sms() {
+  DeviceInfo* d = device_info(nullptr);
+  return (d && d->sms > 0) ? d->sms : 148;
+}
+
+// ------------------------------------------------------------ self-test kernel
+__global__ void evo_wait_selftest_kernel(uint64_t limit_ns, int* status) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ volatile int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(smem_u32(&bar), 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  const WaitGuard g{limit_ns, status, &abort_flag};
+  // Nothing ever arrives on `bar`: the wait runs out and records the timeout.
+  mbar_wait(smem_u32(&bar), 0, g);
+}
+
+cudaError_t launch_wait_selftest(uint64_t limit_ns, int* status, cudaStream_t st) {
+  evo_wait_selftest_kernel<<<1, 32, 0, st>>>(limit_ns, status);
+  return cudaGetLastError();
+}
+
+}  // namespace evo
+
+using namespace evo;
+
+extern "C" {
+
+int evo_attn_abi_version(void) { return EVO_ATTN_ABI_VERSION; }
+
+const char* evo_status_string(evo_status_t s) {
+  switch (s) {
+    case EVO_OK: return "ok";
+    case EVO_ERR_NULL_POINTER: return "a required pointer is NULL";
+    case EVO_ERR_BAD_SHAPE: return "unsupported shape (B,N,H>=1, 1<=L<=32768, D in 8..64 step 8)";
+    case EVO_ERR_BAD_DTYPE: return "dtype must be EVO_F16 or EVO_BF16";
+    case EVO_ERR_MISALIGNED: return "a pointer is not suitably aligned (16 B tensors, 2 B bias1, 4 B lse, 256 B workspace)";
+    case EVO_ERR_WORKSPACE_TOO_SMALL: return "workspace smaller than evo_attn_bwd_workspace_bytes()";
+    case EVO_ERR_ARCH: return "current device is not compute capability 10.3 (GB300, sm_103a)";
+    case EVO_ERR_CUDA: return "a CUDA call or kernel launch failed";
+    case EVO_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait ran out; outputs are undefined";
+    case EVO_ERR_ALIASING: return "an output buffer overlaps an input buffer";
+    case EVO_ERR_BAD_ARGUMENT: return "invalid argument combination";
+  }
+  return "unknown status";
+}
+
+void evo_attn_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns < 1000 ? 1000 : ns); }
+
+evo_status_t evo_attn_fwd(const void* q, const void* k, const void* v, const void* bias1, const void* bias2,
+                          void* out, float* lse, evo_shape_t shape, evo_dtype_t dtype, void* stream) {
+  if (!q || !k || !v || !out || !lse) return EVO_ERR_NULL_POINTER;
+  if (dtype != EVO_F16 && dtype != EVO_BF16) return EVO_ERR_BAD_DTYPE;
+  evo_status_t st = check_shape(shape);
+  if (st != EVO_OK) return st;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) || !aligned(lse, 4) ||
+      (bias1 && !aligned(bias1, 2)) || (bias2 && !aligned(bias2, 16)))
+    return EVO_ERR_MISALIGNED;
+  const Range ins[5] = {{q, qkv_bytes(shape)}, {k, qkv_bytes(shape)}, {v, qkv_bytes(shape)},
+                        {bias1, bias1 ? bias1_bytes(shape) : 0}, {bias2, bias2 ? bias2_bytes(shape) : 0}};
+  const Range outs[2] = {{out, qkv_bytes(shape)}, {lse, lse_bytes(shape)}};
+  for (const Range& o : outs)
+    for (const Range& i : ins)
+      if (overlap(o, i)) return EVO_ERR_ALIASING;
+  if (overlap(outs[0], outs[1])) return EVO_ERR_ALIASING;
+  DeviceInfo* dev = nullptr;
+  if ((st = check_device(&dev)) != EVO_OK) return st;
+
+  const bool bf16 = dtype == EVO_BF16;
+  FwdArgs a;
+  std::memset(&a, 0, sizeof(a));
+  if (!map_qkv(&a.tq, q, shape, bf16) || !map_qkv(&a.tk, k, shape, bf16) || !map_qkv(&a.tv, v, shape, bf16))
+    return EVO_ERR_CUDA;
+  a.bias2_mode = kBias2None;
+  if (bias2) {
+    if (shape.L % 8 == 0) {
+      if (!map_bias2(&a.tb2, bias2, shape, bf16, 64, CU_TENSOR_MAP_SWIZZLE_128B)) return EVO_ERR_CUDA;
+      a.bias2_mode = kBias2Tma;
+    } else {
+      a.bias2_mode = kBias2Loads;
+    }
+  }
+  a.bias1 = static_cast<const uint16_t*>(bias1);
+  a.bias2 = static_cast<const uint16_t*>(bias2);
+  a.out = static_cast<uint16_t*>(out);
+  a.lse = lse;
+  a.B = static_cast<int>(shape.B);
+  a.N = static_cast<int>(shape.N);
+  a.L = static_cast<int>(shape.L);
+  a.H = static_cast<int>(shape.H);
+  a.D = static_cast<int>(shape.D);
+  a.QT = static_cast<int>((shape.L + kTile - 1) / kTile);
+  a.items = shape.B * shape.N * shape.H * a.QT;
+  a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(shape.D)));
+  a.wait_ns = g_wait_limit_ns.load();
+  a.status = dev->status;
+  cudaError_t e = launch_fwd(a, padded_dim(shape.D), bf16, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? EVO_OK : EVO_ERR_CUDA;
+}
+
+size_t evo_attn_bwd_workspace_bytes(evo_shape_t shape, evo_dtype_t dtype, int has_bias2) {
+  if (dtype != EVO_F16 && dtype != EVO_BF16) return 0;
+  if (check_shape(shape) != EVO_OK) return 0;
+  return ws_layout(shape, has_bias2 != 0).total;
+}
+
+evo_status_t evo_attn_bwd(const void* q, const void* k, const void* v, const void* bias1, const void* bias2,
+                          const void* out, const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                          void* dbias2, void* workspace, size_t workspace_bytes, evo_shape_t shape,
+                          evo_dtype_t dtype, void* stream) {
+  if (!q || !k || !v || !out || !lse || !dout || !dq || !dk || !dv || !workspace) return EVO_ERR_NULL_POINTER;
+  if (dtype != EVO_F16 && dtype != EVO_BF16) return EVO_ERR_BAD_DTYPE;
+  evo_status_t st = check_shape(shape);
+  if (st != EVO_OK) return st;
+  if ((bias2 != nullptr) != (dbias2 != nullptr)) return EVO_ERR_BAD_ARGUMENT;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) || !aligned(dout, 16) ||
+      !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(lse, 4) ||
+      (bias1 && !aligned(bias1, 2)) || (bias2 && !aligned(bias2, 16)) || (dbias2 && !aligned(dbias2, 16)) ||
+      !aligned(workspace, 256))
+    return EVO_ERR_MISALIGNED;
+  const WsLayout w = ws_layout(shape, bias2 != nullptr);
+  if (workspace_bytes < w.total) return EVO_ERR_WORKSPACE_TOO_SMALL;
+  const size_t nq = qkv_bytes(shape);
+  const Range ins[8] = {{q, nq}, {k, nq}, {v, nq}, {bias1, bias1 ? bias1_bytes(shape) : 0},
+                        {bias2, bias2 ? bias2_bytes(shape) : 0}, {out, nq}, {lse, lse_bytes(shape)}, {dout, nq}};
+  const Range outs[5] = {{dq, nq}, {dk, nq}, {dv, nq}, {dbias2, dbias2 ? bias2_bytes(shape) : 0},
+                         {workspace, w.total}};
+  for (int i = 0; i < 5; ++i) {
+    for (const Range& r : ins)
+      if (overlap(outs[i], r)) return EVO_ERR_ALIASING;
+    for (int j = i + 1; j < 5; ++j)
+      if (overlap(outs[i], outs[j])) return EVO_ERR_ALIASING;
+  }
+  DeviceInfo* dev = nullptr;
+  if ((st = check_device(&dev)) != EVO_OK) return st;
+
+  const bool bf16 = dtype == EVO_BF16;
+  BwdArgs a;
+  std::memset(&a, 0, sizeof(a));
+  if (!map_qkv(&a.tq, q, shape, bf16) || !map_qkv(&a.tk, k, shape, bf16) || !map_qkv(&a.tv, v, shape, bf16) ||
+      !map_qkv(&a.tdo, dout, shape, bf16))
+    return EVO_ERR_CUDA;
+  a.bias2_mode = kBias2None;
+  if (bias2) {
+    if (shape.L % 8 == 0) {
+      if (!map_bias2(&a.tb2t, bias2, shape, bf16, 128, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+          !map_bias2(&a.tb2, bias2, shape, bf16, 64, CU_TENSOR_MAP_SWIZZLE_128B))
+        return EVO_ERR_CUDA;
+      a.bias2_mode = kBias2Tma;
+    } else {
+      a.bias2_mode = kBias2Loads;
+    }
+  }
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  a.q = static_cast<const uint16_t*>(q);
+  a.out = static_cast<const uint16_t*>(out);
+  a.dout = static_cast<const uint16_t*>(dout);
+  a.bias1 = static_cast<const uint16_t*>(bias1);
+  a.bias2 = static_cast<const uint16_t*>(bias2);
+  a.lse = lse;
+  a.dq = static_cast<uint16_t*>(dq);
+  a.dk = static_cast<uint16_t*>(dk);
+  a.dv = static_cast<uint16_t*>(dv);
+  a.dbias2 = static_cast<uint16_t*>(dbias2);
+  a.delta = reinterpret_cast<float*>(ws + w.delta);
+  a.dq_acc = reinterpret_cast<float*>(ws + w.dq_acc);
+  a.db2_part = bias2 ? reinterpret_cast<float*>(ws + w.db2) : nullptr;
+  a.B = static_cast<int>(shape.B);
+  a.N = static_cast<int>(shape.N);
+  a.L = static_cast<int>(shape.L);
+  a.H = static_cast<int>(shape.H);
+  a.D = static_cast<int>(shape.D);
+  a.QT = static_cast<int>((shape.L + kTile - 1) / kTile);
+  bwd_groups(shape, &a.groups, &a.group_size);
+  a.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(shape.D)));
+  a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(shape.D)));
+  a.wait_ns = g_wait_limit_ns.load();
+  a.status = dev->status;
+  cudaError_t e = launch_bwd(a, padded_dim(shape.D), bf16, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? EVO_OK : EVO_ERR_CUDA;
+}
+
+evo_status_t evo_attn_device_status(void* stream) {
+  DeviceInfo* dev = device_info(nullptr);
+  if (!dev || dev->err != cudaSuccess) return EVO_ERR_CUDA;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return EVO_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_evo_status, sizeof(int)) != cudaSuccess) return EVO_ERR_CUDA;
+  if (v != 0) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_evo_status, &zero, sizeof(int)) != cudaSuccess) return EVO_ERR_CUDA;
+    return EVO_ERR_DEVICE_TIMEOUT;
+  }
+  return EVO_OK;
+}
+
+evo_status_t evo_attn_selftest_wait_timeout(uint64_t limit_ns, void* stream) {
+  DeviceInfo* dev = nullptr;
+  evo_status_t st = check_device(&dev);
+  if (st != EVO_OK) return st;
+  if (limit_ns < 1000) limit_ns = 1000;
+  if (limit_ns > 1000000000ull) limit_ns = 1000000000ull;
+  return launch_wait_selftest(limit_ns, dev->status, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? EVO_OK
+             : EVO_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,65 @@
+// evo_internal.h — launch interfaces between the C-ABI host layer
+// (evo_host.cu) and the kernel translation units.  Not part of the ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace evo {
+
+constexpr int kTile = 128;  // queries (and keys) per tile
+
+// How the pair bias reaches shared memory.
+enum Bias2Mode : int { kBias2None = 0, kBias2Tma = 1, kBias2Loads = 2 };
+
+struct FwdArgs {
+  CUtensorMap tq, tk, tv;   // 4-D [B*N][L][H][D] views, box (DP, 1, 128, 1)
+  CUtensorMap tb2;          // 3-D [B*H][L][L] view, box (64, 128, 1), 128B swizzle (kBias2Tma)
+  const uint16_t* bias1;    // [B,N,L] or nullptr
+  const uint16_t* bias2;    // [B,H,L,L] or nullptr
+  uint16_t* out;            // [B,N,L,H,D]
+  float* lse;               // [B,N,H,L]
+  int B, N, L, H, D;
+  int QT;                   // ceil(L / 128)
+  long long items;          // B*N*H*QT work items (b, n, h, query tile)
+  float scale_log2;         // D^-1/2 * log2(e)
+  int bias2_mode;
+  uint64_t wait_ns;
+  int* status;
+};
+
+struct BwdArgs {
+  CUtensorMap tq, tk, tv, tdo;  // 4-D views like the forward, box (DP, 1, 128, 1)
+  CUtensorMap tb2t;             // 3-D [B*H][L][L] view, box (128, 128, 1), no swizzle
+  CUtensorMap tb2;              // 3-D [B*H][L][L] view, box (64, 128, 1), 128B swizzle
+  const uint16_t* q;
+  const uint16_t* out;
+  const uint16_t* dout;
+  const uint16_t* bias1;
+  const uint16_t* bias2;
+  const float* lse;
+  uint16_t* dq;
+  uint16_t* dk;
+  uint16_t* dv;
+  uint16_t* dbias2;
+  float* delta;             // workspace [B,N,H,L]
+  float* dq_acc;            // workspace [B,N,L,H,D]
+  float* db2_part;          // workspace [G][B,H,L,L]
+  int B, N, L, H, D;
+  int QT;
+  int groups;               // G: n-groups of the pair-bias gradient
+  int group_size;           // ceil(N / G)
+  float scale;              // D^-1/2
+  float scale_log2;         // D^-1/2 * log2(e)
+  int bias2_mode;
+  uint64_t wait_ns;
+  int* status;
+};
+
+int num_sms();
+cudaError_t launch_fwd(const FwdArgs& a, int DP, bool bf16, cudaStream_t st);
+cudaError_t launch_bwd(const BwdArgs& a, int DP, bool bf16, cudaStream_t st);
+cudaError_t launch_wait_selftest(uint64_t limit_ns, int* status, cudaStream_t st);
+
+}  // namespace evo

@@ -1,0 +1,186 @@
+"""ctypes binding to libevo_attn.so — argument marshalling only.
+
+Every step of the attention runs in the library's sm_103a kernels; this module
+checks tensor properties, allocates outputs with PyTorch when the caller does
+not pass them, and forwards raw device pointers, sizes and the current CUDA
+stream to the C ABI declared in include/evo_attn.h.  There is no CPU or
+PyTorch fallback: if the library is missing, every call raises.
+
+Names follow the C ABI: ``evo_attn_fwd``, ``evo_attn_bwd``,
+``evo_attn_bwd_workspace_bytes``, ``evo_attn_device_status``,
+``evo_attn_set_wait_limit_ns``, ``evo_attn_selftest_wait_timeout``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_lib", "libevo_attn.so")
+
+EVO_OK = 0
+STATUS_NAMES = {
+    0: "EVO_OK", 1: "EVO_ERR_NULL_POINTER", 2: "EVO_ERR_BAD_SHAPE", 3: "EVO_ERR_BAD_DTYPE",
+    4: "EVO_ERR_MISALIGNED", 5: "EVO_ERR_WORKSPACE_TOO_SMALL", 6: "EVO_ERR_ARCH", 7: "EVO_ERR_CUDA",
+    8: "EVO_ERR_DEVICE_TIMEOUT", 9: "EVO_ERR_ALIASING", 10: "EVO_ERR_BAD_ARGUMENT",
+}
+EXPORTED = ("evo_attn_abi_version", "evo_status_string", "evo_attn_fwd", "evo_attn_bwd_workspace_bytes",
+            "evo_attn_bwd", "evo_attn_device_status", "evo_attn_set_wait_limit_ns",
+            "evo_attn_selftest_wait_timeout")
+
+_DTYPE_CODE = {torch.float16: 0, torch.bfloat16: 1}
+
+
+class EvoShape(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int64), ("N", ctypes.c_int64), ("L", ctypes.c_int64),
+                ("H", ctypes.c_int64), ("D", ctypes.c_int64)]
+
+
+class EvoAttnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        name = STATUS_NAMES.get(status, str(status))
+        msg = f"{where}: {name}"
+        try:
+            msg += f" ({load().evo_status_string(status).decode()})"
+        except Exception:  # pragma: no cover
+            pass
+        super().__init__(msg)
+
+
+_lib = None
+
+
+def load(path: Optional[str] = None):
+    """Load libevo_attn.so (built by memory_efficient_biased_gb300.build); raises if absent."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"libevo_attn.so not built at {p}: run `python -m memory_efficient_biased_gb300.build`")
+    lib = ctypes.CDLL(p)
+    vp, sz, i32, u64 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_uint64
+    lib.evo_attn_abi_version.restype = i32
+    lib.evo_status_string.restype = ctypes.c_char_p
+    lib.evo_status_string.argtypes = [i32]
+    lib.evo_attn_fwd.restype = i32
+    lib.evo_attn_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, EvoShape, i32, vp]
+    lib.evo_attn_bwd_workspace_bytes.restype = sz
+    lib.evo_attn_bwd_workspace_bytes.argtypes = [EvoShape, i32, i32]
+    lib.evo_attn_bwd.restype = i32
+    lib.evo_attn_bwd.argtypes = [vp] * 12 + [vp, sz, EvoShape, i32, vp]
+    lib.evo_attn_device_status.restype = i32
+    lib.evo_attn_device_status.argtypes = [vp]
+    lib.evo_attn_set_wait_limit_ns.restype = None
+    lib.evo_attn_set_wait_limit_ns.argtypes = [u64]
+    lib.evo_attn_selftest_wait_timeout.restype = i32
+    lib.evo_attn_selftest_wait_timeout.argtypes = [u64, vp]
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_ptr(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(t: Optional[torch.Tensor], name: str, shape=None, dtype=None):
+    if t is None:
+        return
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} has dtype {t.dtype}, expected {dtype}")
+
+
+def shape_of(q: torch.Tensor) -> EvoShape:
+    B, N, L, H, D = q.shape
+    return EvoShape(B, N, L, H, D)
+
+
+def evo_attn_fwd(q, k, v, bias1=None, bias2=None, out=None, lse=None, stream=None):
+    """O = softmax(Q Kᵀ D^-1/2 + bias1 + bias2) V and the fp32 lse [B,N,H,L]."""
+    if q.dim() != 5:
+        raise ValueError("q must be [B, N, L, H, D]")
+    B, N, L, H, D = q.shape
+    dt = q.dtype
+    if dt not in _DTYPE_CODE:
+        raise ValueError("inputs must be float16 or bfloat16")
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check(t, n, q.shape, dt)
+    _check(bias1, "bias1", (B, N, 1, 1, L), dt)
+    _check(bias2, "bias2", (B, 1, H, L, L), dt)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, N, H, L), dtype=torch.float32, device=q.device)
+    _check(out, "out", q.shape, dt)
+    _check(lse, "lse", (B, N, H, L), torch.float32)
+    st = load().evo_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(bias1), _ptr(bias2), _ptr(out), _ptr(lse),
+                             shape_of(q), _DTYPE_CODE[dt], _stream_ptr(stream))
+    if st != EVO_OK:
+        raise EvoAttnError(st, "evo_attn_fwd")
+    return out, lse
+
+
+def evo_attn_bwd_workspace_bytes(shape, dtype, has_bias2: bool) -> int:
+    return int(load().evo_attn_bwd_workspace_bytes(EvoShape(*shape), _DTYPE_CODE[dtype], int(bool(has_bias2))))
+
+
+def evo_attn_bwd(q, k, v, bias1, bias2, out, lse, dout, dq=None, dk=None, dv=None, dbias2=None,
+                 workspace=None, stream=None):
+    """dQ, dK, dV (and dbias2 when bias2 is given); returns (dq, dk, dv, dbias2)."""
+    B, N, L, H, D = q.shape
+    dt = q.dtype
+    if dt not in _DTYPE_CODE:
+        raise ValueError("inputs must be float16 or bfloat16")
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out"), (dout, "dout")):
+        _check(t, n, q.shape, dt)
+    _check(bias1, "bias1", (B, N, 1, 1, L), dt)
+    _check(bias2, "bias2", (B, 1, H, L, L), dt)
+    _check(lse, "lse", (B, N, H, L), torch.float32)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    if bias2 is not None and dbias2 is None:
+        dbias2 = torch.empty_like(bias2)
+    for t, n in ((dq, "dq"), (dk, "dk"), (dv, "dv")):
+        _check(t, n, q.shape, dt)
+    _check(dbias2, "dbias2", (B, 1, H, L, L), dt)
+    need = evo_attn_bwd_workspace_bytes(tuple(q.shape), dt, bias2 is not None)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    _check(workspace, "workspace")
+    st = load().evo_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(bias1), _ptr(bias2), _ptr(out), _ptr(lse),
+                             _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dbias2), _ptr(workspace),
+                             workspace.numel() * workspace.element_size(), shape_of(q), _DTYPE_CODE[dt],
+                             _stream_ptr(stream))
+    if st != EVO_OK:
+        raise EvoAttnError(st, "evo_attn_bwd")
+    return dq, dk, dv, dbias2
+
+
+def evo_attn_device_status(stream=None) -> int:
+    return int(load().evo_attn_device_status(_stream_ptr(stream)))
+
+
+def evo_attn_set_wait_limit_ns(ns: int) -> None:
+    load().evo_attn_set_wait_limit_ns(int(ns))
+
+
+def evo_attn_selftest_wait_timeout(limit_ns: int, stream=None) -> int:
+    return int(load().evo_attn_selftest_wait_timeout(int(limit_ns), _stream_ptr(stream)))
