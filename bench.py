@@ -1,0 +1,447 @@
+#!/usr/bin/env python3
+"""Benchmark of memory-efficient biased Evoformer attention on GB300.
+
+One step = forward + backward of O = softmax(Q Kᵀ D^-1/2 + bias1 + bias2) V
+over one batch of the named workload (default: MSA row-wise attention with
+pair bias, B=1, N=256, L=256, H=4, D=32, bf16), i.e. every kernel of the hot
+path: forward, delta/accumulator set-up, main backward, dQ cast, and the two
+deterministic pair-bias gradient stages.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--dtype bf16|fp16]
+
+Prints one JSON line (rank 0).  `value` is whole-job fwd+bwd TFLOP/s with
+nominal FLOPs (forward 4·B·N·H·L²·D, backward 2.5× forward) and inputs
+resident in HBM; `fwd_tflops` is the forward kernel alone; `e2e` is the same
+metric through the host-buffer C-ABI step (evo_attn_step_host) with the
+host↔device copies inside the timed region.  The timed steps are CUDA-graph
+replays over R input replicas whose total exceeds 3× the L2 cache, so no step
+reads inputs left in L2 by the previous one.  Per-kernel times come from CUDA
+events that the library records around each of its launches inside the timed
+replays (evo_attn_profile_events).  `--impl reference` times the fp64 CPU
+oracle on bounded samples of the same workload (it is the reference arm).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+from datetime import datetime
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "Evoformer attn fwd & fwd+bwd TFLOP/s and fraction of GB300 dense tensor peak"
+L2_BYTES = 129 * 1000 * 1000
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# --------------------------------------------------------------------------- helpers
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="msa_row")
+    ap.add_argument("--dtype", default="bf16", choices=("bf16", "fp16"))
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def flops(w):
+    fwd = 4.0 * w.B * w.N * w.H * w.L * w.L * w.D
+    return {"fwd": fwd, "bwd": 2.5 * fwd, "step": 3.5 * fwd}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained")}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = sum(i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas")
+        if n > 0:
+            return n
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def oracle_step(inp, rows):
+    """fp64 oracle forward + backward on rows n < rows of batch 0 (bias2 is shared over n)."""
+    from oracle import evo_oracle as O
+    sl = lambda t: None if t is None else t[:1, :rows].double().numpy()
+    b2 = None if inp["bias2"] is None else inp["bias2"][:1].double().numpy()
+    q, k, v, do, b1 = sl(inp["q"]), sl(inp["k"]), sl(inp["v"]), sl(inp["do"]), sl(inp["bias1"])
+    O.forward(q, k, v, b1, b2)
+    O.backward(q, k, v, b1, b2, do)
+
+
+def oracle_row_seconds(inp):
+    t0 = time.perf_counter()
+    oracle_step(inp, 1)
+    return max(time.perf_counter() - t0, 1e-6)
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 100 ms in the background."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.gpu = gpu_index
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return []
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append({"t": ts, "sm": float(parts[2]), "max": float(parts[3]),
+                             "power": float(parts[4]) if parts[4] not in ("[N/A]", "N/A") else None,
+                             "hw": parts[6], "hw_thermal": parts[7], "sw_thermal": parts[8], "sw_power": parts[9]})
+            except ValueError:
+                continue
+        return rows
+
+
+def summarize_clocks(rows, t0, t1):
+    inside = [r for r in rows if t0 <= r["t"] <= t1]
+    window = "timed"
+    if not inside:
+        inside, window = rows, "whole run (timed region shorter than the 100 ms sampling interval)"
+    if not inside:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"], "samples": 0}
+    reasons = set()
+    for r in inside:
+        for key, name in (("hw", "hw_slowdown"), ("hw_thermal", "hw_thermal_slowdown"),
+                          ("sw_thermal", "sw_thermal_slowdown"), ("sw_power", "sw_power_cap")):
+            if r[key].lower() == "active":
+                reasons.add(name)
+    return {"sm_mhz": statistics.median(r["sm"] for r in inside), "sm_max_mhz": max(r["max"] for r in inside),
+            "reasons": sorted(reasons), "samples": len(inside), "window": window}
+
+
+def traffic_for(kernel):
+    """ncu DRAM bytes per launch for `kernel`, if measured on the current source."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f).get(kernel)
+    if not d:
+        return None
+    src = os.path.join(ROOT, d["source"])
+    if not os.path.exists(src):
+        return None
+    with open(src, "rb") as f:
+        if hashlib.sha256(f.read()).hexdigest() != d["source_sha256"]:
+            return None  # kernel changed since the counters were taken
+    return d["dram_bytes_per_launch"]
+
+
+# --------------------------------------------------------------------------- distributed
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# --------------------------------------------------------------------------- reference arm
+def run_reference(args):
+    world, rank, _ = dist_setup(args)
+    if rank != 0:
+        return 0
+    from memory_efficient_biased_gb300.workload import WORKLOADS, workload_inputs
+    w = WORKLOADS[args.workload]
+    inp = workload_inputs(args.workload, args.dtype)
+    t_row = oracle_row_seconds(inp)
+    budget = min(2.0, 150.0 / max(1, args.steps + args.warmup))
+    rows = int(max(1, min(w.N, budget // t_row)))
+    for _ in range(args.warmup):
+        oracle_step(inp, rows)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle_step(inp, rows)
+        times.append(time.perf_counter() - t0)
+    per_step = sum(times) / len(times)
+    f = flops(w)["step"] * rows / w.N
+    value = f / per_step / 1e12
+    sample = f"fp64 numpy oracle fwd+bwd of rows n<{rows} of N={w.N} (batch 0) per step"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "N": w.N, "L": w.L, "H": w.H, "D": w.D,
+                       "input_dtype": args.dtype, "rows_per_step": rows},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# --------------------------------------------------------------------------- our arm
+def run_ours(args):
+    import torch
+    world, rank, local = dist_setup(args)
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    from memory_efficient_biased_gb300 import build as _build
+    _build.build()
+    from memory_efficient_biased_gb300 import evo_attn as E
+    from memory_efficient_biased_gb300.workload import WORKLOADS, workload_inputs
+
+    w = WORKLOADS[args.workload]
+    dt = {"bf16": torch.bfloat16, "fp16": torch.float16}[args.dtype]
+    inp = workload_inputs(args.workload, args.dtype, seed=rank)
+    has_b1, has_b2 = inp["bias1"] is not None, inp["bias2"] is not None
+    shape = (w.B, w.N, w.L, w.H, w.D)
+    ws_bytes = E.evo_attn_bwd_workspace_bytes(shape, dt, has_b2)
+    qkv = inp["q"].numel() * 2
+    per_rep = 9 * qkv + ws_bytes + (2 * inp["bias2"].numel() * 2 if has_b2 else 0)
+    R = int(min(8, max(1, math.ceil(3 * L2_BYTES / per_rep))))
+
+    def replica():
+        d = {k: (None if v is None else v.cuda()) for k, v in inp.items()}
+        d["out"] = torch.empty_like(d["q"])
+        d["lse"] = torch.empty((w.B, w.N, w.H, w.L), dtype=torch.float32, device="cuda")
+        for k in ("dq", "dk", "dv"):
+            d[k] = torch.empty_like(d["q"])
+        d["db2"] = torch.empty_like(d["bias2"]) if has_b2 else None
+        d["ws"] = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device="cuda")
+        return d
+
+    reps = [replica() for _ in range(R)]
+
+    def step(d):
+        E.evo_attn_fwd(d["q"], d["k"], d["v"], d["bias1"], d["bias2"], out=d["out"], lse=d["lse"])
+        E.evo_attn_bwd(d["q"], d["k"], d["v"], d["bias1"], d["bias2"], d["out"], d["lse"], d["do"],
+                       dq=d["dq"], dk=d["dk"], dv=d["dv"], dbias2=d["db2"], workspace=d["ws"])
+
+    # peak device memory per call (outputs + workspace the call needs), before anything else is cached
+    torch.cuda.synchronize()
+    d0 = reps[0]
+    torch.cuda.reset_peak_memory_stats()
+    base = torch.cuda.memory_allocated()
+    out, lse = E.evo_attn_fwd(d0["q"], d0["k"], d0["v"], d0["bias1"], d0["bias2"])
+    torch.cuda.synchronize()
+    peak_fwd = torch.cuda.max_memory_allocated() - base
+    torch.cuda.reset_peak_memory_stats()
+    base = torch.cuda.memory_allocated()
+    E.evo_attn_bwd(d0["q"], d0["k"], d0["v"], d0["bias1"], d0["bias2"], out, lse, d0["do"])
+    torch.cuda.synchronize()
+    peak_bwd = torch.cuda.max_memory_allocated() - base
+    del out, lse
+    if E.evo_attn_device_status() != 0:
+        raise RuntimeError("device wait timed out during set-up")
+
+    # capture one graph per replica, with profiling events recorded inside each replay
+    n_ev = 8 if has_b2 else 6
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(R)]
+    for d in reps:
+        step(d)  # lazy one-time set-up outside capture
+    torch.cuda.synchronize()
+    graphs = []
+    cap_stream = torch.cuda.Stream()
+    for r, d in enumerate(reps):
+        g = torch.cuda.CUDAGraph()
+        E.evo_attn_profile_events(evs[r])
+        with torch.cuda.graph(g, stream=cap_stream):
+            step(d)
+        E.evo_attn_profile_events(None)
+        graphs.append(g)
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    for k in range(args.warmup):
+        graphs[k % R].replay()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    wall0 = time.time()
+    t_start.record()
+    for k in range(args.steps):
+        graphs[k % R].replay()
+    t_end.record()
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    if world > 1:
+        torch.distributed.barrier()
+    ms_total = t_start.elapsed_time(t_end)
+    if world > 1:
+        t = torch.tensor([ms_total], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_total = float(t.item())
+    clock_rows = sampler.stop() if sampler else []
+    if E.evo_attn_device_status() != 0:
+        raise RuntimeError("device wait timed out during the timed region")
+
+    # per-kernel durations from the last replay of each replica's graph (inside the timed region)
+    names = ["fwd", "bwd_pre", "bwd_main", "bwd_dq_cast"] + (["bwd_db2_part", "bwd_db2_sum"] if has_b2 else [])
+    pairs = [(0, 1), (2, 3), (3, 4), (4, 5)] + ([(5, 6), (6, 7)] if has_b2 else [])
+    used = min(R, args.steps)
+    kern_ms = {n: statistics.mean(evs[r][a].elapsed_time(evs[r][b]) for r in range(used))
+               for n, (a, b) in zip(names, pairs)}
+
+    F = flops(w)
+    ms_step = ms_total / args.steps
+    value = world * F["step"] / (ms_step * 1e-3) / 1e12
+    fwd_tflops = F["fwd"] / (kern_ms["fwd"] * 1e-3) / 1e12
+    peaks, peak_src = load_peaks()
+    # algorithmic work of each kernel per launch
+    E_el = w.B * w.N * w.H * w.L * w.L
+    bnhl = w.B * w.N * w.H * w.L
+    b1b = w.B * w.N * w.L * 2 if has_b1 else 0
+    b2b = w.B * w.H * w.L * w.L * 2 if has_b2 else 0
+    work = {
+        "fwd": ("tensor", F["fwd"]),
+        "bwd_main": ("tensor", F["bwd"]),
+        "bwd_db2_part": ("tensor", 4.0 * E_el * w.D),
+        "bwd_pre": ("hbm", 2 * qkv + bnhl * 4 + 2 * qkv),
+        "bwd_dq_cast": ("hbm", 2 * qkv + qkv),
+        "bwd_db2_sum": ("hbm", 0),
+    }
+    if has_b2:
+        import ctypes  # noqa: F401
+        groups = (ws_bytes - (bnhl * 4 + 2 * qkv)) // (w.B * w.H * w.L * w.L * 4)
+        work["bwd_db2_sum"] = ("hbm", groups * w.B * w.H * w.L * w.L * 4 + b2b)
+    dom = max(kern_ms, key=kern_ms.get)
+    bound, amount = work[dom]
+    if bound == "tensor":
+        achieved = amount / (kern_ms[dom] * 1e-3) / 1e12
+        peak = peaks["bf16_tflops_sustained"]
+        unit = "TFLOP/s"
+    else:
+        achieved = amount / (kern_ms[dom] * 1e-3) / 1e9
+        peak = peaks["hbm_gbs"]
+        unit = "GB/s"
+    roofline = {"kernel": dom, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+                "frac": achieved / peak, "traffic": traffic_for(dom),
+                "peak_source": f"{peak_src} ({'bf16_tflops_sustained' if bound == 'tensor' else 'hbm_gbs'})"}
+
+    # end to end through the host-buffer C-ABI step, pinned host memory
+    pin = lambda t: None if t is None else t.pin_memory()
+    h = {k: pin(v) for k, v in inp.items()}
+    hout = {k: torch.empty_like(h["q"]).pin_memory() for k in ("out", "dq", "dk", "dv")}
+    hdb2 = torch.empty_like(h["bias2"]).pin_memory() if has_b2 else None
+    arena = torch.empty(E.evo_attn_step_host_arena_bytes(shape, dt, has_b1, has_b2), dtype=torch.uint8,
+                        device="cuda")
+    for d in reps[1:]:
+        for key in list(d):
+            d[key] = None
+    torch.cuda.empty_cache()
+
+    def host_step():
+        E.evo_attn_step_host(h["q"], h["k"], h["v"], h["bias1"], h["bias2"], h["do"], hout["out"], None,
+                             hout["dq"], hout["dk"], hout["dv"], hdb2, arena)
+
+    for _ in range(2):
+        host_step()
+    torch.cuda.synchronize()
+    n_e2e = max(1, min(args.e2e_steps, args.steps))
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(n_e2e):
+        host_step()
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / n_e2e
+    if world > 1:
+        t = torch.tensor([e2e_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    if E.evo_attn_device_status() != 0:
+        raise RuntimeError("device wait timed out during the end-to-end run")
+    h2d = sum(t.numel() * t.element_size() for t in (h["q"], h["k"], h["v"], h["do"], h["bias1"], h["bias2"])
+              if t is not None)
+    d2h = 4 * qkv + (hdb2.numel() * 2 if has_b2 else 0)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        t_row = oracle_row_seconds(inp)
+        rows = int(max(1, min(w.N, 12.0 // t_row)))
+        t0 = time.perf_counter()
+        oracle_step(inp, rows)
+        dt_cpu = time.perf_counter() - t0
+        cpu = {"value": F["step"] * rows / w.N / dt_cpu / 1e12, "unit": "TFLOP/s", "cores": blas_threads(),
+               "kind": "oracle",
+               "sample": f"fp64 numpy oracle fwd+bwd of rows n<{rows} of N={w.N} (batch 0), {dt_cpu:.1f} s"}
+
+    launches_per_step = 1 + 3 + (2 if has_b2 else 0)
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": args.dtype, "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "N": w.N, "L": w.L, "H": w.H, "D": w.D,
+                       "bias1": w.mask and f"{w.mask[0]} {w.mask[1]}", "bias2": has_b2,
+                       "l2": f"inputs larger than L2: {R} rotating replicas of {per_rep / 1e6:.0f} MB",
+                       "parallelism": f"{world} independent replicas" if world > 1 else "single GPU"},
+            "fwd_tflops": fwd_tflops,
+            "fwd_frac_of_peak": fwd_tflops / peaks["bf16_tflops_sustained"],
+            "fwd_bwd_frac_of_peak": value / world / peaks["bf16_tflops_sustained"],
+            "kernel_ms": kern_ms,
+            "peak_mem_bytes": {"fwd_call": peak_fwd, "bwd_call": peak_bwd},
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": {"value": world * F["step"] / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                    "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": summarize_clocks(clock_rows, wall0, wall1),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -163,6 +163,47 @@ EVO_API void evo_attn_set_wait_limit_ns(uint64_t ns);
  */
 EVO_API evo_status_t evo_attn_selftest_wait_timeout(uint64_t limit_ns, void* stream);
 
+/*
+ * Profiling hook (process-wide, not for concurrent callers).  With
+ * events != NULL and count > 0, later calls record caller-owned CUDA events
+ * (cudaEvent_t, created with timing enabled) on their stream around each
+ * kernel they launch:
+ *   evo_attn_fwd : events[0] before its kernel, events[1] after it;
+ *   evo_attn_bwd : events[2] before its first kernel, then one event after
+ *                  each kernel in launch order — events[3] after delta /
+ *                  accumulator set-up, events[4] after the main backward
+ *                  kernel, events[5] after the dQ cast, and with a pair bias
+ *                  events[6] after the per-group pair-bias partials and
+ *                  events[7] after their fixed-order sum.
+ * Indices >= count are skipped.  evo_attn_profile_events(NULL, 0) turns it off.
+ * Recording works inside stream capture (the records become graph nodes).
+ */
+EVO_API void evo_attn_profile_events(void* const* events, int count);
+
+/*
+ * Bytes of device arena evo_attn_step_host needs for this problem (0 on a bad
+ * shape or dtype): room for the inputs, outputs, lse and backward workspace.
+ */
+EVO_API size_t evo_attn_step_host_arena_bytes(evo_shape_t shape, evo_dtype_t dtype, int has_bias1,
+                                              int has_bias2);
+
+/*
+ * One forward + backward step from and to HOST memory.  Copies q, k, v,
+ * bias1, bias2 (nullable as in evo_attn_fwd) and dout from host buffers into
+ * the caller's device arena (one cudaMemcpyAsync per tensor), runs
+ * evo_attn_fwd and evo_attn_bwd there, and copies out, dq, dk, dv, dbias2
+ * (required iff bias2 != NULL) and, when lse != NULL, lse back to host
+ * buffers.  Host buffers should be page-locked for the copies to be
+ * asynchronous; all work is queued on `stream`, so synchronise it before
+ * reading the outputs.  arena: device memory of at least
+ * evo_attn_step_host_arena_bytes(...) bytes, 256-byte aligned, caller-owned.
+ * Host pointers have no alignment rule.  Validation as in evo_attn_fwd/bwd.
+ */
+EVO_API evo_status_t evo_attn_step_host(const void* q, const void* k, const void* v, const void* bias1,
+                                        const void* bias2, const void* dout, void* out, float* lse, void* dq,
+                                        void* dk, void* dv, void* dbias2, void* arena, size_t arena_bytes,
+                                        evo_shape_t shape, evo_dtype_t dtype, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -440,7 +440,8 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t st) {
   // TMEM columns, and a second resident CTA would stall in tcgen05.alloc.
   const size_t smem = (lay.total + 1024 > 116u * 1024u) ? lay.total + 1024 : 116u * 1024u;
   auto kern = evo_fwd_kernel<DP, BF16, HAS_B2>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  static bool limit_set[64] = {};
+  cudaError_t e = ensure_smem_limit(kern, smem, limit_set);
   if (e != cudaSuccess) return e;
   const long long grid = a.items < num_sms() ? a.items : num_sms();
   kern<<<static_cast<unsigned>(grid), 192, smem, st>>>(a);

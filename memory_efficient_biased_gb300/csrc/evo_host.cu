@@ -25,6 +25,7 @@ namespace evo {
 __device__ int g_evo_status = 0;
 
 static std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
+static ProfileEvents g_prof{{nullptr}, 0};
 
 namespace {
 
@@ -276,7 +277,10 @@ evo_status_t evo_attn_fwd(const void* q, const void* k, const void* v, const voi
   a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(shape.D)));
   a.wait_ns = g_wait_limit_ns.load();
   a.status = dev->status;
-  cudaError_t e = launch_fwd(a, padded_dim(shape.D), bf16, static_cast<cudaStream_t>(stream));
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  prof_record(&g_prof, 0, cs);
+  cudaError_t e = launch_fwd(a, padded_dim(shape.D), bf16, cs);
+  prof_record(&g_prof, 1, cs);
   return e == cudaSuccess ? EVO_OK : EVO_ERR_CUDA;
 }
 
@@ -325,8 +329,7 @@ evo_status_t evo_attn_bwd(const void* q, const void* k, const void* v, const voi
   a.bias2_mode = kBias2None;
   if (bias2) {
     if (shape.L % 8 == 0) {
-      if (!map_bias2(&a.tb2t, bias2, shape, bf16, 128, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-          !map_bias2(&a.tb2, bias2, shape, bf16, 64, CU_TENSOR_MAP_SWIZZLE_128B))
+      if (!map_bias2(&a.tb2, bias2, shape, bf16, 64, CU_TENSOR_MAP_SWIZZLE_128B))
         return EVO_ERR_CUDA;
       a.bias2_mode = kBias2Tma;
     } else {
@@ -358,7 +361,7 @@ evo_status_t evo_attn_bwd(const void* q, const void* k, const void* v, const voi
   a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(shape.D)));
   a.wait_ns = g_wait_limit_ns.load();
   a.status = dev->status;
-  cudaError_t e = launch_bwd(a, padded_dim(shape.D), bf16, static_cast<cudaStream_t>(stream));
+  cudaError_t e = launch_bwd(a, padded_dim(shape.D), bf16, static_cast<cudaStream_t>(stream), &g_prof);
   return e == cudaSuccess ? EVO_OK : EVO_ERR_CUDA;
 }
 
@@ -385,6 +388,90 @@ evo_status_t evo_attn_selftest_wait_timeout(uint64_t limit_ns, void* stream) {
   return launch_wait_selftest(limit_ns, dev->status, static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? EVO_OK
              : EVO_ERR_CUDA;
+}
+
+void evo_attn_profile_events(void* const* events, int count) {
+  ProfileEvents p{{nullptr}, 0};
+  if (events && count > 0) {
+    p.count = count > 8 ? 8 : count;
+    for (int i = 0; i < p.count; ++i) p.ev[i] = events[i];
+  }
+  g_prof = p;
+}
+
+namespace {
+struct ArenaLayout {
+  size_t q, k, v, dout, out, dq, dk, dv, b1, b2, db2, lse, ws, total;
+};
+ArenaLayout arena_layout(const evo_shape_t& s, bool has_b1, bool has_b2) {
+  ArenaLayout a{};
+  size_t off = 0;
+  const size_t nq = round256(qkv_bytes(s));
+  size_t* qkv[8] = {&a.q, &a.k, &a.v, &a.dout, &a.out, &a.dq, &a.dk, &a.dv};
+  for (size_t* p : qkv) {
+    *p = off;
+    off += nq;
+  }
+  a.b1 = off;
+  if (has_b1) off += round256(bias1_bytes(s));
+  a.b2 = off;
+  if (has_b2) off += round256(bias2_bytes(s));
+  a.db2 = off;
+  if (has_b2) off += round256(bias2_bytes(s));
+  a.lse = off;
+  off += round256(lse_bytes(s));
+  a.ws = off;
+  off += ws_layout(s, has_b2).total;
+  a.total = off;
+  return a;
+}
+}  // namespace
+
+size_t evo_attn_step_host_arena_bytes(evo_shape_t shape, evo_dtype_t dtype, int has_bias1, int has_bias2) {
+  if (dtype != EVO_F16 && dtype != EVO_BF16) return 0;
+  if (check_shape(shape) != EVO_OK) return 0;
+  return arena_layout(shape, has_bias1 != 0, has_bias2 != 0).total;
+}
+
+evo_status_t evo_attn_step_host(const void* q, const void* k, const void* v, const void* bias1, const void* bias2,
+                                const void* dout, void* out, float* lse, void* dq, void* dk, void* dv, void* dbias2,
+                                void* arena, size_t arena_bytes, evo_shape_t shape, evo_dtype_t dtype,
+                                void* stream) {
+  if (!q || !k || !v || !dout || !out || !dq || !dk || !dv || !arena) return EVO_ERR_NULL_POINTER;
+  if (dtype != EVO_F16 && dtype != EVO_BF16) return EVO_ERR_BAD_DTYPE;
+  evo_status_t st = check_shape(shape);
+  if (st != EVO_OK) return st;
+  if ((bias2 != nullptr) != (dbias2 != nullptr)) return EVO_ERR_BAD_ARGUMENT;
+  if (!aligned(arena, 256)) return EVO_ERR_MISALIGNED;
+  const ArenaLayout L = arena_layout(shape, bias1 != nullptr, bias2 != nullptr);
+  if (arena_bytes < L.total) return EVO_ERR_WORKSPACE_TOO_SMALL;
+  DeviceInfo* dev = nullptr;
+  if ((st = check_device(&dev)) != EVO_OK) return st;
+  uint8_t* A = static_cast<uint8_t*>(arena);
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t nq = qkv_bytes(shape);
+  auto h2d = [&](size_t off, const void* src, size_t bytes) {
+    return cudaMemcpyAsync(A + off, src, bytes, cudaMemcpyHostToDevice, s) == cudaSuccess;
+  };
+  auto d2h = [&](void* dst, size_t off, size_t bytes) {
+    return cudaMemcpyAsync(dst, A + off, bytes, cudaMemcpyDeviceToHost, s) == cudaSuccess;
+  };
+  if (!h2d(L.q, q, nq) || !h2d(L.k, k, nq) || !h2d(L.v, v, nq) || !h2d(L.dout, dout, nq) ||
+      (bias1 && !h2d(L.b1, bias1, bias1_bytes(shape))) || (bias2 && !h2d(L.b2, bias2, bias2_bytes(shape))))
+    return EVO_ERR_CUDA;
+  const void* db1 = bias1 ? A + L.b1 : nullptr;
+  const void* db2 = bias2 ? A + L.b2 : nullptr;
+  st = evo_attn_fwd(A + L.q, A + L.k, A + L.v, db1, db2, A + L.out, reinterpret_cast<float*>(A + L.lse), shape,
+                    dtype, stream);
+  if (st != EVO_OK) return st;
+  st = evo_attn_bwd(A + L.q, A + L.k, A + L.v, db1, db2, A + L.out, reinterpret_cast<const float*>(A + L.lse),
+                    A + L.dout, A + L.dq, A + L.dk, A + L.dv, bias2 ? A + L.db2 : nullptr, A + L.ws,
+                    arena_bytes - L.ws, shape, dtype, stream);
+  if (st != EVO_OK) return st;
+  if (!d2h(out, L.out, nq) || !d2h(dq, L.dq, nq) || !d2h(dk, L.dk, nq) || !d2h(dv, L.dv, nq) ||
+      (dbias2 && !d2h(dbias2, L.db2, bias2_bytes(shape))) || (lse && !d2h(lse, L.lse, lse_bytes(shape))))
+    return EVO_ERR_CUDA;
+  return EVO_OK;
 }
 
 }  // extern "C"

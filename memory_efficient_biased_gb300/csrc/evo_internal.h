@@ -31,7 +31,6 @@ struct FwdArgs {
 
 struct BwdArgs {
   CUtensorMap tq, tk, tv, tdo;  // 4-D views like the forward, box (DP, 1, 128, 1)
-  CUtensorMap tb2t;             // 3-D [B*H][L][L] view, box (128, 128, 1), no swizzle
   CUtensorMap tb2;              // 3-D [B*H][L][L] view, box (64, 128, 1), 128B swizzle
   const uint16_t* q;
   const uint16_t* out;
@@ -57,9 +56,31 @@ struct BwdArgs {
   int* status;
 };
 
+// Caller-owned CUDA events recorded around the library's launches (profiling hook).
+struct ProfileEvents {
+  void* ev[8];
+  int count;
+};
+inline void prof_record(const ProfileEvents* p, int idx, cudaStream_t st) {
+  if (p && idx < p->count && p->ev[idx]) cudaEventRecord(static_cast<cudaEvent_t>(p->ev[idx]), st);
+}
+
+// Raise a kernel's dynamic shared-memory limit once per device (so that later
+// launches, including those under stream capture, issue nothing but the launch).
+template <typename Kernel>
+cudaError_t ensure_smem_limit(Kernel kern, size_t bytes, bool (&done)[64]) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+  if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
+  return e;
+}
+
 int num_sms();
 cudaError_t launch_fwd(const FwdArgs& a, int DP, bool bf16, cudaStream_t st);
-cudaError_t launch_bwd(const BwdArgs& a, int DP, bool bf16, cudaStream_t st);
+cudaError_t launch_bwd(const BwdArgs& a, int DP, bool bf16, cudaStream_t st, const ProfileEvents* prof);
 cudaError_t launch_wait_selftest(uint64_t limit_ns, int* status, cudaStream_t st);
 
 }  // namespace evo

@@ -29,7 +29,8 @@ STATUS_NAMES = {
 }
 EXPORTED = ("evo_attn_abi_version", "evo_status_string", "evo_attn_fwd", "evo_attn_bwd_workspace_bytes",
             "evo_attn_bwd", "evo_attn_device_status", "evo_attn_set_wait_limit_ns",
-            "evo_attn_selftest_wait_timeout")
+            "evo_attn_selftest_wait_timeout", "evo_attn_profile_events", "evo_attn_step_host_arena_bytes",
+            "evo_attn_step_host")
 
 _DTYPE_CODE = {torch.float16: 0, torch.bfloat16: 1}
 
@@ -79,6 +80,12 @@ def load(path: Optional[str] = None):
     lib.evo_attn_set_wait_limit_ns.argtypes = [u64]
     lib.evo_attn_selftest_wait_timeout.restype = i32
     lib.evo_attn_selftest_wait_timeout.argtypes = [u64, vp]
+    lib.evo_attn_profile_events.restype = None
+    lib.evo_attn_profile_events.argtypes = [ctypes.POINTER(vp), i32]
+    lib.evo_attn_step_host_arena_bytes.restype = sz
+    lib.evo_attn_step_host_arena_bytes.argtypes = [EvoShape, i32, i32, i32]
+    lib.evo_attn_step_host.restype = i32
+    lib.evo_attn_step_host.argtypes = [vp] * 13 + [sz, EvoShape, i32, vp]
     if path is None:
         _lib = lib
     return lib
@@ -184,3 +191,37 @@ def evo_attn_set_wait_limit_ns(ns: int) -> None:
 
 def evo_attn_selftest_wait_timeout(limit_ns: int, stream=None) -> int:
     return int(load().evo_attn_selftest_wait_timeout(int(limit_ns), _stream_ptr(stream)))
+
+
+def evo_attn_profile_events(events) -> None:
+    """Record the given torch.cuda.Event objects around the library's launches
+    (see include/evo_attn.h for the index of each); ``None`` turns it off."""
+    if not events:
+        load().evo_attn_profile_events(None, 0)
+        return
+    for e in events:
+        if e.cuda_event == 0:  # torch creates the CUDA event lazily
+            e.record()
+    arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+    load().evo_attn_profile_events(arr, len(events))
+
+
+def evo_attn_step_host_arena_bytes(shape, dtype, has_bias1: bool, has_bias2: bool) -> int:
+    return int(load().evo_attn_step_host_arena_bytes(EvoShape(*shape), _DTYPE_CODE[dtype], int(bool(has_bias1)),
+                                                     int(bool(has_bias2))))
+
+
+def evo_attn_step_host(q, k, v, bias1, bias2, dout, out, lse, dq, dk, dv, dbias2, arena, stream=None):
+    """Forward + backward from and to host (ideally pinned) CPU tensors through
+    a caller-owned device arena; queued on ``stream`` (synchronise before use)."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (dout, "dout"), (out, "out"), (dq, "dq"), (dk, "dk"), (dv, "dv")):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous host tensor")
+    if not arena.is_cuda:
+        raise ValueError("arena must be a CUDA tensor")
+    st = load().evo_attn_step_host(_ptr(q), _ptr(k), _ptr(v), _ptr(bias1), _ptr(bias2), _ptr(dout), _ptr(out),
+                                   _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dbias2), _ptr(arena),
+                                   arena.numel() * arena.element_size(), shape_of(q), _DTYPE_CODE[q.dtype],
+                                   _stream_ptr(stream))
+    if st != EVO_OK:
+        raise EvoAttnError(st, "evo_attn_step_host")
