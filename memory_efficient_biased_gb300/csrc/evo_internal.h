@@ -61,8 +61,11 @@ struct ProfileEvents {
   void* ev[8];
   int count;
 };
+// External records: under stream capture they become timestamped event-record
+// nodes of the graph (a plain record would only become a dependency edge).
 inline void prof_record(const ProfileEvents* p, int idx, cudaStream_t st) {
-  if (p && idx < p->count && p->ev[idx]) cudaEventRecord(static_cast<cudaEvent_t>(p->ev[idx]), st);
+  if (p && idx < p->count && p->ev[idx])
+    cudaEventRecordWithFlags(static_cast<cudaEvent_t>(p->ev[idx]), st, cudaEventRecordExternal);
 }
 
 // Raise a kernel's dynamic shared-memory limit once per device (so that later
