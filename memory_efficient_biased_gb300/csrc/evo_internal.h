@@ -61,11 +61,18 @@ struct ProfileEvents {
   void* ev[8];
   int count;
 };
-// External records: under stream capture they become timestamped event-record
-// nodes of the graph (a plain record would only become a dependency edge).
+// Under stream capture the record must be external to become a timestamped
+// event-record node of the graph (a plain record would only become a
+// dependency edge); outside capture the external flag is invalid.
 inline void prof_record(const ProfileEvents* p, int idx, cudaStream_t st) {
-  if (p && idx < p->count && p->ev[idx])
-    cudaEventRecordWithFlags(static_cast<cudaEvent_t>(p->ev[idx]), st, cudaEventRecordExternal);
+  if (!p || idx >= p->count || !p->ev[idx]) return;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) cs = cudaStreamCaptureStatusNone;
+  const cudaEvent_t ev = static_cast<cudaEvent_t>(p->ev[idx]);
+  if (cs == cudaStreamCaptureStatusActive)
+    cudaEventRecordWithFlags(ev, st, cudaEventRecordExternal);
+  else
+    cudaEventRecord(ev, st);
 }
 
 // Raise a kernel's dynamic shared-memory limit once per device (so that later
