@@ -81,8 +81,10 @@ typedef enum {
   EVO_ERR_CUDA = 7,                /* a CUDA runtime/driver call or launch failed   */
   EVO_ERR_DEVICE_TIMEOUT = 8,      /* a bounded device-side wait ran out            */
   EVO_ERR_ALIASING = 9,            /* an output overlaps an input                   */
-  EVO_ERR_BAD_ARGUMENT = 10        /* any other invalid argument (e.g. dbias2 given
+  EVO_ERR_BAD_ARGUMENT = 10,       /* any other invalid argument (e.g. dbias2 given
                                       without bias2, or missing with bias2)         */
+  EVO_ERR_SCRATCH_LIMIT = 11       /* evo_attn_bwd_noalloc: the problem needs more
+                                      scratch than EVO_NOALLOC_SCRATCH_BYTES         */
 } evo_status_t;
 
 typedef enum { EVO_F16 = 0, EVO_BF16 = 1 } evo_dtype_t;
@@ -203,6 +205,42 @@ EVO_API evo_status_t evo_attn_step_host(const void* q, const void* k, const void
                                         const void* bias2, const void* dout, void* out, float* lse, void* dq,
                                         void* dk, void* dv, void* dbias2, void* arena, size_t arena_bytes,
                                         evo_shape_t shape, evo_dtype_t dtype, void* stream);
+
+/*
+ * Backward for callers that cannot allocate device memory.
+ *
+ * The method's pages have no counterpart to this entry point; it exists for
+ * the library's users.  evo_attn_bwd needs a device workspace from its
+ * caller, and some callers cannot provide one: code that runs where
+ * cudaMalloc is unavailable or forbidden (inside a memory-pool-managed
+ * framework that owns every allocation, a real-time or embedded loop that
+ * must not allocate after start-up, a plugin without access to the host
+ * application's allocator).  This variant runs the same backward but takes
+ * its scratch from a fixed array inside the library: a file-scope
+ * __device__ array of EVO_NOALLOC_SCRATCH_BYTES (16 MiB) that every GPU
+ * which loads this part of the library holds until the process exits.  It
+ * calls no cudaMalloc, cudaFree or other allocating routine.
+ *
+ * Arguments and outputs are those of evo_attn_bwd without the workspace.
+ * Problems whose backward workspace (evo_attn_bwd_workspace_bytes) exceeds
+ * EVO_NOALLOC_SCRATCH_BYTES are rejected with EVO_ERR_SCRATCH_LIMIT before
+ * anything is launched.
+ *
+ * The first call on a device looks up the array's device address on that
+ * device (cudaGetSymbolAddress, with the device current); make that first
+ * call before any stream capture on the device.  Every call on a device
+ * shares the one array, which keeps the previous call's contents (the
+ * kernels clear what must start at zero themselves): calls whose work
+ * overlaps on the GPU — on different streams, or from different host
+ * threads — race on the scratch and give wrong results.  Serialise them.
+ */
+#define EVO_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+EVO_API evo_status_t evo_attn_bwd_noalloc(const void* q, const void* k, const void* v,
+                                          const void* bias1, const void* bias2,
+                                          const void* out, const float* lse, const void* dout,
+                                          void* dq, void* dk, void* dv, void* dbias2,
+                                          evo_shape_t shape, evo_dtype_t dtype, void* stream);
 
 #ifdef __cplusplus
 }

@@ -224,6 +224,8 @@ const char* evo_status_string(evo_status_t s) {
     case EVO_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait ran out; outputs are undefined";
     case EVO_ERR_ALIASING: return "an output buffer overlaps an input buffer";
     case EVO_ERR_BAD_ARGUMENT: return "invalid argument combination";
+    case EVO_ERR_SCRATCH_LIMIT:
+      return "backward workspace exceeds the fixed 16 MiB scratch of evo_attn_bwd_noalloc; use evo_attn_bwd";
   }
   return "unknown status";
 }

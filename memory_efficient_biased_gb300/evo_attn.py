@@ -26,11 +26,13 @@ STATUS_NAMES = {
     0: "EVO_OK", 1: "EVO_ERR_NULL_POINTER", 2: "EVO_ERR_BAD_SHAPE", 3: "EVO_ERR_BAD_DTYPE",
     4: "EVO_ERR_MISALIGNED", 5: "EVO_ERR_WORKSPACE_TOO_SMALL", 6: "EVO_ERR_ARCH", 7: "EVO_ERR_CUDA",
     8: "EVO_ERR_DEVICE_TIMEOUT", 9: "EVO_ERR_ALIASING", 10: "EVO_ERR_BAD_ARGUMENT",
+    11: "EVO_ERR_SCRATCH_LIMIT",
 }
+NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 EXPORTED = ("evo_attn_abi_version", "evo_status_string", "evo_attn_fwd", "evo_attn_bwd_workspace_bytes",
             "evo_attn_bwd", "evo_attn_device_status", "evo_attn_set_wait_limit_ns",
             "evo_attn_selftest_wait_timeout", "evo_attn_profile_events", "evo_attn_step_host_arena_bytes",
-            "evo_attn_step_host")
+            "evo_attn_step_host", "evo_attn_bwd_noalloc")
 
 _DTYPE_CODE = {torch.float16: 0, torch.bfloat16: 1}
 
@@ -86,6 +88,8 @@ def load(path: Optional[str] = None):
     lib.evo_attn_step_host_arena_bytes.argtypes = [EvoShape, i32, i32, i32]
     lib.evo_attn_step_host.restype = i32
     lib.evo_attn_step_host.argtypes = [vp] * 13 + [sz, EvoShape, i32, vp]
+    lib.evo_attn_bwd_noalloc.restype = i32
+    lib.evo_attn_bwd_noalloc.argtypes = [vp] * 12 + [EvoShape, i32, vp]
     if path is None:
         _lib = lib
     return lib
@@ -225,3 +229,26 @@ def evo_attn_step_host(q, k, v, bias1, bias2, dout, out, lse, dq, dk, dv, dbias2
                                    _stream_ptr(stream))
     if st != EVO_OK:
         raise EvoAttnError(st, "evo_attn_step_host")
+
+
+def evo_attn_bwd_noalloc(q, k, v, bias1, bias2, out, lse, dout, dq, dk, dv, dbias2=None, stream=None):
+    """The backward for callers that cannot allocate device memory: no
+    workspace argument; the library's fixed 16 MiB scratch array is used
+    instead (see include/evo_attn.h).  Output tensors must be passed in.
+    Calls on one device must not overlap on the GPU: they share the scratch."""
+    B, N, L, H, D = q.shape
+    dt = q.dtype
+    if dt not in _DTYPE_CODE:
+        raise ValueError("inputs must be float16 or bfloat16")
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out"), (dout, "dout"), (dq, "dq"), (dk, "dk"), (dv, "dv")):
+        _check(t, n, q.shape, dt)
+    _check(bias1, "bias1", (B, N, 1, 1, L), dt)
+    _check(bias2, "bias2", (B, 1, H, L, L), dt)
+    _check(dbias2, "dbias2", (B, 1, H, L, L), dt)
+    _check(lse, "lse", (B, N, H, L), torch.float32)
+    st = load().evo_attn_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(bias1), _ptr(bias2), _ptr(out), _ptr(lse),
+                                     _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dbias2), shape_of(q),
+                                     _DTYPE_CODE[dt], _stream_ptr(stream))
+    if st != EVO_OK:
+        raise EvoAttnError(st, "evo_attn_bwd_noalloc")
+    return dq, dk, dv, dbias2
