@@ -8,16 +8,28 @@
 // softmax, times V) and §3.7 (fp32 lse saved for the backward; bias1 is
 // (B, N, 1, 1, L), bias2 is (B, 1, H, L, L)).
 //
-// Structure (one CTA per SM, persistent over work items (b, n, h, q-tile)):
-//   warp 4      TMA producer: Q tile per item; K, V tiles, the pair-bias tile
-//               and the key-mask chunk per key tile, into a 2-stage ring.
-//   warp 5      MMA issuer (one thread): S = Q·Kᵀ into TMEM (2 buffers),
-//               then O_j = P_j·V_j into TMEM (2 buffers), issued one key tile
-//               behind S so the tensor core overlaps the softmax.
-//   warps 0..3  softmax, one query row per thread (TMEM lane = row): scale and
-//               bias in the log2 domain, online max / sum, P (fp16/bf16) into
-//               swizzled shared memory for the P·V MMA, running rescale of the
-//               fp32 output accumulator held in registers, epilogue.
+// Structure (one CTA per SM, persistent over a contiguous range of work items
+// ordered (b, h, q-tile, n), so that consecutive items share their pair-bias
+// rows).  The kernel streams key tiles across item boundaries:
+//   warp 8      TMA producer: Q tile per item (2 buffers); K, V tiles and the
+//               key-mask chunk per key tile into a ring of up to 4 stages; the
+//               pair-bias tiles of the current (b, h, q-tile) once per group
+//               (resident), or per key tile for long sequences (streaming).
+//   warp 9      MMA issuer (one thread): S_u = Q·K_uᵀ into TMEM (2 buffers),
+//               then O_u = P_u·V_u (P read from TMEM), issued one key tile
+//               behind S — also across items, so the tensor core never waits
+//               for an epilogue.
+//   warps 0..7  softmax.  Warp w owns query rows 32·(w%4).. (its TMEM lane
+//               quadrant) and key columns 64·(w/4).. of every tile, and runs an
+//               independent online softmax over its key half: its own running
+//               max and sum, its P half (fp16/bf16, into TMEM) and its own P·V
+//               accumulator (the MMA thread issues one K = 64 P·V per half).  The
+//               two halves of a row are merged once per item, in the epilogue
+//               (rescaled by 2^(m_half - m)), so the two warps never wait on each
+//               other inside the key loop.  Scale and biases are applied in the
+//               log2 domain with packed f32x2 arithmetic; each warp keeps its
+//               half's output row in fp32 registers and finishes an item's
+//               epilogue while the next item's first tile is already running.
 // Key columns past L carry a -inf key-mask entry, so no other masking is
 // needed; query rows past L are computed and not stored.
 #include "evo_internal.h"
@@ -26,17 +38,35 @@
 namespace evo {
 namespace {
 
-constexpr int kStages = 2;
+constexpr int kMaxStages = 4;
+constexpr int kSoftmaxWarps = 8;
+constexpr int kThreads = (kSoftmaxWarps + 2) * 32;
+constexpr int kProducerWarp = kSoftmaxWarps, kMmaWarp = kSoftmaxWarps + 1;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 320;  // TMEM columns
+// TMEM columns: S (2 buffers of 128), P (2 buffers of 64 columns of packed
+// pairs; half h of the keys in columns 32h..), O (per key half and buffer, DP
+// columns each: 2 buffers when DP <= 32, else 1).
+__device__ __forceinline__ uint32_t col_s(uint32_t b) { return b ? 128u : 0u; }
+__device__ __forceinline__ uint32_t col_p(uint32_t b) { return b ? 320u : 256u; }
+template <int DP>
+__device__ __forceinline__ uint32_t col_o(uint32_t b, uint32_t half) {
+  return 384u + (DP <= 32 ? (b * 2 + half) : half) * DP;
+}
+template <int DP>
+__host__ __device__ constexpr int o_buffers() { return DP <= 32 ? 2 : 1; }
+
+// Pair-bias handling: none, resident per (b, h, q-tile) group, or streamed per key tile.
+enum B2Kind : int { kB2None = 0, kB2Resident = 1, kB2Stream = 2 };
 
 struct FwdBars {
-  uint64_t q_full, q_empty;
-  uint64_t kv_full[kStages], kv_empty[kStages];
+  uint64_t q_full[2], q_empty[2];
+  uint64_t kv_full[kMaxStages], kv_empty[kMaxStages];
+  uint64_t b2_full, b2_empty;
   uint64_t s_full[2], s_free[2];
   uint64_t p_full[2], p_empty[2];
   uint64_t o_full[2], o_free[2];
+  uint64_t xsum[4], xdone[4];  // per lane quadrant: the two warps sharing those rows (epilogue merge)
   uint64_t drain;
   uint32_t tmem_slot;
   int abort;
@@ -45,41 +75,56 @@ struct FwdBars {
 template <int DP>
 struct FwdLayout {
   static constexpr uint32_t kTileBytes = kTile * DP * 2;
-  uint32_t q, k[kStages], v[kStages], b2[kStages], p[2], b1[kStages], bars, total;
-  __host__ __device__ explicit FwdLayout(bool has_b2) {
+  uint32_t q[2], k[kMaxStages], v[kMaxStages], b1[kMaxStages], b2s[kMaxStages], b2r, xchg, bars, total;
+  __host__ __device__ FwdLayout(int b2kind, int stages, int KT) {
     uint32_t off = 0;
-    q = off;
-    off += kTileBytes;
-    for (int s = 0; s < kStages; ++s) k[s] = off + s * kTileBytes;
-    off += kStages * kTileBytes;
-    for (int s = 0; s < kStages; ++s) v[s] = off + s * kTileBytes;
-    off += kStages * kTileBytes;
-    for (int s = 0; s < kStages; ++s) b2[s] = off + s * 32768u;
-    if (has_b2) off += kStages * 32768u;
-    for (int b = 0; b < 2; ++b) p[b] = off + b * 32768u;
-    off += 2 * 32768u;
-    for (int s = 0; s < kStages; ++s) b1[s] = off + s * 512u;
-    off += kStages * 512u;
+    for (int s = 0; s < 2; ++s) q[s] = off + s * kTileBytes;
+    off += 2 * kTileBytes;
+    for (int s = 0; s < kMaxStages; ++s) {
+      k[s] = off + (s < stages ? s : 0) * 2 * kTileBytes;
+      v[s] = k[s] + kTileBytes;
+    }
+    off += stages * 2 * kTileBytes;
+    for (int s = 0; s < kMaxStages; ++s) b2s[s] = off + (s < stages ? s : 0) * 32768u;
+    if (b2kind == kB2Stream) off += stages * 32768u;
+    b2r = off;
+    if (b2kind == kB2Resident) off += KT * 32768u;
+    for (int s = 0; s < kMaxStages; ++s) b1[s] = off + (s < stages ? s : 0) * 512u;
+    off += stages * 512u;
+    xchg = off;  // epilogue merge: per half, (m, l) and the partner's DP/2 output columns, [value][row]
+    off += 2 * (2 + DP / 2) * 128 * 4;
     bars = off;
     off += (sizeof(FwdBars) + 127) & ~127u;
     total = off;
   }
 };
 
-struct ItemCoord {
-  int b, n, h, qt;
+// Work items are ordered (b, h, q-tile, n), n fastest; a CTA walks a
+// contiguous range with an incremental iterator (no integer division per item).
+struct ItemIter {
+  int b, h, qt, n;
+  __device__ __forceinline__ void init(long long item, const FwdArgs& a) {
+    long long t = item;
+    n = static_cast<int>(t % a.N);
+    t /= a.N;
+    qt = static_cast<int>(t % a.QT);
+    t /= a.QT;
+    h = static_cast<int>(t % a.H);
+    b = static_cast<int>(t / a.H);
+  }
+  __device__ __forceinline__ void next(const FwdArgs& a) {
+    if (++n == a.N) {
+      n = 0;
+      if (++qt == a.QT) {
+        qt = 0;
+        if (++h == a.H) {
+          h = 0;
+          ++b;
+        }
+      }
+    }
+  }
 };
-__device__ __forceinline__ ItemCoord decode_item(long long item, const FwdArgs& a) {
-  ItemCoord c;
-  long long t = item;
-  c.qt = static_cast<int>(t % a.QT);
-  t /= a.QT;
-  c.h = static_cast<int>(t % a.H);
-  t /= a.H;
-  c.n = static_cast<int>(t % a.N);
-  c.b = static_cast<int>(t / a.N);
-  return c;
-}
 
 // Bounded wait that ignores the abort flag: used only to drain work this
 // thread itself put in flight before the CTA exits.
@@ -89,30 +134,83 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64
   mbar_wait(bar, parity, g);
 }
 
-// ------------------------------------------------------------ producer (warp 4)
-template <int DP, bool BF16, bool HAS_B2>
+// Pair-bias tile (query rows i0.., key columns j0..) by plain loads into the
+// 128B-swizzled two-half layout the TMA map writes (used when L % 8 != 0).
+__device__ __forceinline__ void fill_b2_loads(uint8_t* dst, const uint16_t* b2, int L, int i0, int j0, int lane) {
+  const int cc = lane * 4, half = cc >> 6, chunk = (cc & 63) >> 3, within = cc & 7;
+  for (int r = 0; r < kTile; ++r) {
+    const int i = i0 + r;
+    uint32_t w[2] = {0u, 0u};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int j = j0 + cc + e;
+      const uint32_t val = (i < L && j < L) ? b2[static_cast<size_t>(i) * L + j] : 0u;
+      w[e >> 1] |= val << (16 * (e & 1));
+    }
+    *reinterpret_cast<uint2*>(dst + half * 16384 + swz_offset(r, chunk, 128) + within * 2) = make_uint2(w[0], w[1]);
+  }
+}
+
+// ------------------------------------------------------------ producer (one warp)
+template <int DP, bool BF16, int B2>
 __device__ __forceinline__ void fwd_producer(const FwdArgs& a, uint8_t* base, const FwdLayout<DP>& lay,
-                                             FwdBars* bars, const WaitGuard& g, int lane) {
+                                             FwdBars* bars, const WaitGuard& g, int lane, long long i0,
+                                             long long i1) {
   constexpr uint32_t kTB = FwdLayout<DP>::kTileBytes;
-  const uint32_t kv_bytes = 2 * kTB + ((HAS_B2 && a.bias2_mode == kBias2Tma) ? 32768u : 0u);
-  const int KT = a.QT;
-  uint32_t kv_it = 0, q_it = 0;
+  const int S = a.stages, KT = a.QT;
+  const bool tma_b2 = a.bias2_mode == kBias2Tma;
+  const uint32_t kv_bytes = 2 * kTB + ((B2 == kB2Stream && tma_b2) ? 32768u : 0u);
+  uint32_t u = 0, q_it = 0, grp_it = 0, s = 0, ph = 0;
+  ItemIter c;
+  c.init(i0, a);
   bool ok = true;
-  for (long long item = blockIdx.x; ok && item < a.items; item += gridDim.x) {
-    const ItemCoord c = decode_item(item, a);
-    const int bn = c.b * a.N + c.n;
-    if (!mbar_wait(smem_u32(&bars->q_empty), (q_it & 1) ^ 1, g)) { ok = false; break; }
+  for (long long item = i0; ok && item < i1; ++item, c.next(a)) {
+    const int bn = c.b * a.N + c.n, bh = c.b * a.H + c.h;
+    if (B2 == kB2Resident && (item == i0 || c.n == 0)) {
+      // all softmax warps are done with the previous group's tiles
+      if (!mbar_wait(smem_u32(&bars->b2_empty), (grp_it & 1) ^ 1, g)) { ok = false; break; }
+      const uint32_t full = smem_u32(&bars->b2_full);
+      if (tma_b2) {
+        if (lane == 0) {
+          mbar_expect_tx(full, KT * 32768u);
+          for (int t = 0; t < KT; ++t) {
+            tma_load_3d(smem_u32(base + lay.b2r + t * 32768u), &a.tb2, full, t * kTile, c.qt * kTile, bh);
+            tma_load_3d(smem_u32(base + lay.b2r + t * 32768u + 16384u), &a.tb2, full, t * kTile + 64,
+                        c.qt * kTile, bh);
+          }
+        }
+      } else {
+        for (int t = 0; t < KT; ++t)
+          fill_b2_loads(base + lay.b2r + t * 32768u, a.bias2 + static_cast<size_t>(bh) * a.L * a.L, a.L,
+                        c.qt * kTile, t * kTile, lane);
+      }
+      mbar_arrive(full);
+      ++grp_it;
+    }
+    const uint32_t qs = q_it & 1;
+    if (!mbar_wait(smem_u32(&bars->q_empty[qs]), ((q_it >> 1) & 1) ^ 1, g)) { ok = false; break; }
     if (lane == 0) {
-      mbar_arrive_expect_tx(smem_u32(&bars->q_full), kTB);
-      tma_load_4d(smem_u32(base + lay.q), &a.tq, smem_u32(&bars->q_full), 0, c.h, c.qt * kTile, bn);
+      mbar_arrive_expect_tx(smem_u32(&bars->q_full[qs]), kTB);
+      tma_load_4d(smem_u32(base + lay.q[qs]), &a.tq, smem_u32(&bars->q_full[qs]), 0, c.h, c.qt * kTile, bn);
     }
     ++q_it;
     const uint16_t* b1row = a.bias1 ? a.bias1 + static_cast<size_t>(bn) * a.L : nullptr;
-    for (int jt = 0; jt < KT; ++jt, ++kv_it) {
-      const uint32_t s = kv_it % kStages, ph = (kv_it / kStages) & 1;
+    for (int jt = 0; jt < KT; ++jt, ++u) {
       if (!mbar_wait(smem_u32(&bars->kv_empty[s]), ph ^ 1, g)) { ok = false; break; }
-      // key-mask chunk, fp32 in the log2 domain; -inf past L
-      {
+      const uint32_t full = smem_u32(&bars->kv_full[s]);
+      if (lane == 0) {  // copies first: the key-mask loads below must not delay them
+        mbar_expect_tx(full, kv_bytes);
+        tma_load_4d(smem_u32(base + lay.k[s]), &a.tk, full, 0, c.h, jt * kTile, bn);
+        tma_load_4d(smem_u32(base + lay.v[s]), &a.tv, full, 0, c.h, jt * kTile, bn);
+        if (B2 == kB2Stream && tma_b2) {
+          tma_load_3d(smem_u32(base + lay.b2s[s]), &a.tb2, full, jt * kTile, c.qt * kTile, bh);
+          tma_load_3d(smem_u32(base + lay.b2s[s] + 16384), &a.tb2, full, jt * kTile + 64, c.qt * kTile, bh);
+        }
+      }
+      if (B2 == kB2Stream && !tma_b2)
+        fill_b2_loads(base + lay.b2s[s], a.bias2 + static_cast<size_t>(bh) * a.L * a.L, a.L, c.qt * kTile,
+                      jt * kTile, lane);
+      {  // key-mask chunk, fp32 in the log2 domain; -inf past L
         float4 m4;
         float* mv = reinterpret_cast<float*>(&m4);
 #pragma unroll
@@ -124,290 +222,371 @@ __device__ __forceinline__ void fwd_producer(const FwdArgs& a, uint8_t* base, co
         }
         *reinterpret_cast<float4*>(base + lay.b1[s] + lane * 16) = m4;
       }
-      if (HAS_B2 && a.bias2_mode == kBias2Loads) {
-        // generic path for L % 8 != 0: plain loads into the same swizzled layout
-        const uint16_t* b2 = a.bias2 + static_cast<size_t>(c.b * a.H + c.h) * a.L * a.L;
-        const int cc = lane * 4, half = cc >> 6, chunk = (cc & 63) >> 3, within = cc & 7;
-        for (int r = 0; r < kTile; ++r) {
-          const int i = c.qt * kTile + r;
-          uint32_t w[2] = {0u, 0u};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int j = jt * kTile + cc + e;
-            const uint32_t val = (i < a.L && j < a.L) ? b2[static_cast<size_t>(i) * a.L + j] : 0u;
-            w[e >> 1] |= val << (16 * (e & 1));
-          }
-          *reinterpret_cast<uint2*>(base + lay.b2[s] + half * 16384 + swz_offset(r, chunk, 128) +
-                                    within * 2) = make_uint2(w[0], w[1]);
-        }
-      }
-      const uint32_t full = smem_u32(&bars->kv_full[s]);
-      if (lane == 0) {
-        mbar_arrive_expect_tx(full, kv_bytes);
-        tma_load_4d(smem_u32(base + lay.k[s]), &a.tk, full, 0, c.h, jt * kTile, bn);
-        tma_load_4d(smem_u32(base + lay.v[s]), &a.tv, full, 0, c.h, jt * kTile, bn);
-        if (HAS_B2 && a.bias2_mode == kBias2Tma) {
-          const int bh = c.b * a.H + c.h;
-          tma_load_3d(smem_u32(base + lay.b2[s]), &a.tb2, full, jt * kTile, c.qt * kTile, bh);
-          tma_load_3d(smem_u32(base + lay.b2[s] + 16384), &a.tb2, full, jt * kTile + 64, c.qt * kTile, bh);
-        }
-      } else {
-        mbar_arrive(full);
+      mbar_arrive(full);
+      if (++s == static_cast<uint32_t>(S)) {
+        s = 0;
+        ph ^= 1;
       }
     }
   }
   // Drain: every copy this warp started has landed before the CTA may exit.
-  if (q_it > 0) drain_wait(smem_u32(&bars->q_full), (q_it - 1) & 1, a.wait_ns, a.status);
-  for (uint32_t s = 0; s < kStages; ++s) {
-    const uint32_t issued = (kv_it + kStages - 1 - s) / kStages;
-    if (issued > 0) drain_wait(smem_u32(&bars->kv_full[s]), (issued - 1) & 1, a.wait_ns, a.status);
+  for (uint32_t q = 0; q < 2; ++q) {
+    const uint32_t issued = (q_it + 1 - q) / 2;
+    if (issued > 0) drain_wait(smem_u32(&bars->q_full[q]), (issued - 1) & 1, a.wait_ns, a.status);
   }
+  for (uint32_t st = 0; st < static_cast<uint32_t>(S); ++st) {
+    const uint32_t issued = (u + S - 1 - st) / S;
+    if (issued > 0) drain_wait(smem_u32(&bars->kv_full[st]), (issued - 1) & 1, a.wait_ns, a.status);
+  }
+  if (B2 == kB2Resident && grp_it > 0) drain_wait(smem_u32(&bars->b2_full), (grp_it - 1) & 1, a.wait_ns, a.status);
 }
 
-// ------------------------------------------------------------ MMA issuer (warp 5, one thread)
+// ------------------------------------------------------------ MMA issuer (one thread)
+// O_v,half = P_v,half · V_v,half for both key halves (K = 64 keys each), P from TMEM.
 template <int DP, bool BF16>
-__device__ __forceinline__ bool fwd_issue_pv(uint32_t u, uint32_t su, uint8_t* base, const FwdLayout<DP>& lay,
+__device__ __forceinline__ bool fwd_issue_pv(uint32_t v, uint32_t sv, uint8_t* base, const FwdLayout<DP>& lay,
                                              FwdBars* bars, uint32_t tmem, const WaitGuard& g) {
   constexpr uint32_t RB = DP * 2;
   constexpr uint32_t SWZ = swizzle_for_row(RB);
   constexpr uint32_t id_o = idesc_f16(128, DP, BF16, false, true);
-  const uint32_t ub = u & 1, uph = (u >> 1) & 1;
-  if (!mbar_wait(smem_u32(&bars->p_full[ub]), uph, g)) return false;
-  if (!mbar_wait(smem_u32(&bars->o_free[ub]), uph ^ 1, g)) return false;
+  constexpr int NB = o_buffers<DP>();
+  const uint32_t vb = v & 1, vph = (v >> 1) & 1;
+  const uint32_t ob = v % NB, oph = (v / NB) & 1;
+  if (!mbar_wait(smem_u32(&bars->p_full[vb]), vph, g)) return false;
+  if (!mbar_wait(smem_u32(&bars->o_free[ob]), oph ^ 1, g)) return false;
   tc_fence_after();
-  const uint32_t p_addr = smem_u32(base + lay.p[ub]);
-  const uint32_t v_addr = smem_u32(base + lay.v[su]);
-  const uint32_t d = tmem + (ub ? kColO1 : kColO0);
+  const uint32_t v_addr = smem_u32(base + lay.v[sv]);
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const uint64_t ad = smem_desc(p_addr + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024, kSwizzle128B);
-    const uint64_t bd = smem_desc(v_addr + k * 16 * RB, kTile * RB, 8 * RB, SWZ);
-    umma_ss(d, ad, bd, id_o, k > 0);
+  for (int half = 0; half < 2; ++half) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {  // 64 keys in steps of 16 (8 TMEM columns of packed pairs)
+      const uint64_t bd = smem_desc(v_addr + (half * 64 + k * 16) * RB, kTile * RB, 8 * RB, SWZ);
+      umma_ts(tmem + col_o<DP>(ob, half), tmem + col_p(vb) + half * 32 + k * 8, bd, id_o, k > 0);
+    }
   }
-  umma_commit(smem_u32(&bars->o_full[ub]));
-  umma_commit(smem_u32(&bars->p_empty[ub]));
-  umma_commit(smem_u32(&bars->kv_empty[su]));
+  umma_commit(smem_u32(&bars->o_full[ob]));
+  umma_commit(smem_u32(&bars->p_empty[vb]));
+  umma_commit(smem_u32(&bars->kv_empty[sv]));
   return true;
 }
 
 template <int DP, bool BF16>
 __device__ __forceinline__ void fwd_mma(const FwdArgs& a, uint8_t* base, const FwdLayout<DP>& lay, FwdBars* bars,
-                                        uint32_t tmem, const WaitGuard& g) {
+                                        uint32_t tmem, const WaitGuard& g, long long i0, long long i1) {
   constexpr uint32_t RB = DP * 2;
   constexpr uint32_t SWZ = swizzle_for_row(RB);
   constexpr uint32_t id_s = idesc_f16(128, 128, BF16, false, false);
-  const int KT = a.QT;
-  uint32_t kv_it = 0, t_it = 0, q_it = 0, prev_stage = 0;
+  const int S = a.stages, KT = a.QT;
+  uint32_t u = 0, q_it = 0, prev_stage = 0, s = 0, ph = 0;
   bool ok = true;
-  for (long long item = blockIdx.x; ok && item < a.items; item += gridDim.x) {
-    if (!mbar_wait(smem_u32(&bars->q_full), q_it & 1, g)) { ok = false; break; }
+  for (long long item = i0; ok && item < i1; ++item) {
+    const uint32_t qs = q_it & 1;
+    if (!mbar_wait(smem_u32(&bars->q_full[qs]), (q_it >> 1) & 1, g)) { ok = false; break; }
     ++q_it;
     tc_fence_after();
-    const uint32_t q_addr = smem_u32(base + lay.q);
+    const uint32_t q_addr = smem_u32(base + lay.q[qs]);
     for (int jt = 0; jt < KT; ++jt) {
-      const uint32_t s = kv_it % kStages, kph = (kv_it / kStages) & 1;
-      if (!mbar_wait(smem_u32(&bars->kv_full[s]), kph, g)) { ok = false; break; }
-      const uint32_t buf = t_it & 1, bph = (t_it >> 1) & 1;
-      if (!mbar_wait(smem_u32(&bars->s_free[buf]), bph ^ 1, g)) { ok = false; break; }
+      if (!mbar_wait(smem_u32(&bars->kv_full[s]), ph, g)) { ok = false; break; }
+      const uint32_t buf = u & 1;
+      if (!mbar_wait(smem_u32(&bars->s_free[buf]), ((u >> 1) & 1) ^ 1, g)) { ok = false; break; }
       tc_fence_after();
       const uint32_t k_addr = smem_u32(base + lay.k[s]);
-      const uint32_t d = tmem + (buf ? kColS1 : kColS0);
 #pragma unroll
       for (int k = 0; k < DP / 16; ++k) {
         const uint64_t ad = smem_desc(q_addr + k * 32, 16, 8 * RB, SWZ);
         const uint64_t bd = smem_desc(k_addr + k * 32, 16, 8 * RB, SWZ);
-        umma_ss(d, ad, bd, id_s, k > 0);
+        umma_ss(tmem + col_s(buf), ad, bd, id_s, k > 0);
       }
       umma_commit(smem_u32(&bars->s_full[buf]));
-      if (jt == KT - 1) umma_commit(smem_u32(&bars->q_empty));
-      if (jt > 0 && !fwd_issue_pv<DP, BF16>(t_it - 1, prev_stage, base, lay, bars, tmem, g)) { ok = false; break; }
+      if (jt == KT - 1) umma_commit(smem_u32(&bars->q_empty[qs]));
+      if (u > 0 && !fwd_issue_pv<DP, BF16>(u - 1, prev_stage, base, lay, bars, tmem, g)) { ok = false; break; }
       prev_stage = s;
-      ++t_it;
-      ++kv_it;
+      ++u;
+      if (++s == static_cast<uint32_t>(S)) {
+        s = 0;
+        ph ^= 1;
+      }
     }
-    if (ok && !fwd_issue_pv<DP, BF16>(t_it - 1, prev_stage, base, lay, bars, tmem, g)) ok = false;
   }
+  if (ok && u > 0) fwd_issue_pv<DP, BF16>(u - 1, prev_stage, base, lay, bars, tmem, g);
   // Drain: all MMAs this thread issued are complete before TMEM is freed.
   umma_commit(smem_u32(&bars->drain));
   drain_wait(smem_u32(&bars->drain), 0, a.wait_ns, a.status);
 }
 
-// ------------------------------------------------------------ softmax (warps 0..3)
+// ------------------------------------------------------------ softmax (warps 0..7)
+// acc (this warp's key half: all DP output columns of its row) = acc·alpha + O tile v.
 template <int DP>
-__device__ __forceinline__ bool fwd_consume_o(uint32_t u, float alpha, float (&acc)[DP], FwdBars* bars,
-                                              uint32_t trow, int lane, const WaitGuard& g) {
-  const uint32_t ub = u & 1, uph = (u >> 1) & 1;
-  if (!mbar_wait(smem_u32(&bars->o_full[ub]), uph, g)) return false;
+__device__ __forceinline__ bool fwd_consume_o(uint32_t v, float alpha, float (&acc)[DP], FwdBars* bars,
+                                              uint32_t trow, int hc, int lane, const WaitGuard& g) {
+  constexpr int NB = o_buffers<DP>();
+  const uint32_t ob = v % NB;
+  if (!mbar_wait(smem_u32(&bars->o_full[ob]), (v / NB) & 1, g)) return false;
   tc_fence_after();
-  const uint32_t col = trow + (ub ? kColO1 : kColO0);
+  const uint32_t col = trow + col_o<DP>(ob, hc);
   uint32_t o[DP / 16][16];
 #pragma unroll
   for (int c = 0; c < DP / 16; ++c) tmem_ld16(col + c * 16, o[c]);
 #pragma unroll
   for (int c = 0; c < DP / 16; ++c) tmem_wait_ld(o[c]);
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(smem_u32(&bars->o_free[ob]));
 #pragma unroll
   for (int c = 0; c < DP / 16; ++c)
 #pragma unroll
     for (int e = 0; e < 16; ++e) acc[c * 16 + e] = fmaf(acc[c * 16 + e], alpha, __uint_as_float(o[c][e]));
-  tc_fence_before();
-  __syncwarp();
-  if (lane == 0) mbar_arrive(smem_u32(&bars->o_free[ub]));
   return true;
 }
 
-template <int DP, bool BF16, bool HAS_B2>
-__device__ __forceinline__ void fwd_softmax(const FwdArgs& a, uint8_t* base, const FwdLayout<DP>& lay,
-                                            FwdBars* bars, uint32_t tmem, const WaitGuard& g) {
-  const int r = threadIdx.x;  // query row within the tile == TMEM lane
-  const int warp = r >> 5, lane = r & 31;
-  const uint32_t trow = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-  const int KT = a.QT;
-  uint32_t kv_it = 0, t_it = 0;
-  bool ok = true;
-  for (long long item = blockIdx.x; ok && item < a.items; item += gridDim.x) {
-    const ItemCoord c = decode_item(item, a);
-    float m = -INFINITY, l = 0.0f, a_prev = 0.0f;
-    float acc[DP];
+// Merge the two key halves of a finished item's rows and write O and lse.
+// Each warp writes its (m, l) and the partner's DP/2 output columns to shared
+// memory, then finishes its own DP/2 columns.
+template <int DP, bool BF16>
+__device__ __forceinline__ bool fwd_epilogue(const FwdArgs& a, const ItemIter& c, const float (&acc)[DP], float m,
+                                             float l, uint32_t fin, FwdBars* bars, float* xchg, int quad, int hc,
+                                             int r, int lane, const WaitGuard& g) {
+  constexpr int HD = DP / 2;
+  constexpr int NV = 2 + HD;  // values per row and half: m, l, HD output columns
+  if (fin > 0 && !mbar_wait(smem_u32(&bars->xdone[quad]), (fin - 1) & 1, g)) return false;
+  // keep: this warp's own output columns; give: the partner's (compile-time indices only)
+  float keep[HD], give[HD];
+  if (hc == 0) {
 #pragma unroll
-    for (int d = 0; d < DP; ++d) acc[d] = 0.0f;
+    for (int e = 0; e < HD; ++e) {
+      keep[e] = acc[e];
+      give[e] = acc[HD + e];
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < HD; ++e) {
+      keep[e] = acc[HD + e];
+      give[e] = acc[e];
+    }
+  }
+  float* mine = xchg + hc * NV * 128;
+  mine[0 * 128 + r] = m;
+  mine[1 * 128 + r] = l;
+#pragma unroll
+  for (int e = 0; e < HD; ++e) mine[(2 + e) * 128 + r] = give[e];
+  __syncwarp();
+  if (lane == 0) mbar_arrive(smem_u32(&bars->xsum[quad]));
+  if (!mbar_wait(smem_u32(&bars->xsum[quad]), fin & 1, g)) return false;
+  const float* other = xchg + (hc ^ 1) * NV * 128;
+  const float m_o = other[r], l_o = other[128 + r];
+  float po[HD];
+#pragma unroll
+  for (int e = 0; e < HD; ++e) po[e] = other[(2 + e) * 128 + r];
+  __syncwarp();
+  if (lane == 0) mbar_arrive(smem_u32(&bars->xdone[quad]));
+  const float mm = fmaxf(m, m_o);
+  const float m_use = (mm == -INFINITY) ? 0.0f : mm;
+  const float s_me = ex2(m - m_use), s_o = ex2(m_o - m_use);
+  const float lt = fmaf(l, s_me, l_o * s_o);
+  const int i = c.qt * kTile + r;
+  if (i < a.L) {
+    const float inv = lt > 0.0f ? 1.0f / lt : 0.0f;
+    const float f_me = s_me * inv, f_o = s_o * inv;
+    const size_t bn = static_cast<size_t>(c.b) * a.N + c.n;
+    uint16_t* orow = a.out + ((bn * a.L + i) * a.H + c.h) * a.D + hc * HD;
+    float o[HD];
+#pragma unroll
+    for (int e = 0; e < HD; ++e) o[e] = fmaf(keep[e], f_me, po[e] * f_o);
+#pragma unroll
+    for (int c8 = 0; c8 < HD / 8; ++c8) {
+      if (hc * HD + c8 * 8 < a.D) {
+        uint4 pk;
+        pk.x = pack2<BF16>(o[c8 * 8 + 0], o[c8 * 8 + 1]);
+        pk.y = pack2<BF16>(o[c8 * 8 + 2], o[c8 * 8 + 3]);
+        pk.z = pack2<BF16>(o[c8 * 8 + 4], o[c8 * 8 + 5]);
+        pk.w = pack2<BF16>(o[c8 * 8 + 6], o[c8 * 8 + 7]);
+        *reinterpret_cast<uint4*>(orow + c8 * 8) = pk;
+      }
+    }
+    if (hc == 0) a.lse[(bn * a.H + c.h) * a.L + i] = lt > 0.0f ? (m_use + lg2(lt)) * kLn2 : -INFINITY;
+  }
+  return true;
+}
+
+template <int DP, bool BF16, int B2>
+__device__ __forceinline__ void fwd_softmax(const FwdArgs& a, uint8_t* base, const FwdLayout<DP>& lay,
+                                            FwdBars* bars, uint32_t tmem, const WaitGuard& g, long long i0,
+                                            long long i1) {
+  constexpr bool kHasB2 = B2 != kB2None;
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int quad = w & 3, hc = w >> 2;  // TMEM lane quadrant, key-column half
+  const int r = quad * 32 + lane;       // query row within the tile == TMEM lane
+  const uint32_t trow = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+  float* xchg = reinterpret_cast<float*>(base + lay.xchg);
+  const float2 sl2 = make_float2(a.scale_log2, a.scale_log2);
+  const float2 l2e2 = make_float2(kLog2e, kLog2e);
+  const int S = a.stages, KT = a.QT;
+  uint32_t u = 0, fin = 0, grp_it = 0, s = 0, ph = 0;
+  float m = -INFINITY, l = 0.0f, a_prev = 0.0f, m_fin = 0.0f, l_fin = 0.0f;
+  float acc[DP];
+#pragma unroll
+  for (int d = 0; d < DP; ++d) acc[d] = 0.0f;
+  ItemIter cur, prev;
+  cur.init(i0, a);
+  prev = cur;
+  bool ok = true;
+  for (long long item = i0; ok && item < i1; ++item) {
+    if (item > i0) {
+      prev = cur;
+      cur.next(a);
+    }
+    const bool grp_last = item + 1 == i1 || cur.n == a.N - 1;
+    if (B2 == kB2Resident && (item == i0 || cur.n == 0)) {
+      if (!mbar_wait(smem_u32(&bars->b2_full), grp_it & 1, g)) { ok = false; break; }
+      ++grp_it;
+    }
     for (int jt = 0; jt < KT; ++jt) {
-      const uint32_t s = kv_it % kStages, kph = (kv_it / kStages) & 1;
-      const uint32_t buf = t_it & 1, bph = (t_it >> 1) & 1;
-      if (!mbar_wait(smem_u32(&bars->kv_full[s]), kph, g)) { ok = false; break; }
+      if (jt == 0) {  // the previous item's row statistics wait for its last O tile
+        m_fin = m;
+        l_fin = l;
+        m = -INFINITY;
+        l = 0.0f;
+      }
+      const uint32_t buf = u & 1, bph = (u >> 1) & 1;
+      if (!mbar_wait(smem_u32(&bars->kv_full[s]), ph, g)) { ok = false; break; }
       if (!mbar_wait(smem_u32(&bars->s_full[buf]), bph, g)) { ok = false; break; }
       tc_fence_after();
-      float y[kTile];
+      float y[64];
       {
-        uint32_t sr[4][32];
-        const uint32_t col = trow + (buf ? kColS1 : kColS0);
+        uint32_t sr[2][32];
+        const uint32_t col = trow + col_s(buf) + hc * 64;
+        tmem_ld32(col, sr[0]);
+        tmem_ld32(col + 32, sr[1]);
+        tmem_wait_ld(sr[0]);
+        tmem_wait_ld(sr[1]);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) tmem_ld32(col + q * 32, sr[q]);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) tmem_wait_ld(sr[q]);
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-#pragma unroll
-          for (int e = 0; e < 32; ++e) y[q * 32 + e] = __uint_as_float(sr[q][e]);
-      }
-      // y = S·s·log2e + bias1·log2e + bias2·log2e ; running max
-      float tmax = -INFINITY;
-      const float* b1 = reinterpret_cast<const float*>(base + lay.b1[s]);
-#pragma unroll
-      for (int c8 = 0; c8 < 16; ++c8) {
-        const float4 m0 = *reinterpret_cast<const float4*>(b1 + c8 * 8);
-        const float4 m1 = *reinterpret_cast<const float4*>(b1 + c8 * 8 + 4);
-        const float mk[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
-        uint4 pb = make_uint4(0u, 0u, 0u, 0u);
-        if (HAS_B2)
-          pb = *reinterpret_cast<const uint4*>(base + lay.b2[s] + (c8 >> 3) * 16384 + swz_offset(r, c8 & 7, 128));
-        const uint32_t pw[4] = {pb.x, pb.y, pb.z, pb.w};
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          float t = fmaf(y[c8 * 8 + e], a.scale_log2, mk[e]);
-          if (HAS_B2) {
-            const float b2v = (e & 1) ? unpack_hi<BF16>(pw[e >> 1]) : unpack_lo<BF16>(pw[e >> 1]);
-            t = fmaf(b2v, kLog2e, t);
-          }
-          y[c8 * 8 + e] = t;
-          tmax = fmaxf(tmax, t);
+        for (int e = 0; e < 32; ++e) {
+          y[e] = __uint_as_float(sr[0][e]);
+          y[32 + e] = __uint_as_float(sr[1][e]);
         }
       }
-      // S buffer and the stage's bias tiles are no longer read by this warp
+      // y = S·s·log2e + bias1·log2e (+ bias2·log2e); row max over this half (4 chains)
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      const float* b1 = reinterpret_cast<const float*>(base + lay.b1[s]) + hc * 64;
+      const uint8_t* b2t = base + (B2 == kB2Resident ? lay.b2r + jt * 32768u : lay.b2s[s]) + hc * 16384;
+#pragma unroll
+      for (int c8 = 0; c8 < 8; ++c8) {
+        const float4 m0 = *reinterpret_cast<const float4*>(b1 + c8 * 8);
+        const float4 m1 = *reinterpret_cast<const float4*>(b1 + c8 * 8 + 4);
+        const float2 mk[4] = {make_float2(m0.x, m0.y), make_float2(m0.z, m0.w), make_float2(m1.x, m1.y),
+                              make_float2(m1.z, m1.w)};
+        uint4 pb = make_uint4(0u, 0u, 0u, 0u);
+        if (kHasB2) pb = *reinterpret_cast<const uint4*>(b2t + swz_offset(r, c8, 128));
+        const uint32_t pw[4] = {pb.x, pb.y, pb.z, pb.w};
+#pragma unroll
+        for (int e2 = 0; e2 < 4; ++e2) {
+          const int x = c8 * 8 + e2 * 2;
+          float2 t = fma2(make_float2(y[x], y[x + 1]), sl2, mk[e2]);
+          if (kHasB2) t = fma2(unpack2<BF16>(pw[e2]), l2e2, t);
+          y[x] = t.x;
+          y[x + 1] = t.y;
+          mx[e2] = max3(mx[e2], t.x, t.y);
+        }
+      }
+      // this half of S and the stage's bias data are no longer read by this warp
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(smem_u32(&bars->s_free[buf]));
         mbar_arrive(smem_u32(&bars->kv_empty[s]));
+        if (B2 == kB2Resident && grp_last && jt == KT - 1) mbar_arrive(smem_u32(&bars->b2_empty));
       }
-      const float m_new = fmaxf(m, tmax);
+      const float m_new = fmaxf(m, fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])));
       const float m_use = (m_new == -INFINITY) ? 0.0f : m_new;
       const float alpha = ex2(m - m_use);
-      float rs = 0.0f;
+      const float2 nm2 = make_float2(-m_use, -m_use);
+      float2 rs[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
+      uint32_t pp[32];
 #pragma unroll
-      for (int e = 0; e < kTile; ++e) {
-        y[e] = ex2(y[e] - m_use);
-        rs += y[e];
+      for (int x = 0; x < 64; x += 2) {
+        const float2 t = add2(make_float2(y[x], y[x + 1]), nm2);
+        const float p0 = ex2(t.x), p1 = ex2(t.y);
+        rs[(x >> 1) & 1] = add2(rs[(x >> 1) & 1], make_float2(p0, p1));
+        pp[x >> 1] = pack2<BF16>(p0, p1);
       }
-      l = fmaf(l, alpha, rs);
-      // P -> shared memory (K-major, 128B swizzle, two 64-key halves)
+      l = fmaf(l, alpha, (rs[0].x + rs[0].y) + (rs[1].x + rs[1].y));
+      // P half -> TMEM (64 keys = 32 columns of packed pairs)
       if (!mbar_wait(smem_u32(&bars->p_empty[buf]), bph ^ 1, g)) { ok = false; break; }
-      uint8_t* pbase = base + lay.p[buf];
-#pragma unroll
-      for (int c8 = 0; c8 < 16; ++c8) {
-        uint4 pk;
-        pk.x = pack2<BF16>(y[c8 * 8 + 0], y[c8 * 8 + 1]);
-        pk.y = pack2<BF16>(y[c8 * 8 + 2], y[c8 * 8 + 3]);
-        pk.z = pack2<BF16>(y[c8 * 8 + 4], y[c8 * 8 + 5]);
-        pk.w = pack2<BF16>(y[c8 * 8 + 6], y[c8 * 8 + 7]);
-        *reinterpret_cast<uint4*>(pbase + (c8 >> 3) * 16384 + swz_offset(r, c8 & 7, 128)) = pk;
-      }
-      fence_proxy_async_smem();
+      tc_fence_after();
+      tmem_st32(trow + col_p(buf) + hc * 32, pp);
+      tmem_wait_st();
+      tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&bars->p_full[buf]));
-      if (jt > 0 && !fwd_consume_o<DP>(t_it - 1, a_prev, acc, bars, trow, lane, g)) { ok = false; break; }
-      a_prev = alpha;
-      m = m_new;
-      ++t_it;
-      ++kv_it;
-    }
-    if (!ok) break;
-    if (!fwd_consume_o<DP>(t_it - 1, a_prev, acc, bars, trow, lane, g)) { ok = false; break; }
-    // epilogue
-    const int i = c.qt * kTile + r;
-    if (i < a.L) {
-      const float inv = l > 0.0f ? 1.0f / l : 0.0f;
-      const size_t bn = static_cast<size_t>(c.b) * a.N + c.n;
-      uint16_t* orow = a.out + ((bn * a.L + i) * a.H + c.h) * a.D;
+      if (u > 0) {
+        if (!fwd_consume_o<DP>(u - 1, a_prev, acc, bars, trow, hc, lane, g)) { ok = false; break; }
+        if (jt == 0) {  // tile u-1 was the last of the previous item
+          if (!fwd_epilogue<DP, BF16>(a, prev, acc, m_fin, l_fin, fin++, bars, xchg, quad, hc, r, lane, g)) {
+            ok = false;
+            break;
+          }
 #pragma unroll
-      for (int c8 = 0; c8 < DP / 8; ++c8) {
-        if (c8 * 8 < a.D) {
-          uint4 pk;
-          pk.x = pack2<BF16>(acc[c8 * 8 + 0] * inv, acc[c8 * 8 + 1] * inv);
-          pk.y = pack2<BF16>(acc[c8 * 8 + 2] * inv, acc[c8 * 8 + 3] * inv);
-          pk.z = pack2<BF16>(acc[c8 * 8 + 4] * inv, acc[c8 * 8 + 5] * inv);
-          pk.w = pack2<BF16>(acc[c8 * 8 + 6] * inv, acc[c8 * 8 + 7] * inv);
-          *reinterpret_cast<uint4*>(orow + c8 * 8) = pk;
+          for (int d = 0; d < DP; ++d) acc[d] = 0.0f;
         }
       }
-      const float m_fin = (m == -INFINITY) ? 0.0f : m;
-      a.lse[(bn * a.H + c.h) * a.L + i] = l > 0.0f ? (m_fin + lg2(l)) * kLn2 : -INFINITY;
+      a_prev = alpha;
+      m = m_new;
+      ++u;
+      if (++s == static_cast<uint32_t>(S)) {
+        s = 0;
+        ph ^= 1;
+      }
     }
+  }
+  if (ok && u > 0) {
+    if (fwd_consume_o<DP>(u - 1, a_prev, acc, bars, trow, hc, lane, g))
+      fwd_epilogue<DP, BF16>(a, cur, acc, m, l, fin++, bars, xchg, quad, hc, r, lane, g);
   }
 }
 
-template <int DP, bool BF16, bool HAS_B2>
-__global__ void __launch_bounds__(192, 1) evo_fwd_kernel(const __grid_constant__ FwdArgs a) {
+template <int DP, bool BF16, int B2>
+__global__ void __launch_bounds__(kThreads, 1) evo_fwd_kernel(const __grid_constant__ FwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const FwdLayout<DP> lay(HAS_B2);
+  const FwdLayout<DP> lay(B2, a.stages, a.QT);
   FwdBars* bars = reinterpret_cast<FwdBars*>(base + lay.bars);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long i0 = static_cast<long long>(blockIdx.x) * a.chunk;
+  const long long i1 = i0 + a.chunk < a.items ? i0 + a.chunk : a.items;
   if (threadIdx.x == 0) {
     bars->abort = 0;
-    mbar_init(smem_u32(&bars->q_full), 1);
-    mbar_init(smem_u32(&bars->q_empty), 1);
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(smem_u32(&bars->kv_full[s]), 32);
-      mbar_init(smem_u32(&bars->kv_empty[s]), 1 + 4);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_u32(&bars->q_full[s]), 1);
+      mbar_init(smem_u32(&bars->q_empty[s]), 1);
     }
+    for (int s = 0; s < kMaxStages; ++s) {
+      mbar_init(smem_u32(&bars->kv_full[s]), 32);
+      mbar_init(smem_u32(&bars->kv_empty[s]), 1 + kSoftmaxWarps);
+    }
+    mbar_init(smem_u32(&bars->b2_full), 32);
+    mbar_init(smem_u32(&bars->b2_empty), kSoftmaxWarps);
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&bars->s_full[b]), 1);
-      mbar_init(smem_u32(&bars->s_free[b]), 4);
-      mbar_init(smem_u32(&bars->p_full[b]), 4);
+      mbar_init(smem_u32(&bars->s_free[b]), kSoftmaxWarps);
+      mbar_init(smem_u32(&bars->p_full[b]), kSoftmaxWarps);
       mbar_init(smem_u32(&bars->p_empty[b]), 1);
       mbar_init(smem_u32(&bars->o_full[b]), 1);
-      mbar_init(smem_u32(&bars->o_free[b]), 4);
+      mbar_init(smem_u32(&bars->o_free[b]), kSoftmaxWarps);
+    }
+    for (int q = 0; q < 4; ++q) {
+      mbar_init(smem_u32(&bars->xsum[q]), 2);
+      mbar_init(smem_u32(&bars->xdone[q]), 2);
     }
     mbar_init(smem_u32(&bars->drain), 1);
     fence_barrier_init();
   }
-  if (warp == 4 && lane == 0) {
+  if (warp == kProducerWarp && lane == 0) {
     tma_prefetch_desc(&a.tq);
     tma_prefetch_desc(&a.tk);
     tma_prefetch_desc(&a.tv);
-    if (HAS_B2 && a.bias2_mode == kBias2Tma) tma_prefetch_desc(&a.tb2);
+    if (B2 != kB2None && a.bias2_mode == kBias2Tma) tma_prefetch_desc(&a.tb2);
   }
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(&bars->tmem_slot), 512);
     tmem_relinquish();
   }
@@ -416,41 +595,61 @@ __global__ void __launch_bounds__(192, 1) evo_fwd_kernel(const __grid_constant__
   const uint32_t tmem = bars->tmem_slot;
   const WaitGuard g{a.wait_ns, a.status, &bars->abort};
 
-  if (warp == 4) {
-    fwd_producer<DP, BF16, HAS_B2>(a, base, lay, bars, g, lane);
-  } else if (warp == 5) {
-    if (lane == 0) fwd_mma<DP, BF16>(a, base, lay, bars, tmem, g);
+  if (warp == kProducerWarp) {
+    fwd_producer<DP, BF16, B2>(a, base, lay, bars, g, lane, i0, i1);
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) fwd_mma<DP, BF16>(a, base, lay, bars, tmem, g, i0, i1);
     __syncwarp();
   } else {
-    fwd_softmax<DP, BF16, HAS_B2>(a, base, lay, bars, tmem, g);
+    fwd_softmax<DP, BF16, B2>(a, base, lay, bars, tmem, g, i0, i1);
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
 }
 
-template <int DP, bool BF16, bool HAS_B2>
-cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t st) {
-  const FwdLayout<DP> lay(HAS_B2);
+constexpr size_t kMaxSmem = 232448;  // 227 KB opt-in limit per block
+
+template <int DP, bool BF16, int B2>
+cudaError_t launch_fwd_t(FwdArgs a, cudaStream_t st) {
+  const FwdLayout<DP> lay(B2, a.stages, a.QT);
   // At least 116 KB so that two CTAs never share an SM: each allocates all 512
   // TMEM columns, and a second resident CTA would stall in tcgen05.alloc.
   const size_t smem = (lay.total + 1024 > 116u * 1024u) ? lay.total + 1024 : 116u * 1024u;
-  auto kern = evo_fwd_kernel<DP, BF16, HAS_B2>;
+  auto kern = evo_fwd_kernel<DP, BF16, B2>;
   static bool limit_set[64] = {};
-  cudaError_t e = ensure_smem_limit(kern, smem, limit_set);
+  cudaError_t e = ensure_smem_limit(kern, kMaxSmem, limit_set);
   if (e != cudaSuccess) return e;
-  const long long grid = a.items < num_sms() ? a.items : num_sms();
-  kern<<<static_cast<unsigned>(grid), 192, smem, st>>>(a);
+  const long long sms = num_sms();
+  a.chunk = (a.items + sms - 1) / sms;
+  const long long grid = (a.items + a.chunk - 1) / a.chunk;
+  kern<<<static_cast<unsigned>(grid), kThreads, smem, st>>>(a);
   return cudaGetLastError();
 }
 
+// Deepest K/V ring that fits, and whether the pair-bias tiles of one
+// (b, h, q-tile) group can stay resident.
 template <int DP, bool BF16>
-cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t st) {
-  return a.bias2_mode == kBias2None ? launch_fwd_t<DP, BF16, false>(a, st) : launch_fwd_t<DP, BF16, true>(a, st);
+cudaError_t launch_fwd_d(FwdArgs a, cudaStream_t st) {
+  auto fits = [&](int kind, int stages) { return FwdLayout<DP>(kind, stages, a.QT).total + 1024 <= kMaxSmem; };
+  if (a.bias2_mode == kBias2None) {
+    a.stages = fits(kB2None, 4) ? 4 : 2;
+    return launch_fwd_t<DP, BF16, kB2None>(a, st);
+  }
+  for (int stages = 4; stages >= 2; --stages) {
+    if (a.QT <= 4 && fits(kB2Resident, stages)) {
+      a.stages = stages;
+      a.b2_resident = 1;
+      return launch_fwd_t<DP, BF16, kB2Resident>(a, st);
+    }
+  }
+  a.stages = 2;
+  a.b2_resident = 0;
+  return launch_fwd_t<DP, BF16, kB2Stream>(a, st);
 }
 
 }  // namespace

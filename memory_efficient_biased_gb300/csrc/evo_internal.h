@@ -22,7 +22,10 @@ struct FwdArgs {
   float* lse;               // [B,N,H,L]
   int B, N, L, H, D;
   int QT;                   // ceil(L / 128)
-  long long items;          // B*N*H*QT work items (b, n, h, query tile)
+  long long items;          // B*H*QT*N work items, ordered (b, h, query tile, n)
+  long long chunk;          // consecutive items per CTA
+  int stages;               // depth of the K/V ring (2..4)
+  int b2_resident;          // pair-bias tiles of the current (b, h, q-tile) kept in smem
   float scale_log2;         // D^-1/2 * log2(e)
   int bias2_mode;
   uint64_t wait_ns;
