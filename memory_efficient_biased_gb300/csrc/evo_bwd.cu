@@ -13,18 +13,22 @@
 //
 // Kernels, in launch order on the caller's stream:
 //   evo_bwd_pre       delta [B,N,H,L] fp32; zeroes the fp32 dQ accumulator.
-//   evo_bwd_main      persistent over (b, n, h, key tile).  Per query tile the
-//                     MMA thread computes S = Q Kᵀ and dP = dO Vᵀ into TMEM
-//                     (lane = query); four compute warps form P and dS (fp16 /
-//                     bf16) in swizzled shared memory; the MMA thread then
-//                     accumulates dV += Pᵀ dO and dK += dSᵀ Q in TMEM (the same
-//                     smem tiles read as MN-major A operands) and forms
-//                     dQ_tile = dS K, which the compute warps add into the fp32
-//                     accumulator.  dK and dV are written once per item.
+//   evo_bwd_main      persistent over a contiguous range of (b, h, key tile, n)
+//                     items, streamed as one sequence of (item, query tile)
+//                     steps.  The MMA thread computes S = Q Kᵀ and dP = dO Vᵀ
+//                     into TMEM (lane = query) one step ahead; eight compute
+//                     warps (each 32 query rows × 64 keys) form P and dS
+//                     (fp16 / bf16) in swizzled shared memory; the MMA thread
+//                     then accumulates dV += Pᵀ dO and dK += dSᵀ Q in TMEM (the
+//                     same smem tiles read as MN-major A operands, dK/dV double-
+//                     buffered across items) and forms dQ_tile = dS K, which
+//                     the compute warps add into the fp32 accumulator.
 //   evo_bwd_dq_cast   dQ = accumulator rounded to the dtype.
 //   evo_bwd_db2_part  (pair bias only) per (b, h, query tile, key tile,
-//                     n-group): recompute S, dP, P, dS and sum dS over the
-//                     group's n in a fixed order in registers; write fp32.
+//                     n-group): recompute S and dP (double-buffered in TMEM),
+//                     form P and dS, and sum dS over the group's n in a fixed
+//                     order in registers (eight warps, 32 rows × 64 keys each);
+//                     write fp32.
 //   evo_bwd_db2_sum   dbias2 = Σ_groups partial in fixed order, cast.
 // Both pair-bias stages run in a fixed order, so dbias2 is bitwise
 // reproducible.  dQ uses fp32 atomics and is not.
@@ -103,6 +107,11 @@ __global__ void __launch_bounds__(256) evo_bwd_db2_sum(const BwdArgs a) {
 }
 
 // ============================================================ shared pieces
+constexpr int kComputeWarps = 8;
+constexpr int kThreads = (kComputeWarps + 2) * 32;
+constexpr int kProducerWarp = kComputeWarps, kMmaWarp = kComputeWarps + 1;
+constexpr size_t kMaxSmem = 232448;  // 227 KB opt-in limit per block
+
 // Pair-bias tile [128 queries][128 keys] in two 64-key halves, 128B swizzle —
 // the layout the 3-D TMA map with box (64, 128, 1) writes.  Generic-load fill
 // for L % 8 != 0 (no TMA: the row pitch is not a multiple of 16 bytes).
@@ -138,31 +147,74 @@ __device__ __forceinline__ void fill_b1_chunk(float* dst, const uint16_t* b1row,
   reinterpret_cast<float4*>(dst)[lane] = m4;
 }
 
-// P (or dS) row of one thread -> [query][key] tile, K-major 128B swizzle, two 64-key halves.
-template <bool BF16>
-__device__ __forceinline__ void store_row_chunk(uint8_t* tile, int r, int c, const float (&x)[32]) {
+// lse (× log2 e; +inf for rows past L or with an empty softmax, so P = 0) and
+// delta for queries i0..i0+127 of slice bnh.
+__device__ __forceinline__ void fill_lse_delta(float* dst, const float* lse, const float* delta, size_t bnh, int L,
+                                               int i0, int lane) {
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const int chunk16 = c * 4 + q;  // 16-byte chunk index 0..15 along the 128 keys
-    uint4 pk;
-    pk.x = pack2<BF16>(x[q * 8 + 0], x[q * 8 + 1]);
-    pk.y = pack2<BF16>(x[q * 8 + 2], x[q * 8 + 3]);
-    pk.z = pack2<BF16>(x[q * 8 + 4], x[q * 8 + 5]);
-    pk.w = pack2<BF16>(x[q * 8 + 6], x[q * 8 + 7]);
-    *reinterpret_cast<uint4*>(tile + (chunk16 >> 3) * 16384 + swz_offset(r, chunk16 & 7, 128)) = pk;
+  for (int e = 0; e < 4; ++e) {
+    const int i = i0 + lane * 4 + e;
+    float lv = INFINITY, dv = 0.0f;
+    if (i < L) {
+      const float x = lse[bnh * L + i];
+      lv = (x == -INFINITY) ? INFINITY : x * kLog2e;
+      dv = delta[bnh * L + i];
+    }
+    dst[lane * 4 + e] = lv;
+    dst[128 + lane * 4 + e] = dv;
   }
 }
 
+// Incremental (b, h, key tile, n) iterator, n fastest.
+struct KvIter {
+  int b, h, jt, n;
+  __device__ __forceinline__ void init(long long item, const BwdArgs& a) {
+    long long t = item;
+    n = static_cast<int>(t % a.N);
+    t /= a.N;
+    jt = static_cast<int>(t % a.QT);
+    t /= a.QT;
+    h = static_cast<int>(t % a.H);
+    b = static_cast<int>(t / a.H);
+  }
+  __device__ __forceinline__ void next(const BwdArgs& a) {
+    if (++n == a.N) {
+      n = 0;
+      if (++jt == a.QT) {
+        jt = 0;
+        if (++h == a.H) {
+          h = 0;
+          ++b;
+        }
+      }
+    }
+  }
+};
+
 // ============================================================ evo_bwd_main
-constexpr uint32_t kColS = 0, kColDP = 128, kColDK = 256, kColDV = 320, kColDQ0 = 384, kColDQ1 = 448;
+enum B2Kind : int { kB2None = 0, kB2Resident = 1, kB2Stream = 2 };
+
+__device__ __forceinline__ uint32_t col_s() { return 0u; }
+__device__ __forceinline__ uint32_t col_dp() { return 128u; }
+template <int DP>
+__host__ __device__ constexpr int kv_acc_buffers() { return DP <= 32 ? 2 : 1; }
+template <int DP>
+__device__ __forceinline__ uint32_t col_dk(uint32_t b) { return 256u + b * 2 * DP; }
+template <int DP>
+__device__ __forceinline__ uint32_t col_dv(uint32_t b) { return 256u + b * 2 * DP + DP; }
+template <int DP>
+__device__ __forceinline__ uint32_t col_dq(uint32_t b) { return 256u + kv_acc_buffers<DP>() * 2 * DP + b * DP; }
+
+constexpr int kMaxQStages = 4;
 
 struct MainBars {
-  uint64_t kv_full, kv_empty;
-  uint64_t q_full[2], q_empty[2];
+  uint64_t kv_full[2], kv_empty[2];
+  uint64_t q_full[kMaxQStages], q_empty[kMaxQStages];
+  uint64_t b2_full, b2_empty;
   uint64_t st_full, st_free;
   uint64_t ds_full, ds_empty;
   uint64_t dq_full[2], dq_free[2];
-  uint64_t dkdv_full, dkdv_free;
+  uint64_t dkdv_full[2], dkdv_free[2];
   uint64_t drain;
   uint32_t tmem_slot;
   int abort;
@@ -170,345 +222,522 @@ struct MainBars {
 
 template <int DP>
 struct MainLayout {
-  static constexpr int kStages = DP == 64 ? 1 : 2;
   static constexpr uint32_t kTB = kTile * DP * 2;
-  uint32_t k, v, q[2], d_o[2], b2[2], b1, p, ds, bars, total;
-  __host__ __device__ explicit MainLayout(bool has_b2) {
+  uint32_t k[2], v[2], b1[2], q[kMaxQStages], d_o[kMaxQStages], ld[kMaxQStages], b2s[kMaxQStages], b2r, p, ds,
+      bars, total;
+  __host__ __device__ MainLayout(int b2kind, int qs, int QT) {
     uint32_t off = 0;
-    k = off;
-    off += kTB;
-    v = off;
-    off += kTB;
-    for (int s = 0; s < kStages; ++s) q[s] = off + s * kTB;
-    off += kStages * kTB;
-    for (int s = 0; s < kStages; ++s) d_o[s] = off + s * kTB;
-    off += kStages * kTB;
-    for (int s = 0; s < kStages; ++s) b2[s] = off + s * 32768u;
-    if (has_b2) off += kStages * 32768u;
+    for (int s = 0; s < 2; ++s) {
+      k[s] = off;
+      v[s] = off + kTB;
+      off += 2 * kTB;
+    }
+    for (int s = 0; s < kMaxQStages; ++s) {
+      const int t = s < qs ? s : 0;
+      q[s] = off + t * 2 * kTB;
+      d_o[s] = q[s] + kTB;
+    }
+    off += qs * 2 * kTB;
+    for (int s = 0; s < kMaxQStages; ++s) b2s[s] = off + (s < qs ? s : 0) * 32768u;
+    if (b2kind == kB2Stream) off += qs * 32768u;
+    b2r = off;
+    if (b2kind == kB2Resident) off += QT * 32768u;
     p = off;
     off += 32768u;
     ds = off;
     off += 32768u;
-    b1 = off;
+    for (int s = 0; s < 2; ++s) b1[s] = off + s * 512u;
     off += 1024u;
+    for (int s = 0; s < kMaxQStages; ++s) ld[s] = off + (s < qs ? s : 0) * 1024u;
+    off += qs * 1024u;
     bars = off;
     off += (sizeof(MainBars) + 127) & ~127u;
     total = off;
   }
 };
 
-struct MainItem {
-  int b, n, h, jt;
-};
-__device__ __forceinline__ MainItem main_item(long long item, const BwdArgs& a) {
-  MainItem c;
-  long long t = item;
-  c.jt = static_cast<int>(t % a.QT);
-  t /= a.QT;
-  c.h = static_cast<int>(t % a.H);
-  t /= a.H;
-  c.n = static_cast<int>(t % a.N);
-  c.b = static_cast<int>(t / a.N);
-  return c;
-}
-
-template <int DP, bool BF16, bool HAS_B2>
+template <int DP, bool BF16, int B2>
 __device__ __forceinline__ void main_producer(const BwdArgs& a, uint8_t* base, const MainLayout<DP>& lay,
-                                              MainBars* bars, const WaitGuard& g, int lane, long long items) {
-  constexpr int NS = MainLayout<DP>::kStages;
+                                              MainBars* bars, const WaitGuard& g, int lane, long long i0,
+                                              long long i1) {
   constexpr uint32_t kTB = MainLayout<DP>::kTB;
-  const uint32_t q_bytes = 2 * kTB + ((HAS_B2 && a.bias2_mode == kBias2Tma) ? 32768u : 0u);
-  uint32_t it_ctr = 0, item_ctr = 0;
+  const int QS = a.q_stages, QT = a.QT;
+  const bool tma_b2 = a.bias2_mode == kBias2Tma;
+  const uint32_t q_bytes = 2 * kTB + ((B2 == kB2Stream && tma_b2) ? 32768u : 0u);
+  uint32_t it_ctr = 0, item_ctr = 0, grp_it = 0, s = 0, ph = 0;
+  KvIter c;
+  c.init(i0, a);
   bool ok = true;
-  for (long long item = blockIdx.x; ok && item < items; item += gridDim.x, ++item_ctr) {
-    const MainItem c = main_item(item, a);
-    const int bn = c.b * a.N + c.n;
-    if (!mbar_wait(smem_u32(&bars->kv_empty), (item_ctr & 1) ^ 1, g)) { ok = false; break; }
-    fill_b1_chunk<BF16>(reinterpret_cast<float*>(base + lay.b1),
-                        a.bias1 ? a.bias1 + static_cast<size_t>(bn) * a.L : nullptr, a.L, c.jt * kTile, lane);
-    if (lane == 0) {
-      const uint32_t full = smem_u32(&bars->kv_full);
-      mbar_arrive_expect_tx(full, 2 * kTB);
-      tma_load_4d(smem_u32(base + lay.k), &a.tk, full, 0, c.h, c.jt * kTile, bn);
-      tma_load_4d(smem_u32(base + lay.v), &a.tv, full, 0, c.h, c.jt * kTile, bn);
-    } else {
-      mbar_arrive(smem_u32(&bars->kv_full));
-    }
-    for (int it = 0; it < a.QT; ++it, ++it_ctr) {
-      const uint32_t s = it_ctr % NS, ph = (it_ctr / NS) & 1;
-      if (!mbar_wait(smem_u32(&bars->q_empty[s]), ph ^ 1, g)) { ok = false; break; }
-      if (HAS_B2 && a.bias2_mode == kBias2Loads)
-        fill_b2_tile_loads(base + lay.b2[s], a.bias2 + static_cast<size_t>(c.b * a.H + c.h) * a.L * a.L, a.L,
-                           it * kTile, c.jt * kTile, lane);
-      const uint32_t full = smem_u32(&bars->q_full[s]);
-      if (lane == 0) {
-        mbar_arrive_expect_tx(full, q_bytes);
-        tma_load_4d(smem_u32(base + lay.q[s]), &a.tq, full, 0, c.h, it * kTile, bn);
-        tma_load_4d(smem_u32(base + lay.d_o[s]), &a.tdo, full, 0, c.h, it * kTile, bn);
-        if (HAS_B2 && a.bias2_mode == kBias2Tma) {
-          const int bh = c.b * a.H + c.h;
-          tma_load_3d(smem_u32(base + lay.b2[s]), &a.tb2, full, c.jt * kTile, it * kTile, bh);
-          tma_load_3d(smem_u32(base + lay.b2[s] + 16384), &a.tb2, full, c.jt * kTile + 64, it * kTile, bh);
+  for (long long item = i0; ok && item < i1; ++item, ++item_ctr, c.next(a)) {
+    const int bn = c.b * a.N + c.n, bh = c.b * a.H + c.h;
+    const size_t bnh = static_cast<size_t>(bn) * a.H + c.h;
+    if (B2 == kB2Resident && (item == i0 || c.n == 0)) {
+      if (!mbar_wait(smem_u32(&bars->b2_empty), (grp_it & 1) ^ 1, g)) { ok = false; break; }
+      const uint32_t full = smem_u32(&bars->b2_full);
+      if (tma_b2) {
+        if (lane == 0) {
+          mbar_expect_tx(full, QT * 32768u);
+          for (int t = 0; t < QT; ++t) {
+            tma_load_3d(smem_u32(base + lay.b2r + t * 32768u), &a.tb2, full, c.jt * kTile, t * kTile, bh);
+            tma_load_3d(smem_u32(base + lay.b2r + t * 32768u + 16384u), &a.tb2, full, c.jt * kTile + 64,
+                        t * kTile, bh);
+          }
         }
       } else {
-        mbar_arrive(full);
+        for (int t = 0; t < QT; ++t)
+          fill_b2_tile_loads(base + lay.b2r + t * 32768u, a.bias2 + static_cast<size_t>(bh) * a.L * a.L, a.L,
+                             t * kTile, c.jt * kTile, lane);
+      }
+      mbar_arrive(full);
+      ++grp_it;
+    }
+    const uint32_t kb = item_ctr & 1;
+    if (!mbar_wait(smem_u32(&bars->kv_empty[kb]), ((item_ctr >> 1) & 1) ^ 1, g)) { ok = false; break; }
+    {
+      const uint32_t full = smem_u32(&bars->kv_full[kb]);
+      if (lane == 0) {
+        mbar_expect_tx(full, 2 * kTB);
+        tma_load_4d(smem_u32(base + lay.k[kb]), &a.tk, full, 0, c.h, c.jt * kTile, bn);
+        tma_load_4d(smem_u32(base + lay.v[kb]), &a.tv, full, 0, c.h, c.jt * kTile, bn);
+      }
+      fill_b1_chunk<BF16>(reinterpret_cast<float*>(base + lay.b1[kb]),
+                          a.bias1 ? a.bias1 + static_cast<size_t>(bn) * a.L : nullptr, a.L, c.jt * kTile, lane);
+      mbar_arrive(full);
+    }
+    for (int it = 0; it < QT; ++it, ++it_ctr) {
+      if (!mbar_wait(smem_u32(&bars->q_empty[s]), ph ^ 1, g)) { ok = false; break; }
+      const uint32_t full = smem_u32(&bars->q_full[s]);
+      if (lane == 0) {
+        mbar_expect_tx(full, q_bytes);
+        tma_load_4d(smem_u32(base + lay.q[s]), &a.tq, full, 0, c.h, it * kTile, bn);
+        tma_load_4d(smem_u32(base + lay.d_o[s]), &a.tdo, full, 0, c.h, it * kTile, bn);
+        if (B2 == kB2Stream && tma_b2) {
+          tma_load_3d(smem_u32(base + lay.b2s[s]), &a.tb2, full, c.jt * kTile, it * kTile, bh);
+          tma_load_3d(smem_u32(base + lay.b2s[s] + 16384), &a.tb2, full, c.jt * kTile + 64, it * kTile, bh);
+        }
+      }
+      if (B2 == kB2Stream && !tma_b2)
+        fill_b2_tile_loads(base + lay.b2s[s], a.bias2 + static_cast<size_t>(bh) * a.L * a.L, a.L, it * kTile,
+                           c.jt * kTile, lane);
+      fill_lse_delta(reinterpret_cast<float*>(base + lay.ld[s]), a.lse, a.delta, bnh, a.L, it * kTile, lane);
+      mbar_arrive(full);
+      if (++s == static_cast<uint32_t>(QS)) {
+        s = 0;
+        ph ^= 1;
       }
     }
   }
-  if (item_ctr > 0) drain_wait(smem_u32(&bars->kv_full), (item_ctr - 1) & 1, a.wait_ns, a.status);
-  for (uint32_t s = 0; s < static_cast<uint32_t>(NS); ++s) {
-    const uint32_t issued = (it_ctr + NS - 1 - s) / NS;
-    if (issued > 0) drain_wait(smem_u32(&bars->q_full[s]), (issued - 1) & 1, a.wait_ns, a.status);
+  for (uint32_t b = 0; b < 2; ++b) {
+    const uint32_t issued = (item_ctr + 1 - b) / 2;
+    if (issued > 0) drain_wait(smem_u32(&bars->kv_full[b]), (issued - 1) & 1, a.wait_ns, a.status);
   }
+  for (uint32_t st = 0; st < static_cast<uint32_t>(QS); ++st) {
+    const uint32_t issued = (it_ctr + QS - 1 - st) / QS;
+    if (issued > 0) drain_wait(smem_u32(&bars->q_full[st]), (issued - 1) & 1, a.wait_ns, a.status);
+  }
+  if (B2 == kB2Resident && grp_it > 0) drain_wait(smem_u32(&bars->b2_full), (grp_it - 1) & 1, a.wait_ns, a.status);
+}
+
+// Step bookkeeping shared by the MMA thread: step u = (item index, query tile).
+struct Step {
+  uint32_t u, item_ctr;
+  int it;
+  uint32_t qs, qph;  // Q/dO ring stage and phase of this step
+};
+
+template <int DP, bool BF16>
+__device__ __forceinline__ bool main_issue_sdp(const Step& st, uint8_t* base, const MainLayout<DP>& lay,
+                                               MainBars* bars, uint32_t tmem, const WaitGuard& g) {
+  constexpr uint32_t RB = DP * 2;
+  constexpr uint32_t SWZ = swizzle_for_row(RB);
+  constexpr uint32_t id_s = idesc_f16(128, 128, BF16, false, false);  // K-major A and B
+  const uint32_t kb = st.item_ctr & 1;
+  if (st.it == 0 && !mbar_wait(smem_u32(&bars->kv_full[kb]), (st.item_ctr >> 1) & 1, g)) return false;
+  if (!mbar_wait(smem_u32(&bars->q_full[st.qs]), st.qph, g)) return false;
+  if (!mbar_wait(smem_u32(&bars->st_free), (st.u & 1) ^ 1, g)) return false;
+  tc_fence_after();
+  const uint32_t q_addr = smem_u32(base + lay.q[st.qs]), do_addr = smem_u32(base + lay.d_o[st.qs]);
+  const uint32_t k_addr = smem_u32(base + lay.k[kb]), v_addr = smem_u32(base + lay.v[kb]);
+#pragma unroll
+  for (int k = 0; k < DP / 16; ++k)
+    umma_ss(tmem + col_s(), smem_desc(q_addr + k * 32, 16, 8 * RB, SWZ), smem_desc(k_addr + k * 32, 16, 8 * RB, SWZ),
+            id_s, k > 0);
+#pragma unroll
+  for (int k = 0; k < DP / 16; ++k)
+    umma_ss(tmem + col_dp(), smem_desc(do_addr + k * 32, 16, 8 * RB, SWZ),
+            smem_desc(v_addr + k * 32, 16, 8 * RB, SWZ), id_s, k > 0);
+  umma_commit(smem_u32(&bars->st_full));
+  return true;
 }
 
 template <int DP, bool BF16>
-__device__ __forceinline__ void main_mma(const BwdArgs& a, uint8_t* base, const MainLayout<DP>& lay,
-                                         MainBars* bars, uint32_t tmem, const WaitGuard& g, long long items) {
-  constexpr int NS = MainLayout<DP>::kStages;
+__device__ __forceinline__ bool main_issue_grads(const Step& st, int QT, uint8_t* base, const MainLayout<DP>& lay,
+                                                 MainBars* bars, uint32_t tmem, const WaitGuard& g) {
   constexpr uint32_t RB = DP * 2;
   constexpr uint32_t SWZ = swizzle_for_row(RB);
-  constexpr uint32_t id_s = idesc_f16(128, 128, BF16, false, false);   // S, dP: K-major A and B
-  constexpr uint32_t id_kv = idesc_f16(128, DP, BF16, true, true);     // dV, dK: MN-major A and B
-  constexpr uint32_t id_q = idesc_f16(128, DP, BF16, false, true);     // dQ: K-major A, MN-major B
+  constexpr uint32_t id_kv = idesc_f16(128, DP, BF16, true, true);  // dV, dK: MN-major A and B
+  constexpr uint32_t id_q = idesc_f16(128, DP, BF16, false, true);  // dQ: K-major A, MN-major B
+  constexpr int NB = kv_acc_buffers<DP>();
+  const uint32_t kb = st.item_ctr & 1;
+  const uint32_t db = st.item_ctr % NB, dph = (st.item_ctr / NB) & 1;
+  const uint32_t qb = st.u & 1;
+  if (!mbar_wait(smem_u32(&bars->ds_full), st.u & 1, g)) return false;
+  if (st.it == 0 && !mbar_wait(smem_u32(&bars->dkdv_free[db]), dph ^ 1, g)) return false;
+  if (!mbar_wait(smem_u32(&bars->dq_free[qb]), ((st.u >> 1) & 1) ^ 1, g)) return false;
+  tc_fence_after();
   const uint32_t p_addr = smem_u32(base + lay.p), ds_addr = smem_u32(base + lay.ds);
-  const uint32_t k_addr = smem_u32(base + lay.k), v_addr = smem_u32(base + lay.v);
-  uint32_t it_ctr = 0, item_ctr = 0;
-  bool ok = true;
-  for (long long item = blockIdx.x; ok && item < items; item += gridDim.x, ++item_ctr) {
-    if (!mbar_wait(smem_u32(&bars->kv_full), item_ctr & 1, g)) { ok = false; break; }
-    // dK / dV of the previous item have been read out of TMEM
-    if (!mbar_wait(smem_u32(&bars->dkdv_free), (item_ctr & 1) ^ 1, g)) { ok = false; break; }
-    for (int it = 0; it < a.QT; ++it, ++it_ctr) {
-      const uint32_t s = it_ctr % NS, ph = (it_ctr / NS) & 1;
-      if (!mbar_wait(smem_u32(&bars->q_full[s]), ph, g)) { ok = false; break; }
-      if (!mbar_wait(smem_u32(&bars->st_free), (it_ctr & 1) ^ 1, g)) { ok = false; break; }
-      tc_fence_after();
-      const uint32_t q_addr = smem_u32(base + lay.q[s]), do_addr = smem_u32(base + lay.d_o[s]);
+  const uint32_t q_addr = smem_u32(base + lay.q[st.qs]), do_addr = smem_u32(base + lay.d_o[st.qs]);
+  const uint32_t k_addr = smem_u32(base + lay.k[kb]);
 #pragma unroll
-      for (int k = 0; k < DP / 16; ++k) {
-        umma_ss(tmem + kColS, smem_desc(q_addr + k * 32, 16, 8 * RB, SWZ), smem_desc(k_addr + k * 32, 16, 8 * RB, SWZ),
-                id_s, k > 0);
-      }
+  for (int k = 0; k < 8; ++k) {  // dV += Pᵀ dO   (K = 128 queries)
+    const uint64_t ad = smem_desc(p_addr + k * 16 * 128, 16384, 1024, kSwizzle128B);
+    const uint64_t bd = smem_desc(do_addr + k * 16 * RB, kTile * RB, 8 * RB, SWZ);
+    umma_ss(tmem + col_dv<DP>(db), ad, bd, id_kv, (st.it > 0 || k > 0) ? 1u : 0u);
+  }
 #pragma unroll
-      for (int k = 0; k < DP / 16; ++k) {
-        umma_ss(tmem + kColDP, smem_desc(do_addr + k * 32, 16, 8 * RB, SWZ),
-                smem_desc(v_addr + k * 32, 16, 8 * RB, SWZ), id_s, k > 0);
-      }
-      umma_commit(smem_u32(&bars->st_full));
-      // P and dS of this query tile are in shared memory
-      if (!mbar_wait(smem_u32(&bars->ds_full), it_ctr & 1, g)) { ok = false; break; }
-      const uint32_t qb = it_ctr & 1;
-      if (!mbar_wait(smem_u32(&bars->dq_free[qb]), ((it_ctr >> 1) & 1) ^ 1, g)) { ok = false; break; }
-      tc_fence_after();
+  for (int k = 0; k < 8; ++k) {  // dK += dSᵀ Q
+    const uint64_t ad = smem_desc(ds_addr + k * 16 * 128, 16384, 1024, kSwizzle128B);
+    const uint64_t bd = smem_desc(q_addr + k * 16 * RB, kTile * RB, 8 * RB, SWZ);
+    umma_ss(tmem + col_dk<DP>(db), ad, bd, id_kv, (st.it > 0 || k > 0) ? 1u : 0u);
+  }
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {  // dV += Pᵀ dO   (K = 128 queries)
-        const uint64_t ad = smem_desc(p_addr + k * 16 * 128, 16384, 1024, kSwizzle128B);
-        const uint64_t bd = smem_desc(do_addr + k * 16 * RB, kTile * RB, 8 * RB, SWZ);
-        umma_ss(tmem + kColDV, ad, bd, id_kv, (it > 0 || k > 0) ? 1u : 0u);
-      }
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {  // dK += dSᵀ Q
-        const uint64_t ad = smem_desc(ds_addr + k * 16 * 128, 16384, 1024, kSwizzle128B);
-        const uint64_t bd = smem_desc(q_addr + k * 16 * RB, kTile * RB, 8 * RB, SWZ);
-        umma_ss(tmem + kColDK, ad, bd, id_kv, (it > 0 || k > 0) ? 1u : 0u);
-      }
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {  // dQ_tile = dS K   (K = 128 keys)
-        const uint64_t ad = smem_desc(ds_addr + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024, kSwizzle128B);
-        const uint64_t bd = smem_desc(k_addr + k * 16 * RB, kTile * RB, 8 * RB, SWZ);
-        umma_ss(tmem + (qb ? kColDQ1 : kColDQ0), ad, bd, id_q, k > 0);
-      }
-      umma_commit(smem_u32(&bars->ds_empty));
-      umma_commit(smem_u32(&bars->q_empty[s]));
-      umma_commit(smem_u32(&bars->dq_full[qb]));
+  for (int k = 0; k < 8; ++k) {  // dQ_tile = dS K   (K = 128 keys)
+    const uint64_t ad = smem_desc(ds_addr + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024, kSwizzle128B);
+    const uint64_t bd = smem_desc(k_addr + k * 16 * RB, kTile * RB, 8 * RB, SWZ);
+    umma_ss(tmem + col_dq<DP>(qb), ad, bd, id_q, k > 0);
+  }
+  umma_commit(smem_u32(&bars->ds_empty));
+  umma_commit(smem_u32(&bars->q_empty[st.qs]));
+  umma_commit(smem_u32(&bars->dq_full[qb]));
+  if (st.it == QT - 1) {
+    umma_commit(smem_u32(&bars->dkdv_full[db]));
+    umma_commit(smem_u32(&bars->kv_empty[kb]));
+  }
+  return true;
+}
+
+template <int DP, bool BF16>
+__device__ __forceinline__ void main_mma(const BwdArgs& a, uint8_t* base, const MainLayout<DP>& lay, MainBars* bars,
+                                         uint32_t tmem, const WaitGuard& g, long long i0, long long i1) {
+  const int QS = a.q_stages, QT = a.QT;
+  const uint32_t total = static_cast<uint32_t>((i1 - i0) * QT);
+  auto step_of = [&](Step& st) {  // advance to the next step
+    ++st.u;
+    if (++st.it == QT) {
+      st.it = 0;
+      ++st.item_ctr;
     }
-    if (!ok) break;
-    umma_commit(smem_u32(&bars->dkdv_full));
-    umma_commit(smem_u32(&bars->kv_empty));
+    if (++st.qs == static_cast<uint32_t>(QS)) {
+      st.qs = 0;
+      st.qph ^= 1;
+    }
+  };
+  bool ok = total > 0;
+  Step cur{0, 0, 0, 0, 0};
+  if (QS >= 2) {
+    // S/dP of step u+1 go ahead of step u's gradient MMAs, so the compute warps
+    // can start on u+1 while the tensor core finishes u.  (Needs a second
+    // Q/dO stage: step u's stage is released by its gradient MMAs.)
+    if (ok) ok = main_issue_sdp<DP, BF16>(cur, base, lay, bars, tmem, g);
+    for (uint32_t u = 0; ok && u < total; ++u) {
+      Step nxt = cur;
+      step_of(nxt);
+      if (u + 1 < total && !main_issue_sdp<DP, BF16>(nxt, base, lay, bars, tmem, g)) { ok = false; break; }
+      if (!main_issue_grads<DP, BF16>(cur, QT, base, lay, bars, tmem, g)) { ok = false; break; }
+      cur = nxt;
+    }
+  } else {
+    for (uint32_t u = 0; ok && u < total; ++u) {
+      if (!main_issue_sdp<DP, BF16>(cur, base, lay, bars, tmem, g)) { ok = false; break; }
+      if (!main_issue_grads<DP, BF16>(cur, QT, base, lay, bars, tmem, g)) { ok = false; break; }
+      step_of(cur);
+    }
   }
   umma_commit(smem_u32(&bars->drain));
   drain_wait(smem_u32(&bars->drain), 0, a.wait_ns, a.status);
 }
 
-// dQ tile (TMEM lanes = queries of tile it) -> fp32 accumulator (scaled by s).
+// dQ tile (TMEM lanes = queries of tile it): this warp's DP/2 columns, × s, into the fp32 accumulator.
 template <int DP>
-__device__ __forceinline__ bool main_consume_dq(const BwdArgs& a, const MainItem& c, int it, uint32_t ctr,
-                                                MainBars* bars, uint32_t trow, int r, int lane, const WaitGuard& g) {
-  const uint32_t qb = ctr & 1;
-  if (!mbar_wait(smem_u32(&bars->dq_full[qb]), (ctr >> 1) & 1, g)) return false;
+__device__ __forceinline__ bool main_consume_dq(const BwdArgs& a, const KvIter& c, int it, uint32_t u,
+                                                MainBars* bars, uint32_t trow, int r, int hc, int lane,
+                                                const WaitGuard& g) {
+  constexpr int HD = DP / 2;
+  const uint32_t qb = u & 1;
+  if (!mbar_wait(smem_u32(&bars->dq_full[qb]), (u >> 1) & 1, g)) return false;
   tc_fence_after();
-  uint32_t v[DP / 16][16];
+  float v[HD];
+  const uint32_t col = trow + col_dq<DP>(qb) + hc * HD;
+  if constexpr (HD == 8) {
+    uint32_t x[8];
+    tmem_ld8(col, x);
+    tmem_wait_ld(x);
 #pragma unroll
-  for (int q = 0; q < DP / 16; ++q) tmem_ld16(trow + (qb ? kColDQ1 : kColDQ0) + q * 16, v[q]);
+    for (int e = 0; e < 8; ++e) v[e] = __uint_as_float(x[e]);
+  } else {
+    uint32_t x[HD / 16][16];
 #pragma unroll
-  for (int q = 0; q < DP / 16; ++q) tmem_wait_ld(v[q]);
+    for (int q = 0; q < HD / 16; ++q) tmem_ld16(col + q * 16, x[q]);
+#pragma unroll
+    for (int q = 0; q < HD / 16; ++q) tmem_wait_ld(x[q]);
+#pragma unroll
+    for (int q = 0; q < HD / 16; ++q)
+#pragma unroll
+      for (int e = 0; e < 16; ++e) v[q * 16 + e] = __uint_as_float(x[q][e]);
+  }
   tc_fence_before();
   __syncwarp();
   if (lane == 0) mbar_arrive(smem_u32(&bars->dq_free[qb]));
   const int i = it * kTile + r;
   if (i < a.L) {
-    float* dst = a.dq_acc + ((static_cast<size_t>(c.b) * a.N + c.n) * a.L + i) * a.H * a.D + static_cast<size_t>(c.h) * a.D;
+    float* dst = a.dq_acc + ((static_cast<size_t>(c.b) * a.N + c.n) * a.L + i) * a.H * a.D +
+                 static_cast<size_t>(c.h) * a.D + hc * HD;
 #pragma unroll
-    for (int q = 0; q < DP / 16; ++q)
-#pragma unroll
-      for (int e = 0; e < 16; e += 4)
-        if (q * 16 + e < a.D)
-          red_add_v4(dst + q * 16 + e, __uint_as_float(v[q][e]) * a.scale, __uint_as_float(v[q][e + 1]) * a.scale,
-                     __uint_as_float(v[q][e + 2]) * a.scale, __uint_as_float(v[q][e + 3]) * a.scale);
+    for (int e = 0; e < HD; e += 4)
+      if (hc * HD + e < a.D)
+        red_add_v4(dst + e, v[e] * a.scale, v[e + 1] * a.scale, v[e + 2] * a.scale, v[e + 3] * a.scale);
   }
   return true;
 }
 
-template <int DP, bool BF16, bool HAS_B2>
-__device__ __forceinline__ void main_compute(const BwdArgs& a, uint8_t* base, const MainLayout<DP>& lay,
-                                             MainBars* bars, uint32_t tmem, const WaitGuard& g, long long items) {
-  constexpr int NS = MainLayout<DP>::kStages;
-  const int r = threadIdx.x;  // query row within the tile == TMEM lane (for S, dP, dQ) and key row (dK, dV)
-  const int warp = r >> 5, lane = r & 31;
-  const uint32_t trow = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-  const float* b1s = reinterpret_cast<const float*>(base + lay.b1);
-  uint32_t it_ctr = 0, item_ctr = 0;
-  bool ok = true;
-  for (long long item = blockIdx.x; ok && item < items; item += gridDim.x, ++item_ctr) {
-    const MainItem c = main_item(item, a);
-    const size_t bnh = (static_cast<size_t>(c.b) * a.N + c.n) * a.H + c.h;
-    if (!mbar_wait(smem_u32(&bars->kv_full), item_ctr & 1, g)) { ok = false; break; }
-    for (int it = 0; it < a.QT; ++it, ++it_ctr) {
-      const uint32_t s = it_ctr % NS, ph = (it_ctr / NS) & 1;
-      const int i = it * kTile + r;
-      float lse2 = INFINITY, dlt = 0.0f;  // rows past L (and empty rows) get P = 0
-      if (i < a.L) {
-        const float lv = a.lse[bnh * a.L + i];
-        lse2 = (lv == -INFINITY) ? INFINITY : lv * kLog2e;
-        dlt = a.delta[bnh * a.L + i];
+// dK, dV of a finished item (TMEM lanes = keys of its key tile): this warp's DP/2 columns.
+template <int DP, bool BF16>
+__device__ __forceinline__ bool main_write_dkdv(const BwdArgs& a, const KvIter& c, uint32_t item_ctr,
+                                                MainBars* bars, uint32_t trow, int r, int hc, int lane,
+                                                const WaitGuard& g) {
+  constexpr int HD = DP / 2;
+  constexpr int NB = kv_acc_buffers<DP>();
+  const uint32_t db = item_ctr % NB;
+  if (!mbar_wait(smem_u32(&bars->dkdv_full[db]), (item_ctr / NB) & 1, g)) return false;
+  tc_fence_after();
+  float kx[HD], vx[HD];
+  const uint32_t ck = trow + col_dk<DP>(db) + hc * HD, cv = trow + col_dv<DP>(db) + hc * HD;
+  if constexpr (HD == 8) {
+    uint32_t x[8], y[8];
+    tmem_ld8(ck, x);
+    tmem_ld8(cv, y);
+    tmem_wait_ld(x);
+    tmem_wait_ld(y);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      kx[e] = __uint_as_float(x[e]);
+      vx[e] = __uint_as_float(y[e]);
+    }
+  } else {
+    uint32_t x[HD / 16][16], y[HD / 16][16];
+#pragma unroll
+    for (int q = 0; q < HD / 16; ++q) {
+      tmem_ld16(ck + q * 16, x[q]);
+      tmem_ld16(cv + q * 16, y[q]);
+    }
+#pragma unroll
+    for (int q = 0; q < HD / 16; ++q) {
+      tmem_wait_ld(x[q]);
+      tmem_wait_ld(y[q]);
+    }
+#pragma unroll
+    for (int q = 0; q < HD / 16; ++q)
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        kx[q * 16 + e] = __uint_as_float(x[q][e]);
+        vx[q * 16 + e] = __uint_as_float(y[q][e]);
       }
-      if (!mbar_wait(smem_u32(&bars->q_full[s]), ph, g)) { ok = false; break; }
-      if (!mbar_wait(smem_u32(&bars->st_full), it_ctr & 1, g)) { ok = false; break; }
-      if (!mbar_wait(smem_u32(&bars->ds_empty), (it_ctr & 1) ^ 1, g)) { ok = false; break; }
-      tc_fence_after();
-      const uint8_t* b2t = base + lay.b2[s];
-#pragma unroll 1
-      for (int cc = 0; cc < 4; ++cc) {
-        uint32_t sv[32], pv[32];
-        tmem_ld32(trow + kColS + cc * 32, sv);
-        tmem_ld32(trow + kColDP + cc * 32, pv);
-        tmem_wait_ld(sv);
-        tmem_wait_ld(pv);
-        float p[32], ds[32];
+  }
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(smem_u32(&bars->dkdv_free[db]));
+  const int j = c.jt * kTile + r;
+  if (j < a.L) {
+    const size_t off = ((static_cast<size_t>(c.b) * a.N + c.n) * a.L + j) * a.H * a.D +
+                       static_cast<size_t>(c.h) * a.D + hc * HD;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int chunk16 = cc * 4 + q;
-          uint4 pb = make_uint4(0u, 0u, 0u, 0u);
-          if (HAS_B2) pb = *reinterpret_cast<const uint4*>(b2t + (chunk16 >> 3) * 16384 + swz_offset(r, chunk16 & 7, 128));
-          const uint32_t pw[4] = {pb.x, pb.y, pb.z, pb.w};
-          const float4 m0 = *reinterpret_cast<const float4*>(b1s + chunk16 * 8);
-          const float4 m1 = *reinterpret_cast<const float4*>(b1s + chunk16 * 8 + 4);
-          const float mk[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int x = q * 8 + e;
-            float y = fmaf(__uint_as_float(sv[x]), a.scale_log2, mk[e]);
-            if (HAS_B2) y = fmaf((e & 1) ? unpack_hi<BF16>(pw[e >> 1]) : unpack_lo<BF16>(pw[e >> 1]), kLog2e, y);
-            const float pr = ex2(y - lse2);
-            p[x] = pr;
-            ds[x] = pr * (__uint_as_float(pv[x]) - dlt);
-          }
-        }
-        store_row_chunk<BF16>(base + lay.p, r, cc, p);
-        store_row_chunk<BF16>(base + lay.ds, r, cc, ds);
+    for (int e = 0; e < HD; e += 8)
+      if (hc * HD + e < a.D) {
+        uint4 pk, pv4;
+        pk.x = pack2<BF16>(kx[e + 0] * a.scale, kx[e + 1] * a.scale);
+        pk.y = pack2<BF16>(kx[e + 2] * a.scale, kx[e + 3] * a.scale);
+        pk.z = pack2<BF16>(kx[e + 4] * a.scale, kx[e + 5] * a.scale);
+        pk.w = pack2<BF16>(kx[e + 6] * a.scale, kx[e + 7] * a.scale);
+        pv4.x = pack2<BF16>(vx[e + 0], vx[e + 1]);
+        pv4.y = pack2<BF16>(vx[e + 2], vx[e + 3]);
+        pv4.z = pack2<BF16>(vx[e + 4], vx[e + 5]);
+        pv4.w = pack2<BF16>(vx[e + 6], vx[e + 7]);
+        *reinterpret_cast<uint4*>(a.dk + off + e) = pk;
+        *reinterpret_cast<uint4*>(a.dv + off + e) = pv4;
       }
-      tc_fence_before();
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(smem_u32(&bars->st_free));
-        mbar_arrive(smem_u32(&bars->q_empty[s]));
-        mbar_arrive(smem_u32(&bars->ds_full));
-      }
-      if (it > 0 && !main_consume_dq<DP>(a, c, it - 1, it_ctr - 1, bars, trow, r, lane, g)) { ok = false; break; }
-    }
-    if (!ok) break;
-    if (!main_consume_dq<DP>(a, c, a.QT - 1, it_ctr - 1, bars, trow, r, lane, g)) { ok = false; break; }
-    // dK, dV (TMEM lanes = keys of this item's key tile)
-    if (!mbar_wait(smem_u32(&bars->dkdv_full), item_ctr & 1, g)) { ok = false; break; }
-    tc_fence_after();
-    uint32_t kv[DP / 16][16], vv[DP / 16][16];
+  }
+  return true;
+}
+
+// P and dS for one 32-key chunk of this warp (S, dP already loaded from TMEM),
+// written to the [query][key] P and dS tiles (K-major, 128B swizzle).
+template <bool BF16, bool HAS_B2>
+__device__ __forceinline__ void main_chunk(const uint32_t (&sv)[32], const uint32_t (&pv)[32], const float* b1c,
+                                           const uint8_t* b2half, uint8_t* pt, uint8_t* dt, int r, int c4,
+                                           float lse2, float dlt, float2 sl2) {
+  const float2 nl2 = make_float2(-lse2, -lse2), l2e2 = make_float2(kLog2e, kLog2e), nd2 = make_float2(-dlt, -dlt);
 #pragma unroll
-    for (int q = 0; q < DP / 16; ++q) {
-      tmem_ld16(trow + kColDK + q * 16, kv[q]);
-      tmem_ld16(trow + kColDV + q * 16, vv[q]);
-    }
+  for (int q = 0; q < 4; ++q) {  // 8 keys (one 16-byte chunk of the tiles) per q
+    const float4 m0 = *reinterpret_cast<const float4*>(b1c + q * 8);
+    const float4 m1 = *reinterpret_cast<const float4*>(b1c + q * 8 + 4);
+    const float2 mk[4] = {make_float2(m0.x, m0.y), make_float2(m0.z, m0.w), make_float2(m1.x, m1.y),
+                          make_float2(m1.z, m1.w)};
+    uint4 pb = make_uint4(0u, 0u, 0u, 0u);
+    if (HAS_B2) pb = *reinterpret_cast<const uint4*>(b2half + swz_offset(r, c4 * 4 + q, 128));
+    const uint32_t pw[4] = {pb.x, pb.y, pb.z, pb.w};
+    uint32_t pp[4], dd[4];
 #pragma unroll
-    for (int q = 0; q < DP / 16; ++q) {
-      tmem_wait_ld(kv[q]);
-      tmem_wait_ld(vv[q]);
+    for (int e2 = 0; e2 < 4; ++e2) {
+      const int x = q * 8 + e2 * 2;
+      float2 t = fma2(make_float2(__uint_as_float(sv[x]), __uint_as_float(sv[x + 1])), sl2, mk[e2]);
+      if (HAS_B2) t = fma2(unpack2<BF16>(pw[e2]), l2e2, t);
+      t = add2(t, nl2);
+      const float p0 = ex2(t.x), p1 = ex2(t.y);
+      const float2 dpd = add2(make_float2(__uint_as_float(pv[x]), __uint_as_float(pv[x + 1])), nd2);
+      const float2 ds = mul2(make_float2(p0, p1), dpd);
+      pp[e2] = pack2<BF16>(p0, p1);
+      dd[e2] = pack2<BF16>(ds.x, ds.y);
     }
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) {
-      mbar_arrive(smem_u32(&bars->dkdv_free));
-      mbar_arrive(smem_u32(&bars->kv_empty));
-    }
-    const int j = c.jt * kTile + r;
-    if (j < a.L) {
-      const size_t off = ((static_cast<size_t>(c.b) * a.N + c.n) * a.L + j) * a.H * a.D + static_cast<size_t>(c.h) * a.D;
-#pragma unroll
-      for (int q = 0; q < DP / 16; ++q)
-#pragma unroll
-        for (int e = 0; e < 16; e += 8)
-          if (q * 16 + e < a.D) {
-            uint4 pk, pv4;
-            pk.x = pack2<BF16>(__uint_as_float(kv[q][e + 0]) * a.scale, __uint_as_float(kv[q][e + 1]) * a.scale);
-            pk.y = pack2<BF16>(__uint_as_float(kv[q][e + 2]) * a.scale, __uint_as_float(kv[q][e + 3]) * a.scale);
-            pk.z = pack2<BF16>(__uint_as_float(kv[q][e + 4]) * a.scale, __uint_as_float(kv[q][e + 5]) * a.scale);
-            pk.w = pack2<BF16>(__uint_as_float(kv[q][e + 6]) * a.scale, __uint_as_float(kv[q][e + 7]) * a.scale);
-            pv4.x = pack2<BF16>(__uint_as_float(vv[q][e + 0]), __uint_as_float(vv[q][e + 1]));
-            pv4.y = pack2<BF16>(__uint_as_float(vv[q][e + 2]), __uint_as_float(vv[q][e + 3]));
-            pv4.z = pack2<BF16>(__uint_as_float(vv[q][e + 4]), __uint_as_float(vv[q][e + 5]));
-            pv4.w = pack2<BF16>(__uint_as_float(vv[q][e + 6]), __uint_as_float(vv[q][e + 7]));
-            *reinterpret_cast<uint4*>(a.dk + off + q * 16 + e) = pk;
-            *reinterpret_cast<uint4*>(a.dv + off + q * 16 + e) = pv4;
-          }
-    }
+    const uint32_t off = swz_offset(r, c4 * 4 + q, 128);
+    *reinterpret_cast<uint4*>(pt + off) = make_uint4(pp[0], pp[1], pp[2], pp[3]);
+    *reinterpret_cast<uint4*>(dt + off) = make_uint4(dd[0], dd[1], dd[2], dd[3]);
   }
 }
 
-template <int DP, bool BF16, bool HAS_B2>
-__global__ void __launch_bounds__(192, 1) evo_bwd_main(const __grid_constant__ BwdArgs a) {
+template <int DP, bool BF16, int B2>
+__device__ __forceinline__ void main_compute(const BwdArgs& a, uint8_t* base, const MainLayout<DP>& lay,
+                                             MainBars* bars, uint32_t tmem, const WaitGuard& g, long long i0,
+                                             long long i1) {
+  constexpr bool kHasB2 = B2 != kB2None;
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int quad = w & 3, hc = w >> 2;
+  const int r = quad * 32 + lane;  // query row (S, dP, dQ) or key row (dK, dV) within the tile == TMEM lane
+  const uint32_t trow = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+  const float2 sl2 = make_float2(a.scale_log2, a.scale_log2);
+  const int QS = a.q_stages, QT = a.QT;
+  uint32_t u = 0, item_ctr = 0, grp_it = 0, s = 0, ph = 0;
+  KvIter cur, prev;
+  cur.init(i0, a);
+  prev = cur;
+  int prev_it = 0;
+  bool ok = true;
+  for (long long item = i0; ok && item < i1; ++item, ++item_ctr) {
+    if (item > i0) {
+      prev = cur;
+      cur.next(a);
+    }
+    const bool grp_last = item + 1 == i1 || cur.n == a.N - 1;
+    if (B2 == kB2Resident && (item == i0 || cur.n == 0)) {
+      if (!mbar_wait(smem_u32(&bars->b2_full), grp_it & 1, g)) { ok = false; break; }
+      ++grp_it;
+    }
+    const uint32_t kb = item_ctr & 1;
+    if (!mbar_wait(smem_u32(&bars->kv_full[kb]), (item_ctr >> 1) & 1, g)) { ok = false; break; }
+    const float* b1 = reinterpret_cast<const float*>(base + lay.b1[kb]) + hc * 64;
+    for (int it = 0; it < QT; ++it, ++u) {
+      if (!mbar_wait(smem_u32(&bars->q_full[s]), ph, g)) { ok = false; break; }
+      const float* ld = reinterpret_cast<const float*>(base + lay.ld[s]);
+      const float lse2 = ld[r], dlt = ld[128 + r];
+      const uint8_t* b2half = base + (B2 == kB2Resident ? lay.b2r + it * 32768u : lay.b2s[s]) + hc * 16384;
+      if (!mbar_wait(smem_u32(&bars->st_full), u & 1, g)) { ok = false; break; }
+      // the P and dS tiles are free once the previous step's gradient MMAs have read them
+      if (!mbar_wait(smem_u32(&bars->ds_empty), (u & 1) ^ 1, g)) { ok = false; break; }
+      tc_fence_after();
+      uint8_t* pt = base + lay.p + hc * 16384;
+      uint8_t* dt = base + lay.ds + hc * 16384;
+      {
+        uint32_t sv[32], pv[32];
+        tmem_ld32(trow + col_s() + hc * 64, sv);
+        tmem_ld32(trow + col_dp() + hc * 64, pv);
+        tmem_wait_ld(sv);
+        tmem_wait_ld(pv);
+        main_chunk<BF16, kHasB2>(sv, pv, b1, b2half, pt, dt, r, 0, lse2, dlt, sl2);
+      }
+      {
+        uint32_t sv[32], pv[32];
+        tmem_ld32(trow + col_s() + hc * 64 + 32, sv);
+        tmem_ld32(trow + col_dp() + hc * 64 + 32, pv);
+        tmem_wait_ld(sv);
+        tmem_wait_ld(pv);
+        // S and dP of this step are in registers: the next step's MMAs may overwrite them
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bars->st_free));
+        main_chunk<BF16, kHasB2>(sv, pv, b1 + 32, b2half, pt, dt, r, 1, lse2, dlt, sl2);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(smem_u32(&bars->ds_full));
+        mbar_arrive(smem_u32(&bars->q_empty[s]));
+        if (it == QT - 1) {
+          mbar_arrive(smem_u32(&bars->kv_empty[kb]));
+          if (B2 == kB2Resident && grp_last) mbar_arrive(smem_u32(&bars->b2_empty));
+        }
+      }
+      if (u > 0) {
+        if (!main_consume_dq<DP>(a, it == 0 ? prev : cur, prev_it, u - 1, bars, trow, r, hc, lane, g)) {
+          ok = false;
+          break;
+        }
+        if (it == 0 && !main_write_dkdv<DP, BF16>(a, prev, item_ctr - 1, bars, trow, r, hc, lane, g)) {
+          ok = false;
+          break;
+        }
+      }
+      prev_it = it;
+      if (++s == static_cast<uint32_t>(QS)) {
+        s = 0;
+        ph ^= 1;
+      }
+    }
+  }
+  if (ok && u > 0) {
+    if (main_consume_dq<DP>(a, cur, prev_it, u - 1, bars, trow, r, hc, lane, g))
+      main_write_dkdv<DP, BF16>(a, cur, item_ctr - 1, bars, trow, r, hc, lane, g);
+  }
+}
+
+template <int DP, bool BF16, int B2>
+__global__ void __launch_bounds__(kThreads, 1) evo_bwd_main(const __grid_constant__ BwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const MainLayout<DP> lay(HAS_B2);
+  const MainLayout<DP> lay(B2, a.q_stages, a.QT);
   MainBars* bars = reinterpret_cast<MainBars*>(base + lay.bars);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long items = static_cast<long long>(a.B) * a.N * a.H * a.QT;
+  const long long i0 = static_cast<long long>(blockIdx.x) * a.chunk;
+  const long long i1 = i0 + a.chunk < a.items ? i0 + a.chunk : a.items;
   if (threadIdx.x == 0) {
     bars->abort = 0;
-    mbar_init(smem_u32(&bars->kv_full), 32);
-    mbar_init(smem_u32(&bars->kv_empty), 1 + 4);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(smem_u32(&bars->q_full[s]), 32);
-      mbar_init(smem_u32(&bars->q_empty[s]), 1 + 4);
+      mbar_init(smem_u32(&bars->kv_full[s]), 32);
+      mbar_init(smem_u32(&bars->kv_empty[s]), 1 + kComputeWarps);
       mbar_init(smem_u32(&bars->dq_full[s]), 1);
-      mbar_init(smem_u32(&bars->dq_free[s]), 4);
+      mbar_init(smem_u32(&bars->dq_free[s]), kComputeWarps);
+      mbar_init(smem_u32(&bars->dkdv_full[s]), 1);
+      mbar_init(smem_u32(&bars->dkdv_free[s]), kComputeWarps);
     }
+    for (int s = 0; s < kMaxQStages; ++s) {
+      mbar_init(smem_u32(&bars->q_full[s]), 32);
+      mbar_init(smem_u32(&bars->q_empty[s]), 1 + kComputeWarps);
+    }
+    mbar_init(smem_u32(&bars->b2_full), 32);
+    mbar_init(smem_u32(&bars->b2_empty), kComputeWarps);
     mbar_init(smem_u32(&bars->st_full), 1);
-    mbar_init(smem_u32(&bars->st_free), 4);
-    mbar_init(smem_u32(&bars->ds_full), 4);
+    mbar_init(smem_u32(&bars->st_free), kComputeWarps);
+    mbar_init(smem_u32(&bars->ds_full), kComputeWarps);
     mbar_init(smem_u32(&bars->ds_empty), 1);
-    mbar_init(smem_u32(&bars->dkdv_full), 1);
-    mbar_init(smem_u32(&bars->dkdv_free), 4);
     mbar_init(smem_u32(&bars->drain), 1);
     fence_barrier_init();
   }
-  if (warp == 4 && lane == 0) {
+  if (warp == kProducerWarp && lane == 0) {
     tma_prefetch_desc(&a.tq);
     tma_prefetch_desc(&a.tk);
     tma_prefetch_desc(&a.tv);
     tma_prefetch_desc(&a.tdo);
-    if (HAS_B2 && a.bias2_mode == kBias2Tma) tma_prefetch_desc(&a.tb2);
+    if (B2 != kB2None && a.bias2_mode == kBias2Tma) tma_prefetch_desc(&a.tb2);
   }
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(&bars->tmem_slot), 512);
     tmem_relinquish();
   }
@@ -516,29 +745,29 @@ __global__ void __launch_bounds__(192, 1) evo_bwd_main(const __grid_constant__ B
   tc_fence_after();
   const uint32_t tmem = bars->tmem_slot;
   const WaitGuard g{a.wait_ns, a.status, &bars->abort};
-  if (warp == 4) {
-    main_producer<DP, BF16, HAS_B2>(a, base, lay, bars, g, lane, items);
-  } else if (warp == 5) {
-    if (lane == 0) main_mma<DP, BF16>(a, base, lay, bars, tmem, g, items);
+  if (warp == kProducerWarp) {
+    main_producer<DP, BF16, B2>(a, base, lay, bars, g, lane, i0, i1);
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) main_mma<DP, BF16>(a, base, lay, bars, tmem, g, i0, i1);
     __syncwarp();
   } else {
-    main_compute<DP, BF16, HAS_B2>(a, base, lay, bars, tmem, g, items);
+    main_compute<DP, BF16, B2>(a, base, lay, bars, tmem, g, i0, i1);
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
 }
 
 // ============================================================ evo_bwd_db2_part
-constexpr uint32_t kColS_0 = 0, kColDP_0 = 128, kColS_1 = 256, kColDP_1 = 384;
+constexpr int kMaxPartStages = 3;
 
 struct PartBars {
   uint64_t b2_full;
-  uint64_t st_full[2], st_free[2];      // stage ring (Q, dO, K, V, key mask)
-  uint64_t mm_full[2], mm_free[2];      // TMEM S/dP double buffer
+  uint64_t st_full[kMaxPartStages], st_free[kMaxPartStages];  // stage ring (Q, dO, K, V, key mask, lse, delta)
+  uint64_t mm_full[2], mm_free[2];                            // TMEM S/dP double buffer
   uint64_t drain;
   uint32_t tmem_slot;
   int abort;
@@ -547,25 +776,33 @@ struct PartBars {
 template <int DP>
 struct PartLayout {
   static constexpr uint32_t kTB = kTile * DP * 2;
-  uint32_t q[2], d_o[2], k[2], v[2], b1[2], b2, bars, total;
-  __host__ __device__ PartLayout() {
+  uint32_t q[kMaxPartStages], d_o[kMaxPartStages], k[kMaxPartStages], v[kMaxPartStages], b1[kMaxPartStages],
+      ld[kMaxPartStages], b2, bars, total;
+  __host__ __device__ explicit PartLayout(int ns) {
     uint32_t off = 0;
-    for (int s = 0; s < 2; ++s) {
-      q[s] = off;
-      d_o[s] = off + kTB;
-      k[s] = off + 2 * kTB;
-      v[s] = off + 3 * kTB;
-      off += 4 * kTB;
+    for (int s = 0; s < kMaxPartStages; ++s) {
+      const uint32_t o = off + (s < ns ? s : 0) * 4 * kTB;
+      q[s] = o;
+      d_o[s] = o + kTB;
+      k[s] = o + 2 * kTB;
+      v[s] = o + 3 * kTB;
     }
+    off += ns * 4 * kTB;
     b2 = off;
     off += 32768u;
-    for (int s = 0; s < 2; ++s) b1[s] = off + s * 512u;
-    off += 1024u;
+    for (int s = 0; s < kMaxPartStages; ++s) {
+      b1[s] = off + (s < ns ? s : 0) * 1536u;
+      ld[s] = b1[s] + 512u;
+    }
+    off += ns * 1536u;
     bars = off;
     off += (sizeof(PartBars) + 127) & ~127u;
     total = off;
   }
 };
+
+__device__ __forceinline__ uint32_t col_ps(uint32_t b) { return b ? 256u : 0u; }
+__device__ __forceinline__ uint32_t col_pdp(uint32_t b) { return b ? 384u : 128u; }
 
 struct PartItem {
   int b, h, it, jt, grp, n0, n1;
@@ -587,10 +824,11 @@ __device__ __forceinline__ PartItem part_item(const BwdArgs& a) {
 }
 
 template <int DP, bool BF16>
-__global__ void __launch_bounds__(192, 1) evo_bwd_db2_part(const __grid_constant__ BwdArgs a) {
+__global__ void __launch_bounds__(kThreads, 1) evo_bwd_db2_part(const __grid_constant__ BwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const PartLayout<DP> lay;
+  const int NS = a.part_stages;
+  const PartLayout<DP> lay(NS);
   PartBars* bars = reinterpret_cast<PartBars*>(base + lay.bars);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const PartItem c = part_item(a);
@@ -598,16 +836,18 @@ __global__ void __launch_bounds__(192, 1) evo_bwd_db2_part(const __grid_constant
   if (threadIdx.x == 0) {
     bars->abort = 0;
     mbar_init(smem_u32(&bars->b2_full), 32);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kMaxPartStages; ++s) {
       mbar_init(smem_u32(&bars->st_full[s]), 32);
-      mbar_init(smem_u32(&bars->st_free[s]), 1 + 4);
+      mbar_init(smem_u32(&bars->st_free[s]), 1 + kComputeWarps);
+    }
+    for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(&bars->mm_full[s]), 1);
-      mbar_init(smem_u32(&bars->mm_free[s]), 4);
+      mbar_init(smem_u32(&bars->mm_free[s]), kComputeWarps);
     }
     mbar_init(smem_u32(&bars->drain), 1);
     fence_barrier_init();
   }
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(&bars->tmem_slot), 512);
     tmem_relinquish();
   }
@@ -618,138 +858,152 @@ __global__ void __launch_bounds__(192, 1) evo_bwd_db2_part(const __grid_constant
   constexpr uint32_t kTB = PartLayout<DP>::kTB;
   const int bh = c.b * a.H + c.h;
 
-  if (warp == 4) {  // ---------------- producer
-    if (a.bias2_mode == kBias2Loads)
-      fill_b2_tile_loads(base + lay.b2, a.bias2 + static_cast<size_t>(bh) * a.L * a.L, a.L, c.it * kTile,
-                         c.jt * kTile, lane);
-    if (lane == 0) {
-      const uint32_t full = smem_u32(&bars->b2_full);
-      if (a.bias2_mode == kBias2Tma) {
-        mbar_arrive_expect_tx(full, 32768u);
-        tma_load_3d(smem_u32(base + lay.b2), &a.tb2, full, c.jt * kTile, c.it * kTile, bh);
-        tma_load_3d(smem_u32(base + lay.b2 + 16384), &a.tb2, full, c.jt * kTile + 64, c.it * kTile, bh);
-      } else {
-        mbar_arrive(full);
+  if (warp == kProducerWarp) {  // ---------------- producer
+    const uint32_t full_b2 = smem_u32(&bars->b2_full);
+    if (a.bias2_mode == kBias2Tma) {
+      if (lane == 0) {
+        mbar_expect_tx(full_b2, 32768u);
+        tma_load_3d(smem_u32(base + lay.b2), &a.tb2, full_b2, c.jt * kTile, c.it * kTile, bh);
+        tma_load_3d(smem_u32(base + lay.b2 + 16384), &a.tb2, full_b2, c.jt * kTile + 64, c.it * kTile, bh);
       }
     } else {
-      mbar_arrive(smem_u32(&bars->b2_full));
+      fill_b2_tile_loads(base + lay.b2, a.bias2 + static_cast<size_t>(bh) * a.L * a.L, a.L, c.it * kTile,
+                         c.jt * kTile, lane);
     }
-    int k = 0;
+    mbar_arrive(full_b2);
+    int k = 0, s = 0, ph = 0;
     for (; k < nn; ++k) {
-      const int s = k & 1, ph = (k >> 1) & 1;
       if (!mbar_wait(smem_u32(&bars->st_free[s]), ph ^ 1, g)) break;
       const int bn = c.b * a.N + c.n0 + k;
-      fill_b1_chunk<BF16>(reinterpret_cast<float*>(base + lay.b1[s]),
-                          a.bias1 ? a.bias1 + static_cast<size_t>(bn) * a.L : nullptr, a.L, c.jt * kTile, lane);
       const uint32_t full = smem_u32(&bars->st_full[s]);
       if (lane == 0) {
-        mbar_arrive_expect_tx(full, 4 * kTB);
+        mbar_expect_tx(full, 4 * kTB);
         tma_load_4d(smem_u32(base + lay.q[s]), &a.tq, full, 0, c.h, c.it * kTile, bn);
         tma_load_4d(smem_u32(base + lay.d_o[s]), &a.tdo, full, 0, c.h, c.it * kTile, bn);
         tma_load_4d(smem_u32(base + lay.k[s]), &a.tk, full, 0, c.h, c.jt * kTile, bn);
         tma_load_4d(smem_u32(base + lay.v[s]), &a.tv, full, 0, c.h, c.jt * kTile, bn);
-      } else {
-        mbar_arrive(full);
+      }
+      fill_b1_chunk<BF16>(reinterpret_cast<float*>(base + lay.b1[s]),
+                          a.bias1 ? a.bias1 + static_cast<size_t>(bn) * a.L : nullptr, a.L, c.jt * kTile, lane);
+      fill_lse_delta(reinterpret_cast<float*>(base + lay.ld[s]), a.lse, a.delta,
+                     static_cast<size_t>(bn) * a.H + c.h, a.L, c.it * kTile, lane);
+      mbar_arrive(full);
+      if (++s == NS) {
+        s = 0;
+        ph ^= 1;
       }
     }
-    drain_wait(smem_u32(&bars->b2_full), 0, a.wait_ns, a.status);
-    for (int s = 0; s < 2; ++s) {
-      const int issued = (k + 1 - s) / 2;
-      if (issued > 0) drain_wait(smem_u32(&bars->st_full[s]), (issued - 1) & 1, a.wait_ns, a.status);
+    drain_wait(full_b2, 0, a.wait_ns, a.status);
+    for (int st = 0; st < NS; ++st) {
+      const int issued = (k + NS - 1 - st) / NS;
+      if (issued > 0) drain_wait(smem_u32(&bars->st_full[st]), (issued - 1) & 1, a.wait_ns, a.status);
     }
-  } else if (warp == 5) {  // ---------------- MMA
+  } else if (warp == kMmaWarp) {  // ---------------- MMA
     if (lane == 0) {
       constexpr uint32_t RB = DP * 2;
       constexpr uint32_t SWZ = swizzle_for_row(RB);
       constexpr uint32_t id_s = idesc_f16(128, 128, BF16, false, false);
+      int s = 0, ph = 0;
       for (int k = 0; k < nn; ++k) {
-        const int s = k & 1, ph = (k >> 1) & 1;
+        const uint32_t mb = k & 1;
         if (!mbar_wait(smem_u32(&bars->st_full[s]), ph, g)) break;
-        if (!mbar_wait(smem_u32(&bars->mm_free[s]), ph ^ 1, g)) break;
+        if (!mbar_wait(smem_u32(&bars->mm_free[mb]), ((k >> 1) & 1) ^ 1, g)) break;
         tc_fence_after();
         const uint32_t q_addr = smem_u32(base + lay.q[s]), do_addr = smem_u32(base + lay.d_o[s]);
         const uint32_t k_addr = smem_u32(base + lay.k[s]), v_addr = smem_u32(base + lay.v[s]);
 #pragma unroll
         for (int kk = 0; kk < DP / 16; ++kk)
-          umma_ss(tmem + (s ? kColS_1 : kColS_0), smem_desc(q_addr + kk * 32, 16, 8 * RB, SWZ),
+          umma_ss(tmem + col_ps(mb), smem_desc(q_addr + kk * 32, 16, 8 * RB, SWZ),
                   smem_desc(k_addr + kk * 32, 16, 8 * RB, SWZ), id_s, kk > 0);
 #pragma unroll
         for (int kk = 0; kk < DP / 16; ++kk)
-          umma_ss(tmem + (s ? kColDP_1 : kColDP_0), smem_desc(do_addr + kk * 32, 16, 8 * RB, SWZ),
+          umma_ss(tmem + col_pdp(mb), smem_desc(do_addr + kk * 32, 16, 8 * RB, SWZ),
                   smem_desc(v_addr + kk * 32, 16, 8 * RB, SWZ), id_s, kk > 0);
-        umma_commit(smem_u32(&bars->mm_full[s]));
+        umma_commit(smem_u32(&bars->mm_full[mb]));
         umma_commit(smem_u32(&bars->st_free[s]));
+        if (++s == NS) {
+          s = 0;
+          ph ^= 1;
+        }
       }
       umma_commit(smem_u32(&bars->drain));
       drain_wait(smem_u32(&bars->drain), 0, a.wait_ns, a.status);
     }
     __syncwarp();
-  } else {  // ---------------- compute: thread r = query row of the tile
-    const int r = threadIdx.x;
-    const uint32_t trow = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    const int i = c.it * kTile + r;
-    float acc[kTile];
+  } else {  // ---------------- compute: warp (quad, half) = 32 query rows × 64 keys
+    const int quad = warp & 3, hc = warp >> 2;
+    const int r = quad * 32 + lane;
+    const uint32_t trow = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    const float2 sl2 = make_float2(a.scale_log2, a.scale_log2);
+    const uint8_t* b2half = base + lay.b2 + hc * 16384;
+    float acc[64];
 #pragma unroll
-    for (int e = 0; e < kTile; ++e) acc[e] = 0.0f;
+    for (int e = 0; e < 64; ++e) acc[e] = 0.0f;
     bool ok = mbar_wait(smem_u32(&bars->b2_full), 0, g);
+    int s = 0, ph = 0;
     for (int k = 0; ok && k < nn; ++k) {
-      const int s = k & 1, ph = (k >> 1) & 1;
-      const size_t bnh = (static_cast<size_t>(c.b) * a.N + c.n0 + k) * a.H + c.h;
-      float lse2 = INFINITY, dlt = 0.0f;
-      if (i < a.L) {
-        const float lv = a.lse[bnh * a.L + i];
-        lse2 = (lv == -INFINITY) ? INFINITY : lv * kLog2e;
-        dlt = a.delta[bnh * a.L + i];
-      }
+      const uint32_t mb = k & 1;
       if (!mbar_wait(smem_u32(&bars->st_full[s]), ph, g)) { ok = false; break; }
-      if (!mbar_wait(smem_u32(&bars->mm_full[s]), ph, g)) { ok = false; break; }
+      const float* ld = reinterpret_cast<const float*>(base + lay.ld[s]);
+      const float lse2 = ld[r], dlt = ld[128 + r];
+      const float* b1 = reinterpret_cast<const float*>(base + lay.b1[s]) + hc * 64;
+      if (!mbar_wait(smem_u32(&bars->mm_full[mb]), (k >> 1) & 1, g)) { ok = false; break; }
       tc_fence_after();
-      const float* b1s = reinterpret_cast<const float*>(base + lay.b1[s]);
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
+      for (int c4 = 0; c4 < 2; ++c4) {
         uint32_t sv[32], pv[32];
-        tmem_ld32(trow + (s ? kColS_1 : kColS_0) + cc * 32, sv);
-        tmem_ld32(trow + (s ? kColDP_1 : kColDP_0) + cc * 32, pv);
+        tmem_ld32(trow + col_ps(mb) + hc * 64 + c4 * 32, sv);
+        tmem_ld32(trow + col_pdp(mb) + hc * 64 + c4 * 32, pv);
         tmem_wait_ld(sv);
         tmem_wait_ld(pv);
+        const float2 nl2 = make_float2(-lse2, -lse2), l2e2 = make_float2(kLog2e, kLog2e),
+                     nd2 = make_float2(-dlt, -dlt);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const int chunk16 = cc * 4 + q;
-          const uint4 pb = *reinterpret_cast<const uint4*>(base + lay.b2 + (chunk16 >> 3) * 16384 +
-                                                           swz_offset(r, chunk16 & 7, 128));
+          const float4 m0 = *reinterpret_cast<const float4*>(b1 + c4 * 32 + q * 8);
+          const float4 m1 = *reinterpret_cast<const float4*>(b1 + c4 * 32 + q * 8 + 4);
+          const float2 mk[4] = {make_float2(m0.x, m0.y), make_float2(m0.z, m0.w), make_float2(m1.x, m1.y),
+                                make_float2(m1.z, m1.w)};
+          const uint4 pb = *reinterpret_cast<const uint4*>(b2half + swz_offset(r, c4 * 4 + q, 128));
           const uint32_t pw[4] = {pb.x, pb.y, pb.z, pb.w};
-          const float4 m0 = *reinterpret_cast<const float4*>(b1s + chunk16 * 8);
-          const float4 m1 = *reinterpret_cast<const float4*>(b1s + chunk16 * 8 + 4);
-          const float mk[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int x = q * 8 + e;
-            float y = fmaf(__uint_as_float(sv[x]), a.scale_log2, mk[e]);
-            y = fmaf((e & 1) ? unpack_hi<BF16>(pw[e >> 1]) : unpack_lo<BF16>(pw[e >> 1]), kLog2e, y);
-            const float pr = ex2(y - lse2);
-            acc[cc * 32 + x] += pr * (__uint_as_float(pv[x]) - dlt);
+          for (int e2 = 0; e2 < 4; ++e2) {
+            const int x = q * 8 + e2 * 2;
+            float2 t = fma2(make_float2(__uint_as_float(sv[x]), __uint_as_float(sv[x + 1])), sl2, mk[e2]);
+            t = fma2(unpack2<BF16>(pw[e2]), l2e2, t);
+            t = add2(t, nl2);
+            const float2 pr = make_float2(ex2(t.x), ex2(t.y));
+            const float2 dpd = add2(make_float2(__uint_as_float(pv[x]), __uint_as_float(pv[x + 1])), nd2);
+            const float2 a2 = fma2(pr, dpd, make_float2(acc[c4 * 32 + x], acc[c4 * 32 + x + 1]));
+            acc[c4 * 32 + x] = a2.x;
+            acc[c4 * 32 + x + 1] = a2.y;
           }
         }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(smem_u32(&bars->mm_free[s]));
+        mbar_arrive(smem_u32(&bars->mm_free[mb]));
         mbar_arrive(smem_u32(&bars->st_free[s]));
       }
+      if (++s == NS) {
+        s = 0;
+        ph ^= 1;
+      }
     }
+    const int i = c.it * kTile + r;
     if (ok && i < a.L) {
       const long long plane = static_cast<long long>(a.B) * a.H * a.L * a.L;
       float* dst = a.db2_part + c.grp * plane + (static_cast<long long>(bh) * a.L + i) * a.L;
-      const int j0 = c.jt * kTile;
+      const int j0 = c.jt * kTile + hc * 64;
 #pragma unroll
-      for (int e = 0; e < kTile; ++e)
+      for (int e = 0; e < 64; ++e)
         if (j0 + e < a.L) dst[j0 + e] = acc[e];
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -765,39 +1019,65 @@ unsigned grid_for(long long work, long long per_block) {
   return static_cast<unsigned>(g < 1 ? 1 : g);
 }
 
-template <int DP, bool BF16, bool HAS_B2>
-cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t st, const ProfileEvents* prof) {
+template <int DP, bool BF16, int B2>
+cudaError_t launch_main(BwdArgs a, cudaStream_t st) {
+  const MainLayout<DP> lay(B2, a.q_stages, a.QT);
+  const size_t smem = one_cta_per_sm(lay.total + 1024);
+  auto kern = evo_bwd_main<DP, BF16, B2>;
+  static bool limit_set[64] = {};
+  cudaError_t e = ensure_smem_limit(kern, kMaxSmem, limit_set);
+  if (e != cudaSuccess) return e;
+  const long long sms = num_sms();
+  a.chunk = (a.items + sms - 1) / sms;
+  const long long grid = (a.items + a.chunk - 1) / a.chunk;
+  kern<<<static_cast<unsigned>(grid), kThreads, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+template <int DP, bool BF16>
+cudaError_t launch_bwd_d(BwdArgs a, cudaStream_t st, const ProfileEvents* prof) {
+  const bool has_b2 = a.bias2_mode != kBias2None;
   const long long rows = static_cast<long long>(a.B) * a.N * a.L * a.H;
+  a.items = static_cast<long long>(a.B) * a.H * a.QT * a.N;
   prof_record(prof, 2, st);
   evo_bwd_pre<DP, BF16><<<grid_for(rows, 256), 256, 0, st>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   prof_record(prof, 3, st);
 
-  {
-    const MainLayout<DP> lay(HAS_B2);
-    const size_t smem = one_cta_per_sm(lay.total + 1024);
-    auto kern = evo_bwd_main<DP, BF16, HAS_B2>;
-    static bool limit_set[64] = {};
-    if ((e = ensure_smem_limit(kern, smem, limit_set)) != cudaSuccess) return e;
-    const long long items = static_cast<long long>(a.B) * a.N * a.H * a.QT;
-    const long long grid = items < num_sms() ? items : num_sms();
-    kern<<<static_cast<unsigned>(grid), 192, smem, st>>>(a);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  // main kernel: deepest Q/dO ring that fits, resident pair-bias tiles when possible
+  auto fits = [&](int kind, int qs) { return MainLayout<DP>(kind, qs, a.QT).total + 1024 <= kMaxSmem; };
+  if (!has_b2) {
+    a.q_stages = fits(kB2None, 4) ? 4 : (fits(kB2None, 3) ? 3 : (fits(kB2None, 2) ? 2 : 1));
+    e = launch_main<DP, BF16, kB2None>(a, st);
+  } else {
+    int kind = kB2Stream, qs = 1;
+    for (int q = 4; q >= 2; --q)
+      if (fits(kB2Resident, q)) {
+        kind = kB2Resident;
+        qs = q;
+        break;
+      }
+    if (kind == kB2Stream) qs = fits(kB2Stream, 3) ? 3 : (fits(kB2Stream, 2) ? 2 : 1);
+    a.q_stages = qs;
+    a.b2_resident = kind == kB2Resident;
+    e = kind == kB2Resident ? launch_main<DP, BF16, kB2Resident>(a, st) : launch_main<DP, BF16, kB2Stream>(a, st);
   }
+  if (e != cudaSuccess) return e;
   prof_record(prof, 4, st);
   evo_bwd_dq_cast<BF16><<<grid_for(rows * a.D / 8, 256), 256, 0, st>>>(a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   prof_record(prof, 5, st);
 
-  if (HAS_B2) {
-    const PartLayout<DP> lay;
+  if (has_b2) {
+    a.part_stages = PartLayout<DP>(3).total + 1024 <= kMaxSmem ? 3 : 2;
+    const PartLayout<DP> lay(a.part_stages);
     const size_t smem = one_cta_per_sm(lay.total + 1024);
     auto kern = evo_bwd_db2_part<DP, BF16>;
     static bool limit_set[64] = {};
-    if ((e = ensure_smem_limit(kern, smem, limit_set)) != cudaSuccess) return e;
+    if ((e = ensure_smem_limit(kern, kMaxSmem, limit_set)) != cudaSuccess) return e;
     const long long blocks = static_cast<long long>(a.B) * a.H * a.groups * a.QT * a.QT;
-    kern<<<static_cast<unsigned>(blocks), 192, smem, st>>>(a);
+    kern<<<static_cast<unsigned>(blocks), kThreads, smem, st>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     prof_record(prof, 6, st);
     const long long plane = static_cast<long long>(a.B) * a.H * a.L * a.L;
@@ -806,11 +1086,6 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t st, const ProfileEvents*
     prof_record(prof, 7, st);
   }
   return cudaSuccess;
-}
-
-template <int DP, bool BF16>
-cudaError_t launch_bwd_d(const BwdArgs& a, cudaStream_t st, const ProfileEvents* p) {
-  return a.bias2_mode == kBias2None ? launch_bwd_t<DP, BF16, false>(a, st, p) : launch_bwd_t<DP, BF16, true>(a, st, p);
 }
 
 }  // namespace

@@ -52,6 +52,11 @@ struct BwdArgs {
   int QT;
   int groups;               // G: n-groups of the pair-bias gradient
   int group_size;           // ceil(N / G)
+  long long items;          // main kernel: B*H*QT*N items (b, h, key tile, n), n fastest
+  long long chunk;          // main kernel: consecutive items per CTA
+  int q_stages;             // main kernel: depth of the Q/dO ring
+  int b2_resident;          // main kernel: pair-bias tiles of the (b, h, key tile) group stay in smem
+  int part_stages;          // pair-bias partial kernel: depth of its ring
   float scale;              // D^-1/2
   float scale_log2;         // D^-1/2 * log2(e)
   int bias2_mode;
