@@ -70,8 +70,10 @@ __global__ void __launch_bounds__(256) evo_bwd_pre(const BwdArgs a) {
           sum = fmaf(unpack_lo<BF16>(ow[e]), unpack_lo<BF16>(gw[e]), sum);
           sum = fmaf(unpack_hi<BF16>(ow[e]), unpack_hi<BF16>(gw[e]), sum);
         }
-        acc[2 * c] = make_float4(0.f, 0.f, 0.f, 0.f);
-        acc[2 * c + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (a.zero_dq) {
+          acc[2 * c] = make_float4(0.f, 0.f, 0.f, 0.f);
+          acc[2 * c + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
       }
     }
     a.delta[(bn * a.H + h) * a.L + i] = sum;
@@ -147,22 +149,58 @@ __device__ __forceinline__ void fill_b1_chunk(float* dst, const uint16_t* b1row,
   reinterpret_cast<float4*>(dst)[lane] = m4;
 }
 
+// The same chunk in two halves: loads issued one stage ahead (raw values held
+// in registers, so their latency overlaps the wait for a free stage), then
+// converted and written when the stage is filled.
+struct B1Raw {
+  uint16_t v[4];
+};
+__device__ __forceinline__ void b1_prefetch(B1Raw& raw, const uint16_t* b1row, int L, int j0, int lane) {
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const int j = j0 + lane * 4 + e;
+    raw.v[e] = (b1row && j < L) ? b1row[j] : static_cast<uint16_t>(0);
+  }
+}
+template <bool BF16>
+__device__ __forceinline__ void b1_store(float* dst, const B1Raw& raw, bool has_b1, int L, int j0, int lane) {
+  float4 m4;
+  float* mv = reinterpret_cast<float*>(&m4);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const int j = j0 + lane * 4 + e;
+    mv[e] = j < L ? (has_b1 ? to_f32<BF16>(raw.v[e]) * kLog2e : 0.0f) : -INFINITY;
+  }
+  reinterpret_cast<float4*>(dst)[lane] = m4;
+}
+
 // lse (× log2 e; +inf for rows past L or with an empty softmax, so P = 0) and
-// delta for queries i0..i0+127 of slice bnh.
-__device__ __forceinline__ void fill_lse_delta(float* dst, const float* lse, const float* delta, size_t bnh, int L,
-                                               int i0, int lane) {
+// delta for queries i0..i0+127 of slice bnh, prefetched like the key mask.
+struct LdRaw {
+  float l[4], d[4];
+};
+__device__ __forceinline__ void ld_prefetch(LdRaw& raw, const float* lse, const float* delta, size_t bnh, int L,
+                                            int i0, int lane) {
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
     const int i = i0 + lane * 4 + e;
-    float lv = INFINITY, dv = 0.0f;
-    if (i < L) {
-      const float x = lse[bnh * L + i];
-      lv = (x == -INFINITY) ? INFINITY : x * kLog2e;
-      dv = delta[bnh * L + i];
-    }
-    dst[lane * 4 + e] = lv;
-    dst[128 + lane * 4 + e] = dv;
+    raw.l[e] = i < L ? lse[bnh * L + i] : -INFINITY;
+    raw.d[e] = i < L ? delta[bnh * L + i] : 0.0f;
   }
+}
+__device__ __forceinline__ void ld_store(float* dst, const LdRaw& raw, int lane) {
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float x = raw.l[e];
+    dst[lane * 4 + e] = (x == -INFINITY) ? INFINITY : x * kLog2e;
+    dst[128 + lane * 4 + e] = raw.d[e];
+  }
+}
+__device__ __forceinline__ void fill_lse_delta(float* dst, const float* lse, const float* delta, size_t bnh, int L,
+                                               int i0, int lane) {
+  LdRaw raw;
+  ld_prefetch(raw, lse, delta, bnh, L, i0, lane);
+  ld_store(dst, raw, lane);
 }
 
 // Incremental (b, h, key tile, n) iterator, n fastest.
@@ -761,6 +799,607 @@ __global__ void __launch_bounds__(kThreads, 1) evo_bwd_main(const __grid_constan
   }
 }
 
+// ============================================================ evo_bwd_slice
+// One CTA owns whole (b, n, h) slices (when TMEM has room for every dQ tile of
+// a slice): for each key tile jt, for each query tile it, S and dP into TMEM;
+// P and dS into the swizzled smem tiles (A operands of dV += Pᵀ dO and
+// dK += dSᵀ Q) and dS also into TMEM, where it is the A operand of
+// dQ_it += dS·K_jt (TS form; dQ stays in TMEM across key tiles).  dK and dV
+// are written per key tile, dQ once per slice: no atomics, no fp32 dQ
+// accumulator in device memory.
+//
+// TMEM columns: S 0..127, dP 128..255, dS (packed pairs) 256..319, dK, dV,
+// then the QT dQ tiles.
+constexpr uint32_t kSlColS = 0u, kSlColDP = 128u, kSlColDsT = 256u;
+// dK/dV accumulators are double-buffered across key tiles when TMEM has room.
+__host__ __device__ constexpr int slice_kv_bufs(int DP, int QT) { return 320 + 4 * DP + QT * DP <= 512 ? 2 : 1; }
+template <int DP>
+__device__ __forceinline__ uint32_t sl_col_dk(uint32_t b) { return 320u + b * 2 * DP; }
+template <int DP>
+__device__ __forceinline__ uint32_t sl_col_dv(uint32_t b) { return 320u + b * 2 * DP + DP; }
+template <int DP>
+__device__ __forceinline__ uint32_t sl_col_dq(int it, int nb) { return 320u + nb * 2 * DP + it * DP; }
+template <int DP>
+__host__ __device__ constexpr bool slice_tmem_fits(int QT) { return 320 + 2 * DP + QT * DP <= 512; }
+
+struct SliceBars {
+  uint64_t kv_full[2], kv_empty[2];
+  uint64_t q_full[kMaxQStages], q_empty[kMaxQStages];
+  uint64_t st_full, st_free, ds_full, ds_empty;
+  uint64_t dkdv_full[2], dkdv_free[2], dq_full, dq_free;
+  uint64_t drain;
+  uint32_t tmem_slot;
+  int abort;
+};
+
+template <int DP>
+struct SliceLayout {
+  static constexpr uint32_t kTB = kTile * DP * 2;
+  uint32_t k[2], v[2], b1[2], q[kMaxQStages], d_o[kMaxQStages], b2s[kMaxQStages], ld[kMaxQStages], p, ds, bars,
+      total;
+  __host__ __device__ SliceLayout(bool has_b2, int qs) {
+    uint32_t off = 0;
+    for (int s = 0; s < 2; ++s) {
+      k[s] = off;
+      v[s] = off + kTB;
+      off += 2 * kTB;
+    }
+    for (int s = 0; s < kMaxQStages; ++s) {
+      q[s] = off + (s < qs ? s : 0) * 2 * kTB;
+      d_o[s] = q[s] + kTB;
+    }
+    off += qs * 2 * kTB;
+    for (int s = 0; s < kMaxQStages; ++s) b2s[s] = off + (s < qs ? s : 0) * 32768u;
+    if (has_b2) off += qs * 32768u;
+    p = off;
+    off += 32768u;
+    ds = off;
+    off += 32768u;
+    for (int s = 0; s < 2; ++s) b1[s] = off + s * 512u;
+    off += 1024u;
+    for (int s = 0; s < kMaxQStages; ++s) ld[s] = off + (s < qs ? s : 0) * 1024u;
+    off += qs * 1024u;
+    bars = off;
+    off += (sizeof(SliceBars) + 127) & ~127u;
+    total = off;
+  }
+};
+
+// (b, h, n) slice iterator, n fastest.
+struct SlIter {
+  int b, h, n;
+  __device__ __forceinline__ void init(long long item, const BwdArgs& a) {
+    n = static_cast<int>(item % a.N);
+    const long long t = item / a.N;
+    h = static_cast<int>(t % a.H);
+    b = static_cast<int>(t / a.H);
+  }
+  __device__ __forceinline__ void next(const BwdArgs& a) {
+    if (++n == a.N) {
+      n = 0;
+      if (++h == a.H) {
+        h = 0;
+        ++b;
+      }
+    }
+  }
+};
+
+template <int DP, bool BF16, bool HAS_B2>
+__device__ __forceinline__ void slice_producer(const BwdArgs& a, uint8_t* base, const SliceLayout<DP>& lay,
+                                               SliceBars* bars, const WaitGuard& g, int lane, long long i0,
+                                               long long i1) {
+  constexpr uint32_t kTB = SliceLayout<DP>::kTB;
+  const int QS = a.q_stages, QT = a.QT;
+  const bool tma_b2 = a.bias2_mode == kBias2Tma;
+  const uint32_t q_bytes = 2 * kTB + ((HAS_B2 && tma_b2) ? 32768u : 0u);
+  uint32_t grp = 0, steps = 0, s = 0, ph = 0;
+  SlIter c;
+  c.init(i0, a);
+  // next step's lse/delta and next key tile's mask, loaded one step ahead
+  SlIter pc = c;
+  int pjt = 0, pit = 0;
+  LdRaw ldr;
+  B1Raw b1r;
+  auto prefetch_ld = [&]() {
+    if (pc.b < a.B)
+      ld_prefetch(ldr, a.lse, a.delta, (static_cast<size_t>(pc.b) * a.N + pc.n) * a.H + pc.h, a.L, pit * kTile,
+                  lane);
+  };
+  auto advance_pf = [&]() {
+    if (++pit == QT) {
+      pit = 0;
+      if (++pjt == QT) {
+        pjt = 0;
+        pc.next(a);
+      }
+    }
+  };
+  b1_prefetch(b1r, a.bias1 ? a.bias1 + (static_cast<size_t>(c.b) * a.N + c.n) * a.L : nullptr, a.L, 0, lane);
+  prefetch_ld();
+  bool ok = true;
+  for (long long item = i0; ok && item < i1; ++item, c.next(a)) {
+    const int bn = c.b * a.N + c.n, bh = c.b * a.H + c.h;
+    for (int jt = 0; ok && jt < QT; ++jt, ++grp) {
+      const uint32_t kb = grp & 1;
+      if (!mbar_wait(smem_u32(&bars->kv_empty[kb]), ((grp >> 1) & 1) ^ 1, g)) { ok = false; break; }
+      {
+        const uint32_t full = smem_u32(&bars->kv_full[kb]);
+        if (lane == 0) {
+          mbar_expect_tx(full, 2 * kTB);
+          tma_load_4d(smem_u32(base + lay.k[kb]), &a.tk, full, 0, c.h, jt * kTile, bn);
+          tma_load_4d(smem_u32(base + lay.v[kb]), &a.tv, full, 0, c.h, jt * kTile, bn);
+        }
+        b1_store<BF16>(reinterpret_cast<float*>(base + lay.b1[kb]), b1r, a.bias1 != nullptr, a.L, jt * kTile, lane);
+        mbar_arrive(full);
+        // mask chunk of the next key tile (this slice's next jt, or the next slice's first)
+        const int njt = jt + 1 < QT ? jt + 1 : 0;
+        SlIter nc = c;
+        if (njt == 0) nc.next(a);
+        if (nc.b < a.B)
+          b1_prefetch(b1r, a.bias1 ? a.bias1 + (static_cast<size_t>(nc.b) * a.N + nc.n) * a.L : nullptr, a.L,
+                      njt * kTile, lane);
+      }
+      for (int it = 0; it < QT; ++it, ++steps) {
+        if (!mbar_wait(smem_u32(&bars->q_empty[s]), ph ^ 1, g)) { ok = false; break; }
+        const uint32_t full = smem_u32(&bars->q_full[s]);
+        if (lane == 0) {
+          mbar_expect_tx(full, q_bytes);
+          tma_load_4d(smem_u32(base + lay.q[s]), &a.tq, full, 0, c.h, it * kTile, bn);
+          tma_load_4d(smem_u32(base + lay.d_o[s]), &a.tdo, full, 0, c.h, it * kTile, bn);
+          if (HAS_B2 && tma_b2) {
+            tma_load_3d(smem_u32(base + lay.b2s[s]), &a.tb2, full, jt * kTile, it * kTile, bh);
+            tma_load_3d(smem_u32(base + lay.b2s[s] + 16384), &a.tb2, full, jt * kTile + 64, it * kTile, bh);
+          }
+        }
+        if (HAS_B2 && !tma_b2)
+          fill_b2_tile_loads(base + lay.b2s[s], a.bias2 + static_cast<size_t>(bh) * a.L * a.L, a.L, it * kTile,
+                             jt * kTile, lane);
+        ld_store(reinterpret_cast<float*>(base + lay.ld[s]), ldr, lane);
+        mbar_arrive(full);
+        advance_pf();
+        prefetch_ld();
+        if (++s == static_cast<uint32_t>(QS)) {
+          s = 0;
+          ph ^= 1;
+        }
+      }
+    }
+  }
+  for (uint32_t b = 0; b < 2; ++b) {
+    const uint32_t issued = (grp + 1 - b) / 2;
+    if (issued > 0) drain_wait(smem_u32(&bars->kv_full[b]), (issued - 1) & 1, a.wait_ns, a.status);
+  }
+  for (uint32_t st = 0; st < static_cast<uint32_t>(QS); ++st) {
+    const uint32_t issued = (steps + QS - 1 - st) / QS;
+    if (issued > 0) drain_wait(smem_u32(&bars->q_full[st]), (issued - 1) & 1, a.wait_ns, a.status);
+  }
+}
+
+struct SlStep {
+  uint32_t u, grp, slice;
+  int jt, it;
+  uint32_t qs, qph;
+};
+
+template <int DP, bool BF16>
+__device__ __forceinline__ bool slice_issue_sdp(const SlStep& st, uint8_t* base, const SliceLayout<DP>& lay,
+                                                SliceBars* bars, uint32_t tmem, const WaitGuard& g) {
+  constexpr uint32_t RB = DP * 2;
+  constexpr uint32_t SWZ = swizzle_for_row(RB);
+  constexpr uint32_t id_s = idesc_f16(128, 128, BF16, false, false);
+  const uint32_t kb = st.grp & 1;
+  if (st.it == 0 && !mbar_wait(smem_u32(&bars->kv_full[kb]), (st.grp >> 1) & 1, g)) return false;
+  if (!mbar_wait(smem_u32(&bars->q_full[st.qs]), st.qph, g)) return false;
+  if (!mbar_wait(smem_u32(&bars->st_free), (st.u & 1) ^ 1, g)) return false;
+  tc_fence_after();
+  const uint32_t q_addr = smem_u32(base + lay.q[st.qs]), do_addr = smem_u32(base + lay.d_o[st.qs]);
+  const uint32_t k_addr = smem_u32(base + lay.k[kb]), v_addr = smem_u32(base + lay.v[kb]);
+#pragma unroll
+  for (int k = 0; k < DP / 16; ++k)
+    umma_ss(tmem + kSlColS, smem_desc(q_addr + k * 32, 16, 8 * RB, SWZ), smem_desc(k_addr + k * 32, 16, 8 * RB, SWZ),
+            id_s, k > 0);
+#pragma unroll
+  for (int k = 0; k < DP / 16; ++k)
+    umma_ss(tmem + kSlColDP, smem_desc(do_addr + k * 32, 16, 8 * RB, SWZ),
+            smem_desc(v_addr + k * 32, 16, 8 * RB, SWZ), id_s, k > 0);
+  umma_commit(smem_u32(&bars->st_full));
+  return true;
+}
+
+template <int DP, bool BF16>
+__device__ __forceinline__ bool slice_issue_grads(const SlStep& st, int QT, uint8_t* base, const SliceLayout<DP>& lay,
+                                                  SliceBars* bars, uint32_t tmem, const WaitGuard& g) {
+  constexpr uint32_t RB = DP * 2;
+  constexpr uint32_t SWZ = swizzle_for_row(RB);
+  constexpr uint32_t id_kv = idesc_f16(128, DP, BF16, true, true);  // dV, dK: MN-major A (smem) and B
+  constexpr uint32_t id_q = idesc_f16(128, DP, BF16, false, true);  // dQ: A from TMEM, MN-major B
+  const uint32_t kb = st.grp & 1;
+  const int nb = slice_kv_bufs(DP, QT);
+  const uint32_t db = st.grp % nb, dph = (st.grp / nb) & 1;
+  if (!mbar_wait(smem_u32(&bars->ds_full), st.u & 1, g)) return false;
+  if (st.it == 0 && !mbar_wait(smem_u32(&bars->dkdv_free[db]), dph ^ 1, g)) return false;
+  if (st.it == 0 && st.jt == 0 && !mbar_wait(smem_u32(&bars->dq_free), (st.slice & 1) ^ 1, g)) return false;
+  tc_fence_after();
+  const uint32_t p_addr = smem_u32(base + lay.p), ds_addr = smem_u32(base + lay.ds);
+  const uint32_t q_addr = smem_u32(base + lay.q[st.qs]), do_addr = smem_u32(base + lay.d_o[st.qs]);
+  const uint32_t k_addr = smem_u32(base + lay.k[kb]);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {  // dV += Pᵀ dO   (K = 128 queries)
+    const uint64_t ad = smem_desc(p_addr + k * 16 * 128, 16384, 1024, kSwizzle128B);
+    const uint64_t bd = smem_desc(do_addr + k * 16 * RB, kTile * RB, 8 * RB, SWZ);
+    umma_ss(tmem + sl_col_dv<DP>(db), ad, bd, id_kv, (st.it > 0 || k > 0) ? 1u : 0u);
+  }
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {  // dK += dSᵀ Q
+    const uint64_t ad = smem_desc(ds_addr + k * 16 * 128, 16384, 1024, kSwizzle128B);
+    const uint64_t bd = smem_desc(q_addr + k * 16 * RB, kTile * RB, 8 * RB, SWZ);
+    umma_ss(tmem + sl_col_dk<DP>(db), ad, bd, id_kv, (st.it > 0 || k > 0) ? 1u : 0u);
+  }
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {  // dQ_it += dS K_jt   (K = 128 keys; dS from TMEM)
+    const uint64_t bd = smem_desc(k_addr + k * 16 * RB, kTile * RB, 8 * RB, SWZ);
+    umma_ts(tmem + sl_col_dq<DP>(st.it, nb), tmem + kSlColDsT + k * 8, bd, id_q, (st.jt > 0 || k > 0) ? 1u : 0u);
+  }
+  umma_commit(smem_u32(&bars->ds_empty));
+  umma_commit(smem_u32(&bars->q_empty[st.qs]));
+  if (st.it == QT - 1) {
+    umma_commit(smem_u32(&bars->dkdv_full[db]));
+    umma_commit(smem_u32(&bars->kv_empty[kb]));
+    if (st.jt == QT - 1) umma_commit(smem_u32(&bars->dq_full));
+  }
+  return true;
+}
+
+template <int DP, bool BF16>
+__device__ __forceinline__ void slice_mma(const BwdArgs& a, uint8_t* base, const SliceLayout<DP>& lay,
+                                          SliceBars* bars, uint32_t tmem, const WaitGuard& g, long long i0,
+                                          long long i1) {
+  const int QS = a.q_stages, QT = a.QT;
+  const uint32_t total = static_cast<uint32_t>((i1 - i0) * QT * QT);
+  auto advance = [&](SlStep& st) {
+    ++st.u;
+    if (++st.it == QT) {
+      st.it = 0;
+      ++st.grp;
+      if (++st.jt == QT) {
+        st.jt = 0;
+        ++st.slice;
+      }
+    }
+    if (++st.qs == static_cast<uint32_t>(QS)) {
+      st.qs = 0;
+      st.qph ^= 1;
+    }
+  };
+  bool ok = total > 0;
+  SlStep cur{0, 0, 0, 0, 0, 0, 0};
+  if (QS >= 2) {
+    if (ok) ok = slice_issue_sdp<DP, BF16>(cur, base, lay, bars, tmem, g);
+    for (uint32_t u = 0; ok && u < total; ++u) {
+      SlStep nxt = cur;
+      advance(nxt);
+      if (u + 1 < total && !slice_issue_sdp<DP, BF16>(nxt, base, lay, bars, tmem, g)) { ok = false; break; }
+      if (!slice_issue_grads<DP, BF16>(cur, QT, base, lay, bars, tmem, g)) { ok = false; break; }
+      cur = nxt;
+    }
+  } else {
+    for (uint32_t u = 0; ok && u < total; ++u) {
+      if (!slice_issue_sdp<DP, BF16>(cur, base, lay, bars, tmem, g)) { ok = false; break; }
+      if (!slice_issue_grads<DP, BF16>(cur, QT, base, lay, bars, tmem, g)) { ok = false; break; }
+      advance(cur);
+    }
+  }
+  umma_commit(smem_u32(&bars->drain));
+  drain_wait(smem_u32(&bars->drain), 0, a.wait_ns, a.status);
+}
+
+// P and dS for one 32-key chunk: the P/dS smem tiles as in the main kernel, and dS
+// (packed pairs, 16 columns) into TMEM for the dQ MMA.
+template <bool BF16, bool HAS_B2>
+__device__ __forceinline__ void slice_chunk(const uint32_t (&sv)[32], const uint32_t (&pv)[32], const float* b1c,
+                                            const uint8_t* b2half, uint8_t* pt, uint8_t* dt, uint32_t ds_tcol, int r,
+                                            int c4, float lse2, float dlt, float2 sl2) {
+  const float2 nl2 = make_float2(-lse2, -lse2), l2e2 = make_float2(kLog2e, kLog2e), nd2 = make_float2(-dlt, -dlt);
+  uint32_t ddt[16];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float4 m0 = *reinterpret_cast<const float4*>(b1c + q * 8);
+    const float4 m1 = *reinterpret_cast<const float4*>(b1c + q * 8 + 4);
+    const float2 mk[4] = {make_float2(m0.x, m0.y), make_float2(m0.z, m0.w), make_float2(m1.x, m1.y),
+                          make_float2(m1.z, m1.w)};
+    uint4 pb = make_uint4(0u, 0u, 0u, 0u);
+    if (HAS_B2) pb = *reinterpret_cast<const uint4*>(b2half + swz_offset(r, c4 * 4 + q, 128));
+    const uint32_t pw[4] = {pb.x, pb.y, pb.z, pb.w};
+    uint32_t pp[4];
+#pragma unroll
+    for (int e2 = 0; e2 < 4; ++e2) {
+      const int x = q * 8 + e2 * 2;
+      float2 t = fma2(make_float2(__uint_as_float(sv[x]), __uint_as_float(sv[x + 1])), sl2, mk[e2]);
+      if (HAS_B2) t = fma2(unpack2<BF16>(pw[e2]), l2e2, t);
+      t = add2(t, nl2);
+      const float p0 = ex2(t.x), p1 = ex2(t.y);
+      const float2 dpd = add2(make_float2(__uint_as_float(pv[x]), __uint_as_float(pv[x + 1])), nd2);
+      const float2 ds = mul2(make_float2(p0, p1), dpd);
+      pp[e2] = pack2<BF16>(p0, p1);
+      ddt[q * 4 + e2] = pack2<BF16>(ds.x, ds.y);
+    }
+    const uint32_t off = swz_offset(r, c4 * 4 + q, 128);
+    *reinterpret_cast<uint4*>(pt + off) = make_uint4(pp[0], pp[1], pp[2], pp[3]);
+    *reinterpret_cast<uint4*>(dt + off) = make_uint4(ddt[q * 4], ddt[q * 4 + 1], ddt[q * 4 + 2], ddt[q * 4 + 3]);
+  }
+  tmem_st16(ds_tcol, ddt);
+}
+
+// dK, dV of key tile jt of slice c (TMEM lanes = keys): this warp's DP/2 columns.
+template <int DP, bool BF16>
+__device__ __forceinline__ bool slice_write_dkdv(const BwdArgs& a, const SlIter& c, int jt, uint32_t grp,
+                                                 SliceBars* bars, uint32_t trow, int r, int hc, int lane,
+                                                 const WaitGuard& g) {
+  constexpr int HD = DP / 2;
+  const int nb = slice_kv_bufs(DP, a.QT);
+  const uint32_t db = grp % nb;
+  if (!mbar_wait(smem_u32(&bars->dkdv_full[db]), (grp / nb) & 1, g)) return false;
+  tc_fence_after();
+  float kx[HD], vx[HD];
+  const uint32_t ck = trow + sl_col_dk<DP>(db) + hc * HD, cv = trow + sl_col_dv<DP>(db) + hc * HD;
+  if constexpr (HD == 8) {
+    uint32_t x[8], y[8];
+    tmem_ld8(ck, x);
+    tmem_ld8(cv, y);
+    tmem_wait_ld(x);
+    tmem_wait_ld(y);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      kx[e] = __uint_as_float(x[e]);
+      vx[e] = __uint_as_float(y[e]);
+    }
+  } else {
+    uint32_t x[HD / 16][16], y[HD / 16][16];
+#pragma unroll
+    for (int q = 0; q < HD / 16; ++q) {
+      tmem_ld16(ck + q * 16, x[q]);
+      tmem_ld16(cv + q * 16, y[q]);
+    }
+#pragma unroll
+    for (int q = 0; q < HD / 16; ++q) {
+      tmem_wait_ld(x[q]);
+      tmem_wait_ld(y[q]);
+    }
+#pragma unroll
+    for (int q = 0; q < HD / 16; ++q)
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        kx[q * 16 + e] = __uint_as_float(x[q][e]);
+        vx[q * 16 + e] = __uint_as_float(y[q][e]);
+      }
+  }
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(smem_u32(&bars->dkdv_free[db]));
+  const int j = jt * kTile + r;
+  if (j < a.L) {
+    const size_t off = ((static_cast<size_t>(c.b) * a.N + c.n) * a.L + j) * a.H * a.D +
+                       static_cast<size_t>(c.h) * a.D + hc * HD;
+#pragma unroll
+    for (int e = 0; e < HD; e += 8)
+      if (hc * HD + e < a.D) {
+        uint4 pk, pv4;
+        pk.x = pack2<BF16>(kx[e + 0] * a.scale, kx[e + 1] * a.scale);
+        pk.y = pack2<BF16>(kx[e + 2] * a.scale, kx[e + 3] * a.scale);
+        pk.z = pack2<BF16>(kx[e + 4] * a.scale, kx[e + 5] * a.scale);
+        pk.w = pack2<BF16>(kx[e + 6] * a.scale, kx[e + 7] * a.scale);
+        pv4.x = pack2<BF16>(vx[e + 0], vx[e + 1]);
+        pv4.y = pack2<BF16>(vx[e + 2], vx[e + 3]);
+        pv4.z = pack2<BF16>(vx[e + 4], vx[e + 5]);
+        pv4.w = pack2<BF16>(vx[e + 6], vx[e + 7]);
+        *reinterpret_cast<uint4*>(a.dk + off + e) = pk;
+        *reinterpret_cast<uint4*>(a.dv + off + e) = pv4;
+      }
+  }
+  return true;
+}
+
+// dQ of slice c (TMEM lanes = queries of each query tile): this warp's DP/2 columns, × s.
+template <int DP, bool BF16>
+__device__ __forceinline__ bool slice_write_dq(const BwdArgs& a, const SlIter& c, uint32_t slice, SliceBars* bars,
+                                               uint32_t trow, int r, int hc, int lane, const WaitGuard& g) {
+  constexpr int HD = DP / 2;
+  if (!mbar_wait(smem_u32(&bars->dq_full), slice & 1, g)) return false;
+  tc_fence_after();
+  const size_t bn = static_cast<size_t>(c.b) * a.N + c.n;
+  for (int it = 0; it < a.QT; ++it) {
+    float v[HD];
+    const uint32_t col = trow + sl_col_dq<DP>(it, slice_kv_bufs(DP, a.QT)) + hc * HD;
+    if constexpr (HD == 8) {
+      uint32_t x[8];
+      tmem_ld8(col, x);
+      tmem_wait_ld(x);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) v[e] = __uint_as_float(x[e]);
+    } else {
+      uint32_t x[HD / 16][16];
+#pragma unroll
+      for (int q = 0; q < HD / 16; ++q) tmem_ld16(col + q * 16, x[q]);
+#pragma unroll
+      for (int q = 0; q < HD / 16; ++q) tmem_wait_ld(x[q]);
+#pragma unroll
+      for (int q = 0; q < HD / 16; ++q)
+#pragma unroll
+        for (int e = 0; e < 16; ++e) v[q * 16 + e] = __uint_as_float(x[q][e]);
+    }
+    const int i = it * kTile + r;
+    if (i < a.L) {
+      uint16_t* dst = a.dq + (bn * a.L + i) * a.H * a.D + static_cast<size_t>(c.h) * a.D + hc * HD;
+#pragma unroll
+      for (int e = 0; e < HD; e += 8)
+        if (hc * HD + e < a.D) {
+          uint4 pk;
+          pk.x = pack2<BF16>(v[e + 0] * a.scale, v[e + 1] * a.scale);
+          pk.y = pack2<BF16>(v[e + 2] * a.scale, v[e + 3] * a.scale);
+          pk.z = pack2<BF16>(v[e + 4] * a.scale, v[e + 5] * a.scale);
+          pk.w = pack2<BF16>(v[e + 6] * a.scale, v[e + 7] * a.scale);
+          *reinterpret_cast<uint4*>(dst + e) = pk;
+        }
+    }
+  }
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(smem_u32(&bars->dq_free));
+  return true;
+}
+
+template <int DP, bool BF16, bool HAS_B2>
+__device__ __forceinline__ void slice_compute(const BwdArgs& a, uint8_t* base, const SliceLayout<DP>& lay,
+                                              SliceBars* bars, uint32_t tmem, const WaitGuard& g, long long i0,
+                                              long long i1) {
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int quad = w & 3, hc = w >> 2;
+  const int r = quad * 32 + lane;
+  const uint32_t trow = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+  const float2 sl2 = make_float2(a.scale_log2, a.scale_log2);
+  const int QS = a.q_stages, QT = a.QT;
+  uint32_t u = 0, grp = 0, slice = 0, s = 0, ph = 0;
+  SlIter cur, prev;
+  cur.init(i0, a);
+  prev = cur;
+  bool ok = true;
+  for (long long item = i0; ok && item < i1; ++item, ++slice) {
+    if (item > i0) {
+      prev = cur;
+      cur.next(a);
+    }
+    for (int jt = 0; ok && jt < QT; ++jt, ++grp) {
+      const uint32_t kb = grp & 1;
+      if (!mbar_wait(smem_u32(&bars->kv_full[kb]), (grp >> 1) & 1, g)) { ok = false; break; }
+      const float* b1 = reinterpret_cast<const float*>(base + lay.b1[kb]) + hc * 64;
+      for (int it = 0; it < QT; ++it, ++u) {
+        if (!mbar_wait(smem_u32(&bars->q_full[s]), ph, g)) { ok = false; break; }
+        const float* ld = reinterpret_cast<const float*>(base + lay.ld[s]);
+        const float lse2 = ld[r], dlt = ld[128 + r];
+        const uint8_t* b2half = base + lay.b2s[s] + hc * 16384;
+        if (!mbar_wait(smem_u32(&bars->st_full), u & 1, g)) { ok = false; break; }
+        if (!mbar_wait(smem_u32(&bars->ds_empty), (u & 1) ^ 1, g)) { ok = false; break; }
+        tc_fence_after();
+        uint8_t* pt = base + lay.p + hc * 16384;
+        uint8_t* dt = base + lay.ds + hc * 16384;
+        const uint32_t dst = trow + kSlColDsT + hc * 32;
+        {
+          uint32_t sv[32], pv[32];
+          tmem_ld32(trow + kSlColS + hc * 64, sv);
+          tmem_ld32(trow + kSlColDP + hc * 64, pv);
+          tmem_wait_ld(sv);
+          tmem_wait_ld(pv);
+          slice_chunk<BF16, HAS_B2>(sv, pv, b1, b2half, pt, dt, dst, r, 0, lse2, dlt, sl2);
+        }
+        {
+          uint32_t sv[32], pv[32];
+          tmem_ld32(trow + kSlColS + hc * 64 + 32, sv);
+          tmem_ld32(trow + kSlColDP + hc * 64 + 32, pv);
+          tmem_wait_ld(sv);
+          tmem_wait_ld(pv);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&bars->st_free));
+          slice_chunk<BF16, HAS_B2>(sv, pv, b1 + 32, b2half, pt, dt, dst + 16, r, 1, lse2, dlt, sl2);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(smem_u32(&bars->ds_full));
+          mbar_arrive(smem_u32(&bars->q_empty[s]));
+          if (it == QT - 1) mbar_arrive(smem_u32(&bars->kv_empty[kb]));
+        }
+        if (it == 0 && grp > 0) {
+          // the previous key tile's dK/dV are complete (of this slice, or of the previous one)
+          if (!slice_write_dkdv<DP, BF16>(a, jt > 0 ? cur : prev, jt > 0 ? jt - 1 : QT - 1, grp - 1, bars, trow, r,
+                                          hc, lane, g)) {
+            ok = false;
+            break;
+          }
+          if (jt == 0 && !slice_write_dq<DP, BF16>(a, prev, slice - 1, bars, trow, r, hc, lane, g)) {
+            ok = false;
+            break;
+          }
+        }
+        if (++s == static_cast<uint32_t>(QS)) {
+          s = 0;
+          ph ^= 1;
+        }
+      }
+    }
+  }
+  if (ok && grp > 0) {
+    if (slice_write_dkdv<DP, BF16>(a, cur, QT - 1, grp - 1, bars, trow, r, hc, lane, g))
+      slice_write_dq<DP, BF16>(a, cur, slice - 1, bars, trow, r, hc, lane, g);
+  }
+}
+
+template <int DP, bool BF16, bool HAS_B2>
+__global__ void __launch_bounds__(kThreads, 1) evo_bwd_slice(const __grid_constant__ BwdArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const SliceLayout<DP> lay(HAS_B2, a.q_stages);
+  SliceBars* bars = reinterpret_cast<SliceBars*>(base + lay.bars);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long i0 = static_cast<long long>(blockIdx.x) * a.chunk;
+  const long long i1 = i0 + a.chunk < a.items ? i0 + a.chunk : a.items;
+  if (threadIdx.x == 0) {
+    bars->abort = 0;
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_u32(&bars->kv_full[s]), 32);
+      mbar_init(smem_u32(&bars->kv_empty[s]), 1 + kComputeWarps);
+    }
+    for (int s = 0; s < kMaxQStages; ++s) {
+      mbar_init(smem_u32(&bars->q_full[s]), 32);
+      mbar_init(smem_u32(&bars->q_empty[s]), 1 + kComputeWarps);
+    }
+    mbar_init(smem_u32(&bars->st_full), 1);
+    mbar_init(smem_u32(&bars->st_free), kComputeWarps);
+    mbar_init(smem_u32(&bars->ds_full), kComputeWarps);
+    mbar_init(smem_u32(&bars->ds_empty), 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&bars->dkdv_full[b]), 1);
+      mbar_init(smem_u32(&bars->dkdv_free[b]), kComputeWarps);
+    }
+    mbar_init(smem_u32(&bars->dq_full), 1);
+    mbar_init(smem_u32(&bars->dq_free), kComputeWarps);
+    mbar_init(smem_u32(&bars->drain), 1);
+    fence_barrier_init();
+  }
+  if (warp == kProducerWarp && lane == 0) {
+    tma_prefetch_desc(&a.tq);
+    tma_prefetch_desc(&a.tk);
+    tma_prefetch_desc(&a.tv);
+    tma_prefetch_desc(&a.tdo);
+    if (HAS_B2 && a.bias2_mode == kBias2Tma) tma_prefetch_desc(&a.tb2);
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(&bars->tmem_slot), 512);
+    tmem_relinquish();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_slot;
+  const WaitGuard g{a.wait_ns, a.status, &bars->abort};
+  if (warp == kProducerWarp) {
+    slice_producer<DP, BF16, HAS_B2>(a, base, lay, bars, g, lane, i0, i1);
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) slice_mma<DP, BF16>(a, base, lay, bars, tmem, g, i0, i1);
+    __syncwarp();
+  } else {
+    slice_compute<DP, BF16, HAS_B2>(a, base, lay, bars, tmem, g, i0, i1);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
 // ============================================================ evo_bwd_db2_part
 constexpr int kMaxPartStages = 3;
 
@@ -872,6 +1511,14 @@ __global__ void __launch_bounds__(kThreads, 1) evo_bwd_db2_part(const __grid_con
     }
     mbar_arrive(full_b2);
     int k = 0, s = 0, ph = 0;
+    B1Raw b1r;
+    LdRaw ldr;
+    auto prefetch = [&](int kk) {
+      const int bn = c.b * a.N + c.n0 + kk;
+      b1_prefetch(b1r, a.bias1 ? a.bias1 + static_cast<size_t>(bn) * a.L : nullptr, a.L, c.jt * kTile, lane);
+      ld_prefetch(ldr, a.lse, a.delta, static_cast<size_t>(bn) * a.H + c.h, a.L, c.it * kTile, lane);
+    };
+    if (nn > 0) prefetch(0);
     for (; k < nn; ++k) {
       if (!mbar_wait(smem_u32(&bars->st_free[s]), ph ^ 1, g)) break;
       const int bn = c.b * a.N + c.n0 + k;
@@ -883,11 +1530,10 @@ __global__ void __launch_bounds__(kThreads, 1) evo_bwd_db2_part(const __grid_con
         tma_load_4d(smem_u32(base + lay.k[s]), &a.tk, full, 0, c.h, c.jt * kTile, bn);
         tma_load_4d(smem_u32(base + lay.v[s]), &a.tv, full, 0, c.h, c.jt * kTile, bn);
       }
-      fill_b1_chunk<BF16>(reinterpret_cast<float*>(base + lay.b1[s]),
-                          a.bias1 ? a.bias1 + static_cast<size_t>(bn) * a.L : nullptr, a.L, c.jt * kTile, lane);
-      fill_lse_delta(reinterpret_cast<float*>(base + lay.ld[s]), a.lse, a.delta,
-                     static_cast<size_t>(bn) * a.H + c.h, a.L, c.it * kTile, lane);
+      b1_store<BF16>(reinterpret_cast<float*>(base + lay.b1[s]), b1r, a.bias1 != nullptr, a.L, c.jt * kTile, lane);
+      ld_store(reinterpret_cast<float*>(base + lay.ld[s]), ldr, lane);
       mbar_arrive(full);
+      if (k + 1 < nn) prefetch(k + 1);
       if (++s == NS) {
         s = 0;
         ph ^= 1;
@@ -1034,16 +1680,48 @@ cudaError_t launch_main(BwdArgs a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+template <int DP, bool BF16, bool HAS_B2>
+cudaError_t launch_slice(BwdArgs a, cudaStream_t st) {
+  const SliceLayout<DP> lay(HAS_B2, a.q_stages);
+  const size_t smem = one_cta_per_sm(lay.total + 1024);
+  auto kern = evo_bwd_slice<DP, BF16, HAS_B2>;
+  static bool limit_set[64] = {};
+  cudaError_t e = ensure_smem_limit(kern, kMaxSmem, limit_set);
+  if (e != cudaSuccess) return e;
+  a.items = static_cast<long long>(a.B) * a.H * a.N;
+  const long long sms = num_sms();
+  a.chunk = (a.items + sms - 1) / sms;
+  const long long grid = (a.items + a.chunk - 1) / a.chunk;
+  kern<<<static_cast<unsigned>(grid), kThreads, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
 template <int DP, bool BF16>
 cudaError_t launch_bwd_d(BwdArgs a, cudaStream_t st, const ProfileEvents* prof) {
   const bool has_b2 = a.bias2_mode != kBias2None;
   const long long rows = static_cast<long long>(a.B) * a.N * a.L * a.H;
   a.items = static_cast<long long>(a.B) * a.H * a.QT * a.N;
+  // slice mode: every dQ tile of a (b, n, h) slice stays in TMEM (no atomics)
+  int slice_qs = 0;
+  if (slice_tmem_fits<DP>(a.QT))
+    for (int q = 3; q >= 2; --q)
+      if (SliceLayout<DP>(has_b2, q).total + 1024 <= kMaxSmem) {
+        slice_qs = q;
+        break;
+      }
+  a.zero_dq = slice_qs == 0;
   prof_record(prof, 2, st);
   evo_bwd_pre<DP, BF16><<<grid_for(rows, 256), 256, 0, st>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   prof_record(prof, 3, st);
+  if (slice_qs > 0) {
+    a.q_stages = slice_qs;
+    e = has_b2 ? launch_slice<DP, BF16, true>(a, st) : launch_slice<DP, BF16, false>(a, st);
+    if (e != cudaSuccess) return e;
+    prof_record(prof, 4, st);
+    prof_record(prof, 5, st);  // no dQ cast in slice mode
+  } else {
 
   // main kernel: deepest Q/dO ring that fits, resident pair-bias tiles when possible
   auto fits = [&](int kind, int qs) { return MainLayout<DP>(kind, qs, a.QT).total + 1024 <= kMaxSmem; };
@@ -1068,6 +1746,7 @@ cudaError_t launch_bwd_d(BwdArgs a, cudaStream_t st, const ProfileEvents* prof) 
   evo_bwd_dq_cast<BF16><<<grid_for(rows * a.D / 8, 256), 256, 0, st>>>(a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   prof_record(prof, 5, st);
+  }
 
   if (has_b2) {
     a.part_stages = PartLayout<DP>(3).total + 1024 <= kMaxSmem ? 3 : 2;

@@ -163,6 +163,18 @@ __device__ __forceinline__ void fwd_producer(const FwdArgs& a, uint8_t* base, co
   uint32_t u = 0, q_it = 0, grp_it = 0, s = 0, ph = 0;
   ItemIter c;
   c.init(i0, a);
+  // raw key-mask values of the next tile, loaded one tile ahead so that their
+  // latency overlaps the wait for a free stage
+  uint16_t b1raw[4];
+  auto b1_prefetch = [&](const ItemIter& t, int jt) {
+    const uint16_t* row = (a.bias1 && t.b < a.B) ? a.bias1 + (static_cast<size_t>(t.b) * a.N + t.n) * a.L : nullptr;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int j = jt * kTile + lane * 4 + e;
+      b1raw[e] = (row && j < a.L) ? row[j] : static_cast<uint16_t>(0);
+    }
+  };
+  b1_prefetch(c, 0);
   bool ok = true;
   for (long long item = i0; ok && item < i1; ++item, c.next(a)) {
     const int bn = c.b * a.N + c.n, bh = c.b * a.H + c.h;
@@ -194,7 +206,6 @@ __device__ __forceinline__ void fwd_producer(const FwdArgs& a, uint8_t* base, co
       tma_load_4d(smem_u32(base + lay.q[qs]), &a.tq, smem_u32(&bars->q_full[qs]), 0, c.h, c.qt * kTile, bn);
     }
     ++q_it;
-    const uint16_t* b1row = a.bias1 ? a.bias1 + static_cast<size_t>(bn) * a.L : nullptr;
     for (int jt = 0; jt < KT; ++jt, ++u) {
       if (!mbar_wait(smem_u32(&bars->kv_empty[s]), ph ^ 1, g)) { ok = false; break; }
       const uint32_t full = smem_u32(&bars->kv_full[s]);
@@ -216,13 +227,18 @@ __device__ __forceinline__ void fwd_producer(const FwdArgs& a, uint8_t* base, co
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int j = jt * kTile + lane * 4 + e;
-          float val = -INFINITY;
-          if (j < a.L) val = b1row ? to_f32<BF16>(b1row[j]) * kLog2e : 0.0f;
-          mv[e] = val;
+          mv[e] = j < a.L ? (a.bias1 ? to_f32<BF16>(b1raw[e]) * kLog2e : 0.0f) : -INFINITY;
         }
         *reinterpret_cast<float4*>(base + lay.b1[s] + lane * 16) = m4;
       }
       mbar_arrive(full);
+      if (jt + 1 < KT) {
+        b1_prefetch(c, jt + 1);
+      } else {
+        ItemIter nc = c;
+        nc.next(a);
+        b1_prefetch(nc, 0);
+      }
       if (++s == static_cast<uint32_t>(S)) {
         s = 0;
         ph ^= 1;

@@ -57,6 +57,7 @@ struct BwdArgs {
   int q_stages;             // main kernel: depth of the Q/dO ring
   int b2_resident;          // main kernel: pair-bias tiles of the (b, h, key tile) group stay in smem
   int part_stages;          // pair-bias partial kernel: depth of its ring
+  int zero_dq;              // delta kernel also clears the fp32 dQ accumulator
   float scale;              // D^-1/2
   float scale_log2;         // D^-1/2 * log2(e)
   int bias2_mode;
