@@ -181,6 +181,18 @@ def dist_setup(args):
     return world, rank, local
 
 
+def max_over_ranks(x: float) -> float:
+    """Maximum of a per-rank float over the process group (identity without one)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 # --------------------------------------------------------------------------- reference arm
 def run_reference(args):
     world, rank, _ = dist_setup(args)
@@ -307,11 +319,7 @@ def run_ours(args):
     wall1 = time.time()
     if world > 1:
         torch.distributed.barrier()
-    ms_total = t_start.elapsed_time(t_end)
-    if world > 1:
-        t = torch.tensor([ms_total], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(t_start.elapsed_time(t_end))
     clock_rows = sampler.stop() if sampler else []
     if E.evo_attn_device_status() != 0:
         raise RuntimeError("device wait timed out during the timed region")
@@ -386,11 +394,7 @@ def run_ours(args):
         host_step()
     e1.record()
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / n_e2e
-    if world > 1:
-        t = torch.tensor([e2e_ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / n_e2e)
     if E.evo_attn_device_status() != 0:
         raise RuntimeError("device wait timed out during the end-to-end run")
     h2d = sum(t.numel() * t.element_size() for t in (h["q"], h["k"], h["v"], h["do"], h["bias1"], h["bias2"])
