@@ -420,7 +420,9 @@ def run_ours(args):
             "vs_baseline": None, "dtype": args.dtype, "data": "synthetic",
             "config": {"workload": w.name, "B": w.B, "N": w.N, "L": w.L, "H": w.H, "D": w.D,
                        "bias1": w.mask and f"{w.mask[0]} {w.mask[1]}", "bias2": has_b2,
-                       "l2": f"inputs larger than L2: {R} rotating replicas of {per_rep / 1e6:.0f} MB",
+                       "l2": (f"inputs larger than L2: {R} rotating replicas of {per_rep / 1e6:.0f} MB"
+                              if R * per_rep >= L2_BYTES else
+                              f"L2-warm: {R} replicas of {per_rep / 1e6:.1f} MB fit in L2 (small case)"),
                        "parallelism": f"{world} independent replicas" if world > 1 else "single GPU"},
             "fwd_tflops": fwd_tflops,
             "fwd_frac_of_peak": fwd_tflops / peaks["bf16_tflops_sustained"],
