@@ -32,19 +32,11 @@
 //   evo_bwd_db2_sum   dbias2 = Σ_groups partial in fixed order, cast.
 // Both pair-bias stages run in a fixed order, so dbias2 is bitwise
 // reproducible.  dQ uses fp32 atomics and is not.
-#include "evo_internal.h"
-#include "evo_ptx.cuh"
+#include "evo_bwd_common.cuh"
 
 namespace evo {
 namespace {
 
-constexpr float kLog2e = 1.4426950408889634f;
-
-__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns, int* status) {
-  volatile int never = 0;
-  WaitGuard g{limit_ns, status, &never};
-  mbar_wait(bar, parity, g);
-}
 
 // ============================================================ evo_bwd_pre
 template <int DP, bool BF16>
@@ -78,6 +70,27 @@ __global__ void __launch_bounds__(256) evo_bwd_pre(const BwdArgs a) {
     }
     a.delta[(bn * a.H + h) * a.L + i] = sum;
   }
+  if (a.b2t) {  // transposed pair bias for the key-major kernel, in 32 x 32 tiles through smem
+    __shared__ uint16_t tile[32][34];
+    const int TL = (a.L + 31) / 32, lane = threadIdx.x & 31, row0 = threadIdx.x >> 5;
+    const long long tiles = static_cast<long long>(a.B) * a.H * TL * TL;
+    for (long long t = blockIdx.x; t < tiles; t += gridDim.x) {
+      const int tj = static_cast<int>(t % TL), ti = static_cast<int>((t / TL) % TL);
+      const long long bh = t / (static_cast<long long>(TL) * TL);
+      const uint16_t* src = a.bias2 + bh * a.L * a.L;
+      for (int rr = row0; rr < 32; rr += 8) {
+        const int i = ti * 32 + rr, j = tj * 32 + lane;
+        tile[rr][lane] = (i < a.L && j < a.L) ? src[static_cast<size_t>(i) * a.L + j] : static_cast<uint16_t>(0);
+      }
+      __syncthreads();
+      uint16_t* dst = a.b2t + bh * a.L * a.b2t_pitch;
+      for (int rr = row0; rr < 32; rr += 8) {
+        const int j = tj * 32 + rr, i = ti * 32 + lane;
+        if (j < a.L && i < a.L) dst[static_cast<size_t>(j) * a.b2t_pitch + i] = tile[lane][rr];
+      }
+      __syncthreads();
+    }
+  }
 }
 
 // ============================================================ evo_bwd_dq_cast
@@ -108,126 +121,6 @@ __global__ void __launch_bounds__(256) evo_bwd_db2_sum(const BwdArgs a) {
   }
 }
 
-// ============================================================ shared pieces
-constexpr int kComputeWarps = 8;
-constexpr int kThreads = (kComputeWarps + 2) * 32;
-constexpr int kProducerWarp = kComputeWarps, kMmaWarp = kComputeWarps + 1;
-constexpr size_t kMaxSmem = 232448;  // 227 KB opt-in limit per block
-
-// Pair-bias tile [128 queries][128 keys] in two 64-key halves, 128B swizzle —
-// the layout the 3-D TMA map with box (64, 128, 1) writes.  Generic-load fill
-// for L % 8 != 0 (no TMA: the row pitch is not a multiple of 16 bytes).
-__device__ __forceinline__ void fill_b2_tile_loads(uint8_t* dst, const uint16_t* b2, int L, int i0, int j0,
-                                                   int lane) {
-  const int cc = lane * 4, half = cc >> 6, chunk = (cc & 63) >> 3, within = cc & 7;
-  for (int r = 0; r < kTile; ++r) {
-    const int i = i0 + r;
-    uint32_t w[2] = {0u, 0u};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int j = j0 + cc + e;
-      const uint32_t val = (i < L && j < L) ? b2[static_cast<size_t>(i) * L + j] : 0u;
-      w[e >> 1] |= val << (16 * (e & 1));
-    }
-    *reinterpret_cast<uint2*>(dst + half * 16384 + swz_offset(r, chunk, 128) + within * 2) =
-        make_uint2(w[0], w[1]);
-  }
-}
-
-// Key-mask chunk for keys j0..j0+127: fp32 × log2(e); -inf past L.
-template <bool BF16>
-__device__ __forceinline__ void fill_b1_chunk(float* dst, const uint16_t* b1row, int L, int j0, int lane) {
-  float4 m4;
-  float* mv = reinterpret_cast<float*>(&m4);
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const int j = j0 + lane * 4 + e;
-    float val = -INFINITY;
-    if (j < L) val = b1row ? to_f32<BF16>(b1row[j]) * kLog2e : 0.0f;
-    mv[e] = val;
-  }
-  reinterpret_cast<float4*>(dst)[lane] = m4;
-}
-
-// The same chunk in two halves: loads issued one stage ahead (raw values held
-// in registers, so their latency overlaps the wait for a free stage), then
-// converted and written when the stage is filled.
-struct B1Raw {
-  uint16_t v[4];
-};
-__device__ __forceinline__ void b1_prefetch(B1Raw& raw, const uint16_t* b1row, int L, int j0, int lane) {
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const int j = j0 + lane * 4 + e;
-    raw.v[e] = (b1row && j < L) ? b1row[j] : static_cast<uint16_t>(0);
-  }
-}
-template <bool BF16>
-__device__ __forceinline__ void b1_store(float* dst, const B1Raw& raw, bool has_b1, int L, int j0, int lane) {
-  float4 m4;
-  float* mv = reinterpret_cast<float*>(&m4);
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const int j = j0 + lane * 4 + e;
-    mv[e] = j < L ? (has_b1 ? to_f32<BF16>(raw.v[e]) * kLog2e : 0.0f) : -INFINITY;
-  }
-  reinterpret_cast<float4*>(dst)[lane] = m4;
-}
-
-// lse (× log2 e; +inf for rows past L or with an empty softmax, so P = 0) and
-// delta for queries i0..i0+127 of slice bnh, prefetched like the key mask.
-struct LdRaw {
-  float l[4], d[4];
-};
-__device__ __forceinline__ void ld_prefetch(LdRaw& raw, const float* lse, const float* delta, size_t bnh, int L,
-                                            int i0, int lane) {
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const int i = i0 + lane * 4 + e;
-    raw.l[e] = i < L ? lse[bnh * L + i] : -INFINITY;
-    raw.d[e] = i < L ? delta[bnh * L + i] : 0.0f;
-  }
-}
-__device__ __forceinline__ void ld_store(float* dst, const LdRaw& raw, int lane) {
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const float x = raw.l[e];
-    dst[lane * 4 + e] = (x == -INFINITY) ? INFINITY : x * kLog2e;
-    dst[128 + lane * 4 + e] = raw.d[e];
-  }
-}
-__device__ __forceinline__ void fill_lse_delta(float* dst, const float* lse, const float* delta, size_t bnh, int L,
-                                               int i0, int lane) {
-  LdRaw raw;
-  ld_prefetch(raw, lse, delta, bnh, L, i0, lane);
-  ld_store(dst, raw, lane);
-}
-
-// Incremental (b, h, key tile, n) iterator, n fastest.
-struct KvIter {
-  int b, h, jt, n;
-  __device__ __forceinline__ void init(long long item, const BwdArgs& a) {
-    long long t = item;
-    n = static_cast<int>(t % a.N);
-    t /= a.N;
-    jt = static_cast<int>(t % a.QT);
-    t /= a.QT;
-    h = static_cast<int>(t % a.H);
-    b = static_cast<int>(t / a.H);
-  }
-  __device__ __forceinline__ void next(const BwdArgs& a) {
-    if (++n == a.N) {
-      n = 0;
-      if (++jt == a.QT) {
-        jt = 0;
-        if (++h == a.H) {
-          h = 0;
-          ++b;
-        }
-      }
-    }
-  }
-};
 
 // ============================================================ evo_bwd_main
 enum B2Kind : int { kB2None = 0, kB2Resident = 1, kB2Stream = 2 };
@@ -865,25 +758,6 @@ struct SliceLayout {
   }
 };
 
-// (b, h, n) slice iterator, n fastest.
-struct SlIter {
-  int b, h, n;
-  __device__ __forceinline__ void init(long long item, const BwdArgs& a) {
-    n = static_cast<int>(item % a.N);
-    const long long t = item / a.N;
-    h = static_cast<int>(t % a.H);
-    b = static_cast<int>(t / a.H);
-  }
-  __device__ __forceinline__ void next(const BwdArgs& a) {
-    if (++n == a.N) {
-      n = 0;
-      if (++h == a.H) {
-        h = 0;
-        ++b;
-      }
-    }
-  }
-};
 
 template <int DP, bool BF16, bool HAS_B2>
 __device__ __forceinline__ void slice_producer(const BwdArgs& a, uint8_t* base, const SliceLayout<DP>& lay,
@@ -1656,7 +1530,6 @@ __global__ void __launch_bounds__(kThreads, 1) evo_bwd_db2_part(const __grid_con
 }
 
 // ============================================================ launch
-size_t one_cta_per_sm(size_t bytes) { return bytes > 116u * 1024u ? bytes : 116u * 1024u; }
 
 unsigned grid_for(long long work, long long per_block) {
   long long g = (work + per_block - 1) / per_block;
@@ -1696,26 +1569,35 @@ cudaError_t launch_slice(BwdArgs a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+// Query-major slice mode: every dQ tile of a (b, n, h) slice stays in TMEM (no atomics).
+template <int DP>
+int slice_q_stages(int QT, bool has_b2) {
+  if (!slice_tmem_fits<DP>(QT)) return 0;
+  for (int q = 3; q >= 2; --q)
+    if (SliceLayout<DP>(has_b2, q).total + 1024 <= kMaxSmem) return q;
+  return 0;
+}
+
 template <int DP, bool BF16>
 cudaError_t launch_bwd_d(BwdArgs a, cudaStream_t st, const ProfileEvents* prof) {
   const bool has_b2 = a.bias2_mode != kBias2None;
   const long long rows = static_cast<long long>(a.B) * a.N * a.L * a.H;
   a.items = static_cast<long long>(a.B) * a.H * a.QT * a.N;
-  // slice mode: every dQ tile of a (b, n, h) slice stays in TMEM (no atomics)
-  int slice_qs = 0;
-  if (slice_tmem_fits<DP>(a.QT))
-    for (int q = 3; q >= 2; --q)
-      if (SliceLayout<DP>(has_b2, q).total + 1024 <= kMaxSmem) {
-        slice_qs = q;
-        break;
-      }
-  a.zero_dq = slice_qs == 0;
+  const BwdPlan plan = bwd_plan(DP, a.QT, has_b2);
+  const int slice_qs = plan.mode == kBwdSlice ? plan.q_stages : 0;
+  a.zero_dq = plan.mode == kBwdMain;
+  if (plan.mode != kBwdKeyMajor) a.b2t = nullptr;
   prof_record(prof, 2, st);
   evo_bwd_pre<DP, BF16><<<grid_for(rows, 256), 256, 0, st>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   prof_record(prof, 3, st);
-  if (slice_qs > 0) {
+  if (plan.mode == kBwdKeyMajor) {
+    a.q_stages = plan.q_stages;
+    if ((e = launch_bwd_kmajor(a, DP, BF16, has_b2, st)) != cudaSuccess) return e;
+    prof_record(prof, 4, st);
+    prof_record(prof, 5, st);  // no dQ cast: dQ stays in TMEM
+  } else if (slice_qs > 0) {
     a.q_stages = slice_qs;
     e = has_b2 ? launch_slice<DP, BF16, true>(a, st) : launch_slice<DP, BF16, false>(a, st);
     if (e != cudaSuccess) return e;
@@ -1767,7 +1649,24 @@ cudaError_t launch_bwd_d(BwdArgs a, cudaStream_t st, const ProfileEvents* prof) 
   return cudaSuccess;
 }
 
+template <int DP>
+BwdPlan plan_d(int QT, bool has_b2) {
+  const int km = kmajor_q_stages(DP, QT, has_b2);
+  if (km > 0) return {kBwdKeyMajor, km};
+  const int sl = slice_q_stages<DP>(QT, has_b2);
+  if (sl > 0) return {kBwdSlice, sl};
+  return {kBwdMain, 0};
+}
+
 }  // namespace
+
+BwdPlan bwd_plan(int DP, int QT, bool has_b2) {
+  switch (DP) {
+    case 16: return plan_d<16>(QT, has_b2);
+    case 32: return plan_d<32>(QT, has_b2);
+    default: return plan_d<64>(QT, has_b2);
+  }
+}
 
 cudaError_t launch_bwd(const BwdArgs& a, int DP, bool bf16, cudaStream_t st, const ProfileEvents* p) {
   switch (DP) {

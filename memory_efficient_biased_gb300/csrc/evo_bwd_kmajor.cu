@@ -1,0 +1,668 @@
+// evo_bwd_kmajor.cu — key-major slice backward of memory-efficient biased
+// Evoformer attention for sm_103a.
+//
+// Definition: web page "DeepSpeed4Science 技术指南：AI4Science 大模型长序列训练
+// 与 Evoformer 内存高效注意力内核实战" §3.7 (the backward forms delta, then dQ, dK,
+// dV from the probabilities rebuilt with the saved lse) and §3.2 (recompute
+// instead of storing the attention matrix).
+//
+// One CTA owns whole (b, n, h) slices, like the query-major slice kernel, but
+// the scores are formed transposed: for key tile jt and query tile it,
+//   Sᵀ = K Qᵀ and dPᵀ = V dOᵀ      (TMEM lane = key, column = query)
+// so that each compute thread owns one key j of the tile.  It rebuilds
+//   Pᵀ_ji = exp2(s·log2e·S_ij + mask_j·log2e + bias2_ij·log2e − lse_i·log2e)
+//   dSᵀ_ji = Pᵀ_ji (dP_ij − delta_i)
+// writes Pᵀ (fp16 / bf16 pairs) into one of two TMEM buffers, the A operand of
+// the TS-form MMA  dV += Pᵀ dO, and dS into one of two swizzled shared-memory
+// tiles [key][query], read as the K-major A operand of  dK += dSᵀ Q  and as the
+// MN-major A operand of  dQ_it += dS K  (dQ tiles stay in TMEM across key
+// tiles).  Both buffers are double, so the compute warps form step u+1 while
+// the gradient MMAs of step u run; S and dP of step u+1 are computed while the
+// compute warps work on step u.  Finished dK, dV and dQ tiles leave through
+// shared memory by TMA tile stores, one step after their last MMA.  The pair
+// bias is read from a transposed copy [B,H,L,L'] (L' = L rounded up to 8) that
+// the delta kernel writes, so each thread reads its key's row.
+//
+// TMEM columns: Sᵀ 0..127, dPᵀ 128..255, Pᵀ buffers 256..319 and 320..383
+// (packed pairs), then dK, dV (one or two buffers) and the QT dQ tiles.
+#include "evo_bwd_common.cuh"
+
+namespace evo {
+namespace {
+
+constexpr int kKmMaxQS = 4;
+constexpr uint32_t kKmS = 0u, kKmDP = 128u, kKmP = 256u, kKmAcc = 384u;
+__device__ __forceinline__ uint32_t km_col_p(uint32_t b) { return kKmP + b * 64u; }
+
+__host__ __device__ constexpr bool km_tmem_fits(int DP, int QT) { return 384 + 2 * DP + QT * DP <= 512; }
+__host__ __device__ constexpr int km_kv_bufs(int DP, int QT) { return 384 + 4 * DP + QT * DP <= 512 ? 2 : 1; }
+template <int DP>
+__device__ __forceinline__ uint32_t km_col_dk(uint32_t b) { return kKmAcc + b * 2 * DP; }
+template <int DP>
+__device__ __forceinline__ uint32_t km_col_dv(uint32_t b) { return kKmAcc + b * 2 * DP + DP; }
+template <int DP>
+__device__ __forceinline__ uint32_t km_col_dq(int it, int nb) { return kKmAcc + nb * 2 * DP + it * DP; }
+
+struct KmBars {
+  uint64_t kv_full[2], kv_empty[2];
+  uint64_t q_full[kKmMaxQS], q_empty[kKmMaxQS];
+  uint64_t st_full, st_free, pds_full, buf_free[2];
+  uint64_t dkdv_full[2], dkdv_free[2], dq_full, dq_free;
+  uint64_t stg_free, stg_full;  // staging tiles: free to write (thread 0) / written (compute warps)
+  uint64_t drain;
+  uint32_t tmem_slot;
+  int abort;
+};
+
+template <int DP>
+struct KmLayout {
+  static constexpr uint32_t kTB = kTile * DP * 2;
+  uint32_t ds[2], b2t[kKmMaxQS], stg[2], k[2], v[2], q[kKmMaxQS], d_o[kKmMaxQS], b1[2], ld[kKmMaxQS], bars,
+      total;
+  __host__ __device__ KmLayout(bool has_b2, int qs) {
+    uint32_t off = 0;
+    for (int s = 0; s < 2; ++s) {  // 128B-swizzled tiles first (1024-byte aligned)
+      ds[s] = off;
+      off += 32768u;
+    }
+    for (int s = 0; s < 2; ++s) {  // staging of finished dK / dV / dQ tiles for the TMA stores
+      stg[s] = off;
+      off += kTB;
+    }
+    for (int s = 0; s < kKmMaxQS; ++s) b2t[s] = off + (s < qs ? s : 0) * 32768u;
+    if (has_b2) off += qs * 32768u;
+    for (int s = 0; s < 2; ++s) {
+      k[s] = off;
+      v[s] = off + kTB;
+      off += 2 * kTB;
+    }
+    for (int s = 0; s < kKmMaxQS; ++s) {
+      q[s] = off + (s < qs ? s : 0) * 2 * kTB;
+      d_o[s] = q[s] + kTB;
+    }
+    off += qs * 2 * kTB;
+    for (int s = 0; s < 2; ++s) b1[s] = off + s * 512u;
+    off += 1024u;
+    for (int s = 0; s < kKmMaxQS; ++s) ld[s] = off + (s < qs ? s : 0) * 1024u;
+    off += qs * 1024u;
+    bars = off;
+    off += (sizeof(KmBars) + 127) & ~127u;
+    total = off;
+  }
+};
+
+// −lse·log2e (−inf for rows past L or with an empty softmax, so P = 0) and
+// −delta for the 128 queries of a step: the per-column terms of the exponent
+// and of dS.
+__device__ __forceinline__ void ld_store_neg(float* dst, const LdRaw& raw, int lane) {
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float x = raw.l[e];
+    dst[lane * 4 + e] = (x == -INFINITY) ? -INFINITY : -x * kLog2e;
+    dst[128 + lane * 4 + e] = -raw.d[e];
+  }
+}
+
+template <int DP, bool BF16, bool HAS_B2>
+__device__ __forceinline__ void km_producer(const BwdArgs& a, uint8_t* base, const KmLayout<DP>& lay, KmBars* bars,
+                                            const WaitGuard& g, int lane, long long i0, long long i1) {
+  constexpr uint32_t kTB = KmLayout<DP>::kTB;
+  const int QS = a.q_stages, QT = a.QT;
+  const uint32_t q_bytes = 2 * kTB + (HAS_B2 ? 32768u : 0u);
+  uint32_t grp = 0, steps = 0, s = 0, ph = 0;
+  SlIter c;
+  c.init(i0, a);
+  SlIter pc = c;  // lse / delta of the next step and the mask of the next key tile, loaded one step ahead
+  int pjt = 0, pit = 0;
+  LdRaw ldr;
+  B1Raw b1r;
+  auto prefetch_ld = [&]() {
+    if (pc.b < a.B)
+      ld_prefetch(ldr, a.lse, a.delta, (static_cast<size_t>(pc.b) * a.N + pc.n) * a.H + pc.h, a.L, pit * kTile,
+                  lane);
+  };
+  auto advance_pf = [&]() {
+    if (++pit == QT) {
+      pit = 0;
+      if (++pjt == QT) {
+        pjt = 0;
+        pc.next(a);
+      }
+    }
+  };
+  b1_prefetch(b1r, a.bias1 ? a.bias1 + (static_cast<size_t>(c.b) * a.N + c.n) * a.L : nullptr, a.L, 0, lane);
+  prefetch_ld();
+  bool ok = true;
+  for (long long item = i0; ok && item < i1; ++item, c.next(a)) {
+    const int bn = c.b * a.N + c.n, bh = c.b * a.H + c.h;
+    for (int jt = 0; ok && jt < QT; ++jt, ++grp) {
+      const uint32_t kb = grp & 1;
+      if (!mbar_wait(smem_u32(&bars->kv_empty[kb]), ((grp >> 1) & 1) ^ 1, g)) { ok = false; break; }
+      {
+        const uint32_t full = smem_u32(&bars->kv_full[kb]);
+        if (lane == 0) {
+          mbar_expect_tx(full, 2 * kTB);
+          tma_load_4d(smem_u32(base + lay.k[kb]), &a.tk, full, 0, c.h, jt * kTile, bn);
+          tma_load_4d(smem_u32(base + lay.v[kb]), &a.tv, full, 0, c.h, jt * kTile, bn);
+        }
+        b1_store<BF16>(reinterpret_cast<float*>(base + lay.b1[kb]), b1r, a.bias1 != nullptr, a.L, jt * kTile, lane);
+        mbar_arrive(full);
+        const int njt = jt + 1 < QT ? jt + 1 : 0;
+        SlIter nc = c;
+        if (njt == 0) nc.next(a);
+        if (nc.b < a.B)
+          b1_prefetch(b1r, a.bias1 ? a.bias1 + (static_cast<size_t>(nc.b) * a.N + nc.n) * a.L : nullptr, a.L,
+                      njt * kTile, lane);
+      }
+      for (int it = 0; it < QT; ++it, ++steps) {
+        if (!mbar_wait(smem_u32(&bars->q_empty[s]), ph ^ 1, g)) { ok = false; break; }
+        const uint32_t full = smem_u32(&bars->q_full[s]);
+        if (lane == 0) {
+          mbar_expect_tx(full, q_bytes);
+          tma_load_4d(smem_u32(base + lay.q[s]), &a.tq, full, 0, c.h, it * kTile, bn);
+          tma_load_4d(smem_u32(base + lay.d_o[s]), &a.tdo, full, 0, c.h, it * kTile, bn);
+          if (HAS_B2) {  // transposed pair bias: rows = keys of tile jt, columns = queries of tile it
+            tma_load_3d(smem_u32(base + lay.b2t[s]), &a.tb2t, full, it * kTile, jt * kTile, bh);
+            tma_load_3d(smem_u32(base + lay.b2t[s] + 16384), &a.tb2t, full, it * kTile + 64, jt * kTile, bh);
+          }
+        }
+        ld_store_neg(reinterpret_cast<float*>(base + lay.ld[s]), ldr, lane);
+        mbar_arrive(full);
+        advance_pf();
+        prefetch_ld();
+        if (++s == static_cast<uint32_t>(QS)) {
+          s = 0;
+          ph ^= 1;
+        }
+      }
+    }
+  }
+  for (uint32_t b = 0; b < 2; ++b) {
+    const uint32_t issued = (grp + 1 - b) / 2;
+    if (issued > 0) drain_wait(smem_u32(&bars->kv_full[b]), (issued - 1) & 1, a.wait_ns, a.status);
+  }
+  for (uint32_t st = 0; st < static_cast<uint32_t>(QS); ++st) {
+    const uint32_t issued = (steps + QS - 1 - st) / QS;
+    if (issued > 0) drain_wait(smem_u32(&bars->q_full[st]), (issued - 1) & 1, a.wait_ns, a.status);
+  }
+}
+
+struct KmStep {
+  uint32_t u, grp, slice;
+  int jt, it;
+  uint32_t qs, qph;
+};
+
+// Sᵀ = K Qᵀ and dPᵀ = V dOᵀ of one step into TMEM.
+template <int DP, bool BF16>
+__device__ __forceinline__ bool km_issue_sdp(const KmStep& st, uint8_t* base, const KmLayout<DP>& lay, KmBars* bars,
+                                             uint32_t tmem, const WaitGuard& g) {
+  constexpr uint32_t RB = DP * 2;
+  constexpr uint32_t SWZ = swizzle_for_row(RB);
+  constexpr uint32_t id_s = idesc_f16(128, 128, BF16, false, false);
+  const uint32_t kb = st.grp & 1;
+  if (st.it == 0 && !mbar_wait(smem_u32(&bars->kv_full[kb]), (st.grp >> 1) & 1, g)) return false;
+  if (!mbar_wait(smem_u32(&bars->q_full[st.qs]), st.qph, g)) return false;
+  if (!mbar_wait(smem_u32(&bars->st_free), (st.u & 1) ^ 1, g)) return false;
+  tc_fence_after();
+  const uint32_t q_addr = smem_u32(base + lay.q[st.qs]), do_addr = smem_u32(base + lay.d_o[st.qs]);
+  const uint32_t k_addr = smem_u32(base + lay.k[kb]), v_addr = smem_u32(base + lay.v[kb]);
+#pragma unroll
+  for (int k = 0; k < DP / 16; ++k)
+    umma_ss(tmem + kKmS, smem_desc(k_addr + k * 32, 16, 8 * RB, SWZ), smem_desc(q_addr + k * 32, 16, 8 * RB, SWZ),
+            id_s, k > 0);
+#pragma unroll
+  for (int k = 0; k < DP / 16; ++k)
+    umma_ss(tmem + kKmDP, smem_desc(v_addr + k * 32, 16, 8 * RB, SWZ),
+            smem_desc(do_addr + k * 32, 16, 8 * RB, SWZ), id_s, k > 0);
+  umma_commit(smem_u32(&bars->st_full));
+  return true;
+}
+
+// dV += Pᵀ dO (A = Pᵀ in TMEM), dK += dSᵀ Q (A = the dS tile, K-major), then
+// dQ_it += dS K (A = the same tile, MN-major).
+template <int DP, bool BF16>
+__device__ __forceinline__ bool km_issue_grads(const KmStep& st, int QT, uint8_t* base, const KmLayout<DP>& lay,
+                                               KmBars* bars, uint32_t tmem, const WaitGuard& g) {
+  constexpr uint32_t RB = DP * 2;
+  constexpr uint32_t SWZ = swizzle_for_row(RB);
+  constexpr uint32_t id_v = idesc_f16(128, DP, BF16, false, true);   // A from TMEM, MN-major B
+  constexpr uint32_t id_k = idesc_f16(128, DP, BF16, false, true);   // K-major A (smem), MN-major B
+  constexpr uint32_t id_q = idesc_f16(128, DP, BF16, true, true);    // MN-major A, MN-major B
+  const uint32_t kb = st.grp & 1;
+  const int nb = km_kv_bufs(DP, QT);
+  const uint32_t db = st.grp % nb, dph = (st.grp / nb) & 1;
+  const uint32_t b = st.u & 1;
+  if (!mbar_wait(smem_u32(&bars->pds_full), st.u & 1, g)) return false;
+  if (st.it == 0 && !mbar_wait(smem_u32(&bars->dkdv_free[db]), dph ^ 1, g)) return false;
+  tc_fence_after();
+  const uint32_t q_addr = smem_u32(base + lay.q[st.qs]), do_addr = smem_u32(base + lay.d_o[st.qs]);
+  const uint32_t k_addr = smem_u32(base + lay.k[kb]), ds_addr = smem_u32(base + lay.ds[b]);
+  const uint32_t pcol = tmem + km_col_p(b);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {  // dV += Pᵀ dO   (K = 128 queries)
+    const uint64_t bd = smem_desc(do_addr + k * 16 * RB, kTile * RB, 8 * RB, SWZ);
+    umma_ts(tmem + km_col_dv<DP>(db), pcol + k * 8, bd, id_v, (st.it > 0 || k > 0) ? 1u : 0u);
+  }
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {  // dK += dSᵀ Q
+    const uint64_t ad = smem_desc(ds_addr + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024, kSwizzle128B);
+    const uint64_t bd = smem_desc(q_addr + k * 16 * RB, kTile * RB, 8 * RB, SWZ);
+    umma_ss(tmem + km_col_dk<DP>(db), ad, bd, id_k, (st.it > 0 || k > 0) ? 1u : 0u);
+  }
+  umma_commit(smem_u32(&bars->q_empty[st.qs]));
+  if (st.it == QT - 1) umma_commit(smem_u32(&bars->dkdv_full[db]));
+  if (st.it == 0 && st.jt == 0 && !mbar_wait(smem_u32(&bars->dq_free), (st.slice & 1) ^ 1, g)) return false;
+  tc_fence_after();
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {  // dQ_it += dS K_jt   (K = 128 keys)
+    const uint64_t ad = smem_desc(ds_addr + k * 16 * 128, 16384, 1024, kSwizzle128B);
+    const uint64_t bd = smem_desc(k_addr + k * 16 * RB, kTile * RB, 8 * RB, SWZ);
+    umma_ss(tmem + km_col_dq<DP>(st.it, nb), ad, bd, id_q, (st.jt > 0 || k > 0) ? 1u : 0u);
+  }
+  umma_commit(smem_u32(&bars->buf_free[b]));
+  if (st.it == QT - 1) {
+    umma_commit(smem_u32(&bars->kv_empty[kb]));
+    if (st.jt == QT - 1) umma_commit(smem_u32(&bars->dq_full));
+  }
+  return true;
+}
+
+template <int DP, bool BF16>
+__device__ __forceinline__ void km_mma(const BwdArgs& a, uint8_t* base, const KmLayout<DP>& lay, KmBars* bars,
+                                       uint32_t tmem, const WaitGuard& g, long long i0, long long i1) {
+  const int QS = a.q_stages, QT = a.QT;
+  const uint32_t total = static_cast<uint32_t>((i1 - i0) * QT * QT);
+  auto advance = [&](KmStep& st) {
+    ++st.u;
+    if (++st.it == QT) {
+      st.it = 0;
+      ++st.grp;
+      if (++st.jt == QT) {
+        st.jt = 0;
+        ++st.slice;
+      }
+    }
+    if (++st.qs == static_cast<uint32_t>(QS)) {
+      st.qs = 0;
+      st.qph ^= 1;
+    }
+  };
+  // S/dP of step u+1 are issued before the gradients of step u (needs two Q/dO stages)
+  bool ok = total > 0;
+  KmStep cur{0, 0, 0, 0, 0, 0, 0};
+  if (ok) ok = km_issue_sdp<DP, BF16>(cur, base, lay, bars, tmem, g);
+  for (uint32_t u = 0; ok && u < total; ++u) {
+    KmStep nxt = cur;
+    advance(nxt);
+    if (u + 1 < total && !km_issue_sdp<DP, BF16>(nxt, base, lay, bars, tmem, g)) break;
+    if (!km_issue_grads<DP, BF16>(cur, QT, base, lay, bars, tmem, g)) break;
+    cur = nxt;
+  }
+  umma_commit(smem_u32(&bars->drain));
+  drain_wait(smem_u32(&bars->drain), 0, a.wait_ns, a.status);
+}
+
+// Pᵀ for 32 queries of this thread's key into TMEM (packed pairs) and dS into
+// the swizzled smem tile.  nl / nd: −lse·log2e and −delta of the 32 queries.
+template <bool BF16, bool HAS_B2>
+__device__ __forceinline__ void km_chunk(const uint32_t (&sv)[32], const uint32_t (&pv)[32], float b1j,
+                                         const float* nl, const float* nd, const uint8_t* b2half, uint8_t* dshalf,
+                                         uint32_t p_tcol, int r, int c, float2 sl2) {
+  const float2 mk = make_float2(b1j, b1j), l2e2 = make_float2(kLog2e, kLog2e);
+  uint32_t pp[16], dd[16];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float4 l0 = *reinterpret_cast<const float4*>(nl + q * 8);
+    const float4 l1 = *reinterpret_cast<const float4*>(nl + q * 8 + 4);
+    const float4 d0 = *reinterpret_cast<const float4*>(nd + q * 8);
+    const float4 d1 = *reinterpret_cast<const float4*>(nd + q * 8 + 4);
+    const float2 nl2[4] = {make_float2(l0.x, l0.y), make_float2(l0.z, l0.w), make_float2(l1.x, l1.y),
+                           make_float2(l1.z, l1.w)};
+    const float2 nd2[4] = {make_float2(d0.x, d0.y), make_float2(d0.z, d0.w), make_float2(d1.x, d1.y),
+                           make_float2(d1.z, d1.w)};
+    uint4 pb = make_uint4(0u, 0u, 0u, 0u);
+    if (HAS_B2) pb = *reinterpret_cast<const uint4*>(b2half + swz_offset(r, c * 4 + q, 128));
+    const uint32_t pw[4] = {pb.x, pb.y, pb.z, pb.w};
+#pragma unroll
+    for (int e2 = 0; e2 < 4; ++e2) {
+      const int x = q * 8 + e2 * 2;
+      float2 t = fma2(make_float2(__uint_as_float(sv[x]), __uint_as_float(sv[x + 1])), sl2, mk);
+      if (HAS_B2) t = fma2(unpack2<BF16>(pw[e2]), l2e2, t);
+      t = add2(t, nl2[e2]);
+      const float p0 = ex2(t.x), p1 = ex2(t.y);
+      const float2 dpd = add2(make_float2(__uint_as_float(pv[x]), __uint_as_float(pv[x + 1])), nd2[e2]);
+      const float2 ds = mul2(make_float2(p0, p1), dpd);
+      pp[q * 4 + e2] = pack2<BF16>(p0, p1);
+      dd[q * 4 + e2] = pack2<BF16>(ds.x, ds.y);
+    }
+    *reinterpret_cast<uint4*>(dshalf + swz_offset(r, c * 4 + q, 128)) =
+        make_uint4(dd[q * 4], dd[q * 4 + 1], dd[q * 4 + 2], dd[q * 4 + 3]);
+  }
+  tmem_st16(p_tcol, pp);
+}
+
+// HD fp32 TMEM columns of this thread's lane into v.
+template <int HD>
+__device__ __forceinline__ void km_load_cols(uint32_t col, float (&v)[HD]) {
+  if constexpr (HD == 8) {
+    uint32_t x[8];
+    tmem_ld8(col, x);
+    tmem_wait_ld(x);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[e] = __uint_as_float(x[e]);
+  } else {
+    uint32_t x[HD / 16][16];
+#pragma unroll
+    for (int q = 0; q < HD / 16; ++q) tmem_ld16(col + q * 16, x[q]);
+#pragma unroll
+    for (int q = 0; q < HD / 16; ++q) tmem_wait_ld(x[q]);
+#pragma unroll
+    for (int q = 0; q < HD / 16; ++q)
+#pragma unroll
+      for (int e = 0; e < 16; ++e) v[q * 16 + e] = __uint_as_float(x[q][e]);
+  }
+}
+
+// HD values × mul, rounded to the dtype, into row r (columns d0..d0+HD) of a
+// staging tile [128][DP] laid out like the tensor maps' boxes (2·DP-byte swizzle).
+template <int DP, int HD, bool BF16>
+__device__ __forceinline__ void km_stage_row(uint8_t* tile, const float (&v)[HD], float mul, int r, int d0) {
+#pragma unroll
+  for (int e = 0; e < HD; e += 8) {
+    uint4 pk;
+    pk.x = pack2<BF16>(v[e + 0] * mul, v[e + 1] * mul);
+    pk.y = pack2<BF16>(v[e + 2] * mul, v[e + 3] * mul);
+    pk.z = pack2<BF16>(v[e + 4] * mul, v[e + 5] * mul);
+    pk.w = pack2<BF16>(v[e + 6] * mul, v[e + 7] * mul);
+    *reinterpret_cast<uint4*>(tile + swz_offset(r, (d0 + e) >> 3, DP * 2)) = pk;
+  }
+}
+
+// Staging rounds between the compute warps and thread 0, on mbarriers (bounded
+// waits).  Round k: thread 0 waits until its earlier tile stores have read the
+// staging tiles and opens them; every warp writes; thread 0 waits for all eight
+// warps and issues the stores.
+__device__ __forceinline__ bool km_stage_begin(KmBars* bars, uint32_t rnd, const WaitGuard& g) {
+  if (threadIdx.x == 0) {
+    bulk_wait_read_all();
+    mbar_arrive(smem_u32(&bars->stg_free));
+  }
+  return mbar_wait(smem_u32(&bars->stg_free), rnd & 1, g);
+}
+__device__ __forceinline__ bool km_stage_end(KmBars* bars, uint32_t rnd, int lane, const WaitGuard& g) {
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(smem_u32(&bars->stg_full));
+  return threadIdx.x != 0 || mbar_wait(smem_u32(&bars->stg_full), rnd & 1, g);
+}
+
+// dK (× s) and dV of key tile jt of slice c: TMEM → staging → tile stores.
+template <int DP, bool BF16>
+__device__ __forceinline__ bool km_write_dkdv(const BwdArgs& a, const SlIter& c, int jt, uint32_t grp, uint8_t* base,
+                                              const KmLayout<DP>& lay, KmBars* bars, uint32_t trow, int r, int hc,
+                                              int lane, uint32_t& rnd, const WaitGuard& g) {
+  constexpr int HD = DP / 2;
+  const int nb = km_kv_bufs(DP, a.QT);
+  const uint32_t db = grp % nb;
+  if (!mbar_wait(smem_u32(&bars->dkdv_full[db]), (grp / nb) & 1, g)) return false;
+  tc_fence_after();
+  float kx[HD], vx[HD];
+  km_load_cols<HD>(trow + km_col_dk<DP>(db) + hc * HD, kx);
+  km_load_cols<HD>(trow + km_col_dv<DP>(db) + hc * HD, vx);
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(smem_u32(&bars->dkdv_free[db]));
+  if (!km_stage_begin(bars, rnd, g)) return false;
+  km_stage_row<DP, HD, BF16>(base + lay.stg[0], kx, a.scale, r, hc * HD);
+  km_stage_row<DP, HD, BF16>(base + lay.stg[1], vx, 1.0f, r, hc * HD);
+  if (!km_stage_end(bars, rnd++, lane, g)) return false;
+  if (threadIdx.x == 0) {
+    const int bn = c.b * a.N + c.n;
+    tma_store_4d(&a.tdk, smem_u32(base + lay.stg[0]), 0, c.h, jt * kTile, bn);
+    tma_store_4d(&a.tdv, smem_u32(base + lay.stg[1]), 0, c.h, jt * kTile, bn);
+    bulk_commit_group();
+  }
+  return true;
+}
+
+// dQ (× s) of slice c: every query tile, two tiles per round through the staging tiles.
+template <int DP, bool BF16>
+__device__ __forceinline__ bool km_write_dq(const BwdArgs& a, const SlIter& c, uint32_t slice, uint8_t* base,
+                                            const KmLayout<DP>& lay, KmBars* bars, uint32_t trow, int r, int hc,
+                                            int lane, uint32_t& rnd, const WaitGuard& g) {
+  constexpr int HD = DP / 2;
+  if (!mbar_wait(smem_u32(&bars->dq_full), slice & 1, g)) return false;
+  tc_fence_after();
+  const int nb = km_kv_bufs(DP, a.QT);
+  const int bn = c.b * a.N + c.n;
+  for (int it0 = 0; it0 < a.QT; it0 += 2) {
+    const bool two = it0 + 1 < a.QT;
+    float v0[HD], v1[HD];
+    km_load_cols<HD>(trow + km_col_dq<DP>(it0, nb) + hc * HD, v0);
+    if (two) km_load_cols<HD>(trow + km_col_dq<DP>(it0 + 1, nb) + hc * HD, v1);
+    if (it0 + 2 >= a.QT) {  // every dQ column read: the next slice may overwrite them
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bars->dq_free));
+    }
+    if (!km_stage_begin(bars, rnd, g)) return false;
+    km_stage_row<DP, HD, BF16>(base + lay.stg[0], v0, a.scale, r, hc * HD);
+    if (two) km_stage_row<DP, HD, BF16>(base + lay.stg[1], v1, a.scale, r, hc * HD);
+    if (!km_stage_end(bars, rnd++, lane, g)) return false;
+    if (threadIdx.x == 0) {
+      tma_store_4d(&a.tdq, smem_u32(base + lay.stg[0]), 0, c.h, it0 * kTile, bn);
+      if (two) tma_store_4d(&a.tdq, smem_u32(base + lay.stg[1]), 0, c.h, (it0 + 1) * kTile, bn);
+      bulk_commit_group();
+    }
+  }
+  return true;
+}
+
+template <int DP, bool BF16, bool HAS_B2>
+__device__ __forceinline__ void km_compute(const BwdArgs& a, uint8_t* base, const KmLayout<DP>& lay, KmBars* bars,
+                                           uint32_t tmem, const WaitGuard& g, long long i0, long long i1) {
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int quad = w & 3, hc = w >> 2;
+  const int r = quad * 32 + lane;  // key row of the tile (TMEM lane)
+  const uint32_t trow = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+  const float2 sl2 = make_float2(a.scale_log2, a.scale_log2);
+  const int QS = a.q_stages, QT = a.QT;
+  uint32_t u = 0, grp = 0, slice = 0, s = 0, ph = 0;
+  SlIter cur, prev;
+  cur.init(i0, a);
+  prev = cur;
+  float b1j = 0.0f;
+  uint32_t rnd = 0;  // staging rounds
+  bool ok = true;
+  for (long long item = i0; ok && item < i1; ++item, ++slice) {
+    if (item > i0) {
+      prev = cur;
+      cur.next(a);
+    }
+    for (int jt = 0; ok && jt < QT; ++jt, ++grp) {
+      const uint32_t kb = grp & 1;
+      for (int it = 0; it < QT; ++it, ++u) {
+        if (it == 0) {
+          if (!mbar_wait(smem_u32(&bars->kv_full[kb]), (grp >> 1) & 1, g)) { ok = false; break; }
+          b1j = reinterpret_cast<const float*>(base + lay.b1[kb])[r];
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&bars->kv_empty[kb]));
+        }
+        if (!mbar_wait(smem_u32(&bars->q_full[s]), ph, g)) { ok = false; break; }
+        if (!mbar_wait(smem_u32(&bars->st_full), u & 1, g)) { ok = false; break; }
+        if (!mbar_wait(smem_u32(&bars->buf_free[u & 1]), ((u >> 1) & 1) ^ 1, g)) { ok = false; break; }
+        tc_fence_after();
+        const float* ld = reinterpret_cast<const float*>(base + lay.ld[s]) + hc * 64;
+        const uint8_t* b2half = base + lay.b2t[s] + hc * 16384;
+        uint8_t* dshalf = base + lay.ds[u & 1] + hc * 16384;
+        const uint32_t pcol = trow + km_col_p(u & 1) + hc * 32;
+        {
+          uint32_t sv[32], pv[32];
+          tmem_ld32(trow + kKmS + hc * 64, sv);
+          tmem_ld32(trow + kKmDP + hc * 64, pv);
+          tmem_wait_ld(sv);
+          tmem_wait_ld(pv);
+          km_chunk<BF16, HAS_B2>(sv, pv, b1j, ld, ld + 128, b2half, dshalf, pcol, r, 0, sl2);
+        }
+        {
+          uint32_t sv[32], pv[32];
+          tmem_ld32(trow + kKmS + hc * 64 + 32, sv);
+          tmem_ld32(trow + kKmDP + hc * 64 + 32, pv);
+          tmem_wait_ld(sv);
+          tmem_wait_ld(pv);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&bars->st_free));
+          km_chunk<BF16, HAS_B2>(sv, pv, b1j, ld + 32, ld + 160, b2half, dshalf, pcol + 16, r, 1, sl2);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(smem_u32(&bars->pds_full));
+          mbar_arrive(smem_u32(&bars->q_empty[s]));
+        }
+        if (++s == static_cast<uint32_t>(QS)) {
+          s = 0;
+          ph ^= 1;
+        }
+        // one step late (their MMAs are done by now): dK/dV of the previous key tile and,
+        // at a slice boundary, the previous slice's dQ
+        if (it == 0 && grp > 0 &&
+            !km_write_dkdv<DP, BF16>(a, jt > 0 ? cur : prev, jt > 0 ? jt - 1 : QT - 1, grp - 1, base, lay, bars,
+                                     trow, r, hc, lane, rnd, g)) {
+          ok = false;
+          break;
+        }
+        if (it == 0 && jt == 0 && slice > 0 &&
+            !km_write_dq<DP, BF16>(a, prev, slice - 1, base, lay, bars, trow, r, hc, lane, rnd, g)) {
+          ok = false;
+          break;
+        }
+      }
+    }
+  }
+  if (ok && grp > 0) {
+    if (km_write_dkdv<DP, BF16>(a, cur, QT - 1, grp - 1, base, lay, bars, trow, r, hc, lane, rnd, g))
+      km_write_dq<DP, BF16>(a, cur, slice - 1, base, lay, bars, trow, r, hc, lane, rnd, g);
+  }
+  if (threadIdx.x == 0) bulk_wait_all();  // tile stores complete before the CTA's smem goes away
+}
+
+template <int DP, bool BF16, bool HAS_B2>
+__global__ void __launch_bounds__(kThreads, 1) evo_bwd_kmajor(const __grid_constant__ BwdArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const KmLayout<DP> lay(HAS_B2, a.q_stages);
+  KmBars* bars = reinterpret_cast<KmBars*>(base + lay.bars);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long i0 = static_cast<long long>(blockIdx.x) * a.chunk;
+  const long long i1 = i0 + a.chunk < a.items ? i0 + a.chunk : a.items;
+  if (threadIdx.x == 0) {
+    bars->abort = 0;
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_u32(&bars->kv_full[s]), 32);
+      mbar_init(smem_u32(&bars->kv_empty[s]), 1 + kComputeWarps);
+      mbar_init(smem_u32(&bars->buf_free[s]), 1);
+      mbar_init(smem_u32(&bars->dkdv_full[s]), 1);
+      mbar_init(smem_u32(&bars->dkdv_free[s]), kComputeWarps);
+    }
+    for (int s = 0; s < kKmMaxQS; ++s) {
+      mbar_init(smem_u32(&bars->q_full[s]), 32);
+      mbar_init(smem_u32(&bars->q_empty[s]), 1 + kComputeWarps);
+    }
+    mbar_init(smem_u32(&bars->st_full), 1);
+    mbar_init(smem_u32(&bars->st_free), kComputeWarps);
+    mbar_init(smem_u32(&bars->pds_full), kComputeWarps);
+    mbar_init(smem_u32(&bars->dq_full), 1);
+    mbar_init(smem_u32(&bars->dq_free), kComputeWarps);
+    mbar_init(smem_u32(&bars->stg_free), 1);
+    mbar_init(smem_u32(&bars->stg_full), kComputeWarps);
+    mbar_init(smem_u32(&bars->drain), 1);
+    fence_barrier_init();
+  }
+  if (warp == kProducerWarp && lane == 0) {
+    tma_prefetch_desc(&a.tq);
+    tma_prefetch_desc(&a.tk);
+    tma_prefetch_desc(&a.tv);
+    tma_prefetch_desc(&a.tdo);
+    if (HAS_B2) tma_prefetch_desc(&a.tb2t);
+    tma_prefetch_desc(&a.tdq);
+    tma_prefetch_desc(&a.tdk);
+    tma_prefetch_desc(&a.tdv);
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(&bars->tmem_slot), 512);
+    tmem_relinquish();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_slot;
+  const WaitGuard g{a.wait_ns, a.status, &bars->abort};
+  if (warp == kProducerWarp) {
+    km_producer<DP, BF16, HAS_B2>(a, base, lay, bars, g, lane, i0, i1);
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) km_mma<DP, BF16>(a, base, lay, bars, tmem, g, i0, i1);
+    __syncwarp();
+  } else {
+    km_compute<DP, BF16, HAS_B2>(a, base, lay, bars, tmem, g, i0, i1);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int DP>
+int km_stages(int QT, bool has_b2) {
+  if (!km_tmem_fits(DP, QT)) return 0;
+  for (int qs = kKmMaxQS; qs >= 2; --qs)
+    if (KmLayout<DP>(has_b2, qs).total + 1024 <= kMaxSmem) return qs;
+  return 0;
+}
+
+template <int DP, bool BF16, bool HAS_B2>
+cudaError_t launch_km(BwdArgs a, cudaStream_t st) {
+  const KmLayout<DP> lay(HAS_B2, a.q_stages);
+  const size_t smem = one_cta_per_sm(lay.total + 1024);
+  auto kern = evo_bwd_kmajor<DP, BF16, HAS_B2>;
+  static bool limit_set[64] = {};
+  cudaError_t e = ensure_smem_limit(kern, kMaxSmem, limit_set);
+  if (e != cudaSuccess) return e;
+  a.items = static_cast<long long>(a.B) * a.H * a.N;
+  const long long sms = num_sms();
+  a.chunk = (a.items + sms - 1) / sms;
+  const long long grid = (a.items + a.chunk - 1) / a.chunk;
+  kern<<<static_cast<unsigned>(grid), kThreads, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+template <int DP>
+cudaError_t launch_km_d(const BwdArgs& a, bool bf16, bool has_b2, cudaStream_t st) {
+  if (bf16) return has_b2 ? launch_km<DP, true, true>(a, st) : launch_km<DP, true, false>(a, st);
+  return has_b2 ? launch_km<DP, false, true>(a, st) : launch_km<DP, false, false>(a, st);
+}
+
+}  // namespace
+
+int kmajor_q_stages(int DP, int QT, bool has_b2) {
+  switch (DP) {
+    case 16: return km_stages<16>(QT, has_b2);
+    case 32: return km_stages<32>(QT, has_b2);
+    default: return 0;
+  }
+}
+
+cudaError_t launch_bwd_kmajor(const BwdArgs& a, int DP, bool bf16, bool has_b2, cudaStream_t st) {
+  switch (DP) {
+    case 16: return launch_km_d<16>(a, bf16, has_b2, st);
+    case 32: return launch_km_d<32>(a, bf16, has_b2, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace evo

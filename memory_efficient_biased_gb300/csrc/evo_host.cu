@@ -104,6 +104,16 @@ bool map_bias2(CUtensorMap* m, const void* p, const evo_shape_t& s, bool bf16, i
   return encode(m, p, bf16, 3, dims, strides, box, swz);
 }
 
+// Transposed pair-bias copy [B*H][L][pitch] (pitch = L rounded up to 8) viewed as
+// 3-D (query i, key j, B*H); box (64, 128, 1), 128B swizzle.
+bool map_b2t(CUtensorMap* m, const void* p, const evo_shape_t& s, bool bf16, int pitch) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(s.L), static_cast<cuuint64_t>(s.L),
+                        static_cast<cuuint64_t>(s.B * s.H)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(pitch) * 2, static_cast<cuuint64_t>(s.L) * pitch * 2};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kTile), 1};
+  return encode(m, p, bf16, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 struct Range {
@@ -156,16 +166,25 @@ void bwd_groups(const evo_shape_t& s, int* groups, int* group_size) {
   *group_size = static_cast<int>(gs);
 }
 
+int b2t_pitch(const evo_shape_t& s) { return static_cast<int>((s.L + 7) / 8 * 8); }
+
+// Backward workspace: delta always; the fp32 dQ accumulator only for the
+// per-key-tile kernel; the transposed pair bias only for the key-major kernel;
+// the pair-bias partial planes whenever there is a pair bias.
 struct WsLayout {
-  size_t delta, dq_acc, db2, total;
+  BwdPlan plan;
+  size_t delta, dq_acc, b2t, db2, total;
 };
 WsLayout ws_layout(const evo_shape_t& s, bool has_bias2) {
   WsLayout w{};
+  w.plan = bwd_plan(padded_dim(s.D), static_cast<int>((s.L + kTile - 1) / kTile), has_bias2);
   size_t off = 0;
   w.delta = off;
   off += round256(size_t(s.B) * s.N * s.H * s.L * 4);
   w.dq_acc = off;
-  off += round256(size_t(s.B) * s.N * s.L * s.H * s.D * 4);
+  if (w.plan.mode == kBwdMain) off += round256(size_t(s.B) * s.N * s.L * s.H * s.D * 4);
+  w.b2t = off;
+  if (w.plan.mode == kBwdKeyMajor && has_bias2) off += round256(size_t(s.B) * s.H * s.L * b2t_pitch(s) * 2);
   w.db2 = off;
   if (has_bias2) {
     int g = 0, gs = 0;
@@ -326,7 +345,8 @@ evo_status_t evo_attn_bwd(const void* q, const void* k, const void* v, const voi
   BwdArgs a;
   std::memset(&a, 0, sizeof(a));
   if (!map_qkv(&a.tq, q, shape, bf16) || !map_qkv(&a.tk, k, shape, bf16) || !map_qkv(&a.tv, v, shape, bf16) ||
-      !map_qkv(&a.tdo, dout, shape, bf16))
+      !map_qkv(&a.tdo, dout, shape, bf16) || !map_qkv(&a.tdq, dq, shape, bf16) ||
+      !map_qkv(&a.tdk, dk, shape, bf16) || !map_qkv(&a.tdv, dv, shape, bf16))
     return EVO_ERR_CUDA;
   a.bias2_mode = kBias2None;
   if (bias2) {
@@ -352,6 +372,11 @@ evo_status_t evo_attn_bwd(const void* q, const void* k, const void* v, const voi
   a.delta = reinterpret_cast<float*>(ws + w.delta);
   a.dq_acc = reinterpret_cast<float*>(ws + w.dq_acc);
   a.db2_part = bias2 ? reinterpret_cast<float*>(ws + w.db2) : nullptr;
+  if (bias2 && w.plan.mode == kBwdKeyMajor) {
+    a.b2t = reinterpret_cast<uint16_t*>(ws + w.b2t);
+    a.b2t_pitch = b2t_pitch(shape);
+    if (!map_b2t(&a.tb2t, a.b2t, shape, bf16, a.b2t_pitch)) return EVO_ERR_CUDA;
+  }
   a.B = static_cast<int>(shape.B);
   a.N = static_cast<int>(shape.N);
   a.L = static_cast<int>(shape.L);

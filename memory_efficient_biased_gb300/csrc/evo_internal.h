@@ -35,6 +35,8 @@ struct FwdArgs {
 struct BwdArgs {
   CUtensorMap tq, tk, tv, tdo;  // 4-D views like the forward, box (DP, 1, 128, 1)
   CUtensorMap tb2;              // 3-D [B*H][L][L] view, box (64, 128, 1), 128B swizzle
+  CUtensorMap tb2t;             // key-major kernel: the transposed copy b2t, same box and swizzle
+  CUtensorMap tdq, tdk, tdv;    // key-major kernel: output views for tile stores, like tq
   const uint16_t* q;
   const uint16_t* out;
   const uint16_t* dout;
@@ -48,6 +50,8 @@ struct BwdArgs {
   float* delta;             // workspace [B,N,H,L]
   float* dq_acc;            // workspace [B,N,L,H,D]
   float* db2_part;          // workspace [G][B,H,L,L]
+  uint16_t* b2t;            // workspace [B,H,L,b2t_pitch]: b2t[bh][j][i] = bias2[bh][i][j] (key-major kernel)
+  int b2t_pitch;            // L rounded up to a multiple of 8 (16-byte rows for TMA)
   int B, N, L, H, D;
   int QT;
   int groups;               // G: n-groups of the pair-bias gradient
@@ -96,6 +100,18 @@ cudaError_t ensure_smem_limit(Kernel kern, size_t bytes, bool (&done)[64]) {
   if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
   return e;
 }
+
+// Which backward kernel runs for a shape (shared by workspace sizing and launch):
+// key-major slice kernel, query-major slice kernel (both keep dQ in TMEM), or the
+// per-key-tile kernel with an fp32 dQ accumulator in the workspace.
+enum BwdMode : int { kBwdKeyMajor = 0, kBwdSlice = 1, kBwdMain = 2 };
+struct BwdPlan {
+  int mode;
+  int q_stages;
+};
+BwdPlan bwd_plan(int DP, int QT, bool has_b2);
+int kmajor_q_stages(int DP, int QT, bool has_b2);
+cudaError_t launch_bwd_kmajor(const BwdArgs& a, int DP, bool bf16, bool has_b2, cudaStream_t st);
 
 int num_sms();
 cudaError_t launch_fwd(const FwdArgs& a, int DP, bool bf16, cudaStream_t st);

@@ -103,11 +103,14 @@ def test_workspace_bytes(lib):
     no_b2 = lib.evo_attn_bwd_workspace_bytes(s, 1, 0)
     with_b2 = lib.evo_attn_bwd_workspace_bytes(s, 1, 1)
     delta = 1 * 256 * 4 * 256 * 4
-    dq_acc = 1 * 256 * 256 * 4 * 32 * 4
-    assert no_b2 == delta + dq_acc
-    # partials: a whole number of fp32 [B,H,L,L] planes, at least one
-    extra = with_b2 - no_b2
+    # key-major backward (D <= 32, L <= 256): dQ stays in TMEM, no fp32 accumulator
+    assert no_b2 == delta
+    # with a pair bias: its transposed bf16 copy plus a whole number of fp32 [B,H,L,L] partial planes
+    extra = with_b2 - no_b2 - 1 * 4 * 256 * 256 * 2
     plane = 1 * 4 * 256 * 256 * 4
     assert extra % plane == 0 and 1 <= extra // plane <= 256
+    # per-key-tile backward (D = 64, L = 384): delta plus the fp32 dQ accumulator
+    big = shape(B=1, N=4, L=384, H=2, D=64)
+    assert lib.evo_attn_bwd_workspace_bytes(big, 1, 0) == 4 * 2 * 384 * 4 + 4 * 384 * 2 * 64 * 4
     assert lib.evo_attn_bwd_workspace_bytes(shape(D=12), 1, 0) == 0
     assert lib.evo_attn_bwd_workspace_bytes(s, 7, 0) == 0
