@@ -48,7 +48,6 @@ struct KmBars {
   uint64_t q_full[kKmMaxQS], q_empty[kKmMaxQS];
   uint64_t st_full, st_free, pds_full, buf_free[2];
   uint64_t dkdv_full[2], dkdv_free[2], dq_full, dq_free;
-  uint64_t stg_free, stg_full;  // staging tiles: free to write (thread 0) / written (compute warps)
   uint64_t drain;
   uint32_t tmem_slot;
   int abort;
@@ -65,7 +64,7 @@ struct KmLayout {
       ds[s] = off;
       off += 32768u;
     }
-    for (int s = 0; s < 2; ++s) {  // staging of finished dK / dV / dQ tiles for the TMA stores
+    for (int s = 0; s < 2; ++s) {  // staging of finished dK / dV / dQ: per warp two [32][DP/2] blocks
       stg[s] = off;
       off += kTB;
     }
@@ -130,6 +129,35 @@ __device__ __forceinline__ void km_producer(const BwdArgs& a, uint8_t* base, con
       }
     }
   };
+  // L2 prefetch of the Q / dO / pair-bias tiles kPfAhead steps ahead of the load being issued
+  constexpr int kPfAhead = 2;
+  SlIter fc = c;
+  int fjt = 0, fit = 0;
+  auto advance_l2 = [&]() {
+    if (++fit == QT) {
+      fit = 0;
+      if (++fjt == QT) {
+        fjt = 0;
+        fc.next(a);
+      }
+    }
+  };
+  auto prefetch_l2 = [&]() {
+    if (lane == 0 && fc.b < a.B) {
+      const int fbn = fc.b * a.N + fc.n;
+      tma_prefetch_4d(&a.tq, 0, fc.h, fit * kTile, fbn);
+      tma_prefetch_4d(&a.tdo, 0, fc.h, fit * kTile, fbn);
+      if (HAS_B2) {
+        const int fbh = fc.b * a.H + fc.h;
+        tma_prefetch_3d(&a.tb2t, fit * kTile, fjt * kTile, fbh);
+        tma_prefetch_3d(&a.tb2t, fit * kTile + 64, fjt * kTile, fbh);
+      }
+    }
+  };
+  for (int k = 0; k < kPfAhead; ++k) {
+    advance_l2();
+    prefetch_l2();
+  }
   b1_prefetch(b1r, a.bias1 ? a.bias1 + (static_cast<size_t>(c.b) * a.N + c.n) * a.L : nullptr, a.L, 0, lane);
   prefetch_ld();
   bool ok = true;
@@ -150,6 +178,10 @@ __device__ __forceinline__ void km_producer(const BwdArgs& a, uint8_t* base, con
         const int njt = jt + 1 < QT ? jt + 1 : 0;
         SlIter nc = c;
         if (njt == 0) nc.next(a);
+        if (lane == 0 && nc.b < a.B) {  // next key tile's K and V into L2
+          tma_prefetch_4d(&a.tk, 0, nc.h, njt * kTile, nc.b * a.N + nc.n);
+          tma_prefetch_4d(&a.tv, 0, nc.h, njt * kTile, nc.b * a.N + nc.n);
+        }
         if (nc.b < a.B)
           b1_prefetch(b1r, a.bias1 ? a.bias1 + (static_cast<size_t>(nc.b) * a.N + nc.n) * a.L : nullptr, a.L,
                       njt * kTile, lane);
@@ -170,6 +202,8 @@ __device__ __forceinline__ void km_producer(const BwdArgs& a, uint8_t* base, con
         mbar_arrive(full);
         advance_pf();
         prefetch_ld();
+        advance_l2();
+        prefetch_l2();
         if (++s == static_cast<uint32_t>(QS)) {
           s = 0;
           ph ^= 1;
@@ -205,16 +239,15 @@ __device__ __forceinline__ bool km_issue_sdp(const KmStep& st, uint8_t* base, co
   if (!mbar_wait(smem_u32(&bars->q_full[st.qs]), st.qph, g)) return false;
   if (!mbar_wait(smem_u32(&bars->st_free), (st.u & 1) ^ 1, g)) return false;
   tc_fence_after();
-  const uint32_t q_addr = smem_u32(base + lay.q[st.qs]), do_addr = smem_u32(base + lay.d_o[st.qs]);
-  const uint32_t k_addr = smem_u32(base + lay.k[kb]), v_addr = smem_u32(base + lay.v[kb]);
+  // descriptors: start-address field (bits 0-13, 16-byte units) advanced by constants
+  const uint64_t kd = smem_desc(smem_u32(base + lay.k[kb]), 16, 8 * RB, SWZ);
+  const uint64_t vd = smem_desc(smem_u32(base + lay.v[kb]), 16, 8 * RB, SWZ);
+  const uint64_t qd = smem_desc(smem_u32(base + lay.q[st.qs]), 16, 8 * RB, SWZ);
+  const uint64_t dod = smem_desc(smem_u32(base + lay.d_o[st.qs]), 16, 8 * RB, SWZ);
 #pragma unroll
-  for (int k = 0; k < DP / 16; ++k)
-    umma_ss(tmem + kKmS, smem_desc(k_addr + k * 32, 16, 8 * RB, SWZ), smem_desc(q_addr + k * 32, 16, 8 * RB, SWZ),
-            id_s, k > 0);
+  for (int k = 0; k < DP / 16; ++k) umma_ss(tmem + kKmS, kd + k * 2, qd + k * 2, id_s, k > 0);
 #pragma unroll
-  for (int k = 0; k < DP / 16; ++k)
-    umma_ss(tmem + kKmDP, smem_desc(v_addr + k * 32, 16, 8 * RB, SWZ),
-            smem_desc(do_addr + k * 32, 16, 8 * RB, SWZ), id_s, k > 0);
+  for (int k = 0; k < DP / 16; ++k) umma_ss(tmem + kKmDP, vd + k * 2, dod + k * 2, id_s, k > 0);
   umma_commit(smem_u32(&bars->st_full));
   return true;
 }
@@ -236,30 +269,30 @@ __device__ __forceinline__ bool km_issue_grads(const KmStep& st, int QT, uint8_t
   if (!mbar_wait(smem_u32(&bars->pds_full), st.u & 1, g)) return false;
   if (st.it == 0 && !mbar_wait(smem_u32(&bars->dkdv_free[db]), dph ^ 1, g)) return false;
   tc_fence_after();
-  const uint32_t q_addr = smem_u32(base + lay.q[st.qs]), do_addr = smem_u32(base + lay.d_o[st.qs]);
-  const uint32_t k_addr = smem_u32(base + lay.k[kb]), ds_addr = smem_u32(base + lay.ds[b]);
+  // descriptors: start-address field (bits 0-13, 16-byte units) advanced by constants
+  const uint64_t dod = smem_desc(smem_u32(base + lay.d_o[st.qs]), kTile * RB, 8 * RB, SWZ);
+  const uint64_t qd = smem_desc(smem_u32(base + lay.q[st.qs]), kTile * RB, 8 * RB, SWZ);
+  const uint64_t kd = smem_desc(smem_u32(base + lay.k[kb]), kTile * RB, 8 * RB, SWZ);
+  const uint32_t ds_addr = smem_u32(base + lay.ds[b]);
+  const uint64_t dskd = smem_desc(ds_addr, 16, 1024, kSwizzle128B);         // dSᵀ as K-major A
+  const uint64_t dsmd = smem_desc(ds_addr, 16384, 1024, kSwizzle128B);      // dS as MN-major A
   const uint32_t pcol = tmem + km_col_p(b);
+  const uint32_t acc_v = (st.it > 0) ? 1u : 0u;
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {  // dV += Pᵀ dO   (K = 128 queries)
-    const uint64_t bd = smem_desc(do_addr + k * 16 * RB, kTile * RB, 8 * RB, SWZ);
-    umma_ts(tmem + km_col_dv<DP>(db), pcol + k * 8, bd, id_v, (st.it > 0 || k > 0) ? 1u : 0u);
-  }
+  for (int k = 0; k < 8; ++k)  // dV += Pᵀ dO   (K = 128 queries)
+    umma_ts(tmem + km_col_dv<DP>(db), pcol + k * 8, dod + k * RB, id_v, (acc_v | k) ? 1u : 0u);
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {  // dK += dSᵀ Q
-    const uint64_t ad = smem_desc(ds_addr + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024, kSwizzle128B);
-    const uint64_t bd = smem_desc(q_addr + k * 16 * RB, kTile * RB, 8 * RB, SWZ);
-    umma_ss(tmem + km_col_dk<DP>(db), ad, bd, id_k, (st.it > 0 || k > 0) ? 1u : 0u);
-  }
+  for (int k = 0; k < 8; ++k)  // dK += dSᵀ Q
+    umma_ss(tmem + km_col_dk<DP>(db), dskd + (k >> 2) * 1024 + (k & 3) * 2, qd + k * RB, id_k,
+            (acc_v | k) ? 1u : 0u);
   umma_commit(smem_u32(&bars->q_empty[st.qs]));
   if (st.it == QT - 1) umma_commit(smem_u32(&bars->dkdv_full[db]));
   if (st.it == 0 && st.jt == 0 && !mbar_wait(smem_u32(&bars->dq_free), (st.slice & 1) ^ 1, g)) return false;
   tc_fence_after();
+  const uint32_t acc_q = (st.jt > 0) ? 1u : 0u;
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {  // dQ_it += dS K_jt   (K = 128 keys)
-    const uint64_t ad = smem_desc(ds_addr + k * 16 * 128, 16384, 1024, kSwizzle128B);
-    const uint64_t bd = smem_desc(k_addr + k * 16 * RB, kTile * RB, 8 * RB, SWZ);
-    umma_ss(tmem + km_col_dq<DP>(st.it, nb), ad, bd, id_q, (st.jt > 0 || k > 0) ? 1u : 0u);
-  }
+  for (int k = 0; k < 8; ++k)  // dQ_it += dS K_jt   (K = 128 keys)
+    umma_ss(tmem + km_col_dq<DP>(st.it, nb), dsmd + k * 128, kd + k * RB, id_q, (acc_q | k) ? 1u : 0u);
   umma_commit(smem_u32(&bars->buf_free[b]));
   if (st.it == QT - 1) {
     umma_commit(smem_u32(&bars->kv_empty[kb]));
@@ -364,10 +397,18 @@ __device__ __forceinline__ void km_load_cols(uint32_t col, float (&v)[HD]) {
   }
 }
 
-// HD values × mul, rounded to the dtype, into row r (columns d0..d0+HD) of a
-// staging tile [128][DP] laid out like the tensor maps' boxes (2·DP-byte swizzle).
+// Each compute warp writes its own share of a finished tile — its 32 rows
+// (TMEM lanes) × DP/2 columns — through a private staging block and one TMA
+// store issued by its lane 0, so write-outs need no synchronisation between
+// warps.  Block t of warp w: [32][DP/2] fp16/bf16, 32-byte swizzle when the
+// rows are 32 bytes (the layout of the output maps' boxes).
+template <int DP>
+__device__ __forceinline__ uint8_t* km_stage_block(uint8_t* base, const KmLayout<DP>& lay, int w, int t) {
+  return base + lay.stg[0] + (w * 2 + t) * (32 * DP);
+}
+
 template <int DP, int HD, bool BF16>
-__device__ __forceinline__ void km_stage_row(uint8_t* tile, const float (&v)[HD], float mul, int r, int d0) {
+__device__ __forceinline__ void km_stage_row(uint8_t* blk, const float (&v)[HD], float mul, int lane) {
 #pragma unroll
   for (int e = 0; e < HD; e += 8) {
     uint4 pk;
@@ -375,33 +416,26 @@ __device__ __forceinline__ void km_stage_row(uint8_t* tile, const float (&v)[HD]
     pk.y = pack2<BF16>(v[e + 2] * mul, v[e + 3] * mul);
     pk.z = pack2<BF16>(v[e + 4] * mul, v[e + 5] * mul);
     pk.w = pack2<BF16>(v[e + 6] * mul, v[e + 7] * mul);
-    *reinterpret_cast<uint4*>(tile + swz_offset(r, (d0 + e) >> 3, DP * 2)) = pk;
+    const uint32_t off = HD == 16 ? swz_offset(lane, e >> 3, 32) : lane * 16u;
+    *reinterpret_cast<uint4*>(blk + off) = pk;
   }
 }
 
-// Staging rounds between the compute warps and thread 0, on mbarriers (bounded
-// waits).  Round k: thread 0 waits until its earlier tile stores have read the
-// staging tiles and opens them; every warp writes; thread 0 waits for all eight
-// warps and issues the stores.
-__device__ __forceinline__ bool km_stage_begin(KmBars* bars, uint32_t rnd, const WaitGuard& g) {
-  if (threadIdx.x == 0) {
-    bulk_wait_read_all();
-    mbar_arrive(smem_u32(&bars->stg_free));
-  }
-  return mbar_wait(smem_u32(&bars->stg_free), rnd & 1, g);
+// Before writing the warp's staging blocks: its previous stores have read them.
+__device__ __forceinline__ void km_stage_open(int lane) {
+  if (lane == 0) bulk_wait_read_all();
+  __syncwarp();
 }
-__device__ __forceinline__ bool km_stage_end(KmBars* bars, uint32_t rnd, int lane, const WaitGuard& g) {
+__device__ __forceinline__ void km_stage_close() {
   fence_proxy_async_smem();
   __syncwarp();
-  if (lane == 0) mbar_arrive(smem_u32(&bars->stg_full));
-  return threadIdx.x != 0 || mbar_wait(smem_u32(&bars->stg_full), rnd & 1, g);
 }
 
-// dK (× s) and dV of key tile jt of slice c: TMEM → staging → tile stores.
+// dK (× s) and dV of key tile jt of slice c.
 template <int DP, bool BF16>
 __device__ __forceinline__ bool km_write_dkdv(const BwdArgs& a, const SlIter& c, int jt, uint32_t grp, uint8_t* base,
-                                              const KmLayout<DP>& lay, KmBars* bars, uint32_t trow, int r, int hc,
-                                              int lane, uint32_t& rnd, const WaitGuard& g) {
+                                              const KmLayout<DP>& lay, KmBars* bars, uint32_t trow, int w, int hc,
+                                              int lane, const WaitGuard& g) {
   constexpr int HD = DP / 2;
   const int nb = km_kv_bufs(DP, a.QT);
   const uint32_t db = grp % nb;
@@ -413,24 +447,26 @@ __device__ __forceinline__ bool km_write_dkdv(const BwdArgs& a, const SlIter& c,
   tc_fence_before();
   __syncwarp();
   if (lane == 0) mbar_arrive(smem_u32(&bars->dkdv_free[db]));
-  if (!km_stage_begin(bars, rnd, g)) return false;
-  km_stage_row<DP, HD, BF16>(base + lay.stg[0], kx, a.scale, r, hc * HD);
-  km_stage_row<DP, HD, BF16>(base + lay.stg[1], vx, 1.0f, r, hc * HD);
-  if (!km_stage_end(bars, rnd++, lane, g)) return false;
-  if (threadIdx.x == 0) {
-    const int bn = c.b * a.N + c.n;
-    tma_store_4d(&a.tdk, smem_u32(base + lay.stg[0]), 0, c.h, jt * kTile, bn);
-    tma_store_4d(&a.tdv, smem_u32(base + lay.stg[1]), 0, c.h, jt * kTile, bn);
+  uint8_t* bk = km_stage_block<DP>(base, lay, w, 0);
+  uint8_t* bv = km_stage_block<DP>(base, lay, w, 1);
+  km_stage_open(lane);
+  km_stage_row<DP, HD, BF16>(bk, kx, a.scale, lane);
+  km_stage_row<DP, HD, BF16>(bv, vx, 1.0f, lane);
+  km_stage_close();
+  if (lane == 0) {
+    const int bn = c.b * a.N + c.n, row = jt * kTile + (w & 3) * 32;
+    tma_store_4d(&a.tdk, smem_u32(bk), hc * HD, c.h, row, bn);
+    tma_store_4d(&a.tdv, smem_u32(bv), hc * HD, c.h, row, bn);
     bulk_commit_group();
   }
   return true;
 }
 
-// dQ (× s) of slice c: every query tile, two tiles per round through the staging tiles.
+// dQ (× s) of slice c: every query tile, two per round through the staging blocks.
 template <int DP, bool BF16>
 __device__ __forceinline__ bool km_write_dq(const BwdArgs& a, const SlIter& c, uint32_t slice, uint8_t* base,
-                                            const KmLayout<DP>& lay, KmBars* bars, uint32_t trow, int r, int hc,
-                                            int lane, uint32_t& rnd, const WaitGuard& g) {
+                                            const KmLayout<DP>& lay, KmBars* bars, uint32_t trow, int w, int hc,
+                                            int lane, const WaitGuard& g) {
   constexpr int HD = DP / 2;
   if (!mbar_wait(smem_u32(&bars->dq_full), slice & 1, g)) return false;
   tc_fence_after();
@@ -446,13 +482,16 @@ __device__ __forceinline__ bool km_write_dq(const BwdArgs& a, const SlIter& c, u
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&bars->dq_free));
     }
-    if (!km_stage_begin(bars, rnd, g)) return false;
-    km_stage_row<DP, HD, BF16>(base + lay.stg[0], v0, a.scale, r, hc * HD);
-    if (two) km_stage_row<DP, HD, BF16>(base + lay.stg[1], v1, a.scale, r, hc * HD);
-    if (!km_stage_end(bars, rnd++, lane, g)) return false;
-    if (threadIdx.x == 0) {
-      tma_store_4d(&a.tdq, smem_u32(base + lay.stg[0]), 0, c.h, it0 * kTile, bn);
-      if (two) tma_store_4d(&a.tdq, smem_u32(base + lay.stg[1]), 0, c.h, (it0 + 1) * kTile, bn);
+    uint8_t* b0 = km_stage_block<DP>(base, lay, w, 0);
+    uint8_t* b1 = km_stage_block<DP>(base, lay, w, 1);
+    km_stage_open(lane);
+    km_stage_row<DP, HD, BF16>(b0, v0, a.scale, lane);
+    if (two) km_stage_row<DP, HD, BF16>(b1, v1, a.scale, lane);
+    km_stage_close();
+    if (lane == 0) {
+      const int row = (w & 3) * 32;
+      tma_store_4d(&a.tdq, smem_u32(b0), hc * HD, c.h, it0 * kTile + row, bn);
+      if (two) tma_store_4d(&a.tdq, smem_u32(b1), hc * HD, c.h, (it0 + 1) * kTile + row, bn);
       bulk_commit_group();
     }
   }
@@ -473,7 +512,6 @@ __device__ __forceinline__ void km_compute(const BwdArgs& a, uint8_t* base, cons
   cur.init(i0, a);
   prev = cur;
   float b1j = 0.0f;
-  uint32_t rnd = 0;  // staging rounds
   bool ok = true;
   for (long long item = i0; ok && item < i1; ++item, ++slice) {
     if (item > i0) {
@@ -532,12 +570,12 @@ __device__ __forceinline__ void km_compute(const BwdArgs& a, uint8_t* base, cons
         // at a slice boundary, the previous slice's dQ
         if (it == 0 && grp > 0 &&
             !km_write_dkdv<DP, BF16>(a, jt > 0 ? cur : prev, jt > 0 ? jt - 1 : QT - 1, grp - 1, base, lay, bars,
-                                     trow, r, hc, lane, rnd, g)) {
+                                     trow, w, hc, lane, g)) {
           ok = false;
           break;
         }
         if (it == 0 && jt == 0 && slice > 0 &&
-            !km_write_dq<DP, BF16>(a, prev, slice - 1, base, lay, bars, trow, r, hc, lane, rnd, g)) {
+            !km_write_dq<DP, BF16>(a, prev, slice - 1, base, lay, bars, trow, w, hc, lane, g)) {
           ok = false;
           break;
         }
@@ -545,10 +583,10 @@ __device__ __forceinline__ void km_compute(const BwdArgs& a, uint8_t* base, cons
     }
   }
   if (ok && grp > 0) {
-    if (km_write_dkdv<DP, BF16>(a, cur, QT - 1, grp - 1, base, lay, bars, trow, r, hc, lane, rnd, g))
-      km_write_dq<DP, BF16>(a, cur, slice - 1, base, lay, bars, trow, r, hc, lane, rnd, g);
+    if (km_write_dkdv<DP, BF16>(a, cur, QT - 1, grp - 1, base, lay, bars, trow, w, hc, lane, g))
+      km_write_dq<DP, BF16>(a, cur, slice - 1, base, lay, bars, trow, w, hc, lane, g);
   }
-  if (threadIdx.x == 0) bulk_wait_all();  // tile stores complete before the CTA's smem goes away
+  if (lane == 0) bulk_wait_all();  // this warp's tile stores complete before the CTA's smem goes away
 }
 
 template <int DP, bool BF16, bool HAS_B2>
@@ -578,8 +616,6 @@ __global__ void __launch_bounds__(kThreads, 1) evo_bwd_kmajor(const __grid_const
     mbar_init(smem_u32(&bars->pds_full), kComputeWarps);
     mbar_init(smem_u32(&bars->dq_full), 1);
     mbar_init(smem_u32(&bars->dq_free), kComputeWarps);
-    mbar_init(smem_u32(&bars->stg_free), 1);
-    mbar_init(smem_u32(&bars->stg_full), kComputeWarps);
     mbar_init(smem_u32(&bars->drain), 1);
     fence_barrier_init();
   }

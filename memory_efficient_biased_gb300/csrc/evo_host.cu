@@ -95,6 +95,19 @@ bool map_qkv(CUtensorMap* m, const void* p, const evo_shape_t& s, bool bf16) {
   return encode(m, p, bf16, 4, dims, strides, box, swz);
 }
 
+// The same 4-D view with a box of one warp's share of an output tile: (DP/2, 1, 32, 1);
+// 32-byte swizzle when the box rows are 32 bytes, none when they are 16.
+bool map_rows_half(CUtensorMap* m, const void* p, const evo_shape_t& s, bool bf16) {
+  const int DP = padded_dim(s.D);
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(s.D), static_cast<cuuint64_t>(s.H), static_cast<cuuint64_t>(s.L),
+                        static_cast<cuuint64_t>(s.B * s.N)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(s.D * 2), static_cast<cuuint64_t>(s.H * s.D * 2),
+                           static_cast<cuuint64_t>(s.L * s.H * s.D * 2)};
+  cuuint32_t box[4] = {static_cast<cuuint32_t>(DP / 2), 1, 32, 1};
+  return encode(m, p, bf16, 4, dims, strides, box,
+                DP == 32 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
 // [B,1,H,L,L] viewed as 3-D (key j, query i, B*H).
 bool map_bias2(CUtensorMap* m, const void* p, const evo_shape_t& s, bool bf16, int box_j, CUtensorMapSwizzle swz) {
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(s.L), static_cast<cuuint64_t>(s.L),
@@ -345,8 +358,10 @@ evo_status_t evo_attn_bwd(const void* q, const void* k, const void* v, const voi
   BwdArgs a;
   std::memset(&a, 0, sizeof(a));
   if (!map_qkv(&a.tq, q, shape, bf16) || !map_qkv(&a.tk, k, shape, bf16) || !map_qkv(&a.tv, v, shape, bf16) ||
-      !map_qkv(&a.tdo, dout, shape, bf16) || !map_qkv(&a.tdq, dq, shape, bf16) ||
-      !map_qkv(&a.tdk, dk, shape, bf16) || !map_qkv(&a.tdv, dv, shape, bf16))
+      !map_qkv(&a.tdo, dout, shape, bf16))
+    return EVO_ERR_CUDA;
+  if (padded_dim(shape.D) <= 32 && (!map_rows_half(&a.tdq, dq, shape, bf16) ||
+                                    !map_rows_half(&a.tdk, dk, shape, bf16) || !map_rows_half(&a.tdv, dv, shape, bf16)))
     return EVO_ERR_CUDA;
   a.bias2_mode = kBias2None;
   if (bias2) {

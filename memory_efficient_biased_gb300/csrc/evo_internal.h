@@ -36,7 +36,7 @@ struct BwdArgs {
   CUtensorMap tq, tk, tv, tdo;  // 4-D views like the forward, box (DP, 1, 128, 1)
   CUtensorMap tb2;              // 3-D [B*H][L][L] view, box (64, 128, 1), 128B swizzle
   CUtensorMap tb2t;             // key-major kernel: the transposed copy b2t, same box and swizzle
-  CUtensorMap tdq, tdk, tdv;    // key-major kernel: output views for tile stores, like tq
+  CUtensorMap tdq, tdk, tdv;    // key-major kernel: output views, box (DP/2, 1, 32, 1) = one warp's share
   const uint16_t* q;
   const uint16_t* out;
   const uint16_t* dout;
