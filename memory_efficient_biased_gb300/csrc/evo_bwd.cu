@@ -115,7 +115,15 @@ __global__ void __launch_bounds__(256) evo_bwd_db2_sum(const BwdArgs a) {
   const long long plane = static_cast<long long>(a.B) * a.H * a.L * a.L;
   for (long long e = blockIdx.x * 256ll + threadIdx.x; e < plane; e += gridDim.x * 256ll) {
     float s = 0.0f;
-    for (int g = 0; g < a.groups; ++g) s += a.db2_part[g * plane + e];  // fixed group order
+    int g = 0;
+    for (; g + 8 <= a.groups; g += 8) {  // eight loads in flight, added in group order
+      float v[8];
+#pragma unroll
+      for (int t = 0; t < 8; ++t) v[t] = __ldg(a.db2_part + (g + t) * plane + e);
+#pragma unroll
+      for (int t = 0; t < 8; ++t) s += v[t];
+    }
+    for (; g < a.groups; ++g) s += __ldg(a.db2_part + g * plane + e);
     const uint32_t p = pack2<BF16>(s, 0.0f);
     a.dbias2[e] = static_cast<uint16_t>(p & 0xFFFFu);
   }
@@ -1290,8 +1298,9 @@ template <int DP>
 struct PartLayout {
   static constexpr uint32_t kTB = kTile * DP * 2;
   uint32_t q[kMaxPartStages], d_o[kMaxPartStages], k[kMaxPartStages], v[kMaxPartStages], b1[kMaxPartStages],
-      ld[kMaxPartStages], b2, bars, total;
-  __host__ __device__ explicit PartLayout(int ns) {
+      ld[kMaxPartStages], b2, stg, bars, total;
+  // stage: also 64 KB of staging for the tile stores of the partial sums (8 KB per compute warp)
+  __host__ __device__ PartLayout(int ns, bool stage) {
     uint32_t off = 0;
     for (int s = 0; s < kMaxPartStages; ++s) {
       const uint32_t o = off + (s < ns ? s : 0) * 4 * kTB;
@@ -1303,6 +1312,8 @@ struct PartLayout {
     off += ns * 4 * kTB;
     b2 = off;
     off += 32768u;
+    stg = off;
+    if (stage) off += 65536u;
     for (int s = 0; s < kMaxPartStages; ++s) {
       b1[s] = off + (s < ns ? s : 0) * 1536u;
       ld[s] = b1[s] + 512u;
@@ -1341,7 +1352,7 @@ __global__ void __launch_bounds__(kThreads, 1) evo_bwd_db2_part(const __grid_con
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int NS = a.part_stages;
-  const PartLayout<DP> lay(NS);
+  const PartLayout<DP> lay(NS, a.db2p_tma != 0);
   PartBars* bars = reinterpret_cast<PartBars*>(base + lay.bars);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const PartItem c = part_item(a);
@@ -1512,7 +1523,26 @@ __global__ void __launch_bounds__(kThreads, 1) evo_bwd_db2_part(const __grid_con
       }
     }
     const int i = c.it * kTile + r;
-    if (ok && i < a.L) {
+    if (ok && a.db2p_tma) {
+      // this warp's 32 rows × 64 keys: two [32][32] fp32 blocks (128B swizzle) → two tile stores
+      uint8_t* blk = base + lay.stg + warp * 8192;
+#pragma unroll
+      for (int hb = 0; hb < 2; ++hb)
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch)
+          *reinterpret_cast<float4*>(blk + hb * 4096 + swz_offset(lane, ch, 128)) =
+              make_float4(acc[hb * 32 + ch * 4], acc[hb * 32 + ch * 4 + 1], acc[hb * 32 + ch * 4 + 2],
+                          acc[hb * 32 + ch * 4 + 3]);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        const int plane = c.grp * a.B * a.H + bh, j0 = c.jt * kTile + hc * 64, i0 = c.it * kTile + quad * 32;
+        tma_store_3d(&a.tdb2p, smem_u32(blk), j0, i0, plane);
+        tma_store_3d(&a.tdb2p, smem_u32(blk + 4096), j0 + 32, i0, plane);
+        bulk_commit_group();
+        bulk_wait_all();
+      }
+    } else if (ok && i < a.L) {
       const long long plane = static_cast<long long>(a.B) * a.H * a.L * a.L;
       float* dst = a.db2_part + c.grp * plane + (static_cast<long long>(bh) * a.L + i) * a.L;
       const int j0 = c.jt * kTile + hc * 64;
@@ -1631,8 +1661,12 @@ cudaError_t launch_bwd_d(BwdArgs a, cudaStream_t st, const ProfileEvents* prof) 
   }
 
   if (has_b2) {
-    a.part_stages = PartLayout<DP>(3).total + 1024 <= kMaxSmem ? 3 : 2;
-    const PartLayout<DP> lay(a.part_stages);
+    // deepest ring that fits; staging for tile stores of the partials when it fits too
+    auto pfits = [&](int ns, bool stg) { return PartLayout<DP>(ns, stg).total + 1024 <= kMaxSmem; };
+    if (a.db2p_tma && !pfits(2, true)) a.db2p_tma = 0;
+    const bool stg = a.db2p_tma != 0;
+    a.part_stages = pfits(3, stg) ? 3 : 2;
+    const PartLayout<DP> lay(a.part_stages, stg);
     const size_t smem = one_cta_per_sm(lay.total + 1024);
     auto kern = evo_bwd_db2_part<DP, BF16>;
     static bool limit_set[64] = {};

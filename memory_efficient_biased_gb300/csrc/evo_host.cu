@@ -67,16 +67,30 @@ PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
   return fn;
 }
 
-bool encode(CUtensorMap* m, const void* base, bool bf16, int rank, const cuuint64_t* dims,
-            const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle swz) {
+bool encode_t(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int rank, const cuuint64_t* dims,
+              const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle swz) {
   auto fn = tmap_encoder();
   if (!fn) return false;
   cuuint32_t es[5] = {1, 1, 1, 1, 1};
-  CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+  CUresult r = fn(m, dt,
                   static_cast<cuuint32_t>(rank), const_cast<void*>(base), dims, strides, box, es,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+bool encode(CUtensorMap* m, const void* base, bool bf16, int rank, const cuuint64_t* dims,
+            const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle swz) {
+  return encode_t(m, base, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, rank, dims,
+                  strides, box, swz);
+}
+
+// fp32 pair-bias partial planes [G*B*H][L][L] as 3-D (j, i, plane); box (32, 32, 1), 128B swizzle.
+bool map_db2_part(CUtensorMap* m, const void* p, const evo_shape_t& s, int groups) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(s.L), static_cast<cuuint64_t>(s.L),
+                        static_cast<cuuint64_t>(groups) * s.B * s.H};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(s.L) * 4, static_cast<cuuint64_t>(s.L) * s.L * 4};
+  cuuint32_t box[3] = {32, 32, 1};
+  return encode_t(m, p, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 int padded_dim(int64_t D) { return D <= 16 ? 16 : (D <= 32 ? 32 : 64); }
@@ -399,6 +413,10 @@ evo_status_t evo_attn_bwd(const void* q, const void* k, const void* v, const voi
   a.D = static_cast<int>(shape.D);
   a.QT = static_cast<int>((shape.L + kTile - 1) / kTile);
   bwd_groups(shape, &a.groups, &a.group_size);
+  if (bias2 && shape.L % 4 == 0) {
+    if (!map_db2_part(&a.tdb2p, a.db2_part, shape, a.groups)) return EVO_ERR_CUDA;
+    a.db2p_tma = 1;
+  }
   a.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(shape.D)));
   a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(shape.D)));
   a.wait_ns = g_wait_limit_ns.load();

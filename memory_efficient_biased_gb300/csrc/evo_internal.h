@@ -37,6 +37,7 @@ struct BwdArgs {
   CUtensorMap tb2;              // 3-D [B*H][L][L] view, box (64, 128, 1), 128B swizzle
   CUtensorMap tb2t;             // key-major kernel: the transposed copy b2t, same box and swizzle
   CUtensorMap tdq, tdk, tdv;    // key-major kernel: output views, box (DP/2, 1, 32, 1) = one warp's share
+  CUtensorMap tdb2p;            // fp32 partial planes as 3-D (j, i, G*B*H), box (32, 32, 1), 128B swizzle
   const uint16_t* q;
   const uint16_t* out;
   const uint16_t* dout;
@@ -61,6 +62,7 @@ struct BwdArgs {
   int q_stages;             // main kernel: depth of the Q/dO ring
   int b2_resident;          // main kernel: pair-bias tiles of the (b, h, key tile) group stay in smem
   int part_stages;          // pair-bias partial kernel: depth of its ring
+  int db2p_tma;             // pair-bias partial kernel: tile stores through tdb2p (L % 4 == 0)
   int zero_dq;              // delta kernel also clears the fp32 dQ accumulator
   float scale;              // D^-1/2
   float scale_log2;         // D^-1/2 * log2(e)
