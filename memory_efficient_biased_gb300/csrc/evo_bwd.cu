@@ -162,22 +162,17 @@ struct MainBars {
 template <int DP>
 struct MainLayout {
   static constexpr uint32_t kTB = kTile * DP * 2;
-  uint32_t k[2], v[2], b1[2], q[kMaxQStages], d_o[kMaxQStages], ld[kMaxQStages], b2s[kMaxQStages], b2r, p, ds,
-      bars, total;
+  Ring k, v, b1, q, d_o, ld, b2s;
+  uint32_t b2r, p, ds, bars, total;
   __host__ __device__ MainLayout(int b2kind, int qs, int QT) {
     uint32_t off = 0;
-    for (int s = 0; s < 2; ++s) {
-      k[s] = off;
-      v[s] = off + kTB;
-      off += 2 * kTB;
-    }
-    for (int s = 0; s < kMaxQStages; ++s) {
-      const int t = s < qs ? s : 0;
-      q[s] = off + t * 2 * kTB;
-      d_o[s] = q[s] + kTB;
-    }
+    k = Ring{off, 2 * kTB};
+    v = Ring{off + kTB, 2 * kTB};
+    off += 4 * kTB;
+    q = Ring{off, 2 * kTB};
+    d_o = Ring{off + kTB, 2 * kTB};
     off += qs * 2 * kTB;
-    for (int s = 0; s < kMaxQStages; ++s) b2s[s] = off + (s < qs ? s : 0) * 32768u;
+    b2s = Ring{off, 32768u};
     if (b2kind == kB2Stream) off += qs * 32768u;
     b2r = off;
     if (b2kind == kB2Resident) off += QT * 32768u;
@@ -185,9 +180,9 @@ struct MainLayout {
     off += 32768u;
     ds = off;
     off += 32768u;
-    for (int s = 0; s < 2; ++s) b1[s] = off + s * 512u;
+    b1 = Ring{off, 512u};
     off += 1024u;
-    for (int s = 0; s < kMaxQStages; ++s) ld[s] = off + (s < qs ? s : 0) * 1024u;
+    ld = Ring{off, 1024u};
     off += qs * 1024u;
     bars = off;
     off += (sizeof(MainBars) + 127) & ~127u;
@@ -736,29 +731,25 @@ struct SliceBars {
 template <int DP>
 struct SliceLayout {
   static constexpr uint32_t kTB = kTile * DP * 2;
-  uint32_t k[2], v[2], b1[2], q[kMaxQStages], d_o[kMaxQStages], b2s[kMaxQStages], ld[kMaxQStages], p, ds, bars,
-      total;
+  Ring k, v, b1, q, d_o, b2s, ld;
+  uint32_t p, ds, bars, total;
   __host__ __device__ SliceLayout(bool has_b2, int qs) {
     uint32_t off = 0;
-    for (int s = 0; s < 2; ++s) {
-      k[s] = off;
-      v[s] = off + kTB;
-      off += 2 * kTB;
-    }
-    for (int s = 0; s < kMaxQStages; ++s) {
-      q[s] = off + (s < qs ? s : 0) * 2 * kTB;
-      d_o[s] = q[s] + kTB;
-    }
+    k = Ring{off, 2 * kTB};
+    v = Ring{off + kTB, 2 * kTB};
+    off += 4 * kTB;
+    q = Ring{off, 2 * kTB};
+    d_o = Ring{off + kTB, 2 * kTB};
     off += qs * 2 * kTB;
-    for (int s = 0; s < kMaxQStages; ++s) b2s[s] = off + (s < qs ? s : 0) * 32768u;
+    b2s = Ring{off, 32768u};
     if (has_b2) off += qs * 32768u;
     p = off;
     off += 32768u;
     ds = off;
     off += 32768u;
-    for (int s = 0; s < 2; ++s) b1[s] = off + s * 512u;
+    b1 = Ring{off, 512u};
     off += 1024u;
-    for (int s = 0; s < kMaxQStages; ++s) ld[s] = off + (s < qs ? s : 0) * 1024u;
+    ld = Ring{off, 1024u};
     off += qs * 1024u;
     bars = off;
     off += (sizeof(SliceBars) + 127) & ~127u;
@@ -1297,27 +1288,22 @@ struct PartBars {
 template <int DP>
 struct PartLayout {
   static constexpr uint32_t kTB = kTile * DP * 2;
-  uint32_t q[kMaxPartStages], d_o[kMaxPartStages], k[kMaxPartStages], v[kMaxPartStages], b1[kMaxPartStages],
-      ld[kMaxPartStages], b2, stg, bars, total;
+  Ring q, d_o, k, v, b1, ld;
+  uint32_t b2, stg, bars, total;
   // stage: also 64 KB of staging for the tile stores of the partial sums (8 KB per compute warp)
   __host__ __device__ PartLayout(int ns, bool stage) {
     uint32_t off = 0;
-    for (int s = 0; s < kMaxPartStages; ++s) {
-      const uint32_t o = off + (s < ns ? s : 0) * 4 * kTB;
-      q[s] = o;
-      d_o[s] = o + kTB;
-      k[s] = o + 2 * kTB;
-      v[s] = o + 3 * kTB;
-    }
+    q = Ring{off, 4 * kTB};
+    d_o = Ring{off + kTB, 4 * kTB};
+    k = Ring{off + 2 * kTB, 4 * kTB};
+    v = Ring{off + 3 * kTB, 4 * kTB};
     off += ns * 4 * kTB;
     b2 = off;
     off += 32768u;
     stg = off;
     if (stage) off += 65536u;
-    for (int s = 0; s < kMaxPartStages; ++s) {
-      b1[s] = off + (s < ns ? s : 0) * 1536u;
-      ld[s] = b1[s] + 512u;
-    }
+    b1 = Ring{off, 1536u};
+    ld = Ring{off + 512u, 1536u};
     off += ns * 1536u;
     bars = off;
     off += (sizeof(PartBars) + 127) & ~127u;

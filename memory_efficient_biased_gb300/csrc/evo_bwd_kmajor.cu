@@ -56,33 +56,25 @@ struct KmBars {
 template <int DP>
 struct KmLayout {
   static constexpr uint32_t kTB = kTile * DP * 2;
-  uint32_t ds[2], b2t[kKmMaxQS], stg[2], k[2], v[2], q[kKmMaxQS], d_o[kKmMaxQS], b1[2], ld[kKmMaxQS], bars,
-      total;
+  Ring ds, stg, b2t, k, v, q, d_o, b1, ld;
+  uint32_t bars, total;
   __host__ __device__ KmLayout(bool has_b2, int qs) {
     uint32_t off = 0;
-    for (int s = 0; s < 2; ++s) {  // 128B-swizzled tiles first (1024-byte aligned)
-      ds[s] = off;
-      off += 32768u;
-    }
-    for (int s = 0; s < 2; ++s) {  // staging of finished dK / dV / dQ: per warp two [32][DP/2] blocks
-      stg[s] = off;
-      off += kTB;
-    }
-    for (int s = 0; s < kKmMaxQS; ++s) b2t[s] = off + (s < qs ? s : 0) * 32768u;
+    ds = Ring{off, 32768u};  // 128B-swizzled tiles first (1024-byte aligned)
+    off += 2 * 32768u;
+    stg = Ring{off, kTB};    // staging of finished dK / dV / dQ: per warp two [32][DP/2] blocks
+    off += 2 * kTB;
+    b2t = Ring{off, 32768u};
     if (has_b2) off += qs * 32768u;
-    for (int s = 0; s < 2; ++s) {
-      k[s] = off;
-      v[s] = off + kTB;
-      off += 2 * kTB;
-    }
-    for (int s = 0; s < kKmMaxQS; ++s) {
-      q[s] = off + (s < qs ? s : 0) * 2 * kTB;
-      d_o[s] = q[s] + kTB;
-    }
+    k = Ring{off, 2 * kTB};
+    v = Ring{off + kTB, 2 * kTB};
+    off += 4 * kTB;
+    q = Ring{off, 2 * kTB};
+    d_o = Ring{off + kTB, 2 * kTB};
     off += qs * 2 * kTB;
-    for (int s = 0; s < 2; ++s) b1[s] = off + s * 512u;
+    b1 = Ring{off, 512u};
     off += 1024u;
-    for (int s = 0; s < kKmMaxQS; ++s) ld[s] = off + (s < qs ? s : 0) * 1024u;
+    ld = Ring{off, 1024u};
     off += qs * 1024u;
     bars = off;
     off += (sizeof(KmBars) + 127) & ~127u;

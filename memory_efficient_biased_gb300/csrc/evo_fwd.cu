@@ -75,21 +75,20 @@ struct FwdBars {
 template <int DP>
 struct FwdLayout {
   static constexpr uint32_t kTileBytes = kTile * DP * 2;
-  uint32_t q[2], k[kMaxStages], v[kMaxStages], b1[kMaxStages], b2s[kMaxStages], b2r, xchg, bars, total;
+  Ring q, k, v, b1, b2s;
+  uint32_t b2r, xchg, bars, total;
   __host__ __device__ FwdLayout(int b2kind, int stages, int KT) {
     uint32_t off = 0;
-    for (int s = 0; s < 2; ++s) q[s] = off + s * kTileBytes;
+    q = Ring{off, kTileBytes};
     off += 2 * kTileBytes;
-    for (int s = 0; s < kMaxStages; ++s) {
-      k[s] = off + (s < stages ? s : 0) * 2 * kTileBytes;
-      v[s] = k[s] + kTileBytes;
-    }
+    k = Ring{off, 2 * kTileBytes};
+    v = Ring{off + kTileBytes, 2 * kTileBytes};
     off += stages * 2 * kTileBytes;
-    for (int s = 0; s < kMaxStages; ++s) b2s[s] = off + (s < stages ? s : 0) * 32768u;
+    b2s = Ring{off, 32768u};
     if (b2kind == kB2Stream) off += stages * 32768u;
     b2r = off;
     if (b2kind == kB2Resident) off += KT * 32768u;
-    for (int s = 0; s < kMaxStages; ++s) b1[s] = off + (s < stages ? s : 0) * 512u;
+    b1 = Ring{off, 512u};
     off += stages * 512u;
     xchg = off;  // epilogue merge: per half, (m, l) and the partner's DP/2 output columns, [value][row]
     off += 2 * (2 + DP / 2) * 128 * 4;

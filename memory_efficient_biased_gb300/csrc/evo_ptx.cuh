@@ -12,6 +12,14 @@ namespace evo {
 // Device status codes written by kernels (match evo_status_t).
 constexpr int kStatusTimeout = 8;
 
+// Shared-memory offsets of a ring of equally sized buffers: ring[s] = base + s·stride.
+// (Arithmetic rather than an array, so that a run-time stage index never forces
+// the layout into local memory.)
+struct Ring {
+  uint32_t base, stride;
+  __host__ __device__ constexpr uint32_t operator[](uint32_t s) const { return base + s * stride; }
+};
+
 struct WaitGuard {
   uint64_t limit_ns;       // bound on any single wait
   int* status;             // global status word (set on timeout)
