@@ -41,7 +41,75 @@ namespace {
 // ============================================================ evo_bwd_pre
 template <int DP, bool BF16>
 __global__ void __launch_bounds__(256) evo_bwd_pre(const BwdArgs a) {
+  if (a.b2t) {  // transposed pair bias for the key-major kernel, in 32 x 32 tiles through smem
+    __shared__ uint16_t tile[32][34];
+    const int TL = (a.L + 31) / 32, lane = threadIdx.x & 31, row0 = threadIdx.x >> 5;
+    const long long tiles = static_cast<long long>(a.B) * a.H * TL * TL;
+    for (long long t = blockIdx.x; t < tiles; t += gridDim.x) {
+      const int tj = static_cast<int>(t % TL), ti = static_cast<int>((t / TL) % TL);
+      const long long bh = t / (static_cast<long long>(TL) * TL);
+      const uint16_t* src = a.bias2 + bh * a.L * a.L;
+      for (int rr = row0; rr < 32; rr += 8) {
+        const int i = ti * 32 + rr, j = tj * 32 + lane;
+        tile[rr][lane] = (i < a.L && j < a.L) ? src[static_cast<size_t>(i) * a.L + j] : static_cast<uint16_t>(0);
+      }
+      __syncthreads();
+      uint16_t* dst = a.b2t + bh * a.L * a.b2t_pitch;
+      for (int rr = row0; rr < 32; rr += 8) {
+        const int j = tj * 32 + rr, i = ti * 32 + lane;
+        if (j < a.L && i < a.L) dst[static_cast<size_t>(j) * a.b2t_pitch + i] = tile[lane][rr];
+      }
+      __syncthreads();
+    }
+  }
   const long long rows = static_cast<long long>(a.B) * a.N * a.L * a.H;
+  if (!a.zero_dq && (a.D == 8 || a.D == 16 || a.D == 32 || a.D == 64)) {
+    // Coalesced: each lane takes one 16-byte chunk (8 elements) of O and dO; the D/8
+    // lanes of a row (adjacent) reduce their partial dot products with shuffles.
+    const int lpr = a.D / 8;                                   // lanes per row
+    const long long chunks = rows * lpr;
+    const int lane = threadIdx.x & 31;
+    const long long stride = gridDim.x * 256ll;
+    constexpr int U = 4;  // chunks per thread per round (all loads issued first)
+    for (long long c0 = blockIdx.x * 256ll + threadIdx.x; c0 - lane < chunks; c0 += U * stride) {
+      uint4 ov[U], gv[U];
+#pragma unroll
+      for (int q = 0; q < U; ++q) {
+        const long long ch = c0 + q * stride;
+        ov[q] = ch < chunks ? __ldg(reinterpret_cast<const uint4*>(a.out) + ch) : make_uint4(0u, 0u, 0u, 0u);
+        gv[q] = ch < chunks ? __ldg(reinterpret_cast<const uint4*>(a.dout) + ch) : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int q = 0; q < U; ++q) {
+        const long long ch = c0 + q * stride;
+        if (ch - lane >= chunks) break;  // uniform across the warp
+        const uint32_t ow[4] = {ov[q].x, ov[q].y, ov[q].z, ov[q].w}, gw[4] = {gv[q].x, gv[q].y, gv[q].z, gv[q].w};
+        float sum = 0.0f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          sum = fmaf(unpack_lo<BF16>(ow[e]), unpack_lo<BF16>(gw[e]), sum);
+          sum = fmaf(unpack_hi<BF16>(ow[e]), unpack_hi<BF16>(gw[e]), sum);
+        }
+        for (int off = 1; off < lpr; off <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+        if (ch < chunks && (lane & (lpr - 1)) == 0) {
+          // row (b, n, i, h) in memory order of [B,N,L,H,D] -> delta [B,N,H,L]; 32-bit
+          // division when the row count allows it (64-bit division is far slower)
+          const long long row = ch / lpr;
+          long long dst;
+          if (rows < (1ll << 31)) {
+            const uint32_t r32 = static_cast<uint32_t>(row), H = a.H, L = a.L;
+            const uint32_t t = r32 / H, h = r32 - t * H, bn = t / L, i = t - bn * L;
+            dst = (static_cast<long long>(bn) * H + h) * L + i;
+          } else {
+            const int h = static_cast<int>(row % a.H);
+            const long long t = row / a.H;
+            dst = (t / a.L * a.H + h) * a.L + t % a.L;
+          }
+          a.delta[dst] = sum;
+        }
+      }
+    }
+  } else
   for (long long row = blockIdx.x * 256ll + threadIdx.x; row < rows; row += gridDim.x * 256ll) {
     // row enumerates (b, n, i, h) in memory order of [B,N,L,H,D]
     const int h = static_cast<int>(row % a.H);
@@ -70,27 +138,7 @@ __global__ void __launch_bounds__(256) evo_bwd_pre(const BwdArgs a) {
     }
     a.delta[(bn * a.H + h) * a.L + i] = sum;
   }
-  if (a.b2t) {  // transposed pair bias for the key-major kernel, in 32 x 32 tiles through smem
-    __shared__ uint16_t tile[32][34];
-    const int TL = (a.L + 31) / 32, lane = threadIdx.x & 31, row0 = threadIdx.x >> 5;
-    const long long tiles = static_cast<long long>(a.B) * a.H * TL * TL;
-    for (long long t = blockIdx.x; t < tiles; t += gridDim.x) {
-      const int tj = static_cast<int>(t % TL), ti = static_cast<int>((t / TL) % TL);
-      const long long bh = t / (static_cast<long long>(TL) * TL);
-      const uint16_t* src = a.bias2 + bh * a.L * a.L;
-      for (int rr = row0; rr < 32; rr += 8) {
-        const int i = ti * 32 + rr, j = tj * 32 + lane;
-        tile[rr][lane] = (i < a.L && j < a.L) ? src[static_cast<size_t>(i) * a.L + j] : static_cast<uint16_t>(0);
-      }
-      __syncthreads();
-      uint16_t* dst = a.b2t + bh * a.L * a.b2t_pitch;
-      for (int rr = row0; rr < 32; rr += 8) {
-        const int j = tj * 32 + rr, i = ti * 32 + lane;
-        if (j < a.L && i < a.L) dst[static_cast<size_t>(j) * a.b2t_pitch + i] = tile[lane][rr];
-      }
-      __syncthreads();
-    }
-  }
+
 }
 
 // ============================================================ evo_bwd_dq_cast
@@ -113,6 +161,50 @@ __global__ void __launch_bounds__(256) evo_bwd_dq_cast(const BwdArgs a) {
 template <bool BF16>
 __global__ void __launch_bounds__(256) evo_bwd_db2_sum(const BwdArgs a) {
   const long long plane = static_cast<long long>(a.B) * a.H * a.L * a.L;
+  if ((plane & 3) == 0) {  // four consecutive elements per thread, same fixed group order
+    const float4* part = reinterpret_cast<const float4*>(a.db2_part);
+    const long long p4 = plane / 4;
+    for (long long e = blockIdx.x * 256ll + threadIdx.x; e < p4; e += gridDim.x * 256ll) {
+      float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+      int g = 0;
+      for (; g + 16 <= a.groups; g += 16) {
+        float4 v[16];
+#pragma unroll
+        for (int t = 0; t < 16; ++t) v[t] = __ldg(part + (g + t) * p4 + e);
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+          s.x += v[t].x;
+          s.y += v[t].y;
+          s.z += v[t].z;
+          s.w += v[t].w;
+        }
+      }
+      for (; g + 4 <= a.groups; g += 4) {
+        float4 v[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) v[t] = __ldg(part + (g + t) * p4 + e);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          s.x += v[t].x;
+          s.y += v[t].y;
+          s.z += v[t].z;
+          s.w += v[t].w;
+        }
+      }
+      for (; g < a.groups; ++g) {
+        const float4 v = __ldg(part + g * p4 + e);
+        s.x += v.x;
+        s.y += v.y;
+        s.z += v.z;
+        s.w += v.w;
+      }
+      uint2 pk;
+      pk.x = pack2<BF16>(s.x, s.y);
+      pk.y = pack2<BF16>(s.z, s.w);
+      reinterpret_cast<uint2*>(a.dbias2)[e] = pk;
+    }
+    return;
+  }
   for (long long e = blockIdx.x * 256ll + threadIdx.x; e < plane; e += gridDim.x * 256ll) {
     float s = 0.0f;
     int g = 0;
