@@ -21,15 +21,19 @@
 //               for an epilogue.
 //   warps 0..7  softmax.  Warp w owns query rows 32·(w%4).. (its TMEM lane
 //               quadrant) and key columns 64·(w/4).. of every tile, and runs an
-//               independent online softmax over its key half: its own running
-//               max and sum, its P half (fp16/bf16, into TMEM) and its own P·V
-//               accumulator (the MMA thread issues one K = 64 P·V per half).  The
-//               two halves of a row are merged once per item, in the epilogue
-//               (rescaled by 2^(m_half - m)), so the two warps never wait on each
-//               other inside the key loop.  Scale and biases are applied in the
-//               log2 domain with packed f32x2 arithmetic; each warp keeps its
-//               half's output row in fp32 registers and finishes an item's
-//               epilogue while the next item's first tile is already running.
+//               independent online softmax over its key half: its own reference
+//               max and sum, its P half (fp16/bf16, into TMEM).  P·V accumulates
+//               in TMEM across all key tiles of an item (one accumulator per key
+//               half, double-buffered across items).  The reference max moves
+//               only when a tile's max exceeds it by more than 2^8 (P stays
+//               below 256, exact in fp16/bf16); then the warp rescales its
+//               accumulator in TMEM once the previous P·V is done.  The two
+//               halves of a row are merged once per item, in the epilogue: each
+//               warp reads its DP/2 output columns of both accumulators and the
+//               partner's (max, sum) from shared memory, and writes its share
+//               of O through shared memory with a TMA tile store.  Scale and
+//               biases are applied in the log2 domain with packed f32x2
+//               arithmetic.
 // Key columns past L carry a -inf key-mask entry, so no other masking is
 // needed; query rows past L are computed and not stored.
 #include "evo_internal.h"
@@ -66,6 +70,7 @@ struct FwdBars {
   uint64_t s_full[2], s_free[2];
   uint64_t p_full[2], p_empty[2];
   uint64_t o_full[2], o_free[2];
+  uint64_t pv_done;            // one phase per P·V tile (waited on only before a rescale)
   uint64_t xsum[4], xdone[4];  // per lane quadrant: the two warps sharing those rows (epilogue merge)
   uint64_t drain;
   uint32_t tmem_slot;
@@ -76,7 +81,7 @@ template <int DP>
 struct FwdLayout {
   static constexpr uint32_t kTileBytes = kTile * DP * 2;
   Ring q, k, v, b1, b2s;
-  uint32_t b2r, xchg, bars, total;
+  uint32_t b2r, xchg, stg, bars, total;
   __host__ __device__ FwdLayout(int b2kind, int stages, int KT) {
     uint32_t off = 0;
     q = Ring{off, kTileBytes};
@@ -90,8 +95,11 @@ struct FwdLayout {
     if (b2kind == kB2Resident) off += KT * 32768u;
     b1 = Ring{off, 512u};
     off += stages * 512u;
-    xchg = off;  // epilogue merge: per half, (m, l) and the partner's DP/2 output columns, [value][row]
-    off += 2 * (2 + DP / 2) * 128 * 4;
+    xchg = off;  // epilogue merge: per half, (max, sum) of each row, [value][row]
+    off += 2 * 2 * 128 * 4;
+    off = (off + 1023u) & ~1023u;
+    stg = off;   // O staging: per softmax warp [32 rows][DP/2] (box row swizzle)
+    off += kSoftmaxWarps * 32u * DP;
     bars = off;
     off += (sizeof(FwdBars) + 127) & ~127u;
     total = off;
@@ -257,29 +265,32 @@ __device__ __forceinline__ void fwd_producer(const FwdArgs& a, uint8_t* base, co
 }
 
 // ------------------------------------------------------------ MMA issuer (one thread)
-// O_v,half = P_v,half · V_v,half for both key halves (K = 64 keys each), P from TMEM.
+// O_half (+)= P_v,half · V_v,half for both key halves (K = 64 keys each), P from
+// TMEM, accumulated over the key tiles of item `item` (tile jt of KT).
 template <int DP, bool BF16>
-__device__ __forceinline__ bool fwd_issue_pv(uint32_t v, uint32_t sv, uint8_t* base, const FwdLayout<DP>& lay,
-                                             FwdBars* bars, uint32_t tmem, const WaitGuard& g) {
+__device__ __forceinline__ bool fwd_issue_pv(uint32_t v, uint32_t sv, int jt, int KT, uint32_t item, uint8_t* base,
+                                             const FwdLayout<DP>& lay, FwdBars* bars, uint32_t tmem,
+                                             const WaitGuard& g) {
   constexpr uint32_t RB = DP * 2;
   constexpr uint32_t SWZ = swizzle_for_row(RB);
   constexpr uint32_t id_o = idesc_f16(128, DP, BF16, false, true);
   constexpr int NB = o_buffers<DP>();
   const uint32_t vb = v & 1, vph = (v >> 1) & 1;
-  const uint32_t ob = v % NB, oph = (v / NB) & 1;
+  const uint32_t ob = item % NB, oph = (item / NB) & 1;
   if (!mbar_wait(smem_u32(&bars->p_full[vb]), vph, g)) return false;
-  if (!mbar_wait(smem_u32(&bars->o_free[ob]), oph ^ 1, g)) return false;
+  if (jt == 0 && !mbar_wait(smem_u32(&bars->o_free[ob]), oph ^ 1, g)) return false;
   tc_fence_after();
-  const uint32_t v_addr = smem_u32(base + lay.v[sv]);
+  const uint64_t vd = smem_desc(smem_u32(base + lay.v[sv]), kTile * RB, 8 * RB, SWZ);
+  const uint32_t acc = jt > 0 ? 1u : 0u;
 #pragma unroll
   for (int half = 0; half < 2; ++half) {
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {  // 64 keys in steps of 16 (8 TMEM columns of packed pairs)
-      const uint64_t bd = smem_desc(v_addr + (half * 64 + k * 16) * RB, kTile * RB, 8 * RB, SWZ);
-      umma_ts(tmem + col_o<DP>(ob, half), tmem + col_p(vb) + half * 32 + k * 8, bd, id_o, k > 0);
-    }
+    for (int k = 0; k < 4; ++k)  // 64 keys in steps of 16 (8 TMEM columns of packed pairs)
+      umma_ts(tmem + col_o<DP>(ob, half), tmem + col_p(vb) + half * 32 + k * 8, vd + (half * 64 + k * 16) * RB / 16,
+              id_o, (acc | k) ? 1u : 0u);
   }
-  umma_commit(smem_u32(&bars->o_full[ob]));
+  umma_commit(smem_u32(&bars->pv_done));
+  if (jt == KT - 1) umma_commit(smem_u32(&bars->o_full[ob]));
   umma_commit(smem_u32(&bars->p_empty[vb]));
   umma_commit(smem_u32(&bars->kv_empty[sv]));
   return true;
@@ -292,30 +303,32 @@ __device__ __forceinline__ void fwd_mma(const FwdArgs& a, uint8_t* base, const F
   constexpr uint32_t SWZ = swizzle_for_row(RB);
   constexpr uint32_t id_s = idesc_f16(128, 128, BF16, false, false);
   const int S = a.stages, KT = a.QT;
-  uint32_t u = 0, q_it = 0, prev_stage = 0, s = 0, ph = 0;
+  uint32_t u = 0, q_it = 0, prev_stage = 0, s = 0, ph = 0, item_ord = 0, prev_item = 0;
+  int prev_jt = 0;
   bool ok = true;
-  for (long long item = i0; ok && item < i1; ++item) {
+  for (long long item = i0; ok && item < i1; ++item, ++item_ord) {
     const uint32_t qs = q_it & 1;
     if (!mbar_wait(smem_u32(&bars->q_full[qs]), (q_it >> 1) & 1, g)) { ok = false; break; }
     ++q_it;
     tc_fence_after();
-    const uint32_t q_addr = smem_u32(base + lay.q[qs]);
+    const uint64_t qd = smem_desc(smem_u32(base + lay.q[qs]), 16, 8 * RB, SWZ);
     for (int jt = 0; jt < KT; ++jt) {
       if (!mbar_wait(smem_u32(&bars->kv_full[s]), ph, g)) { ok = false; break; }
       const uint32_t buf = u & 1;
       if (!mbar_wait(smem_u32(&bars->s_free[buf]), ((u >> 1) & 1) ^ 1, g)) { ok = false; break; }
       tc_fence_after();
-      const uint32_t k_addr = smem_u32(base + lay.k[s]);
+      const uint64_t kd = smem_desc(smem_u32(base + lay.k[s]), 16, 8 * RB, SWZ);
 #pragma unroll
-      for (int k = 0; k < DP / 16; ++k) {
-        const uint64_t ad = smem_desc(q_addr + k * 32, 16, 8 * RB, SWZ);
-        const uint64_t bd = smem_desc(k_addr + k * 32, 16, 8 * RB, SWZ);
-        umma_ss(tmem + col_s(buf), ad, bd, id_s, k > 0);
-      }
+      for (int k = 0; k < DP / 16; ++k) umma_ss(tmem + col_s(buf), qd + k * 2, kd + k * 2, id_s, k > 0);
       umma_commit(smem_u32(&bars->s_full[buf]));
       if (jt == KT - 1) umma_commit(smem_u32(&bars->q_empty[qs]));
-      if (u > 0 && !fwd_issue_pv<DP, BF16>(u - 1, prev_stage, base, lay, bars, tmem, g)) { ok = false; break; }
+      if (u > 0 && !fwd_issue_pv<DP, BF16>(u - 1, prev_stage, prev_jt, KT, prev_item, base, lay, bars, tmem, g)) {
+        ok = false;
+        break;
+      }
       prev_stage = s;
+      prev_jt = jt;
+      prev_item = item_ord;
       ++u;
       if (++s == static_cast<uint32_t>(S)) {
         s = 0;
@@ -323,103 +336,113 @@ __device__ __forceinline__ void fwd_mma(const FwdArgs& a, uint8_t* base, const F
       }
     }
   }
-  if (ok && u > 0) fwd_issue_pv<DP, BF16>(u - 1, prev_stage, base, lay, bars, tmem, g);
+  if (ok && u > 0) fwd_issue_pv<DP, BF16>(u - 1, prev_stage, prev_jt, KT, prev_item, base, lay, bars, tmem, g);
   // Drain: all MMAs this thread issued are complete before TMEM is freed.
   umma_commit(smem_u32(&bars->drain));
   drain_wait(smem_u32(&bars->drain), 0, a.wait_ns, a.status);
 }
 
 // ------------------------------------------------------------ softmax (warps 0..7)
-// acc (this warp's key half: all DP output columns of its row) = acc·alpha + O tile v.
-template <int DP>
-__device__ __forceinline__ bool fwd_consume_o(uint32_t v, float alpha, float (&acc)[DP], FwdBars* bars,
-                                              uint32_t trow, int hc, int lane, const WaitGuard& g) {
-  constexpr int NB = o_buffers<DP>();
-  const uint32_t ob = v % NB;
-  if (!mbar_wait(smem_u32(&bars->o_full[ob]), (v / NB) & 1, g)) return false;
-  tc_fence_after();
-  const uint32_t col = trow + col_o<DP>(ob, hc);
-  uint32_t o[DP / 16][16];
+constexpr float kRescaleLog2 = 8.0f;  // the reference max moves only past this margin
+
+// n fp32 TMEM columns of this thread's lane (n a multiple of 8) into v.
+template <int N>
+__device__ __forceinline__ void tmem_load_cols(uint32_t col, float (&v)[N]) {
+  if constexpr (N == 8) {
+    uint32_t x[8];
+    tmem_ld8(col, x);
+    tmem_wait_ld(x);
 #pragma unroll
-  for (int c = 0; c < DP / 16; ++c) tmem_ld16(col + c * 16, o[c]);
+    for (int e = 0; e < 8; ++e) v[e] = __uint_as_float(x[e]);
+  } else {
+    uint32_t x[N / 16][16];
 #pragma unroll
-  for (int c = 0; c < DP / 16; ++c) tmem_wait_ld(o[c]);
-  tc_fence_before();
-  __syncwarp();
-  if (lane == 0) mbar_arrive(smem_u32(&bars->o_free[ob]));
+    for (int q = 0; q < N / 16; ++q) tmem_ld16(col + q * 16, x[q]);
 #pragma unroll
-  for (int c = 0; c < DP / 16; ++c)
+    for (int q = 0; q < N / 16; ++q) tmem_wait_ld(x[q]);
 #pragma unroll
-    for (int e = 0; e < 16; ++e) acc[c * 16 + e] = fmaf(acc[c * 16 + e], alpha, __uint_as_float(o[c][e]));
-  return true;
+    for (int q = 0; q < N / 16; ++q)
+#pragma unroll
+      for (int e = 0; e < 16; ++e) v[q * 16 + e] = __uint_as_float(x[q][e]);
+  }
 }
 
-// Merge the two key halves of a finished item's rows and write O and lse.
-// Each warp writes its (m, l) and the partner's DP/2 output columns to shared
-// memory, then finishes its own DP/2 columns.
-template <int DP, bool BF16>
-__device__ __forceinline__ bool fwd_epilogue(const FwdArgs& a, const ItemIter& c, const float (&acc)[DP], float m,
-                                             float l, uint32_t fin, FwdBars* bars, float* xchg, int quad, int hc,
-                                             int r, int lane, const WaitGuard& g) {
-  constexpr int HD = DP / 2;
-  constexpr int NV = 2 + HD;  // values per row and half: m, l, HD output columns
-  if (fin > 0 && !mbar_wait(smem_u32(&bars->xdone[quad]), (fin - 1) & 1, g)) return false;
-  // keep: this warp's own output columns; give: the partner's (compile-time indices only)
-  float keep[HD], give[HD];
-  if (hc == 0) {
+// This warp's accumulator (its key half, all DP columns) *= alpha, in place.
+template <int DP>
+__device__ __forceinline__ void fwd_rescale_o(uint32_t col, float alpha) {
 #pragma unroll
-    for (int e = 0; e < HD; ++e) {
-      keep[e] = acc[e];
-      give[e] = acc[HD + e];
-    }
-  } else {
+  for (int c = 0; c < DP / 16; ++c) {
+    uint32_t x[16];
+    tmem_ld16(col + c * 16, x);
+    tmem_wait_ld(x);
 #pragma unroll
-    for (int e = 0; e < HD; ++e) {
-      keep[e] = acc[HD + e];
-      give[e] = acc[e];
-    }
+    for (int e = 0; e < 16; ++e) x[e] = __float_as_uint(__uint_as_float(x[e]) * alpha);
+    tmem_st16(col + c * 16, x);
   }
-  float* mine = xchg + hc * NV * 128;
-  mine[0 * 128 + r] = m;
-  mine[1 * 128 + r] = l;
-#pragma unroll
-  for (int e = 0; e < HD; ++e) mine[(2 + e) * 128 + r] = give[e];
+  tmem_wait_st();
+}
+
+// Merge the two key halves of a finished item's rows and write O and lse (m: the
+// half's reference max in log2 units, -inf when none of its keys is unmasked).  Each
+// warp exchanges its (max, sum) with the partner warp of its lane quadrant, reads
+// its DP/2 output columns of both accumulators from TMEM, and stores its
+// [32 rows][DP/2] share of O through shared memory with one TMA tile store.
+template <int DP, bool BF16>
+__device__ __forceinline__ bool fwd_epilogue(const FwdArgs& a, const ItemIter& c, float m, float l, uint32_t fin,
+                                             uint8_t* base, const FwdLayout<DP>& lay, FwdBars* bars, uint32_t trow,
+                                             int w, int quad, int hc, int r, int lane, const WaitGuard& g) {
+  constexpr int HD = DP / 2;
+  constexpr int NB = o_buffers<DP>();
+  const uint32_t ob = fin % NB;
+  float* xchg = reinterpret_cast<float*>(base + lay.xchg);
+  if (fin > 0 && !mbar_wait(smem_u32(&bars->xdone[quad]), (fin - 1) & 1, g)) return false;
+  float* mine = xchg + hc * 256;
+  mine[r] = m;
+  mine[128 + r] = l;
   __syncwarp();
   if (lane == 0) mbar_arrive(smem_u32(&bars->xsum[quad]));
   if (!mbar_wait(smem_u32(&bars->xsum[quad]), fin & 1, g)) return false;
-  const float* other = xchg + (hc ^ 1) * NV * 128;
+  const float* other = xchg + (hc ^ 1) * 256;
   const float m_o = other[r], l_o = other[128 + r];
-  float po[HD];
-#pragma unroll
-  for (int e = 0; e < HD; ++e) po[e] = other[(2 + e) * 128 + r];
   __syncwarp();
   if (lane == 0) mbar_arrive(smem_u32(&bars->xdone[quad]));
-  const float mm = fmaxf(m, m_o);
-  const float m_use = (mm == -INFINITY) ? 0.0f : mm;
-  const float s_me = ex2(m - m_use), s_o = ex2(m_o - m_use);
+  const float mx = fmaxf(m, m_o);
+  const float mm = mx == -INFINITY ? 0.0f : mx;  // both halves empty: O = 0, lse = -inf
+  const float s_me = ex2(m - mm), s_o = ex2(m_o - mm);
   const float lt = fmaf(l, s_me, l_o * s_o);
-  const int i = c.qt * kTile + r;
-  if (i < a.L) {
-    const float inv = lt > 0.0f ? 1.0f / lt : 0.0f;
-    const float f_me = s_me * inv, f_o = s_o * inv;
-    const size_t bn = static_cast<size_t>(c.b) * a.N + c.n;
-    uint16_t* orow = a.out + ((bn * a.L + i) * a.H + c.h) * a.D + hc * HD;
-    float o[HD];
+  const float inv = lt > 0.0f ? 1.0f / lt : 0.0f;
+  const float f_me = s_me * inv, f_o = s_o * inv;
+  // both accumulators' columns hc·HD.. of this lane, once every P·V of the item is done
+  if (!mbar_wait(smem_u32(&bars->o_full[ob]), (fin / NB) & 1, g)) return false;
+  tc_fence_after();
+  float om[HD], oo[HD];
+  tmem_load_cols<HD>(trow + col_o<DP>(ob, hc) + hc * HD, om);
+  tmem_load_cols<HD>(trow + col_o<DP>(ob, hc ^ 1) + hc * HD, oo);
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(smem_u32(&bars->o_free[ob]));
+  uint8_t* blk = base + lay.stg + w * 32 * DP;
+  if (lane == 0) bulk_wait_read_all();  // the previous item's store has read the staging block
+  __syncwarp();
 #pragma unroll
-    for (int e = 0; e < HD; ++e) o[e] = fmaf(keep[e], f_me, po[e] * f_o);
-#pragma unroll
-    for (int c8 = 0; c8 < HD / 8; ++c8) {
-      if (hc * HD + c8 * 8 < a.D) {
-        uint4 pk;
-        pk.x = pack2<BF16>(o[c8 * 8 + 0], o[c8 * 8 + 1]);
-        pk.y = pack2<BF16>(o[c8 * 8 + 2], o[c8 * 8 + 3]);
-        pk.z = pack2<BF16>(o[c8 * 8 + 4], o[c8 * 8 + 5]);
-        pk.w = pack2<BF16>(o[c8 * 8 + 6], o[c8 * 8 + 7]);
-        *reinterpret_cast<uint4*>(orow + c8 * 8) = pk;
-      }
-    }
-    if (hc == 0) a.lse[(bn * a.H + c.h) * a.L + i] = lt > 0.0f ? (m_use + lg2(lt)) * kLn2 : -INFINITY;
+  for (int e = 0; e < HD; e += 8) {
+    uint4 pk;
+    pk.x = pack2<BF16>(fmaf(om[e + 0], f_me, oo[e + 0] * f_o), fmaf(om[e + 1], f_me, oo[e + 1] * f_o));
+    pk.y = pack2<BF16>(fmaf(om[e + 2], f_me, oo[e + 2] * f_o), fmaf(om[e + 3], f_me, oo[e + 3] * f_o));
+    pk.z = pack2<BF16>(fmaf(om[e + 4], f_me, oo[e + 4] * f_o), fmaf(om[e + 5], f_me, oo[e + 5] * f_o));
+    pk.w = pack2<BF16>(fmaf(om[e + 6], f_me, oo[e + 6] * f_o), fmaf(om[e + 7], f_me, oo[e + 7] * f_o));
+    const uint32_t off = HD == 8 ? lane * 16u : swz_offset(lane, e >> 3, DP);
+    *reinterpret_cast<uint4*>(blk + off) = pk;
   }
+  fence_proxy_async_smem();
+  __syncwarp();
+  const size_t bn = static_cast<size_t>(c.b) * a.N + c.n;
+  if (lane == 0) {
+    tma_store_4d(&a.tout, smem_u32(blk), hc * HD, c.h, c.qt * kTile + quad * 32, static_cast<int>(bn));
+    bulk_commit_group();
+  }
+  const int i = c.qt * kTile + r;
+  if (hc == 0 && i < a.L) a.lse[(bn * a.H + c.h) * a.L + i] = lt > 0.0f ? (mm + lg2(lt)) * kLn2 : -INFINITY;
   return true;
 }
 
@@ -428,24 +451,22 @@ __device__ __forceinline__ void fwd_softmax(const FwdArgs& a, uint8_t* base, con
                                             FwdBars* bars, uint32_t tmem, const WaitGuard& g, long long i0,
                                             long long i1) {
   constexpr bool kHasB2 = B2 != kB2None;
+  constexpr int NB = o_buffers<DP>();
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quad = w & 3, hc = w >> 2;  // TMEM lane quadrant, key-column half
   const int r = quad * 32 + lane;       // query row within the tile == TMEM lane
   const uint32_t trow = tmem + (static_cast<uint32_t>(quad * 32) << 16);
-  float* xchg = reinterpret_cast<float*>(base + lay.xchg);
   const float2 sl2 = make_float2(a.scale_log2, a.scale_log2);
   const float2 l2e2 = make_float2(kLog2e, kLog2e);
   const int S = a.stages, KT = a.QT;
-  uint32_t u = 0, fin = 0, grp_it = 0, s = 0, ph = 0;
-  float m = -INFINITY, l = 0.0f, a_prev = 0.0f, m_fin = 0.0f, l_fin = 0.0f;
-  float acc[DP];
-#pragma unroll
-  for (int d = 0; d < DP; ++d) acc[d] = 0.0f;
+  uint32_t u = 0, fin = 0, grp_it = 0, s = 0, ph = 0, item_ord = 0;
+  float m = 0.0f, l = 0.0f, m_fin = 0.0f, l_fin = 0.0f;  // reference max (log2 units) and sum of this half
+  bool have = false;
   ItemIter cur, prev;
   cur.init(i0, a);
   prev = cur;
   bool ok = true;
-  for (long long item = i0; ok && item < i1; ++item) {
+  for (long long item = i0; ok && item < i1; ++item, ++item_ord) {
     if (item > i0) {
       prev = cur;
       cur.next(a);
@@ -456,11 +477,9 @@ __device__ __forceinline__ void fwd_softmax(const FwdArgs& a, uint8_t* base, con
       ++grp_it;
     }
     for (int jt = 0; jt < KT; ++jt) {
-      if (jt == 0) {  // the previous item's row statistics wait for its last O tile
-        m_fin = m;
+      if (jt == 0) {  // the previous item's statistics, for its epilogue (-inf: no unmasked key)
+        m_fin = have ? m : -INFINITY;
         l_fin = l;
-        m = -INFINITY;
-        l = 0.0f;
       }
       const uint32_t buf = u & 1, bph = (u >> 1) & 1;
       if (!mbar_wait(smem_u32(&bars->kv_full[s]), ph, g)) { ok = false; break; }
@@ -511,10 +530,22 @@ __device__ __forceinline__ void fwd_softmax(const FwdArgs& a, uint8_t* base, con
         mbar_arrive(smem_u32(&bars->kv_empty[s]));
         if (B2 == kB2Resident && grp_last && jt == KT - 1) mbar_arrive(smem_u32(&bars->b2_empty));
       }
-      const float m_new = fmaxf(m, fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])));
-      const float m_use = (m_new == -INFINITY) ? 0.0f : m_new;
-      const float alpha = ex2(m - m_use);
-      const float2 nm2 = make_float2(-m_use, -m_use);
+      const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+      // reference max: the first tile's max (0 when every key so far is masked); later
+      // tiles move it only past the margin, and then the accumulator is rescaled
+      // (have: a finite reference exists; until then every P is exactly 0 and so is
+      // the accumulator, so the first unmasked tile just sets the reference)
+      float alpha = 1.0f;
+      if (jt == 0 || !have) {
+        have = mt != -INFINITY;
+        m = have ? mt : 0.0f;
+        if (jt == 0) l = 0.0f;
+      } else if (mt > m + kRescaleLog2) {
+        alpha = ex2(m - mt);
+        m = mt;
+        l *= alpha;
+      }
+      const float2 nm2 = make_float2(-m, -m);
       float2 rs[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
       uint32_t pp[32];
 #pragma unroll
@@ -524,28 +555,28 @@ __device__ __forceinline__ void fwd_softmax(const FwdArgs& a, uint8_t* base, con
         rs[(x >> 1) & 1] = add2(rs[(x >> 1) & 1], make_float2(p0, p1));
         pp[x >> 1] = pack2<BF16>(p0, p1);
       }
-      l = fmaf(l, alpha, (rs[0].x + rs[0].y) + (rs[1].x + rs[1].y));
-      // P half -> TMEM (64 keys = 32 columns of packed pairs)
+      l += (rs[0].x + rs[0].y) + (rs[1].x + rs[1].y);
+      // P half -> TMEM (64 keys = 32 columns of packed pairs), after P·V of tile u-2
       if (!mbar_wait(smem_u32(&bars->p_empty[buf]), bph ^ 1, g)) { ok = false; break; }
       tc_fence_after();
+      // rare: rescale this half's accumulator once P·V of tile u-1 is done.  The TMEM
+      // loads and stores are warp-collective, so the whole warp takes this path when any
+      // of its rows needs it (the other rows scale by 1).
+      if (__any_sync(0xffffffffu, alpha != 1.0f)) {
+        if (!mbar_wait(smem_u32(&bars->pv_done), (u - 1) & 1, g)) { ok = false; break; }
+        tc_fence_after();
+        fwd_rescale_o<DP>(trow + col_o<DP>(item_ord % NB, hc), alpha);
+      }
       tmem_st32(trow + col_p(buf) + hc * 32, pp);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&bars->p_full[buf]));
-      if (u > 0) {
-        if (!fwd_consume_o<DP>(u - 1, a_prev, acc, bars, trow, hc, lane, g)) { ok = false; break; }
-        if (jt == 0) {  // tile u-1 was the last of the previous item
-          if (!fwd_epilogue<DP, BF16>(a, prev, acc, m_fin, l_fin, fin++, bars, xchg, quad, hc, r, lane, g)) {
-            ok = false;
-            break;
-          }
-#pragma unroll
-          for (int d = 0; d < DP; ++d) acc[d] = 0.0f;
-        }
+      if (jt == 0 && u > 0 &&
+          !fwd_epilogue<DP, BF16>(a, prev, m_fin, l_fin, fin++, base, lay, bars, trow, w, quad, hc, r, lane, g)) {
+        ok = false;
+        break;
       }
-      a_prev = alpha;
-      m = m_new;
       ++u;
       if (++s == static_cast<uint32_t>(S)) {
         s = 0;
@@ -553,10 +584,9 @@ __device__ __forceinline__ void fwd_softmax(const FwdArgs& a, uint8_t* base, con
       }
     }
   }
-  if (ok && u > 0) {
-    if (fwd_consume_o<DP>(u - 1, a_prev, acc, bars, trow, hc, lane, g))
-      fwd_epilogue<DP, BF16>(a, cur, acc, m, l, fin++, bars, xchg, quad, hc, r, lane, g);
-  }
+  if (ok && u > 0)
+    fwd_epilogue<DP, BF16>(a, cur, have ? m : -INFINITY, l, fin++, base, lay, bars, trow, w, quad, hc, r, lane, g);
+  if (lane == 0) bulk_wait_all();  // this warp's O stores complete before the CTA's smem goes away
 }
 
 template <int DP, bool BF16, int B2>
@@ -588,6 +618,7 @@ __global__ void __launch_bounds__(kThreads, 1) evo_fwd_kernel(const __grid_const
       mbar_init(smem_u32(&bars->o_full[b]), 1);
       mbar_init(smem_u32(&bars->o_free[b]), kSoftmaxWarps);
     }
+    mbar_init(smem_u32(&bars->pv_done), 1);
     for (int q = 0; q < 4; ++q) {
       mbar_init(smem_u32(&bars->xsum[q]), 2);
       mbar_init(smem_u32(&bars->xdone[q]), 2);
@@ -600,6 +631,7 @@ __global__ void __launch_bounds__(kThreads, 1) evo_fwd_kernel(const __grid_const
     tma_prefetch_desc(&a.tk);
     tma_prefetch_desc(&a.tv);
     if (B2 != kB2None && a.bias2_mode == kBias2Tma) tma_prefetch_desc(&a.tb2);
+    tma_prefetch_desc(&a.tout);
   }
   if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(&bars->tmem_slot), 512);

@@ -110,7 +110,7 @@ bool map_qkv(CUtensorMap* m, const void* p, const evo_shape_t& s, bool bf16) {
 }
 
 // The same 4-D view with a box of one warp's share of an output tile: (DP/2, 1, 32, 1);
-// 32-byte swizzle when the box rows are 32 bytes, none when they are 16.
+// swizzle = the box row (DP bytes): none for 16, 32B for 32, 64B for 64.
 bool map_rows_half(CUtensorMap* m, const void* p, const evo_shape_t& s, bool bf16) {
   const int DP = padded_dim(s.D);
   cuuint64_t dims[4] = {static_cast<cuuint64_t>(s.D), static_cast<cuuint64_t>(s.H), static_cast<cuuint64_t>(s.L),
@@ -119,7 +119,9 @@ bool map_rows_half(CUtensorMap* m, const void* p, const evo_shape_t& s, bool bf1
                            static_cast<cuuint64_t>(s.L * s.H * s.D * 2)};
   cuuint32_t box[4] = {static_cast<cuuint32_t>(DP / 2), 1, 32, 1};
   return encode(m, p, bf16, 4, dims, strides, box,
-                DP == 32 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_NONE);
+                DP == 64   ? CU_TENSOR_MAP_SWIZZLE_64B
+                : DP == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
+                           : CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 // [B,1,H,L,L] viewed as 3-D (key j, query i, B*H).
@@ -300,7 +302,8 @@ evo_status_t evo_attn_fwd(const void* q, const void* k, const void* v, const voi
   const bool bf16 = dtype == EVO_BF16;
   FwdArgs a;
   std::memset(&a, 0, sizeof(a));
-  if (!map_qkv(&a.tq, q, shape, bf16) || !map_qkv(&a.tk, k, shape, bf16) || !map_qkv(&a.tv, v, shape, bf16))
+  if (!map_qkv(&a.tq, q, shape, bf16) || !map_qkv(&a.tk, k, shape, bf16) || !map_qkv(&a.tv, v, shape, bf16) ||
+      !map_rows_half(&a.tout, out, shape, bf16))
     return EVO_ERR_CUDA;
   a.bias2_mode = kBias2None;
   if (bias2) {

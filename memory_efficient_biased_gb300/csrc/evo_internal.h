@@ -16,6 +16,7 @@ enum Bias2Mode : int { kBias2None = 0, kBias2Tma = 1, kBias2Loads = 2 };
 struct FwdArgs {
   CUtensorMap tq, tk, tv;   // 4-D [B*N][L][H][D] views, box (DP, 1, 128, 1)
   CUtensorMap tb2;          // 3-D [B*H][L][L] view, box (64, 128, 1), 128B swizzle (kBias2Tma)
+  CUtensorMap tout;         // O as the 4-D view with box (DP/2, 1, 32, 1): one softmax warp's share
   const uint16_t* bias1;    // [B,N,L] or nullptr
   const uint16_t* bias2;    // [B,H,L,L] or nullptr
   uint16_t* out;            // [B,N,L,H,D]

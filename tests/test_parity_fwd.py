@@ -48,6 +48,30 @@ def test_small(case):
     _compare(inp, inp["q"].dtype)
 
 
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("rows", ["all", "even"])
+def test_rising_scores_across_key_tiles(dtype, rows):
+    """A pair bias that rises ~10 log2 units per 128 keys: later key tiles hold much
+    larger scores than the first, so the running reference max must move (and the
+    partial output be rescaled) inside an item.  With the ramp on even query rows
+    only, neighbouring rows of one warp take different paths."""
+    inp = make_inputs(1, 3, 384, 2, 32, dtype=dtype, mask=("random", 0.05), bias2_sigma=0.5, seed=17)
+    ramp = torch.arange(384, dtype=torch.float32) * (7.0 / 128.0)
+    sel = torch.ones(384) if rows == "all" else (torch.arange(384) % 2 == 0).float()
+    b2 = inp["bias2"].float() + sel.view(1, 1, 1, 384, 1) * ramp.view(1, 1, 1, 1, 384)
+    inp["bias2"] = b2.to(inp["bias2"].dtype)
+    _compare(inp, inp["q"].dtype)
+
+
+def test_first_key_tile_masked_then_very_negative_fp16():
+    """Every key of the first tile masked (-inf in fp16) and the remaining scores near
+    -100: the output is the softmax over the later keys alone."""
+    inp = make_inputs(1, 2, 300, 2, 16, dtype="fp16", mask=None, bias2_sigma=0.5, seed=23)
+    inp["bias1"][..., :128] = float("-inf")
+    inp["bias2"] = (inp["bias2"].float() - 100.0).to(torch.float16)
+    _compare(inp, torch.float16)
+
+
 def test_fully_masked_rows_fp16():
     """Every key of one (b, n) row masked (-1e9 -> -inf in fp16): O = 0, lse = -inf, like the oracle."""
     inp = make_inputs(1, 3, 70, 2, 16, dtype="fp16", mask=("random", 0.1), seed=5)
