@@ -181,6 +181,27 @@ def dist_setup(args):
     return world, rank, local
 
 
+def bias2_groups(w) -> int:
+    """n-groups of the two-stage pair-bias gradient: the library's rule (enough
+    (b, h, query tile, key tile, group) blocks for two waves on 152 SMs)."""
+    qt = -(-w.L // 128)
+    tiles = w.B * w.H * qt * qt
+    g = max(1, min(w.N, -(-304 // tiles)))
+    gs = -(-w.N // g)
+    return -(-w.N // gs)
+
+
+def bwd_mode(w) -> str:
+    """Which backward kernel the library runs for this shape (its TMEM-fit rule)."""
+    dp = 16 if w.D <= 16 else (32 if w.D <= 32 else 64)
+    qt = -(-w.L // 128)
+    if dp <= 32 and 384 + 2 * dp + qt * dp <= 512:
+        return "key-major"
+    if 320 + 2 * dp + qt * dp <= 512:
+        return "slice"
+    return "main"
+
+
 def max_over_ranks(x: float) -> float:
     """Maximum of a per-rank float over the process group (identity without one)."""
     import torch
@@ -219,6 +240,7 @@ def run_reference(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": w.name, "B": w.B, "N": w.N, "L": w.L, "H": w.H, "D": w.D,
+                       "backward": mode,
                        "input_dtype": args.dtype, "rows_per_step": rows},
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
                              "sample": sample},
@@ -341,18 +363,18 @@ def run_ours(args):
     bnhl = w.B * w.N * w.H * w.L
     b1b = w.B * w.N * w.L * 2 if has_b1 else 0
     b2b = w.B * w.H * w.L * w.L * 2 if has_b2 else 0
+    mode = bwd_mode(w)
     work = {
         "fwd": ("tensor", F["fwd"]),
         "bwd_main": ("tensor", F["bwd"]),
         "bwd_db2_part": ("tensor", 4.0 * E_el * w.D),
-        "bwd_pre": ("hbm", 2 * qkv + bnhl * 4 + 2 * qkv),
+        # O, dO read, delta written; plus clearing the fp32 dQ accumulator (per-key-tile mode)
+        # or the transposed pair-bias copy (key-major mode)
+        "bwd_pre": ("hbm", 2 * qkv + bnhl * 4 + (2 * qkv if mode == "main" else 0)
+                    + (2 * b2b if mode == "key-major" else 0)),
         "bwd_dq_cast": ("hbm", 2 * qkv + qkv),
-        "bwd_db2_sum": ("hbm", 0),
+        "bwd_db2_sum": ("hbm", bias2_groups(w) * w.B * w.H * w.L * w.L * 4 + b2b if has_b2 else 0),
     }
-    if has_b2:
-        import ctypes  # noqa: F401
-        groups = (ws_bytes - (bnhl * 4 + 2 * qkv)) // (w.B * w.H * w.L * w.L * 4)
-        work["bwd_db2_sum"] = ("hbm", groups * w.B * w.H * w.L * w.L * 4 + b2b)
     dom = max(kern_ms, key=kern_ms.get)
     bound, amount = work[dom]
     if bound == "tensor":
