@@ -60,7 +60,7 @@
 extern "C" {
 #endif
 
-#define EVO_ATTN_ABI_VERSION 1
+#define EVO_ATTN_ABI_VERSION 2
 
 /* Every entry point below is exported from libevo_attn.so; nothing else is. */
 #if defined(__GNUC__)
@@ -111,13 +111,21 @@ EVO_API evo_status_t evo_attn_fwd(const void* q, const void* k, const void* v,
                           void* out, float* lse,
                           evo_shape_t shape, evo_dtype_t dtype, void* stream);
 
+/* Flags of evo_attn_bwd_workspace_bytes (bit 0 keeps the meaning of the
+ * former has_bias2 argument, so passing 0 / 1 still works). */
+#define EVO_WS_BIAS2 1  /* the call has a pair bias (and computes dbias2)  */
+#define EVO_WS_DBIAS1 2 /* the call computes dbias1 (evo_attn_bwd_ex)       */
+
 /*
  * Bytes of device workspace the backward needs for this problem (0 on a bad
- * shape).  It holds the fp32 row terms delta [B,N,H,L], the fp32 dQ
- * accumulator [B,N,L,H,D] and, when has_bias2 != 0, the fp32 per-group
- * partial sums of the pair-bias gradient.  Depends only on its arguments.
+ * shape or dtype).  It holds the fp32 row terms delta [B,N,H,L]; the fp32 dQ
+ * accumulator [B,N,L,H,D] for the shapes whose dQ tiles do not fit in tensor
+ * memory; with EVO_WS_BIAS2, the fp32 per-group partial sums of the pair-bias
+ * gradient and, where a key-major kernel runs, a transposed copy of the pair
+ * bias; with EVO_WS_DBIAS1, fp32 per-(b, n, h) partial sums of the key-mask
+ * gradient.  Depends only on its arguments.
  */
-EVO_API size_t evo_attn_bwd_workspace_bytes(evo_shape_t shape, evo_dtype_t dtype, int has_bias2);
+EVO_API size_t evo_attn_bwd_workspace_bytes(evo_shape_t shape, evo_dtype_t dtype, int flags);
 
 /*
  * Backward (page §3.7: delta first, then dQ/dK/dV and the bias gradient).
@@ -132,7 +140,7 @@ EVO_API size_t evo_attn_bwd_workspace_bytes(evo_shape_t shape, evo_dtype_t dtype
  *                           groups), so repeated calls give identical bytes;
  *   workspace             : >= evo_attn_bwd_workspace_bytes(...) bytes, caller-owned,
  *                           contents need not be initialised; clobbered.
- * The gradient of bias1 is not produced by this version.
+ * The gradient of bias1 is produced by evo_attn_bwd_ex.
  */
 EVO_API evo_status_t evo_attn_bwd(const void* q, const void* k, const void* v,
                           const void* bias1, const void* bias2,
@@ -140,6 +148,24 @@ EVO_API evo_status_t evo_attn_bwd(const void* q, const void* k, const void* v,
                           void* dq, void* dk, void* dv, void* dbias2,
                           void* workspace, size_t workspace_bytes,
                           evo_shape_t shape, evo_dtype_t dtype, void* stream);
+
+/*
+ * evo_attn_bwd plus the key-mask gradient (page §3.7: the backward returns the
+ * gradients of both biases):
+ *   dbias1 : [B,N,1,1,L] output in dtype, or NULL (then exactly evo_attn_bwd).
+ *            dbias1[b,n,j] = Σ_h Σ_i dS[b,n,h,i,j], summed in fp32 in a fixed
+ *            order (per-(b,n,h) partials, then a fixed-order sum over h), so
+ *            repeated calls give identical bytes.  Requires bias1 != NULL.
+ *   workspace : >= evo_attn_bwd_workspace_bytes(shape, dtype,
+ *               (bias2 ? EVO_WS_BIAS2 : 0) | (dbias1 ? EVO_WS_DBIAS1 : 0)).
+ * Errors as evo_attn_bwd; EVO_ERR_BAD_ARGUMENT if dbias1 is given without bias1.
+ */
+EVO_API evo_status_t evo_attn_bwd_ex(const void* q, const void* k, const void* v,
+                             const void* bias1, const void* bias2,
+                             const void* out, const float* lse, const void* dout,
+                             void* dq, void* dk, void* dv, void* dbias1, void* dbias2,
+                             void* workspace, size_t workspace_bytes,
+                             evo_shape_t shape, evo_dtype_t dtype, void* stream);
 
 /*
  * Synchronises `stream`, then reads and clears the library's device status

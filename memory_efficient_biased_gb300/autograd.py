@@ -1,0 +1,52 @@
+"""PyTorch autograd over the C ABI: ``evoformer_attention(q, k, v, biases)``.
+
+The call form of the pages' ``DS4Sci_EvoformerAttention(Q, K, V, biases)``
+(web page "DeepSpeed4Science 技术指南…" §3.6–§3.7): q, k, v are [B, N, L, H, D]
+fp16/bf16 CUDA tensors, ``biases`` a list of at most two tensors — the key mask
+[B, N, 1, 1, L] and the pair bias [B, 1, H, L, L], either may be None or left out.
+The forward saves O and the fp32 log-sum-exp; the backward returns the gradients
+of q, k, v and of whichever biases require them (§3.7: both bias gradients).
+Every step runs in the library's sm_103a kernels; there is no fallback.
+"""
+from typing import List, Optional
+
+import torch
+
+from . import evo_attn as E
+
+
+class EvoformerAttentionFunction(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, q, k, v, bias1, bias2):
+        q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
+        bias1 = None if bias1 is None else bias1.contiguous()
+        bias2 = None if bias2 is None else bias2.contiguous()
+        out, lse = E.evo_attn_fwd(q, k, v, bias1, bias2)
+        ctx.save_for_backward(q, k, v, bias1, bias2, out, lse)
+        return out
+
+    @staticmethod
+    def backward(ctx, dout):
+        q, k, v, bias1, bias2, out, lse = ctx.saved_tensors
+        dout = dout.contiguous()
+        want_db1 = bias1 is not None and ctx.needs_input_grad[3]
+        if want_db1:
+            dq, dk, dv, db1, db2 = E.evo_attn_bwd_ex(q, k, v, bias1, bias2, out, lse, dout)
+        else:
+            dq, dk, dv, db2 = E.evo_attn_bwd(q, k, v, bias1, bias2, out, lse, dout)
+            db1 = None
+        return dq, dk, dv, db1, (db2 if ctx.needs_input_grad[4] else None)
+
+
+def evoformer_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                        biases: Optional[List[Optional[torch.Tensor]]] = None) -> torch.Tensor:
+    """softmax(q kᵀ D^-1/2 + bias1 + bias2) v over [B, N, L, H, D], differentiable."""
+    biases = list(biases or [])
+    if len(biases) > 2:
+        raise ValueError("at most two biases: the key mask [B,N,1,1,L] and the pair bias [B,1,H,L,L]")
+    biases += [None] * (2 - len(biases))
+    return EvoformerAttentionFunction.apply(q, k, v, biases[0], biases[1])
+
+
+# The pages' name for the same call.
+DS4Sci_EvoformerAttention = evoformer_attention

@@ -1694,7 +1694,7 @@ cudaError_t launch_bwd_d(BwdArgs a, cudaStream_t st, const ProfileEvents* prof) 
   const BwdPlan plan = bwd_plan(DP, a.QT, has_b2);
   const int slice_qs = plan.mode == kBwdSlice ? plan.q_stages : 0;
   a.zero_dq = plan.mode == kBwdMain;
-  if (plan.mode != kBwdKeyMajor) a.b2t = nullptr;
+  if (plan.mode != kBwdKeyMajor && !a.db1p) a.b2t = nullptr;
   prof_record(prof, 2, st);
   evo_bwd_pre<DP, BF16><<<grid_for(rows, 256), 256, 0, st>>>(a);
   cudaError_t e = cudaGetLastError();
@@ -1738,6 +1738,11 @@ cudaError_t launch_bwd_d(BwdArgs a, cudaStream_t st, const ProfileEvents* prof) 
   prof_record(prof, 5, st);
   }
 
+  if (a.db1p) {  // key-mask gradient: partials (by the key-major kernel, or a separate pass), then the sum
+    if (plan.mode != kBwdKeyMajor && (e = launch_bwd_db1_partials(a, DP, BF16, has_b2, st)) != cudaSuccess)
+      return e;
+    if ((e = launch_bwd_db1_sum(a, BF16, st)) != cudaSuccess) return e;
+  }
   if (has_b2) {
     // deepest ring that fits; staging for tile stores of the partials when it fits too
     auto pfits = [&](int ns, bool stg) { return PartLayout<DP>(ns, stg).total + 1024 <= kMaxSmem; };

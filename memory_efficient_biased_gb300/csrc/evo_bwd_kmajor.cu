@@ -48,6 +48,7 @@ struct KmBars {
   uint64_t q_full[kKmMaxQS], q_empty[kKmMaxQS];
   uint64_t st_full, st_free, pds_full, buf_free[2];
   uint64_t dkdv_full[2], dkdv_free[2], dq_full, dq_free;
+  uint64_t sd_full[2], sd_free[2];  // key-mask gradient pass: Sᵀ / dPᵀ double buffer
   uint64_t drain;
   uint32_t tmem_slot;
   int abort;
@@ -58,12 +59,14 @@ struct KmLayout {
   static constexpr uint32_t kTB = kTile * DP * 2;
   Ring ds, stg, b2t, k, v, q, d_o, b1, ld;
   uint32_t bars, total;
-  __host__ __device__ KmLayout(bool has_b2, int qs) {
+  // grads: the full backward (dS tiles and output staging); without, the key-mask
+  // gradient pass that only recomputes dS
+  __host__ __device__ KmLayout(bool has_b2, int qs, bool grads = true) {
     uint32_t off = 0;
     ds = Ring{off, 32768u};  // 128B-swizzled tiles first (1024-byte aligned)
-    off += 2 * 32768u;
+    if (grads) off += 2 * 32768u;
     stg = Ring{off, kTB};    // staging of finished dK / dV / dQ: per warp two [32][DP/2] blocks
-    off += 2 * kTB;
+    if (grads) off += 2 * kTB;
     b2t = Ring{off, 32768u};
     if (has_b2) off += qs * 32768u;
     k = Ring{off, 2 * kTB};
@@ -330,10 +333,11 @@ __device__ __forceinline__ void km_mma(const BwdArgs& a, uint8_t* base, const Km
 
 // Pᵀ for 32 queries of this thread's key into TMEM (packed pairs) and dS into
 // the swizzled smem tile.  nl / nd: −lse·log2e and −delta of the 32 queries.
-template <bool BF16, bool HAS_B2>
+// DB1: also add this thread's dS values into dsum (the key's share of the key-mask gradient).
+template <bool BF16, bool HAS_B2, bool DB1>
 __device__ __forceinline__ void km_chunk(const uint32_t (&sv)[32], const uint32_t (&pv)[32], float b1j,
                                          const float* nl, const float* nd, const uint8_t* b2half, uint8_t* dshalf,
-                                         uint32_t p_tcol, int r, int c, float2 sl2) {
+                                         uint32_t p_tcol, int r, int c, float2 sl2, float2& dsum) {
   const float2 mk = make_float2(b1j, b1j), l2e2 = make_float2(kLog2e, kLog2e);
   uint32_t pp[16], dd[16];
 #pragma unroll
@@ -358,6 +362,7 @@ __device__ __forceinline__ void km_chunk(const uint32_t (&sv)[32], const uint32_
       const float p0 = ex2(t.x), p1 = ex2(t.y);
       const float2 dpd = add2(make_float2(__uint_as_float(pv[x]), __uint_as_float(pv[x + 1])), nd2[e2]);
       const float2 ds = mul2(make_float2(p0, p1), dpd);
+      if (DB1) dsum = add2(dsum, ds);
       pp[q * 4 + e2] = pack2<BF16>(p0, p1);
       dd[q * 4 + e2] = pack2<BF16>(ds.x, ds.y);
     }
@@ -490,7 +495,13 @@ __device__ __forceinline__ bool km_write_dq(const BwdArgs& a, const SlIter& c, u
   return true;
 }
 
-template <int DP, bool BF16, bool HAS_B2>
+// Key-mask gradient partial of key j of slice c, query half hc: [B·N·H][2][L] fp32.
+__device__ __forceinline__ void km_store_db1(const BwdArgs& a, const SlIter& c, int hc, int j, float v) {
+  if (j < a.L)
+    a.db1p[((static_cast<size_t>(c.b * a.N + c.n) * a.H + c.h) * 2 + hc) * a.L + j] = v;
+}
+
+template <int DP, bool BF16, bool HAS_B2, bool DB1>
 __device__ __forceinline__ void km_compute(const BwdArgs& a, uint8_t* base, const KmLayout<DP>& lay, KmBars* bars,
                                            uint32_t tmem, const WaitGuard& g, long long i0, long long i1) {
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -504,6 +515,7 @@ __device__ __forceinline__ void km_compute(const BwdArgs& a, uint8_t* base, cons
   cur.init(i0, a);
   prev = cur;
   float b1j = 0.0f;
+  float2 dsum = make_float2(0.0f, 0.0f);  // DB1: Σ over the key tile's queries of this key's dS
   bool ok = true;
   for (long long item = i0; ok && item < i1; ++item, ++slice) {
     if (item > i0) {
@@ -533,7 +545,7 @@ __device__ __forceinline__ void km_compute(const BwdArgs& a, uint8_t* base, cons
           tmem_ld32(trow + kKmDP + hc * 64, pv);
           tmem_wait_ld(sv);
           tmem_wait_ld(pv);
-          km_chunk<BF16, HAS_B2>(sv, pv, b1j, ld, ld + 128, b2half, dshalf, pcol, r, 0, sl2);
+          km_chunk<BF16, HAS_B2, DB1>(sv, pv, b1j, ld, ld + 128, b2half, dshalf, pcol, r, 0, sl2, dsum);
         }
         {
           uint32_t sv[32], pv[32];
@@ -544,7 +556,8 @@ __device__ __forceinline__ void km_compute(const BwdArgs& a, uint8_t* base, cons
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&bars->st_free));
-          km_chunk<BF16, HAS_B2>(sv, pv, b1j, ld + 32, ld + 160, b2half, dshalf, pcol + 16, r, 1, sl2);
+          km_chunk<BF16, HAS_B2, DB1>(sv, pv, b1j, ld + 32, ld + 160, b2half, dshalf, pcol + 16, r, 1, sl2,
+                                      dsum);
         }
         tmem_wait_st();
         tc_fence_before();
@@ -557,6 +570,10 @@ __device__ __forceinline__ void km_compute(const BwdArgs& a, uint8_t* base, cons
         if (++s == static_cast<uint32_t>(QS)) {
           s = 0;
           ph ^= 1;
+        }
+        if (DB1 && it == QT - 1) {  // this key's share over the slice's queries, per query half
+          km_store_db1(a, cur, hc, jt * kTile + r, dsum.x + dsum.y);
+          dsum = make_float2(0.0f, 0.0f);
         }
         // one step late (their MMAs are done by now): dK/dV of the previous key tile and,
         // at a slice boundary, the previous slice's dQ
@@ -581,7 +598,7 @@ __device__ __forceinline__ void km_compute(const BwdArgs& a, uint8_t* base, cons
   if (lane == 0) bulk_wait_all();  // this warp's tile stores complete before the CTA's smem goes away
 }
 
-template <int DP, bool BF16, bool HAS_B2>
+template <int DP, bool BF16, bool HAS_B2, bool DB1>
 __global__ void __launch_bounds__(kThreads, 1) evo_bwd_kmajor(const __grid_constant__ BwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -635,7 +652,7 @@ __global__ void __launch_bounds__(kThreads, 1) evo_bwd_kmajor(const __grid_const
     if (lane == 0) km_mma<DP, BF16>(a, base, lay, bars, tmem, g, i0, i1);
     __syncwarp();
   } else {
-    km_compute<DP, BF16, HAS_B2>(a, base, lay, bars, tmem, g, i0, i1);
+    km_compute<DP, BF16, HAS_B2, DB1>(a, base, lay, bars, tmem, g, i0, i1);
   }
   tc_fence_before();
   __syncthreads();
@@ -645,19 +662,229 @@ __global__ void __launch_bounds__(kThreads, 1) evo_bwd_kmajor(const __grid_const
   }
 }
 
-template <int DP>
-int km_stages(int QT, bool has_b2) {
-  if (!km_tmem_fits(DP, QT)) return 0;
-  for (int qs = kKmMaxQS; qs >= 2; --qs)
-    if (KmLayout<DP>(has_b2, qs).total + 1024 <= kMaxSmem) return qs;
-  return 0;
+// ============================================================ key-mask gradient pass
+// For the schedules whose main kernel does not produce the key-mask gradient:
+// the key-major score recompute alone (Sᵀ, dPᵀ double-buffered in TMEM), each
+// thread summing its key's dS over the slice's queries; same producer, same
+// partial layout as the key-major kernel with DB1.
+
+template <bool BF16, bool HAS_B2>
+__device__ __forceinline__ void km_chunk_sum(const uint32_t (&sv)[32], const uint32_t (&pv)[32], float b1j,
+                                             const float* nl, const float* nd, const uint8_t* b2half, int r, int c,
+                                             float2 sl2, float2& dsum) {
+  const float2 mk = make_float2(b1j, b1j), l2e2 = make_float2(kLog2e, kLog2e);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float4 l0 = *reinterpret_cast<const float4*>(nl + q * 8);
+    const float4 l1 = *reinterpret_cast<const float4*>(nl + q * 8 + 4);
+    const float4 d0 = *reinterpret_cast<const float4*>(nd + q * 8);
+    const float4 d1 = *reinterpret_cast<const float4*>(nd + q * 8 + 4);
+    const float2 nl2[4] = {make_float2(l0.x, l0.y), make_float2(l0.z, l0.w), make_float2(l1.x, l1.y),
+                           make_float2(l1.z, l1.w)};
+    const float2 nd2[4] = {make_float2(d0.x, d0.y), make_float2(d0.z, d0.w), make_float2(d1.x, d1.y),
+                           make_float2(d1.z, d1.w)};
+    uint4 pb = make_uint4(0u, 0u, 0u, 0u);
+    if (HAS_B2) pb = *reinterpret_cast<const uint4*>(b2half + swz_offset(r, c * 4 + q, 128));
+    const uint32_t pw[4] = {pb.x, pb.y, pb.z, pb.w};
+#pragma unroll
+    for (int e2 = 0; e2 < 4; ++e2) {
+      const int x = q * 8 + e2 * 2;
+      float2 t = fma2(make_float2(__uint_as_float(sv[x]), __uint_as_float(sv[x + 1])), sl2, mk);
+      if (HAS_B2) t = fma2(unpack2<BF16>(pw[e2]), l2e2, t);
+      t = add2(t, nl2[e2]);
+      const float2 dpd = add2(make_float2(__uint_as_float(pv[x]), __uint_as_float(pv[x + 1])), nd2[e2]);
+      dsum = fma2(make_float2(ex2(t.x), ex2(t.y)), dpd, dsum);
+    }
+  }
+}
+
+template <int DP, bool BF16>
+__device__ __forceinline__ void km_db1_mma(const BwdArgs& a, uint8_t* base, const KmLayout<DP>& lay, KmBars* bars,
+                                           uint32_t tmem, const WaitGuard& g, long long i0, long long i1) {
+  constexpr uint32_t RB = DP * 2;
+  constexpr uint32_t SWZ = swizzle_for_row(RB);
+  constexpr uint32_t id_s = idesc_f16(128, 128, BF16, false, false);
+  const int QS = a.q_stages, QT = a.QT;
+  uint32_t u = 0, grp = 0, qs = 0, qph = 0;
+  bool ok = true;
+  for (long long item = i0; ok && item < i1; ++item) {
+    for (int jt = 0; ok && jt < QT; ++jt, ++grp) {
+      const uint32_t kb = grp & 1;
+      for (int it = 0; it < QT; ++it, ++u) {
+        const uint32_t b = u & 1;
+        if (it == 0 && !mbar_wait(smem_u32(&bars->kv_full[kb]), (grp >> 1) & 1, g)) { ok = false; break; }
+        if (!mbar_wait(smem_u32(&bars->q_full[qs]), qph, g)) { ok = false; break; }
+        if (!mbar_wait(smem_u32(&bars->sd_free[b]), ((u >> 1) & 1) ^ 1, g)) { ok = false; break; }
+        tc_fence_after();
+        const uint64_t kd = smem_desc(smem_u32(base + lay.k[kb]), 16, 8 * RB, SWZ);
+        const uint64_t vd = smem_desc(smem_u32(base + lay.v[kb]), 16, 8 * RB, SWZ);
+        const uint64_t qd = smem_desc(smem_u32(base + lay.q[qs]), 16, 8 * RB, SWZ);
+        const uint64_t dod = smem_desc(smem_u32(base + lay.d_o[qs]), 16, 8 * RB, SWZ);
+#pragma unroll
+        for (int k = 0; k < DP / 16; ++k) umma_ss(tmem + b * 256u, kd + k * 2, qd + k * 2, id_s, k > 0);
+#pragma unroll
+        for (int k = 0; k < DP / 16; ++k) umma_ss(tmem + b * 256u + 128u, vd + k * 2, dod + k * 2, id_s, k > 0);
+        umma_commit(smem_u32(&bars->sd_full[b]));
+        umma_commit(smem_u32(&bars->q_empty[qs]));
+        if (it == QT - 1) umma_commit(smem_u32(&bars->kv_empty[kb]));
+        if (++qs == static_cast<uint32_t>(QS)) {
+          qs = 0;
+          qph ^= 1;
+        }
+      }
+    }
+  }
+  umma_commit(smem_u32(&bars->drain));
+  drain_wait(smem_u32(&bars->drain), 0, a.wait_ns, a.status);
 }
 
 template <int DP, bool BF16, bool HAS_B2>
-cudaError_t launch_km(BwdArgs a, cudaStream_t st) {
-  const KmLayout<DP> lay(HAS_B2, a.q_stages);
+__device__ __forceinline__ void km_db1_compute(const BwdArgs& a, uint8_t* base, const KmLayout<DP>& lay,
+                                               KmBars* bars, uint32_t tmem, const WaitGuard& g, long long i0,
+                                               long long i1) {
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int quad = w & 3, hc = w >> 2;
+  const int r = quad * 32 + lane;
+  const uint32_t trow = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+  const float2 sl2 = make_float2(a.scale_log2, a.scale_log2);
+  const int QS = a.q_stages, QT = a.QT;
+  uint32_t u = 0, grp = 0, s = 0, ph = 0;
+  SlIter cur;
+  cur.init(i0, a);
+  float b1j = 0.0f;
+  float2 dsum = make_float2(0.0f, 0.0f);
+  bool ok = true;
+  for (long long item = i0; ok && item < i1; ++item) {
+    if (item > i0) cur.next(a);
+    for (int jt = 0; ok && jt < QT; ++jt, ++grp) {
+      const uint32_t kb = grp & 1;
+      for (int it = 0; it < QT; ++it, ++u) {
+        const uint32_t b = u & 1;
+        if (it == 0) {
+          if (!mbar_wait(smem_u32(&bars->kv_full[kb]), (grp >> 1) & 1, g)) { ok = false; break; }
+          b1j = reinterpret_cast<const float*>(base + lay.b1[kb])[r];
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&bars->kv_empty[kb]));
+        }
+        if (!mbar_wait(smem_u32(&bars->q_full[s]), ph, g)) { ok = false; break; }
+        if (!mbar_wait(smem_u32(&bars->sd_full[b]), (u >> 1) & 1, g)) { ok = false; break; }
+        tc_fence_after();
+        const float* ld = reinterpret_cast<const float*>(base + lay.ld[s]) + hc * 64;
+        const uint8_t* b2half = base + lay.b2t[s] + hc * 16384;
+        const uint32_t cs = trow + b * 256u + hc * 64, cp = cs + 128u;
+        {
+          uint32_t sv[32], pv[32];
+          tmem_ld32(cs, sv);
+          tmem_ld32(cp, pv);
+          tmem_wait_ld(sv);
+          tmem_wait_ld(pv);
+          km_chunk_sum<BF16, HAS_B2>(sv, pv, b1j, ld, ld + 128, b2half, r, 0, sl2, dsum);
+        }
+        {
+          uint32_t sv[32], pv[32];
+          tmem_ld32(cs + 32, sv);
+          tmem_ld32(cp + 32, pv);
+          tmem_wait_ld(sv);
+          tmem_wait_ld(pv);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&bars->sd_free[b]));
+          km_chunk_sum<BF16, HAS_B2>(sv, pv, b1j, ld + 32, ld + 160, b2half, r, 1, sl2, dsum);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bars->q_empty[s]));
+        if (++s == static_cast<uint32_t>(QS)) {
+          s = 0;
+          ph ^= 1;
+        }
+        if (it == QT - 1) {
+          km_store_db1(a, cur, hc, jt * kTile + r, dsum.x + dsum.y);
+          dsum = make_float2(0.0f, 0.0f);
+        }
+      }
+    }
+  }
+}
+
+template <int DP, bool BF16, bool HAS_B2>
+__global__ void __launch_bounds__(kThreads, 1) evo_bwd_db1(const __grid_constant__ BwdArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const KmLayout<DP> lay(HAS_B2, a.q_stages, false);
+  KmBars* bars = reinterpret_cast<KmBars*>(base + lay.bars);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long i0 = static_cast<long long>(blockIdx.x) * a.chunk;
+  const long long i1 = i0 + a.chunk < a.items ? i0 + a.chunk : a.items;
+  if (threadIdx.x == 0) {
+    bars->abort = 0;
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_u32(&bars->kv_full[s]), 32);
+      mbar_init(smem_u32(&bars->kv_empty[s]), 1 + kComputeWarps);
+      mbar_init(smem_u32(&bars->sd_full[s]), 1);
+      mbar_init(smem_u32(&bars->sd_free[s]), kComputeWarps);
+    }
+    for (int s = 0; s < kKmMaxQS; ++s) {
+      mbar_init(smem_u32(&bars->q_full[s]), 32);
+      mbar_init(smem_u32(&bars->q_empty[s]), 1 + kComputeWarps);
+    }
+    mbar_init(smem_u32(&bars->drain), 1);
+    fence_barrier_init();
+  }
+  if (warp == kProducerWarp && lane == 0) {
+    tma_prefetch_desc(&a.tq);
+    tma_prefetch_desc(&a.tk);
+    tma_prefetch_desc(&a.tv);
+    tma_prefetch_desc(&a.tdo);
+    if (HAS_B2) tma_prefetch_desc(&a.tb2t);
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(&bars->tmem_slot), 512);
+    tmem_relinquish();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_slot;
+  const WaitGuard g{a.wait_ns, a.status, &bars->abort};
+  if (warp == kProducerWarp) {
+    km_producer<DP, BF16, HAS_B2>(a, base, lay, bars, g, lane, i0, i1);
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) km_db1_mma<DP, BF16>(a, base, lay, bars, tmem, g, i0, i1);
+    __syncwarp();
+  } else {
+    km_db1_compute<DP, BF16, HAS_B2>(a, base, lay, bars, tmem, g, i0, i1);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// dbias1[b,n,j] = Σ_h Σ_half partial[b,n,h,half,j] in this fixed order, rounded to the dtype.
+template <bool BF16>
+__global__ void __launch_bounds__(256) evo_bwd_db1_sum(const BwdArgs a) {
+  const long long total = static_cast<long long>(a.B) * a.N * a.L;
+  for (long long e = blockIdx.x * 256ll + threadIdx.x; e < total; e += gridDim.x * 256ll) {
+    const long long bn = e / a.L;
+    const int j = static_cast<int>(e - bn * a.L);
+    const float* p = a.db1p + bn * a.H * 2 * a.L + j;
+    float sum = 0.0f;
+    for (int t = 0; t < 2 * a.H; ++t) sum += p[static_cast<size_t>(t) * a.L];
+    a.dbias1[e] = static_cast<uint16_t>(pack2<BF16>(sum, 0.0f) & 0xFFFFu);
+  }
+}
+
+template <int DP, bool BF16, bool HAS_B2>
+cudaError_t launch_db1(BwdArgs a, cudaStream_t st) {
+  int qs = 0;
+  for (int q = kKmMaxQS; q >= 2 && qs == 0; --q)
+    if (KmLayout<DP>(HAS_B2, q, false).total + 1024 <= kMaxSmem) qs = q;
+  if (qs == 0) return cudaErrorInvalidValue;
+  a.q_stages = qs;
+  const KmLayout<DP> lay(HAS_B2, qs, false);
   const size_t smem = one_cta_per_sm(lay.total + 1024);
-  auto kern = evo_bwd_kmajor<DP, BF16, HAS_B2>;
+  auto kern = evo_bwd_db1<DP, BF16, HAS_B2>;
   static bool limit_set[64] = {};
   cudaError_t e = ensure_smem_limit(kern, kMaxSmem, limit_set);
   if (e != cudaSuccess) return e;
@@ -670,9 +897,44 @@ cudaError_t launch_km(BwdArgs a, cudaStream_t st) {
 }
 
 template <int DP>
+cudaError_t launch_db1_d(const BwdArgs& a, bool bf16, bool has_b2, cudaStream_t st) {
+  if (bf16) return has_b2 ? launch_db1<DP, true, true>(a, st) : launch_db1<DP, true, false>(a, st);
+  return has_b2 ? launch_db1<DP, false, true>(a, st) : launch_db1<DP, false, false>(a, st);
+}
+
+template <int DP>
+int km_stages(int QT, bool has_b2) {
+  if (!km_tmem_fits(DP, QT)) return 0;
+  for (int qs = kKmMaxQS; qs >= 2; --qs)
+    if (KmLayout<DP>(has_b2, qs).total + 1024 <= kMaxSmem) return qs;
+  return 0;
+}
+
+template <int DP, bool BF16, bool HAS_B2, bool DB1>
+cudaError_t launch_km(BwdArgs a, cudaStream_t st) {
+  const KmLayout<DP> lay(HAS_B2, a.q_stages);
+  const size_t smem = one_cta_per_sm(lay.total + 1024);
+  auto kern = evo_bwd_kmajor<DP, BF16, HAS_B2, DB1>;
+  static bool limit_set[64] = {};
+  cudaError_t e = ensure_smem_limit(kern, kMaxSmem, limit_set);
+  if (e != cudaSuccess) return e;
+  a.items = static_cast<long long>(a.B) * a.H * a.N;
+  const long long sms = num_sms();
+  a.chunk = (a.items + sms - 1) / sms;
+  const long long grid = (a.items + a.chunk - 1) / a.chunk;
+  kern<<<static_cast<unsigned>(grid), kThreads, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+template <int DP, bool BF16>
+cudaError_t launch_km_b(const BwdArgs& a, bool has_b2, cudaStream_t st) {
+  if (a.db1p) return has_b2 ? launch_km<DP, BF16, true, true>(a, st) : launch_km<DP, BF16, false, true>(a, st);
+  return has_b2 ? launch_km<DP, BF16, true, false>(a, st) : launch_km<DP, BF16, false, false>(a, st);
+}
+
+template <int DP>
 cudaError_t launch_km_d(const BwdArgs& a, bool bf16, bool has_b2, cudaStream_t st) {
-  if (bf16) return has_b2 ? launch_km<DP, true, true>(a, st) : launch_km<DP, true, false>(a, st);
-  return has_b2 ? launch_km<DP, false, true>(a, st) : launch_km<DP, false, false>(a, st);
+  return bf16 ? launch_km_b<DP, true>(a, has_b2, st) : launch_km_b<DP, false>(a, has_b2, st);
 }
 
 }  // namespace
@@ -683,6 +945,27 @@ int kmajor_q_stages(int DP, int QT, bool has_b2) {
     case 32: return km_stages<32>(QT, has_b2);
     default: return 0;
   }
+}
+
+cudaError_t launch_bwd_db1_partials(const BwdArgs& a, int DP, bool bf16, bool has_b2, cudaStream_t st) {
+  switch (DP) {
+    case 16: return launch_db1_d<16>(a, bf16, has_b2, st);
+    case 32: return launch_db1_d<32>(a, bf16, has_b2, st);
+    case 64: return launch_db1_d<64>(a, bf16, has_b2, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_bwd_db1_sum(const BwdArgs& a, bool bf16, cudaStream_t st) {
+  const long long total = static_cast<long long>(a.B) * a.N * a.L;
+  long long grid = (total + 255) / 256;
+  const long long cap = static_cast<long long>(num_sms()) * 8;
+  if (grid > cap) grid = cap;
+  if (bf16)
+    evo_bwd_db1_sum<true><<<static_cast<unsigned>(grid), 256, 0, st>>>(a);
+  else
+    evo_bwd_db1_sum<false><<<static_cast<unsigned>(grid), 256, 0, st>>>(a);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_kmajor(const BwdArgs& a, int DP, bool bf16, bool has_b2, cudaStream_t st) {

@@ -198,13 +198,15 @@ void bwd_groups(const evo_shape_t& s, int* groups, int* group_size) {
 int b2t_pitch(const evo_shape_t& s) { return static_cast<int>((s.L + 7) / 8 * 8); }
 
 // Backward workspace: delta always; the fp32 dQ accumulator only for the
-// per-key-tile kernel; the transposed pair bias only for the key-major kernel;
-// the pair-bias partial planes whenever there is a pair bias.
+// per-key-tile kernel; the transposed pair bias wherever a key-major kernel
+// reads it (the key-major schedule, or the key-mask gradient pass); the
+// key-mask gradient partials when dbias1 is wanted; the pair-bias partial
+// planes whenever there is a pair bias.
 struct WsLayout {
   BwdPlan plan;
-  size_t delta, dq_acc, b2t, db2, total;
+  size_t delta, dq_acc, b2t, db1p, db2, total;
 };
-WsLayout ws_layout(const evo_shape_t& s, bool has_bias2) {
+WsLayout ws_layout(const evo_shape_t& s, bool has_bias2, bool has_db1 = false) {
   WsLayout w{};
   w.plan = bwd_plan(padded_dim(s.D), static_cast<int>((s.L + kTile - 1) / kTile), has_bias2);
   size_t off = 0;
@@ -213,7 +215,10 @@ WsLayout ws_layout(const evo_shape_t& s, bool has_bias2) {
   w.dq_acc = off;
   if (w.plan.mode == kBwdMain) off += round256(size_t(s.B) * s.N * s.L * s.H * s.D * 4);
   w.b2t = off;
-  if (w.plan.mode == kBwdKeyMajor && has_bias2) off += round256(size_t(s.B) * s.H * s.L * b2t_pitch(s) * 2);
+  if ((w.plan.mode == kBwdKeyMajor || has_db1) && has_bias2)
+    off += round256(size_t(s.B) * s.H * s.L * b2t_pitch(s) * 2);
+  w.db1p = off;
+  if (has_db1) off += round256(size_t(s.B) * s.N * s.H * 2 * s.L * 4);
   w.db2 = off;
   if (has_bias2) {
     int g = 0, gs = 0;
@@ -335,37 +340,46 @@ evo_status_t evo_attn_fwd(const void* q, const void* k, const void* v, const voi
   return e == cudaSuccess ? EVO_OK : EVO_ERR_CUDA;
 }
 
-size_t evo_attn_bwd_workspace_bytes(evo_shape_t shape, evo_dtype_t dtype, int has_bias2) {
+size_t evo_attn_bwd_workspace_bytes(evo_shape_t shape, evo_dtype_t dtype, int flags) {
   if (dtype != EVO_F16 && dtype != EVO_BF16) return 0;
   if (check_shape(shape) != EVO_OK) return 0;
-  return ws_layout(shape, has_bias2 != 0).total;
+  return ws_layout(shape, (flags & EVO_WS_BIAS2) != 0, (flags & EVO_WS_DBIAS1) != 0).total;
 }
 
 evo_status_t evo_attn_bwd(const void* q, const void* k, const void* v, const void* bias1, const void* bias2,
                           const void* out, const float* lse, const void* dout, void* dq, void* dk, void* dv,
                           void* dbias2, void* workspace, size_t workspace_bytes, evo_shape_t shape,
                           evo_dtype_t dtype, void* stream) {
+  return evo_attn_bwd_ex(q, k, v, bias1, bias2, out, lse, dout, dq, dk, dv, nullptr, dbias2, workspace,
+                         workspace_bytes, shape, dtype, stream);
+}
+
+evo_status_t evo_attn_bwd_ex(const void* q, const void* k, const void* v, const void* bias1, const void* bias2,
+                             const void* out, const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                             void* dbias1, void* dbias2, void* workspace, size_t workspace_bytes,
+                             evo_shape_t shape, evo_dtype_t dtype, void* stream) {
   if (!q || !k || !v || !out || !lse || !dout || !dq || !dk || !dv || !workspace) return EVO_ERR_NULL_POINTER;
   if (dtype != EVO_F16 && dtype != EVO_BF16) return EVO_ERR_BAD_DTYPE;
   evo_status_t st = check_shape(shape);
   if (st != EVO_OK) return st;
   if ((bias2 != nullptr) != (dbias2 != nullptr)) return EVO_ERR_BAD_ARGUMENT;
+  if (dbias1 && !bias1) return EVO_ERR_BAD_ARGUMENT;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) || !aligned(dout, 16) ||
       !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(lse, 4) ||
       (bias1 && !aligned(bias1, 2)) || (bias2 && !aligned(bias2, 16)) || (dbias2 && !aligned(dbias2, 16)) ||
-      !aligned(workspace, 256))
+      (dbias1 && !aligned(dbias1, 2)) || !aligned(workspace, 256))
     return EVO_ERR_MISALIGNED;
-  const WsLayout w = ws_layout(shape, bias2 != nullptr);
+  const WsLayout w = ws_layout(shape, bias2 != nullptr, dbias1 != nullptr);
   if (workspace_bytes < w.total) return EVO_ERR_WORKSPACE_TOO_SMALL;
   const size_t nq = qkv_bytes(shape);
   const Range ins[8] = {{q, nq}, {k, nq}, {v, nq}, {bias1, bias1 ? bias1_bytes(shape) : 0},
                         {bias2, bias2 ? bias2_bytes(shape) : 0}, {out, nq}, {lse, lse_bytes(shape)}, {dout, nq}};
-  const Range outs[5] = {{dq, nq}, {dk, nq}, {dv, nq}, {dbias2, dbias2 ? bias2_bytes(shape) : 0},
-                         {workspace, w.total}};
-  for (int i = 0; i < 5; ++i) {
+  const Range outs[6] = {{dq, nq}, {dk, nq}, {dv, nq}, {dbias2, dbias2 ? bias2_bytes(shape) : 0},
+                         {dbias1, dbias1 ? bias1_bytes(shape) : 0}, {workspace, w.total}};
+  for (int i = 0; i < 6; ++i) {
     for (const Range& r : ins)
       if (overlap(outs[i], r)) return EVO_ERR_ALIASING;
-    for (int j = i + 1; j < 5; ++j)
+    for (int j = i + 1; j < 6; ++j)
       if (overlap(outs[i], outs[j])) return EVO_ERR_ALIASING;
   }
   DeviceInfo* dev = nullptr;
@@ -404,7 +418,11 @@ evo_status_t evo_attn_bwd(const void* q, const void* k, const void* v, const voi
   a.delta = reinterpret_cast<float*>(ws + w.delta);
   a.dq_acc = reinterpret_cast<float*>(ws + w.dq_acc);
   a.db2_part = bias2 ? reinterpret_cast<float*>(ws + w.db2) : nullptr;
-  if (bias2 && w.plan.mode == kBwdKeyMajor) {
+  if (dbias1) {
+    a.dbias1 = static_cast<uint16_t*>(dbias1);
+    a.db1p = reinterpret_cast<float*>(ws + w.db1p);
+  }
+  if (bias2 && (w.plan.mode == kBwdKeyMajor || dbias1)) {
     a.b2t = reinterpret_cast<uint16_t*>(ws + w.b2t);
     a.b2t_pitch = b2t_pitch(shape);
     if (!map_b2t(&a.tb2t, a.b2t, shape, bf16, a.b2t_pitch)) return EVO_ERR_CUDA;

@@ -52,6 +52,8 @@ struct BwdArgs {
   float* delta;             // workspace [B,N,H,L]
   float* dq_acc;            // workspace [B,N,L,H,D]
   float* db2_part;          // workspace [G][B,H,L,L]
+  uint16_t* dbias1;         // [B,N,L] or nullptr
+  float* db1p;              // workspace [B*N*H][2][L]: key-mask gradient partials (per key half of the queries)
   uint16_t* b2t;            // workspace [B,H,L,b2t_pitch]: b2t[bh][j][i] = bias2[bh][i][j] (key-major kernel)
   int b2t_pitch;            // L rounded up to a multiple of 8 (16-byte rows for TMA)
   int B, N, L, H, D;
@@ -115,6 +117,10 @@ struct BwdPlan {
 BwdPlan bwd_plan(int DP, int QT, bool has_b2);
 int kmajor_q_stages(int DP, int QT, bool has_b2);
 cudaError_t launch_bwd_kmajor(const BwdArgs& a, int DP, bool bf16, bool has_b2, cudaStream_t st);
+// Key-mask gradient partials (a.db1p) by the key-major score recompute alone, for the
+// schedules whose main kernel does not produce them; then the fixed-order sum into a.dbias1.
+cudaError_t launch_bwd_db1_partials(const BwdArgs& a, int DP, bool bf16, bool has_b2, cudaStream_t st);
+cudaError_t launch_bwd_db1_sum(const BwdArgs& a, bool bf16, cudaStream_t st);
 
 int num_sms();
 cudaError_t launch_fwd(const FwdArgs& a, int DP, bool bf16, cudaStream_t st);

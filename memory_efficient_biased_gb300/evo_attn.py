@@ -32,7 +32,7 @@ NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 EXPORTED = ("evo_attn_abi_version", "evo_status_string", "evo_attn_fwd", "evo_attn_bwd_workspace_bytes",
             "evo_attn_bwd", "evo_attn_device_status", "evo_attn_set_wait_limit_ns",
             "evo_attn_selftest_wait_timeout", "evo_attn_profile_events", "evo_attn_step_host_arena_bytes",
-            "evo_attn_step_host", "evo_attn_bwd_noalloc")
+            "evo_attn_step_host", "evo_attn_bwd_noalloc", "evo_attn_bwd_ex")
 
 _DTYPE_CODE = {torch.float16: 0, torch.bfloat16: 1}
 
@@ -90,6 +90,8 @@ def load(path: Optional[str] = None):
     lib.evo_attn_step_host.argtypes = [vp] * 13 + [sz, EvoShape, i32, vp]
     lib.evo_attn_bwd_noalloc.restype = i32
     lib.evo_attn_bwd_noalloc.argtypes = [vp] * 12 + [EvoShape, i32, vp]
+    lib.evo_attn_bwd_ex.restype = i32
+    lib.evo_attn_bwd_ex.argtypes = [vp] * 14 + [sz, EvoShape, i32, vp]
     if path is None:
         _lib = lib
     return lib
@@ -148,8 +150,12 @@ def evo_attn_fwd(q, k, v, bias1=None, bias2=None, out=None, lse=None, stream=Non
     return out, lse
 
 
-def evo_attn_bwd_workspace_bytes(shape, dtype, has_bias2: bool) -> int:
-    return int(load().evo_attn_bwd_workspace_bytes(EvoShape(*shape), _DTYPE_CODE[dtype], int(bool(has_bias2))))
+WS_BIAS2, WS_DBIAS1 = 1, 2  # flags of evo_attn_bwd_workspace_bytes
+
+
+def evo_attn_bwd_workspace_bytes(shape, dtype, has_bias2: bool, want_dbias1: bool = False) -> int:
+    flags = (WS_BIAS2 if has_bias2 else 0) | (WS_DBIAS1 if want_dbias1 else 0)
+    return int(load().evo_attn_bwd_workspace_bytes(EvoShape(*shape), _DTYPE_CODE[dtype], flags))
 
 
 def evo_attn_bwd(q, k, v, bias1, bias2, out, lse, dout, dq=None, dk=None, dv=None, dbias2=None,
@@ -183,6 +189,45 @@ def evo_attn_bwd(q, k, v, bias1, bias2, out, lse, dout, dq=None, dk=None, dv=Non
     if st != EVO_OK:
         raise EvoAttnError(st, "evo_attn_bwd")
     return dq, dk, dv, dbias2
+
+
+def evo_attn_bwd_ex(q, k, v, bias1, bias2, out, lse, dout, dq=None, dk=None, dv=None, dbias1=None, dbias2=None,
+                    workspace=None, stream=None, want_dbias1=True):
+    """evo_attn_bwd plus the key-mask gradient dbias1 [B,N,1,1,L] (requires bias1);
+    returns (dq, dk, dv, dbias1, dbias2)."""
+    B, N, L, H, D = q.shape
+    dt = q.dtype
+    if dt not in _DTYPE_CODE:
+        raise ValueError("inputs must be float16 or bfloat16")
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out"), (dout, "dout")):
+        _check(t, n, q.shape, dt)
+    _check(bias1, "bias1", (B, N, 1, 1, L), dt)
+    _check(bias2, "bias2", (B, 1, H, L, L), dt)
+    _check(lse, "lse", (B, N, H, L), torch.float32)
+    if want_dbias1 and bias1 is None:
+        raise ValueError("dbias1 needs bias1")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    if want_dbias1 and dbias1 is None:
+        dbias1 = torch.empty_like(bias1)
+    if bias2 is not None and dbias2 is None:
+        dbias2 = torch.empty_like(bias2)
+    for t, n in ((dq, "dq"), (dk, "dk"), (dv, "dv")):
+        _check(t, n, q.shape, dt)
+    _check(dbias1, "dbias1", (B, N, 1, 1, L), dt)
+    _check(dbias2, "dbias2", (B, 1, H, L, L), dt)
+    need = evo_attn_bwd_workspace_bytes(tuple(q.shape), dt, bias2 is not None, dbias1 is not None)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    _check(workspace, "workspace")
+    st = load().evo_attn_bwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(bias1), _ptr(bias2), _ptr(out), _ptr(lse),
+                                _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dbias1), _ptr(dbias2),
+                                _ptr(workspace), workspace.numel() * workspace.element_size(), shape_of(q),
+                                _DTYPE_CODE[dt], _stream_ptr(stream))
+    if st != EVO_OK:
+        raise EvoAttnError(st, "evo_attn_bwd_ex")
+    return dq, dk, dv, dbias1, dbias2
 
 
 def evo_attn_device_status(stream=None) -> int:

@@ -37,7 +37,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_strings(lib):
-    assert lib.evo_attn_abi_version() == 1
+    assert lib.evo_attn_abi_version() == 2
     for code in range(11):
         s = lib.evo_status_string(code).decode()
         assert s and s != "unknown status"
@@ -98,6 +98,25 @@ def test_bwd_validation(lib):
     assert r in (6, 7) or r == 0
 
 
+def bwd_ex(lib, db1=None, b1=None, ws_bytes=None):
+    vp = lambda x: None if x is None else ctypes.c_void_p(x)
+    s = shape()
+    need = lib.evo_attn_bwd_workspace_bytes(s, 1, 2)
+    return lib.evo_attn_bwd_ex(vp(A), vp(2 * A), vp(3 * A), vp(b1), None, vp(4 * A), vp(5 * A), vp(6 * A),
+                               vp(7 * A), vp(8 * A), vp(9 * A), vp(db1), None, vp(16 * A),
+                               need if ws_bytes is None else ws_bytes, s, 1, None)
+
+
+def test_bwd_ex_validation(lib):
+    assert bwd_ex(lib, db1=11 * A) == 10                 # dbias1 without bias1
+    assert bwd_ex(lib, db1=11 * A + 1, b1=12 * A) == 4   # dbias1 must be 2-byte aligned
+    assert bwd_ex(lib, db1=7 * A, b1=12 * A) == 9         # dbias1 aliases dq
+    # the key-mask gradient needs its partials in the workspace
+    assert bwd_ex(lib, db1=11 * A, b1=12 * A, ws_bytes=lib.evo_attn_bwd_workspace_bytes(shape(), 1, 0)) == 5
+    r = bwd_ex(lib, db1=11 * A, b1=12 * A)
+    assert r in (6, 7) or r == 0
+
+
 def test_workspace_bytes(lib):
     s = shape(B=1, N=256, L=256, H=4, D=32)
     no_b2 = lib.evo_attn_bwd_workspace_bytes(s, 1, 0)
@@ -112,5 +131,7 @@ def test_workspace_bytes(lib):
     # per-key-tile backward (D = 64, L = 384): delta plus the fp32 dQ accumulator
     big = shape(B=1, N=4, L=384, H=2, D=64)
     assert lib.evo_attn_bwd_workspace_bytes(big, 1, 0) == 4 * 2 * 384 * 4 + 4 * 384 * 2 * 64 * 4
+    # EVO_WS_DBIAS1 adds the fp32 [B,N,H,2,L] key-mask gradient partials
+    assert lib.evo_attn_bwd_workspace_bytes(s, 1, 2) - no_b2 == 1 * 256 * 4 * 2 * 256 * 4
     assert lib.evo_attn_bwd_workspace_bytes(shape(D=12), 1, 0) == 0
     assert lib.evo_attn_bwd_workspace_bytes(s, 7, 0) == 0
