@@ -181,6 +181,43 @@ def dist_setup(args):
     return world, rank, local
 
 
+def memory_versus_dense(d):
+    """Peak device memory of one differentiable fwd + bwd beyond the resident inputs:
+    this library (autograd wrapper, both bias gradients) against plain PyTorch
+    attention that materialises the L×L scores (context for the pages' memory claim)."""
+    import torch
+    from memory_efficient_biased_gb300.autograd import evoformer_attention
+
+    def dense(q, k, v, b1, b2):
+        sc = torch.einsum("bnihd,bnjhd->bnhij", q, k) * (q.shape[-1] ** -0.5)
+        if b1 is not None:
+            sc = sc + b1
+        if b2 is not None:
+            sc = sc + b2
+        return torch.einsum("bnhij,bnjhd->bnihd", torch.softmax(sc, dim=-1), v)
+
+    peaks = {}
+    for name in ("ours", "dense"):
+        leaves = [None if d[n] is None else d[n].detach().clone().requires_grad_(True)
+                  for n in ("q", "k", "v", "bias1", "bias2")]
+        torch.cuda.synchronize()
+        base = torch.cuda.memory_allocated()
+        torch.cuda.reset_peak_memory_stats()
+        try:
+            q, k, v, b1, b2 = leaves
+            out = evoformer_attention(q, k, v, [b1, b2]) if name == "ours" else dense(q, k, v, b1, b2)
+            out.backward(d["do"])
+            torch.cuda.synchronize()
+            peaks[name] = torch.cuda.max_memory_allocated() - base
+        except torch.cuda.OutOfMemoryError:
+            peaks[name] = None
+        del leaves
+        out = q = k = v = b1 = b2 = None
+        torch.cuda.empty_cache()
+    ratio = peaks["dense"] / peaks["ours"] if peaks["dense"] and peaks["ours"] else None
+    return {"ours_fwd_bwd_bytes": peaks["ours"], "dense_fwd_bwd_bytes": peaks["dense"], "dense_over_ours": ratio}
+
+
 def bias2_groups(w) -> int:
     """n-groups of the two-stage pair-bias gradient: the library's rule (enough
     (b, h, query tile, key tile, group) blocks for two waves on 152 SMs)."""
@@ -302,6 +339,7 @@ def run_ours(args):
     E.evo_attn_bwd(d0["q"], d0["k"], d0["v"], d0["bias1"], d0["bias2"], out, lse, d0["do"])
     torch.cuda.synchronize()
     peak_bwd = torch.cuda.max_memory_allocated() - base
+    memory = memory_versus_dense(d0) if rank == 0 else None
     del out, lse
     if E.evo_attn_device_status() != 0:
         raise RuntimeError("device wait timed out during set-up")
@@ -451,6 +489,7 @@ def run_ours(args):
             "fwd_bwd_frac_of_peak": value / world / peaks["bf16_tflops_sustained"],
             "kernel_ms": kern_ms,
             "peak_mem_bytes": {"fwd_call": peak_fwd, "bwd_call": peak_bwd},
+            "memory_vs_dense": memory,
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": {"value": world * F["step"] / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",

@@ -93,6 +93,11 @@ typedef struct {
   int64_t B, N, L, H, D;
 } evo_shape_t;
 
+/* For the calling thread's last call that returned EVO_ERR_CUDA: which step
+ * failed and the CUDA error name and code (static thread-local text, valid
+ * until this thread's next failing call; "" if none failed). */
+EVO_API const char* evo_attn_last_error_detail(void);
+
 /* ABI version of the loaded library (EVO_ATTN_ABI_VERSION at build time). */
 EVO_API int evo_attn_abi_version(void);
 

@@ -18,6 +18,7 @@
 #include "evo_attn.h"
 #include "evo_internal.h"
 #include "evo_ptx.cuh"
+#include <cstdio>
 
 namespace evo {
 
@@ -26,6 +27,16 @@ __device__ int g_evo_status = 0;
 
 static std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
 static ProfileEvents g_prof{{nullptr}, 0};
+
+// What made this thread's last call return EVO_ERR_CUDA (evo_attn_last_error_detail).
+static thread_local char g_detail[192] = "";
+static void set_detail(const char* what, int code, const char* name) {
+  std::snprintf(g_detail, sizeof(g_detail), "%s: %s (%d)", what, name ? name : "?", code);
+}
+static evo_status_t cuda_fail(const char* what, cudaError_t e) {
+  set_detail(what, static_cast<int>(e), cudaGetErrorName(e));
+  return EVO_ERR_CUDA;
+}
 
 namespace {
 
@@ -70,12 +81,16 @@ PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
 bool encode_t(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int rank, const cuuint64_t* dims,
               const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle swz) {
   auto fn = tmap_encoder();
-  if (!fn) return false;
+  if (!fn) {
+    set_detail("cuTensorMapEncodeTiled entry point", 0, "not found");
+    return false;
+  }
   cuuint32_t es[5] = {1, 1, 1, 1, 1};
   CUresult r = fn(m, dt,
                   static_cast<cuuint32_t>(rank), const_cast<void*>(base), dims, strides, box, es,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) set_detail("cuTensorMapEncodeTiled", static_cast<int>(r), "CUresult");
   return r == CUDA_SUCCESS;
 }
 bool encode(CUtensorMap* m, const void* base, bool bf16, int rank, const cuuint64_t* dims,
@@ -168,9 +183,15 @@ evo_status_t check_shape(const evo_shape_t& s) {
 }
 
 evo_status_t check_device(DeviceInfo** out) {
-  DeviceInfo* d = device_info(nullptr);
-  if (!d || d->err != cudaSuccess) return EVO_ERR_CUDA;
+  int dev = 0;
+  DeviceInfo* d = device_info(&dev);
+  if (!d || d->err != cudaSuccess) return d ? cuda_fail("device query", d->err) : EVO_ERR_CUDA;
   if (d->cc_major != 10 || d->cc_minor != 3) return EVO_ERR_ARCH;
+  // Make the device's primary context current on this thread: the tensor maps are
+  // encoded through the driver API, which needs one (e.g. on a framework's worker
+  // thread whose first CUDA call is ours).
+  const cudaError_t e = cudaSetDevice(dev);
+  if (e != cudaSuccess) return cuda_fail("cudaSetDevice", e);
   *out = d;
   return EVO_OK;
 }
@@ -337,7 +358,7 @@ evo_status_t evo_attn_fwd(const void* q, const void* k, const void* v, const voi
   prof_record(&g_prof, 0, cs);
   cudaError_t e = launch_fwd(a, padded_dim(shape.D), bf16, cs);
   prof_record(&g_prof, 1, cs);
-  return e == cudaSuccess ? EVO_OK : EVO_ERR_CUDA;
+  return e == cudaSuccess ? EVO_OK : cuda_fail("forward launch", e);
 }
 
 size_t evo_attn_bwd_workspace_bytes(evo_shape_t shape, evo_dtype_t dtype, int flags) {
@@ -443,8 +464,10 @@ evo_status_t evo_attn_bwd_ex(const void* q, const void* k, const void* v, const 
   a.wait_ns = g_wait_limit_ns.load();
   a.status = dev->status;
   cudaError_t e = launch_bwd(a, padded_dim(shape.D), bf16, static_cast<cudaStream_t>(stream), &g_prof);
-  return e == cudaSuccess ? EVO_OK : EVO_ERR_CUDA;
+  return e == cudaSuccess ? EVO_OK : cuda_fail("backward launches", e);
 }
+
+const char* evo_attn_last_error_detail(void) { return g_detail; }
 
 evo_status_t evo_attn_device_status(void* stream) {
   DeviceInfo* dev = device_info(nullptr);

@@ -22,6 +22,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "_lib", "libevo_attn.so")
 
 EVO_OK = 0
+EVO_ERR_CUDA = 7
 STATUS_NAMES = {
     0: "EVO_OK", 1: "EVO_ERR_NULL_POINTER", 2: "EVO_ERR_BAD_SHAPE", 3: "EVO_ERR_BAD_DTYPE",
     4: "EVO_ERR_MISALIGNED", 5: "EVO_ERR_WORKSPACE_TOO_SMALL", 6: "EVO_ERR_ARCH", 7: "EVO_ERR_CUDA",
@@ -32,7 +33,7 @@ NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 EXPORTED = ("evo_attn_abi_version", "evo_status_string", "evo_attn_fwd", "evo_attn_bwd_workspace_bytes",
             "evo_attn_bwd", "evo_attn_device_status", "evo_attn_set_wait_limit_ns",
             "evo_attn_selftest_wait_timeout", "evo_attn_profile_events", "evo_attn_step_host_arena_bytes",
-            "evo_attn_step_host", "evo_attn_bwd_noalloc", "evo_attn_bwd_ex")
+            "evo_attn_step_host", "evo_attn_bwd_noalloc", "evo_attn_bwd_ex", "evo_attn_last_error_detail")
 
 _DTYPE_CODE = {torch.float16: 0, torch.bfloat16: 1}
 
@@ -49,6 +50,8 @@ class EvoAttnError(RuntimeError):
         msg = f"{where}: {name}"
         try:
             msg += f" ({load().evo_status_string(status).decode()})"
+            if status == EVO_ERR_CUDA:
+                msg += f" [{load().evo_attn_last_error_detail().decode()}]"
         except Exception:  # pragma: no cover
             pass
         super().__init__(msg)
@@ -90,6 +93,8 @@ def load(path: Optional[str] = None):
     lib.evo_attn_step_host.argtypes = [vp] * 13 + [sz, EvoShape, i32, vp]
     lib.evo_attn_bwd_noalloc.restype = i32
     lib.evo_attn_bwd_noalloc.argtypes = [vp] * 12 + [EvoShape, i32, vp]
+    lib.evo_attn_last_error_detail.restype = ctypes.c_char_p
+    lib.evo_attn_last_error_detail.argtypes = []
     lib.evo_attn_bwd_ex.restype = i32
     lib.evo_attn_bwd_ex.argtypes = [vp] * 14 + [sz, EvoShape, i32, vp]
     if path is None:

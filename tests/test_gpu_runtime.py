@@ -93,3 +93,32 @@ def test_profile_events_and_side_stream():
     assert E.evo_attn_device_status() == 0
     ms = [evs[i].elapsed_time(evs[i + 1]) for i in (0, 2, 3, 4, 5, 6)]
     assert all(m >= 0.0 for m in ms) and ms[0] > 0.0 and ms[2] > 0.0
+
+
+def test_call_from_a_fresh_thread():
+    """A thread whose first CUDA call is the library's (as on a framework's autograd
+    worker thread): the tensor maps still encode, the results match."""
+    import threading
+    inp = _inputs()
+    d = to_dev(inp)
+    out, lse = run_fwd(d)
+    ref = [t.clone() for t in run_bwd(d, out, lse)]
+    o2, l2 = torch.empty_like(out), torch.empty_like(lse)
+    got, err = {}, []
+
+    def work():
+        try:
+            E.evo_attn_fwd(d["q"], d["k"], d["v"], d["bias1"], d["bias2"], out=o2, lse=l2)
+            got["bwd"] = E.evo_attn_bwd_ex(d["q"], d["k"], d["v"], d["bias1"], d["bias2"], o2, l2, d["do"])
+        except Exception as e:  # surfaced below
+            err.append(e)
+
+    t = threading.Thread(target=work)
+    t.start()
+    t.join()
+    assert not err, err
+    torch.cuda.synchronize()
+    assert E.evo_attn_device_status() == 0
+    assert torch.equal(o2, out) and torch.equal(l2, lse)
+    dq, dk, dv, db1, db2 = got["bwd"]
+    assert torch.equal(dk, ref[1]) and torch.equal(dv, ref[2]) and torch.equal(db2, ref[3])
