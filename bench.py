@@ -277,7 +277,6 @@ def run_reference(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": w.name, "B": w.B, "N": w.N, "L": w.L, "H": w.H, "D": w.D,
-                       "backward": mode,
                        "input_dtype": args.dtype, "rows_per_step": rows},
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
                              "sample": sample},
@@ -479,7 +478,7 @@ def run_ours(args):
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": args.dtype, "data": "synthetic",
             "config": {"workload": w.name, "B": w.B, "N": w.N, "L": w.L, "H": w.H, "D": w.D,
-                       "bias1": w.mask and f"{w.mask[0]} {w.mask[1]}", "bias2": has_b2,
+                       "bias1": w.mask and f"{w.mask[0]} {w.mask[1]}", "bias2": has_b2, "backward": mode,
                        "l2": (f"inputs larger than L2: {R} rotating replicas of {per_rep / 1e6:.0f} MB"
                               if R * per_rep >= L2_BYTES else
                               f"L2-warm: {R} replicas of {per_rep / 1e6:.1f} MB fit in L2 (small case)"),
