@@ -17,7 +17,8 @@
  * backward; the backward forms delta first, then dQ, dK, dV and the bias
  * gradients, accumulating bias gradients in fp32 before casting back).
  *
- * Layouts (all dense, row-major, no padding):
+ * Layouts (dense, row-major, no padding; the *_strided entry points also take
+ * strided q, k, v, out, dout, dq, dk, dv, see evo_layout_t):
  *     q, k, v, out, dout, dq, dk, dv : [B, N, L, H, D]   dtype
  *     bias1 (key mask)               : [B, N, 1, 1, L]   dtype, nullable
  *     bias2 (pair bias)              : [B, 1, H, L, L]   dtype, nullable
@@ -60,7 +61,7 @@
 extern "C" {
 #endif
 
-#define EVO_ATTN_ABI_VERSION 2
+#define EVO_ATTN_ABI_VERSION 3
 
 /* Every entry point below is exported from libevo_attn.so; nothing else is. */
 #if defined(__GNUC__)
@@ -83,8 +84,9 @@ typedef enum {
   EVO_ERR_ALIASING = 9,            /* an output overlaps an input                   */
   EVO_ERR_BAD_ARGUMENT = 10,       /* any other invalid argument (e.g. dbias2 given
                                       without bias2, or missing with bias2)         */
-  EVO_ERR_SCRATCH_LIMIT = 11       /* evo_attn_bwd_noalloc: the problem needs more
+  EVO_ERR_SCRATCH_LIMIT = 11,      /* evo_attn_bwd_noalloc: the problem needs more
                                       scratch than EVO_NOALLOC_SCRATCH_BYTES         */
+  EVO_ERR_BAD_LAYOUT = 12          /* a stride of evo_layout_t breaks its rules      */
 } evo_status_t;
 
 typedef enum { EVO_F16 = 0, EVO_BF16 = 1 } evo_dtype_t;
@@ -92,6 +94,36 @@ typedef enum { EVO_F16 = 0, EVO_BF16 = 1 } evo_dtype_t;
 typedef struct {
   int64_t B, N, L, H, D;
 } evo_shape_t;
+
+/*
+ * Strided layout of one [B,N,L,H,D] tensor (evo_attn_fwd_strided,
+ * evo_attn_bwd_strided): the element strides of its B, N and L dimensions.
+ * Its H and D dimensions stay packed (strides D and 1), so each token row of
+ * H*D elements is contiguous.  Packed: b = N*L*H*D, n = L*H*D, l = H*D.
+ *
+ * This is how the Evoformer's transposed usages reach the kernels without a
+ * copy (page §3.6: column-wise MSA attention runs over the other axis of the
+ * MSA; triangle attention around the ending node over the other axis of the
+ * pair representation): pass the [B, N_res, N_seq, H, D] view of a
+ * [B, N_seq, N_res, H, D] buffer as b = N_seq*N_res*H*D, n = H*D,
+ * l = N_res*H*D.
+ *
+ * Rules (else EVO_ERR_BAD_LAYOUT): the strides of dimensions of extent > 1 are
+ * positive multiples of 8 below 2^36; no two token rows overlap (taken in
+ * order of stride, each stride is at least the extent in elements of the
+ * dimensions inside it, the innermost at least H*D); the whole span is below
+ * 2^44 elements.  Strides of dimensions of extent 1 are ignored.
+ */
+typedef struct {
+  int64_t b, n, l;
+} evo_strides_t;
+
+/* Layouts of the [B,N,L,H,D] tensors of one call.  The forward reads q, k, v
+ * and out; the backward all eight.  bias1, bias2, lse and the bias gradients
+ * keep their packed layouts. */
+typedef struct {
+  evo_strides_t q, k, v, out, dout, dq, dk, dv;
+} evo_layout_t;
 
 /* For the calling thread's last call that returned EVO_ERR_CUDA: which step
  * failed and the CUDA error name and code (static thread-local text, valid
@@ -116,6 +148,18 @@ EVO_API evo_status_t evo_attn_fwd(const void* q, const void* k, const void* v,
                           void* out, float* lse,
                           evo_shape_t shape, evo_dtype_t dtype, void* stream);
 
+/*
+ * evo_attn_fwd on strided tensors: q, k, v and out laid out as `layout` says
+ * (NULL = packed, exactly evo_attn_fwd).  The alignment rule applies to the
+ * first element.  Tensors whose batch stride is not N times their row stride
+ * (with B > 1 and N > 1) are processed one batch at a time, one launch each.
+ */
+EVO_API evo_status_t evo_attn_fwd_strided(const void* q, const void* k, const void* v,
+                                          const void* bias1, const void* bias2,
+                                          void* out, float* lse,
+                                          evo_shape_t shape, evo_dtype_t dtype,
+                                          const evo_layout_t* layout, void* stream);
+
 /* Flags of evo_attn_bwd_workspace_bytes (bit 0 keeps the meaning of the
  * former has_bias2 argument, so passing 0 / 1 still works). */
 #define EVO_WS_BIAS2 1  /* the call has a pair bias (and computes dbias2)  */
@@ -128,7 +172,8 @@ EVO_API evo_status_t evo_attn_fwd(const void* q, const void* k, const void* v,
  * memory; with EVO_WS_BIAS2, the fp32 per-group partial sums of the pair-bias
  * gradient and, where a key-major kernel runs, a transposed copy of the pair
  * bias; with EVO_WS_DBIAS1, fp32 per-(b, n, h) partial sums of the key-mask
- * gradient.  Depends only on its arguments.
+ * gradient.  Depends only on its arguments; enough for every layout of
+ * evo_attn_bwd_strided.
  */
 EVO_API size_t evo_attn_bwd_workspace_bytes(evo_shape_t shape, evo_dtype_t dtype, int flags);
 
@@ -171,6 +216,22 @@ EVO_API evo_status_t evo_attn_bwd_ex(const void* q, const void* k, const void* v
                              void* dq, void* dk, void* dv, void* dbias1, void* dbias2,
                              void* workspace, size_t workspace_bytes,
                              evo_shape_t shape, evo_dtype_t dtype, void* stream);
+
+/*
+ * evo_attn_bwd_ex on strided tensors: q, k, v, out, dout, dq, dk and dv laid
+ * out as `layout` says (NULL = packed, exactly evo_attn_bwd_ex).  Outputs are
+ * written only at their own elements; bytes between rows are left alone.
+ * With B > 1 and a tensor whose batch stride is not N times its row stride the
+ * call runs one batch at a time (the workspace is reused by each; the
+ * profiling events then bracket the last batch).
+ */
+EVO_API evo_status_t evo_attn_bwd_strided(const void* q, const void* k, const void* v,
+                                          const void* bias1, const void* bias2,
+                                          const void* out, const float* lse, const void* dout,
+                                          void* dq, void* dk, void* dv, void* dbias1, void* dbias2,
+                                          void* workspace, size_t workspace_bytes,
+                                          evo_shape_t shape, evo_dtype_t dtype,
+                                          const evo_layout_t* layout, void* stream);
 
 /*
  * Synchronises `stream`, then reads and clears the library's device status

@@ -38,6 +38,11 @@ namespace evo {
 namespace {
 
 
+// x / d in 32-bit arithmetic when x < 2^31 (64-bit division is far slower).
+__device__ __forceinline__ long long idiv(long long x, long long d, bool small) {
+  return small ? static_cast<long long>(static_cast<uint32_t>(x) / static_cast<uint32_t>(d)) : x / d;
+}
+
 // ============================================================ evo_bwd_pre
 template <int DP, bool BF16>
 __global__ void __launch_bounds__(256) evo_bwd_pre(const BwdArgs a) {
@@ -73,11 +78,28 @@ __global__ void __launch_bounds__(256) evo_bwd_pre(const BwdArgs a) {
     constexpr int U = 4;  // chunks per thread per round (all loads issued first)
     for (long long c0 = blockIdx.x * 256ll + threadIdx.x; c0 - lane < chunks; c0 += U * stride) {
       uint4 ov[U], gv[U];
+      if (a.packed) {
 #pragma unroll
-      for (int q = 0; q < U; ++q) {
-        const long long ch = c0 + q * stride;
-        ov[q] = ch < chunks ? __ldg(reinterpret_cast<const uint4*>(a.out) + ch) : make_uint4(0u, 0u, 0u, 0u);
-        gv[q] = ch < chunks ? __ldg(reinterpret_cast<const uint4*>(a.dout) + ch) : make_uint4(0u, 0u, 0u, 0u);
+        for (int q = 0; q < U; ++q) {
+          const long long ch = c0 + q * stride;
+          ov[q] = ch < chunks ? __ldg(reinterpret_cast<const uint4*>(a.out) + ch) : make_uint4(0u, 0u, 0u, 0u);
+          gv[q] = ch < chunks ? __ldg(reinterpret_cast<const uint4*>(a.dout) + ch) : make_uint4(0u, 0u, 0u, 0u);
+        }
+      } else {
+        // strided rows: chunk ch is chunk c of token (bn, i), cpt = H*D/8 chunks per token
+        const long long cpt = static_cast<long long>(a.H) * lpr;
+        const bool small = chunks < (1ll << 31);
+#pragma unroll
+        for (int q = 0; q < U; ++q) {
+          const long long ch = c0 + q * stride;
+          ov[q] = gv[q] = make_uint4(0u, 0u, 0u, 0u);
+          if (ch < chunks) {
+            const long long t = idiv(ch, cpt, small), bn = idiv(t, a.L, small);
+            const long long c = ch - t * cpt, i = t - bn * a.L;
+            ov[q] = __ldg(reinterpret_cast<const uint4*>(a.out + bn * a.r_out.bn + i * a.r_out.l) + c);
+            gv[q] = __ldg(reinterpret_cast<const uint4*>(a.dout + bn * a.r_dout.bn + i * a.r_dout.l) + c);
+          }
+        }
       }
 #pragma unroll
       for (int q = 0; q < U; ++q) {
@@ -116,8 +138,8 @@ __global__ void __launch_bounds__(256) evo_bwd_pre(const BwdArgs a) {
     long long t = row / a.H;
     const int i = static_cast<int>(t % a.L);
     const long long bn = t / a.L;
-    const uint4* o = reinterpret_cast<const uint4*>(a.out + row * a.D);
-    const uint4* g = reinterpret_cast<const uint4*>(a.dout + row * a.D);
+    const uint4* o = reinterpret_cast<const uint4*>(a.out + bn * a.r_out.bn + i * a.r_out.l + h * a.D);
+    const uint4* g = reinterpret_cast<const uint4*>(a.dout + bn * a.r_dout.bn + i * a.r_dout.l + h * a.D);
     float4* acc = reinterpret_cast<float4*>(a.dq_acc + row * a.D);
     float sum = 0.0f;
 #pragma unroll
@@ -145,6 +167,8 @@ __global__ void __launch_bounds__(256) evo_bwd_pre(const BwdArgs a) {
 template <bool BF16>
 __global__ void __launch_bounds__(256) evo_bwd_dq_cast(const BwdArgs a) {
   const long long n8 = static_cast<long long>(a.B) * a.N * a.L * a.H * a.D / 8;
+  const long long cpt = static_cast<long long>(a.H) * a.D / 8;  // 8-element chunks per token
+  const bool small = n8 < (1ll << 31);
   for (long long v = blockIdx.x * 256ll + threadIdx.x; v < n8; v += gridDim.x * 256ll) {
     const float4 x = reinterpret_cast<const float4*>(a.dq_acc)[2 * v];
     const float4 y = reinterpret_cast<const float4*>(a.dq_acc)[2 * v + 1];
@@ -153,7 +177,12 @@ __global__ void __launch_bounds__(256) evo_bwd_dq_cast(const BwdArgs a) {
     pk.y = pack2<BF16>(x.z, x.w);
     pk.z = pack2<BF16>(y.x, y.y);
     pk.w = pack2<BF16>(y.z, y.w);
-    reinterpret_cast<uint4*>(a.dq)[v] = pk;
+    if (a.packed) {
+      reinterpret_cast<uint4*>(a.dq)[v] = pk;
+    } else {
+      const long long t = idiv(v, cpt, small), bn = idiv(t, a.L, small);
+      *reinterpret_cast<uint4*>(a.dq + bn * a.r_dq.bn + (t - bn * a.L) * a.r_dq.l + (v - t * cpt) * 8) = pk;
+    }
   }
 }
 
@@ -574,8 +603,9 @@ __device__ __forceinline__ bool main_write_dkdv(const BwdArgs& a, const KvIter& 
   if (lane == 0) mbar_arrive(smem_u32(&bars->dkdv_free[db]));
   const int j = c.jt * kTile + r;
   if (j < a.L) {
-    const size_t off = ((static_cast<size_t>(c.b) * a.N + c.n) * a.L + j) * a.H * a.D +
-                       static_cast<size_t>(c.h) * a.D + hc * HD;
+    const long long bn = static_cast<long long>(c.b) * a.N + c.n, inner = c.h * a.D + hc * HD;
+    uint16_t* dk = a.dk + bn * a.r_dk.bn + j * a.r_dk.l + inner;
+    uint16_t* dv = a.dv + bn * a.r_dv.bn + j * a.r_dv.l + inner;
 #pragma unroll
     for (int e = 0; e < HD; e += 8)
       if (hc * HD + e < a.D) {
@@ -588,8 +618,8 @@ __device__ __forceinline__ bool main_write_dkdv(const BwdArgs& a, const KvIter& 
         pv4.y = pack2<BF16>(vx[e + 2], vx[e + 3]);
         pv4.z = pack2<BF16>(vx[e + 4], vx[e + 5]);
         pv4.w = pack2<BF16>(vx[e + 6], vx[e + 7]);
-        *reinterpret_cast<uint4*>(a.dk + off + e) = pk;
-        *reinterpret_cast<uint4*>(a.dv + off + e) = pv4;
+        *reinterpret_cast<uint4*>(dk + e) = pk;
+        *reinterpret_cast<uint4*>(dv + e) = pv4;
       }
   }
   return true;
@@ -1144,8 +1174,9 @@ __device__ __forceinline__ bool slice_write_dkdv(const BwdArgs& a, const SlIter&
   if (lane == 0) mbar_arrive(smem_u32(&bars->dkdv_free[db]));
   const int j = jt * kTile + r;
   if (j < a.L) {
-    const size_t off = ((static_cast<size_t>(c.b) * a.N + c.n) * a.L + j) * a.H * a.D +
-                       static_cast<size_t>(c.h) * a.D + hc * HD;
+    const long long bn = static_cast<long long>(c.b) * a.N + c.n, inner = c.h * a.D + hc * HD;
+    uint16_t* dk = a.dk + bn * a.r_dk.bn + j * a.r_dk.l + inner;
+    uint16_t* dv = a.dv + bn * a.r_dv.bn + j * a.r_dv.l + inner;
 #pragma unroll
     for (int e = 0; e < HD; e += 8)
       if (hc * HD + e < a.D) {
@@ -1158,8 +1189,8 @@ __device__ __forceinline__ bool slice_write_dkdv(const BwdArgs& a, const SlIter&
         pv4.y = pack2<BF16>(vx[e + 2], vx[e + 3]);
         pv4.z = pack2<BF16>(vx[e + 4], vx[e + 5]);
         pv4.w = pack2<BF16>(vx[e + 6], vx[e + 7]);
-        *reinterpret_cast<uint4*>(a.dk + off + e) = pk;
-        *reinterpret_cast<uint4*>(a.dv + off + e) = pv4;
+        *reinterpret_cast<uint4*>(dk + e) = pk;
+        *reinterpret_cast<uint4*>(dv + e) = pv4;
       }
   }
   return true;
@@ -1172,7 +1203,7 @@ __device__ __forceinline__ bool slice_write_dq(const BwdArgs& a, const SlIter& c
   constexpr int HD = DP / 2;
   if (!mbar_wait(smem_u32(&bars->dq_full), slice & 1, g)) return false;
   tc_fence_after();
-  const size_t bn = static_cast<size_t>(c.b) * a.N + c.n;
+  const long long bn = static_cast<long long>(c.b) * a.N + c.n;
   for (int it = 0; it < a.QT; ++it) {
     float v[HD];
     const uint32_t col = trow + sl_col_dq<DP>(it, slice_kv_bufs(DP, a.QT)) + hc * HD;
@@ -1195,7 +1226,7 @@ __device__ __forceinline__ bool slice_write_dq(const BwdArgs& a, const SlIter& c
     }
     const int i = it * kTile + r;
     if (i < a.L) {
-      uint16_t* dst = a.dq + (bn * a.L + i) * a.H * a.D + static_cast<size_t>(c.h) * a.D + hc * HD;
+      uint16_t* dst = a.dq + bn * a.r_dq.bn + static_cast<long long>(i) * a.r_dq.l + c.h * a.D + hc * HD;
 #pragma unroll
       for (int e = 0; e < HD; e += 8)
         if (hc * HD + e < a.D) {

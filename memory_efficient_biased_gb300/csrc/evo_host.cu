@@ -110,13 +110,16 @@ bool map_db2_part(CUtensorMap* m, const void* p, const evo_shape_t& s, int group
 
 int padded_dim(int64_t D) { return D <= 16 ? 16 : (D <= 32 ? 32 : 64); }
 
-// [B,N,L,H,D] viewed as 4-D (D, H, L, B*N); box (DP, 1, 128, 1), swizzle = 2*DP bytes.
-bool map_qkv(CUtensorMap* m, const void* p, const evo_shape_t& s, bool bf16) {
+Rows packed_rows(const evo_shape_t& s) { return {s.L * s.H * s.D, s.H * s.D}; }
+
+// [B,N,L,H,D] with row strides r viewed as 4-D (D, H, L, B*N); box (DP, 1, 128, 1),
+// swizzle = 2*DP bytes.
+bool map_qkv(CUtensorMap* m, const void* p, const evo_shape_t& s, bool bf16, const Rows& r) {
   const int DP = padded_dim(s.D);
   cuuint64_t dims[4] = {static_cast<cuuint64_t>(s.D), static_cast<cuuint64_t>(s.H), static_cast<cuuint64_t>(s.L),
                         static_cast<cuuint64_t>(s.B * s.N)};
-  cuuint64_t strides[3] = {static_cast<cuuint64_t>(s.D * 2), static_cast<cuuint64_t>(s.H * s.D * 2),
-                           static_cast<cuuint64_t>(s.L * s.H * s.D * 2)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(s.D * 2), static_cast<cuuint64_t>(r.l * 2),
+                           static_cast<cuuint64_t>(r.bn * 2)};
   cuuint32_t box[4] = {static_cast<cuuint32_t>(DP), 1, static_cast<cuuint32_t>(kTile), 1};
   const CUtensorMapSwizzle swz = DP == 64   ? CU_TENSOR_MAP_SWIZZLE_128B
                                  : DP == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
@@ -126,12 +129,12 @@ bool map_qkv(CUtensorMap* m, const void* p, const evo_shape_t& s, bool bf16) {
 
 // The same 4-D view with a box of one warp's share of an output tile: (DP/2, 1, 32, 1);
 // swizzle = the box row (DP bytes): none for 16, 32B for 32, 64B for 64.
-bool map_rows_half(CUtensorMap* m, const void* p, const evo_shape_t& s, bool bf16) {
+bool map_rows_half(CUtensorMap* m, const void* p, const evo_shape_t& s, bool bf16, const Rows& r) {
   const int DP = padded_dim(s.D);
   cuuint64_t dims[4] = {static_cast<cuuint64_t>(s.D), static_cast<cuuint64_t>(s.H), static_cast<cuuint64_t>(s.L),
                         static_cast<cuuint64_t>(s.B * s.N)};
-  cuuint64_t strides[3] = {static_cast<cuuint64_t>(s.D * 2), static_cast<cuuint64_t>(s.H * s.D * 2),
-                           static_cast<cuuint64_t>(s.L * s.H * s.D * 2)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(s.D * 2), static_cast<cuuint64_t>(r.l * 2),
+                           static_cast<cuuint64_t>(r.bn * 2)};
   cuuint32_t box[4] = {static_cast<cuuint32_t>(DP / 2), 1, 32, 1};
   return encode(m, p, bf16, 4, dims, strides, box,
                 DP == 64   ? CU_TENSOR_MAP_SWIZZLE_64B
@@ -169,6 +172,60 @@ bool overlap(const Range& a, const Range& b) {
   const uintptr_t a0 = reinterpret_cast<uintptr_t>(a.p), b0 = reinterpret_cast<uintptr_t>(b.p);
   return a0 < b0 + b.bytes && b0 < a0 + a.bytes;
 }
+
+// ---- strided [B,N,L,H,D] tensors (evo_attn_fwd_strided / evo_attn_bwd_strided)
+
+evo_strides_t packed_strides(const evo_shape_t& s) { return {s.N * s.L * s.H * s.D, s.L * s.H * s.D, s.H * s.D}; }
+
+// Strides of extent-1 dimensions address nothing: replace them by the packed values.
+evo_strides_t normalised(evo_strides_t t, const evo_shape_t& s) {
+  const evo_strides_t p = packed_strides(s);
+  if (s.B == 1) t.b = p.b;
+  if (s.N == 1) t.n = p.n;
+  if (s.L == 1) t.l = p.l;
+  return t;
+}
+
+// Every stride a positive multiple of 8 elements (16 bytes, the tensor-map rule)
+// below 2^36 elements; no two token rows (H*D elements each) overlap: taken in
+// order of stride, each dimension's stride covers the whole extent of the
+// dimensions inside it; the addressed span stays below 2^44 elements.
+bool strides_ok(const evo_strides_t& t, const evo_shape_t& s) {
+  struct Dim {
+    int64_t ext, str;
+  } d[3] = {{s.B, t.b}, {s.N, t.n}, {s.L, t.l}};
+  for (const Dim& x : d)
+    if (x.str <= 0 || x.str % 8 != 0 || x.str >= (int64_t(1) << 36)) return false;
+  auto order = [](Dim& x, Dim& y) {
+    if (y.str < x.str) {
+      const Dim z = x;
+      x = y;
+      y = z;
+    }
+  };
+  order(d[0], d[1]);
+  order(d[1], d[2]);
+  order(d[0], d[1]);
+  double need = double(s.H) * double(s.D);
+  for (const Dim& x : d) {
+    if (x.ext == 1) continue;
+    if (double(x.str) < need) return false;
+    need = double(x.str) * double(x.ext);
+  }
+  return need < 17592186044416.0;
+}
+
+// Bytes from the tensor's first element to one past its last.
+size_t span_bytes(const evo_strides_t& t, const evo_shape_t& s) {
+  return size_t((s.B - 1) * t.b + (s.N - 1) * t.n + (s.L - 1) * t.l + s.H * s.D) * 2;
+}
+
+// The kernels address (b, n) as one tensor-map dimension of extent B*N: possible
+// when B == 1, N == 1, or the batch stride is N times the row stride.  Otherwise
+// the call runs batch by batch.
+bool merges(const evo_strides_t& t, const evo_shape_t& s) { return s.B == 1 || s.N == 1 || t.b == s.N * t.n; }
+Rows rows_of(const evo_strides_t& t, const evo_shape_t& s) { return {s.N == 1 ? t.b : t.n, t.l}; }
+bool same_rows(const Rows& x, const Rows& y) { return x.bn == y.bn && x.l == y.l; }
 
 evo_status_t check_shape(const evo_shape_t& s) {
   if (s.B < 1 || s.N < 1 || s.H < 1 || s.L < 1 || s.L > 32768) return EVO_ERR_BAD_SHAPE;
@@ -300,6 +357,8 @@ const char* evo_status_string(evo_status_t s) {
     case EVO_ERR_BAD_ARGUMENT: return "invalid argument combination";
     case EVO_ERR_SCRATCH_LIMIT:
       return "backward workspace exceeds the fixed 16 MiB scratch of evo_attn_bwd_noalloc; use evo_attn_bwd";
+    case EVO_ERR_BAD_LAYOUT:
+      return "a stride breaks the layout rules (multiples of 8, rows must not overlap)";
   }
   return "unknown status";
 }
@@ -308,16 +367,30 @@ void evo_attn_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns < 1000 ?
 
 evo_status_t evo_attn_fwd(const void* q, const void* k, const void* v, const void* bias1, const void* bias2,
                           void* out, float* lse, evo_shape_t shape, evo_dtype_t dtype, void* stream) {
+  return evo_attn_fwd_strided(q, k, v, bias1, bias2, out, lse, shape, dtype, nullptr, stream);
+}
+
+evo_status_t evo_attn_fwd_strided(const void* q, const void* k, const void* v, const void* bias1,
+                                  const void* bias2, void* out, float* lse, evo_shape_t shape, evo_dtype_t dtype,
+                                  const evo_layout_t* layout, void* stream) {
   if (!q || !k || !v || !out || !lse) return EVO_ERR_NULL_POINTER;
   if (dtype != EVO_F16 && dtype != EVO_BF16) return EVO_ERR_BAD_DTYPE;
   evo_status_t st = check_shape(shape);
   if (st != EVO_OK) return st;
+  evo_strides_t t[4];  // q, k, v, out
+  for (int i = 0; i < 4; ++i) {
+    const evo_strides_t* given = layout ? (i == 0 ? &layout->q : i == 1 ? &layout->k : i == 2 ? &layout->v
+                                                                                       : &layout->out)
+                                        : nullptr;
+    t[i] = normalised(given ? *given : packed_strides(shape), shape);
+    if (!strides_ok(t[i], shape)) return EVO_ERR_BAD_LAYOUT;
+  }
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) || !aligned(lse, 4) ||
       (bias1 && !aligned(bias1, 2)) || (bias2 && !aligned(bias2, 16)))
     return EVO_ERR_MISALIGNED;
-  const Range ins[5] = {{q, qkv_bytes(shape)}, {k, qkv_bytes(shape)}, {v, qkv_bytes(shape)},
+  const Range ins[5] = {{q, span_bytes(t[0], shape)}, {k, span_bytes(t[1], shape)}, {v, span_bytes(t[2], shape)},
                         {bias1, bias1 ? bias1_bytes(shape) : 0}, {bias2, bias2 ? bias2_bytes(shape) : 0}};
-  const Range outs[2] = {{out, qkv_bytes(shape)}, {lse, lse_bytes(shape)}};
+  const Range outs[2] = {{out, span_bytes(t[3], shape)}, {lse, lse_bytes(shape)}};
   for (const Range& o : outs)
     for (const Range& i : ins)
       if (overlap(o, i)) return EVO_ERR_ALIASING;
@@ -326,77 +399,126 @@ evo_status_t evo_attn_fwd(const void* q, const void* k, const void* v, const voi
   if ((st = check_device(&dev)) != EVO_OK) return st;
 
   const bool bf16 = dtype == EVO_BF16;
-  FwdArgs a;
-  std::memset(&a, 0, sizeof(a));
-  if (!map_qkv(&a.tq, q, shape, bf16) || !map_qkv(&a.tk, k, shape, bf16) || !map_qkv(&a.tv, v, shape, bf16) ||
-      !map_rows_half(&a.tout, out, shape, bf16))
-    return EVO_ERR_CUDA;
-  a.bias2_mode = kBias2None;
-  if (bias2) {
-    if (shape.L % 8 == 0) {
-      if (!map_bias2(&a.tb2, bias2, shape, bf16, 64, CU_TENSOR_MAP_SWIZZLE_128B)) return EVO_ERR_CUDA;
-      a.bias2_mode = kBias2Tma;
-    } else {
-      a.bias2_mode = kBias2Loads;
-    }
-  }
-  a.bias1 = static_cast<const uint16_t*>(bias1);
-  a.bias2 = static_cast<const uint16_t*>(bias2);
-  a.out = static_cast<uint16_t*>(out);
-  a.lse = lse;
-  a.B = static_cast<int>(shape.B);
-  a.N = static_cast<int>(shape.N);
-  a.L = static_cast<int>(shape.L);
-  a.H = static_cast<int>(shape.H);
-  a.D = static_cast<int>(shape.D);
-  a.QT = static_cast<int>((shape.L + kTile - 1) / kTile);
-  a.items = shape.B * shape.N * shape.H * a.QT;
-  a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(shape.D)));
-  a.wait_ns = g_wait_limit_ns.load();
-  a.status = dev->status;
+  bool whole = true;
+  for (const evo_strides_t& x : t) whole = whole && merges(x, shape);
+  evo_shape_t sub = shape;
+  sub.B = whole ? shape.B : 1;
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);
   prof_record(&g_prof, 0, cs);
-  cudaError_t e = launch_fwd(a, padded_dim(shape.D), bf16, cs);
+  for (int64_t b = 0; b < shape.B; b += sub.B) {
+    const auto at = [&](const void* p, const evo_strides_t& x) {
+      return static_cast<const uint8_t*>(p) + size_t(b * x.b) * 2;
+    };
+    FwdArgs a;
+    std::memset(&a, 0, sizeof(a));
+    if (!map_qkv(&a.tq, at(q, t[0]), sub, bf16, rows_of(t[0], sub)) ||
+        !map_qkv(&a.tk, at(k, t[1]), sub, bf16, rows_of(t[1], sub)) ||
+        !map_qkv(&a.tv, at(v, t[2]), sub, bf16, rows_of(t[2], sub)) ||
+        !map_rows_half(&a.tout, at(out, t[3]), sub, bf16, rows_of(t[3], sub)))
+      return EVO_ERR_CUDA;
+    const uint16_t* b2 = bias2 ? static_cast<const uint16_t*>(bias2) + b * shape.H * shape.L * shape.L : nullptr;
+    a.bias2_mode = kBias2None;
+    if (b2) {
+      if (shape.L % 8 == 0) {
+        if (!map_bias2(&a.tb2, b2, sub, bf16, 64, CU_TENSOR_MAP_SWIZZLE_128B)) return EVO_ERR_CUDA;
+        a.bias2_mode = kBias2Tma;
+      } else {
+        a.bias2_mode = kBias2Loads;
+      }
+    }
+    a.bias1 = bias1 ? static_cast<const uint16_t*>(bias1) + b * shape.N * shape.L : nullptr;
+    a.bias2 = b2;
+    a.out = static_cast<uint16_t*>(const_cast<void*>(static_cast<const void*>(at(out, t[3]))));
+    a.lse = lse + b * shape.N * shape.H * shape.L;
+    a.B = static_cast<int>(sub.B);
+    a.N = static_cast<int>(shape.N);
+    a.L = static_cast<int>(shape.L);
+    a.H = static_cast<int>(shape.H);
+    a.D = static_cast<int>(shape.D);
+    a.QT = static_cast<int>((shape.L + kTile - 1) / kTile);
+    a.items = sub.B * shape.N * shape.H * a.QT;
+    a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(shape.D)));
+    a.wait_ns = g_wait_limit_ns.load();
+    a.status = dev->status;
+    const cudaError_t e = launch_fwd(a, padded_dim(shape.D), bf16, cs);
+    if (e != cudaSuccess) return cuda_fail("forward launch", e);
+  }
   prof_record(&g_prof, 1, cs);
-  return e == cudaSuccess ? EVO_OK : cuda_fail("forward launch", e);
+  return EVO_OK;
 }
 
 size_t evo_attn_bwd_workspace_bytes(evo_shape_t shape, evo_dtype_t dtype, int flags) {
   if (dtype != EVO_F16 && dtype != EVO_BF16) return 0;
   if (check_shape(shape) != EVO_OK) return 0;
-  return ws_layout(shape, (flags & EVO_WS_BIAS2) != 0, (flags & EVO_WS_DBIAS1) != 0).total;
+  const bool b2 = (flags & EVO_WS_BIAS2) != 0, db1 = (flags & EVO_WS_DBIAS1) != 0;
+  // enough for the whole batch at once and for one batch at a time (strided layouts
+  // whose batch and row dimensions do not merge)
+  evo_shape_t one = shape;
+  one.B = 1;
+  const size_t whole = ws_layout(shape, b2, db1).total, each = ws_layout(one, b2, db1).total;
+  return whole > each ? whole : each;
 }
 
 evo_status_t evo_attn_bwd(const void* q, const void* k, const void* v, const void* bias1, const void* bias2,
                           const void* out, const float* lse, const void* dout, void* dq, void* dk, void* dv,
                           void* dbias2, void* workspace, size_t workspace_bytes, evo_shape_t shape,
                           evo_dtype_t dtype, void* stream) {
-  return evo_attn_bwd_ex(q, k, v, bias1, bias2, out, lse, dout, dq, dk, dv, nullptr, dbias2, workspace,
-                         workspace_bytes, shape, dtype, stream);
+  return evo_attn_bwd_strided(q, k, v, bias1, bias2, out, lse, dout, dq, dk, dv, nullptr, dbias2, workspace,
+                              workspace_bytes, shape, dtype, nullptr, stream);
 }
 
 evo_status_t evo_attn_bwd_ex(const void* q, const void* k, const void* v, const void* bias1, const void* bias2,
                              const void* out, const float* lse, const void* dout, void* dq, void* dk, void* dv,
                              void* dbias1, void* dbias2, void* workspace, size_t workspace_bytes,
                              evo_shape_t shape, evo_dtype_t dtype, void* stream) {
+  return evo_attn_bwd_strided(q, k, v, bias1, bias2, out, lse, dout, dq, dk, dv, dbias1, dbias2, workspace,
+                              workspace_bytes, shape, dtype, nullptr, stream);
+}
+
+evo_status_t evo_attn_bwd_strided(const void* q, const void* k, const void* v, const void* bias1,
+                                  const void* bias2, const void* out, const float* lse, const void* dout, void* dq,
+                                  void* dk, void* dv, void* dbias1, void* dbias2, void* workspace,
+                                  size_t workspace_bytes, evo_shape_t shape, evo_dtype_t dtype,
+                                  const evo_layout_t* layout, void* stream) {
   if (!q || !k || !v || !out || !lse || !dout || !dq || !dk || !dv || !workspace) return EVO_ERR_NULL_POINTER;
   if (dtype != EVO_F16 && dtype != EVO_BF16) return EVO_ERR_BAD_DTYPE;
   evo_status_t st = check_shape(shape);
   if (st != EVO_OK) return st;
   if ((bias2 != nullptr) != (dbias2 != nullptr)) return EVO_ERR_BAD_ARGUMENT;
   if (dbias1 && !bias1) return EVO_ERR_BAD_ARGUMENT;
+  enum { Q, K, V, O, DO, DQ, DK, DV };
+  evo_strides_t t[8];
+  for (int i = 0; i < 8; ++i) {
+    const evo_strides_t* g = nullptr;
+    if (layout) {
+      const evo_strides_t* all[8] = {&layout->q,    &layout->k,  &layout->v,  &layout->out,
+                                     &layout->dout, &layout->dq, &layout->dk, &layout->dv};
+      g = all[i];
+    }
+    t[i] = normalised(g ? *g : packed_strides(shape), shape);
+    if (!strides_ok(t[i], shape)) return EVO_ERR_BAD_LAYOUT;
+  }
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) || !aligned(dout, 16) ||
       !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(lse, 4) ||
       (bias1 && !aligned(bias1, 2)) || (bias2 && !aligned(bias2, 16)) || (dbias2 && !aligned(dbias2, 16)) ||
       (dbias1 && !aligned(dbias1, 2)) || !aligned(workspace, 256))
     return EVO_ERR_MISALIGNED;
-  const WsLayout w = ws_layout(shape, bias2 != nullptr, dbias1 != nullptr);
+  bool whole = true;
+  for (const evo_strides_t& x : t) whole = whole && merges(x, shape);
+  evo_shape_t sub = shape;
+  sub.B = whole ? shape.B : 1;
+  const WsLayout w = ws_layout(sub, bias2 != nullptr, dbias1 != nullptr);
   if (workspace_bytes < w.total) return EVO_ERR_WORKSPACE_TOO_SMALL;
-  const size_t nq = qkv_bytes(shape);
-  const Range ins[8] = {{q, nq}, {k, nq}, {v, nq}, {bias1, bias1 ? bias1_bytes(shape) : 0},
-                        {bias2, bias2 ? bias2_bytes(shape) : 0}, {out, nq}, {lse, lse_bytes(shape)}, {dout, nq}};
-  const Range outs[6] = {{dq, nq}, {dk, nq}, {dv, nq}, {dbias2, dbias2 ? bias2_bytes(shape) : 0},
-                         {dbias1, dbias1 ? bias1_bytes(shape) : 0}, {workspace, w.total}};
+  const Range ins[8] = {{q, span_bytes(t[Q], shape)},      {k, span_bytes(t[K], shape)},
+                        {v, span_bytes(t[V], shape)},      {bias1, bias1 ? bias1_bytes(shape) : 0},
+                        {bias2, bias2 ? bias2_bytes(shape) : 0}, {out, span_bytes(t[O], shape)},
+                        {lse, lse_bytes(shape)},           {dout, span_bytes(t[DO], shape)}};
+  const Range outs[6] = {{dq, span_bytes(t[DQ], shape)},
+                         {dk, span_bytes(t[DK], shape)},
+                         {dv, span_bytes(t[DV], shape)},
+                         {dbias2, dbias2 ? bias2_bytes(shape) : 0},
+                         {dbias1, dbias1 ? bias1_bytes(shape) : 0},
+                         {workspace, w.total}};
   for (int i = 0; i < 6; ++i) {
     for (const Range& r : ins)
       if (overlap(outs[i], r)) return EVO_ERR_ALIASING;
@@ -407,64 +529,82 @@ evo_status_t evo_attn_bwd_ex(const void* q, const void* k, const void* v, const 
   if ((st = check_device(&dev)) != EVO_OK) return st;
 
   const bool bf16 = dtype == EVO_BF16;
-  BwdArgs a;
-  std::memset(&a, 0, sizeof(a));
-  if (!map_qkv(&a.tq, q, shape, bf16) || !map_qkv(&a.tk, k, shape, bf16) || !map_qkv(&a.tv, v, shape, bf16) ||
-      !map_qkv(&a.tdo, dout, shape, bf16))
-    return EVO_ERR_CUDA;
-  if (padded_dim(shape.D) <= 32 && (!map_rows_half(&a.tdq, dq, shape, bf16) ||
-                                    !map_rows_half(&a.tdk, dk, shape, bf16) || !map_rows_half(&a.tdv, dv, shape, bf16)))
-    return EVO_ERR_CUDA;
-  a.bias2_mode = kBias2None;
-  if (bias2) {
-    if (shape.L % 8 == 0) {
-      if (!map_bias2(&a.tb2, bias2, shape, bf16, 64, CU_TENSOR_MAP_SWIZZLE_128B))
-        return EVO_ERR_CUDA;
-      a.bias2_mode = kBias2Tma;
-    } else {
-      a.bias2_mode = kBias2Loads;
-    }
-  }
+  const Rows packed = packed_rows(sub);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  a.q = static_cast<const uint16_t*>(q);
-  a.out = static_cast<const uint16_t*>(out);
-  a.dout = static_cast<const uint16_t*>(dout);
-  a.bias1 = static_cast<const uint16_t*>(bias1);
-  a.bias2 = static_cast<const uint16_t*>(bias2);
-  a.lse = lse;
-  a.dq = static_cast<uint16_t*>(dq);
-  a.dk = static_cast<uint16_t*>(dk);
-  a.dv = static_cast<uint16_t*>(dv);
-  a.dbias2 = static_cast<uint16_t*>(dbias2);
-  a.delta = reinterpret_cast<float*>(ws + w.delta);
-  a.dq_acc = reinterpret_cast<float*>(ws + w.dq_acc);
-  a.db2_part = bias2 ? reinterpret_cast<float*>(ws + w.db2) : nullptr;
-  if (dbias1) {
-    a.dbias1 = static_cast<uint16_t*>(dbias1);
-    a.db1p = reinterpret_cast<float*>(ws + w.db1p);
+  for (int64_t b = 0; b < shape.B; b += sub.B) {
+    const auto at = [&](const void* p, int which) {
+      return const_cast<uint16_t*>(reinterpret_cast<const uint16_t*>(static_cast<const uint8_t*>(p) +
+                                                                     size_t(b * t[which].b) * 2));
+    };
+    const size_t b1_off = size_t(b * shape.N * shape.L), b2_off = size_t(b * shape.H * shape.L * shape.L);
+    BwdArgs a;
+    std::memset(&a, 0, sizeof(a));
+    if (!map_qkv(&a.tq, at(q, Q), sub, bf16, rows_of(t[Q], sub)) ||
+        !map_qkv(&a.tk, at(k, K), sub, bf16, rows_of(t[K], sub)) ||
+        !map_qkv(&a.tv, at(v, V), sub, bf16, rows_of(t[V], sub)) ||
+        !map_qkv(&a.tdo, at(dout, DO), sub, bf16, rows_of(t[DO], sub)))
+      return EVO_ERR_CUDA;
+    if (padded_dim(shape.D) <= 32 && (!map_rows_half(&a.tdq, at(dq, DQ), sub, bf16, rows_of(t[DQ], sub)) ||
+                                      !map_rows_half(&a.tdk, at(dk, DK), sub, bf16, rows_of(t[DK], sub)) ||
+                                      !map_rows_half(&a.tdv, at(dv, DV), sub, bf16, rows_of(t[DV], sub))))
+      return EVO_ERR_CUDA;
+    a.bias1 = bias1 ? static_cast<const uint16_t*>(bias1) + b1_off : nullptr;
+    a.bias2 = bias2 ? static_cast<const uint16_t*>(bias2) + b2_off : nullptr;
+    a.bias2_mode = kBias2None;
+    if (a.bias2) {
+      if (shape.L % 8 == 0) {
+        if (!map_bias2(&a.tb2, a.bias2, sub, bf16, 64, CU_TENSOR_MAP_SWIZZLE_128B)) return EVO_ERR_CUDA;
+        a.bias2_mode = kBias2Tma;
+      } else {
+        a.bias2_mode = kBias2Loads;
+      }
+    }
+    a.q = at(q, Q);
+    a.out = at(out, O);
+    a.dout = at(dout, DO);
+    a.lse = lse + b * shape.N * shape.H * shape.L;
+    a.dq = at(dq, DQ);
+    a.dk = at(dk, DK);
+    a.dv = at(dv, DV);
+    a.r_out = rows_of(t[O], sub);
+    a.r_dout = rows_of(t[DO], sub);
+    a.r_dq = rows_of(t[DQ], sub);
+    a.r_dk = rows_of(t[DK], sub);
+    a.r_dv = rows_of(t[DV], sub);
+    a.packed = same_rows(a.r_out, packed) && same_rows(a.r_dout, packed) && same_rows(a.r_dq, packed) &&
+               same_rows(a.r_dk, packed) && same_rows(a.r_dv, packed);
+    a.dbias2 = dbias2 ? static_cast<uint16_t*>(dbias2) + b2_off : nullptr;
+    a.delta = reinterpret_cast<float*>(ws + w.delta);
+    a.dq_acc = reinterpret_cast<float*>(ws + w.dq_acc);
+    a.db2_part = bias2 ? reinterpret_cast<float*>(ws + w.db2) : nullptr;
+    if (dbias1) {
+      a.dbias1 = static_cast<uint16_t*>(dbias1) + b1_off;
+      a.db1p = reinterpret_cast<float*>(ws + w.db1p);
+    }
+    if (bias2 && (w.plan.mode == kBwdKeyMajor || dbias1)) {
+      a.b2t = reinterpret_cast<uint16_t*>(ws + w.b2t);
+      a.b2t_pitch = b2t_pitch(sub);
+      if (!map_b2t(&a.tb2t, a.b2t, sub, bf16, a.b2t_pitch)) return EVO_ERR_CUDA;
+    }
+    a.B = static_cast<int>(sub.B);
+    a.N = static_cast<int>(shape.N);
+    a.L = static_cast<int>(shape.L);
+    a.H = static_cast<int>(shape.H);
+    a.D = static_cast<int>(shape.D);
+    a.QT = static_cast<int>((shape.L + kTile - 1) / kTile);
+    bwd_groups(sub, &a.groups, &a.group_size);
+    if (bias2 && shape.L % 4 == 0) {
+      if (!map_db2_part(&a.tdb2p, a.db2_part, sub, a.groups)) return EVO_ERR_CUDA;
+      a.db2p_tma = 1;
+    }
+    a.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(shape.D)));
+    a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(shape.D)));
+    a.wait_ns = g_wait_limit_ns.load();
+    a.status = dev->status;
+    const cudaError_t e = launch_bwd(a, padded_dim(shape.D), bf16, static_cast<cudaStream_t>(stream), &g_prof);
+    if (e != cudaSuccess) return cuda_fail("backward launches", e);
   }
-  if (bias2 && (w.plan.mode == kBwdKeyMajor || dbias1)) {
-    a.b2t = reinterpret_cast<uint16_t*>(ws + w.b2t);
-    a.b2t_pitch = b2t_pitch(shape);
-    if (!map_b2t(&a.tb2t, a.b2t, shape, bf16, a.b2t_pitch)) return EVO_ERR_CUDA;
-  }
-  a.B = static_cast<int>(shape.B);
-  a.N = static_cast<int>(shape.N);
-  a.L = static_cast<int>(shape.L);
-  a.H = static_cast<int>(shape.H);
-  a.D = static_cast<int>(shape.D);
-  a.QT = static_cast<int>((shape.L + kTile - 1) / kTile);
-  bwd_groups(shape, &a.groups, &a.group_size);
-  if (bias2 && shape.L % 4 == 0) {
-    if (!map_db2_part(&a.tdb2p, a.db2_part, shape, a.groups)) return EVO_ERR_CUDA;
-    a.db2p_tma = 1;
-  }
-  a.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(shape.D)));
-  a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(shape.D)));
-  a.wait_ns = g_wait_limit_ns.load();
-  a.status = dev->status;
-  cudaError_t e = launch_bwd(a, padded_dim(shape.D), bf16, static_cast<cudaStream_t>(stream), &g_prof);
-  return e == cudaSuccess ? EVO_OK : cuda_fail("backward launches", e);
+  return EVO_OK;
 }
 
 const char* evo_attn_last_error_detail(void) { return g_detail; }

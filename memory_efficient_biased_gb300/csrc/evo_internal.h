@@ -10,11 +10,18 @@ namespace evo {
 
 constexpr int kTile = 128;  // queries (and keys) per tile
 
+// Element strides of the (b·n) and token dimensions of one [B,N,L,H,D] tensor
+// whose H·D elements per token are packed: element (bn, l, h, d) sits at
+// bn·bn_stride + l·l_stride + h·D + d.  Packed: bn = L·H·D, l = H·D.
+struct Rows {
+  long long bn, l;
+};
+
 // How the pair bias reaches shared memory.
 enum Bias2Mode : int { kBias2None = 0, kBias2Tma = 1, kBias2Loads = 2 };
 
 struct FwdArgs {
-  CUtensorMap tq, tk, tv;   // 4-D [B*N][L][H][D] views, box (DP, 1, 128, 1)
+  CUtensorMap tq, tk, tv;   // 4-D (D, H, L, B*N) views with the tensors' own strides, box (DP, 1, 128, 1)
   CUtensorMap tb2;          // 3-D [B*H][L][L] view, box (64, 128, 1), 128B swizzle (kBias2Tma)
   CUtensorMap tout;         // O as the 4-D view with box (DP/2, 1, 32, 1): one softmax warp's share
   const uint16_t* bias1;    // [B,N,L] or nullptr
@@ -49,6 +56,9 @@ struct BwdArgs {
   uint16_t* dk;
   uint16_t* dv;
   uint16_t* dbias2;
+  Rows r_out, r_dout;       // row strides of the plain (non-TMA) reads of O and dO
+  Rows r_dq, r_dk, r_dv;    // row strides of the plain writes of dQ, dK, dV
+  int packed;               // all five of the above are packed [B*N][L][H*D]
   float* delta;             // workspace [B,N,H,L]
   float* dq_acc;            // workspace [B,N,L,H,D]
   float* db2_part;          // workspace [G][B,H,L,L]

@@ -6,7 +6,8 @@ not pass them, and forwards raw device pointers, sizes and the current CUDA
 stream to the C ABI declared in include/evo_attn.h.  There is no CPU or
 PyTorch fallback: if the library is missing, every call raises.
 
-Names follow the C ABI: ``evo_attn_fwd``, ``evo_attn_bwd``,
+Names follow the C ABI: ``evo_attn_fwd``, ``evo_attn_bwd``, ``evo_attn_bwd_ex``,
+``evo_attn_fwd_strided``, ``evo_attn_bwd_strided``,
 ``evo_attn_bwd_workspace_bytes``, ``evo_attn_device_status``,
 ``evo_attn_set_wait_limit_ns``, ``evo_attn_selftest_wait_timeout``.
 """
@@ -27,13 +28,14 @@ STATUS_NAMES = {
     0: "EVO_OK", 1: "EVO_ERR_NULL_POINTER", 2: "EVO_ERR_BAD_SHAPE", 3: "EVO_ERR_BAD_DTYPE",
     4: "EVO_ERR_MISALIGNED", 5: "EVO_ERR_WORKSPACE_TOO_SMALL", 6: "EVO_ERR_ARCH", 7: "EVO_ERR_CUDA",
     8: "EVO_ERR_DEVICE_TIMEOUT", 9: "EVO_ERR_ALIASING", 10: "EVO_ERR_BAD_ARGUMENT",
-    11: "EVO_ERR_SCRATCH_LIMIT",
+    11: "EVO_ERR_SCRATCH_LIMIT", 12: "EVO_ERR_BAD_LAYOUT",
 }
 NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 EXPORTED = ("evo_attn_abi_version", "evo_status_string", "evo_attn_fwd", "evo_attn_bwd_workspace_bytes",
             "evo_attn_bwd", "evo_attn_device_status", "evo_attn_set_wait_limit_ns",
             "evo_attn_selftest_wait_timeout", "evo_attn_profile_events", "evo_attn_step_host_arena_bytes",
-            "evo_attn_step_host", "evo_attn_bwd_noalloc", "evo_attn_bwd_ex", "evo_attn_last_error_detail")
+            "evo_attn_step_host", "evo_attn_bwd_noalloc", "evo_attn_bwd_ex", "evo_attn_last_error_detail",
+            "evo_attn_fwd_strided", "evo_attn_bwd_strided")
 
 _DTYPE_CODE = {torch.float16: 0, torch.bfloat16: 1}
 
@@ -41,6 +43,18 @@ _DTYPE_CODE = {torch.float16: 0, torch.bfloat16: 1}
 class EvoShape(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int64), ("N", ctypes.c_int64), ("L", ctypes.c_int64),
                 ("H", ctypes.c_int64), ("D", ctypes.c_int64)]
+
+
+class EvoStrides(ctypes.Structure):
+    """Element strides of the B, N and L dimensions of one [B,N,L,H,D] tensor."""
+    _fields_ = [("b", ctypes.c_int64), ("n", ctypes.c_int64), ("l", ctypes.c_int64)]
+
+
+LAYOUT_FIELDS = ("q", "k", "v", "out", "dout", "dq", "dk", "dv")
+
+
+class EvoLayout(ctypes.Structure):
+    _fields_ = [(n, EvoStrides) for n in LAYOUT_FIELDS]
 
 
 class EvoAttnError(RuntimeError):
@@ -97,6 +111,10 @@ def load(path: Optional[str] = None):
     lib.evo_attn_last_error_detail.argtypes = []
     lib.evo_attn_bwd_ex.restype = i32
     lib.evo_attn_bwd_ex.argtypes = [vp] * 14 + [sz, EvoShape, i32, vp]
+    lib.evo_attn_fwd_strided.restype = i32
+    lib.evo_attn_fwd_strided.argtypes = [vp] * 7 + [EvoShape, i32, ctypes.POINTER(EvoLayout), vp]
+    lib.evo_attn_bwd_strided.restype = i32
+    lib.evo_attn_bwd_strided.argtypes = [vp] * 14 + [sz, EvoShape, i32, ctypes.POINTER(EvoLayout), vp]
     if path is None:
         _lib = lib
     return lib
@@ -123,6 +141,38 @@ def _check(t: Optional[torch.Tensor], name: str, shape=None, dtype=None):
         raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
     if dtype is not None and t.dtype != dtype:
         raise ValueError(f"{name} has dtype {t.dtype}, expected {dtype}")
+
+
+def row_strided(t: torch.Tensor) -> bool:
+    """A [B,N,L,H,D] tensor whose H*D elements per token are packed (any B, N, L strides)."""
+    H, D = t.shape[3], t.shape[4]
+    return (D == 1 or t.stride(4) == 1) and (H == 1 or t.stride(3) == D)
+
+
+def _check_rows(t: Optional[torch.Tensor], name: str, shape, dtype):
+    if t is None:
+        return
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if not row_strided(t):
+        raise ValueError(f"{name} must have packed (H, D) dimensions")
+
+
+def layout_of(**tensors) -> EvoLayout:
+    """EvoLayout from the strides of the given tensors (q=, k=, ...); packed for the rest."""
+    lay = EvoLayout()
+    for name in LAYOUT_FIELDS:
+        t = tensors.get(name)
+        if t is not None:
+            setattr(lay, name, EvoStrides(t.stride(0), t.stride(1), t.stride(2)))
+        else:
+            B, N, L, H, D = next(x for x in tensors.values() if x is not None).shape
+            setattr(lay, name, EvoStrides(N * L * H * D, L * H * D, H * D))
+    return lay
 
 
 def shape_of(q: torch.Tensor) -> EvoShape:
@@ -232,6 +282,71 @@ def evo_attn_bwd_ex(q, k, v, bias1, bias2, out, lse, dout, dq=None, dk=None, dv=
                                 _DTYPE_CODE[dt], _stream_ptr(stream))
     if st != EVO_OK:
         raise EvoAttnError(st, "evo_attn_bwd_ex")
+    return dq, dk, dv, dbias1, dbias2
+
+
+def evo_attn_fwd_strided(q, k, v, bias1=None, bias2=None, out=None, lse=None, stream=None):
+    """evo_attn_fwd on tensors with any B, N, L strides (H and D packed), e.g. the
+    transposed view of column-wise MSA or ending-node triangle attention; the
+    tensors are read in place.  ``out`` defaults to a new packed tensor."""
+    if q.dim() != 5:
+        raise ValueError("q must be [B, N, L, H, D]")
+    B, N, L, H, D = q.shape
+    dt = q.dtype
+    if dt not in _DTYPE_CODE:
+        raise ValueError("inputs must be float16 or bfloat16")
+    if out is None:
+        out = torch.empty(q.shape, dtype=dt, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, N, H, L), dtype=torch.float32, device=q.device)
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out")):
+        _check_rows(t, n, q.shape, dt)
+    _check(bias1, "bias1", (B, N, 1, 1, L), dt)
+    _check(bias2, "bias2", (B, 1, H, L, L), dt)
+    _check(lse, "lse", (B, N, H, L), torch.float32)
+    lay = layout_of(q=q, k=k, v=v, out=out)
+    st = load().evo_attn_fwd_strided(_ptr(q), _ptr(k), _ptr(v), _ptr(bias1), _ptr(bias2), _ptr(out), _ptr(lse),
+                                     shape_of(q), _DTYPE_CODE[dt], ctypes.byref(lay), _stream_ptr(stream))
+    if st != EVO_OK:
+        raise EvoAttnError(st, "evo_attn_fwd_strided")
+    return out, lse
+
+
+def evo_attn_bwd_strided(q, k, v, bias1, bias2, out, lse, dout, dq=None, dk=None, dv=None, dbias1=None,
+                         dbias2=None, workspace=None, stream=None, want_dbias1=False):
+    """evo_attn_bwd_ex on tensors with any B, N, L strides (H and D packed); missing
+    gradient outputs are allocated packed.  Returns (dq, dk, dv, dbias1, dbias2)."""
+    B, N, L, H, D = q.shape
+    dt = q.dtype
+    if dt not in _DTYPE_CODE:
+        raise ValueError("inputs must be float16 or bfloat16")
+    if want_dbias1 and bias1 is None:
+        raise ValueError("dbias1 needs bias1")
+    dq = torch.empty(q.shape, dtype=dt, device=q.device) if dq is None else dq
+    dk = torch.empty(q.shape, dtype=dt, device=q.device) if dk is None else dk
+    dv = torch.empty(q.shape, dtype=dt, device=q.device) if dv is None else dv
+    if want_dbias1 and dbias1 is None:
+        dbias1 = torch.empty_like(bias1)
+    if bias2 is not None and dbias2 is None:
+        dbias2 = torch.empty_like(bias2)
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out"), (dout, "dout"), (dq, "dq"), (dk, "dk"), (dv, "dv")):
+        _check_rows(t, n, q.shape, dt)
+    _check(bias1, "bias1", (B, N, 1, 1, L), dt)
+    _check(bias2, "bias2", (B, 1, H, L, L), dt)
+    _check(lse, "lse", (B, N, H, L), torch.float32)
+    _check(dbias1, "dbias1", (B, N, 1, 1, L), dt)
+    _check(dbias2, "dbias2", (B, 1, H, L, L), dt)
+    need = evo_attn_bwd_workspace_bytes(tuple(q.shape), dt, bias2 is not None, dbias1 is not None)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    _check(workspace, "workspace")
+    lay = layout_of(q=q, k=k, v=v, out=out, dout=dout, dq=dq, dk=dk, dv=dv)
+    st = load().evo_attn_bwd_strided(_ptr(q), _ptr(k), _ptr(v), _ptr(bias1), _ptr(bias2), _ptr(out), _ptr(lse),
+                                     _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dbias1), _ptr(dbias2),
+                                     _ptr(workspace), workspace.numel() * workspace.element_size(), shape_of(q),
+                                     _DTYPE_CODE[dt], ctypes.byref(lay), _stream_ptr(stream))
+    if st != EVO_OK:
+        raise EvoAttnError(st, "evo_attn_bwd_strided")
     return dq, dk, dv, dbias1, dbias2
 
 

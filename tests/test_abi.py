@@ -37,8 +37,8 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_strings(lib):
-    assert lib.evo_attn_abi_version() == 2
-    for code in range(11):
+    assert lib.evo_attn_abi_version() == 3
+    for code in range(13):
         s = lib.evo_status_string(code).decode()
         assert s and s != "unknown status"
     assert lib.evo_status_string(99).decode() == "unknown status"
@@ -135,3 +135,75 @@ def test_workspace_bytes(lib):
     assert lib.evo_attn_bwd_workspace_bytes(s, 1, 2) - no_b2 == 1 * 256 * 4 * 2 * 256 * 4
     assert lib.evo_attn_bwd_workspace_bytes(shape(D=12), 1, 0) == 0
     assert lib.evo_attn_bwd_workspace_bytes(s, 7, 0) == 0
+
+
+def packed_layout(s):
+    hd = s.H * s.D
+    st = E.EvoStrides(s.N * s.L * hd, s.L * hd, hd)
+    return E.EvoLayout(*([st] * 8))
+
+
+def transposed_strides(s):
+    """[B,N,L,H,D] view of a [B,L,N,H,D] buffer."""
+    hd = s.H * s.D
+    return E.EvoStrides(s.N * s.L * hd, hd, s.N * hd)
+
+
+def fwd_s(lib, lay, s=None, out=4 * A):
+    vp = ctypes.c_void_p
+    return lib.evo_attn_fwd_strided(vp(A), vp(2 * A), vp(3 * A), None, None, vp(out), vp(5 * A), s or shape(), 1,
+                                    ctypes.byref(lay) if lay is not None else None, None)
+
+
+def test_fwd_strided_validation(lib):
+    s = shape()  # (1, 2, 64, 2, 32): H*D = 64
+    reach = (6, 7, 0)  # valid arguments reach the device check
+    assert fwd_s(lib, None) in reach
+    assert fwd_s(lib, packed_layout(s)) in reach
+    lay = packed_layout(s)
+    lay.q = transposed_strides(s)
+    assert fwd_s(lib, lay) in reach
+    for bad in ((8192, 0, 64), (8192, 4096, 60), (8192, 4096, 32), (8192, 64, 64), (8192, -4096, 64),
+                (8192, 4096, 1 << 36)):
+        lay = packed_layout(s)
+        lay.k = E.EvoStrides(*bad)
+        assert fwd_s(lib, lay) == 12, bad  # EVO_ERR_BAD_LAYOUT
+    # strides of extent-1 dimensions are ignored (B = 1 here)
+    lay = packed_layout(s)
+    lay.v = E.EvoStrides(3, 4096, 64)
+    assert fwd_s(lib, lay) in reach
+    # the output's span follows its strides: a padded out reaching into lse's range aliases
+    lay = packed_layout(s)
+    lay.out = E.EvoStrides(1 << 20, 1 << 19, 64)  # n = 1 starts 1 MiB after out, i.e. at lse
+    assert fwd_s(lib, lay) == 9
+
+
+def bwd_s(lib, lay, s, ws_bytes):
+    vp = ctypes.c_void_p
+    return lib.evo_attn_bwd_strided(vp(A), vp(2 * A), vp(3 * A), None, None, vp(4 * A), vp(5 * A), vp(6 * A),
+                                    vp(7 * A), vp(8 * A), vp(9 * A), None, None, vp(16 * A), ws_bytes, s, 1,
+                                    ctypes.byref(lay), None)
+
+
+def test_bwd_strided_validation(lib):
+    s = shape(B=2, N=2, L=64, H=2, D=32)
+    per_batch = lib.evo_attn_bwd_workspace_bytes(shape(B=1, N=2, L=64, H=2, D=32), 1, 0)
+    whole = lib.evo_attn_bwd_workspace_bytes(s, 1, 0)
+    assert whole >= per_batch
+    reach = (6, 7, 0)
+    assert bwd_s(lib, packed_layout(s), s, whole) in reach
+    assert bwd_s(lib, packed_layout(s), s, per_batch) == 5
+    # a transposed dout with B = 2 cannot merge (b, n): the call runs batch by batch and
+    # needs only one batch's workspace
+    lay = packed_layout(s)
+    lay.dout = transposed_strides(s)
+    assert bwd_s(lib, lay, s, per_batch) in reach
+    lay.dq = E.EvoStrides(8192, 4096, 40)  # rows overlap
+    assert bwd_s(lib, lay, s, whole) == 12
+
+
+def test_workspace_covers_batch_by_batch(lib):
+    for B, N, L, H, D in ((2, 10, 128, 1, 64), (3, 7, 200, 2, 32), (4, 384, 64, 8, 32)):
+        for flags in (0, 1, 3):
+            one = lib.evo_attn_bwd_workspace_bytes(shape(1, N, L, H, D), 1, flags)
+            assert lib.evo_attn_bwd_workspace_bytes(shape(B, N, L, H, D), 1, flags) >= one
