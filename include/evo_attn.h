@@ -172,8 +172,9 @@ EVO_API evo_status_t evo_attn_fwd_strided(const void* q, const void* k, const vo
  * memory; with EVO_WS_BIAS2, the fp32 per-group partial sums of the pair-bias
  * gradient and, where a key-major kernel runs, a transposed copy of the pair
  * bias; with EVO_WS_DBIAS1, fp32 per-(b, n, h) partial sums of the key-mask
- * gradient.  Depends only on its arguments; enough for every layout of
- * evo_attn_bwd_strided.
+ * gradient; for the shapes whose dQ goes through the accumulator, room for the
+ * work list of masked key-tile skipping.  Depends only on its arguments; enough
+ * for every layout of evo_attn_bwd_strided.
  */
 EVO_API size_t evo_attn_bwd_workspace_bytes(evo_shape_t shape, evo_dtype_t dtype, int flags);
 
@@ -247,6 +248,23 @@ EVO_API evo_status_t evo_attn_device_status(void* stream);
  * process-wide; meant for tests of the timeout path.
  */
 EVO_API void evo_attn_set_wait_limit_ns(uint64_t ns);
+
+/*
+ * Masked key-tile skipping (host-side, process-wide, read by later calls; off by
+ * default).  With enable != 0, a key j of row (b, n) counts as masked when
+ * bias1[b,n,j] <= threshold (a NaN counts as kept), and later calls with a bias1 skip
+ * every 128-key tile of a row whose keys are all masked, as long as the row keeps at
+ * least one key (a row with no kept key skips nothing).  The forward skips them on
+ * every shape with L <= 8192; the backward on the shapes whose dQ goes through the
+ * fp32 accumulator (its per-key-tile schedule), writing their dK and dV as zeros.
+ *
+ * The results are those of the unskipped computation whenever each masked key's
+ * scaled, biased score lies more than 88 below its row's largest one: its fp32
+ * exponential is then exactly 0 either way (page §3.6's key mask, a very large
+ * negative bias, meets this by far).  Skipped tiles still count in any nominal FLOP
+ * figure derived from the shape.
+ */
+EVO_API void evo_attn_set_masked_tile_skip(int enable, float threshold);
 
 /*
  * Self-test of the bounded-wait path: launches one block that waits on a

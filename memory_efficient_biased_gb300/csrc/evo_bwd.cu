@@ -186,6 +186,84 @@ __global__ void __launch_bounds__(256) evo_bwd_dq_cast(const BwdArgs a) {
   }
 }
 
+// ============================================================ masked key tiles
+// Masked key-tile skipping for the per-key-tile kernel.  evo_bwd_tile_mask: the key
+// tiles of each (b, n) row to skip (one warp per row), and zeros for dK and dV of those
+// tiles in every head, since the per-key-tile kernel will not run them.
+template <bool BF16>
+__global__ void __launch_bounds__(256) evo_bwd_tile_mask(const BwdArgs a) {
+  const int lane = threadIdx.x & 31;
+  const long long rows = static_cast<long long>(a.B) * a.N;
+  const unsigned long long all = a.QT >= 64 ? ~0ull : ((1ull << a.QT) - 1);
+  const int cpr = a.H * a.D / 8;  // 16-byte chunks per token row
+  for (long long bn = (blockIdx.x * 256ll + threadIdx.x) >> 5; bn < rows; bn += gridDim.x * 8ll) {
+    const unsigned long long kept = kept_tiles<BF16>(a.bias1 + bn * a.L, a.L, a.skip_at, lane);
+    const unsigned long long skip = kept ? (~kept & all) : 0ull;
+    if (lane == 0) a.tskip[bn] = skip;
+    for (unsigned long long rem = skip; rem; rem &= rem - 1) {
+      const int j0 = (__ffsll(static_cast<long long>(rem)) - 1) * kTile;
+      const int nj = a.L - j0 < kTile ? a.L - j0 : kTile;
+      for (int e = lane; e < nj * cpr; e += 32) {
+        const int j = j0 + e / cpr, c = e % cpr;
+        *reinterpret_cast<uint4*>(a.dk + bn * a.r_dk.bn + static_cast<long long>(j) * a.r_dk.l + c * 8) =
+            make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4*>(a.dv + bn * a.r_dv.bn + static_cast<long long>(j) * a.r_dv.l + c * 8) =
+            make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+  }
+}
+
+// evo_bwd_worklist (one block): the items (b, h, key tile, n) of the per-key-tile kernel
+// whose key tile row (b, n) keeps, in item order.  The kept n depend on (b, key tile)
+// only, so each (b, key tile) pair lists them once (one warp per pair), and every head
+// copies that list into its place.
+__global__ void __launch_bounds__(1024) evo_bwd_worklist(const BwdArgs a) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, KT = a.QT;
+  const int pairs = a.B * KT;
+  uint32_t* cnt = a.wl_cnt;               // [B*KT] kept n of each (b, key tile)
+  uint32_t* pre = a.wl_cnt + pairs;       // [B*KT] their offsets within one head of b
+  uint32_t* per_head = pre + pairs;       // [B] items of one head of b
+  uint32_t* start = per_head + a.B;       // [B] where b's items start
+  for (int p = warp; p < pairs; p += 32) {
+    const int b = p / KT, jt = p % KT;
+    uint32_t c = 0;
+    for (int n0 = 0; n0 < a.N; n0 += 32) {
+      const int n = n0 + lane;
+      const bool keep = n < a.N && !((a.tskip[static_cast<long long>(b) * a.N + n] >> jt) & 1ull);
+      const uint32_t bal = __ballot_sync(0xffffffffu, keep);
+      if (keep) a.wl_n[static_cast<long long>(p) * a.N + c + __popc(bal & ((1u << lane) - 1u))] = n;
+      c += __popc(bal);
+    }
+    if (lane == 0) cnt[p] = c;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t at = 0;
+    for (int b = 0; b < a.B; ++b) {
+      uint32_t sum = 0;
+      for (int jt = 0; jt < KT; ++jt) {
+        pre[b * KT + jt] = sum;
+        sum += cnt[b * KT + jt];
+      }
+      per_head[b] = sum;
+      start[b] = at;
+      at += sum * a.H;
+    }
+    *a.wl_total = at;
+  }
+  __syncthreads();
+  const long long groups = static_cast<long long>(a.B) * a.H * KT;  // (b, h, key tile), in item order
+  for (long long grp = warp; grp < groups; grp += 32) {
+    const int jt = static_cast<int>(grp % KT);
+    const long long bh = grp / KT;
+    const int h = static_cast<int>(bh % a.H), b = static_cast<int>(bh / a.H), p = b * KT + jt;
+    const uint32_t at = start[b] + h * per_head[b] + pre[p];
+    for (uint32_t r = lane; r < cnt[p]; r += 32)
+      a.wl[at + r] = static_cast<uint32_t>(grp * a.N + a.wl_n[static_cast<long long>(p) * a.N + r]);
+  }
+}
+
 // ============================================================ evo_bwd_db2_sum
 template <bool BF16>
 __global__ void __launch_bounds__(256) evo_bwd_db2_sum(const BwdArgs a) {
@@ -320,13 +398,18 @@ __device__ __forceinline__ void main_producer(const BwdArgs& a, uint8_t* base, c
   const bool tma_b2 = a.bias2_mode == kBias2Tma;
   const uint32_t q_bytes = 2 * kTB + ((B2 == kB2Stream && tma_b2) ? 32768u : 0u);
   uint32_t it_ctr = 0, item_ctr = 0, grp_it = 0, s = 0, ph = 0;
-  KvIter c;
-  c.init(i0, a);
+  KvIter c, p;
+  c.init(item_at(a, i0), a);
+  p = c;
   bool ok = true;
-  for (long long item = i0; ok && item < i1; ++item, ++item_ctr, c.next(a)) {
+  for (long long item = i0; ok && item < i1; ++item, ++item_ctr) {
+    if (item > i0) {
+      p = c;
+      advance(c, a, item);
+    }
     const int bn = c.b * a.N + c.n, bh = c.b * a.H + c.h;
     const size_t bnh = static_cast<size_t>(bn) * a.H + c.h;
-    if (B2 == kB2Resident && (item == i0 || c.n == 0)) {
+    if (B2 == kB2Resident && (item == i0 || !c.same_group(p))) {
       if (!mbar_wait(smem_u32(&bars->b2_empty), (grp_it & 1) ^ 1, g)) { ok = false; break; }
       const uint32_t full = smem_u32(&bars->b2_full);
       if (tma_b2) {
@@ -673,17 +756,22 @@ __device__ __forceinline__ void main_compute(const BwdArgs& a, uint8_t* base, co
   const int QS = a.q_stages, QT = a.QT;
   uint32_t u = 0, item_ctr = 0, grp_it = 0, s = 0, ph = 0;
   KvIter cur, prev;
-  cur.init(i0, a);
+  cur.init(item_at(a, i0), a);
   prev = cur;
   int prev_it = 0;
   bool ok = true;
   for (long long item = i0; ok && item < i1; ++item, ++item_ctr) {
     if (item > i0) {
       prev = cur;
-      cur.next(a);
+      advance(cur, a, item);
     }
-    const bool grp_last = item + 1 == i1 || cur.n == a.N - 1;
-    if (B2 == kB2Resident && (item == i0 || cur.n == 0)) {
+    bool grp_last = item + 1 == i1;
+    if (B2 == kB2Resident && !grp_last) {
+      KvIter nx = cur;
+      advance(nx, a, item + 1);
+      grp_last = !nx.same_group(cur);
+    }
+    if (B2 == kB2Resident && (item == i0 || !cur.same_group(prev))) {
       if (!mbar_wait(smem_u32(&bars->b2_full), grp_it & 1, g)) { ok = false; break; }
       ++grp_it;
     }
@@ -761,8 +849,12 @@ __global__ void __launch_bounds__(kThreads, 1) evo_bwd_main(const __grid_constan
   const MainLayout<DP> lay(B2, a.q_stages, a.QT);
   MainBars* bars = reinterpret_cast<MainBars*>(base + lay.bars);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long i0 = static_cast<long long>(blockIdx.x) * a.chunk;
-  const long long i1 = i0 + a.chunk < a.items ? i0 + a.chunk : a.items;
+  // the CTA's contiguous range of list positions: of the items themselves, or of the
+  // work list of masked-tile skipping (its length known only on the device)
+  const long long items = a.wl ? static_cast<long long>(*a.wl_total) : a.items;
+  const long long chunk = a.wl ? (items + gridDim.x - 1) / gridDim.x : a.chunk;
+  const long long i0 = static_cast<long long>(blockIdx.x) * chunk;
+  const long long i1 = i0 + chunk < items ? i0 + chunk : (items > i0 ? items : i0);  // empty past the end
   if (threadIdx.x == 0) {
     bars->abort = 0;
     for (int s = 0; s < 2; ++s) {
@@ -1687,7 +1779,8 @@ cudaError_t launch_main(BwdArgs a, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   const long long sms = num_sms();
   a.chunk = (a.items + sms - 1) / sms;
-  const long long grid = (a.items + a.chunk - 1) / a.chunk;
+  // with a work list every CTA splits the list's (device-side) length evenly
+  const long long grid = a.wl ? (a.items < sms ? a.items : sms) : (a.items + a.chunk - 1) / a.chunk;
   kern<<<static_cast<unsigned>(grid), kThreads, smem, st>>>(a);
   return cudaGetLastError();
 }
@@ -1744,6 +1837,14 @@ cudaError_t launch_bwd_d(BwdArgs a, cudaStream_t st, const ProfileEvents* prof) 
     prof_record(prof, 5, st);  // no dQ cast in slice mode
   } else {
 
+  if (a.tile_skip) {  // masked key tiles: skip bits and zero dK/dV rows, then the work list
+    evo_bwd_tile_mask<BF16><<<grid_for(static_cast<long long>(a.B) * a.N * 32, 256), 256, 0, st>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    evo_bwd_worklist<<<1, 1024, 0, st>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  } else {
+    a.wl = nullptr;
+  }
   // main kernel: deepest Q/dO ring that fits, resident pair-bias tiles when possible
   auto fits = [&](int kind, int qs) { return MainLayout<DP>(kind, qs, a.QT).total + 1024 <= kMaxSmem; };
   if (!has_b2) {

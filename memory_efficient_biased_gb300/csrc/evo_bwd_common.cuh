@@ -136,7 +136,22 @@ struct KvIter {
       }
     }
   }
+  // same (b, h, key tile): the items that share resident pair-bias tiles
+  __device__ __forceinline__ bool same_group(const KvIter& o) const { return b == o.b && h == o.h && jt == o.jt; }
 };
+
+// Item at position idx of a per-key-tile kernel's range: the position itself, or the
+// entry of the masked-tile-skipping work list.
+__device__ __forceinline__ long long item_at(const BwdArgs& a, long long idx) {
+  return a.wl ? static_cast<long long>(a.wl[idx]) : idx;
+}
+// c becomes the item at position idx, the one after c's position.
+__device__ __forceinline__ void advance(KvIter& c, const BwdArgs& a, long long idx) {
+  if (a.wl)
+    c.init(a.wl[idx], a);
+  else
+    c.next(a);
+}
 
 // (b, h, n) slice iterator, n fastest.
 struct SlIter {

@@ -75,7 +75,16 @@ struct FwdBars {
   uint64_t drain;
   uint32_t tmem_slot;
   int abort;
+  // per K/V stage, written by the producer before it arrives on kv_full: the key tile
+  // held (bits 0-15), first tile of its item (bit 16), last tile of its item (bit 17)
+  uint32_t tile_meta[kMaxStages];
 };
+
+constexpr uint32_t kTileFirst = 1u << 16, kTileLast = 1u << 17;
+// The same tag for tile x of an item that runs all KT tiles (no skipping).
+__device__ __forceinline__ uint32_t tile_meta_all(int x, int KT) {
+  return static_cast<uint32_t>(x) | (x == 0 ? kTileFirst : 0u) | (x + 1 == KT ? kTileLast : 0u);
+}
 
 template <int DP>
 struct FwdLayout {
@@ -159,7 +168,9 @@ __device__ __forceinline__ void fill_b2_loads(uint8_t* dst, const uint16_t* b2, 
 }
 
 // ------------------------------------------------------------ producer (one warp)
-template <int DP, bool BF16, int B2>
+// SKIP: masked-tile skipping; the consumers then follow the stage tags (tile_meta)
+// instead of counting the tiles of an item themselves.
+template <int DP, bool BF16, int B2, bool SKIP>
 __device__ __forceinline__ void fwd_producer(const FwdArgs& a, uint8_t* base, const FwdLayout<DP>& lay,
                                              FwdBars* bars, const WaitGuard& g, int lane, long long i0,
                                              long long i1) {
@@ -173,6 +184,11 @@ __device__ __forceinline__ void fwd_producer(const FwdArgs& a, uint8_t* base, co
   // raw key-mask values of the next tile, loaded one tile ahead so that their
   // latency overlaps the wait for a free stage
   uint16_t b1raw[4];
+  // the item's key tiles: every tile, or with masked-tile skipping those holding a kept key
+  auto tiles_of = [&](const ItemIter& t) -> uint64_t {
+    if (!SKIP || !a.bias1 || t.b >= a.B) return 0ull;
+    return kept_tiles<BF16>(a.bias1 + (static_cast<size_t>(t.b) * a.N + t.n) * a.L, a.L, a.skip_at, lane);
+  };
   auto b1_prefetch = [&](const ItemIter& t, int jt) {
     const uint16_t* row = (a.bias1 && t.b < a.B) ? a.bias1 + (static_cast<size_t>(t.b) * a.N + t.n) * a.L : nullptr;
 #pragma unroll
@@ -181,10 +197,17 @@ __device__ __forceinline__ void fwd_producer(const FwdArgs& a, uint8_t* base, co
       b1raw[e] = (row && j < a.L) ? row[j] : static_cast<uint16_t>(0);
     }
   };
-  b1_prefetch(c, 0);
+  // next item's key-mask row, loaded one item ahead and scanned at the item's last tile
+  // (rows too long for registers are scanned at once)
+  RowScan nscan;
+  const bool scan_ahead = SKIP && a.bias1 && row_scan_fits(a.bias1, a.L);
+  uint64_t act = tiles_of(c);
+  b1_prefetch(c, next_tile(act, -1, KT));
   bool ok = true;
   for (long long item = i0; ok && item < i1; ++item, c.next(a)) {
     const int bn = c.b * a.N + c.n, bh = c.b * a.H + c.h;
+    ItemIter nc = c;
+    nc.next(a);
     if (B2 == kB2Resident && (item == i0 || c.n == 0)) {
       // all softmax warps are done with the previous group's tiles
       if (!mbar_wait(smem_u32(&bars->b2_empty), (grp_it & 1) ^ 1, g)) { ok = false; break; }
@@ -213,10 +236,20 @@ __device__ __forceinline__ void fwd_producer(const FwdArgs& a, uint8_t* base, co
       tma_load_4d(smem_u32(base + lay.q[qs]), &a.tq, smem_u32(&bars->q_full[qs]), 0, c.h, c.qt * kTile, bn);
     }
     ++q_it;
-    for (int jt = 0; jt < KT; ++jt, ++u) {
+    uint64_t next_act = 0;
+    const bool nc_in = nc.b < a.B;
+    if (scan_ahead) {
+      if (nc_in) row_scan_issue(nscan, a.bias1 + (static_cast<size_t>(nc.b) * a.N + nc.n) * a.L, a.L, lane);
+    } else {
+      next_act = tiles_of(nc);
+    }
+    const int jt0 = next_tile(act, -1, KT);
+    for (int jt = jt0; jt < KT; ++u) {
+      const int jn = next_tile(act, jt, KT);
       if (!mbar_wait(smem_u32(&bars->kv_empty[s]), ph ^ 1, g)) { ok = false; break; }
       const uint32_t full = smem_u32(&bars->kv_full[s]);
       if (lane == 0) {  // copies first: the key-mask loads below must not delay them
+        bars->tile_meta[s] = static_cast<uint32_t>(jt) | (jt == jt0 ? kTileFirst : 0u) | (jn >= KT ? kTileLast : 0u);
         mbar_expect_tx(full, kv_bytes);
         tma_load_4d(smem_u32(base + lay.k[s]), &a.tk, full, 0, c.h, jt * kTile, bn);
         tma_load_4d(smem_u32(base + lay.v[s]), &a.tv, full, 0, c.h, jt * kTile, bn);
@@ -239,18 +272,19 @@ __device__ __forceinline__ void fwd_producer(const FwdArgs& a, uint8_t* base, co
         *reinterpret_cast<float4*>(base + lay.b1[s] + lane * 16) = m4;
       }
       mbar_arrive(full);
-      if (jt + 1 < KT) {
-        b1_prefetch(c, jt + 1);
+      if (jn < KT) {
+        b1_prefetch(c, jn);
       } else {
-        ItemIter nc = c;
-        nc.next(a);
-        b1_prefetch(nc, 0);
+        if (scan_ahead && nc_in) next_act = row_scan_finish<BF16>(nscan, a.L, a.skip_at, lane);
+        b1_prefetch(nc, next_tile(next_act, -1, KT));
       }
       if (++s == static_cast<uint32_t>(S)) {
         s = 0;
         ph ^= 1;
       }
+      jt = jn;
     }
+    act = next_act;
   }
   // Drain: every copy this warp started has landed before the CTA may exit.
   for (uint32_t q = 0; q < 2; ++q) {
@@ -266,9 +300,9 @@ __device__ __forceinline__ void fwd_producer(const FwdArgs& a, uint8_t* base, co
 
 // ------------------------------------------------------------ MMA issuer (one thread)
 // O_half (+)= P_v,half · V_v,half for both key halves (K = 64 keys each), P from
-// TMEM, accumulated over the key tiles of item `item` (tile jt of KT).
+// TMEM, accumulated over the key tiles of item `item` (meta: first / last tile of it).
 template <int DP, bool BF16>
-__device__ __forceinline__ bool fwd_issue_pv(uint32_t v, uint32_t sv, int jt, int KT, uint32_t item, uint8_t* base,
+__device__ __forceinline__ bool fwd_issue_pv(uint32_t v, uint32_t sv, uint32_t meta, uint32_t item, uint8_t* base,
                                              const FwdLayout<DP>& lay, FwdBars* bars, uint32_t tmem,
                                              const WaitGuard& g) {
   constexpr uint32_t RB = DP * 2;
@@ -278,10 +312,11 @@ __device__ __forceinline__ bool fwd_issue_pv(uint32_t v, uint32_t sv, int jt, in
   const uint32_t vb = v & 1, vph = (v >> 1) & 1;
   const uint32_t ob = item % NB, oph = (item / NB) & 1;
   if (!mbar_wait(smem_u32(&bars->p_full[vb]), vph, g)) return false;
-  if (jt == 0 && !mbar_wait(smem_u32(&bars->o_free[ob]), oph ^ 1, g)) return false;
+  const bool first = (meta & kTileFirst) != 0;
+  if (first && !mbar_wait(smem_u32(&bars->o_free[ob]), oph ^ 1, g)) return false;
   tc_fence_after();
   const uint64_t vd = smem_desc(smem_u32(base + lay.v[sv]), kTile * RB, 8 * RB, SWZ);
-  const uint32_t acc = jt > 0 ? 1u : 0u;
+  const uint32_t acc = first ? 0u : 1u;
 #pragma unroll
   for (int half = 0; half < 2; ++half) {
 #pragma unroll
@@ -290,21 +325,20 @@ __device__ __forceinline__ bool fwd_issue_pv(uint32_t v, uint32_t sv, int jt, in
               id_o, (acc | k) ? 1u : 0u);
   }
   umma_commit(smem_u32(&bars->pv_done));
-  if (jt == KT - 1) umma_commit(smem_u32(&bars->o_full[ob]));
+  if (meta & kTileLast) umma_commit(smem_u32(&bars->o_full[ob]));
   umma_commit(smem_u32(&bars->p_empty[vb]));
   umma_commit(smem_u32(&bars->kv_empty[sv]));
   return true;
 }
 
-template <int DP, bool BF16>
+template <int DP, bool BF16, bool SKIP>
 __device__ __forceinline__ void fwd_mma(const FwdArgs& a, uint8_t* base, const FwdLayout<DP>& lay, FwdBars* bars,
                                         uint32_t tmem, const WaitGuard& g, long long i0, long long i1) {
   constexpr uint32_t RB = DP * 2;
   constexpr uint32_t SWZ = swizzle_for_row(RB);
   constexpr uint32_t id_s = idesc_f16(128, 128, BF16, false, false);
   const int S = a.stages, KT = a.QT;
-  uint32_t u = 0, q_it = 0, prev_stage = 0, s = 0, ph = 0, item_ord = 0, prev_item = 0;
-  int prev_jt = 0;
+  uint32_t u = 0, q_it = 0, prev_stage = 0, s = 0, ph = 0, item_ord = 0, prev_item = 0, prev_meta = 0;
   bool ok = true;
   for (long long item = i0; ok && item < i1; ++item, ++item_ord) {
     const uint32_t qs = q_it & 1;
@@ -312,8 +346,10 @@ __device__ __forceinline__ void fwd_mma(const FwdArgs& a, uint8_t* base, const F
     ++q_it;
     tc_fence_after();
     const uint64_t qd = smem_desc(smem_u32(base + lay.q[qs]), 16, 8 * RB, SWZ);
-    for (int jt = 0; jt < KT; ++jt) {
+    for (int x = 0; SKIP || x < KT; ++x) {  // with SKIP, up to the tile tagged last
       if (!mbar_wait(smem_u32(&bars->kv_full[s]), ph, g)) { ok = false; break; }
+      const uint32_t meta = SKIP ? bars->tile_meta[s] : tile_meta_all(x, KT);
+      const bool last = (meta & kTileLast) != 0;
       const uint32_t buf = u & 1;
       if (!mbar_wait(smem_u32(&bars->s_free[buf]), ((u >> 1) & 1) ^ 1, g)) { ok = false; break; }
       tc_fence_after();
@@ -321,22 +357,23 @@ __device__ __forceinline__ void fwd_mma(const FwdArgs& a, uint8_t* base, const F
 #pragma unroll
       for (int k = 0; k < DP / 16; ++k) umma_ss(tmem + col_s(buf), qd + k * 2, kd + k * 2, id_s, k > 0);
       umma_commit(smem_u32(&bars->s_full[buf]));
-      if (jt == KT - 1) umma_commit(smem_u32(&bars->q_empty[qs]));
-      if (u > 0 && !fwd_issue_pv<DP, BF16>(u - 1, prev_stage, prev_jt, KT, prev_item, base, lay, bars, tmem, g)) {
+      if (last) umma_commit(smem_u32(&bars->q_empty[qs]));
+      if (u > 0 && !fwd_issue_pv<DP, BF16>(u - 1, prev_stage, prev_meta, prev_item, base, lay, bars, tmem, g)) {
         ok = false;
         break;
       }
       prev_stage = s;
-      prev_jt = jt;
+      prev_meta = meta;
       prev_item = item_ord;
       ++u;
       if (++s == static_cast<uint32_t>(S)) {
         s = 0;
         ph ^= 1;
       }
+      if (SKIP && last) break;
     }
   }
-  if (ok && u > 0) fwd_issue_pv<DP, BF16>(u - 1, prev_stage, prev_jt, KT, prev_item, base, lay, bars, tmem, g);
+  if (ok && u > 0) fwd_issue_pv<DP, BF16>(u - 1, prev_stage, prev_meta, prev_item, base, lay, bars, tmem, g);
   // Drain: all MMAs this thread issued are complete before TMEM is freed.
   umma_commit(smem_u32(&bars->drain));
   drain_wait(smem_u32(&bars->drain), 0, a.wait_ns, a.status);
@@ -446,7 +483,7 @@ __device__ __forceinline__ bool fwd_epilogue(const FwdArgs& a, const ItemIter& c
   return true;
 }
 
-template <int DP, bool BF16, int B2>
+template <int DP, bool BF16, int B2, bool SKIP>
 __device__ __forceinline__ void fwd_softmax(const FwdArgs& a, uint8_t* base, const FwdLayout<DP>& lay,
                                             FwdBars* bars, uint32_t tmem, const WaitGuard& g, long long i0,
                                             long long i1) {
@@ -476,13 +513,17 @@ __device__ __forceinline__ void fwd_softmax(const FwdArgs& a, uint8_t* base, con
       if (!mbar_wait(smem_u32(&bars->b2_full), grp_it & 1, g)) { ok = false; break; }
       ++grp_it;
     }
-    for (int jt = 0; jt < KT; ++jt) {
-      if (jt == 0) {  // the previous item's statistics, for its epilogue (-inf: no unmasked key)
+    for (int x = 0; SKIP || x < KT; ++x) {  // with SKIP, up to the tile tagged last
+      const bool first = x == 0;
+      if (first) {  // the previous item's statistics, for its epilogue (-inf: no unmasked key)
         m_fin = have ? m : -INFINITY;
         l_fin = l;
       }
       const uint32_t buf = u & 1, bph = (u >> 1) & 1;
       if (!mbar_wait(smem_u32(&bars->kv_full[s]), ph, g)) { ok = false; break; }
+      const uint32_t meta = SKIP ? bars->tile_meta[s] : tile_meta_all(x, KT);
+      const int jt = static_cast<int>(meta & 0xffffu);
+      const bool last = (meta & kTileLast) != 0;
       if (!mbar_wait(smem_u32(&bars->s_full[buf]), bph, g)) { ok = false; break; }
       tc_fence_after();
       float y[64];
@@ -528,7 +569,7 @@ __device__ __forceinline__ void fwd_softmax(const FwdArgs& a, uint8_t* base, con
       if (lane == 0) {
         mbar_arrive(smem_u32(&bars->s_free[buf]));
         mbar_arrive(smem_u32(&bars->kv_empty[s]));
-        if (B2 == kB2Resident && grp_last && jt == KT - 1) mbar_arrive(smem_u32(&bars->b2_empty));
+        if (B2 == kB2Resident && grp_last && last) mbar_arrive(smem_u32(&bars->b2_empty));
       }
       const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
       // reference max: the first tile's max (0 when every key so far is masked); later
@@ -536,10 +577,10 @@ __device__ __forceinline__ void fwd_softmax(const FwdArgs& a, uint8_t* base, con
       // (have: a finite reference exists; until then every P is exactly 0 and so is
       // the accumulator, so the first unmasked tile just sets the reference)
       float alpha = 1.0f;
-      if (jt == 0 || !have) {
+      if (first || !have) {
         have = mt != -INFINITY;
         m = have ? mt : 0.0f;
-        if (jt == 0) l = 0.0f;
+        if (first) l = 0.0f;
       } else if (mt > m + kRescaleLog2) {
         alpha = ex2(m - mt);
         m = mt;
@@ -572,7 +613,7 @@ __device__ __forceinline__ void fwd_softmax(const FwdArgs& a, uint8_t* base, con
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&bars->p_full[buf]));
-      if (jt == 0 && u > 0 &&
+      if (first && u > 0 &&
           !fwd_epilogue<DP, BF16>(a, prev, m_fin, l_fin, fin++, base, lay, bars, trow, w, quad, hc, r, lane, g)) {
         ok = false;
         break;
@@ -582,6 +623,7 @@ __device__ __forceinline__ void fwd_softmax(const FwdArgs& a, uint8_t* base, con
         s = 0;
         ph ^= 1;
       }
+      if (SKIP && last) break;
     }
   }
   if (ok && u > 0)
@@ -589,7 +631,7 @@ __device__ __forceinline__ void fwd_softmax(const FwdArgs& a, uint8_t* base, con
   if (lane == 0) bulk_wait_all();  // this warp's O stores complete before the CTA's smem goes away
 }
 
-template <int DP, bool BF16, int B2>
+template <int DP, bool BF16, int B2, bool SKIP>
 __global__ void __launch_bounds__(kThreads, 1) evo_fwd_kernel(const __grid_constant__ FwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -643,12 +685,12 @@ __global__ void __launch_bounds__(kThreads, 1) evo_fwd_kernel(const __grid_const
   const WaitGuard g{a.wait_ns, a.status, &bars->abort};
 
   if (warp == kProducerWarp) {
-    fwd_producer<DP, BF16, B2>(a, base, lay, bars, g, lane, i0, i1);
+    fwd_producer<DP, BF16, B2, SKIP>(a, base, lay, bars, g, lane, i0, i1);
   } else if (warp == kMmaWarp) {
-    if (lane == 0) fwd_mma<DP, BF16>(a, base, lay, bars, tmem, g, i0, i1);
+    if (lane == 0) fwd_mma<DP, BF16, SKIP>(a, base, lay, bars, tmem, g, i0, i1);
     __syncwarp();
   } else {
-    fwd_softmax<DP, BF16, B2>(a, base, lay, bars, tmem, g, i0, i1);
+    fwd_softmax<DP, BF16, B2, SKIP>(a, base, lay, bars, tmem, g, i0, i1);
   }
 
   tc_fence_before();
@@ -661,13 +703,13 @@ __global__ void __launch_bounds__(kThreads, 1) evo_fwd_kernel(const __grid_const
 
 constexpr size_t kMaxSmem = 232448;  // 227 KB opt-in limit per block
 
-template <int DP, bool BF16, int B2>
-cudaError_t launch_fwd_t(FwdArgs a, cudaStream_t st) {
+template <int DP, bool BF16, int B2, bool SKIP>
+cudaError_t launch_fwd_s(FwdArgs a, cudaStream_t st) {
   const FwdLayout<DP> lay(B2, a.stages, a.QT);
   // At least 116 KB so that two CTAs never share an SM: each allocates all 512
   // TMEM columns, and a second resident CTA would stall in tcgen05.alloc.
   const size_t smem = (lay.total + 1024 > 116u * 1024u) ? lay.total + 1024 : 116u * 1024u;
-  auto kern = evo_fwd_kernel<DP, BF16, B2>;
+  auto kern = evo_fwd_kernel<DP, BF16, B2, SKIP>;
   static bool limit_set[64] = {};
   cudaError_t e = ensure_smem_limit(kern, kMaxSmem, limit_set);
   if (e != cudaSuccess) return e;
@@ -676,6 +718,10 @@ cudaError_t launch_fwd_t(FwdArgs a, cudaStream_t st) {
   const long long grid = (a.items + a.chunk - 1) / a.chunk;
   kern<<<static_cast<unsigned>(grid), kThreads, smem, st>>>(a);
   return cudaGetLastError();
+}
+template <int DP, bool BF16, int B2>
+cudaError_t launch_fwd_t(FwdArgs a, cudaStream_t st) {
+  return a.tile_skip ? launch_fwd_s<DP, BF16, B2, true>(a, st) : launch_fwd_s<DP, BF16, B2, false>(a, st);
 }
 
 // Deepest K/V ring that fits, and whether the pair-bias tiles of one

@@ -26,6 +26,9 @@ namespace evo {
 __device__ int g_evo_status = 0;
 
 static std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
+// Masked key-tile skipping (evo_attn_set_masked_tile_skip): off by default.
+static std::atomic<int> g_skip_on{0};
+static std::atomic<float> g_skip_at{-1.0e4f};
 static ProfileEvents g_prof{{nullptr}, 0};
 
 // What made this thread's last call return EVO_ERR_CUDA (evo_attn_last_error_detail).
@@ -282,7 +285,8 @@ int b2t_pitch(const evo_shape_t& s) { return static_cast<int>((s.L + 7) / 8 * 8)
 // planes whenever there is a pair bias.
 struct WsLayout {
   BwdPlan plan;
-  size_t delta, dq_acc, b2t, db1p, db2, total;
+  size_t delta, dq_acc, b2t, db1p, db2, skip, total;
+  bool can_skip;  // room for the masked-tile work list (per-key-tile schedule, at most 64 key tiles)
 };
 WsLayout ws_layout(const evo_shape_t& s, bool has_bias2, bool has_db1 = false) {
   WsLayout w{};
@@ -303,6 +307,14 @@ WsLayout ws_layout(const evo_shape_t& s, bool has_bias2, bool has_db1 = false) {
     bwd_groups(s, &g, &gs);
     off += round256(size_t(g) * s.B * s.H * s.L * s.L * 4);
   }
+  // masked-tile skipping of the per-key-tile kernel: skip bits [B*N] u64, kept n
+  // [B*QT][N], counts and offsets [2*B*QT + 2*B], the work list [items], its length
+  const int64_t QT = (s.L + kTile - 1) / kTile, items = s.B * s.H * QT * s.N;
+  w.skip = off;
+  w.can_skip = w.plan.mode == kBwdMain && QT <= 64 && items <= int64_t(0xffffffffll);
+  if (w.can_skip)
+    off += round256(size_t(s.B) * s.N * 8) +
+           round256((size_t(s.B) * QT * s.N + 2 * size_t(s.B) * QT + 2 * size_t(s.B) + size_t(items) + 1) * 4);
   w.total = off;
   return w;
 }
@@ -364,6 +376,11 @@ const char* evo_status_string(evo_status_t s) {
 }
 
 void evo_attn_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns < 1000 ? 1000 : ns); }
+
+void evo_attn_set_masked_tile_skip(int enable, float threshold) {
+  g_skip_at.store(threshold);
+  g_skip_on.store(enable != 0);
+}
 
 evo_status_t evo_attn_fwd(const void* q, const void* k, const void* v, const void* bias1, const void* bias2,
                           void* out, float* lse, evo_shape_t shape, evo_dtype_t dtype, void* stream) {
@@ -438,6 +455,8 @@ evo_status_t evo_attn_fwd_strided(const void* q, const void* k, const void* v, c
     a.QT = static_cast<int>((shape.L + kTile - 1) / kTile);
     a.items = sub.B * shape.N * shape.H * a.QT;
     a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(shape.D)));
+    a.tile_skip = g_skip_on.load() && bias1 && a.QT <= 64;
+    a.skip_at = g_skip_at.load();
     a.wait_ns = g_wait_limit_ns.load();
     a.status = dev->status;
     const cudaError_t e = launch_fwd(a, padded_dim(shape.D), bf16, cs);
@@ -599,6 +618,16 @@ evo_status_t evo_attn_bwd_strided(const void* q, const void* k, const void* v, c
     }
     a.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(shape.D)));
     a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(shape.D)));
+    if (g_skip_on.load() && bias1 && w.can_skip) {
+      const size_t rows = size_t(sub.B) * shape.N, pairs = size_t(sub.B) * a.QT;
+      a.tile_skip = 1;
+      a.skip_at = g_skip_at.load();
+      a.tskip = reinterpret_cast<unsigned long long*>(ws + w.skip);
+      a.wl_n = reinterpret_cast<uint32_t*>(ws + w.skip + round256(rows * 8));
+      a.wl_cnt = a.wl_n + pairs * shape.N;
+      a.wl = a.wl_cnt + 2 * pairs + 2 * size_t(sub.B);
+      a.wl_total = a.wl + size_t(sub.B) * shape.H * a.QT * shape.N;
+    }
     a.wait_ns = g_wait_limit_ns.load();
     a.status = dev->status;
     const cudaError_t e = launch_bwd(a, padded_dim(shape.D), bf16, static_cast<cudaStream_t>(stream), &g_prof);

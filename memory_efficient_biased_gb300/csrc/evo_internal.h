@@ -36,6 +36,8 @@ struct FwdArgs {
   int b2_resident;          // pair-bias tiles of the current (b, h, q-tile) kept in smem
   float scale_log2;         // D^-1/2 * log2(e)
   int bias2_mode;
+  int tile_skip;            // skip key tiles whose every key mask is <= skip_at (QT <= 64 only)
+  float skip_at;
   uint64_t wait_ns;
   int* status;
 };
@@ -77,6 +79,17 @@ struct BwdArgs {
   int part_stages;          // pair-bias partial kernel: depth of its ring
   int db2p_tma;             // pair-bias partial kernel: tile stores through tdb2p (L % 4 == 0)
   int zero_dq;              // delta kernel also clears the fp32 dQ accumulator
+  // Masked key-tile skipping in the per-key-tile kernel (tile_skip; QT <= 64): the
+  // items it runs come from a work list built on the device, in item order, without the
+  // (b, n, key tile) items whose every key mask is <= skip_at (rows with no kept key skip
+  // nothing); dK and dV of the skipped key tiles are written as zeros.
+  int tile_skip;
+  float skip_at;
+  unsigned long long* tskip;  // workspace [B*N]: key tiles of each row to skip, as bits
+  uint32_t* wl_n;             // workspace [B*QT][N]: the n of each (b, key tile) that are kept
+  uint32_t* wl_cnt;           // workspace [B*QT] counts; then [B*QT] offsets within b; [B] per-b totals
+  uint32_t* wl;               // workspace [items]: the work list (item numbers, ascending)
+  uint32_t* wl_total;         // workspace: its length
   float scale;              // D^-1/2
   float scale_log2;         // D^-1/2 * log2(e)
   int bias2_mode;

@@ -424,6 +424,92 @@ __device__ __forceinline__ float to_f32(uint16_t v) {
   }
 }
 
+// ---------------------------------------------------------------- masked key tiles
+// The 128-key tiles of one (b, n) row that hold at least one key whose bias1 is not at
+// or below `skip_at` (a NaN counts as kept), as a bit set over at most 64 tiles;
+// computed by one warp, the result is the same in every lane.  0 when no key of the
+// row is kept: such a row skips nothing.
+template <bool BF16>
+__device__ __forceinline__ uint64_t kept_tiles(const uint16_t* row, int L, float skip_at, int lane) {
+  uint32_t lo = 0, hi = 0;
+  auto mark = [&](int t) {
+    if (t < 32)
+      lo |= 1u << t;
+    else
+      hi |= 1u << (t - 32);
+  };
+  if ((reinterpret_cast<uintptr_t>(row) & 15) == 0 && (L & 7) == 0) {
+    // 16-byte loads, all in flight together: eight keys each, always of one tile
+    const uint4* r4 = reinterpret_cast<const uint4*>(row);
+#pragma unroll 4
+    for (int c = lane; c < (L >> 3); c += 32) {
+      const uint4 v = __ldg(r4 + c);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      bool kept = false;
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        kept = kept || !(unpack_lo<BF16>(w[e]) <= skip_at) || !(unpack_hi<BF16>(w[e]) <= skip_at);
+      if (kept) mark(c >> 4);
+    }
+  } else {
+#pragma unroll 8
+    for (int j = lane; j < L; j += 32)
+      if (!(to_f32<BF16>(row[j]) <= skip_at)) mark(j >> 7);
+  }
+  lo = __reduce_or_sync(0xffffffffu, lo);
+  hi = __reduce_or_sync(0xffffffffu, hi);
+  return (static_cast<uint64_t>(hi) << 32) | lo;
+}
+
+// kept_tiles in two halves, so that a caller can start the loads long before it needs
+// the answer: rows of at most 8 * 32 * kScanChunks keys, 16-byte aligned, L % 8 == 0.
+constexpr int kScanChunks = 8;
+struct RowScan {
+  uint4 v[kScanChunks];
+};
+__device__ __forceinline__ bool row_scan_fits(const uint16_t* base, int L) {
+  return (reinterpret_cast<uintptr_t>(base) & 15) == 0 && (L & 7) == 0 && L <= 8 * 32 * kScanChunks;
+}
+__device__ __forceinline__ void row_scan_issue(RowScan& r, const uint16_t* row, int L, int lane) {
+  const uint4* r4 = reinterpret_cast<const uint4*>(row);
+#pragma unroll
+  for (int q = 0; q < kScanChunks; ++q) {
+    const int c = lane + 32 * q;
+    r.v[q] = c < (L >> 3) ? __ldg(r4 + c) : make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+template <bool BF16>
+__device__ __forceinline__ uint64_t row_scan_finish(const RowScan& r, int L, float skip_at, int lane) {
+  uint32_t lo = 0, hi = 0;
+#pragma unroll
+  for (int q = 0; q < kScanChunks; ++q) {
+    const int c = lane + 32 * q;
+    const uint32_t w[4] = {r.v[q].x, r.v[q].y, r.v[q].z, r.v[q].w};
+    bool kept = false;
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      kept = kept || !(unpack_lo<BF16>(w[e]) <= skip_at) || !(unpack_hi<BF16>(w[e]) <= skip_at);
+    if (kept && c < (L >> 3)) {
+      const int t = c >> 4;
+      if (t < 32)
+        lo |= 1u << t;
+      else
+        hi |= 1u << (t - 32);
+    }
+  }
+  lo = __reduce_or_sync(0xffffffffu, lo);
+  hi = __reduce_or_sync(0xffffffffu, hi);
+  return (static_cast<uint64_t>(hi) << 32) | lo;
+}
+
+// The first tile after `jt` in the set `act` (jt = -1: the first one); KT when none is
+// left.  act == 0 stands for every tile, in order.
+__device__ __forceinline__ int next_tile(uint64_t act, int jt, int KT) {
+  if (act == 0) return jt + 1 < KT ? jt + 1 : KT;
+  const uint64_t rest = jt >= 63 ? 0ull : act & (~0ull << (jt + 1));
+  return rest ? __ffsll(static_cast<long long>(rest)) - 1 : KT;
+}
+
 __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
   asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a),
                "f"(b), "f"(c), "f"(d)

@@ -35,7 +35,7 @@ EXPORTED = ("evo_attn_abi_version", "evo_status_string", "evo_attn_fwd", "evo_at
             "evo_attn_bwd", "evo_attn_device_status", "evo_attn_set_wait_limit_ns",
             "evo_attn_selftest_wait_timeout", "evo_attn_profile_events", "evo_attn_step_host_arena_bytes",
             "evo_attn_step_host", "evo_attn_bwd_noalloc", "evo_attn_bwd_ex", "evo_attn_last_error_detail",
-            "evo_attn_fwd_strided", "evo_attn_bwd_strided")
+            "evo_attn_fwd_strided", "evo_attn_bwd_strided", "evo_attn_set_masked_tile_skip")
 
 _DTYPE_CODE = {torch.float16: 0, torch.bfloat16: 1}
 
@@ -111,6 +111,8 @@ def load(path: Optional[str] = None):
     lib.evo_attn_last_error_detail.argtypes = []
     lib.evo_attn_bwd_ex.restype = i32
     lib.evo_attn_bwd_ex.argtypes = [vp] * 14 + [sz, EvoShape, i32, vp]
+    lib.evo_attn_set_masked_tile_skip.restype = None
+    lib.evo_attn_set_masked_tile_skip.argtypes = [i32, ctypes.c_float]
     lib.evo_attn_fwd_strided.restype = i32
     lib.evo_attn_fwd_strided.argtypes = [vp] * 7 + [EvoShape, i32, ctypes.POINTER(EvoLayout), vp]
     lib.evo_attn_bwd_strided.restype = i32
@@ -356,6 +358,13 @@ def evo_attn_device_status(stream=None) -> int:
 
 def evo_attn_set_wait_limit_ns(ns: int) -> None:
     load().evo_attn_set_wait_limit_ns(int(ns))
+
+
+def evo_attn_set_masked_tile_skip(enable: bool, threshold: float = -1.0e4) -> None:
+    """Masked key-tile skipping for later calls (process-wide; see include/evo_attn.h):
+    keys whose bias1 is <= threshold are masked, and 128-key tiles of a row that hold
+    only masked keys are skipped where the row keeps some key."""
+    load().evo_attn_set_masked_tile_skip(int(bool(enable)), float(threshold))
 
 
 def evo_attn_selftest_wait_timeout(limit_ns: int, stream=None) -> int:

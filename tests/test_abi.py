@@ -128,9 +128,14 @@ def test_workspace_bytes(lib):
     extra = with_b2 - no_b2 - 1 * 4 * 256 * 256 * 2
     plane = 1 * 4 * 256 * 256 * 4
     assert extra % plane == 0 and 1 <= extra // plane <= 256
-    # per-key-tile backward (D = 64, L = 384): delta plus the fp32 dQ accumulator
+    # per-key-tile backward (D = 64, L = 384): delta, the fp32 dQ accumulator and the
+    # masked-tile work list: skip bits [B*N] u64, then u32 kept n [B*QT*N], counts and
+    # offsets [2*B*QT + 2*B], the list [items = B*H*QT*N] and its length, each part
+    # rounded up to 256 bytes
     big = shape(B=1, N=4, L=384, H=2, D=64)
-    assert lib.evo_attn_bwd_workspace_bytes(big, 1, 0) == 4 * 2 * 384 * 4 + 4 * 384 * 2 * 64 * 4
+    r256 = lambda x: (x + 255) // 256 * 256
+    skip = r256(4 * 8) + r256((3 * 4 + 2 * 3 + 2 + 2 * 3 * 4 + 1) * 4)
+    assert lib.evo_attn_bwd_workspace_bytes(big, 1, 0) == 4 * 2 * 384 * 4 + 4 * 384 * 2 * 64 * 4 + skip
     # EVO_WS_DBIAS1 adds the fp32 [B,N,H,2,L] key-mask gradient partials
     assert lib.evo_attn_bwd_workspace_bytes(s, 1, 2) - no_b2 == 1 * 256 * 4 * 2 * 256 * 4
     assert lib.evo_attn_bwd_workspace_bytes(shape(D=12), 1, 0) == 0

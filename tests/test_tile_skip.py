@@ -1,0 +1,143 @@
+"""GPU tests of masked key-tile skipping (evo_attn_set_masked_tile_skip).
+
+A key tile whose keys are all masked contributes exactly nothing once exp
+underflows to 0 (web page "DeepSpeed4Science 技术指南…" §3.6: the key mask is
+a large negative bias), so skipping it must leave every result unchanged:
+O, lse, dK, dV and both bias gradients bitwise; dQ, summed by fp32 atomics in
+no fixed order on the per-key-tile schedule, to within rounding.  Cases cover
+tail masks (the same tiles masked in every row), per-row masks (some n of a
+(b, key tile) group skipped, others not — the resident pair-bias path of the
+backward's work list), a streamed pair bias, several batches, strided outputs,
+and a row whose every key is masked (nothing skipped there).
+"""
+import numpy as np
+import pytest
+import torch
+
+from memory_efficient_biased_gb300 import evo_attn as E
+from memory_efficient_biased_gb300.workload import MASK_VALUE, make_inputs
+from oracle import evo_oracle as O
+from tests.parity_util import FWD_TOL, GRAD_TOL, fwd_rel_err, lse_err, np64, rel_l2, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _skip_off_afterwards():
+    yield
+    E.evo_attn_set_masked_tile_skip(False)
+
+
+def masked_rows(inp, spec, seed=0):
+    """Overwrite bias1 by `spec`: ("tail", j0) masks keys >= j0 in every row;
+    ("tiles", p) masks each whole 128-key tile of each row with probability p
+    (keeping tile 0 kept in every row but the last one of each b, which is
+    masked entirely)."""
+    b1 = inp["bias1"].float()
+    B, N, _, _, L = b1.shape
+    kind, arg = spec
+    if kind == "tail":
+        b1[..., arg:] = MASK_VALUE
+    else:
+        rng = np.random.default_rng(seed)
+        KT = (L + 127) // 128
+        for b in range(B):
+            for n in range(N):
+                for t in range(1, KT):
+                    if rng.random() < arg:
+                        b1[b, n, 0, 0, t * 128:(t + 1) * 128] = MASK_VALUE
+            b1[b, N - 1] = MASK_VALUE  # a row with no kept key
+    inp["bias1"] = b1.to(inp["q"].dtype)
+    return inp
+
+
+def run_all(d, dq=None, dk=None, dv=None):
+    out, lse = E.evo_attn_fwd(d["q"], d["k"], d["v"], d["bias1"], d["bias2"])
+    if dq is None:
+        g = E.evo_attn_bwd_ex(d["q"], d["k"], d["v"], d["bias1"], d["bias2"], out, lse, d["do"])
+    else:
+        g = E.evo_attn_bwd_strided(d["q"], d["k"], d["v"], d["bias1"], d["bias2"], out, lse, d["do"],
+                                   dq=dq, dk=dk, dv=dv, want_dbias1=True)
+    torch.cuda.synchronize()
+    assert E.evo_attn_device_status() == 0
+    return (out, lse) + tuple(g)
+
+
+# (B, N, L, H, D, dtype, bias2_sigma, mask spec): backward schedule on the right
+CASES = [
+    (1, 6, 700, 2, 64, "bf16", None, ("tail", 420)),      # per key tile, no pair bias
+    (1, 6, 700, 2, 32, "fp16", None, ("tail", 420)),      # per key tile (D = 32, 6 key tiles)
+    (2, 5, 300, 2, 64, "bf16", 1.0, ("tiles", 0.5)),      # per key tile, resident pair bias, per-row masks
+    (1, 4, 1100, 1, 64, "fp16", 1.0, ("tiles", 0.4)),     # per key tile, streamed pair bias
+    (1, 4, 256, 3, 32, "bf16", 1.0, ("tiles", 0.5)),      # key-major backward: forward skips only
+    (1, 3, 520, 2, 16, "fp16", 0.5, ("tail", 260)),       # slice or key-major backward
+]
+
+
+def _ids(c):
+    return "x".join(map(str, c[:5])) + f"-{c[5]}-{c[7][0]}"
+
+
+@pytest.mark.parametrize("case", CASES, ids=_ids)
+def test_skipping_changes_nothing(case):
+    B, N, L, H, D, dt, sig, spec = case
+    inp = masked_rows(make_inputs(B, N, L, H, D, dtype=dt, mask=None, bias2_sigma=sig, seed=31), spec, seed=7)
+    d = to_dev(inp)
+    E.evo_attn_set_masked_tile_skip(False)
+    ref = run_all(d)
+    E.evo_attn_set_masked_tile_skip(True, -1.0e4)
+    got = run_all(d)
+    names = ("out", "lse", "dq", "dk", "dv", "dbias1", "dbias2")
+    for name, x, y in zip(names, got, ref):
+        if x is None:
+            assert y is None
+        elif name == "dq":
+            assert rel_l2(np64(x), np64(y)) <= 1e-2
+        else:
+            assert torch.equal(x, y), name
+
+    a = {k: np64(v) for k, v in inp.items()}
+    o_ref, lse_ref = O.forward(a["q"], a["k"], a["v"], a["bias1"], a["bias2"])
+    kept = np.isfinite(lse_ref) if dt == "fp16" else np.ones_like(lse_ref, dtype=bool)
+    if dt == "fp16":  # fp16 masks are -inf: the fully masked rows are empty softmaxes
+        assert lse_err(np64(got[1]), lse_ref) <= 1e-3
+    else:  # bf16 masks are finite: compare the rows that keep a key
+        kept[:, -1] = False
+    o_rows = np.moveaxis(kept, 3, 2)[..., None]  # [B,N,L,H,1]
+    assert fwd_rel_err(np64(got[0]) * o_rows, o_ref * o_rows) <= FWD_TOL[inp["q"].dtype]
+    if dt == "fp16":
+        g = O.backward(a["q"], a["k"], a["v"], a["bias1"], a["bias2"], a["do"])
+        tol = GRAD_TOL[inp["q"].dtype]
+        for name, t in zip(("dq", "dk", "dv"), got[2:5]):
+            assert rel_l2(np64(t), g[name]) <= tol, name
+
+
+def test_skipping_with_strided_gradients():
+    """dK and dV of skipped tiles are written as zeros through the gradients' strides."""
+    B, N, L, H, D = 1, 4, 640, 2, 64
+    inp = masked_rows(make_inputs(B, N, L, H, D, dtype="bf16", mask=None, bias2_sigma=None, seed=2),
+                      ("tail", 300))
+    d = to_dev(inp)
+    E.evo_attn_set_masked_tile_skip(False)
+    ref = run_all(d)
+    E.evo_attn_set_masked_tile_skip(True, -1.0e4)
+    bufs = [torch.full((B, L, N, H, D), 7.0, dtype=torch.bfloat16, device="cuda") for _ in range(3)]
+    views = [b.transpose(1, 2) for b in bufs]
+    for v in views[1:]:
+        v.fill_(3.0)  # the skipped tiles' rows must be overwritten with zeros
+    got = run_all(d, *views)
+    assert torch.equal(got[3], ref[3]) and torch.equal(got[4], ref[4])
+    assert torch.all(got[3][:, :, 384:] == 0) and torch.all(got[4][:, :, 384:] == 0)
+    assert rel_l2(np64(got[2]), np64(ref[2])) <= 1e-2
+
+
+def test_threshold_decides_what_is_masked():
+    """With a threshold below the mask value nothing counts as masked: same results."""
+    inp = masked_rows(make_inputs(1, 3, 600, 1, 64, dtype="bf16", mask=None, bias2_sigma=None, seed=4),
+                      ("tail", 256))
+    d = to_dev(inp)
+    E.evo_attn_set_masked_tile_skip(False)
+    ref = run_all(d)
+    E.evo_attn_set_masked_tile_skip(True, -3.0e38)
+    got = run_all(d)
+    assert torch.equal(got[0], ref[0]) and torch.equal(got[3], ref[3])
