@@ -158,13 +158,14 @@ def summarize_clocks(rows, t0, t1):
             "reasons": sorted(reasons), "samples": len(inside), "window": window}
 
 
-def traffic_for(kernel):
-    """ncu DRAM bytes per launch for `kernel`, if measured on the current source."""
+def traffic_for(case, kernel):
+    """ncu DRAM bytes per launch of the kernel in slot `kernel` on workload `case`
+    ("<workload> <dtype>"), if measured on the current source."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
-        d = json.load(f).get(kernel)
+        d = json.load(f).get(case, {}).get(kernel)
     if not d:
         return None
     src = os.path.join(ROOT, d["source"])
@@ -427,7 +428,7 @@ def run_ours(args):
         peak = peaks["hbm_gbs"]
         unit = "GB/s"
     roofline = {"kernel": dom, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
-                "frac": achieved / peak, "traffic": traffic_for(dom),
+                "frac": achieved / peak, "traffic": traffic_for(f"{w.name} {args.dtype}", dom),
                 "peak_source": f"{peak_src} ({'bf16_tflops_sustained' if bound == 'tensor' else 'hbm_gbs'})"}
 
     # end to end through the host-buffer C-ABI step, pinned host memory
