@@ -329,3 +329,32 @@ def test_sampled_helpers_match_full_oracle():
     rows = [0, 4, 10]
     ds = O.dbias2_sample(q, k, v, b1, b2, do, 1, 1, rows)
     np.testing.assert_allclose(ds, g["dbias2"][1, 0, 1, rows], atol=1e-13)
+
+
+# ---------------------------------------------------------------- masked key tail
+def test_masked_key_tail_contributes_nothing():
+    """Keys with a -1e9 key mask drop out exactly: the result on L keys equals the
+    result on the kept prefix alone, and those keys get zero dK, dV (and zero
+    pair-bias gradient in their columns).  This is what makes skipping a key tile
+    whose keys are all masked exact."""
+    rng = np.random.default_rng(77)
+    B, N, L, H, D, j0 = 1, 2, 12, 2, 8, 7
+    q, k, v, do, _, b2 = rand_problem(B, N, L, H, D, rng, bias1=False)
+    b1 = rng.standard_normal((B, N, 1, 1, L))
+    b1[..., j0:] = -1e9
+    o, lse = O.forward(q, k, v, b1, b2)
+    g = O.backward(q, k, v, b1, b2, do)
+    # the same attention over the kept keys only (L queries, j0 keys), written out here
+    # since the oracle takes square problems
+    s = 1.0 / math.sqrt(D)
+    for b in range(B):
+        for n in range(N):
+            for h in range(H):
+                sc = s * q[b, n, :, h] @ k[b, n, :j0, h].T + b1[b, n, 0, 0, :j0] + b2[b, 0, h, :, :j0]
+                m = sc.max(axis=1, keepdims=True)
+                p = np.exp(sc - m)
+                ref = (p / p.sum(axis=1, keepdims=True)) @ v[b, n, :j0, h]
+                assert np.allclose(o[b, n, :, h], ref, rtol=0, atol=1e-12)
+                assert np.allclose(lse[b, n, h], (m[:, 0] + np.log(p.sum(axis=1))), rtol=0, atol=1e-12)
+    assert np.all(g["dk"][:, :, j0:] == 0) and np.all(g["dv"][:, :, j0:] == 0)
+    assert np.all(g["dbias2"][..., j0:] == 0) and np.all(g["dbias1"][..., j0:] == 0)

@@ -141,3 +141,22 @@ def test_threshold_decides_what_is_masked():
     E.evo_attn_set_masked_tile_skip(True, -3.0e38)
     got = run_all(d)
     assert torch.equal(got[0], ref[0]) and torch.equal(got[3], ref[3])
+
+
+def test_full_size_column_workload():
+    """MSA column-wise attention at full size (keys >= 870 masked: the last key tile of
+    every row is skipped), in the configuration the bench times with skipping on:
+    the same bytes as the unskipped run, whose parity with the oracle is tested on
+    sampled slices elsewhere."""
+    from memory_efficient_biased_gb300.workload import workload_inputs
+    d = to_dev(workload_inputs("msa_col", "bf16"))
+    E.evo_attn_set_masked_tile_skip(False)
+    ref = run_all(d)
+    E.evo_attn_set_masked_tile_skip(True, -1.0e4)
+    got = run_all(d)
+    for name, x, y in zip(("out", "lse", "dq", "dk", "dv", "dbias1"), got, ref):
+        if name == "dq":
+            assert rel_l2(np64(x), np64(y)) <= 1e-2
+        else:
+            assert torch.equal(x, y), name
+    assert torch.all(got[3][:, :, 896:] == 0) and torch.all(got[4][:, :, 896:] == 0)
