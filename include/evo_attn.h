@@ -284,9 +284,14 @@ EVO_API evo_status_t evo_attn_selftest_wait_timeout(uint64_t limit_ns, void* str
  *   evo_attn_bwd : events[2] before its first kernel, then one event after
  *                  each kernel in launch order — events[3] after delta /
  *                  accumulator set-up, events[4] after the main backward
- *                  kernel, events[5] after the dQ cast, and with a pair bias
- *                  events[6] after the per-group pair-bias partials and
- *                  events[7] after their fixed-order sum.
+ *                  kernel (with masked key-tile skipping on the per-key-tile
+ *                  schedule, its two work-list kernels run between events[3]
+ *                  and events[4]), events[5] after the dQ cast, and with a
+ *                  pair bias events[6] after the per-group pair-bias partials
+ *                  and events[7] after their fixed-order sum.  With dbias1,
+ *                  its partial and sum kernels run between events[5] and
+ *                  events[6].  A call split batch by batch (strided layouts)
+ *                  records them for its last batch.
  * Indices >= count are skipped.  evo_attn_profile_events(NULL, 0) turns it off.
  * Recording works inside stream capture (the records become graph nodes).
  */
