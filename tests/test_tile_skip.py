@@ -160,3 +160,44 @@ def test_full_size_column_workload():
         else:
             assert torch.equal(x, y), name
     assert torch.all(got[3][:, :, 896:] == 0) and torch.all(got[4][:, :, 896:] == 0)
+
+
+def test_skipping_with_batch_by_batch_strided_call():
+    """B = 2 with transposed inputs and outputs runs batch by batch; each batch builds
+    its own work list in the shared workspace."""
+    B, N, L, H, D = 2, 3, 520, 2, 64
+    inp = masked_rows(make_inputs(B, N, L, H, D, dtype="bf16", mask=None, bias2_sigma=1.0, seed=9), ("tiles", 0.5))
+    d = to_dev(inp)
+    E.evo_attn_set_masked_tile_skip(False)
+    ref = run_all(d)
+    E.evo_attn_set_masked_tile_skip(True, -1.0e4)
+
+    def tr(t):
+        buf = torch.empty((B, L, N, H, D), dtype=t.dtype, device=t.device)
+        v = buf.transpose(1, 2)
+        v.copy_(t)
+        return v
+
+    q, k, v, do = (tr(d[n]) for n in ("q", "k", "v", "do"))
+    out, lse = E.evo_attn_fwd_strided(q, k, v, d["bias1"], d["bias2"], out=tr(torch.zeros_like(d["q"])))
+    g = E.evo_attn_bwd_strided(q, k, v, d["bias1"], d["bias2"], out, lse, do, dq=tr(d["q"]), dk=tr(d["q"]),
+                               dv=tr(d["q"]), want_dbias1=True)
+    torch.cuda.synchronize()
+    assert E.evo_attn_device_status() == 0
+    assert torch.equal(out, ref[0]) and torch.equal(lse, ref[1])
+    assert torch.equal(g[1], ref[3]) and torch.equal(g[2], ref[4]) and torch.equal(g[3], ref[5])
+    assert torch.equal(g[4], ref[6])
+    assert rel_l2(np64(g[0]), np64(ref[2])) <= 1e-2
+
+
+def test_more_than_64_key_tiles_skip_nothing():
+    """Past 64 key tiles the skip bit sets do not reach: skipping switches itself off."""
+    inp = masked_rows(make_inputs(1, 1, 65 * 128, 1, 16, dtype="fp16", mask=None, bias2_sigma=None, seed=3),
+                      ("tail", 64 * 128))
+    d = to_dev(inp)
+    E.evo_attn_set_masked_tile_skip(False)
+    ref = run_all(d)
+    E.evo_attn_set_masked_tile_skip(True, -1.0e4)
+    got = run_all(d)
+    assert torch.equal(got[0], ref[0]) and torch.equal(got[1], ref[1])
+    assert torch.equal(got[3], ref[3]) and torch.equal(got[4], ref[4])
