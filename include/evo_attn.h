@@ -113,6 +113,11 @@ typedef struct {
  * order of stride, each stride is at least the extent in elements of the
  * dimensions inside it, the innermost at least H*D); the whole span is below
  * 2^44 elements.  Strides of dimensions of extent 1 are ignored.
+ *
+ * The aliasing rule (EVO_ERR_ALIASING) compares each tensor's span, from its
+ * first element to its last: tensors interleaved in one buffer (for instance
+ * q and out as two slots of one [.., 4, H, D] buffer) count as overlapping
+ * even where their elements are disjoint.
  */
 typedef struct {
   int64_t b, n, l;

@@ -445,7 +445,7 @@ evo_status_t evo_attn_fwd_strided(const void* q, const void* k, const void* v, c
     }
     a.bias1 = bias1 ? static_cast<const uint16_t*>(bias1) + b * shape.N * shape.L : nullptr;
     a.bias2 = b2;
-    a.out = static_cast<uint16_t*>(const_cast<void*>(static_cast<const void*>(at(out, t[3]))));
+    a.out = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(out) + size_t(b * t[3].b) * 2);
     a.lse = lse + b * shape.N * shape.H * shape.L;
     a.B = static_cast<int>(sub.B);
     a.N = static_cast<int>(shape.N);

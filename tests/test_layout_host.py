@@ -65,3 +65,14 @@ def test_extent_one_dimensions_ignore_their_strides():
     # a size-1 dimension may carry any stride
     y = torch.as_strided(x, x.shape, (3, 5, 64, 16, 1))
     assert readable_in_place(y)
+
+
+def test_slots_of_a_packed_projection_are_read_in_place():
+    """q, k, v as the three slots of one [B, N, L, 3, H, D] projection output: token
+    stride 3·H·D, (H, D) packed."""
+    qkv = torch.zeros((1, 6, 40, 3, 4, 16), dtype=torch.bfloat16)
+    q, k, v = qkv.unbind(3)
+    for t in (q, k, v):
+        assert not t.is_contiguous() and readable_in_place(t)
+    lay = E.layout_of(q=q, k=k, v=v)
+    assert (lay.k.n, lay.k.l) == (40 * 3 * 64, 3 * 64)

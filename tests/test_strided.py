@@ -150,3 +150,21 @@ def test_autograd_reads_transposed_views_in_place(dt):
     for n in ("q", "k", "v"):
         g_view = bufs[n].grad.transpose(1, 2)
         assert rel_l2(np64(g_view), np64(packed[n].grad)) <= 1e-2, n
+
+
+def test_slots_of_one_projection_buffer():
+    """q, k, v read in place as the slots of one [B, N, L, 3, H, D] buffer (inputs may share
+    a buffer; only outputs are checked against inputs)."""
+    B, N, L, H, D = 1, 3, 200, 2, 32
+    inp = make_inputs(B, N, L, H, D, dtype="bf16", mask=("random", 0.05), bias2_sigma=1.0, seed=12)
+    d = to_dev(inp)
+    out_p, lse_p = E.evo_attn_fwd(d["q"], d["k"], d["v"], d["bias1"], d["bias2"])
+    ref = E.evo_attn_bwd_ex(d["q"], d["k"], d["v"], d["bias1"], d["bias2"], out_p, lse_p, d["do"])
+    qkv = torch.stack([d["q"], d["k"], d["v"]], dim=3)  # [B, N, L, 3, H, D]
+    q, k, v = qkv.unbind(3)
+    out, lse = E.evo_attn_fwd_strided(q, k, v, d["bias1"], d["bias2"])
+    g = E.evo_attn_bwd_strided(q, k, v, d["bias1"], d["bias2"], out, lse, d["do"], want_dbias1=True)
+    assert E.evo_attn_device_status() == 0
+    assert torch.equal(out, out_p) and torch.equal(lse, lse_p)
+    for x, y in zip(g, ref):
+        assert torch.equal(x, y)
