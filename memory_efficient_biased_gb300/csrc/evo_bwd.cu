@@ -264,6 +264,48 @@ __global__ void __launch_bounds__(1024) evo_bwd_worklist(const BwdArgs a) {
   }
 }
 
+// evo_bwd_worklist_jt (one block): the same list for the key-tile-fastest item order
+// (b, h, n, key tile): the kept key tiles of each row (b, n) in order, the row's count
+// and offset within its b shared by every head.
+__global__ void __launch_bounds__(1024) evo_bwd_worklist_jt(const BwdArgs a) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, KT = a.QT;
+  const long long rows = static_cast<long long>(a.B) * a.N;
+  const unsigned long long all = KT >= 64 ? ~0ull : ((1ull << KT) - 1);
+  uint32_t* pre = a.wl_n;          // [B*N] kept tiles of each row, then their offsets within b
+  uint32_t* per_head = a.wl_cnt;   // [B] items of one head of b
+  uint32_t* start = a.wl_cnt + a.B;  // [B] where b's items start
+  for (long long bn = threadIdx.x; bn < rows; bn += 1024) pre[bn] = __popcll(~a.tskip[bn] & all);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t at = 0;
+    for (int b = 0; b < a.B; ++b) {
+      uint32_t sum = 0;
+      for (int n = 0; n < a.N; ++n) {
+        const uint32_t c = pre[static_cast<long long>(b) * a.N + n];
+        pre[static_cast<long long>(b) * a.N + n] = sum;
+        sum += c;
+      }
+      per_head[b] = sum;
+      start[b] = at;
+      at += sum * a.H;
+    }
+    *a.wl_total = at;
+  }
+  __syncthreads();
+  const long long groups = static_cast<long long>(a.B) * a.H * a.N;  // (b, h, n), in item order
+  for (long long grp = warp; grp < groups; grp += 32) {
+    const int n = static_cast<int>(grp % a.N);
+    const long long bh = grp / a.N;
+    const int h = static_cast<int>(bh % a.H), b = static_cast<int>(bh / a.H);
+    const long long bn = static_cast<long long>(b) * a.N + n;
+    const unsigned long long kept = ~a.tskip[bn] & all;
+    const uint32_t at = start[b] + h * per_head[b] + pre[bn];
+    for (int jt = lane; jt < KT; jt += 32)
+      if ((kept >> jt) & 1ull)
+        a.wl[at + __popcll(kept & ((1ull << jt) - 1ull))] = static_cast<uint32_t>(grp * KT + jt);
+  }
+}
+
 // ============================================================ evo_bwd_db2_sum
 template <bool BF16>
 __global__ void __launch_bounds__(256) evo_bwd_db2_sum(const BwdArgs a) {
@@ -1837,21 +1879,14 @@ cudaError_t launch_bwd_d(BwdArgs a, cudaStream_t st, const ProfileEvents* prof) 
     prof_record(prof, 5, st);  // no dQ cast in slice mode
   } else {
 
-  if (a.tile_skip) {  // masked key tiles: skip bits and zero dK/dV rows, then the work list
-    evo_bwd_tile_mask<BF16><<<grid_for(static_cast<long long>(a.B) * a.N * 32, 256), 256, 0, st>>>(a);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    evo_bwd_worklist<<<1, 1024, 0, st>>>(a);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  } else {
-    a.wl = nullptr;
-  }
-  // main kernel: deepest Q/dO ring that fits, resident pair-bias tiles when possible
+  // main kernel: deepest Q/dO ring that fits, resident pair-bias tiles when possible; without
+  // resident tiles an (n, h)'s key tiles run back to back (its Q, dO and dQ rows stay in L2)
   auto fits = [&](int kind, int qs) { return MainLayout<DP>(kind, qs, a.QT).total + 1024 <= kMaxSmem; };
+  int kind = kB2None, qs = 1;
   if (!has_b2) {
-    a.q_stages = fits(kB2None, 4) ? 4 : (fits(kB2None, 3) ? 3 : (fits(kB2None, 2) ? 2 : 1));
-    e = launch_main<DP, BF16, kB2None>(a, st);
+    qs = fits(kB2None, 4) ? 4 : (fits(kB2None, 3) ? 3 : (fits(kB2None, 2) ? 2 : 1));
   } else {
-    int kind = kB2Stream, qs = 1;
+    kind = kB2Stream;
     for (int q = 4; q >= 2; --q)
       if (fits(kB2Resident, q)) {
         kind = kB2Resident;
@@ -1859,10 +1894,24 @@ cudaError_t launch_bwd_d(BwdArgs a, cudaStream_t st, const ProfileEvents* prof) 
         break;
       }
     if (kind == kB2Stream) qs = fits(kB2Stream, 3) ? 3 : (fits(kB2Stream, 2) ? 2 : 1);
-    a.q_stages = qs;
-    a.b2_resident = kind == kB2Resident;
-    e = kind == kB2Resident ? launch_main<DP, BF16, kB2Resident>(a, st) : launch_main<DP, BF16, kB2Stream>(a, st);
   }
+  a.q_stages = qs;
+  a.b2_resident = kind == kB2Resident;
+  a.jt_fast = kind != kB2Resident;
+  if (a.tile_skip) {  // masked key tiles: skip bits and zero dK/dV rows, then the work list
+    evo_bwd_tile_mask<BF16><<<grid_for(static_cast<long long>(a.B) * a.N * 32, 256), 256, 0, st>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (a.jt_fast)
+      evo_bwd_worklist_jt<<<1, 1024, 0, st>>>(a);
+    else
+      evo_bwd_worklist<<<1, 1024, 0, st>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  } else {
+    a.wl = nullptr;
+  }
+  e = kind == kB2None       ? launch_main<DP, BF16, kB2None>(a, st)
+      : kind == kB2Resident ? launch_main<DP, BF16, kB2Resident>(a, st)
+                            : launch_main<DP, BF16, kB2Stream>(a, st);
   if (e != cudaSuccess) return e;
   prof_record(prof, 4, st);
   evo_bwd_dq_cast<BF16><<<grid_for(rows * a.D / 8, 256), 256, 0, st>>>(a);

@@ -112,23 +112,34 @@ __device__ __forceinline__ void fill_lse_delta(float* dst, const float* lse, con
   ld_store(dst, raw, lane);
 }
 
-// Incremental (b, h, key tile, n) iterator, n fastest.
+// Incremental iterator over the per-key-tile kernel's items: (b, h, key tile, n), n fastest,
+// or with jt_fast (b, h, n, key tile), key tile fastest.
 struct KvIter {
   int b, h, jt, n;
   __device__ __forceinline__ void init(long long item, const BwdArgs& a) {
     long long t = item;
-    n = static_cast<int>(t % a.N);
-    t /= a.N;
-    jt = static_cast<int>(t % a.QT);
-    t /= a.QT;
+    if (a.jt_fast) {
+      jt = static_cast<int>(t % a.QT);
+      t /= a.QT;
+      n = static_cast<int>(t % a.N);
+      t /= a.N;
+    } else {
+      n = static_cast<int>(t % a.N);
+      t /= a.N;
+      jt = static_cast<int>(t % a.QT);
+      t /= a.QT;
+    }
     h = static_cast<int>(t % a.H);
     b = static_cast<int>(t / a.H);
   }
   __device__ __forceinline__ void next(const BwdArgs& a) {
-    if (++n == a.N) {
-      n = 0;
-      if (++jt == a.QT) {
-        jt = 0;
+    int& fast = a.jt_fast ? jt : n;
+    int& slow = a.jt_fast ? n : jt;
+    const int nfast = a.jt_fast ? a.QT : a.N, nslow = a.jt_fast ? a.N : a.QT;
+    if (++fast == nfast) {
+      fast = 0;
+      if (++slow == nslow) {
+        slow = 0;
         if (++h == a.H) {
           h = 0;
           ++b;

@@ -115,24 +115,37 @@ struct FwdLayout {
   }
 };
 
-// Work items are ordered (b, h, q-tile, n), n fastest; a CTA walks a
-// contiguous range with an incremental iterator (no integer division per item).
+// Work items are ordered (b, h, q-tile, n), n fastest, so that the pair-bias tiles of a
+// (b, h, q-tile) stay resident across n; without a resident pair bias (qt_fast) they are
+// ordered (b, h, n, q-tile), so that the query tiles sharing one (n, h)'s K and V run back
+// to back on one CTA and re-read them from L2 instead of DRAM.  A CTA walks a contiguous
+// range with an incremental iterator (no integer division per item).
 struct ItemIter {
   int b, h, qt, n;
   __device__ __forceinline__ void init(long long item, const FwdArgs& a) {
     long long t = item;
-    n = static_cast<int>(t % a.N);
-    t /= a.N;
-    qt = static_cast<int>(t % a.QT);
-    t /= a.QT;
+    if (a.qt_fast) {
+      qt = static_cast<int>(t % a.QT);
+      t /= a.QT;
+      n = static_cast<int>(t % a.N);
+      t /= a.N;
+    } else {
+      n = static_cast<int>(t % a.N);
+      t /= a.N;
+      qt = static_cast<int>(t % a.QT);
+      t /= a.QT;
+    }
     h = static_cast<int>(t % a.H);
     b = static_cast<int>(t / a.H);
   }
   __device__ __forceinline__ void next(const FwdArgs& a) {
-    if (++n == a.N) {
-      n = 0;
-      if (++qt == a.QT) {
-        qt = 0;
+    int& fast = a.qt_fast ? qt : n;
+    int& slow = a.qt_fast ? n : qt;
+    const int nfast = a.qt_fast ? a.QT : a.N, nslow = a.qt_fast ? a.N : a.QT;
+    if (++fast == nfast) {
+      fast = 0;
+      if (++slow == nslow) {
+        slow = 0;
         if (++h == a.H) {
           h = 0;
           ++b;
@@ -731,6 +744,7 @@ cudaError_t launch_fwd_d(FwdArgs a, cudaStream_t st) {
   auto fits = [&](int kind, int stages) { return FwdLayout<DP>(kind, stages, a.QT).total + 1024 <= kMaxSmem; };
   if (a.bias2_mode == kBias2None) {
     a.stages = fits(kB2None, 4) ? 4 : 2;
+    a.qt_fast = 1;
     return launch_fwd_t<DP, BF16, kB2None>(a, st);
   }
   for (int stages = 4; stages >= 2; --stages) {
@@ -742,6 +756,7 @@ cudaError_t launch_fwd_d(FwdArgs a, cudaStream_t st) {
   }
   a.stages = 2;
   a.b2_resident = 0;
+  a.qt_fast = 1;
   return launch_fwd_t<DP, BF16, kB2Stream>(a, st);
 }
 

@@ -81,8 +81,13 @@ PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
   return fn;
 }
 
+// l2: how far the L2 widens a request beyond the box's bytes.  Tiles of whole contiguous
+// rows (pair bias, partial planes) take 256 bytes; one head's rows of a [B,N,L,H,D] tensor
+// take none, since the neighbouring heads' bytes a wider fetch brings in are read by other
+// work items much later (after eviction when the tensors outgrow L2).
 bool encode_t(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int rank, const cuuint64_t* dims,
-              const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle swz) {
+              const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle swz,
+              CUtensorMapL2promotion l2 = CU_TENSOR_MAP_L2_PROMOTION_L2_256B) {
   auto fn = tmap_encoder();
   if (!fn) {
     set_detail("cuTensorMapEncodeTiled entry point", 0, "not found");
@@ -91,15 +96,16 @@ bool encode_t(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int rank
   cuuint32_t es[5] = {1, 1, 1, 1, 1};
   CUresult r = fn(m, dt,
                   static_cast<cuuint32_t>(rank), const_cast<void*>(base), dims, strides, box, es,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swz, l2,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) set_detail("cuTensorMapEncodeTiled", static_cast<int>(r), "CUresult");
   return r == CUDA_SUCCESS;
 }
 bool encode(CUtensorMap* m, const void* base, bool bf16, int rank, const cuuint64_t* dims,
-            const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle swz) {
+            const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle swz,
+            CUtensorMapL2promotion l2 = CU_TENSOR_MAP_L2_PROMOTION_L2_256B) {
   return encode_t(m, base, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, rank, dims,
-                  strides, box, swz);
+                  strides, box, swz, l2);
 }
 
 // fp32 pair-bias partial planes [G*B*H][L][L] as 3-D (j, i, plane); box (32, 32, 1), 128B swizzle.
@@ -127,7 +133,7 @@ bool map_qkv(CUtensorMap* m, const void* p, const evo_shape_t& s, bool bf16, con
   const CUtensorMapSwizzle swz = DP == 64   ? CU_TENSOR_MAP_SWIZZLE_128B
                                  : DP == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
                                             : CU_TENSOR_MAP_SWIZZLE_32B;
-  return encode(m, p, bf16, 4, dims, strides, box, swz);
+  return encode(m, p, bf16, 4, dims, strides, box, swz, CU_TENSOR_MAP_L2_PROMOTION_NONE);
 }
 
 // The same 4-D view with a box of one warp's share of an output tile: (DP/2, 1, 32, 1);
@@ -142,7 +148,8 @@ bool map_rows_half(CUtensorMap* m, const void* p, const evo_shape_t& s, bool bf1
   return encode(m, p, bf16, 4, dims, strides, box,
                 DP == 64   ? CU_TENSOR_MAP_SWIZZLE_64B
                 : DP == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
-                           : CU_TENSOR_MAP_SWIZZLE_NONE);
+                           : CU_TENSOR_MAP_SWIZZLE_NONE,
+                CU_TENSOR_MAP_L2_PROMOTION_NONE);
 }
 
 // [B,1,H,L,L] viewed as 3-D (key j, query i, B*H).

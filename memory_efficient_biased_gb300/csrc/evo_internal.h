@@ -30,7 +30,8 @@ struct FwdArgs {
   float* lse;               // [B,N,H,L]
   int B, N, L, H, D;
   int QT;                   // ceil(L / 128)
-  long long items;          // B*H*QT*N work items, ordered (b, h, query tile, n)
+  long long items;          // B*H*QT*N work items, ordered (b, h, query tile, n), or with qt_fast (b, h, n, query tile)
+  int qt_fast;              // no resident pair bias: an (n, h)'s query tiles run back to back (K/V reuse in L2)
   long long chunk;          // consecutive items per CTA
   int stages;               // depth of the K/V ring (2..4)
   int b2_resident;          // pair-bias tiles of the current (b, h, q-tile) kept in smem
@@ -72,7 +73,10 @@ struct BwdArgs {
   int QT;
   int groups;               // G: n-groups of the pair-bias gradient
   int group_size;           // ceil(N / G)
-  long long items;          // main kernel: B*H*QT*N items (b, h, key tile, n), n fastest
+  long long items;          // main kernel: B*H*QT*N items (b, h, key tile, n), n fastest, or with
+                            // jt_fast (b, h, n, key tile)
+  int jt_fast;              // main kernel without resident pair-bias tiles: an (n, h)'s key tiles
+                            // run back to back, so its Q, dO and dQ accumulator stay in L2
   long long chunk;          // main kernel: consecutive items per CTA
   int q_stages;             // main kernel: depth of the Q/dO ring
   int b2_resident;          // main kernel: pair-bias tiles of the (b, h, key tile) group stay in smem
