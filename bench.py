@@ -2,13 +2,14 @@
 """Benchmark of memory-efficient biased Evoformer attention on GB300.
 
 One step = forward + backward of O = softmax(Q Kᵀ D^-1/2 + bias1 + bias2) V
-over one batch of the named workload (default: MSA row-wise attention with
-pair bias, B=1, N=256, L=256, H=4, D=32, bf16), i.e. every kernel of the hot
-path: forward, delta/accumulator set-up, main backward, dQ cast, and the two
-deterministic pair-bias gradient stages.
+over one batch of the named workload (default: MSA column-wise attention,
+B=1, N=384, L=1024, H=8, D=32, bf16, key mask only — the largest of the five
+configurations), i.e. every kernel of the hot path the workload needs:
+forward, delta/accumulator set-up, main backward, dQ cast, and with a pair
+bias the deterministic pair-bias gradient stages.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--dtype bf16|fp16]
+                    [--workload NAME] [--dtype bf16|fp16] [--micro]
 
 Prints one JSON line (rank 0).  `value` is whole-job fwd+bwd TFLOP/s with
 nominal FLOPs (forward 4·B·N·H·L²·D, backward 2.5× forward) and inputs
@@ -47,10 +48,14 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 def parse_args():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", default="msa_row")
+    ap.add_argument("--workload", default="msa_col",
+                    help="msa_col (default: the largest configuration, B=1 N=384 L=1024 H=8 D=32), msa_row, "
+                         "many_head, triangle or tiny")
+    ap.add_argument("--micro", action="store_true",
+                    help="run the throughput microbenchmarks (exponentials, FMA, tcgen05.mma issue) instead")
     ap.add_argument("--dtype", default="bf16", choices=("bf16", "fp16"))
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -101,61 +106,133 @@ def oracle_row_seconds(inp):
     return max(time.perf_counter() - t0, 1e-6)
 
 
+class _Nvml:
+    """Read-only NVML queries through ctypes (SM clock, max SM clock, power, active
+    clock-event reasons); None when libnvidia-ml is not loadable."""
+    HW_SLOWDOWN, SW_POWER_CAP, SW_THERMAL, HW_THERMAL, HW_POWER_BRAKE = 0x8, 0x4, 0x20, 0x40, 0x80
+
+    def __init__(self, cuda_index):
+        import ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        self.ct = ctypes
+        self.h = ctypes.c_void_p()
+        bus = None
+        try:
+            import torch
+            p = torch.cuda.get_device_properties(cuda_index)
+            bus = f"{p.pci_domain_id:08X}:{p.pci_bus_id:02X}:{p.pci_device_id:02X}.0".encode()
+        except Exception:
+            bus = None
+        ok = bus is not None and self.lib.nvmlDeviceGetHandleByPciBusId_v2(bus, ctypes.byref(self.h)) == 0
+        if not ok and self.lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(cuda_index), ctypes.byref(self.h)) != 0:
+            raise RuntimeError("no NVML handle")
+
+    def sample(self):
+        ct = self.ct
+        sm, mx, pw, rs = ct.c_uint(), ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        self.lib.nvmlDeviceGetClockInfo(self.h, 1, ct.byref(sm))          # NVML_CLOCK_SM
+        self.lib.nvmlDeviceGetMaxClockInfo(self.h, 1, ct.byref(mx))
+        have_pw = self.lib.nvmlDeviceGetPowerUsage(self.h, ct.byref(pw)) == 0
+        self.lib.nvmlDeviceGetCurrentClocksEventReasons(self.h, ct.byref(rs))
+        r = rs.value
+        act = lambda bit: "Active" if r & bit else "Not Active"
+        return {"t": time.time(), "sm": float(sm.value), "max": float(mx.value),
+                "power": pw.value / 1000.0 if have_pw else None,
+                "hw": act(self.HW_SLOWDOWN | self.HW_POWER_BRAKE), "hw_thermal": act(self.HW_THERMAL),
+                "sw_thermal": act(self.SW_THERMAL), "sw_power": act(self.SW_POWER_CAP)}
+
+
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 100 ms in the background."""
+    """SM clock and clock-event reasons sampled in the background every 10 ms
+    (NVML through ctypes; nvidia-smi every 20 ms as the fallback), from before the
+    warm-up to after the measurements, so that even a short timed region is spanned
+    by samples."""
     FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_index):
-        self.proc = None
-        self.gpu = gpu_index
+        import threading
+        self.rows, self.proc, self.nvml = [], None, None
+        self.stop_flag = threading.Event()
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.nvml = _Nvml(gpu_index)
+            self.source = "nvml, 10 ms"
+            self.thread = threading.Thread(target=self._poll, daemon=True)
         except Exception:
-            self.proc = None
+            self.nvml = None
+            self.source = "nvidia-smi, 20 ms"
+            try:
+                self.proc = subprocess.Popen(
+                    ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                     "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True, bufsize=1)
+            except Exception:
+                self.proc = None
+            self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
 
-    def stop(self):
+    def _poll(self):
+        while not self.stop_flag.is_set():
+            try:
+                self.rows.append(self.nvml.sample())
+            except Exception:
+                pass
+            self.stop_flag.wait(0.01)
+
+    def _read(self):
         if self.proc is None:
-            return []
-        self.proc.terminate()
-        try:
-            out, _ = self.proc.communicate(timeout=5)
-        except Exception:
-            self.proc.kill()
-            out, _ = self.proc.communicate()
-        rows = []
-        for line in out.strip().splitlines():
+            return
+        for line in self.proc.stdout:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 10:
                 continue
             try:
-                ts = datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
-                rows.append({"t": ts, "sm": float(parts[2]), "max": float(parts[3]),
-                             "power": float(parts[4]) if parts[4] not in ("[N/A]", "N/A") else None,
-                             "hw": parts[6], "hw_thermal": parts[7], "sw_thermal": parts[8], "sw_power": parts[9]})
+                self.rows.append({"t": time.time(), "sm": float(parts[2]), "max": float(parts[3]),
+                                  "power": float(parts[4]) if parts[4] not in ("[N/A]", "N/A") else None,
+                                  "hw": parts[6], "hw_thermal": parts[7], "sw_thermal": parts[8],
+                                  "sw_power": parts[9]})
             except ValueError:
                 continue
-        return rows
+
+    def wait_first(self, timeout=10.0):
+        t0 = time.time()
+        while not self.rows and time.time() - t0 < timeout:
+            time.sleep(0.01)
+
+    def stop(self):
+        self.stop_flag.set()
+        if self.proc is not None:
+            import signal
+            self.proc.send_signal(signal.SIGINT)
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        self.thread.join(timeout=5)
+        return list(self.rows)
 
 
-def summarize_clocks(rows, t0, t1):
+def summarize_clocks(rows, t0, t1, source=""):
+    """Samples inside [t0, t1], plus the last one before and the first one after it,
+    so that a timed region shorter than the sampling interval is still spanned."""
     inside = [r for r in rows if t0 <= r["t"] <= t1]
-    window = "timed"
-    if not inside:
-        inside, window = rows, "whole run (timed region shorter than the 100 ms sampling interval)"
-    if not inside:
-        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"], "samples": 0}
+    before = [r for r in rows if r["t"] < t0]
+    after = [r for r in rows if r["t"] > t1]
+    span = ([before[-1]] if before else []) + inside + ([after[0]] if after else [])
+    if not span:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no clock samples"], "samples": 0,
+                "source": source}
     reasons = set()
-    for r in inside:
+    for r in span:
         for key, name in (("hw", "hw_slowdown"), ("hw_thermal", "hw_thermal_slowdown"),
                           ("sw_thermal", "sw_thermal_slowdown"), ("sw_power", "sw_power_cap")):
             if r[key].lower() == "active":
                 reasons.add(name)
-    return {"sm_mhz": statistics.median(r["sm"] for r in inside), "sm_max_mhz": max(r["max"] for r in inside),
-            "reasons": sorted(reasons), "samples": len(inside), "window": window}
+    return {"sm_mhz": statistics.median(r["sm"] for r in span), "sm_max_mhz": max(r["max"] for r in span),
+            "reasons": sorted(reasons), "samples": len(span), "samples_inside": len(inside),
+            "window": "timed region, with the nearest sample on each side", "source": source}
 
 
 def traffic_for(case, kernel):
@@ -304,6 +381,8 @@ def run_ours(args):
 
     w = WORKLOADS[args.workload]
     dt = {"bf16": torch.bfloat16, "fp16": torch.float16}[args.dtype]
+    # clocks are sampled from here to the end of the measurements
+    sampler = ClockSampler(local) if rank == 0 else None
     E.evo_attn_set_masked_tile_skip(args.skip_masked_tiles, -1.0e4)
     inp = workload_inputs(args.workload, args.dtype, seed=rank)
     has_b1, has_b2 = inp["bias1"] is not None, inp["bias2"] is not None
@@ -372,7 +451,8 @@ def run_ours(args):
         igraphs.append(gi)
     torch.cuda.synchronize()
 
-    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.wait_first()
     for k in range(args.warmup):
         graphs[k % R].replay()
     torch.cuda.synchronize()
@@ -407,13 +487,16 @@ def run_ours(args):
     clock_rows = sampler.stop() if sampler else []
     if E.evo_attn_device_status() != 0:
         raise RuntimeError("device wait timed out during the instrumented replays")
+    # only the slots of kernels that launched: the dQ cast runs on the per-key-tile schedule alone
+    mode = bwd_mode(w)
     names = ["fwd", "bwd_pre", "bwd_main", "bwd_dq_cast"] + (["bwd_db2_part", "bwd_db2_sum"] if has_b2 else [])
     pairs = [(0, 1), (2, 3), (3, 4), (4, 5)] + ([(5, 6), (6, 7)] if has_b2 else [])
     kern_ms = {n: statistics.mean(evs[r][a].elapsed_time(evs[r][b]) for r in range(R))
-               for n, (a, b) in zip(names, pairs)}
+               for n, (a, b) in zip(names, pairs) if n != "bwd_dq_cast" or mode == "main"}
 
     F = flops(w)
     ms_step = ms_total / args.steps
+    bwd_ms = sum(v for k, v in kern_ms.items() if k != "fwd")  # every backward kernel of the step
     value = world * F["step"] / (ms_step * 1e-3) / 1e12
     fwd_tflops = F["fwd"] / (kern_ms["fwd"] * 1e-3) / 1e12
     peaks, peak_src = load_peaks()
@@ -422,7 +505,6 @@ def run_ours(args):
     bnhl = w.B * w.N * w.H * w.L
     b1b = w.B * w.N * w.L * 2 if has_b1 else 0
     b2b = w.B * w.H * w.L * w.L * 2 if has_b2 else 0
-    mode = bwd_mode(w)
     work = {
         "fwd": ("tensor", F["fwd"]),
         "bwd_main": ("tensor", F["bwd"]),
@@ -434,11 +516,14 @@ def run_ours(args):
         "bwd_dq_cast": ("hbm", 2 * qkv + qkv),
         "bwd_db2_sum": ("hbm", bias2_groups(w) * w.B * w.H * w.L * w.L * 4 + b2b if has_b2 else 0),
     }
+    # The kernels are timed in windows far shorter than the seconds-long loop of the
+    # sustained figure, at full SM clock: the burst bf16 peak is the denominator.
+    tpeak = peaks["bf16_tflops"]
     dom = max(kern_ms, key=kern_ms.get)
     bound, amount = work[dom]
     if bound == "tensor":
         achieved = amount / (kern_ms[dom] * 1e-3) / 1e12
-        peak = peaks["bf16_tflops_sustained"]
+        peak = tpeak
         unit = "TFLOP/s"
     else:
         achieved = amount / (kern_ms[dom] * 1e-3) / 1e9
@@ -446,7 +531,7 @@ def run_ours(args):
         unit = "GB/s"
     roofline = {"kernel": dom, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
                 "frac": achieved / peak, "traffic": traffic_for(f"{w.name} {args.dtype}", dom),
-                "peak_source": f"{peak_src} ({'bf16_tflops_sustained' if bound == 'tensor' else 'hbm_gbs'})"}
+                "peak_source": f"{peak_src} ({'bf16_tflops (burst)' if bound == 'tensor' else 'hbm_gbs'})"}
 
     # end to end through the host-buffer C-ABI step, pinned host memory
     pin = lambda t: None if t is None else t.pin_memory()
@@ -512,8 +597,11 @@ def run_ours(args):
                               f"L2-warm: {R} replicas of {per_rep / 1e6:.1f} MB fit in L2 (small case)"),
                        "parallelism": f"{world} independent replicas" if world > 1 else "single GPU"},
             "fwd_tflops": fwd_tflops,
-            "fwd_frac_of_peak": fwd_tflops / peaks["bf16_tflops_sustained"],
-            "fwd_bwd_frac_of_peak": value / world / peaks["bf16_tflops_sustained"],
+            "fwd_frac_of_peak": fwd_tflops / tpeak,
+            "bwd_tflops": F["bwd"] / (bwd_ms * 1e-3) / 1e12,
+            "bwd_frac_of_peak": F["bwd"] / (bwd_ms * 1e-3) / 1e12 / tpeak,
+            "fwd_bwd_frac_of_peak": value / world / tpeak,
+            "peak_used": f"bf16_tflops (burst) = {tpeak} TFLOP/s, {peak_src}",
             "kernel_ms": kern_ms,
             "kernel_ms_source": (f"CUDA events the library records between its kernels, {ksteps} replays of "
                                  f"instrumented copies of the timed graphs right after the timed region "
@@ -525,7 +613,7 @@ def run_ours(args):
             "e2e": {"value": world * F["step"] / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                     "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches_per_step * args.steps,
-            "clocks": summarize_clocks(clock_rows, wall0, wall1),
+            "clocks": summarize_clocks(clock_rows, wall0, wall1, sampler.source if sampler else ""),
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -533,8 +621,81 @@ def run_ours(args):
     return 0
 
 
+# --------------------------------------------------------------------------- microbenchmarks
+# (kind, name, results per chain step): ops counted are exponentials, or fp32 FMA lane-ops
+MICRO_EXP = [(0, "ex2.approx.ftz.f32", 1), (1, "ex2.approx.f16x2", 2), (2, "ex2.approx.ftz.bf16x2", 2),
+             (3, "polynomial 2^x, scalar fma", 1), (4, "polynomial 2^x, fma.f32x2", 1), (5, "fma.rn.f32", 1),
+             (6, "fma.rn.f32x2", 1), (7, "mix: 6 ex2.f32 + 1 packed polynomial pair", 1)]
+
+
+def run_micro(args):
+    """Per-SM-clock throughput of the exponential forms and of tcgen05.mma issue
+    (libevo_micro.so); one JSON line per measurement."""
+    import ctypes
+    import torch
+    from memory_efficient_biased_gb300 import build as _build
+    _build.build()
+    lib = ctypes.CDLL(_build.MICRO_LIB)
+    torch.cuda.set_device(0)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    sink = torch.zeros(512, dtype=torch.float32, device="cuda")
+    sampler = ClockSampler(0)
+    sampler.wait_first()
+    blocks, iters, threads, chains = 4 * sms, 1 << 14, 512, 8
+    cyc = torch.zeros(blocks, dtype=torch.int64, device="cuda")
+    for kind, name, per_instr in MICRO_EXP:
+        best = None
+        for rep in range(4):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            rc = lib.evo_micro_exp(kind, blocks, iters, ctypes.c_void_p(sink.data_ptr()),
+                                   ctypes.c_void_p(cyc.data_ptr()), stream)
+            e1.record()
+            torch.cuda.synchronize()
+            if rc != 0:
+                raise RuntimeError(f"micro_exp kind {kind}: cuda error {rc}")
+            cycles = statistics.median(cyc.cpu().tolist())
+            if rep > 0 and (best is None or cycles < best[0]):
+                best = (cycles, e0.elapsed_time(e1))
+        cycles, ms = best
+        ops = blocks * threads * iters * chains * per_instr
+        clk = statistics.median(r["sm"] for r in sampler.rows[-20:]) if sampler.rows else None
+        print(json.dumps({"micro": "exp", "op": name, "ops_per_s": ops / (ms * 1e-3),
+                          "ops_per_sm_per_clock_at_sampled_clock": (ops / (ms * 1e-3) / sms / (clk * 1e6)
+                                                                    if clk else None),
+                          "sampled_sm_mhz": clk, "kernel_ms": ms, "blocks": blocks, "threads": threads,
+                          "iters": iters, "chains": chains}), flush=True)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    mcyc = torch.zeros(sms, dtype=torch.int64, device="cuda")
+    reps = 4096
+    for n in (32, 64, 128, 256):
+        for ts in (0, 1):
+            for accs in (1, 2, 4, 8):
+                if accs * n > 256:
+                    continue
+                vals = []
+                for rep in range(3):
+                    rc = lib.evo_micro_mma(n, ts, accs, sms, reps, ctypes.c_void_p(mcyc.data_ptr()),
+                                           ctypes.c_void_p(status.data_ptr()), stream)
+                    torch.cuda.synchronize()
+                    if rc != 0 or int(status.item()) != 0:
+                        raise RuntimeError(f"micro_mma N={n} ts={ts}: rc {rc} status {int(status.item())}")
+                    vals.append(statistics.median(mcyc.cpu().tolist()) / reps)
+                cpi = min(vals[1:])
+                print(json.dumps({"micro": "mma", "form": "TS (A in TMEM)" if ts else "SS (A, B in smem)",
+                                  "M": 128, "N": n, "K": 16, "independent_accumulators": accs,
+                                  "cycles_per_mma": cpi, "flop_per_sm_per_clock": 2 * 128 * n * 16 / cpi}),
+                      flush=True)
+    rows = sampler.stop()
+    print(json.dumps({"micro": "clocks", **summarize_clocks(rows, 0, 1e18, sampler.source)}), flush=True)
+    return 0
+
+
 def main():
     args = parse_args()
+    if args.micro:
+        return run_micro(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

@@ -4,7 +4,9 @@
 
 Each translation unit under csrc/ compiles in parallel to an object under
 _build/, then nvcc links the shared library into memory_efficient_biased_gb300/_lib/.
-Objects are rebuilt only when a source or header is newer than them.
+The throughput microbenchmarks under csrc/micro/ (run by `bench.py --micro`)
+link into a library of their own, libevo_micro.so.  Objects are rebuilt only
+when a source or header is newer than them.
 """
 from __future__ import annotations
 
@@ -22,6 +24,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "libevo_attn.so")
+MICRO_LIB = os.path.join(LIBDIR, "libevo_micro.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
@@ -35,8 +38,9 @@ def nvcc() -> str:
     return p
 
 
-def sources():
-    return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cu"))
+def sources(sub: str = ""):
+    d = os.path.join(CSRC, sub)
+    return sorted(os.path.join(d, f) for f in os.listdir(d) if f.endswith(".cu"))
 
 
 def headers():
@@ -54,12 +58,13 @@ def build(force: bool = False, jobs: int = 8, verbose: bool = False) -> str:
     os.makedirs(LIBDIR, exist_ok=True)
     hdr_time = _newest(headers())
     cmds = []
-    objs = []
-    for src in sources():
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
-        objs.append(obj)
-        if force or not os.path.exists(obj) or os.path.getmtime(obj) < max(os.path.getmtime(src), hdr_time):
-            cmds.append([nvcc(), *ARCH, *CFLAGS, "-c", src, "-o", obj])
+    libs = {LIB: [], MICRO_LIB: []}
+    for lib, sub in ((LIB, ""), (MICRO_LIB, "micro")):
+        for src in sources(sub):
+            obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+            libs[lib].append(obj)
+            if force or not os.path.exists(obj) or os.path.getmtime(obj) < max(os.path.getmtime(src), hdr_time):
+                cmds.append([nvcc(), *ARCH, *CFLAGS, "-c", src, "-o", obj])
 
     def run(cmd):
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -70,12 +75,13 @@ def build(force: bool = False, jobs: int = 8, verbose: bool = False) -> str:
 
     with ThreadPoolExecutor(max_workers=max(1, jobs)) as ex:
         list(ex.map(run, cmds))
-    if cmds or not os.path.exists(LIB) or os.path.getmtime(LIB) < _newest(objs):
-        link = [nvcc(), *ARCH, "-shared", "-Xcompiler", "-fPIC", "-o", LIB, *objs]
-        r = subprocess.run(link, capture_output=True, text=True)
-        if r.returncode:
-            sys.stderr.write(r.stdout + r.stderr)
-            raise RuntimeError("link of libevo_attn.so failed")
+    for lib, objs in libs.items():
+        if cmds or not os.path.exists(lib) or os.path.getmtime(lib) < _newest(objs):
+            link = [nvcc(), *ARCH, "-shared", "-Xcompiler", "-fPIC", "-o", lib, *objs]
+            r = subprocess.run(link, capture_output=True, text=True)
+            if r.returncode:
+                sys.stderr.write(r.stdout + r.stderr)
+                raise RuntimeError(f"link of {os.path.basename(lib)} failed")
     return LIB
 
 

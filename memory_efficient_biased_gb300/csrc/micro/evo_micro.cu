@@ -1,0 +1,280 @@
+// evo_micro.cu — throughput microbenchmarks behind the kernels' design choices
+// (not part of the attention library: built into its own libevo_micro.so and
+// run by `python bench.py --micro`).
+//
+//  * exponentials: sustained rate of the special-function unit for
+//    ex2.approx.ftz.f32, ex2.approx.f16x2 and ex2.approx.ftz.bf16x2, of the
+//    FMA-pipe polynomial 2^x used to offload part of the softmax exponentials,
+//    scalar and packed f32x2, and of plain fma / fma.f32x2 for scale;
+//  * tcgen05.mma issue cost: cycles per kind::f16 instruction (M = 128,
+//    K = 16) with both operands in shared memory (SS) or A in tensor memory
+//    (TS), for N = 32 .. 256.
+//
+// Every kernel records clock64() deltas per block, so the rates come out per SM
+// clock independently of the clock the GPU ran at.  All waits are bounded.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "../evo_ptx.cuh"
+
+#define EVO_MICRO_API extern "C" __attribute__((visibility("default")))
+
+namespace {
+
+using namespace evo;
+
+// ---------------------------------------------------------------- exponentials
+constexpr int kChains = 8;  // independent dependency chains per thread
+
+__device__ __forceinline__ uint32_t ex2_f16x2(uint32_t x) {
+  uint32_t y;
+  asm volatile("{\n\t.reg .b32 t;\n\tneg.f16x2 t, %1;\n\tex2.approx.f16x2 %0, t;\n\t}" : "=r"(y) : "r"(x));
+  return y;
+}
+__device__ __forceinline__ uint32_t ex2_bf16x2(uint32_t x) {
+  uint32_t y;
+  asm volatile("{\n\t.reg .b32 t;\n\tneg.bf16x2 t, %1;\n\tex2.approx.ftz.bf16x2 %0, t;\n\t}" : "=r"(y) : "r"(x));
+  return y;
+}
+__device__ __forceinline__ float ex2_neg(float x) {
+  float y;
+  asm volatile("{\n\t.reg .f32 t;\n\tneg.f32 t, %1;\n\tex2.approx.ftz.f32 %0, t;\n\t}" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// 2^x on the FMA pipe: x = j + f with j = round(x) (the 1.5·2^23 rounding
+// trick), f in [-1/2, 1/2]; 2^f by a degree-3 polynomial fitted for minimal
+// relative error (coefficients from fit_exp2_poly.py in this directory's
+// parent; max relative error 7.5e-5); 2^j added to the exponent field.
+// Valid for x >= -125 (callers clamp), exact powers of two aside.
+constexpr float kRound = 12582912.0f;  // 1.5 * 2^23
+constexpr float kP0 = 0.9999281167984009f, kP1 = 0.6932609677314758f, kP2 = 0.24261054396629333f,
+                kP3 = 0.05517132207751274f;
+__device__ __forceinline__ float exp2_poly(float x) {
+  x = fmaxf(x, -125.0f);
+  const float t = x + kRound;
+  const float f = x - (t - kRound);
+  float p = fmaf(kP3, f, kP2);
+  p = fmaf(p, f, kP1);
+  p = fmaf(p, f, kP0);
+  return __int_as_float(__float_as_int(p) + (__float_as_int(t) << 23));
+}
+__device__ __forceinline__ float2 exp2_poly2(float2 x) {
+  x.x = fmaxf(x.x, -125.0f);
+  x.y = fmaxf(x.y, -125.0f);
+  const float2 r = make_float2(kRound, kRound), nr = make_float2(-kRound, -kRound);
+  const float2 t = add2(x, r);
+  const float2 f = fma2(add2(t, nr), make_float2(-1.0f, -1.0f), x);
+  float2 p = fma2(make_float2(kP3, kP3), f, make_float2(kP2, kP2));
+  p = fma2(p, f, make_float2(kP1, kP1));
+  p = fma2(p, f, make_float2(kP0, kP0));
+  return make_float2(__int_as_float(__float_as_int(p.x) + (__float_as_int(t.x) << 23)),
+                     __int_as_float(__float_as_int(p.y) + (__float_as_int(t.y) << 23)));
+}
+
+enum ExpKind : int {
+  kEx2F32 = 0,     // ex2.approx.ftz.f32 (1 exp / instruction)
+  kEx2F16x2 = 1,   // ex2.approx.f16x2 (2 exps / instruction)
+  kEx2BF16x2 = 2,  // ex2.approx.ftz.bf16x2 (2 exps / instruction)
+  kPoly = 3,       // FMA-pipe polynomial, scalar
+  kPoly2 = 4,      // FMA-pipe polynomial, packed f32x2
+  kFma = 5,        // fma.rn.f32 (1 op / instruction)
+  kFma2 = 6,       // fma.rn.f32x2 (2 ops / instruction)
+  kMix31 = 7,      // 3 ex2.f32 : 1 packed polynomial pair (the softmax offload mix)
+};
+
+template <int K>
+__global__ void __launch_bounds__(512, 4) micro_exp(float* sink, long long* cyc, int iters) {
+  float x[kChains];
+#pragma unroll
+  for (int c = 0; c < kChains; ++c) x[c] = 0.25f + 0.01f * ((threadIdx.x + c) & 15);
+  __syncthreads();
+  const long long t0 = clock64();
+#pragma unroll 4
+  for (int i = 0; i < iters; ++i) {  // unrolled so that loop overhead stays small next to 32 ops
+    if constexpr (K == kEx2F32) {
+#pragma unroll
+      for (int c = 0; c < kChains; ++c) x[c] = ex2_neg(x[c]);
+    } else if constexpr (K == kEx2F16x2 || K == kEx2BF16x2) {
+#pragma unroll
+      for (int c = 0; c < kChains; ++c) {
+        uint32_t v = __float_as_uint(x[c]);
+        v = K == kEx2F16x2 ? ex2_f16x2(v) : ex2_bf16x2(v);
+        x[c] = __uint_as_float(v);
+      }
+    } else if constexpr (K == kPoly) {
+#pragma unroll
+      for (int c = 0; c < kChains; ++c) x[c] = exp2_poly(-x[c]);
+    } else if constexpr (K == kPoly2) {
+#pragma unroll
+      for (int c = 0; c < kChains; c += 2) {
+        const float2 r = exp2_poly2(make_float2(-x[c], -x[c + 1]));
+        x[c] = r.x;
+        x[c + 1] = r.y;
+      }
+    } else if constexpr (K == kFma) {
+#pragma unroll
+      for (int c = 0; c < kChains; ++c) x[c] = fmaf(x[c], 0.999f, 0.001f);
+    } else if constexpr (K == kFma2) {
+#pragma unroll
+      for (int c = 0; c < kChains; c += 2) {
+        const float2 r = fma2(make_float2(x[c], x[c + 1]), make_float2(0.999f, 0.999f), make_float2(0.001f, 0.001f));
+        x[c] = r.x;
+        x[c + 1] = r.y;
+      }
+    } else {  // kMix31: chains 0..5 on the SFU, 6..7 by the packed polynomial
+#pragma unroll
+      for (int c = 0; c < 6; ++c) x[c] = ex2_neg(x[c]);
+      const float2 r = exp2_poly2(make_float2(-x[6], -x[7]));
+      x[6] = r.x;
+      x[7] = r.y;
+    }
+  }
+  __syncthreads();
+  const long long t1 = clock64();
+  float s = 0.0f;
+#pragma unroll
+  for (int c = 0; c < kChains; ++c) s += x[c];
+  if (s == 12345.0f) sink[threadIdx.x] = s;  // keeps the chains live
+  if (threadIdx.x == 0) cyc[blockIdx.x] = t1 - t0;
+}
+
+// ---------------------------------------------------------------- MMA issue cost
+constexpr uint64_t kWaitNs = 1000000000ull;  // 1 s bound on the completion wait
+
+struct MmaSmem {
+  alignas(1024) uint8_t a[128 * 64];  // 128 rows x 64 bytes, 64B swizzle
+  alignas(1024) uint8_t b[256 * 64];  // up to 256 rows x 64 bytes
+  uint64_t done;
+  uint32_t tmem_slot;
+  int abort;
+};
+
+// One thread issues `reps` MMAs (M = 128, N, K = 16; reps a multiple of 16),
+// round robin over ACCS independent accumulators (ACCS * N <= 256 columns), in
+// straight-line groups of 16 with compile-time addresses so that the issue loop
+// itself costs next to nothing; the block reports the cycles from the first issue
+// to the completion of the last.  Operand contents are whatever shared/tensor
+// memory holds: only time matters.
+template <int N, bool TS, int ACCS>
+__global__ void __launch_bounds__(128, 1) micro_mma(long long* cyc, int reps, int* status) {
+  __shared__ MmaSmem sm;
+  const int warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) {
+    sm.abort = 0;
+    mbar_init(smem_u32(&sm.done), 1);
+    fence_barrier_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(&sm.tmem_slot), 512);
+    tmem_relinquish();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_slot;
+  if (threadIdx.x == 0) {
+    constexpr uint32_t id = idesc_f16(128, N, true, false, false);
+    const uint64_t ad = smem_desc(smem_u32(sm.a), 16, 8 * 64, kSwizzle64B);
+    const uint64_t bd = smem_desc(smem_u32(sm.b), 16, 8 * 64, kSwizzle64B);
+    const long long t0 = clock64();
+#pragma unroll 1
+    for (int r = 0; r < reps; r += 16) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const uint32_t k = i & 1;  // alternate the two K = 16 slices of the 32-wide rows
+        const uint32_t d = tmem + static_cast<uint32_t>((i % ACCS) * N);
+        const uint32_t acc = (r > 0 || i >= ACCS) ? 1u : 0u;
+        if (TS)
+          umma_ts(d, tmem + 256 + k * 8, bd + k * 2, id, acc);
+        else
+          umma_ss(d, ad + k * 2, bd + k * 2, id, acc);
+      }
+    }
+    umma_commit(smem_u32(&sm.done));
+    WaitGuard g{kWaitNs, status, &sm.abort};
+    mbar_wait(smem_u32(&sm.done), 0, g);
+    const long long t1 = clock64();
+    cyc[blockIdx.x] = t1 - t0;
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int K>
+cudaError_t run_exp(int blocks, int iters, float* sink, long long* cyc, cudaStream_t st) {
+  micro_exp<K><<<blocks, 512, 0, st>>>(sink, cyc, iters);
+  return cudaGetLastError();
+}
+
+template <int N, bool TS>
+cudaError_t run_mma_t(int blocks, int reps, int accs, long long* cyc, int* status, cudaStream_t st) {
+  switch (accs) {
+    case 1: micro_mma<N, TS, 1><<<blocks, 128, 0, st>>>(cyc, reps, status); break;
+    case 2: micro_mma<N, TS, 2><<<blocks, 128, 0, st>>>(cyc, reps, status); break;
+    case 4:
+      if (4 * N > 256) return cudaErrorInvalidValue;
+      micro_mma<N, TS, (4 * N <= 256 ? 4 : 1)><<<blocks, 128, 0, st>>>(cyc, reps, status);
+      break;
+    case 8:
+      if (8 * N > 256) return cudaErrorInvalidValue;
+      micro_mma<N, TS, (8 * N <= 256 ? 8 : 1)><<<blocks, 128, 0, st>>>(cyc, reps, status);
+      break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+template <int N>
+cudaError_t run_mma(int ts, int blocks, int reps, int accs, long long* cyc, int* status, cudaStream_t st) {
+  if (accs < 1 || accs * N > 256 || reps % 16 != 0) return cudaErrorInvalidValue;
+  return ts ? run_mma_t<N, true>(blocks, reps, accs, cyc, status, st)
+            : run_mma_t<N, false>(blocks, reps, accs, cyc, status, st);
+}
+
+}  // namespace
+
+// Exponential / FMA throughput: `blocks` blocks of 512 threads, each thread running
+// `iters` iterations of 8 independent chains of the op `kind` (ExpKind above).
+// sink: device float[512] (never written in practice); cycles: device int64[blocks],
+// the clock64() span of each block.  Returns a cudaError_t value.
+EVO_MICRO_API int evo_micro_exp(int kind, int blocks, int iters, void* sink, void* cycles, void* stream) {
+  float* s = static_cast<float*>(sink);
+  long long* c = static_cast<long long*>(cycles);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (blocks <= 0 || iters <= 0 || !sink || !cycles) return cudaErrorInvalidValue;
+  switch (kind) {
+    case kEx2F32: return run_exp<kEx2F32>(blocks, iters, s, c, st);
+    case kEx2F16x2: return run_exp<kEx2F16x2>(blocks, iters, s, c, st);
+    case kEx2BF16x2: return run_exp<kEx2BF16x2>(blocks, iters, s, c, st);
+    case kPoly: return run_exp<kPoly>(blocks, iters, s, c, st);
+    case kPoly2: return run_exp<kPoly2>(blocks, iters, s, c, st);
+    case kFma: return run_exp<kFma>(blocks, iters, s, c, st);
+    case kFma2: return run_exp<kFma2>(blocks, iters, s, c, st);
+    case kMix31: return run_exp<kMix31>(blocks, iters, s, c, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+// tcgen05.mma issue cost: `blocks` blocks (one per SM), each issuing `reps` MMAs of
+// M = 128, the given N (32, 64, 128 or 256), K = 16, round robin over `accs`
+// independent accumulators (accs * N <= 256); ts != 0 reads A from tensor memory.
+// cycles: device int64[blocks]; status: device int, set to 8 if the completion wait
+// ran out.  Returns a cudaError_t value.
+EVO_MICRO_API int evo_micro_mma(int n, int ts, int accs, int blocks, int reps, void* cycles, void* status,
+                                void* stream) {
+  long long* c = static_cast<long long*>(cycles);
+  int* s = static_cast<int*>(status);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (blocks <= 0 || reps <= 0 || !cycles || !status) return cudaErrorInvalidValue;
+  switch (n) {
+    case 32: return run_mma<32>(ts, blocks, reps, accs, c, s, st);
+    case 64: return run_mma<64>(ts, blocks, reps, accs, c, s, st);
+    case 128: return run_mma<128>(ts, blocks, reps, accs, c, s, st);
+    case 256: return run_mma<256>(ts, blocks, reps, accs, c, s, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
