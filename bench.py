@@ -19,12 +19,14 @@ host↔device copies inside the timed region.  The timed steps are CUDA-graph
 replays over R input replicas whose total exceeds 3× the L2 cache, so no step
 reads inputs left in L2 by the previous one.  Per-kernel times come from CUDA
 events that the library records around each of its launches inside the timed
-replays (evo_attn_profile_events).  `--impl reference` times the fp64 CPU
+replays (the per-call profiling events of evo_attn_fwd_opts / evo_attn_bwd_opts).
+`--impl reference` times the fp64 CPU
 oracle on bounded samples of the same workload (it is the reference arm).
 """
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -54,6 +56,9 @@ def parse_args():
     ap.add_argument("--workload", default="msa_col",
                     help="msa_col (default: the largest configuration, B=1 N=384 L=1024 H=8 D=32), msa_row, "
                          "many_head, triangle or tiny")
+    ap.add_argument("--rows", type=int, default=0,
+                    help="run the workload with this many rows N instead of its own (same L, H, D, masks): a "
+                         "reduced instance for ncu captures; never a headline")
     ap.add_argument("--micro", action="store_true",
                     help="run the throughput microbenchmarks (exponentials, FMA, tcgen05.mma issue) instead")
     ap.add_argument("--dtype", default="bf16", choices=("bf16", "fp16"))
@@ -380,11 +385,15 @@ def run_ours(args):
     from memory_efficient_biased_gb300.workload import WORKLOADS, workload_inputs
 
     w = WORKLOADS[args.workload]
+    if args.rows:
+        w = dataclasses.replace(w, N=args.rows, name=f"{w.name} (N={args.rows}, reduced for profiling)")
     dt = {"bf16": torch.bfloat16, "fp16": torch.float16}[args.dtype]
     # clocks are sampled from here to the end of the measurements
     sampler = ClockSampler(local) if rank == 0 else None
-    E.evo_attn_set_masked_tile_skip(args.skip_masked_tiles, -1.0e4)
     inp = workload_inputs(args.workload, args.dtype, seed=rank)
+    if args.rows:  # the first rows of the full workload's inputs (bias2 is shared by the rows)
+        inp = {k: (None if v is None else (v if k == "bias2" else v[:, :args.rows].contiguous()))
+               for k, v in inp.items()}
     has_b1, has_b2 = inp["bias1"] is not None, inp["bias2"] is not None
     shape = (w.B, w.N, w.L, w.H, w.D)
     ws_bytes = E.evo_attn_bwd_workspace_bytes(shape, dt, has_b2)
@@ -404,10 +413,18 @@ def run_ours(args):
 
     reps = [replica() for _ in range(R)]
 
-    def step(d):
-        E.evo_attn_fwd(d["q"], d["k"], d["v"], d["bias1"], d["bias2"], out=d["out"], lse=d["lse"])
-        E.evo_attn_bwd(d["q"], d["k"], d["v"], d["bias1"], d["bias2"], d["out"], d["lse"], d["do"],
-                       dq=d["dq"], dk=d["dk"], dv=d["dv"], dbias2=d["db2"], workspace=d["ws"])
+    skip = dict(skip_masked_tiles=args.skip_masked_tiles, skip_threshold=-1.0e4)
+
+    def step(d, events=None):
+        E.evo_attn_fwd_opts(d["q"], d["k"], d["v"], d["bias1"], d["bias2"], out=d["out"], lse=d["lse"],
+                            events=events, **skip)
+        E.evo_attn_bwd_opts(d["q"], d["k"], d["v"], d["bias1"], d["bias2"], d["out"], d["lse"], d["do"],
+                            dq=d["dq"], dk=d["dk"], dv=d["dv"], dbias2=d["db2"], workspace=d["ws"], events=events,
+                            **skip)
+
+    def status_ok():
+        return E.evo_attn_device_status() == 0 and all(E.evo_attn_bwd_status(d["ws"]) == 0 for d in reps if d["ws"]
+                                                       is not None)
 
     # peak device memory per call (outputs + workspace the call needs), before anything else is cached
     torch.cuda.synchronize()
@@ -424,7 +441,7 @@ def run_ours(args):
     peak_bwd = torch.cuda.max_memory_allocated() - base
     memory = memory_versus_dense(d0) if rank == 0 else None
     del out, lse
-    if E.evo_attn_device_status() != 0:
+    if not status_ok():
         raise RuntimeError("device wait timed out during set-up")
 
     # two graphs per replica: the timed one (the step alone) and an instrumented one with
@@ -444,10 +461,8 @@ def run_ours(args):
             step(d)
         graphs.append(g)
         gi = torch.cuda.CUDAGraph()
-        E.evo_attn_profile_events(evs[r])
         with torch.cuda.graph(gi, stream=cap_stream):
-            step(d)
-        E.evo_attn_profile_events(None)
+            step(d, events=evs[r])
         igraphs.append(gi)
     torch.cuda.synchronize()
 
@@ -471,7 +486,7 @@ def run_ours(args):
     if world > 1:
         torch.distributed.barrier()
     ms_total = max_over_ranks(t_start.elapsed_time(t_end))
-    if E.evo_attn_device_status() != 0:
+    if not status_ok():
         raise RuntimeError("device wait timed out during the timed region")
 
     # per-kernel durations: the instrumented graphs, replayed as many steps as were timed
@@ -485,14 +500,14 @@ def run_ours(args):
     torch.cuda.synchronize()
     ms_instrumented = ti0.elapsed_time(ti1) / ksteps
     clock_rows = sampler.stop() if sampler else []
-    if E.evo_attn_device_status() != 0:
+    if not status_ok():
         raise RuntimeError("device wait timed out during the instrumented replays")
-    # only the slots of kernels that launched: the dQ cast runs on the per-key-tile schedule alone
+    # the slots of the kernels that launch (no dQ cast kernel: every schedule writes dQ itself)
     mode = bwd_mode(w)
-    names = ["fwd", "bwd_pre", "bwd_main", "bwd_dq_cast"] + (["bwd_db2_part", "bwd_db2_sum"] if has_b2 else [])
-    pairs = [(0, 1), (2, 3), (3, 4), (4, 5)] + ([(5, 6), (6, 7)] if has_b2 else [])
+    names = ["fwd", "bwd_pre", "bwd_main"] + (["bwd_db2_part", "bwd_db2_sum"] if has_b2 else [])
+    pairs = [(0, 1), (2, 3), (3, 4)] + ([(5, 6), (6, 7)] if has_b2 else [])
     kern_ms = {n: statistics.mean(evs[r][a].elapsed_time(evs[r][b]) for r in range(R))
-               for n, (a, b) in zip(names, pairs) if n != "bwd_dq_cast" or mode == "main"}
+               for n, (a, b) in zip(names, pairs)}
 
     F = flops(w)
     ms_step = ms_total / args.steps
@@ -509,11 +524,8 @@ def run_ours(args):
         "fwd": ("tensor", F["fwd"]),
         "bwd_main": ("tensor", F["bwd"]),
         "bwd_db2_part": ("tensor", 4.0 * E_el * w.D),
-        # O, dO read, delta written; plus clearing the fp32 dQ accumulator (per-key-tile mode)
-        # or the transposed pair-bias copy (key-major mode)
-        "bwd_pre": ("hbm", 2 * qkv + bnhl * 4 + (2 * qkv if mode == "main" else 0)
-                    + (2 * b2b if mode == "key-major" else 0)),
-        "bwd_dq_cast": ("hbm", 2 * qkv + qkv),
+        # O, dO read, delta written; plus the transposed pair-bias copy (key-major mode)
+        "bwd_pre": ("hbm", 2 * qkv + bnhl * 4 + (2 * b2b if mode == "key-major" else 0)),
         "bwd_db2_sum": ("hbm", bias2_groups(w) * w.B * w.H * w.L * w.L * 4 + b2b if has_b2 else 0),
     }
     # The kernels are timed in windows far shorter than the seconds-long loop of the
@@ -578,10 +590,10 @@ def run_ours(args):
                "kind": "oracle",
                "sample": f"fp64 numpy oracle fwd+bwd of rows n<{rows} of N={w.N} (batch 0), {dt_cpu:.1f} s"}
 
-    # forward; delta, the backward kernel, the dQ cast (per-key-tile schedule only), the
-    # skip bits and work list (per-key-tile schedule with skipping); the two pair-bias stages
-    launches_per_step = (1 + 2 + (1 if mode == "main" else 0) + (2 if mode == "main" and args.skip_masked_tiles
-                                                                  and has_b1 else 0) + (2 if has_b2 else 0))
+    # forward; delta, the backward kernel, the skip bits (per-key-tile schedule with
+    # skipping); the two pair-bias stages
+    launches_per_step = (1 + 2 + (1 if mode == "main" and args.skip_masked_tiles and has_b1 else 0)
+                         + (2 if has_b2 else 0))
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -687,6 +699,17 @@ def run_micro(args):
                                   "M": 128, "N": n, "K": 16, "independent_accumulators": accs,
                                   "cycles_per_mma": cpi, "flop_per_sm_per_clock": 2 * 128 * n * 16 / cpi}),
                       flush=True)
+    for pw in (1, 2, 4):
+        vals = []
+        for rep in range(3):
+            rc = lib.evo_micro_tmem_ld(pw, sms, 4096, ctypes.c_void_p(mcyc.data_ptr()), ctypes.c_void_p(sink.data_ptr()),
+                                       stream)
+            torch.cuda.synchronize()
+            if rc != 0:
+                raise RuntimeError(f"micro_tmem_ld {pw}: rc {rc}")
+            vals.append(statistics.median(mcyc.cpu().tolist()) / 4096)
+        print(json.dumps({"micro": "tmem_ld", "loads_per_wait": pw, "columns_per_load": 32,
+                          "cycles_per_round": min(vals[1:])}), flush=True)
     rows = sampler.stop()
     print(json.dumps({"micro": "clocks", **summarize_clocks(rows, 0, 1e18, sampler.source)}), flush=True)
     return 0

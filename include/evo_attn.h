@@ -38,8 +38,15 @@
  *
  * Conventions for every entry point:
  *  - Pointers named as device pointers must point to memory of the current
- *    CUDA device; the caller owns all buffers.  The library keeps no
- *    per-call state and allocates no device memory.
+ *    CUDA device; the caller owns all buffers.  The library allocates no
+ *    device memory and has no settings: everything a call does is decided by
+ *    its arguments (evo_options_t for what goes beyond the tensors), so calls
+ *    from several threads or on several streams do not affect each other.
+ *    What the library itself holds is fixed at load: a per-device cache of
+ *    device properties, one fallback device status word per device (for
+ *    calls given no status location, see evo_attn_device_status), the
+ *    calling thread's last-error text, and the scratch array of
+ *    evo_attn_bwd_noalloc.
  *  - Device buffers of the tensors above must be 16-byte aligned, except
  *    bias1 (2-byte) and lse (4-byte); the backward workspace 256-byte.
  *  - Outputs are overwritten, never accumulated into, and must not overlap
@@ -49,7 +56,10 @@
  *    anything is launched, and leave every buffer untouched.  A failed kernel
  *    launch returns EVO_ERR_CUDA.
  *  - Every device-side wait is bounded.  A wait that runs out sets a device
- *    status word instead of hanging; evo_attn_device_status() reports it.
+ *    status word instead of hanging: the location the call's options give,
+ *    else the backward workspace's own word (evo_attn_bwd_opts, read with
+ *    evo_attn_bwd_status), else the fallback word (read with
+ *    evo_attn_device_status).
  */
 #ifndef EVO_ATTN_H
 #define EVO_ATTN_H
@@ -61,7 +71,7 @@
 extern "C" {
 #endif
 
-#define EVO_ATTN_ABI_VERSION 3
+#define EVO_ATTN_ABI_VERSION 4
 
 /* Every entry point below is exported from libevo_attn.so; nothing else is. */
 #if defined(__GNUC__)
@@ -130,6 +140,69 @@ typedef struct {
   evo_strides_t q, k, v, out, dout, dq, dk, dv;
 } evo_layout_t;
 
+/*
+ * Per-call options of evo_attn_fwd_opts and evo_attn_bwd_opts.  Zero the
+ * struct, set `size` to sizeof(evo_options_t), then set what the call needs;
+ * a NULL options pointer means the defaults (all zero).  Nothing is kept after
+ * the call returns.  A struct whose size is too small, with unknown flag bits,
+ * or with num_events > 0 and events == NULL is EVO_ERR_BAD_ARGUMENT.
+ *
+ *   flags          EVO_OPT_SKIP_MASKED_TILES: masked key-tile skipping.  A key
+ *                  j of row (b, n) counts as masked when bias1[b,n,j] <=
+ *                  skip_threshold (a NaN counts as kept); every 128-key tile of
+ *                  a row whose keys are all masked is skipped, as long as the
+ *                  row keeps some key.  The forward skips on every shape with
+ *                  L <= 8192; the backward on the shapes whose dQ tiles do not
+ *                  fit in tensor memory (its per-key-tile schedule), writing the
+ *                  skipped tiles' dK and dV as zeros.  The results are those of
+ *                  the unskipped computation whenever each masked key's scaled,
+ *                  biased score lies more than 88 below its row's largest one:
+ *                  its fp32 exponential is then exactly 0 either way (page
+ *                  §3.6's key mask, a very large negative bias, meets this by
+ *                  far).  Skipped tiles still count in any nominal FLOP figure
+ *                  derived from the shape.
+ *                  EVO_OPT_NO_DBIAS2 (backward only): do not compute the
+ *                  pair-bias gradient; dbias2 must then be NULL even with a
+ *                  bias2, and the workspace may be sized with EVO_WS_NO_DBIAS2.
+ *   skip_threshold see EVO_OPT_SKIP_MASKED_TILES (e.g. -1e4).
+ *   wait_limit_ns  bound on every device-side wait of the call (0 = 2e9; values
+ *                  below 1000 are raised to 1000).
+ *   status         device int the call's kernels set to EVO_ERR_DEVICE_TIMEOUT
+ *                  if a wait runs out (the caller clears it); NULL: the forward
+ *                  uses the fallback word, the backward its workspace's word.
+ *   events, num_events
+ *                  profiling: caller-owned CUDA events (cudaEvent_t, timing
+ *                  enabled), at most 8 used, recorded on the call's stream
+ *                  around each kernel it launches:
+ *                    forward:  events[0] before its kernel, events[1] after it;
+ *                    backward: events[2] before its first kernel, then one
+ *                    event after each kernel in launch order — events[3] after
+ *                    delta, events[4] after the main backward kernel (with
+ *                    masked-tile skipping on the per-key-tile schedule its
+ *                    skip-bit kernel runs between events[3] and events[4]),
+ *                    events[5] recorded right after events[4], and with the
+ *                    pair-bias gradient events[6] after its per-group partials
+ *                    and events[7] after their fixed-order sum.  With dbias1,
+ *                    its partial and sum kernels run between events[5] and
+ *                    events[6].  A call split batch by batch (strided layouts)
+ *                    records them for its last batch.  Indices >= num_events
+ *                    are skipped.  Recording works inside stream capture (the
+ *                    records become graph nodes).
+ */
+#define EVO_OPT_SKIP_MASKED_TILES 1u
+#define EVO_OPT_NO_DBIAS2 2u
+
+typedef struct {
+  uint32_t size;
+  uint32_t flags;
+  float skip_threshold;
+  uint32_t reserved;
+  uint64_t wait_limit_ns;
+  int* status;
+  void* const* events;
+  int32_t num_events;
+} evo_options_t;
+
 /* For the calling thread's last call that returned EVO_ERR_CUDA: which step
  * failed and the CUDA error name and code (static thread-local text, valid
  * until this thread's next failing call; "" if none failed). */
@@ -165,21 +238,34 @@ EVO_API evo_status_t evo_attn_fwd_strided(const void* q, const void* k, const vo
                                           evo_shape_t shape, evo_dtype_t dtype,
                                           const evo_layout_t* layout, void* stream);
 
+/*
+ * evo_attn_fwd_strided with per-call options (evo_options_t; NULL = defaults,
+ * exactly evo_attn_fwd_strided).  EVO_OPT_NO_DBIAS2 is EVO_ERR_BAD_ARGUMENT here.
+ */
+EVO_API evo_status_t evo_attn_fwd_opts(const void* q, const void* k, const void* v,
+                                       const void* bias1, const void* bias2,
+                                       void* out, float* lse,
+                                       evo_shape_t shape, evo_dtype_t dtype,
+                                       const evo_layout_t* layout, const evo_options_t* opts,
+                                       void* stream);
+
 /* Flags of evo_attn_bwd_workspace_bytes (bit 0 keeps the meaning of the
  * former has_bias2 argument, so passing 0 / 1 still works). */
-#define EVO_WS_BIAS2 1  /* the call has a pair bias (and computes dbias2)  */
-#define EVO_WS_DBIAS1 2 /* the call computes dbias1 (evo_attn_bwd_ex)       */
+#define EVO_WS_BIAS2 1     /* the call has a pair bias (and computes dbias2)     */
+#define EVO_WS_DBIAS1 2    /* the call computes dbias1 (evo_attn_bwd_ex)          */
+#define EVO_WS_NO_DBIAS2 4 /* with a pair bias, no dbias2 (EVO_OPT_NO_DBIAS2)     */
 
 /*
  * Bytes of device workspace the backward needs for this problem (0 on a bad
- * shape or dtype).  It holds the fp32 row terms delta [B,N,H,L]; the fp32 dQ
- * accumulator [B,N,L,H,D] for the shapes whose dQ tiles do not fit in tensor
- * memory; with EVO_WS_BIAS2, the fp32 per-group partial sums of the pair-bias
- * gradient and, where a key-major kernel runs, a transposed copy of the pair
- * bias; with EVO_WS_DBIAS1, fp32 per-(b, n, h) partial sums of the key-mask
- * gradient; for the shapes whose dQ goes through the accumulator, room for the
- * work list of masked key-tile skipping.  Depends only on its arguments; enough
- * for every layout of evo_attn_bwd_strided.
+ * shape, dtype or flag).  It holds the call's status word (256 bytes); the
+ * fp32 row terms delta [B,N,H,L]; for the shapes whose dQ tiles do not fit in
+ * tensor memory, L x DP fp32 dQ rows (DP = D rounded up to 16, 32 or 64) for
+ * each of at most 256 CTAs, and the skip bits of masked key-tile skipping;
+ * with EVO_WS_BIAS2, where a key-major kernel runs, a transposed copy of the
+ * pair bias, and unless EVO_WS_NO_DBIAS2 the fp32 per-group partial sums of the
+ * pair-bias gradient; with EVO_WS_DBIAS1, fp32 per-(b, n, h) partial sums of
+ * the key-mask gradient.  Depends only on its arguments; enough for every
+ * layout of evo_attn_bwd_strided.
  */
 EVO_API size_t evo_attn_bwd_workspace_bytes(evo_shape_t shape, evo_dtype_t dtype, int flags);
 
@@ -193,7 +279,8 @@ EVO_API size_t evo_attn_bwd_workspace_bytes(evo_shape_t shape, evo_dtype_t dtype
  *   dbias2                : [B,1,H,L,L] output, required iff bias2 != NULL.
  *                           Summed over N in fp32 in a fixed order (two stages:
  *                           per-group partials, then a fixed-order sum of the
- *                           groups), so repeated calls give identical bytes;
+ *                           groups).  Every gradient is summed in a fixed order,
+ *                           so repeated calls give identical bytes;
  *   workspace             : >= evo_attn_bwd_workspace_bytes(...) bytes, caller-owned,
  *                           contents need not be initialised; clobbered.
  * The gradient of bias1 is produced by evo_attn_bwd_ex.
@@ -240,67 +327,49 @@ EVO_API evo_status_t evo_attn_bwd_strided(const void* q, const void* k, const vo
                                           const evo_layout_t* layout, void* stream);
 
 /*
- * Synchronises `stream`, then reads and clears the library's device status
+ * evo_attn_bwd_strided with per-call options (evo_options_t; NULL = defaults).
+ * Unlike the entry points above, which record a timeout in the fallback word,
+ * this one records it in its workspace's own status word (cleared by the
+ * call's first kernel) unless opts->status is given; read it with
+ * evo_attn_bwd_status.  With EVO_OPT_NO_DBIAS2, dbias2 must be NULL and no
+ * pair-bias gradient is computed.
+ */
+EVO_API evo_status_t evo_attn_bwd_opts(const void* q, const void* k, const void* v,
+                                       const void* bias1, const void* bias2,
+                                       const void* out, const float* lse, const void* dout,
+                                       void* dq, void* dk, void* dv, void* dbias1, void* dbias2,
+                                       void* workspace, size_t workspace_bytes,
+                                       evo_shape_t shape, evo_dtype_t dtype,
+                                       const evo_layout_t* layout, const evo_options_t* opts,
+                                       void* stream);
+
+/*
+ * Synchronises `stream`, then reads the status word of a workspace last used
+ * by evo_attn_bwd_opts (device pointer, 256-byte aligned): EVO_OK, or
+ * EVO_ERR_DEVICE_TIMEOUT if one of that call's kernels gave up on a bounded
+ * wait (its outputs are then undefined).  EVO_ERR_CUDA if the synchronisation
+ * or the read failed.
+ */
+EVO_API evo_status_t evo_attn_bwd_status(const void* workspace, void* stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the fallback device status
  * word on the current device: EVO_OK, or EVO_ERR_DEVICE_TIMEOUT if some
- * kernel since the last call gave up on a bounded wait (its outputs are then
- * undefined).  EVO_ERR_CUDA if the synchronisation itself failed.
+ * kernel of a call given no status location of its own gave up on a bounded
+ * wait since the last read (its outputs are then undefined).  EVO_ERR_CUDA
+ * if the synchronisation itself failed.
  */
 EVO_API evo_status_t evo_attn_device_status(void* stream);
-
-/*
- * Upper bound, in nanoseconds, on every device-side wait of later launches
- * (default 2e9).  Values below 1000 are raised to 1000.  Host-side setting,
- * process-wide; meant for tests of the timeout path.
- */
-EVO_API void evo_attn_set_wait_limit_ns(uint64_t ns);
-
-/*
- * Masked key-tile skipping (host-side, process-wide, read by later calls; off by
- * default).  With enable != 0, a key j of row (b, n) counts as masked when
- * bias1[b,n,j] <= threshold (a NaN counts as kept), and later calls with a bias1 skip
- * every 128-key tile of a row whose keys are all masked, as long as the row keeps at
- * least one key (a row with no kept key skips nothing).  The forward skips them on
- * every shape with L <= 8192; the backward on the shapes whose dQ goes through the
- * fp32 accumulator (its per-key-tile schedule), writing their dK and dV as zeros.
- *
- * The results are those of the unskipped computation whenever each masked key's
- * scaled, biased score lies more than 88 below its row's largest one: its fp32
- * exponential is then exactly 0 either way (page §3.6's key mask, a very large
- * negative bias, meets this by far).  Skipped tiles still count in any nominal FLOP
- * figure derived from the shape.
- */
-EVO_API void evo_attn_set_masked_tile_skip(int enable, float threshold);
 
 /*
  * Self-test of the bounded-wait path: launches one block that waits on a
  * shared-memory barrier nothing ever signals, with the wait limit given here
  * (clamped to [1000 ns, 1e9 ns]).  The block gives up, records
- * EVO_ERR_DEVICE_TIMEOUT in the status word and exits; read it with
- * evo_attn_device_status().  Faults nothing and leaves the context usable.
+ * EVO_ERR_DEVICE_TIMEOUT in *status (a device int, 4-byte aligned; NULL = the
+ * fallback word, read with evo_attn_device_status) and exits.  Faults nothing
+ * and leaves the context usable.
  */
-EVO_API evo_status_t evo_attn_selftest_wait_timeout(uint64_t limit_ns, void* stream);
-
-/*
- * Profiling hook (process-wide, not for concurrent callers).  With
- * events != NULL and count > 0, later calls record caller-owned CUDA events
- * (cudaEvent_t, created with timing enabled) on their stream around each
- * kernel they launch:
- *   evo_attn_fwd : events[0] before its kernel, events[1] after it;
- *   evo_attn_bwd : events[2] before its first kernel, then one event after
- *                  each kernel in launch order — events[3] after delta /
- *                  accumulator set-up, events[4] after the main backward
- *                  kernel (with masked key-tile skipping on the per-key-tile
- *                  schedule, its two work-list kernels run between events[3]
- *                  and events[4]), events[5] after the dQ cast, and with a
- *                  pair bias events[6] after the per-group pair-bias partials
- *                  and events[7] after their fixed-order sum.  With dbias1,
- *                  its partial and sum kernels run between events[5] and
- *                  events[6].  A call split batch by batch (strided layouts)
- *                  records them for its last batch.
- * Indices >= count are skipped.  evo_attn_profile_events(NULL, 0) turns it off.
- * Recording works inside stream capture (the records become graph nodes).
- */
-EVO_API void evo_attn_profile_events(void* const* events, int count);
+EVO_API evo_status_t evo_attn_selftest_wait_timeout(uint64_t limit_ns, int* status, void* stream);
 
 /*
  * Bytes of device arena evo_attn_step_host needs for this problem (0 on a bad
@@ -346,13 +415,22 @@ EVO_API evo_status_t evo_attn_step_host(const void* q, const void* k, const void
  * EVO_NOALLOC_SCRATCH_BYTES are rejected with EVO_ERR_SCRATCH_LIMIT before
  * anything is launched.
  *
- * The first call on a device looks up the array's device address on that
- * device (cudaGetSymbolAddress, with the device current); make that first
- * call before any stream capture on the device.  Every call on a device
- * shares the one array, which keeps the previous call's contents (the
- * kernels clear what must start at zero themselves): calls whose work
- * overlaps on the GPU — on different streams, or from different host
- * threads — race on the scratch and give wrong results.  Serialise them.
+ * When the array is reserved: with lazy module loading (CUDA_MODULE_LOADING=
+ * LAZY, the default) at the first call on each device, which therefore can
+ * fail with EVO_ERR_CUDA if the device has no 16 MiB left (the reason is in
+ * evo_attn_last_error_detail; a later call tries again); with eager loading,
+ * on every GPU where the process creates a context.  So a caller that must
+ * not allocate after start-up makes one call per device during start-up.
+ * That first call also looks up the array's device address on that device
+ * (cudaGetSymbolAddress, with the device current); make it before any stream
+ * capture on the device.  The address is cached per device index; after a
+ * cudaDeviceReset it is stale, and this entry point must not be used on that
+ * device again in the process.  Every call on a device shares the one array,
+ * which keeps the previous call's contents (the kernels write every byte
+ * before reading it): calls whose work overlaps on the GPU — on different
+ * streams, or from different host threads — race on the scratch and give
+ * wrong results.  Serialise them.  Timeouts of its kernels are recorded in
+ * the fallback status word (evo_attn_device_status).
  */
 #define EVO_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
 

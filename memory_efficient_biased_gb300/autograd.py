@@ -55,8 +55,11 @@ class EvoformerAttentionFunction(torch.autograd.Function):
         q, k, v, bias1, bias2, out, lse = ctx.saved_tensors
         dout = _in_place_or_packed(dout)
         want_db1 = bias1 is not None and ctx.needs_input_grad[3]
-        dq, dk, dv, db1, db2 = E.evo_attn_bwd_strided(q, k, v, bias1, bias2, out, lse, dout, want_dbias1=want_db1)
-        return dq, dk, dv, db1, (db2 if ctx.needs_input_grad[4] else None)
+        want_db2 = bias2 is not None and ctx.needs_input_grad[4]
+        # the pair-bias gradient is computed only when the pair bias needs one
+        dq, dk, dv, db1, db2 = E.evo_attn_bwd_opts(q, k, v, bias1, bias2, out, lse, dout, want_dbias1=want_db1,
+                                                   want_dbias2=want_db2)
+        return dq, dk, dv, db1, db2
 
 
 def evoformer_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,

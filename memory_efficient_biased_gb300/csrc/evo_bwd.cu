@@ -12,26 +12,25 @@
 //   dV = Pᵀ dO      dK = s·dSᵀ Q      dQ = s·dS K      dbias2[b,h] = Σ_n dS
 //
 // Kernels, in launch order on the caller's stream:
-//   evo_bwd_pre       delta [B,N,H,L] fp32; zeroes the fp32 dQ accumulator.
-//   evo_bwd_main      persistent over a contiguous range of (b, h, key tile, n)
-//                     items, streamed as one sequence of (item, query tile)
-//                     steps.  The MMA thread computes S = Q Kᵀ and dP = dO Vᵀ
-//                     into TMEM (lane = query) one step ahead; eight compute
-//                     warps (each 32 query rows × 64 keys) form P and dS
-//                     (fp16 / bf16) in swizzled shared memory; the MMA thread
-//                     then accumulates dV += Pᵀ dO and dK += dSᵀ Q in TMEM (the
-//                     same smem tiles read as MN-major A operands, dK/dV double-
-//                     buffered across items) and forms dQ_tile = dS K, which
-//                     the compute warps add into the fp32 accumulator.
-//   evo_bwd_dq_cast   dQ = accumulator rounded to the dtype.
+//   evo_bwd_pre       delta [B,N,H,L] fp32 (and the transposed pair bias for the
+//                     key-major kernel).
+//   evo_bwd_main      (shapes whose dQ tiles do not fit in TMEM) persistent over
+//                     a contiguous range of whole (b, h, n) slices, streamed as
+//                     one sequence of (key tile, query tile) steps.  The MMA
+//                     thread computes S = Q Kᵀ and dP = dO Vᵀ into TMEM
+//                     (lane = query) one step ahead; eight compute warps (each
+//                     32 query rows × 64 keys) form P and dS (fp16 / bf16) in
+//                     swizzled shared memory; the MMA thread then forms
+//                     dQ_tile = dS K and accumulates dV += Pᵀ dO and dK += dSᵀ Q
+//                     in TMEM; the compute warps sum the dQ tiles of a slice in
+//                     the CTA's fp32 rows and write dQ at its last key tile.
 //   evo_bwd_db2_part  (pair bias only) per (b, h, query tile, key tile,
 //                     n-group): recompute S and dP (double-buffered in TMEM),
 //                     form P and dS, and sum dS over the group's n in a fixed
 //                     order in registers (eight warps, 32 rows × 64 keys each);
 //                     write fp32.
 //   evo_bwd_db2_sum   dbias2 = Σ_groups partial in fixed order, cast.
-// Both pair-bias stages run in a fixed order, so dbias2 is bitwise
-// reproducible.  dQ uses fp32 atomics and is not.
+// Every sum runs in a fixed order, so all gradients are bitwise reproducible.
 #include "evo_bwd_common.cuh"
 
 namespace evo {
@@ -46,6 +45,8 @@ __device__ __forceinline__ long long idiv(long long x, long long d, bool small) 
 // ============================================================ evo_bwd_pre
 template <int DP, bool BF16>
 __global__ void __launch_bounds__(256) evo_bwd_pre(const BwdArgs a) {
+  // the call's own status word starts clear; the later kernels of the call run after this one
+  if (a.clear_status && blockIdx.x == 0 && threadIdx.x == 0) *a.status = 0;
   if (a.b2t) {  // transposed pair bias for the key-major kernel, in 32 x 32 tiles through smem
     __shared__ uint16_t tile[32][34];
     const int TL = (a.L + 31) / 32, lane = threadIdx.x & 31, row0 = threadIdx.x >> 5;
@@ -68,7 +69,7 @@ __global__ void __launch_bounds__(256) evo_bwd_pre(const BwdArgs a) {
     }
   }
   const long long rows = static_cast<long long>(a.B) * a.N * a.L * a.H;
-  if (!a.zero_dq && (a.D == 8 || a.D == 16 || a.D == 32 || a.D == 64)) {
+  if (a.D == 8 || a.D == 16 || a.D == 32 || a.D == 64) {
     // Coalesced: each lane takes one 16-byte chunk (8 elements) of O and dO; the D/8
     // lanes of a row (adjacent) reduce their partial dot products with shuffles.
     const int lpr = a.D / 8;                                   // lanes per row
@@ -140,7 +141,6 @@ __global__ void __launch_bounds__(256) evo_bwd_pre(const BwdArgs a) {
     const long long bn = t / a.L;
     const uint4* o = reinterpret_cast<const uint4*>(a.out + bn * a.r_out.bn + i * a.r_out.l + h * a.D);
     const uint4* g = reinterpret_cast<const uint4*>(a.dout + bn * a.r_dout.bn + i * a.r_dout.l + h * a.D);
-    float4* acc = reinterpret_cast<float4*>(a.dq_acc + row * a.D);
     float sum = 0.0f;
 #pragma unroll
     for (int c = 0; c < DP / 8; ++c) {
@@ -152,10 +152,6 @@ __global__ void __launch_bounds__(256) evo_bwd_pre(const BwdArgs a) {
           sum = fmaf(unpack_lo<BF16>(ow[e]), unpack_lo<BF16>(gw[e]), sum);
           sum = fmaf(unpack_hi<BF16>(ow[e]), unpack_hi<BF16>(gw[e]), sum);
         }
-        if (a.zero_dq) {
-          acc[2 * c] = make_float4(0.f, 0.f, 0.f, 0.f);
-          acc[2 * c + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
       }
     }
     a.delta[(bn * a.H + h) * a.L + i] = sum;
@@ -163,33 +159,11 @@ __global__ void __launch_bounds__(256) evo_bwd_pre(const BwdArgs a) {
 
 }
 
-// ============================================================ evo_bwd_dq_cast
-template <bool BF16>
-__global__ void __launch_bounds__(256) evo_bwd_dq_cast(const BwdArgs a) {
-  const long long n8 = static_cast<long long>(a.B) * a.N * a.L * a.H * a.D / 8;
-  const long long cpt = static_cast<long long>(a.H) * a.D / 8;  // 8-element chunks per token
-  const bool small = n8 < (1ll << 31);
-  for (long long v = blockIdx.x * 256ll + threadIdx.x; v < n8; v += gridDim.x * 256ll) {
-    const float4 x = reinterpret_cast<const float4*>(a.dq_acc)[2 * v];
-    const float4 y = reinterpret_cast<const float4*>(a.dq_acc)[2 * v + 1];
-    uint4 pk;
-    pk.x = pack2<BF16>(x.x, x.y);
-    pk.y = pack2<BF16>(x.z, x.w);
-    pk.z = pack2<BF16>(y.x, y.y);
-    pk.w = pack2<BF16>(y.z, y.w);
-    if (a.packed) {
-      reinterpret_cast<uint4*>(a.dq)[v] = pk;
-    } else {
-      const long long t = idiv(v, cpt, small), bn = idiv(t, a.L, small);
-      *reinterpret_cast<uint4*>(a.dq + bn * a.r_dq.bn + (t - bn * a.L) * a.r_dq.l + (v - t * cpt) * 8) = pk;
-    }
-  }
-}
-
 // ============================================================ masked key tiles
 // Masked key-tile skipping for the per-key-tile kernel.  evo_bwd_tile_mask: the key
 // tiles of each (b, n) row to skip (one warp per row), and zeros for dK and dV of those
-// tiles in every head, since the per-key-tile kernel will not run them.
+// tiles in every head, since the per-key-tile kernel will not run them.  The kernel reads
+// the skip bits of each slice it walks.
 template <bool BF16>
 __global__ void __launch_bounds__(256) evo_bwd_tile_mask(const BwdArgs a) {
   const int lane = threadIdx.x & 31;
@@ -211,98 +185,6 @@ __global__ void __launch_bounds__(256) evo_bwd_tile_mask(const BwdArgs a) {
             make_uint4(0u, 0u, 0u, 0u);
       }
     }
-  }
-}
-
-// evo_bwd_worklist (one block): the items (b, h, key tile, n) of the per-key-tile kernel
-// whose key tile row (b, n) keeps, in item order.  The kept n depend on (b, key tile)
-// only, so each (b, key tile) pair lists them once (one warp per pair), and every head
-// copies that list into its place.
-__global__ void __launch_bounds__(1024) evo_bwd_worklist(const BwdArgs a) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, KT = a.QT;
-  const int pairs = a.B * KT;
-  uint32_t* cnt = a.wl_cnt;               // [B*KT] kept n of each (b, key tile)
-  uint32_t* pre = a.wl_cnt + pairs;       // [B*KT] their offsets within one head of b
-  uint32_t* per_head = pre + pairs;       // [B] items of one head of b
-  uint32_t* start = per_head + a.B;       // [B] where b's items start
-  for (int p = warp; p < pairs; p += 32) {
-    const int b = p / KT, jt = p % KT;
-    uint32_t c = 0;
-    for (int n0 = 0; n0 < a.N; n0 += 32) {
-      const int n = n0 + lane;
-      const bool keep = n < a.N && !((a.tskip[static_cast<long long>(b) * a.N + n] >> jt) & 1ull);
-      const uint32_t bal = __ballot_sync(0xffffffffu, keep);
-      if (keep) a.wl_n[static_cast<long long>(p) * a.N + c + __popc(bal & ((1u << lane) - 1u))] = n;
-      c += __popc(bal);
-    }
-    if (lane == 0) cnt[p] = c;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    uint32_t at = 0;
-    for (int b = 0; b < a.B; ++b) {
-      uint32_t sum = 0;
-      for (int jt = 0; jt < KT; ++jt) {
-        pre[b * KT + jt] = sum;
-        sum += cnt[b * KT + jt];
-      }
-      per_head[b] = sum;
-      start[b] = at;
-      at += sum * a.H;
-    }
-    *a.wl_total = at;
-  }
-  __syncthreads();
-  const long long groups = static_cast<long long>(a.B) * a.H * KT;  // (b, h, key tile), in item order
-  for (long long grp = warp; grp < groups; grp += 32) {
-    const int jt = static_cast<int>(grp % KT);
-    const long long bh = grp / KT;
-    const int h = static_cast<int>(bh % a.H), b = static_cast<int>(bh / a.H), p = b * KT + jt;
-    const uint32_t at = start[b] + h * per_head[b] + pre[p];
-    for (uint32_t r = lane; r < cnt[p]; r += 32)
-      a.wl[at + r] = static_cast<uint32_t>(grp * a.N + a.wl_n[static_cast<long long>(p) * a.N + r]);
-  }
-}
-
-// evo_bwd_worklist_jt (one block): the same list for the key-tile-fastest item order
-// (b, h, n, key tile): the kept key tiles of each row (b, n) in order, the row's count
-// and offset within its b shared by every head.
-__global__ void __launch_bounds__(1024) evo_bwd_worklist_jt(const BwdArgs a) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, KT = a.QT;
-  const long long rows = static_cast<long long>(a.B) * a.N;
-  const unsigned long long all = KT >= 64 ? ~0ull : ((1ull << KT) - 1);
-  uint32_t* pre = a.wl_n;          // [B*N] kept tiles of each row, then their offsets within b
-  uint32_t* per_head = a.wl_cnt;   // [B] items of one head of b
-  uint32_t* start = a.wl_cnt + a.B;  // [B] where b's items start
-  for (long long bn = threadIdx.x; bn < rows; bn += 1024) pre[bn] = __popcll(~a.tskip[bn] & all);
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    uint32_t at = 0;
-    for (int b = 0; b < a.B; ++b) {
-      uint32_t sum = 0;
-      for (int n = 0; n < a.N; ++n) {
-        const uint32_t c = pre[static_cast<long long>(b) * a.N + n];
-        pre[static_cast<long long>(b) * a.N + n] = sum;
-        sum += c;
-      }
-      per_head[b] = sum;
-      start[b] = at;
-      at += sum * a.H;
-    }
-    *a.wl_total = at;
-  }
-  __syncthreads();
-  const long long groups = static_cast<long long>(a.B) * a.H * a.N;  // (b, h, n), in item order
-  for (long long grp = warp; grp < groups; grp += 32) {
-    const int n = static_cast<int>(grp % a.N);
-    const long long bh = grp / a.N;
-    const int h = static_cast<int>(bh % a.H), b = static_cast<int>(bh / a.H);
-    const long long bn = static_cast<long long>(b) * a.N + n;
-    const unsigned long long kept = ~a.tskip[bn] & all;
-    const uint32_t at = start[b] + h * per_head[b] + pre[bn];
-    for (int jt = lane; jt < KT; jt += 32)
-      if ((kept >> jt) & 1ull)
-        a.wl[at + __popcll(kept & ((1ull << jt) - 1ull))] = static_cast<uint32_t>(grp * KT + jt);
   }
 }
 
@@ -372,8 +254,22 @@ __global__ void __launch_bounds__(256) evo_bwd_db2_sum(const BwdArgs a) {
 
 
 // ============================================================ evo_bwd_main
-enum B2Kind : int { kB2None = 0, kB2Resident = 1, kB2Stream = 2 };
-
+// Per-key-tile schedule, for the shapes whose dQ tiles do not all fit in TMEM.  A CTA
+// owns a contiguous range of whole (b, h, n) slices.  For each slice it walks the key
+// tiles jt in order (with masked-tile skipping, the kept ones) and for each key tile the
+// L/128 query tiles it, one step per (jt, it):
+//   S = Q Kᵀ, dP = dO Vᵀ into TMEM (lane = query), one step ahead of the compute warps;
+//   P and dS in the dtype into swizzled shared-memory tiles (two buffers where they fit,
+//   so the compute warps form step u+1 while the gradient MMAs of step u run);
+//   dQ_tile = dS K (issued first, so its consumer starts early), dV += Pᵀ dO and
+//   dK += dSᵀ Q (the same tiles as MN-major A operands; dK, dV double-buffered across
+//   key tiles where TMEM allows).
+// dQ of a slice accumulates in the CTA's own fp32 rows of the workspace: the first key
+// tile of the slice stores its tile, later ones add to it, and the last one adds, scales
+// and writes dQ in the dtype.  Each compute thread owns the same (query row, column
+// half) at every step, so its own program order orders these plain loads and stores;
+// the sum runs over the key tiles in a fixed order, so dQ is bitwise reproducible, and
+// the fp32 rows of one CTA (L × DP floats) stay in L2.
 __device__ __forceinline__ uint32_t col_s() { return 0u; }
 __device__ __forceinline__ uint32_t col_dp() { return 128u; }
 template <int DP>
@@ -390,9 +286,8 @@ constexpr int kMaxQStages = 4;
 struct MainBars {
   uint64_t kv_full[2], kv_empty[2];
   uint64_t q_full[kMaxQStages], q_empty[kMaxQStages];
-  uint64_t b2_full, b2_empty;
   uint64_t st_full, st_free;
-  uint64_t ds_full, ds_empty;
+  uint64_t ds_full[2], ds_empty[2];
   uint64_t dq_full[2], dq_free[2];
   uint64_t dkdv_full[2], dkdv_free[2];
   uint64_t drain;
@@ -400,13 +295,20 @@ struct MainBars {
   int abort;
 };
 
+// Shared memory: the P and dS tiles (pds buffers each, 128B-swizzled, so first), K/V
+// (two buffers), the Q/dO ring (qs stages), streamed pair-bias tiles (one per Q/dO
+// stage), key-mask chunks, lse/delta per stage, barriers.
 template <int DP>
 struct MainLayout {
   static constexpr uint32_t kTB = kTile * DP * 2;
-  Ring k, v, b1, q, d_o, ld, b2s;
-  uint32_t b2r, p, ds, bars, total;
-  __host__ __device__ MainLayout(int b2kind, int qs, int QT) {
+  Ring p, ds, k, v, q, d_o, b2s, b1, ld;
+  uint32_t bars, total;
+  __host__ __device__ MainLayout(bool has_b2, int qs, int pds) {
     uint32_t off = 0;
+    p = Ring{off, 32768u};
+    off += pds * 32768u;
+    ds = Ring{off, 32768u};
+    off += pds * 32768u;
     k = Ring{off, 2 * kTB};
     v = Ring{off + kTB, 2 * kTB};
     off += 4 * kTB;
@@ -414,13 +316,7 @@ struct MainLayout {
     d_o = Ring{off + kTB, 2 * kTB};
     off += qs * 2 * kTB;
     b2s = Ring{off, 32768u};
-    if (b2kind == kB2Stream) off += qs * 32768u;
-    b2r = off;
-    if (b2kind == kB2Resident) off += QT * 32768u;
-    p = off;
-    off += 32768u;
-    ds = off;
-    off += 32768u;
+    if (has_b2) off += qs * 32768u;
     b1 = Ring{off, 512u};
     off += 1024u;
     ld = Ring{off, 1024u};
@@ -431,74 +327,96 @@ struct MainLayout {
   }
 };
 
-template <int DP, bool BF16, int B2>
+// The walk of one CTA over its steps: slices s0 <= s < s1 (order b, h, n), the kept key
+// tiles of each (all, or those not in the row's skip bits), the QT query tiles of each.
+struct MainWalk {
+  int b, h, n, jt;
+  long long s;
+  uint64_t skip;  // key tiles of the current slice to skip
+  __device__ __forceinline__ bool kept(int t) const { return t >= 64 || !((skip >> t) & 1ull); }
+  __device__ __forceinline__ int next_kept(int t, int QT) const {
+    do ++t;
+    while (t < QT && !kept(t));
+    return t;
+  }
+  __device__ __forceinline__ void enter(const BwdArgs& a) {
+    skip = 0;
+    if (a.tile_skip && s < a.items) {
+      const uint64_t all = a.QT >= 64 ? ~0ull : ((1ull << a.QT) - 1ull);
+      skip = a.tskip[static_cast<long long>(b) * a.N + n] & all;
+      if (skip == all) skip = 0;  // a row with no kept key skips nothing
+    }
+    jt = next_kept(-1, a.QT);
+  }
+  __device__ __forceinline__ void init(long long s0, const BwdArgs& a) {
+    s = s0;
+    n = static_cast<int>(s0 % a.N);
+    const long long t = s0 / a.N;
+    h = static_cast<int>(t % a.H);
+    b = static_cast<int>(t / a.H);
+    enter(a);
+  }
+  // to the next kept key tile of the slice, or the first of the next slice
+  __device__ __forceinline__ void next_item(const BwdArgs& a) {
+    jt = next_kept(jt, a.QT);
+    if (jt < a.QT) return;
+    ++s;
+    if (++n == a.N) {
+      n = 0;
+      if (++h == a.H) {
+        h = 0;
+        ++b;
+      }
+    }
+    enter(a);
+  }
+  __device__ __forceinline__ bool first_tile(const BwdArgs& a) const { return next_kept(-1, a.QT) == jt; }
+  __device__ __forceinline__ bool last_tile(const BwdArgs& a) const { return next_kept(jt, a.QT) >= a.QT; }
+};
+
+template <int DP, bool BF16, bool HAS_B2>
 __device__ __forceinline__ void main_producer(const BwdArgs& a, uint8_t* base, const MainLayout<DP>& lay,
-                                              MainBars* bars, const WaitGuard& g, int lane, long long i0,
-                                              long long i1) {
+                                              MainBars* bars, const WaitGuard& g, int lane, long long s0,
+                                              long long s1) {
   constexpr uint32_t kTB = MainLayout<DP>::kTB;
   const int QS = a.q_stages, QT = a.QT;
   const bool tma_b2 = a.bias2_mode == kBias2Tma;
-  const uint32_t q_bytes = 2 * kTB + ((B2 == kB2Stream && tma_b2) ? 32768u : 0u);
-  uint32_t it_ctr = 0, item_ctr = 0, grp_it = 0, s = 0, ph = 0;
-  KvIter c, p;
-  c.init(item_at(a, i0), a);
-  p = c;
+  const uint32_t q_bytes = 2 * kTB + ((HAS_B2 && tma_b2) ? 32768u : 0u);
+  uint32_t it_ctr = 0, item_ctr = 0, s = 0, ph = 0;
+  MainWalk w;
+  w.init(s0, a);
   bool ok = true;
-  for (long long item = i0; ok && item < i1; ++item, ++item_ctr) {
-    if (item > i0) {
-      p = c;
-      advance(c, a, item);
-    }
-    const int bn = c.b * a.N + c.n, bh = c.b * a.H + c.h;
-    const size_t bnh = static_cast<size_t>(bn) * a.H + c.h;
-    if (B2 == kB2Resident && (item == i0 || !c.same_group(p))) {
-      if (!mbar_wait(smem_u32(&bars->b2_empty), (grp_it & 1) ^ 1, g)) { ok = false; break; }
-      const uint32_t full = smem_u32(&bars->b2_full);
-      if (tma_b2) {
-        if (lane == 0) {
-          mbar_expect_tx(full, QT * 32768u);
-          for (int t = 0; t < QT; ++t) {
-            tma_load_3d(smem_u32(base + lay.b2r + t * 32768u), &a.tb2, full, c.jt * kTile, t * kTile, bh);
-            tma_load_3d(smem_u32(base + lay.b2r + t * 32768u + 16384u), &a.tb2, full, c.jt * kTile + 64,
-                        t * kTile, bh);
-          }
-        }
-      } else {
-        for (int t = 0; t < QT; ++t)
-          fill_b2_tile_loads(base + lay.b2r + t * 32768u, a.bias2 + static_cast<size_t>(bh) * a.L * a.L, a.L,
-                             t * kTile, c.jt * kTile, lane);
-      }
-      mbar_arrive(full);
-      ++grp_it;
-    }
+  for (; ok && w.s < s1; ++item_ctr, w.next_item(a)) {
+    const int bn = w.b * a.N + w.n, bh = w.b * a.H + w.h;
+    const size_t bnh = static_cast<size_t>(bn) * a.H + w.h;
     const uint32_t kb = item_ctr & 1;
-    if (!mbar_wait(smem_u32(&bars->kv_empty[kb]), ((item_ctr >> 1) & 1) ^ 1, g)) { ok = false; break; }
+    if (!mbar_wait_warp(smem_u32(&bars->kv_empty[kb]), ((item_ctr >> 1) & 1) ^ 1, g)) { ok = false; break; }
     {
       const uint32_t full = smem_u32(&bars->kv_full[kb]);
       if (lane == 0) {
         mbar_expect_tx(full, 2 * kTB);
-        tma_load_4d(smem_u32(base + lay.k[kb]), &a.tk, full, 0, c.h, c.jt * kTile, bn);
-        tma_load_4d(smem_u32(base + lay.v[kb]), &a.tv, full, 0, c.h, c.jt * kTile, bn);
+        tma_load_4d(smem_u32(base + lay.k[kb]), &a.tk, full, 0, w.h, w.jt * kTile, bn);
+        tma_load_4d(smem_u32(base + lay.v[kb]), &a.tv, full, 0, w.h, w.jt * kTile, bn);
       }
       fill_b1_chunk<BF16>(reinterpret_cast<float*>(base + lay.b1[kb]),
-                          a.bias1 ? a.bias1 + static_cast<size_t>(bn) * a.L : nullptr, a.L, c.jt * kTile, lane);
+                          a.bias1 ? a.bias1 + static_cast<size_t>(bn) * a.L : nullptr, a.L, w.jt * kTile, lane);
       mbar_arrive(full);
     }
     for (int it = 0; it < QT; ++it, ++it_ctr) {
-      if (!mbar_wait(smem_u32(&bars->q_empty[s]), ph ^ 1, g)) { ok = false; break; }
+      if (!mbar_wait_warp(smem_u32(&bars->q_empty[s]), ph ^ 1, g)) { ok = false; break; }
       const uint32_t full = smem_u32(&bars->q_full[s]);
       if (lane == 0) {
         mbar_expect_tx(full, q_bytes);
-        tma_load_4d(smem_u32(base + lay.q[s]), &a.tq, full, 0, c.h, it * kTile, bn);
-        tma_load_4d(smem_u32(base + lay.d_o[s]), &a.tdo, full, 0, c.h, it * kTile, bn);
-        if (B2 == kB2Stream && tma_b2) {
-          tma_load_3d(smem_u32(base + lay.b2s[s]), &a.tb2, full, c.jt * kTile, it * kTile, bh);
-          tma_load_3d(smem_u32(base + lay.b2s[s] + 16384), &a.tb2, full, c.jt * kTile + 64, it * kTile, bh);
+        tma_load_4d(smem_u32(base + lay.q[s]), &a.tq, full, 0, w.h, it * kTile, bn);
+        tma_load_4d(smem_u32(base + lay.d_o[s]), &a.tdo, full, 0, w.h, it * kTile, bn);
+        if (HAS_B2 && tma_b2) {
+          tma_load_3d(smem_u32(base + lay.b2s[s]), &a.tb2, full, w.jt * kTile, it * kTile, bh);
+          tma_load_3d(smem_u32(base + lay.b2s[s] + 16384), &a.tb2, full, w.jt * kTile + 64, it * kTile, bh);
         }
       }
-      if (B2 == kB2Stream && !tma_b2)
+      if (HAS_B2 && !tma_b2)
         fill_b2_tile_loads(base + lay.b2s[s], a.bias2 + static_cast<size_t>(bh) * a.L * a.L, a.L, it * kTile,
-                           c.jt * kTile, lane);
+                           w.jt * kTile, lane);
       fill_lse_delta(reinterpret_cast<float*>(base + lay.ld[s]), a.lse, a.delta, bnh, a.L, it * kTile, lane);
       mbar_arrive(full);
       if (++s == static_cast<uint32_t>(QS)) {
@@ -507,6 +425,7 @@ __device__ __forceinline__ void main_producer(const BwdArgs& a, uint8_t* base, c
       }
     }
   }
+  // Drain: every copy this warp started has landed before the CTA may exit.
   for (uint32_t b = 0; b < 2; ++b) {
     const uint32_t issued = (item_ctr + 1 - b) / 2;
     if (issued > 0) drain_wait(smem_u32(&bars->kv_full[b]), (issued - 1) & 1, a.wait_ns, a.status);
@@ -515,10 +434,9 @@ __device__ __forceinline__ void main_producer(const BwdArgs& a, uint8_t* base, c
     const uint32_t issued = (it_ctr + QS - 1 - st) / QS;
     if (issued > 0) drain_wait(smem_u32(&bars->q_full[st]), (issued - 1) & 1, a.wait_ns, a.status);
   }
-  if (B2 == kB2Resident && grp_it > 0) drain_wait(smem_u32(&bars->b2_full), (grp_it - 1) & 1, a.wait_ns, a.status);
 }
 
-// Step bookkeeping shared by the MMA thread: step u = (item index, query tile).
+// Step bookkeeping of the MMA thread: step u = (item index, query tile).
 struct Step {
   uint32_t u, item_ctr;
   int it;
@@ -551,8 +469,9 @@ __device__ __forceinline__ bool main_issue_sdp(const Step& st, uint8_t* base, co
 }
 
 template <int DP, bool BF16>
-__device__ __forceinline__ bool main_issue_grads(const Step& st, int QT, uint8_t* base, const MainLayout<DP>& lay,
-                                                 MainBars* bars, uint32_t tmem, const WaitGuard& g) {
+__device__ __forceinline__ bool main_issue_grads(const Step& st, int QT, int pds, uint8_t* base,
+                                                 const MainLayout<DP>& lay, MainBars* bars, uint32_t tmem,
+                                                 const WaitGuard& g) {
   constexpr uint32_t RB = DP * 2;
   constexpr uint32_t SWZ = swizzle_for_row(RB);
   constexpr uint32_t id_kv = idesc_f16(128, DP, BF16, true, true);  // dV, dK: MN-major A and B
@@ -561,13 +480,22 @@ __device__ __forceinline__ bool main_issue_grads(const Step& st, int QT, uint8_t
   const uint32_t kb = st.item_ctr & 1;
   const uint32_t db = st.item_ctr % NB, dph = (st.item_ctr / NB) & 1;
   const uint32_t qb = st.u & 1;
-  if (!mbar_wait(smem_u32(&bars->ds_full), st.u & 1, g)) return false;
-  if (st.it == 0 && !mbar_wait(smem_u32(&bars->dkdv_free[db]), dph ^ 1, g)) return false;
+  const uint32_t pb = st.u % pds, pph = (st.u / pds) & 1;
+  if (!mbar_wait(smem_u32(&bars->ds_full[pb]), pph, g)) return false;
   if (!mbar_wait(smem_u32(&bars->dq_free[qb]), ((st.u >> 1) & 1) ^ 1, g)) return false;
   tc_fence_after();
-  const uint32_t p_addr = smem_u32(base + lay.p), ds_addr = smem_u32(base + lay.ds);
+  const uint32_t p_addr = smem_u32(base + lay.p[pb]), ds_addr = smem_u32(base + lay.ds[pb]);
   const uint32_t q_addr = smem_u32(base + lay.q[st.qs]), do_addr = smem_u32(base + lay.d_o[st.qs]);
   const uint32_t k_addr = smem_u32(base + lay.k[kb]);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {  // dQ_tile = dS K   (K = 128 keys)
+    const uint64_t ad = smem_desc(ds_addr + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024, kSwizzle128B);
+    const uint64_t bd = smem_desc(k_addr + k * 16 * RB, kTile * RB, 8 * RB, SWZ);
+    umma_ss(tmem + col_dq<DP>(qb), ad, bd, id_q, k > 0);
+  }
+  umma_commit(smem_u32(&bars->dq_full[qb]));
+  if (st.it == 0 && !mbar_wait(smem_u32(&bars->dkdv_free[db]), dph ^ 1, g)) return false;
+  tc_fence_after();
 #pragma unroll
   for (int k = 0; k < 8; ++k) {  // dV += Pᵀ dO   (K = 128 queries)
     const uint64_t ad = smem_desc(p_addr + k * 16 * 128, 16384, 1024, kSwizzle128B);
@@ -580,15 +508,8 @@ __device__ __forceinline__ bool main_issue_grads(const Step& st, int QT, uint8_t
     const uint64_t bd = smem_desc(q_addr + k * 16 * RB, kTile * RB, 8 * RB, SWZ);
     umma_ss(tmem + col_dk<DP>(db), ad, bd, id_kv, (st.it > 0 || k > 0) ? 1u : 0u);
   }
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {  // dQ_tile = dS K   (K = 128 keys)
-    const uint64_t ad = smem_desc(ds_addr + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024, kSwizzle128B);
-    const uint64_t bd = smem_desc(k_addr + k * 16 * RB, kTile * RB, 8 * RB, SWZ);
-    umma_ss(tmem + col_dq<DP>(qb), ad, bd, id_q, k > 0);
-  }
-  umma_commit(smem_u32(&bars->ds_empty));
+  umma_commit(smem_u32(&bars->ds_empty[pb]));
   umma_commit(smem_u32(&bars->q_empty[st.qs]));
-  umma_commit(smem_u32(&bars->dq_full[qb]));
   if (st.it == QT - 1) {
     umma_commit(smem_u32(&bars->dkdv_full[db]));
     umma_commit(smem_u32(&bars->kv_empty[kb]));
@@ -598,9 +519,8 @@ __device__ __forceinline__ bool main_issue_grads(const Step& st, int QT, uint8_t
 
 template <int DP, bool BF16>
 __device__ __forceinline__ void main_mma(const BwdArgs& a, uint8_t* base, const MainLayout<DP>& lay, MainBars* bars,
-                                         uint32_t tmem, const WaitGuard& g, long long i0, long long i1) {
-  const int QS = a.q_stages, QT = a.QT;
-  const uint32_t total = static_cast<uint32_t>((i1 - i0) * QT);
+                                         uint32_t tmem, const WaitGuard& g, long long s0, long long s1) {
+  const int QS = a.q_stages, QT = a.QT, pds = a.pds_bufs;
   auto step_of = [&](Step& st) {  // advance to the next step
     ++st.u;
     if (++st.it == QT) {
@@ -612,39 +532,59 @@ __device__ __forceinline__ void main_mma(const BwdArgs& a, uint8_t* base, const 
       st.qph ^= 1;
     }
   };
-  bool ok = total > 0;
+  // the walk only decides how many items (kept key tiles) each slice has
+  MainWalk w;
+  w.init(s0, a);
   Step cur{0, 0, 0, 0, 0};
+  bool ok = w.s < s1;
+  auto advance_walk = [&](MainWalk& x, const Step& st) {  // the walk after step st
+    if (st.it == QT - 1) x.next_item(a);
+  };
   if (QS >= 2) {
     // S/dP of step u+1 go ahead of step u's gradient MMAs, so the compute warps
     // can start on u+1 while the tensor core finishes u.  (Needs a second
     // Q/dO stage: step u's stage is released by its gradient MMAs.)
     if (ok) ok = main_issue_sdp<DP, BF16>(cur, base, lay, bars, tmem, g);
-    for (uint32_t u = 0; ok && u < total; ++u) {
+    while (ok) {
       Step nxt = cur;
+      MainWalk wn = w;
+      advance_walk(wn, cur);
       step_of(nxt);
-      if (u + 1 < total && !main_issue_sdp<DP, BF16>(nxt, base, lay, bars, tmem, g)) { ok = false; break; }
-      if (!main_issue_grads<DP, BF16>(cur, QT, base, lay, bars, tmem, g)) { ok = false; break; }
+      const bool more = wn.s < s1;
+      if (more && !main_issue_sdp<DP, BF16>(nxt, base, lay, bars, tmem, g)) { ok = false; break; }
+      if (!main_issue_grads<DP, BF16>(cur, QT, pds, base, lay, bars, tmem, g)) { ok = false; break; }
+      if (!more) break;
       cur = nxt;
+      w = wn;
     }
   } else {
-    for (uint32_t u = 0; ok && u < total; ++u) {
+    while (ok) {
       if (!main_issue_sdp<DP, BF16>(cur, base, lay, bars, tmem, g)) { ok = false; break; }
-      if (!main_issue_grads<DP, BF16>(cur, QT, base, lay, bars, tmem, g)) { ok = false; break; }
+      if (!main_issue_grads<DP, BF16>(cur, QT, pds, base, lay, bars, tmem, g)) { ok = false; break; }
+      advance_walk(w, cur);
       step_of(cur);
+      if (w.s >= s1) break;
     }
   }
   umma_commit(smem_u32(&bars->drain));
   drain_wait(smem_u32(&bars->drain), 0, a.wait_ns, a.status);
 }
 
-// dQ tile (TMEM lanes = queries of tile it): this warp's DP/2 columns, × s, into the fp32 accumulator.
-template <int DP>
-__device__ __forceinline__ bool main_consume_dq(const BwdArgs& a, const KvIter& c, int it, uint32_t u,
-                                                MainBars* bars, uint32_t trow, int r, int hc, int lane,
-                                                const WaitGuard& g) {
+// What the compute warps remember of a step until they consume its dQ tile.
+struct DqStep {
+  int b, n, h, it;
+  bool first, last;  // first / last (kept) key tile of its slice
+};
+
+// dQ tile of a step (TMEM lanes = queries of tile it): this warp's DP/2 columns, into
+// the CTA's fp32 rows (first key tile: store; later: add), and at the slice's last key
+// tile × s into dQ in the dtype.
+template <int DP, bool BF16>
+__device__ __forceinline__ bool main_consume_dq(const BwdArgs& a, const DqStep& d, uint32_t u, MainBars* bars,
+                                                uint32_t trow, int r, int hc, int lane, const WaitGuard& g) {
   constexpr int HD = DP / 2;
   const uint32_t qb = u & 1;
-  if (!mbar_wait(smem_u32(&bars->dq_full[qb]), (u >> 1) & 1, g)) return false;
+  if (!mbar_wait_warp(smem_u32(&bars->dq_full[qb]), (u >> 1) & 1, g)) return false;
   tc_fence_after();
   float v[HD];
   const uint32_t col = trow + col_dq<DP>(qb) + hc * HD;
@@ -668,27 +608,53 @@ __device__ __forceinline__ bool main_consume_dq(const BwdArgs& a, const KvIter& 
   tc_fence_before();
   __syncwarp();
   if (lane == 0) mbar_arrive(smem_u32(&bars->dq_free[qb]));
-  const int i = it * kTile + r;
-  if (i < a.L) {
-    float* dst = a.dq_acc + ((static_cast<size_t>(c.b) * a.N + c.n) * a.L + i) * a.H * a.D +
-                 static_cast<size_t>(c.h) * a.D + hc * HD;
+  const int i = d.it * kTile + r;
+  if (i >= a.L) return true;
+  float4* acc = reinterpret_cast<float4*>(a.dq_scr + (static_cast<size_t>(blockIdx.x) * a.L + i) * DP + hc * HD);
+  if (!d.first) {
 #pragma unroll
-    for (int e = 0; e < HD; e += 4)
-      if (hc * HD + e < a.D)
-        red_add_v4(dst + e, v[e] * a.scale, v[e + 1] * a.scale, v[e + 2] * a.scale, v[e + 3] * a.scale);
+    for (int e = 0; e < HD; e += 4) {
+      const float4 o = acc[e >> 2];
+      v[e] += o.x;
+      v[e + 1] += o.y;
+      v[e + 2] += o.z;
+      v[e + 3] += o.w;
+    }
   }
+  if (!d.last) {
+#pragma unroll
+    for (int e = 0; e < HD; e += 4) acc[e >> 2] = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+    return true;
+  }
+  const long long bn = static_cast<long long>(d.b) * a.N + d.n;
+  uint16_t* dq = a.dq + bn * a.r_dq.bn + static_cast<long long>(i) * a.r_dq.l + d.h * a.D + hc * HD;
+#pragma unroll
+  for (int e = 0; e < HD; e += 8)
+    if (hc * HD + e < a.D) {
+      uint4 pk;
+      pk.x = pack2<BF16>(v[e + 0] * a.scale, v[e + 1] * a.scale);
+      pk.y = pack2<BF16>(v[e + 2] * a.scale, v[e + 3] * a.scale);
+      pk.z = pack2<BF16>(v[e + 4] * a.scale, v[e + 5] * a.scale);
+      pk.w = pack2<BF16>(v[e + 6] * a.scale, v[e + 7] * a.scale);
+      *reinterpret_cast<uint4*>(dq + e) = pk;
+    }
   return true;
 }
 
+// What the compute warps remember of an item until they write its dK and dV.
+struct KvItem {
+  int b, n, h, jt;
+};
+
 // dK, dV of a finished item (TMEM lanes = keys of its key tile): this warp's DP/2 columns.
 template <int DP, bool BF16>
-__device__ __forceinline__ bool main_write_dkdv(const BwdArgs& a, const KvIter& c, uint32_t item_ctr,
+__device__ __forceinline__ bool main_write_dkdv(const BwdArgs& a, const KvItem& c, uint32_t item_ctr,
                                                 MainBars* bars, uint32_t trow, int r, int hc, int lane,
                                                 const WaitGuard& g) {
   constexpr int HD = DP / 2;
   constexpr int NB = kv_acc_buffers<DP>();
   const uint32_t db = item_ctr % NB;
-  if (!mbar_wait(smem_u32(&bars->dkdv_full[db]), (item_ctr / NB) & 1, g)) return false;
+  if (!mbar_wait_warp(smem_u32(&bars->dkdv_full[db]), (item_ctr / NB) & 1, g)) return false;
   tc_fence_after();
   float kx[HD], vx[HD];
   const uint32_t ck = trow + col_dk<DP>(db) + hc * HD, cv = trow + col_dv<DP>(db) + hc * HD;
@@ -750,21 +716,22 @@ __device__ __forceinline__ bool main_write_dkdv(const BwdArgs& a, const KvIter& 
   return true;
 }
 
-// P and dS for one 32-key chunk of this warp (S, dP already loaded from TMEM),
-// written to the [query][key] P and dS tiles (K-major, 128B swizzle).
+// P and dS for one 16-key chunk k (0..3) of this warp's 64 keys (S, dP already loaded
+// from TMEM), written to the [query][key] P and dS tiles (K-major, 128B swizzle).
 template <bool BF16, bool HAS_B2>
-__device__ __forceinline__ void main_chunk(const uint32_t (&sv)[32], const uint32_t (&pv)[32], const float* b1c,
-                                           const uint8_t* b2half, uint8_t* pt, uint8_t* dt, int r, int c4,
-                                           float lse2, float dlt, float2 sl2) {
+__device__ __forceinline__ void main_chunk16(const uint32_t (&sv)[16], const uint32_t (&pv)[16], const float* b1c,
+                                             const uint8_t* b2half, uint8_t* pt, uint8_t* dt, int r, int k,
+                                             float lse2, float dlt, float2 sl2) {
   const float2 nl2 = make_float2(-lse2, -lse2), l2e2 = make_float2(kLog2e, kLog2e), nd2 = make_float2(-dlt, -dlt);
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {  // 8 keys (one 16-byte chunk of the tiles) per q
-    const float4 m0 = *reinterpret_cast<const float4*>(b1c + q * 8);
-    const float4 m1 = *reinterpret_cast<const float4*>(b1c + q * 8 + 4);
+  for (int q = 0; q < 2; ++q) {  // 8 keys (one 16-byte chunk of the tiles) per q
+    const float4 m0 = *reinterpret_cast<const float4*>(b1c + k * 16 + q * 8);
+    const float4 m1 = *reinterpret_cast<const float4*>(b1c + k * 16 + q * 8 + 4);
     const float2 mk[4] = {make_float2(m0.x, m0.y), make_float2(m0.z, m0.w), make_float2(m1.x, m1.y),
                           make_float2(m1.z, m1.w)};
+    const uint32_t off = swz_offset(r, k * 2 + q, 128);
     uint4 pb = make_uint4(0u, 0u, 0u, 0u);
-    if (HAS_B2) pb = *reinterpret_cast<const uint4*>(b2half + swz_offset(r, c4 * 4 + q, 128));
+    if (HAS_B2) pb = *reinterpret_cast<const uint4*>(b2half + off);
     const uint32_t pw[4] = {pb.x, pb.y, pb.z, pb.w};
     uint32_t pp[4], dd[4];
 #pragma unroll
@@ -779,129 +746,124 @@ __device__ __forceinline__ void main_chunk(const uint32_t (&sv)[32], const uint3
       pp[e2] = pack2<BF16>(p0, p1);
       dd[e2] = pack2<BF16>(ds.x, ds.y);
     }
-    const uint32_t off = swz_offset(r, c4 * 4 + q, 128);
     *reinterpret_cast<uint4*>(pt + off) = make_uint4(pp[0], pp[1], pp[2], pp[3]);
     *reinterpret_cast<uint4*>(dt + off) = make_uint4(dd[0], dd[1], dd[2], dd[3]);
   }
 }
 
-template <int DP, bool BF16, int B2>
+template <int DP, bool BF16, bool HAS_B2>
 __device__ __forceinline__ void main_compute(const BwdArgs& a, uint8_t* base, const MainLayout<DP>& lay,
-                                             MainBars* bars, uint32_t tmem, const WaitGuard& g, long long i0,
-                                             long long i1) {
-  constexpr bool kHasB2 = B2 != kB2None;
+                                             MainBars* bars, uint32_t tmem, const WaitGuard& g, long long s0,
+                                             long long s1) {
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quad = w & 3, hc = w >> 2;
   const int r = quad * 32 + lane;  // query row (S, dP, dQ) or key row (dK, dV) within the tile == TMEM lane
   const uint32_t trow = tmem + (static_cast<uint32_t>(quad * 32) << 16);
   const float2 sl2 = make_float2(a.scale_log2, a.scale_log2);
   const int QS = a.q_stages, QT = a.QT;
-  uint32_t u = 0, item_ctr = 0, grp_it = 0, s = 0, ph = 0;
-  KvIter cur, prev;
-  cur.init(item_at(a, i0), a);
-  prev = cur;
-  int prev_it = 0;
+  const uint32_t pds = static_cast<uint32_t>(a.pds_bufs);
+  uint32_t u = 0, item_ctr = 0, s = 0, ph = 0;
+  MainWalk cur;
+  cur.init(s0, a);
+  DqStep pd{0, 0, 0, 0, false, false};
+  KvItem pk{0, 0, 0, 0};
   bool ok = true;
-  for (long long item = i0; ok && item < i1; ++item, ++item_ctr) {
-    if (item > i0) {
-      prev = cur;
-      advance(cur, a, item);
-    }
-    bool grp_last = item + 1 == i1;
-    if (B2 == kB2Resident && !grp_last) {
-      KvIter nx = cur;
-      advance(nx, a, item + 1);
-      grp_last = !nx.same_group(cur);
-    }
-    if (B2 == kB2Resident && (item == i0 || !cur.same_group(prev))) {
-      if (!mbar_wait(smem_u32(&bars->b2_full), grp_it & 1, g)) { ok = false; break; }
-      ++grp_it;
-    }
+  for (; ok && cur.s < s1; ++item_ctr, cur.next_item(a)) {
     const uint32_t kb = item_ctr & 1;
-    if (!mbar_wait(smem_u32(&bars->kv_full[kb]), (item_ctr >> 1) & 1, g)) { ok = false; break; }
+    const bool first = cur.first_tile(a), last = cur.last_tile(a);
+    if (!mbar_wait_warp(smem_u32(&bars->kv_full[kb]), (item_ctr >> 1) & 1, g)) { ok = false; break; }
     const float* b1 = reinterpret_cast<const float*>(base + lay.b1[kb]) + hc * 64;
     for (int it = 0; it < QT; ++it, ++u) {
-      if (!mbar_wait(smem_u32(&bars->q_full[s]), ph, g)) { ok = false; break; }
+      // the fp32 dQ row this thread adds to at the end of the step (the previous step's),
+      // brought into L1 now so that its load does not wait on L2 then
+      if (u > 0 && !pd.first && pd.it * kTile + r < a.L)
+        prefetch_l1(a.dq_scr + (static_cast<size_t>(blockIdx.x) * a.L + pd.it * kTile + r) * DP + hc * (DP / 2));
+      if (!mbar_wait_warp(smem_u32(&bars->q_full[s]), ph, g)) { ok = false; break; }
       const float* ld = reinterpret_cast<const float*>(base + lay.ld[s]);
       const float lse2 = ld[r], dlt = ld[128 + r];
-      const uint8_t* b2half = base + (B2 == kB2Resident ? lay.b2r + it * 32768u : lay.b2s[s]) + hc * 16384;
-      if (!mbar_wait(smem_u32(&bars->st_full), u & 1, g)) { ok = false; break; }
-      // the P and dS tiles are free once the previous step's gradient MMAs have read them
-      if (!mbar_wait(smem_u32(&bars->ds_empty), (u & 1) ^ 1, g)) { ok = false; break; }
+      const uint8_t* b2half = base + lay.b2s[s] + hc * 16384;
+      if (!mbar_wait_warp(smem_u32(&bars->st_full), u & 1, g)) { ok = false; break; }
+      // this step's P and dS buffer is free once the gradient MMAs that last read it are done
+      const uint32_t pb = u % pds;
+      if (!mbar_wait_warp(smem_u32(&bars->ds_empty[pb]), ((u / pds) & 1) ^ 1, g)) { ok = false; break; }
       tc_fence_after();
-      uint8_t* pt = base + lay.p + hc * 16384;
-      uint8_t* dt = base + lay.ds + hc * 16384;
+      uint8_t* pt = base + lay.p[pb] + hc * 16384;
+      uint8_t* dt = base + lay.ds[pb] + hc * 16384;
       {
-        uint32_t sv[32], pv[32];
-        tmem_ld32(trow + col_s() + hc * 64, sv);
-        tmem_ld32(trow + col_dp() + hc * 64, pv);
-        tmem_wait_ld(sv);
-        tmem_wait_ld(pv);
-        main_chunk<BF16, kHasB2>(sv, pv, b1, b2half, pt, dt, r, 0, lse2, dlt, sl2);
-      }
-      {
-        uint32_t sv[32], pv[32];
-        tmem_ld32(trow + col_s() + hc * 64 + 32, sv);
-        tmem_ld32(trow + col_dp() + hc * 64 + 32, pv);
-        tmem_wait_ld(sv);
-        tmem_wait_ld(pv);
+        // 16-key chunks of S and dP: chunk k+1's TMEM loads are in flight while chunk k
+        // is computed (one pair outstanding, so each wait covers the chunk about to be used)
+        const uint32_t cs = trow + col_s() + hc * 64, cp = trow + col_dp() + hc * 64;
+        uint32_t s0[16], p0[16], s1[16], p1[16];
+        tmem_ld16(cs, s0);
+        tmem_ld16(cp, p0);
+        tmem_wait_ld(s0);
+        tmem_wait_ld(p0);
+        tmem_ld16(cs + 16, s1);
+        tmem_ld16(cp + 16, p1);
+        main_chunk16<BF16, HAS_B2>(s0, p0, b1, b2half, pt, dt, r, 0, lse2, dlt, sl2);
+        tmem_wait_ld(s1);
+        tmem_wait_ld(p1);
+        tmem_ld16(cs + 32, s0);
+        tmem_ld16(cp + 32, p0);
+        main_chunk16<BF16, HAS_B2>(s1, p1, b1, b2half, pt, dt, r, 1, lse2, dlt, sl2);
+        tmem_wait_ld(s0);
+        tmem_wait_ld(p0);
+        tmem_ld16(cs + 48, s1);
+        tmem_ld16(cp + 48, p1);
+        main_chunk16<BF16, HAS_B2>(s0, p0, b1, b2half, pt, dt, r, 2, lse2, dlt, sl2);
+        tmem_wait_ld(s1);
+        tmem_wait_ld(p1);
         // S and dP of this step are in registers: the next step's MMAs may overwrite them
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&bars->st_free));
-        main_chunk<BF16, kHasB2>(sv, pv, b1 + 32, b2half, pt, dt, r, 1, lse2, dlt, sl2);
+        main_chunk16<BF16, HAS_B2>(s1, p1, b1, b2half, pt, dt, r, 3, lse2, dlt, sl2);
       }
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(smem_u32(&bars->ds_full));
+        mbar_arrive(smem_u32(&bars->ds_full[pb]));
         mbar_arrive(smem_u32(&bars->q_empty[s]));
-        if (it == QT - 1) {
-          mbar_arrive(smem_u32(&bars->kv_empty[kb]));
-          if (B2 == kB2Resident && grp_last) mbar_arrive(smem_u32(&bars->b2_empty));
-        }
+        if (it == QT - 1) mbar_arrive(smem_u32(&bars->kv_empty[kb]));
       }
       if (u > 0) {
-        if (!main_consume_dq<DP>(a, it == 0 ? prev : cur, prev_it, u - 1, bars, trow, r, hc, lane, g)) {
-          ok = false;
-          break;
-        }
-        if (it == 0 && !main_write_dkdv<DP, BF16>(a, prev, item_ctr - 1, bars, trow, r, hc, lane, g)) {
+        if (!main_consume_dq<DP, BF16>(a, pd, u - 1, bars, trow, r, hc, lane, g)) { ok = false; break; }
+        if (it == 0 && !main_write_dkdv<DP, BF16>(a, pk, item_ctr - 1, bars, trow, r, hc, lane, g)) {
           ok = false;
           break;
         }
       }
-      prev_it = it;
+      pd = DqStep{cur.b, cur.n, cur.h, it, first, last};
       if (++s == static_cast<uint32_t>(QS)) {
         s = 0;
         ph ^= 1;
       }
     }
+    pk = KvItem{cur.b, cur.n, cur.h, cur.jt};
   }
   if (ok && u > 0) {
-    if (main_consume_dq<DP>(a, cur, prev_it, u - 1, bars, trow, r, hc, lane, g))
-      main_write_dkdv<DP, BF16>(a, cur, item_ctr - 1, bars, trow, r, hc, lane, g);
+    if (main_consume_dq<DP, BF16>(a, pd, u - 1, bars, trow, r, hc, lane, g))
+      main_write_dkdv<DP, BF16>(a, pk, item_ctr - 1, bars, trow, r, hc, lane, g);
   }
 }
 
-template <int DP, bool BF16, int B2>
+template <int DP, bool BF16, bool HAS_B2>
 __global__ void __launch_bounds__(kThreads, 1) evo_bwd_main(const __grid_constant__ BwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const MainLayout<DP> lay(B2, a.q_stages, a.QT);
+  const MainLayout<DP> lay(HAS_B2, a.q_stages, a.pds_bufs);
   MainBars* bars = reinterpret_cast<MainBars*>(base + lay.bars);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // the CTA's contiguous range of list positions: of the items themselves, or of the
-  // work list of masked-tile skipping (its length known only on the device)
-  const long long items = a.wl ? static_cast<long long>(*a.wl_total) : a.items;
-  const long long chunk = a.wl ? (items + gridDim.x - 1) / gridDim.x : a.chunk;
-  const long long i0 = static_cast<long long>(blockIdx.x) * chunk;
-  const long long i1 = i0 + chunk < items ? i0 + chunk : (items > i0 ? items : i0);  // empty past the end
+  // the CTA's contiguous range of whole slices
+  const long long s0 = static_cast<long long>(blockIdx.x) * a.chunk;
+  const long long s1 = s0 + a.chunk < a.items ? s0 + a.chunk : a.items;
   if (threadIdx.x == 0) {
     bars->abort = 0;
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(&bars->kv_full[s]), 32);
       mbar_init(smem_u32(&bars->kv_empty[s]), 1 + kComputeWarps);
+      mbar_init(smem_u32(&bars->ds_full[s]), kComputeWarps);
+      mbar_init(smem_u32(&bars->ds_empty[s]), 1);
       mbar_init(smem_u32(&bars->dq_full[s]), 1);
       mbar_init(smem_u32(&bars->dq_free[s]), kComputeWarps);
       mbar_init(smem_u32(&bars->dkdv_full[s]), 1);
@@ -911,12 +873,8 @@ __global__ void __launch_bounds__(kThreads, 1) evo_bwd_main(const __grid_constan
       mbar_init(smem_u32(&bars->q_full[s]), 32);
       mbar_init(smem_u32(&bars->q_empty[s]), 1 + kComputeWarps);
     }
-    mbar_init(smem_u32(&bars->b2_full), 32);
-    mbar_init(smem_u32(&bars->b2_empty), kComputeWarps);
     mbar_init(smem_u32(&bars->st_full), 1);
     mbar_init(smem_u32(&bars->st_free), kComputeWarps);
-    mbar_init(smem_u32(&bars->ds_full), kComputeWarps);
-    mbar_init(smem_u32(&bars->ds_empty), 1);
     mbar_init(smem_u32(&bars->drain), 1);
     fence_barrier_init();
   }
@@ -925,7 +883,7 @@ __global__ void __launch_bounds__(kThreads, 1) evo_bwd_main(const __grid_constan
     tma_prefetch_desc(&a.tk);
     tma_prefetch_desc(&a.tv);
     tma_prefetch_desc(&a.tdo);
-    if (B2 != kB2None && a.bias2_mode == kBias2Tma) tma_prefetch_desc(&a.tb2);
+    if (HAS_B2 && a.bias2_mode == kBias2Tma) tma_prefetch_desc(&a.tb2);
   }
   if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(&bars->tmem_slot), 512);
@@ -935,13 +893,15 @@ __global__ void __launch_bounds__(kThreads, 1) evo_bwd_main(const __grid_constan
   tc_fence_after();
   const uint32_t tmem = bars->tmem_slot;
   const WaitGuard g{a.wait_ns, a.status, &bars->abort};
-  if (warp == kProducerWarp) {
-    main_producer<DP, BF16, B2>(a, base, lay, bars, g, lane, i0, i1);
-  } else if (warp == kMmaWarp) {
-    if (lane == 0) main_mma<DP, BF16>(a, base, lay, bars, tmem, g, i0, i1);
-    __syncwarp();
-  } else {
-    main_compute<DP, BF16, B2>(a, base, lay, bars, tmem, g, i0, i1);
+  if (s0 < s1) {
+    if (warp == kProducerWarp) {
+      main_producer<DP, BF16, HAS_B2>(a, base, lay, bars, g, lane, s0, s1);
+    } else if (warp == kMmaWarp) {
+      if (lane == 0) main_mma<DP, BF16>(a, base, lay, bars, tmem, g, s0, s1);
+      __syncwarp();
+    } else {
+      main_compute<DP, BF16, HAS_B2>(a, base, lay, bars, tmem, g, s0, s1);
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -1051,7 +1011,7 @@ __device__ __forceinline__ void slice_producer(const BwdArgs& a, uint8_t* base, 
     const int bn = c.b * a.N + c.n, bh = c.b * a.H + c.h;
     for (int jt = 0; ok && jt < QT; ++jt, ++grp) {
       const uint32_t kb = grp & 1;
-      if (!mbar_wait(smem_u32(&bars->kv_empty[kb]), ((grp >> 1) & 1) ^ 1, g)) { ok = false; break; }
+      if (!mbar_wait_warp(smem_u32(&bars->kv_empty[kb]), ((grp >> 1) & 1) ^ 1, g)) { ok = false; break; }
       {
         const uint32_t full = smem_u32(&bars->kv_full[kb]);
         if (lane == 0) {
@@ -1070,7 +1030,7 @@ __device__ __forceinline__ void slice_producer(const BwdArgs& a, uint8_t* base, 
                       njt * kTile, lane);
       }
       for (int it = 0; it < QT; ++it, ++steps) {
-        if (!mbar_wait(smem_u32(&bars->q_empty[s]), ph ^ 1, g)) { ok = false; break; }
+        if (!mbar_wait_warp(smem_u32(&bars->q_empty[s]), ph ^ 1, g)) { ok = false; break; }
         const uint32_t full = smem_u32(&bars->q_full[s]);
         if (lane == 0) {
           mbar_expect_tx(full, q_bytes);
@@ -1268,7 +1228,7 @@ __device__ __forceinline__ bool slice_write_dkdv(const BwdArgs& a, const SlIter&
   constexpr int HD = DP / 2;
   const int nb = slice_kv_bufs(DP, a.QT);
   const uint32_t db = grp % nb;
-  if (!mbar_wait(smem_u32(&bars->dkdv_full[db]), (grp / nb) & 1, g)) return false;
+  if (!mbar_wait_warp(smem_u32(&bars->dkdv_full[db]), (grp / nb) & 1, g)) return false;
   tc_fence_after();
   float kx[HD], vx[HD];
   const uint32_t ck = trow + sl_col_dk<DP>(db) + hc * HD, cv = trow + sl_col_dv<DP>(db) + hc * HD;
@@ -1335,7 +1295,7 @@ template <int DP, bool BF16>
 __device__ __forceinline__ bool slice_write_dq(const BwdArgs& a, const SlIter& c, uint32_t slice, SliceBars* bars,
                                                uint32_t trow, int r, int hc, int lane, const WaitGuard& g) {
   constexpr int HD = DP / 2;
-  if (!mbar_wait(smem_u32(&bars->dq_full), slice & 1, g)) return false;
+  if (!mbar_wait_warp(smem_u32(&bars->dq_full), slice & 1, g)) return false;
   tc_fence_after();
   const long long bn = static_cast<long long>(c.b) * a.N + c.n;
   for (int it = 0; it < a.QT; ++it) {
@@ -1401,15 +1361,15 @@ __device__ __forceinline__ void slice_compute(const BwdArgs& a, uint8_t* base, c
     }
     for (int jt = 0; ok && jt < QT; ++jt, ++grp) {
       const uint32_t kb = grp & 1;
-      if (!mbar_wait(smem_u32(&bars->kv_full[kb]), (grp >> 1) & 1, g)) { ok = false; break; }
+      if (!mbar_wait_warp(smem_u32(&bars->kv_full[kb]), (grp >> 1) & 1, g)) { ok = false; break; }
       const float* b1 = reinterpret_cast<const float*>(base + lay.b1[kb]) + hc * 64;
       for (int it = 0; it < QT; ++it, ++u) {
-        if (!mbar_wait(smem_u32(&bars->q_full[s]), ph, g)) { ok = false; break; }
+        if (!mbar_wait_warp(smem_u32(&bars->q_full[s]), ph, g)) { ok = false; break; }
         const float* ld = reinterpret_cast<const float*>(base + lay.ld[s]);
         const float lse2 = ld[r], dlt = ld[128 + r];
         const uint8_t* b2half = base + lay.b2s[s] + hc * 16384;
-        if (!mbar_wait(smem_u32(&bars->st_full), u & 1, g)) { ok = false; break; }
-        if (!mbar_wait(smem_u32(&bars->ds_empty), (u & 1) ^ 1, g)) { ok = false; break; }
+        if (!mbar_wait_warp(smem_u32(&bars->st_full), u & 1, g)) { ok = false; break; }
+        if (!mbar_wait_warp(smem_u32(&bars->ds_empty), (u & 1) ^ 1, g)) { ok = false; break; }
         tc_fence_after();
         uint8_t* pt = base + lay.p + hc * 16384;
         uint8_t* dt = base + lay.ds + hc * 16384;
@@ -1648,7 +1608,7 @@ __global__ void __launch_bounds__(kThreads, 1) evo_bwd_db2_part(const __grid_con
     };
     if (nn > 0) prefetch(0);
     for (; k < nn; ++k) {
-      if (!mbar_wait(smem_u32(&bars->st_free[s]), ph ^ 1, g)) break;
+      if (!mbar_wait_warp(smem_u32(&bars->st_free[s]), ph ^ 1, g)) break;
       const int bn = c.b * a.N + c.n0 + k;
       const uint32_t full = smem_u32(&bars->st_full[s]);
       if (lane == 0) {
@@ -1713,46 +1673,66 @@ __global__ void __launch_bounds__(kThreads, 1) evo_bwd_db2_part(const __grid_con
     float acc[64];
 #pragma unroll
     for (int e = 0; e < 64; ++e) acc[e] = 0.0f;
-    bool ok = mbar_wait(smem_u32(&bars->b2_full), 0, g);
+    bool ok = mbar_wait_warp(smem_u32(&bars->b2_full), 0, g);
     int s = 0, ph = 0;
     for (int k = 0; ok && k < nn; ++k) {
       const uint32_t mb = k & 1;
-      if (!mbar_wait(smem_u32(&bars->st_full[s]), ph, g)) { ok = false; break; }
+      if (!mbar_wait_warp(smem_u32(&bars->st_full[s]), ph, g)) { ok = false; break; }
       const float* ld = reinterpret_cast<const float*>(base + lay.ld[s]);
       const float lse2 = ld[r], dlt = ld[128 + r];
       const float* b1 = reinterpret_cast<const float*>(base + lay.b1[s]) + hc * 64;
-      if (!mbar_wait(smem_u32(&bars->mm_full[mb]), (k >> 1) & 1, g)) { ok = false; break; }
+      if (!mbar_wait_warp(smem_u32(&bars->mm_full[mb]), (k >> 1) & 1, g)) { ok = false; break; }
       tc_fence_after();
+      // 16-key chunks of S and dP: chunk k+1's TMEM loads are in flight while chunk k is
+      // summed (one pair outstanding, so each wait covers the chunk about to be used)
+      const float2 nl2 = make_float2(-lse2, -lse2), l2e2 = make_float2(kLog2e, kLog2e),
+                   nd2 = make_float2(-dlt, -dlt);
+      const uint32_t cs = trow + col_ps(mb) + hc * 64, cpd = trow + col_pdp(mb) + hc * 64;
+      auto chunk16 = [&](const uint32_t (&sv)[16], const uint32_t (&pv)[16], int kc) {
 #pragma unroll
-      for (int c4 = 0; c4 < 2; ++c4) {
-        uint32_t sv[32], pv[32];
-        tmem_ld32(trow + col_ps(mb) + hc * 64 + c4 * 32, sv);
-        tmem_ld32(trow + col_pdp(mb) + hc * 64 + c4 * 32, pv);
-        tmem_wait_ld(sv);
-        tmem_wait_ld(pv);
-        const float2 nl2 = make_float2(-lse2, -lse2), l2e2 = make_float2(kLog2e, kLog2e),
-                     nd2 = make_float2(-dlt, -dlt);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float4 m0 = *reinterpret_cast<const float4*>(b1 + c4 * 32 + q * 8);
-          const float4 m1 = *reinterpret_cast<const float4*>(b1 + c4 * 32 + q * 8 + 4);
+        for (int q = 0; q < 2; ++q) {
+          const float4 m0 = *reinterpret_cast<const float4*>(b1 + kc * 16 + q * 8);
+          const float4 m1 = *reinterpret_cast<const float4*>(b1 + kc * 16 + q * 8 + 4);
           const float2 mk[4] = {make_float2(m0.x, m0.y), make_float2(m0.z, m0.w), make_float2(m1.x, m1.y),
                                 make_float2(m1.z, m1.w)};
-          const uint4 pb = *reinterpret_cast<const uint4*>(b2half + swz_offset(r, c4 * 4 + q, 128));
+          const uint4 pb = *reinterpret_cast<const uint4*>(b2half + swz_offset(r, kc * 2 + q, 128));
           const uint32_t pw[4] = {pb.x, pb.y, pb.z, pb.w};
 #pragma unroll
           for (int e2 = 0; e2 < 4; ++e2) {
-            const int x = q * 8 + e2 * 2;
+            const int x = q * 8 + e2 * 2, y = kc * 16 + x;
             float2 t = fma2(make_float2(__uint_as_float(sv[x]), __uint_as_float(sv[x + 1])), sl2, mk[e2]);
             t = fma2(unpack2<BF16>(pw[e2]), l2e2, t);
             t = add2(t, nl2);
             const float2 pr = make_float2(ex2(t.x), ex2(t.y));
             const float2 dpd = add2(make_float2(__uint_as_float(pv[x]), __uint_as_float(pv[x + 1])), nd2);
-            const float2 a2 = fma2(pr, dpd, make_float2(acc[c4 * 32 + x], acc[c4 * 32 + x + 1]));
-            acc[c4 * 32 + x] = a2.x;
-            acc[c4 * 32 + x + 1] = a2.y;
+            const float2 a2 = fma2(pr, dpd, make_float2(acc[y], acc[y + 1]));
+            acc[y] = a2.x;
+            acc[y + 1] = a2.y;
           }
         }
+      };
+      {
+        uint32_t s0[16], p0[16], s1[16], p1[16];
+        tmem_ld16(cs, s0);
+        tmem_ld16(cpd, p0);
+        tmem_wait_ld(s0);
+        tmem_wait_ld(p0);
+        tmem_ld16(cs + 16, s1);
+        tmem_ld16(cpd + 16, p1);
+        chunk16(s0, p0, 0);
+        tmem_wait_ld(s1);
+        tmem_wait_ld(p1);
+        tmem_ld16(cs + 32, s0);
+        tmem_ld16(cpd + 32, p0);
+        chunk16(s1, p1, 1);
+        tmem_wait_ld(s0);
+        tmem_wait_ld(p0);
+        tmem_ld16(cs + 48, s1);
+        tmem_ld16(cpd + 48, p1);
+        chunk16(s0, p0, 2);
+        tmem_wait_ld(s1);
+        tmem_wait_ld(p1);
+        chunk16(s1, p1, 3);
       }
       tc_fence_before();
       __syncwarp();
@@ -1811,18 +1791,21 @@ unsigned grid_for(long long work, long long per_block) {
   return static_cast<unsigned>(g < 1 ? 1 : g);
 }
 
-template <int DP, bool BF16, int B2>
+template <int DP, bool BF16, bool HAS_B2>
 cudaError_t launch_main(BwdArgs a, cudaStream_t st) {
-  const MainLayout<DP> lay(B2, a.q_stages, a.QT);
+  const MainLayout<DP> lay(HAS_B2, a.q_stages, a.pds_bufs);
   const size_t smem = one_cta_per_sm(lay.total + 1024);
-  auto kern = evo_bwd_main<DP, BF16, B2>;
+  auto kern = evo_bwd_main<DP, BF16, HAS_B2>;
   static bool limit_set[64] = {};
   cudaError_t e = ensure_smem_limit(kern, kMaxSmem, limit_set);
   if (e != cudaSuccess) return e;
-  const long long sms = num_sms();
-  a.chunk = (a.items + sms - 1) / sms;
-  // with a work list every CTA splits the list's (device-side) length evenly
-  const long long grid = a.wl ? (a.items < sms ? a.items : sms) : (a.items + a.chunk - 1) / a.chunk;
+  // whole slices per CTA; at most kMainMaxCtas CTAs (the workspace holds L × DP fp32 dQ
+  // rows for each)
+  a.items = static_cast<long long>(a.B) * a.H * a.N;
+  long long ctas = num_sms();
+  if (ctas > kMainMaxCtas) ctas = kMainMaxCtas;
+  a.chunk = (a.items + ctas - 1) / ctas;
+  const long long grid = (a.items + a.chunk - 1) / a.chunk;
   kern<<<static_cast<unsigned>(grid), kThreads, smem, st>>>(a);
   return cudaGetLastError();
 }
@@ -1859,7 +1842,6 @@ cudaError_t launch_bwd_d(BwdArgs a, cudaStream_t st, const ProfileEvents* prof) 
   a.items = static_cast<long long>(a.B) * a.H * a.QT * a.N;
   const BwdPlan plan = bwd_plan(DP, a.QT, has_b2);
   const int slice_qs = plan.mode == kBwdSlice ? plan.q_stages : 0;
-  a.zero_dq = plan.mode == kBwdMain;
   if (plan.mode != kBwdKeyMajor && !a.db1p) a.b2t = nullptr;
   prof_record(prof, 2, st);
   evo_bwd_pre<DP, BF16><<<grid_for(rows, 256), 256, 0, st>>>(a);
@@ -1879,44 +1861,31 @@ cudaError_t launch_bwd_d(BwdArgs a, cudaStream_t st, const ProfileEvents* prof) 
     prof_record(prof, 5, st);  // no dQ cast in slice mode
   } else {
 
-  // main kernel: deepest Q/dO ring that fits, resident pair-bias tiles when possible; without
-  // resident tiles an (n, h)'s key tiles run back to back (its Q, dO and dQ rows stay in L2)
-  auto fits = [&](int kind, int qs) { return MainLayout<DP>(kind, qs, a.QT).total + 1024 <= kMaxSmem; };
-  int kind = kB2None, qs = 1;
-  if (!has_b2) {
-    qs = fits(kB2None, 4) ? 4 : (fits(kB2None, 3) ? 3 : (fits(kB2None, 2) ? 2 : 1));
-  } else {
-    kind = kB2Stream;
-    for (int q = 4; q >= 2; --q)
-      if (fits(kB2Resident, q)) {
-        kind = kB2Resident;
+  // per-key-tile kernel: double P/dS buffers with the deepest Q/dO ring (at least two
+  // stages) that fits; otherwise single buffers
+  auto fits = [&](int qs, int pds) { return MainLayout<DP>(has_b2, qs, pds).total + 1024 <= kMaxSmem; };
+  int qs = 1, pds = 1;
+  for (int q = 4; q >= 2 && pds == 1; --q)
+    if (fits(q, 2)) {
+      qs = q;
+      pds = 2;
+    }
+  if (pds == 1)
+    for (int q = 4; q >= 1; --q)
+      if (fits(q, 1)) {
         qs = q;
         break;
       }
-    if (kind == kB2Stream) qs = fits(kB2Stream, 3) ? 3 : (fits(kB2Stream, 2) ? 2 : 1);
-  }
   a.q_stages = qs;
-  a.b2_resident = kind == kB2Resident;
-  a.jt_fast = kind != kB2Resident;
-  if (a.tile_skip) {  // masked key tiles: skip bits and zero dK/dV rows, then the work list
+  a.pds_bufs = pds;
+  if (a.tile_skip) {  // masked key tiles: skip bits, and zeros for dK/dV of the skipped tiles
     evo_bwd_tile_mask<BF16><<<grid_for(static_cast<long long>(a.B) * a.N * 32, 256), 256, 0, st>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    if (a.jt_fast)
-      evo_bwd_worklist_jt<<<1, 1024, 0, st>>>(a);
-    else
-      evo_bwd_worklist<<<1, 1024, 0, st>>>(a);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  } else {
-    a.wl = nullptr;
   }
-  e = kind == kB2None       ? launch_main<DP, BF16, kB2None>(a, st)
-      : kind == kB2Resident ? launch_main<DP, BF16, kB2Resident>(a, st)
-                            : launch_main<DP, BF16, kB2Stream>(a, st);
+  e = has_b2 ? launch_main<DP, BF16, true>(a, st) : launch_main<DP, BF16, false>(a, st);
   if (e != cudaSuccess) return e;
   prof_record(prof, 4, st);
-  evo_bwd_dq_cast<BF16><<<grid_for(rows * a.D / 8, 256), 256, 0, st>>>(a);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  prof_record(prof, 5, st);
+  prof_record(prof, 5, st);  // no dQ cast: the kernel writes dQ
   }
 
   if (a.db1p) {  // key-mask gradient: partials (by the key-major kernel, or a separate pass), then the sum
@@ -1924,7 +1893,7 @@ cudaError_t launch_bwd_d(BwdArgs a, cudaStream_t st, const ProfileEvents* prof) 
       return e;
     if ((e = launch_bwd_db1_sum(a, BF16, st)) != cudaSuccess) return e;
   }
-  if (has_b2) {
+  if (has_b2 && a.dbias2) {
     // deepest ring that fits; staging for tile stores of the partials when it fits too
     auto pfits = [&](int ns, bool stg) { return PartLayout<DP>(ns, stg).total + 1024 <= kMaxSmem; };
     if (a.db2p_tma && !pfits(2, true)) a.db2p_tma = 0;

@@ -112,58 +112,6 @@ __device__ __forceinline__ void fill_lse_delta(float* dst, const float* lse, con
   ld_store(dst, raw, lane);
 }
 
-// Incremental iterator over the per-key-tile kernel's items: (b, h, key tile, n), n fastest,
-// or with jt_fast (b, h, n, key tile), key tile fastest.
-struct KvIter {
-  int b, h, jt, n;
-  __device__ __forceinline__ void init(long long item, const BwdArgs& a) {
-    long long t = item;
-    if (a.jt_fast) {
-      jt = static_cast<int>(t % a.QT);
-      t /= a.QT;
-      n = static_cast<int>(t % a.N);
-      t /= a.N;
-    } else {
-      n = static_cast<int>(t % a.N);
-      t /= a.N;
-      jt = static_cast<int>(t % a.QT);
-      t /= a.QT;
-    }
-    h = static_cast<int>(t % a.H);
-    b = static_cast<int>(t / a.H);
-  }
-  __device__ __forceinline__ void next(const BwdArgs& a) {
-    int& fast = a.jt_fast ? jt : n;
-    int& slow = a.jt_fast ? n : jt;
-    const int nfast = a.jt_fast ? a.QT : a.N, nslow = a.jt_fast ? a.N : a.QT;
-    if (++fast == nfast) {
-      fast = 0;
-      if (++slow == nslow) {
-        slow = 0;
-        if (++h == a.H) {
-          h = 0;
-          ++b;
-        }
-      }
-    }
-  }
-  // same (b, h, key tile): the items that share resident pair-bias tiles
-  __device__ __forceinline__ bool same_group(const KvIter& o) const { return b == o.b && h == o.h && jt == o.jt; }
-};
-
-// Item at position idx of a per-key-tile kernel's range: the position itself, or the
-// entry of the masked-tile-skipping work list.
-__device__ __forceinline__ long long item_at(const BwdArgs& a, long long idx) {
-  return a.wl ? static_cast<long long>(a.wl[idx]) : idx;
-}
-// c becomes the item at position idx, the one after c's position.
-__device__ __forceinline__ void advance(KvIter& c, const BwdArgs& a, long long idx) {
-  if (a.wl)
-    c.init(a.wl[idx], a);
-  else
-    c.next(a);
-}
-
 // (b, h, n) slice iterator, n fastest.
 struct SlIter {
   int b, h, n;

@@ -160,7 +160,7 @@ __device__ __forceinline__ void km_producer(const BwdArgs& a, uint8_t* base, con
     const int bn = c.b * a.N + c.n, bh = c.b * a.H + c.h;
     for (int jt = 0; ok && jt < QT; ++jt, ++grp) {
       const uint32_t kb = grp & 1;
-      if (!mbar_wait(smem_u32(&bars->kv_empty[kb]), ((grp >> 1) & 1) ^ 1, g)) { ok = false; break; }
+      if (!mbar_wait_warp(smem_u32(&bars->kv_empty[kb]), ((grp >> 1) & 1) ^ 1, g)) { ok = false; break; }
       {
         const uint32_t full = smem_u32(&bars->kv_full[kb]);
         if (lane == 0) {
@@ -182,7 +182,7 @@ __device__ __forceinline__ void km_producer(const BwdArgs& a, uint8_t* base, con
                       njt * kTile, lane);
       }
       for (int it = 0; it < QT; ++it, ++steps) {
-        if (!mbar_wait(smem_u32(&bars->q_empty[s]), ph ^ 1, g)) { ok = false; break; }
+        if (!mbar_wait_warp(smem_u32(&bars->q_empty[s]), ph ^ 1, g)) { ok = false; break; }
         const uint32_t full = smem_u32(&bars->q_full[s]);
         if (lane == 0) {
           mbar_expect_tx(full, q_bytes);
@@ -372,6 +372,45 @@ __device__ __forceinline__ void km_chunk(const uint32_t (&sv)[32], const uint32_
   tmem_st16(p_tcol, pp);
 }
 
+// The same for one 16-query chunk k (0..3) of this warp's 64 queries: Pᵀ pairs into
+// pp[0..7], dSᵀ into the smem tile.
+template <bool BF16, bool HAS_B2, bool DB1>
+__device__ __forceinline__ void km_chunk16(const uint32_t (&sv)[16], const uint32_t (&pv)[16], float b1j,
+                                           const float* nl, const float* nd, const uint8_t* b2half, uint8_t* dshalf,
+                                           uint32_t* pp, int r, int k, float2 sl2, float2& dsum) {
+  const float2 mk = make_float2(b1j, b1j), l2e2 = make_float2(kLog2e, kLog2e);
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const float4 l0 = *reinterpret_cast<const float4*>(nl + k * 16 + q * 8);
+    const float4 l1 = *reinterpret_cast<const float4*>(nl + k * 16 + q * 8 + 4);
+    const float4 d0 = *reinterpret_cast<const float4*>(nd + k * 16 + q * 8);
+    const float4 d1 = *reinterpret_cast<const float4*>(nd + k * 16 + q * 8 + 4);
+    const float2 nl2[4] = {make_float2(l0.x, l0.y), make_float2(l0.z, l0.w), make_float2(l1.x, l1.y),
+                           make_float2(l1.z, l1.w)};
+    const float2 nd2[4] = {make_float2(d0.x, d0.y), make_float2(d0.z, d0.w), make_float2(d1.x, d1.y),
+                           make_float2(d1.z, d1.w)};
+    const uint32_t off = swz_offset(r, k * 2 + q, 128);
+    uint4 pb = make_uint4(0u, 0u, 0u, 0u);
+    if (HAS_B2) pb = *reinterpret_cast<const uint4*>(b2half + off);
+    const uint32_t pw[4] = {pb.x, pb.y, pb.z, pb.w};
+    uint32_t dd[4];
+#pragma unroll
+    for (int e2 = 0; e2 < 4; ++e2) {
+      const int x = q * 8 + e2 * 2;
+      float2 t = fma2(make_float2(__uint_as_float(sv[x]), __uint_as_float(sv[x + 1])), sl2, mk);
+      if (HAS_B2) t = fma2(unpack2<BF16>(pw[e2]), l2e2, t);
+      t = add2(t, nl2[e2]);
+      const float p0 = ex2(t.x), p1 = ex2(t.y);
+      const float2 dpd = add2(make_float2(__uint_as_float(pv[x]), __uint_as_float(pv[x + 1])), nd2[e2]);
+      const float2 ds = mul2(make_float2(p0, p1), dpd);
+      if (DB1) dsum = add2(dsum, ds);
+      pp[q * 4 + e2] = pack2<BF16>(p0, p1);
+      dd[e2] = pack2<BF16>(ds.x, ds.y);
+    }
+    *reinterpret_cast<uint4*>(dshalf + off) = make_uint4(dd[0], dd[1], dd[2], dd[3]);
+  }
+}
+
 // HD fp32 TMEM columns of this thread's lane into v.
 template <int HD>
 __device__ __forceinline__ void km_load_cols(uint32_t col, float (&v)[HD]) {
@@ -436,7 +475,7 @@ __device__ __forceinline__ bool km_write_dkdv(const BwdArgs& a, const SlIter& c,
   constexpr int HD = DP / 2;
   const int nb = km_kv_bufs(DP, a.QT);
   const uint32_t db = grp % nb;
-  if (!mbar_wait(smem_u32(&bars->dkdv_full[db]), (grp / nb) & 1, g)) return false;
+  if (!mbar_wait_warp(smem_u32(&bars->dkdv_full[db]), (grp / nb) & 1, g)) return false;
   tc_fence_after();
   float kx[HD], vx[HD];
   km_load_cols<HD>(trow + km_col_dk<DP>(db) + hc * HD, kx);
@@ -465,7 +504,7 @@ __device__ __forceinline__ bool km_write_dq(const BwdArgs& a, const SlIter& c, u
                                             const KmLayout<DP>& lay, KmBars* bars, uint32_t trow, int w, int hc,
                                             int lane, const WaitGuard& g) {
   constexpr int HD = DP / 2;
-  if (!mbar_wait(smem_u32(&bars->dq_full), slice & 1, g)) return false;
+  if (!mbar_wait_warp(smem_u32(&bars->dq_full), slice & 1, g)) return false;
   tc_fence_after();
   const int nb = km_kv_bufs(DP, a.QT);
   const int bn = c.b * a.N + c.n;
@@ -526,38 +565,52 @@ __device__ __forceinline__ void km_compute(const BwdArgs& a, uint8_t* base, cons
       const uint32_t kb = grp & 1;
       for (int it = 0; it < QT; ++it, ++u) {
         if (it == 0) {
-          if (!mbar_wait(smem_u32(&bars->kv_full[kb]), (grp >> 1) & 1, g)) { ok = false; break; }
+          if (!mbar_wait_warp(smem_u32(&bars->kv_full[kb]), (grp >> 1) & 1, g)) { ok = false; break; }
           b1j = reinterpret_cast<const float*>(base + lay.b1[kb])[r];
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&bars->kv_empty[kb]));
         }
-        if (!mbar_wait(smem_u32(&bars->q_full[s]), ph, g)) { ok = false; break; }
-        if (!mbar_wait(smem_u32(&bars->st_full), u & 1, g)) { ok = false; break; }
-        if (!mbar_wait(smem_u32(&bars->buf_free[u & 1]), ((u >> 1) & 1) ^ 1, g)) { ok = false; break; }
+        if (!mbar_wait_warp(smem_u32(&bars->q_full[s]), ph, g)) { ok = false; break; }
+        if (!mbar_wait_warp(smem_u32(&bars->st_full), u & 1, g)) { ok = false; break; }
+        if (!mbar_wait_warp(smem_u32(&bars->buf_free[u & 1]), ((u >> 1) & 1) ^ 1, g)) { ok = false; break; }
         tc_fence_after();
         const float* ld = reinterpret_cast<const float*>(base + lay.ld[s]) + hc * 64;
         const uint8_t* b2half = base + lay.b2t[s] + hc * 16384;
         uint8_t* dshalf = base + lay.ds[u & 1] + hc * 16384;
         const uint32_t pcol = trow + km_col_p(u & 1) + hc * 32;
         {
-          uint32_t sv[32], pv[32];
-          tmem_ld32(trow + kKmS + hc * 64, sv);
-          tmem_ld32(trow + kKmDP + hc * 64, pv);
-          tmem_wait_ld(sv);
-          tmem_wait_ld(pv);
-          km_chunk<BF16, HAS_B2, DB1>(sv, pv, b1j, ld, ld + 128, b2half, dshalf, pcol, r, 0, sl2, dsum);
-        }
-        {
-          uint32_t sv[32], pv[32];
-          tmem_ld32(trow + kKmS + hc * 64 + 32, sv);
-          tmem_ld32(trow + kKmDP + hc * 64 + 32, pv);
-          tmem_wait_ld(sv);
-          tmem_wait_ld(pv);
+          // 16-query chunks of Sᵀ and dPᵀ: chunk k+1's TMEM loads are in flight while chunk
+          // k is computed (one pair outstanding, so each wait covers the chunk about to be
+          // used); Pᵀ pairs go to TMEM two chunks at a time
+          const uint32_t cs = trow + kKmS + hc * 64, cpd = trow + kKmDP + hc * 64;
+          const float* nl = ld;
+          const float* nd = ld + 128;
+          uint32_t s0[16], p0[16], s1[16], p1[16], pp[16];
+          tmem_ld16(cs, s0);
+          tmem_ld16(cpd, p0);
+          tmem_wait_ld(s0);
+          tmem_wait_ld(p0);
+          tmem_ld16(cs + 16, s1);
+          tmem_ld16(cpd + 16, p1);
+          km_chunk16<BF16, HAS_B2, DB1>(s0, p0, b1j, nl, nd, b2half, dshalf, pp, r, 0, sl2, dsum);
+          tmem_wait_ld(s1);
+          tmem_wait_ld(p1);
+          tmem_ld16(cs + 32, s0);
+          tmem_ld16(cpd + 32, p0);
+          km_chunk16<BF16, HAS_B2, DB1>(s1, p1, b1j, nl, nd, b2half, dshalf, pp + 8, r, 1, sl2, dsum);
+          tmem_st16(pcol, pp);
+          tmem_wait_ld(s0);
+          tmem_wait_ld(p0);
+          tmem_ld16(cs + 48, s1);
+          tmem_ld16(cpd + 48, p1);
+          km_chunk16<BF16, HAS_B2, DB1>(s0, p0, b1j, nl, nd, b2half, dshalf, pp, r, 2, sl2, dsum);
+          tmem_wait_ld(s1);
+          tmem_wait_ld(p1);
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&bars->st_free));
-          km_chunk<BF16, HAS_B2, DB1>(sv, pv, b1j, ld + 32, ld + 160, b2half, dshalf, pcol + 16, r, 1, sl2,
-                                      dsum);
+          km_chunk16<BF16, HAS_B2, DB1>(s1, p1, b1j, nl, nd, b2half, dshalf, pp + 8, r, 3, sl2, dsum);
+          tmem_st16(pcol + 16, pp);
         }
         tmem_wait_st();
         tc_fence_before();
@@ -761,13 +814,13 @@ __device__ __forceinline__ void km_db1_compute(const BwdArgs& a, uint8_t* base, 
       for (int it = 0; it < QT; ++it, ++u) {
         const uint32_t b = u & 1;
         if (it == 0) {
-          if (!mbar_wait(smem_u32(&bars->kv_full[kb]), (grp >> 1) & 1, g)) { ok = false; break; }
+          if (!mbar_wait_warp(smem_u32(&bars->kv_full[kb]), (grp >> 1) & 1, g)) { ok = false; break; }
           b1j = reinterpret_cast<const float*>(base + lay.b1[kb])[r];
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&bars->kv_empty[kb]));
         }
-        if (!mbar_wait(smem_u32(&bars->q_full[s]), ph, g)) { ok = false; break; }
-        if (!mbar_wait(smem_u32(&bars->sd_full[b]), (u >> 1) & 1, g)) { ok = false; break; }
+        if (!mbar_wait_warp(smem_u32(&bars->q_full[s]), ph, g)) { ok = false; break; }
+        if (!mbar_wait_warp(smem_u32(&bars->sd_full[b]), (u >> 1) & 1, g)) { ok = false; break; }
         tc_fence_after();
         const float* ld = reinterpret_cast<const float*>(base + lay.ld[s]) + hc * 64;
         const uint8_t* b2half = base + lay.b2t[s] + hc * 16384;

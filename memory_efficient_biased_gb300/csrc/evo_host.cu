@@ -22,21 +22,18 @@
 
 namespace evo {
 
-// Device status word: kernels record a bounded wait that ran out here.
+// Fallback device status word: kernels of calls given no status location of their
+// own record a bounded wait that ran out here (evo_attn_device_status reads it).
 __device__ int g_evo_status = 0;
 
-static std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
-// Masked key-tile skipping (evo_attn_set_masked_tile_skip): off by default.
-static std::atomic<int> g_skip_on{0};
-static std::atomic<float> g_skip_at{-1.0e4f};
-static ProfileEvents g_prof{{nullptr}, 0};
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;
 
 // What made this thread's last call return EVO_ERR_CUDA (evo_attn_last_error_detail).
 static thread_local char g_detail[192] = "";
 static void set_detail(const char* what, int code, const char* name) {
   std::snprintf(g_detail, sizeof(g_detail), "%s: %s (%d)", what, name ? name : "?", code);
 }
-static evo_status_t cuda_fail(const char* what, cudaError_t e) {
+evo_status_t cuda_fail(const char* what, cudaError_t e) {
   set_detail(what, static_cast<int>(e), cudaGetErrorName(e));
   return EVO_ERR_CUDA;
 }
@@ -66,6 +63,32 @@ DeviceInfo* device_info(int* dev_out) {
   });
   if (dev_out) *dev_out = dev;
   return &d;
+}
+
+// The settings of one call: from its evo_options_t, or the defaults.
+struct CallOpts {
+  bool skip = false;
+  float skip_at = -1.0e4f;
+  uint64_t wait_ns = kDefaultWaitNs;
+  int* status = nullptr;  // where kernels record a timeout; nullptr = the call's default location
+  bool no_db2 = false;
+  ProfileEvents prof{{nullptr}, 0};
+};
+
+// Reads *o into c; false when the struct is malformed.
+bool read_opts(const evo_options_t* o, CallOpts* c) {
+  if (!o) return true;
+  if (o->size < sizeof(evo_options_t)) return false;
+  if (o->flags & ~static_cast<uint32_t>(EVO_OPT_SKIP_MASKED_TILES | EVO_OPT_NO_DBIAS2)) return false;
+  if (o->num_events < 0 || (o->num_events > 0 && !o->events)) return false;
+  c->skip = (o->flags & EVO_OPT_SKIP_MASKED_TILES) != 0;
+  c->skip_at = o->skip_threshold;
+  c->no_db2 = (o->flags & EVO_OPT_NO_DBIAS2) != 0;
+  if (o->wait_limit_ns) c->wait_ns = o->wait_limit_ns < 1000 ? 1000 : o->wait_limit_ns;
+  c->status = o->status;
+  c->prof.count = o->num_events > 8 ? 8 : o->num_events;
+  for (int i = 0; i < c->prof.count; ++i) c->prof.ev[i] = o->events[i];
+  return true;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
@@ -149,6 +172,22 @@ bool map_rows_half(CUtensorMap* m, const void* p, const evo_shape_t& s, bool bf1
                 DP == 64   ? CU_TENSOR_MAP_SWIZZLE_64B
                 : DP == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
                            : CU_TENSOR_MAP_SWIZZLE_NONE,
+                CU_TENSOR_MAP_L2_PROMOTION_NONE);
+}
+
+// The same 4-D view with a box of 32 whole rows: (DP, 1, 32, 1); swizzle = the box row
+// (2·DP bytes).
+bool map_rows32(CUtensorMap* m, const void* p, const evo_shape_t& s, bool bf16, const Rows& r) {
+  const int DP = padded_dim(s.D);
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(s.D), static_cast<cuuint64_t>(s.H), static_cast<cuuint64_t>(s.L),
+                        static_cast<cuuint64_t>(s.B * s.N)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(s.D * 2), static_cast<cuuint64_t>(r.l * 2),
+                           static_cast<cuuint64_t>(r.bn * 2)};
+  cuuint32_t box[4] = {static_cast<cuuint32_t>(DP), 1, 32, 1};
+  return encode(m, p, bf16, 4, dims, strides, box,
+                DP == 64   ? CU_TENSOR_MAP_SWIZZLE_128B
+                : DP == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
+                           : CU_TENSOR_MAP_SWIZZLE_32B,
                 CU_TENSOR_MAP_L2_PROMOTION_NONE);
 }
 
@@ -285,43 +324,48 @@ void bwd_groups(const evo_shape_t& s, int* groups, int* group_size) {
 
 int b2t_pitch(const evo_shape_t& s) { return static_cast<int>((s.L + 7) / 8 * 8); }
 
-// Backward workspace: delta always; the fp32 dQ accumulator only for the
-// per-key-tile kernel; the transposed pair bias wherever a key-major kernel
-// reads it (the key-major schedule, or the key-mask gradient pass); the
-// key-mask gradient partials when dbias1 is wanted; the pair-bias partial
-// planes whenever there is a pair bias.
+// Backward workspace: delta always; for the per-key-tile kernel, L × DP fp32 dQ
+// rows per CTA (at most kMainMaxCtas CTAs) and the skip bits of masked-tile
+// skipping; the transposed pair bias wherever a key-major kernel reads it (the
+// key-major schedule, or the key-mask gradient pass); the key-mask gradient
+// partials when dbias1 is wanted; the pair-bias partial planes whenever there
+// is a pair bias.
 struct WsLayout {
   BwdPlan plan;
-  size_t delta, dq_acc, b2t, db1p, db2, skip, total;
-  bool can_skip;  // room for the masked-tile work list (per-key-tile schedule, at most 64 key tiles)
+  size_t status, delta, dq_scr, b2t, db1p, db2, skip, total;
+  bool can_skip;  // room for the skip bits (per-key-tile schedule, at most 64 key tiles)
 };
-WsLayout ws_layout(const evo_shape_t& s, bool has_bias2, bool has_db1 = false) {
+// has_db2: the call computes the pair-bias gradient (its partial planes)
+WsLayout ws_layout(const evo_shape_t& s, bool has_bias2, bool has_db1 = false, bool has_db2 = true) {
   WsLayout w{};
   w.plan = bwd_plan(padded_dim(s.D), static_cast<int>((s.L + kTile - 1) / kTile), has_bias2);
   size_t off = 0;
+  w.status = off;  // the call's device status word (evo_attn_bwd_status)
+  off += 256;
   w.delta = off;
   off += round256(size_t(s.B) * s.N * s.H * s.L * 4);
-  w.dq_acc = off;
-  if (w.plan.mode == kBwdMain) off += round256(size_t(s.B) * s.N * s.L * s.H * s.D * 4);
+  w.dq_scr = off;
+  if (w.plan.mode == kBwdMain) {
+    const int64_t slices = s.B * s.H * s.N;
+    const int64_t ctas = slices < kMainMaxCtas ? slices : kMainMaxCtas;
+    off += round256(size_t(ctas) * s.L * padded_dim(s.D) * 4);
+  }
   w.b2t = off;
   if ((w.plan.mode == kBwdKeyMajor || has_db1) && has_bias2)
     off += round256(size_t(s.B) * s.H * s.L * b2t_pitch(s) * 2);
   w.db1p = off;
   if (has_db1) off += round256(size_t(s.B) * s.N * s.H * 2 * s.L * 4);
   w.db2 = off;
-  if (has_bias2) {
+  if (has_bias2 && has_db2) {
     int g = 0, gs = 0;
     bwd_groups(s, &g, &gs);
     off += round256(size_t(g) * s.B * s.H * s.L * s.L * 4);
   }
-  // masked-tile skipping of the per-key-tile kernel: skip bits [B*N] u64, kept n
-  // [B*QT][N], counts and offsets [2*B*QT + 2*B], the work list [items], its length
-  const int64_t QT = (s.L + kTile - 1) / kTile, items = s.B * s.H * QT * s.N;
+  // masked-tile skipping of the per-key-tile kernel: skip bits [B*N] u64
+  const int64_t QT = (s.L + kTile - 1) / kTile;
   w.skip = off;
-  w.can_skip = w.plan.mode == kBwdMain && QT <= 64 && items <= int64_t(0xffffffffll);
-  if (w.can_skip)
-    off += round256(size_t(s.B) * s.N * 8) +
-           round256((size_t(s.B) * QT * s.N + 2 * size_t(s.B) * QT + 2 * size_t(s.B) + size_t(items) + 1) * 4);
+  w.can_skip = w.plan.mode == kBwdMain && QT <= 64;
+  if (w.can_skip) off += round256(size_t(s.B) * s.N * 8);
   w.total = off;
   return w;
 }
@@ -382,21 +426,23 @@ const char* evo_status_string(evo_status_t s) {
   return "unknown status";
 }
 
-void evo_attn_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns < 1000 ? 1000 : ns); }
-
-void evo_attn_set_masked_tile_skip(int enable, float threshold) {
-  g_skip_at.store(threshold);
-  g_skip_on.store(enable != 0);
-}
-
 evo_status_t evo_attn_fwd(const void* q, const void* k, const void* v, const void* bias1, const void* bias2,
                           void* out, float* lse, evo_shape_t shape, evo_dtype_t dtype, void* stream) {
-  return evo_attn_fwd_strided(q, k, v, bias1, bias2, out, lse, shape, dtype, nullptr, stream);
+  return evo_attn_fwd_opts(q, k, v, bias1, bias2, out, lse, shape, dtype, nullptr, nullptr, stream);
 }
 
 evo_status_t evo_attn_fwd_strided(const void* q, const void* k, const void* v, const void* bias1,
                                   const void* bias2, void* out, float* lse, evo_shape_t shape, evo_dtype_t dtype,
                                   const evo_layout_t* layout, void* stream) {
+  return evo_attn_fwd_opts(q, k, v, bias1, bias2, out, lse, shape, dtype, layout, nullptr, stream);
+}
+
+evo_status_t evo_attn_fwd_opts(const void* q, const void* k, const void* v, const void* bias1, const void* bias2,
+                               void* out, float* lse, evo_shape_t shape, evo_dtype_t dtype,
+                               const evo_layout_t* layout, const evo_options_t* opts, void* stream) {
+  CallOpts co;
+  if (!read_opts(opts, &co)) return EVO_ERR_BAD_ARGUMENT;
+  if (co.no_db2) return EVO_ERR_BAD_ARGUMENT;  // a backward-only option
   if (!q || !k || !v || !out || !lse) return EVO_ERR_NULL_POINTER;
   if (dtype != EVO_F16 && dtype != EVO_BF16) return EVO_ERR_BAD_DTYPE;
   evo_status_t st = check_shape(shape);
@@ -428,7 +474,7 @@ evo_status_t evo_attn_fwd_strided(const void* q, const void* k, const void* v, c
   evo_shape_t sub = shape;
   sub.B = whole ? shape.B : 1;
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  prof_record(&g_prof, 0, cs);
+  prof_record(&co.prof, 0, cs);
   for (int64_t b = 0; b < shape.B; b += sub.B) {
     const auto at = [&](const void* p, const evo_strides_t& x) {
       return static_cast<const uint8_t*>(p) + size_t(b * x.b) * 2;
@@ -438,7 +484,8 @@ evo_status_t evo_attn_fwd_strided(const void* q, const void* k, const void* v, c
     if (!map_qkv(&a.tq, at(q, t[0]), sub, bf16, rows_of(t[0], sub)) ||
         !map_qkv(&a.tk, at(k, t[1]), sub, bf16, rows_of(t[1], sub)) ||
         !map_qkv(&a.tv, at(v, t[2]), sub, bf16, rows_of(t[2], sub)) ||
-        !map_rows_half(&a.tout, at(out, t[3]), sub, bf16, rows_of(t[3], sub)))
+        !map_rows32(&a.tout, at(out, t[3]), sub, bf16, rows_of(t[3], sub)) ||
+        !map_rows_half(&a.tout_half, at(out, t[3]), sub, bf16, rows_of(t[3], sub)))
       return EVO_ERR_CUDA;
     const uint16_t* b2 = bias2 ? static_cast<const uint16_t*>(bias2) + b * shape.H * shape.L * shape.L : nullptr;
     a.bias2_mode = kBias2None;
@@ -460,45 +507,57 @@ evo_status_t evo_attn_fwd_strided(const void* q, const void* k, const void* v, c
     a.H = static_cast<int>(shape.H);
     a.D = static_cast<int>(shape.D);
     a.QT = static_cast<int>((shape.L + kTile - 1) / kTile);
-    a.items = sub.B * shape.N * shape.H * a.QT;
+    a.NP = (a.QT + 1) / 2;
+    a.items = sub.B * shape.N * shape.H * a.NP;
     a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(shape.D)));
-    a.tile_skip = g_skip_on.load() && bias1 && a.QT <= 64;
-    a.skip_at = g_skip_at.load();
-    a.wait_ns = g_wait_limit_ns.load();
-    a.status = dev->status;
+    a.tile_skip = co.skip && bias1 && a.QT <= 64;
+    a.skip_at = co.skip_at;
+    a.wait_ns = co.wait_ns;
+    a.status = co.status ? co.status : dev->status;
     const cudaError_t e = launch_fwd(a, padded_dim(shape.D), bf16, cs);
     if (e != cudaSuccess) return cuda_fail("forward launch", e);
   }
-  prof_record(&g_prof, 1, cs);
+  prof_record(&co.prof, 1, cs);
   return EVO_OK;
 }
 
 size_t evo_attn_bwd_workspace_bytes(evo_shape_t shape, evo_dtype_t dtype, int flags) {
   if (dtype != EVO_F16 && dtype != EVO_BF16) return 0;
   if (check_shape(shape) != EVO_OK) return 0;
+  if (flags & ~(EVO_WS_BIAS2 | EVO_WS_DBIAS1 | EVO_WS_NO_DBIAS2)) return 0;
   const bool b2 = (flags & EVO_WS_BIAS2) != 0, db1 = (flags & EVO_WS_DBIAS1) != 0;
+  const bool db2 = (flags & EVO_WS_NO_DBIAS2) == 0;
   // enough for the whole batch at once and for one batch at a time (strided layouts
   // whose batch and row dimensions do not merge)
   evo_shape_t one = shape;
   one.B = 1;
-  const size_t whole = ws_layout(shape, b2, db1).total, each = ws_layout(one, b2, db1).total;
+  const size_t whole = ws_layout(shape, b2, db1, db2).total, each = ws_layout(one, b2, db1, db2).total;
   return whole > each ? whole : each;
 }
+
+namespace {
+// The legacy entry points: default settings, timeouts recorded in the fallback word.
+evo_status_t bwd_impl(const void* q, const void* k, const void* v, const void* bias1, const void* bias2,
+                      const void* out, const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                      void* dbias1, void* dbias2, void* workspace, size_t workspace_bytes, evo_shape_t shape,
+                      evo_dtype_t dtype, const evo_layout_t* layout, const CallOpts& co, bool fallback_status,
+                      void* stream);
+}  // namespace
 
 evo_status_t evo_attn_bwd(const void* q, const void* k, const void* v, const void* bias1, const void* bias2,
                           const void* out, const float* lse, const void* dout, void* dq, void* dk, void* dv,
                           void* dbias2, void* workspace, size_t workspace_bytes, evo_shape_t shape,
                           evo_dtype_t dtype, void* stream) {
-  return evo_attn_bwd_strided(q, k, v, bias1, bias2, out, lse, dout, dq, dk, dv, nullptr, dbias2, workspace,
-                              workspace_bytes, shape, dtype, nullptr, stream);
+  return bwd_impl(q, k, v, bias1, bias2, out, lse, dout, dq, dk, dv, nullptr, dbias2, workspace, workspace_bytes,
+                  shape, dtype, nullptr, CallOpts{}, true, stream);
 }
 
 evo_status_t evo_attn_bwd_ex(const void* q, const void* k, const void* v, const void* bias1, const void* bias2,
                              const void* out, const float* lse, const void* dout, void* dq, void* dk, void* dv,
                              void* dbias1, void* dbias2, void* workspace, size_t workspace_bytes,
                              evo_shape_t shape, evo_dtype_t dtype, void* stream) {
-  return evo_attn_bwd_strided(q, k, v, bias1, bias2, out, lse, dout, dq, dk, dv, dbias1, dbias2, workspace,
-                              workspace_bytes, shape, dtype, nullptr, stream);
+  return bwd_impl(q, k, v, bias1, bias2, out, lse, dout, dq, dk, dv, dbias1, dbias2, workspace, workspace_bytes,
+                  shape, dtype, nullptr, CallOpts{}, true, stream);
 }
 
 evo_status_t evo_attn_bwd_strided(const void* q, const void* k, const void* v, const void* bias1,
@@ -506,11 +565,44 @@ evo_status_t evo_attn_bwd_strided(const void* q, const void* k, const void* v, c
                                   void* dk, void* dv, void* dbias1, void* dbias2, void* workspace,
                                   size_t workspace_bytes, evo_shape_t shape, evo_dtype_t dtype,
                                   const evo_layout_t* layout, void* stream) {
+  return bwd_impl(q, k, v, bias1, bias2, out, lse, dout, dq, dk, dv, dbias1, dbias2, workspace, workspace_bytes,
+                  shape, dtype, layout, CallOpts{}, true, stream);
+}
+
+evo_status_t evo_attn_bwd_opts(const void* q, const void* k, const void* v, const void* bias1, const void* bias2,
+                               const void* out, const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                               void* dbias1, void* dbias2, void* workspace, size_t workspace_bytes,
+                               evo_shape_t shape, evo_dtype_t dtype, const evo_layout_t* layout,
+                               const evo_options_t* opts, void* stream) {
+  CallOpts co;
+  if (!read_opts(opts, &co)) return EVO_ERR_BAD_ARGUMENT;
+  return bwd_impl(q, k, v, bias1, bias2, out, lse, dout, dq, dk, dv, dbias1, dbias2, workspace, workspace_bytes,
+                  shape, dtype, layout, co, false, stream);
+}
+
+evo_status_t evo_attn_bwd_status(const void* workspace, void* stream) {
+  if (!workspace) return EVO_ERR_NULL_POINTER;
+  if (!aligned(workspace, 256)) return EVO_ERR_MISALIGNED;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return EVO_ERR_CUDA;
+  int v = 0;
+  const cudaError_t e = cudaMemcpy(&v, workspace, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail("status read", e);
+  return v == 0 ? EVO_OK : EVO_ERR_DEVICE_TIMEOUT;
+}
+
+namespace {
+evo_status_t bwd_impl(const void* q, const void* k, const void* v, const void* bias1, const void* bias2,
+                      const void* out, const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                      void* dbias1, void* dbias2, void* workspace, size_t workspace_bytes, evo_shape_t shape,
+                      evo_dtype_t dtype, const evo_layout_t* layout, const CallOpts& co, bool fallback_status,
+                      void* stream) {
   if (!q || !k || !v || !out || !lse || !dout || !dq || !dk || !dv || !workspace) return EVO_ERR_NULL_POINTER;
   if (dtype != EVO_F16 && dtype != EVO_BF16) return EVO_ERR_BAD_DTYPE;
   evo_status_t st = check_shape(shape);
   if (st != EVO_OK) return st;
-  if ((bias2 != nullptr) != (dbias2 != nullptr)) return EVO_ERR_BAD_ARGUMENT;
+  if (dbias2 && !bias2) return EVO_ERR_BAD_ARGUMENT;
+  if (bias2 && !dbias2 && !co.no_db2) return EVO_ERR_BAD_ARGUMENT;
+  if (co.no_db2 && dbias2) return EVO_ERR_BAD_ARGUMENT;
   if (dbias1 && !bias1) return EVO_ERR_BAD_ARGUMENT;
   enum { Q, K, V, O, DO, DQ, DK, DV };
   evo_strides_t t[8];
@@ -533,7 +625,7 @@ evo_status_t evo_attn_bwd_strided(const void* q, const void* k, const void* v, c
   for (const evo_strides_t& x : t) whole = whole && merges(x, shape);
   evo_shape_t sub = shape;
   sub.B = whole ? shape.B : 1;
-  const WsLayout w = ws_layout(sub, bias2 != nullptr, dbias1 != nullptr);
+  const WsLayout w = ws_layout(sub, bias2 != nullptr, dbias1 != nullptr, dbias2 != nullptr);
   if (workspace_bytes < w.total) return EVO_ERR_WORKSPACE_TOO_SMALL;
   const Range ins[8] = {{q, span_bytes(t[Q], shape)},      {k, span_bytes(t[K], shape)},
                         {v, span_bytes(t[V], shape)},      {bias1, bias1 ? bias1_bytes(shape) : 0},
@@ -601,8 +693,8 @@ evo_status_t evo_attn_bwd_strided(const void* q, const void* k, const void* v, c
                same_rows(a.r_dk, packed) && same_rows(a.r_dv, packed);
     a.dbias2 = dbias2 ? static_cast<uint16_t*>(dbias2) + b2_off : nullptr;
     a.delta = reinterpret_cast<float*>(ws + w.delta);
-    a.dq_acc = reinterpret_cast<float*>(ws + w.dq_acc);
-    a.db2_part = bias2 ? reinterpret_cast<float*>(ws + w.db2) : nullptr;
+    a.dq_scr = reinterpret_cast<float*>(ws + w.dq_scr);
+    a.db2_part = dbias2 ? reinterpret_cast<float*>(ws + w.db2) : nullptr;
     if (dbias1) {
       a.dbias1 = static_cast<uint16_t*>(dbias1) + b1_off;
       a.db1p = reinterpret_cast<float*>(ws + w.db1p);
@@ -619,29 +711,28 @@ evo_status_t evo_attn_bwd_strided(const void* q, const void* k, const void* v, c
     a.D = static_cast<int>(shape.D);
     a.QT = static_cast<int>((shape.L + kTile - 1) / kTile);
     bwd_groups(sub, &a.groups, &a.group_size);
-    if (bias2 && shape.L % 4 == 0) {
+    if (dbias2 && shape.L % 4 == 0) {
       if (!map_db2_part(&a.tdb2p, a.db2_part, sub, a.groups)) return EVO_ERR_CUDA;
       a.db2p_tma = 1;
     }
     a.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(shape.D)));
     a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(shape.D)));
-    if (g_skip_on.load() && bias1 && w.can_skip) {
-      const size_t rows = size_t(sub.B) * shape.N, pairs = size_t(sub.B) * a.QT;
+    if (co.skip && bias1 && w.can_skip) {
       a.tile_skip = 1;
-      a.skip_at = g_skip_at.load();
+      a.skip_at = co.skip_at;
       a.tskip = reinterpret_cast<unsigned long long*>(ws + w.skip);
-      a.wl_n = reinterpret_cast<uint32_t*>(ws + w.skip + round256(rows * 8));
-      a.wl_cnt = a.wl_n + pairs * shape.N;
-      a.wl = a.wl_cnt + 2 * pairs + 2 * size_t(sub.B);
-      a.wl_total = a.wl + size_t(sub.B) * shape.H * a.QT * shape.N;
     }
-    a.wait_ns = g_wait_limit_ns.load();
-    a.status = dev->status;
-    const cudaError_t e = launch_bwd(a, padded_dim(shape.D), bf16, static_cast<cudaStream_t>(stream), &g_prof);
+    a.wait_ns = co.wait_ns;
+    // the call's status word: given, the workspace's own (cleared by the first kernel), or
+    // the fallback word
+    a.status = co.status ? co.status : (fallback_status ? dev->status : reinterpret_cast<int*>(ws + w.status));
+    a.clear_status = !co.status && !fallback_status && b == 0;
+    const cudaError_t e = launch_bwd(a, padded_dim(shape.D), bf16, static_cast<cudaStream_t>(stream), &co.prof);
     if (e != cudaSuccess) return cuda_fail("backward launches", e);
   }
   return EVO_OK;
 }
+}  // namespace
 
 const char* evo_attn_last_error_detail(void) { return g_detail; }
 
@@ -659,24 +750,17 @@ evo_status_t evo_attn_device_status(void* stream) {
   return EVO_OK;
 }
 
-evo_status_t evo_attn_selftest_wait_timeout(uint64_t limit_ns, void* stream) {
+evo_status_t evo_attn_selftest_wait_timeout(uint64_t limit_ns, int* status, void* stream) {
   DeviceInfo* dev = nullptr;
   evo_status_t st = check_device(&dev);
   if (st != EVO_OK) return st;
+  if (status && !aligned(status, 4)) return EVO_ERR_MISALIGNED;
   if (limit_ns < 1000) limit_ns = 1000;
   if (limit_ns > 1000000000ull) limit_ns = 1000000000ull;
-  return launch_wait_selftest(limit_ns, dev->status, static_cast<cudaStream_t>(stream)) == cudaSuccess
+  return launch_wait_selftest(limit_ns, status ? status : dev->status, static_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
              ? EVO_OK
              : EVO_ERR_CUDA;
-}
-
-void evo_attn_profile_events(void* const* events, int count) {
-  ProfileEvents p{{nullptr}, 0};
-  if (events && count > 0) {
-    p.count = count > 8 ? 8 : count;
-    for (int i = 0; i < p.count; ++i) p.ev[i] = events[i];
-  }
-  g_prof = p;
 }
 
 namespace {
@@ -729,28 +813,134 @@ evo_status_t evo_attn_step_host(const void* q, const void* k, const void* v, con
   if ((st = check_device(&dev)) != EVO_OK) return st;
   uint8_t* A = static_cast<uint8_t*>(arena);
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const size_t nq = qkv_bytes(shape);
+
+  // Chunks of rows (b, n0 .. n0+nn) so that copies overlap compute: the host-to-device
+  // copies of chunk c+1 (stream ci) run while chunk c computes (the caller's stream),
+  // and chunk c-1's results travel back (stream co).  Without a pair bias the backward
+  // runs chunk by chunk too; with one it runs once over all rows (its gradient sums
+  // over every n), and dQ, dK, dV start back as soon as its main kernel is done.
+  const int64_t slices = shape.B * shape.N * shape.H;
+  int64_t target = slices / (2 * static_cast<int64_t>(dev->sms > 0 ? dev->sms : 148));
+  target = target < 1 ? 1 : (target > 8 ? 8 : target);
+  int64_t per_b = (target + shape.B - 1) / shape.B;
+  if (per_b > shape.N) per_b = shape.N;
+  const int64_t nc = (shape.N + per_b - 1) / per_b;  // rows per chunk
+  const int64_t chunks_per_b = (shape.N + nc - 1) / nc;
+  const int64_t chunks = shape.B * chunks_per_b;
+  if (chunks > 64) return EVO_ERR_BAD_SHAPE;  // cannot happen: target <= 8 and B * ceil(8 / B) <= 8 + B
+  const bool chunk_bwd = bias2 == nullptr;
+
+  struct Res {
+    cudaStream_t ci = nullptr, co = nullptr;
+    cudaEvent_t ev[3 * 64 + 3] = {};
+    int nev = 0;
+    ~Res() {  // released once their pending work is done
+      for (int i = 0; i < nev; ++i)
+        if (ev[i]) cudaEventDestroy(ev[i]);
+      if (ci) cudaStreamDestroy(ci);
+      if (co) cudaStreamDestroy(co);
+    }
+  } r;
+  cudaError_t e = cudaStreamCreateWithFlags(&r.ci, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&r.co, cudaStreamNonBlocking);
+  const int nev = static_cast<int>(3 * chunks + 3);
+  for (int i = 0; e == cudaSuccess && i < nev; ++i) {
+    e = cudaEventCreateWithFlags(&r.ev[i], cudaEventDisableTiming);
+    r.nev = i + 1;
+  }
+  if (e != cudaSuccess) return cuda_fail("host step: streams and events", e);
+  cudaEvent_t ev_start = r.ev[0], ev_mid = r.ev[1], ev_done = r.ev[2];
+  auto ev_in = [&](int64_t c) { return r.ev[3 + 3 * c]; };
+  auto ev_fwd = [&](int64_t c) { return r.ev[3 + 3 * c + 1]; };
+  auto ev_bwd = [&](int64_t c) { return r.ev[3 + 3 * c + 2]; };
+  auto ok = [&](cudaError_t x) {
+    if (x != cudaSuccess && e == cudaSuccess) e = x;
+    return x == cudaSuccess;
+  };
+  // the arena may still be in use by earlier work on the caller's stream
+  ok(cudaEventRecord(ev_start, s));
+  ok(cudaStreamWaitEvent(r.ci, ev_start, 0));
+  ok(cudaStreamWaitEvent(r.co, ev_start, 0));
+
+  const size_t row_qkv = size_t(shape.L) * shape.H * shape.D * 2, row_b1 = size_t(shape.L) * 2;
+  const size_t row_lse = size_t(shape.H) * shape.L * 4;
   auto h2d = [&](size_t off, const void* src, size_t bytes) {
-    return cudaMemcpyAsync(A + off, src, bytes, cudaMemcpyHostToDevice, s) == cudaSuccess;
+    ok(cudaMemcpyAsync(A + off, src, bytes, cudaMemcpyHostToDevice, r.ci));
   };
   auto d2h = [&](void* dst, size_t off, size_t bytes) {
-    return cudaMemcpyAsync(dst, A + off, bytes, cudaMemcpyDeviceToHost, s) == cudaSuccess;
+    ok(cudaMemcpyAsync(dst, A + off, bytes, cudaMemcpyDeviceToHost, r.co));
   };
-  if (!h2d(L.q, q, nq) || !h2d(L.k, k, nq) || !h2d(L.v, v, nq) || !h2d(L.dout, dout, nq) ||
-      (bias1 && !h2d(L.b1, bias1, bias1_bytes(shape))) || (bias2 && !h2d(L.b2, bias2, bias2_bytes(shape))))
-    return EVO_ERR_CUDA;
-  const void* db1 = bias1 ? A + L.b1 : nullptr;
-  const void* db2 = bias2 ? A + L.b2 : nullptr;
-  st = evo_attn_fwd(A + L.q, A + L.k, A + L.v, db1, db2, A + L.out, reinterpret_cast<float*>(A + L.lse), shape,
-                    dtype, stream);
+  const auto hp = [](const void* p, size_t off) { return static_cast<const uint8_t*>(p) + off; };
+  const auto hw = [](void* p, size_t off) { return static_cast<uint8_t*>(p) + off; };
+  if (bias2) h2d(L.b2, bias2, bias2_bytes(shape));
+  for (int64_t c = 0; c < chunks; ++c) {
+    const int64_t b = c / chunks_per_b, n0 = (c % chunks_per_b) * nc;
+    const int64_t nn = shape.N - n0 < nc ? shape.N - n0 : nc;
+    const size_t row0 = size_t(b * shape.N + n0), rows = size_t(nn);
+    h2d(L.q + row0 * row_qkv, hp(q, row0 * row_qkv), rows * row_qkv);
+    h2d(L.k + row0 * row_qkv, hp(k, row0 * row_qkv), rows * row_qkv);
+    h2d(L.v + row0 * row_qkv, hp(v, row0 * row_qkv), rows * row_qkv);
+    if (bias1) h2d(L.b1 + row0 * row_b1, hp(bias1, row0 * row_b1), rows * row_b1);
+    h2d(L.dout + row0 * row_qkv, hp(dout, row0 * row_qkv), rows * row_qkv);
+    ok(cudaEventRecord(ev_in(c), r.ci));
+  }
+  for (int64_t c = 0; c < chunks && e == cudaSuccess && st == EVO_OK; ++c) {
+    const int64_t b = c / chunks_per_b, n0 = (c % chunks_per_b) * nc;
+    const int64_t nn = shape.N - n0 < nc ? shape.N - n0 : nc;
+    const size_t row0 = size_t(b * shape.N + n0), rows = size_t(nn);
+    const evo_shape_t sub{1, nn, shape.L, shape.H, shape.D};
+    uint8_t* cq = A + L.q + row0 * row_qkv;
+    uint8_t* ck = A + L.k + row0 * row_qkv;
+    uint8_t* cv = A + L.v + row0 * row_qkv;
+    uint8_t* cout = A + L.out + row0 * row_qkv;
+    uint8_t* cdo = A + L.dout + row0 * row_qkv;
+    const void* cb1 = bias1 ? A + L.b1 + row0 * row_b1 : nullptr;
+    const void* cb2 = bias2 ? A + L.b2 + size_t(b) * shape.H * shape.L * shape.L * 2 : nullptr;
+    float* clse = reinterpret_cast<float*>(A + L.lse + row0 * row_lse);
+    ok(cudaStreamWaitEvent(s, ev_in(c), 0));
+    st = evo_attn_fwd(cq, ck, cv, cb1, cb2, cout, clse, sub, dtype, stream);
+    if (st != EVO_OK) break;
+    ok(cudaEventRecord(ev_fwd(c), s));
+    if (chunk_bwd) {
+      st = evo_attn_bwd(cq, ck, cv, cb1, nullptr, cout, clse, cdo, A + L.dq + row0 * row_qkv,
+                        A + L.dk + row0 * row_qkv, A + L.dv + row0 * row_qkv, nullptr, A + L.ws, arena_bytes - L.ws,
+                        sub, dtype, stream);
+      if (st != EVO_OK) break;
+      ok(cudaEventRecord(ev_bwd(c), s));
+    }
+    ok(cudaStreamWaitEvent(r.co, ev_fwd(c), 0));
+    d2h(hw(out, row0 * row_qkv), L.out + row0 * row_qkv, rows * row_qkv);
+    if (lse) d2h(hw(lse, row0 * row_lse), L.lse + row0 * row_lse, rows * row_lse);
+    if (chunk_bwd) {
+      ok(cudaStreamWaitEvent(r.co, ev_bwd(c), 0));
+      d2h(hw(dq, row0 * row_qkv), L.dq + row0 * row_qkv, rows * row_qkv);
+      d2h(hw(dk, row0 * row_qkv), L.dk + row0 * row_qkv, rows * row_qkv);
+      d2h(hw(dv, row0 * row_qkv), L.dv + row0 * row_qkv, rows * row_qkv);
+    }
+  }
+  if (!chunk_bwd && e == cudaSuccess && st == EVO_OK) {
+    CallOpts co;
+    co.prof.count = 6;
+    co.prof.ev[5] = ev_mid;  // recorded once the main backward kernel is done
+    st = bwd_impl(A + L.q, A + L.k, A + L.v, bias1 ? A + L.b1 : nullptr, A + L.b2, A + L.out,
+                  reinterpret_cast<const float*>(A + L.lse), A + L.dout, A + L.dq, A + L.dk, A + L.dv, nullptr,
+                  A + L.db2, A + L.ws, arena_bytes - L.ws, shape, dtype, nullptr, co, true, stream);
+    if (st == EVO_OK) {
+      ok(cudaEventRecord(ev_bwd(0), s));
+      const size_t nq = qkv_bytes(shape);
+      ok(cudaStreamWaitEvent(r.co, ev_mid, 0));
+      d2h(dq, L.dq, nq);
+      d2h(dk, L.dk, nq);
+      d2h(dv, L.dv, nq);
+      ok(cudaStreamWaitEvent(r.co, ev_bwd(0), 0));
+      d2h(dbias2, L.db2, bias2_bytes(shape));
+    }
+  }
+  // the caller's stream completes with the last copy back
+  ok(cudaEventRecord(ev_done, r.co));
+  ok(cudaStreamWaitEvent(s, ev_done, 0));
   if (st != EVO_OK) return st;
-  st = evo_attn_bwd(A + L.q, A + L.k, A + L.v, db1, db2, A + L.out, reinterpret_cast<const float*>(A + L.lse),
-                    A + L.dout, A + L.dq, A + L.dk, A + L.dv, bias2 ? A + L.db2 : nullptr, A + L.ws,
-                    arena_bytes - L.ws, shape, dtype, stream);
-  if (st != EVO_OK) return st;
-  if (!d2h(out, L.out, nq) || !d2h(dq, L.dq, nq) || !d2h(dk, L.dk, nq) || !d2h(dv, L.dv, nq) ||
-      (dbias2 && !d2h(dbias2, L.db2, bias2_bytes(shape))) || (lse && !d2h(lse, L.lse, lse_bytes(shape))))
-    return EVO_ERR_CUDA;
+  if (e != cudaSuccess) return cuda_fail("host step: copies", e);
   return EVO_OK;
 }
 

@@ -23,15 +23,18 @@ enum Bias2Mode : int { kBias2None = 0, kBias2Tma = 1, kBias2Loads = 2 };
 struct FwdArgs {
   CUtensorMap tq, tk, tv;   // 4-D (D, H, L, B*N) views with the tensors' own strides, box (DP, 1, 128, 1)
   CUtensorMap tb2;          // 3-D [B*H][L][L] view, box (64, 128, 1), 128B swizzle (kBias2Tma)
-  CUtensorMap tout;         // O as the 4-D view with box (DP/2, 1, 32, 1): one softmax warp's share
+  CUtensorMap tout;         // O as the 4-D view with box (DP, 1, 32, 1): one softmax warp's 32 rows
+  CUtensorMap tout_half;    // the same with box (DP/2, 1, 32, 1) (single-tile forward)
   const uint16_t* bias1;    // [B,N,L] or nullptr
   const uint16_t* bias2;    // [B,H,L,L] or nullptr
   uint16_t* out;            // [B,N,L,H,D]
   float* lse;               // [B,N,H,L]
   int B, N, L, H, D;
   int QT;                   // ceil(L / 128)
-  long long items;          // B*H*QT*N work items, ordered (b, h, query tile, n), or with qt_fast (b, h, n, query tile)
-  int qt_fast;              // no resident pair bias: an (n, h)'s query tiles run back to back (K/V reuse in L2)
+  int NP;                   // ceil(QT / 2): pairs of query tiles
+  long long items;          // B*H*NP*N work items (query-tile pairs), ordered (b, h, pair, n), or with
+                            // qt_fast (b, h, n, pair)
+  int qt_fast;              // no resident pair bias: an (n, h)'s pairs run back to back (K/V reuse in L2)
   long long chunk;          // consecutive items per CTA
   int stages;               // depth of the K/V ring (2..4)
   int b2_resident;          // pair-bias tiles of the current (b, h, q-tile) kept in smem
@@ -63,7 +66,7 @@ struct BwdArgs {
   Rows r_dq, r_dk, r_dv;    // row strides of the plain writes of dQ, dK, dV
   int packed;               // all five of the above are packed [B*N][L][H*D]
   float* delta;             // workspace [B,N,H,L]
-  float* dq_acc;            // workspace [B,N,L,H,D]
+  float* dq_scr;            // workspace: per-key-tile kernel, L × DP fp32 dQ rows per CTA
   float* db2_part;          // workspace [G][B,H,L,L]
   uint16_t* dbias1;         // [B,N,L] or nullptr
   float* db1p;              // workspace [B*N*H][2][L]: key-mask gradient partials (per key half of the queries)
@@ -73,32 +76,24 @@ struct BwdArgs {
   int QT;
   int groups;               // G: n-groups of the pair-bias gradient
   int group_size;           // ceil(N / G)
-  long long items;          // main kernel: B*H*QT*N items (b, h, key tile, n), n fastest, or with
-                            // jt_fast (b, h, n, key tile)
-  int jt_fast;              // main kernel without resident pair-bias tiles: an (n, h)'s key tiles
-                            // run back to back, so its Q, dO and dQ accumulator stay in L2
-  long long chunk;          // main kernel: consecutive items per CTA
+  long long items;          // main kernel: B*H*N whole (b, h, n) slices
+  long long chunk;          // main kernel: consecutive slices per CTA
   int q_stages;             // main kernel: depth of the Q/dO ring
-  int b2_resident;          // main kernel: pair-bias tiles of the (b, h, key tile) group stay in smem
+  int pds_bufs;             // main kernel: P and dS shared-memory buffers (1 or 2)
   int part_stages;          // pair-bias partial kernel: depth of its ring
   int db2p_tma;             // pair-bias partial kernel: tile stores through tdb2p (L % 4 == 0)
-  int zero_dq;              // delta kernel also clears the fp32 dQ accumulator
-  // Masked key-tile skipping in the per-key-tile kernel (tile_skip; QT <= 64): the
-  // items it runs come from a work list built on the device, in item order, without the
-  // (b, n, key tile) items whose every key mask is <= skip_at (rows with no kept key skip
-  // nothing); dK and dV of the skipped key tiles are written as zeros.
+  // Masked key-tile skipping in the per-key-tile kernel (tile_skip; QT <= 64): it skips
+  // the key tiles of each slice whose every key mask is <= skip_at (rows with no kept key
+  // skip nothing); dK and dV of the skipped key tiles are written as zeros beforehand.
   int tile_skip;
   float skip_at;
   unsigned long long* tskip;  // workspace [B*N]: key tiles of each row to skip, as bits
-  uint32_t* wl_n;             // workspace [B*QT][N]: the n of each (b, key tile) that are kept
-  uint32_t* wl_cnt;           // workspace [B*QT] counts; then [B*QT] offsets within b; [B] per-b totals
-  uint32_t* wl;               // workspace [items]: the work list (item numbers, ascending)
-  uint32_t* wl_total;         // workspace: its length
   float scale;              // D^-1/2
   float scale_log2;         // D^-1/2 * log2(e)
   int bias2_mode;
   uint64_t wait_ns;
   int* status;
+  int clear_status;         // the first kernel zeroes *status (the workspace's own status word)
 };
 
 // Caller-owned CUDA events recorded around the library's launches (profiling hook).
@@ -119,6 +114,10 @@ inline void prof_record(const ProfileEvents* p, int idx, cudaStream_t st) {
   else
     cudaEventRecord(ev, st);
 }
+
+// At most this many CTAs run the per-key-tile backward kernel; the workspace holds
+// L × DP fp32 dQ rows for each.
+constexpr int kMainMaxCtas = 256;
 
 // Raise a kernel's dynamic shared-memory limit once per device (so that later
 // launches, including those under stream capture, issue nothing but the launch).
@@ -151,6 +150,8 @@ cudaError_t launch_bwd_db1_sum(const BwdArgs& a, bool bf16, cudaStream_t st);
 
 int num_sms();
 cudaError_t launch_fwd(const FwdArgs& a, int DP, bool bf16, cudaStream_t st);
+// The single-query-tile forward (DP = 64 only), for the shapes the paired kernel cannot fit.
+cudaError_t launch_fwd_single(const FwdArgs& a, bool bf16, cudaStream_t st);
 cudaError_t launch_bwd(const BwdArgs& a, int DP, bool bf16, cudaStream_t st, const ProfileEvents* prof);
 cudaError_t launch_wait_selftest(uint64_t limit_ns, int* status, cudaStream_t st);
 

@@ -9,9 +9,14 @@
 // cudaGetSymbolAddress returns for the current device.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "evo_attn.h"
+
+namespace evo {
+evo_status_t cuda_fail(const char* what, cudaError_t e);  // evo_host.cu: records the last-error text
+}
 
 namespace {
 
@@ -20,24 +25,33 @@ constexpr int kMaxDevices = 64;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[EVO_NOALLOC_SCRATCH_BYTES];
 
 struct ScratchSlot {
-  std::once_flag once;
-  void* ptr = nullptr;
-  cudaError_t err = cudaSuccess;
+  std::mutex lock;
+  std::atomic<void*> ptr{nullptr};
 };
 ScratchSlot g_slots[kMaxDevices];
 
-// Device address of the scratch array on the current device, looked up once
-// per device with that device current.
-void* scratch_on_current_device() {
+// Device address of the scratch array on the current device, looked up with that
+// device current.  Only a successful lookup is kept: a failed one (for instance the
+// device out of memory when lazy module loading reserves the array at this first
+// use) is reported and tried again by the next call.
+evo_status_t scratch_on_current_device(void** out) {
   int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return evo::cuda_fail("noalloc scratch: cudaGetDevice", e);
+  if (dev < 0 || dev >= kMaxDevices) return evo::cuda_fail("noalloc scratch: device index", cudaErrorInvalidDevice);
   ScratchSlot& s = g_slots[dev];
-  std::call_once(s.once, [&s]() {
-    void* p = nullptr;
-    s.err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (s.err == cudaSuccess) s.ptr = p;
-  });
-  return s.err == cudaSuccess ? s.ptr : nullptr;
+  void* p = s.ptr.load(std::memory_order_acquire);
+  if (!p) {
+    std::lock_guard<std::mutex> g(s.lock);
+    p = s.ptr.load(std::memory_order_relaxed);
+    if (!p) {
+      e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+      if (e != cudaSuccess) return evo::cuda_fail("noalloc scratch lookup (cudaGetSymbolAddress)", e);
+      s.ptr.store(p, std::memory_order_release);
+    }
+  }
+  *out = p;
+  return EVO_OK;
 }
 
 }  // namespace
@@ -50,10 +64,12 @@ extern "C" evo_status_t evo_attn_bwd_noalloc(const void* q, const void* k, const
   const size_t need = evo_attn_bwd_workspace_bytes(shape, dtype, bias2 != nullptr);
   if (need == 0) return EVO_ERR_BAD_SHAPE;
   if (need > EVO_NOALLOC_SCRATCH_BYTES) return EVO_ERR_SCRATCH_LIMIT;
-  void* scratch = scratch_on_current_device();
-  if (!scratch) return EVO_ERR_CUDA;
-  // The backward clears its dQ accumulator itself and overwrites every other
-  // scratch byte it reads, so stale contents from an earlier call are harmless.
+  void* scratch = nullptr;
+  const evo_status_t st = scratch_on_current_device(&scratch);
+  if (st != EVO_OK) return st;
+  // The backward writes every scratch byte before it reads it (the first key tile of a
+  // slice stores its dQ rows, later ones add to them), so stale contents from an
+  // earlier call are harmless.
   return evo_attn_bwd(q, k, v, bias1, bias2, out, lse, dout, dq, dk, dv, dbias2, scratch,
                       EVO_NOALLOC_SCRATCH_BYTES, shape, dtype, stream);
 }

@@ -90,6 +90,12 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
   if (mbar_try_wait(bar, parity)) return true;
   return mbar_wait_slow(bar, parity, g.limit_ns, g.status, g.abort);
 }
+// mbar_wait for code that a whole warp runs: every lane gets the same answer (false if
+// any lane gave up), so that no lane leaves for the error path while the others go on
+// to a warp-collective instruction.  All 32 lanes must call it together.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, const WaitGuard& g) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, g));
+}
 
 // ---------------------------------------------------------------- fences
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -508,6 +514,11 @@ __device__ __forceinline__ int next_tile(uint64_t act, int jt, int KT) {
   if (act == 0) return jt + 1 < KT ? jt + 1 : KT;
   const uint64_t rest = jt >= 63 ? 0ull : act & (~0ull << (jt + 1));
   return rest ? __ffsll(static_cast<long long>(rest)) - 1 : KT;
+}
+
+// Bring the line holding p into this SM's L1 (no completion, no registers).
+__device__ __forceinline__ void prefetch_l1(const void* p) {
+  asm volatile("prefetch.global.L1 [%0];" ::"l"(p) : "memory");
 }
 
 __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {

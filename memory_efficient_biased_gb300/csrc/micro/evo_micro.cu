@@ -205,6 +205,47 @@ __global__ void __launch_bounds__(128, 1) micro_mma(long long* cyc, int reps, in
   }
 }
 
+// ---------------------------------------------------------------- tensor-memory loads
+// Four warps (one per TMEM lane quadrant) each run `reps` rounds of `per_wait`
+// tcgen05.ld.32x32b.x32 loads followed by one tcgen05.wait::ld; the block reports the
+// cycles of warp 0 (so cycles / reps is the cost of a round: latency when per_wait = 1).
+template <int PW>
+__global__ void __launch_bounds__(128, 1) micro_tmem_ld(long long* cyc, int reps, float* sink) {
+  __shared__ uint32_t slot;
+  const int warp = threadIdx.x >> 5;
+  if (warp == 0) {
+    tmem_alloc(smem_u32(&slot), 512);
+    tmem_relinquish();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = slot + (static_cast<uint32_t>(warp * 32) << 16);
+  float acc = 0.0f;
+  __syncwarp();
+  const long long t0 = clock64();
+#pragma unroll 1
+  for (int r = 0; r < reps; ++r) {
+    uint32_t x[PW][32];
+#pragma unroll
+    for (int q = 0; q < PW; ++q) tmem_ld32(tmem + q * 32 + (r & 1) * 128, x[q]);
+#pragma unroll
+    for (int q = 0; q < PW; ++q) tmem_wait_ld(x[q]);
+#pragma unroll
+    for (int q = 0; q < PW; ++q)
+#pragma unroll
+      for (int e = 0; e < 32; e += 8) acc += __uint_as_float(x[q][e]);  // compile-time indices only
+  }
+  const long long t1 = clock64();
+  if (acc == 12345.0f) sink[threadIdx.x] = acc;
+  if (threadIdx.x == 0) cyc[blockIdx.x] = t1 - t0;
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(slot, 512);
+  }
+}
+
 template <int K>
 cudaError_t run_exp(int blocks, int iters, float* sink, long long* cyc, cudaStream_t st) {
   micro_exp<K><<<blocks, 512, 0, st>>>(sink, cyc, iters);
@@ -257,6 +298,22 @@ EVO_MICRO_API int evo_micro_exp(int kind, int blocks, int iters, void* sink, voi
     case kMix31: return run_exp<kMix31>(blocks, iters, s, c, st);
     default: return cudaErrorInvalidValue;
   }
+}
+
+// tcgen05.ld cost: `blocks` blocks (one per SM) of four warps, each round `per_wait`
+// (1, 2 or 4) x32 loads then one wait; cycles: device int64[blocks] over `reps` rounds.
+EVO_MICRO_API int evo_micro_tmem_ld(int per_wait, int blocks, int reps, void* cycles, void* sink, void* stream) {
+  long long* c = static_cast<long long*>(cycles);
+  float* s = static_cast<float*>(sink);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (blocks <= 0 || reps <= 0 || !cycles || !sink) return cudaErrorInvalidValue;
+  switch (per_wait) {
+    case 1: micro_tmem_ld<1><<<blocks, 128, 0, st>>>(c, reps, s); break;
+    case 2: micro_tmem_ld<2><<<blocks, 128, 0, st>>>(c, reps, s); break;
+    case 4: micro_tmem_ld<4><<<blocks, 128, 0, st>>>(c, reps, s); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
 }
 
 // tcgen05.mma issue cost: `blocks` blocks (one per SM), each issuing `reps` MMAs of

@@ -7,9 +7,11 @@ stream to the C ABI declared in include/evo_attn.h.  There is no CPU or
 PyTorch fallback: if the library is missing, every call raises.
 
 Names follow the C ABI: ``evo_attn_fwd``, ``evo_attn_bwd``, ``evo_attn_bwd_ex``,
-``evo_attn_fwd_strided``, ``evo_attn_bwd_strided``,
-``evo_attn_bwd_workspace_bytes``, ``evo_attn_device_status``,
-``evo_attn_set_wait_limit_ns``, ``evo_attn_selftest_wait_timeout``.
+``evo_attn_fwd_strided``, ``evo_attn_bwd_strided``, ``evo_attn_fwd_opts``,
+``evo_attn_bwd_opts``, ``evo_attn_bwd_status``, ``evo_attn_bwd_workspace_bytes``,
+``evo_attn_device_status``, ``evo_attn_selftest_wait_timeout``.  Every tensor of a
+call must live on the current CUDA device (the library launches there); a tensor
+on another device is refused with ValueError before anything reaches the library.
 """
 from __future__ import annotations
 
@@ -32,10 +34,11 @@ STATUS_NAMES = {
 }
 NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 EXPORTED = ("evo_attn_abi_version", "evo_status_string", "evo_attn_fwd", "evo_attn_bwd_workspace_bytes",
-            "evo_attn_bwd", "evo_attn_device_status", "evo_attn_set_wait_limit_ns",
-            "evo_attn_selftest_wait_timeout", "evo_attn_profile_events", "evo_attn_step_host_arena_bytes",
-            "evo_attn_step_host", "evo_attn_bwd_noalloc", "evo_attn_bwd_ex", "evo_attn_last_error_detail",
-            "evo_attn_fwd_strided", "evo_attn_bwd_strided", "evo_attn_set_masked_tile_skip")
+            "evo_attn_bwd", "evo_attn_device_status", "evo_attn_selftest_wait_timeout",
+            "evo_attn_step_host_arena_bytes", "evo_attn_step_host", "evo_attn_bwd_noalloc", "evo_attn_bwd_ex",
+            "evo_attn_last_error_detail", "evo_attn_fwd_strided", "evo_attn_bwd_strided", "evo_attn_fwd_opts",
+            "evo_attn_bwd_opts", "evo_attn_bwd_status")
+OPT_SKIP_MASKED_TILES, OPT_NO_DBIAS2 = 1, 2  # evo_options_t flags
 
 _DTYPE_CODE = {torch.float16: 0, torch.bfloat16: 1}
 
@@ -55,6 +58,38 @@ LAYOUT_FIELDS = ("q", "k", "v", "out", "dout", "dq", "dk", "dv")
 
 class EvoLayout(ctypes.Structure):
     _fields_ = [(n, EvoStrides) for n in LAYOUT_FIELDS]
+
+
+class EvoOptions(ctypes.Structure):
+    """evo_options_t: the per-call options of evo_attn_fwd_opts / evo_attn_bwd_opts."""
+    _fields_ = [("size", ctypes.c_uint32), ("flags", ctypes.c_uint32), ("skip_threshold", ctypes.c_float),
+                ("reserved", ctypes.c_uint32), ("wait_limit_ns", ctypes.c_uint64), ("status", ctypes.c_void_p),
+                ("events", ctypes.POINTER(ctypes.c_void_p)), ("num_events", ctypes.c_int32)]
+
+
+def make_options(skip_masked_tiles: bool = False, skip_threshold: float = -1.0e4, wait_limit_ns: int = 0,
+                 status: Optional[torch.Tensor] = None, events=None, no_dbias2: bool = False):
+    """An EvoOptions (and the event-handle array it points to, which the caller keeps
+    alive for the call).  ``status``: a CUDA int32 tensor of one element; ``events``:
+    torch.cuda.Event objects created with enable_timing=True."""
+    o = EvoOptions()
+    o.size = ctypes.sizeof(EvoOptions)
+    o.flags = (OPT_SKIP_MASKED_TILES if skip_masked_tiles else 0) | (OPT_NO_DBIAS2 if no_dbias2 else 0)
+    o.skip_threshold = float(skip_threshold)
+    o.wait_limit_ns = int(wait_limit_ns)
+    if status is not None:
+        if not status.is_cuda or status.dtype != torch.int32 or status.numel() < 1:
+            raise ValueError("status must be a CUDA int32 tensor")
+        o.status = status.data_ptr()
+    arr = None
+    if events:
+        for e in events:
+            if e.cuda_event == 0:  # torch creates the CUDA event lazily
+                e.record()
+        arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+        o.events = ctypes.cast(arr, ctypes.POINTER(ctypes.c_void_p))
+        o.num_events = len(events)
+    return o, arr
 
 
 class EvoAttnError(RuntimeError):
@@ -95,12 +130,8 @@ def load(path: Optional[str] = None):
     lib.evo_attn_bwd.argtypes = [vp] * 12 + [vp, sz, EvoShape, i32, vp]
     lib.evo_attn_device_status.restype = i32
     lib.evo_attn_device_status.argtypes = [vp]
-    lib.evo_attn_set_wait_limit_ns.restype = None
-    lib.evo_attn_set_wait_limit_ns.argtypes = [u64]
     lib.evo_attn_selftest_wait_timeout.restype = i32
-    lib.evo_attn_selftest_wait_timeout.argtypes = [u64, vp]
-    lib.evo_attn_profile_events.restype = None
-    lib.evo_attn_profile_events.argtypes = [ctypes.POINTER(vp), i32]
+    lib.evo_attn_selftest_wait_timeout.argtypes = [u64, vp, vp]
     lib.evo_attn_step_host_arena_bytes.restype = sz
     lib.evo_attn_step_host_arena_bytes.argtypes = [EvoShape, i32, i32, i32]
     lib.evo_attn_step_host.restype = i32
@@ -111,12 +142,18 @@ def load(path: Optional[str] = None):
     lib.evo_attn_last_error_detail.argtypes = []
     lib.evo_attn_bwd_ex.restype = i32
     lib.evo_attn_bwd_ex.argtypes = [vp] * 14 + [sz, EvoShape, i32, vp]
-    lib.evo_attn_set_masked_tile_skip.restype = None
-    lib.evo_attn_set_masked_tile_skip.argtypes = [i32, ctypes.c_float]
     lib.evo_attn_fwd_strided.restype = i32
     lib.evo_attn_fwd_strided.argtypes = [vp] * 7 + [EvoShape, i32, ctypes.POINTER(EvoLayout), vp]
     lib.evo_attn_bwd_strided.restype = i32
     lib.evo_attn_bwd_strided.argtypes = [vp] * 14 + [sz, EvoShape, i32, ctypes.POINTER(EvoLayout), vp]
+    lib.evo_attn_fwd_opts.restype = i32
+    lib.evo_attn_fwd_opts.argtypes = [vp] * 7 + [EvoShape, i32, ctypes.POINTER(EvoLayout),
+                                                 ctypes.POINTER(EvoOptions), vp]
+    lib.evo_attn_bwd_opts.restype = i32
+    lib.evo_attn_bwd_opts.argtypes = [vp] * 14 + [sz, EvoShape, i32, ctypes.POINTER(EvoLayout),
+                                                  ctypes.POINTER(EvoOptions), vp]
+    lib.evo_attn_bwd_status.restype = i32
+    lib.evo_attn_bwd_status.argtypes = [vp, vp]
     if path is None:
         _lib = lib
     return lib
@@ -129,14 +166,26 @@ def _ptr(t: Optional[torch.Tensor]):
 def _stream_ptr(stream) -> ctypes.c_void_p:
     if stream is None:
         stream = torch.cuda.current_stream()
+    elif stream.device.index != torch.cuda.current_device():
+        raise ValueError(f"stream is on cuda:{stream.device.index}, the current device is "
+                         f"cuda:{torch.cuda.current_device()}")
     return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _on_current_device(t: torch.Tensor, name: str):
+    """The library launches on the current device and addresses every buffer there."""
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    cur = torch.cuda.current_device()
+    if t.device.index != cur:
+        raise ValueError(f"{name} is on cuda:{t.device.index}, the current device is cuda:{cur}; "
+                         f"call under torch.cuda.device({t.device.index})")
 
 
 def _check(t: Optional[torch.Tensor], name: str, shape=None, dtype=None):
     if t is None:
         return
-    if not t.is_cuda:
-        raise ValueError(f"{name} must be a CUDA tensor")
+    _on_current_device(t, name)
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if shape is not None and tuple(t.shape) != tuple(shape):
@@ -154,8 +203,7 @@ def row_strided(t: torch.Tensor) -> bool:
 def _check_rows(t: Optional[torch.Tensor], name: str, shape, dtype):
     if t is None:
         return
-    if not t.is_cuda:
-        raise ValueError(f"{name} must be a CUDA tensor")
+    _on_current_device(t, name)
     if tuple(t.shape) != tuple(shape):
         raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
     if t.dtype != dtype:
@@ -207,7 +255,7 @@ def evo_attn_fwd(q, k, v, bias1=None, bias2=None, out=None, lse=None, stream=Non
     return out, lse
 
 
-WS_BIAS2, WS_DBIAS1 = 1, 2  # flags of evo_attn_bwd_workspace_bytes
+WS_BIAS2, WS_DBIAS1, WS_NO_DBIAS2 = 1, 2, 4  # flags of evo_attn_bwd_workspace_bytes
 
 
 def evo_attn_bwd_workspace_bytes(shape, dtype, has_bias2: bool, want_dbias1: bool = False) -> int:
@@ -356,32 +404,104 @@ def evo_attn_device_status(stream=None) -> int:
     return int(load().evo_attn_device_status(_stream_ptr(stream)))
 
 
-def evo_attn_set_wait_limit_ns(ns: int) -> None:
-    load().evo_attn_set_wait_limit_ns(int(ns))
+def evo_attn_selftest_wait_timeout(limit_ns: int, status: Optional[torch.Tensor] = None, stream=None) -> int:
+    """Launch the bounded-wait self-test; the timeout lands in ``status`` (a CUDA int32
+    tensor) or, without one, in the fallback word (evo_attn_device_status)."""
+    if status is not None:
+        _check(status, "status", dtype=torch.int32)
+    return int(load().evo_attn_selftest_wait_timeout(int(limit_ns), _ptr(status), _stream_ptr(stream)))
 
 
-def evo_attn_set_masked_tile_skip(enable: bool, threshold: float = -1.0e4) -> None:
-    """Masked key-tile skipping for later calls (process-wide; see include/evo_attn.h):
-    keys whose bias1 is <= threshold are masked, and 128-key tiles of a row that hold
-    only masked keys are skipped where the row keeps some key."""
-    load().evo_attn_set_masked_tile_skip(int(bool(enable)), float(threshold))
+def evo_attn_fwd_opts(q, k, v, bias1=None, bias2=None, out=None, lse=None, stream=None, *,
+                      skip_masked_tiles: bool = False, skip_threshold: float = -1.0e4, wait_limit_ns: int = 0,
+                      status: Optional[torch.Tensor] = None, events=None):
+    """evo_attn_fwd_strided with per-call options (evo_options_t): masked key-tile
+    skipping, the wait limit, a status word of the caller's and profiling events."""
+    if q.dim() != 5:
+        raise ValueError("q must be [B, N, L, H, D]")
+    B, N, L, H, D = q.shape
+    dt = q.dtype
+    if dt not in _DTYPE_CODE:
+        raise ValueError("inputs must be float16 or bfloat16")
+    if out is None:
+        out = torch.empty(q.shape, dtype=dt, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, N, H, L), dtype=torch.float32, device=q.device)
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out")):
+        _check_rows(t, n, q.shape, dt)
+    _check(bias1, "bias1", (B, N, 1, 1, L), dt)
+    _check(bias2, "bias2", (B, 1, H, L, L), dt)
+    _check(lse, "lse", (B, N, H, L), torch.float32)
+    if status is not None:
+        _check(status, "status", dtype=torch.int32)
+    lay = layout_of(q=q, k=k, v=v, out=out)
+    opts, keep = make_options(skip_masked_tiles, skip_threshold, wait_limit_ns, status, events)
+    st = load().evo_attn_fwd_opts(_ptr(q), _ptr(k), _ptr(v), _ptr(bias1), _ptr(bias2), _ptr(out), _ptr(lse),
+                                  shape_of(q), _DTYPE_CODE[dt], ctypes.byref(lay), ctypes.byref(opts),
+                                  _stream_ptr(stream))
+    del keep
+    if st != EVO_OK:
+        raise EvoAttnError(st, "evo_attn_fwd_opts")
+    return out, lse
 
 
-def evo_attn_selftest_wait_timeout(limit_ns: int, stream=None) -> int:
-    return int(load().evo_attn_selftest_wait_timeout(int(limit_ns), _stream_ptr(stream)))
+def evo_attn_bwd_opts(q, k, v, bias1, bias2, out, lse, dout, dq=None, dk=None, dv=None, dbias1=None,
+                      dbias2=None, workspace=None, stream=None, *, want_dbias1: bool = False,
+                      want_dbias2: bool = True, skip_masked_tiles: bool = False, skip_threshold: float = -1.0e4,
+                      wait_limit_ns: int = 0, status: Optional[torch.Tensor] = None, events=None):
+    """evo_attn_bwd_strided with per-call options (evo_options_t).  Without ``status``,
+    a timeout lands in the workspace's own word: read it with evo_attn_bwd_status.
+    ``want_dbias2=False`` skips the pair-bias gradient (EVO_OPT_NO_DBIAS2).
+    Returns (dq, dk, dv, dbias1, dbias2)."""
+    B, N, L, H, D = q.shape
+    dt = q.dtype
+    if dt not in _DTYPE_CODE:
+        raise ValueError("inputs must be float16 or bfloat16")
+    if want_dbias1 and bias1 is None:
+        raise ValueError("dbias1 needs bias1")
+    want_db2 = bias2 is not None and want_dbias2
+    dq = torch.empty(q.shape, dtype=dt, device=q.device) if dq is None else dq
+    dk = torch.empty(q.shape, dtype=dt, device=q.device) if dk is None else dk
+    dv = torch.empty(q.shape, dtype=dt, device=q.device) if dv is None else dv
+    if want_dbias1 and dbias1 is None:
+        dbias1 = torch.empty_like(bias1)
+    if want_db2 and dbias2 is None:
+        dbias2 = torch.empty_like(bias2)
+    if not want_db2:
+        dbias2 = None
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out"), (dout, "dout"), (dq, "dq"), (dk, "dk"), (dv, "dv")):
+        _check_rows(t, n, q.shape, dt)
+    _check(bias1, "bias1", (B, N, 1, 1, L), dt)
+    _check(bias2, "bias2", (B, 1, H, L, L), dt)
+    _check(lse, "lse", (B, N, H, L), torch.float32)
+    _check(dbias1, "dbias1", (B, N, 1, 1, L), dt)
+    _check(dbias2, "dbias2", (B, 1, H, L, L), dt)
+    if status is not None:
+        _check(status, "status", dtype=torch.int32)
+    flags = (WS_BIAS2 if bias2 is not None else 0) | (WS_DBIAS1 if dbias1 is not None else 0) | \
+        (WS_NO_DBIAS2 if bias2 is not None and not want_db2 else 0)
+    need = int(load().evo_attn_bwd_workspace_bytes(shape_of(q), _DTYPE_CODE[dt], flags))
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    _check(workspace, "workspace")
+    lay = layout_of(q=q, k=k, v=v, out=out, dout=dout, dq=dq, dk=dk, dv=dv)
+    opts, keep = make_options(skip_masked_tiles, skip_threshold, wait_limit_ns, status, events,
+                              no_dbias2=bias2 is not None and not want_db2)
+    st = load().evo_attn_bwd_opts(_ptr(q), _ptr(k), _ptr(v), _ptr(bias1), _ptr(bias2), _ptr(out), _ptr(lse),
+                                  _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dbias1), _ptr(dbias2),
+                                  _ptr(workspace), workspace.numel() * workspace.element_size(), shape_of(q),
+                                  _DTYPE_CODE[dt], ctypes.byref(lay), ctypes.byref(opts), _stream_ptr(stream))
+    del keep
+    if st != EVO_OK:
+        raise EvoAttnError(st, "evo_attn_bwd_opts")
+    return dq, dk, dv, dbias1, dbias2
 
 
-def evo_attn_profile_events(events) -> None:
-    """Record the given torch.cuda.Event objects around the library's launches
-    (see include/evo_attn.h for the index of each); ``None`` turns it off."""
-    if not events:
-        load().evo_attn_profile_events(None, 0)
-        return
-    for e in events:
-        if e.cuda_event == 0:  # torch creates the CUDA event lazily
-            e.record()
-    arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
-    load().evo_attn_profile_events(arr, len(events))
+def evo_attn_bwd_status(workspace: torch.Tensor, stream=None) -> int:
+    """Synchronise the stream and read the status word of a workspace last used by
+    evo_attn_bwd_opts (0 = ok, 8 = a device-side wait ran out)."""
+    _check(workspace, "workspace")
+    return int(load().evo_attn_bwd_status(_ptr(workspace), _stream_ptr(stream)))
 
 
 def evo_attn_step_host_arena_bytes(shape, dtype, has_bias1: bool, has_bias2: bool) -> int:

@@ -18,7 +18,7 @@ What it computes (source: the web page "DeepSpeed4Science 技术指南：AI4Scie
 * §3.7 — the forward keeps a per-row log-sum-exp (lse) in fp32; the backward
   first forms ``delta`` and then dQ, dK, dV and the gradients of both biases.
 
-Readings of points the page leaves open (each is repeated in the design doc):
+Readings of points the page leaves open:
 
 * scale s = D^-1/2 with D the true head dimension (the page only says
   "scale factor"; padding D to a multiple of 32 adds zeros and cannot change

@@ -37,7 +37,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_strings(lib):
-    assert lib.evo_attn_abi_version() == 3
+    assert lib.evo_attn_abi_version() == 4
     for code in range(13):
         s = lib.evo_status_string(code).decode()
         assert s and s != "unknown status"
@@ -121,21 +121,27 @@ def test_workspace_bytes(lib):
     s = shape(B=1, N=256, L=256, H=4, D=32)
     no_b2 = lib.evo_attn_bwd_workspace_bytes(s, 1, 0)
     with_b2 = lib.evo_attn_bwd_workspace_bytes(s, 1, 1)
+    status = 256  # the call's own status word, first
     delta = 1 * 256 * 4 * 256 * 4
-    # key-major backward (D <= 32, L <= 256): dQ stays in TMEM, no fp32 accumulator
-    assert no_b2 == delta
+    # key-major backward (D <= 32, L <= 256): dQ stays in TMEM, no fp32 rows
+    assert no_b2 == status + delta
+    # EVO_WS_NO_DBIAS2 leaves the pair-bias partial planes out (the transposed copy stays)
+    assert lib.evo_attn_bwd_workspace_bytes(s, 1, 1 | 4) == no_b2 + 1 * 4 * 256 * 256 * 2
+    assert lib.evo_attn_bwd_workspace_bytes(s, 1, 8) == 0  # unknown flag
     # with a pair bias: its transposed bf16 copy plus a whole number of fp32 [B,H,L,L] partial planes
     extra = with_b2 - no_b2 - 1 * 4 * 256 * 256 * 2
     plane = 1 * 4 * 256 * 256 * 4
     assert extra % plane == 0 and 1 <= extra // plane <= 256
-    # per-key-tile backward (D = 64, L = 384): delta, the fp32 dQ accumulator and the
-    # masked-tile work list: skip bits [B*N] u64, then u32 kept n [B*QT*N], counts and
-    # offsets [2*B*QT + 2*B], the list [items = B*H*QT*N] and its length, each part
-    # rounded up to 256 bytes
+    # per-key-tile backward (D = 64, L = 384): delta, then L × DP fp32 dQ rows for each of
+    # its CTAs (one per (b, h, n) slice here: 8 of them, at most 256) and the masked-tile
+    # skip bits [B*N] u64, each part rounded up to 256 bytes
     big = shape(B=1, N=4, L=384, H=2, D=64)
     r256 = lambda x: (x + 255) // 256 * 256
-    skip = r256(4 * 8) + r256((3 * 4 + 2 * 3 + 2 + 2 * 3 * 4 + 1) * 4)
-    assert lib.evo_attn_bwd_workspace_bytes(big, 1, 0) == 4 * 2 * 384 * 4 + 4 * 384 * 2 * 64 * 4 + skip
+    assert lib.evo_attn_bwd_workspace_bytes(big, 1, 0) == 256 + 4 * 2 * 384 * 4 + 8 * 384 * 64 * 4 + r256(4 * 8)
+    # the dQ rows are capped at 256 CTAs however many slices there are
+    many = shape(B=1, N=512, L=384, H=2, D=64)
+    assert lib.evo_attn_bwd_workspace_bytes(many, 1, 0) == (256 + 512 * 2 * 384 * 4 + 256 * 384 * 64 * 4 +
+                                                             r256(512 * 8))
     # EVO_WS_DBIAS1 adds the fp32 [B,N,H,2,L] key-mask gradient partials
     assert lib.evo_attn_bwd_workspace_bytes(s, 1, 2) - no_b2 == 1 * 256 * 4 * 2 * 256 * 4
     assert lib.evo_attn_bwd_workspace_bytes(shape(D=12), 1, 0) == 0
@@ -212,3 +218,61 @@ def test_workspace_covers_batch_by_batch(lib):
         for flags in (0, 1, 3):
             one = lib.evo_attn_bwd_workspace_bytes(shape(1, N, L, H, D), 1, flags)
             assert lib.evo_attn_bwd_workspace_bytes(shape(B, N, L, H, D), 1, flags) >= one
+
+
+def opts(**kw):
+    o = E.EvoOptions()
+    o.size = ctypes.sizeof(E.EvoOptions)
+    for k, v in kw.items():
+        setattr(o, k, v)
+    return o
+
+
+def fwd_o(lib, o, b1=None):
+    vp = ctypes.c_void_p
+    return lib.evo_attn_fwd_opts(vp(A), vp(2 * A), vp(3 * A), None if b1 is None else vp(b1), None, vp(4 * A),
+                                 vp(5 * A), shape(), 1, None, ctypes.byref(o) if o is not None else None, None)
+
+
+def bwd_o(lib, o, b2=None, db2=None, ws_flags=None):
+    vp = lambda x: None if x is None else ctypes.c_void_p(x)
+    s = shape()
+    flags = ws_flags if ws_flags is not None else int(b2 is not None)
+    need = lib.evo_attn_bwd_workspace_bytes(s, 1, flags)
+    return lib.evo_attn_bwd_opts(vp(A), vp(2 * A), vp(3 * A), None, vp(b2), vp(4 * A), vp(5 * A), vp(6 * A),
+                                 vp(7 * A), vp(8 * A), vp(9 * A), None, vp(db2), vp(16 * A), need, s, 1, None,
+                                 ctypes.byref(o) if o is not None else None, None)
+
+
+def test_options_validation(lib):
+    """evo_options_t is checked before anything else: its size, its flags, its events."""
+    reach = (6, 7, 0)  # valid arguments reach the device check
+    assert fwd_o(lib, None) in reach
+    assert fwd_o(lib, opts()) in reach
+    assert fwd_o(lib, opts(flags=1, skip_threshold=-1e4), b1=11 * A) in reach
+    small = opts()
+    small.size = 8
+    assert fwd_o(lib, small) == 10
+    assert fwd_o(lib, opts(flags=4)) == 10            # unknown flag
+    assert fwd_o(lib, opts(flags=2)) == 10            # no dbias2: a backward option
+    assert fwd_o(lib, opts(num_events=2)) == 10       # events missing
+    assert fwd_o(lib, opts(num_events=-1)) == 10
+    assert bwd_o(lib, opts()) in reach
+    # without EVO_OPT_NO_DBIAS2 a pair bias needs dbias2; with it, dbias2 must be NULL
+    assert bwd_o(lib, opts(), b2=10 * A) == 10
+    assert bwd_o(lib, opts(flags=2), b2=10 * A, ws_flags=1 | 4) in reach
+    assert bwd_o(lib, opts(flags=2), b2=10 * A, db2=12 * A) == 10
+    assert bwd_o(lib, opts(), b2=10 * A, db2=12 * A) in reach
+    # without the pair-bias gradient the smaller workspace suffices; with it, it does not
+    assert bwd_o(lib, opts(), b2=10 * A, db2=12 * A, ws_flags=1 | 4) == 5
+
+
+def test_bwd_status_validation(lib):
+    assert lib.evo_attn_bwd_status(None, None) == 1
+    assert lib.evo_attn_bwd_status(ctypes.c_void_p(A + 128), None) == 4
+
+
+def test_no_process_wide_settings(lib):
+    """The library has no setters: what a call does comes from its arguments."""
+    for name in ("evo_attn_set_wait_limit_ns", "evo_attn_set_masked_tile_skip", "evo_attn_profile_events"):
+        assert not hasattr(lib, name), name

@@ -45,10 +45,9 @@ def test_noalloc_matches_workspace_backward_twice(dtype):
         E.evo_attn_bwd_noalloc(d["q"], d["k"], d["v"], d["bias1"], d["bias2"], out, lse, d["do"], *got)
         torch.cuda.synchronize()
         assert E.evo_attn_device_status() == 0
-        # same kernels, same inputs: dK, dV and the fixed-order dbias2 are identical;
-        # dQ is summed with fp32 atomics, so compare it within the parity tolerance
-        assert torch.equal(got[1], ref[1]) and torch.equal(got[2], ref[2]) and torch.equal(got[3], ref[3])
-        assert rel_l2(np64(got[0]), np64(ref[0])) <= tol
+        # same kernels, same inputs, every gradient summed in a fixed order: identical bytes
+        for x, y in zip(got, ref):
+            assert torch.equal(x, y)
     # and both agree with the fp64 oracle
     a = {k: np64(v) for k, v in inp.items()}
     g = O.backward(a["q"], a["k"], a["v"], a["bias1"], a["bias2"], a["do"])
