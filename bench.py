@@ -699,6 +699,19 @@ def run_micro(args):
                                   "M": 128, "N": n, "K": 16, "independent_accumulators": accs,
                                   "cycles_per_mma": cpi, "flop_per_sm_per_clock": 2 * 128 * n * 16 / cpi}),
                       flush=True)
+    forms = ["A from TMEM, B MN-major 64B (forward P.V)", "A MN-major 128B, B MN-major 64B (backward dV, dK)",
+             "A K-major 128B, B MN-major 64B (backward dQ)", "A and B K-major 64B (reference)"]
+    for form, what in enumerate(forms):
+        vals = []
+        for rep in range(3):
+            rc = lib.evo_micro_mma_form(form, sms, 4096, ctypes.c_void_p(mcyc.data_ptr()),
+                                        ctypes.c_void_p(status.data_ptr()), stream)
+            torch.cuda.synchronize()
+            if rc != 0 or int(status.item()) != 0:
+                raise RuntimeError(f"micro_mma_form {form}: rc {rc} status {int(status.item())}")
+            vals.append(statistics.median(mcyc.cpu().tolist()) / 4096)
+        print(json.dumps({"micro": "mma_form", "form": what, "M": 128, "N": 32, "K": 16,
+                          "cycles_per_mma": min(vals[1:])}), flush=True)
     for pw in (1, 2, 4):
         vals = []
         for rep in range(3):
@@ -710,6 +723,23 @@ def run_micro(args):
             vals.append(statistics.median(mcyc.cpu().tolist()) / 4096)
         print(json.dumps({"micro": "tmem_ld", "loads_per_wait": pw, "columns_per_load": 32,
                           "cycles_per_round": min(vals[1:])}), flush=True)
+    modes = ["none", "TMEM loads (4 x32 per wait)", "TMEM stores (4 x16 per wait)", "TMEM loads then stores",
+             "shared-memory loads and stores", "ex2 chains"]
+    creps = [0, 3000, 3000, 2000, 3000, 600]
+    csink = torch.zeros(384, dtype=torch.float32, device="cuda")
+    for n in (32, 48):
+        for mode, what in enumerate(modes):
+            vals = []
+            for rep in range(3):
+                rc = lib.evo_micro_contend(mode, n, sms, 4096, creps[mode], ctypes.c_void_p(mcyc.data_ptr()),
+                                           ctypes.c_void_p(csink.data_ptr()), ctypes.c_void_p(status.data_ptr()),
+                                           stream)
+                torch.cuda.synchronize()
+                if rc != 0 or int(status.item()) != 0:
+                    raise RuntimeError(f"micro_contend {mode} N={n}: rc {rc} status {int(status.item())}")
+                vals.append(statistics.median(mcyc.cpu().tolist()) / 4096)
+            print(json.dumps({"micro": "mma_contend", "form": "A from TMEM, B MN-major 64B", "N": n,
+                              "other_warps": what, "cycles_per_mma": min(vals[1:])}), flush=True)
     rows = sampler.stop()
     print(json.dumps({"micro": "clocks", **summarize_clocks(rows, 0, 1e18, sampler.source)}), flush=True)
     return 0

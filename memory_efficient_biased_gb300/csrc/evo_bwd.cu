@@ -581,7 +581,8 @@ struct DqStep {
 // tile × s into dQ in the dtype.
 template <int DP, bool BF16>
 __device__ __forceinline__ bool main_consume_dq(const BwdArgs& a, const DqStep& d, uint32_t u, MainBars* bars,
-                                                uint32_t trow, int r, int hc, int lane, const WaitGuard& g) {
+                                                uint32_t trow, int r, int hc, int lane, const WaitGuard& g,
+                                                const float4 (&prev)[DP / 8]) {
   constexpr int HD = DP / 2;
   const uint32_t qb = u & 1;
   if (!mbar_wait_warp(smem_u32(&bars->dq_full[qb]), (u >> 1) & 1, g)) return false;
@@ -611,10 +612,10 @@ __device__ __forceinline__ bool main_consume_dq(const BwdArgs& a, const DqStep& 
   const int i = d.it * kTile + r;
   if (i >= a.L) return true;
   float4* acc = reinterpret_cast<float4*>(a.dq_scr + (static_cast<size_t>(blockIdx.x) * a.L + i) * DP + hc * HD);
-  if (!d.first) {
+  if (!d.first) {  // the rows' earlier sum, loaded at the start of the step
 #pragma unroll
     for (int e = 0; e < HD; e += 4) {
-      const float4 o = acc[e >> 2];
+      const float4 o = prev[e >> 2];
       v[e] += o.x;
       v[e + 1] += o.y;
       v[e + 2] += o.z;
@@ -774,10 +775,17 @@ __device__ __forceinline__ void main_compute(const BwdArgs& a, uint8_t* base, co
     if (!mbar_wait_warp(smem_u32(&bars->kv_full[kb]), (item_ctr >> 1) & 1, g)) { ok = false; break; }
     const float* b1 = reinterpret_cast<const float*>(base + lay.b1[kb]) + hc * 64;
     for (int it = 0; it < QT; ++it, ++u) {
-      // the fp32 dQ row this thread adds to at the end of the step (the previous step's),
-      // brought into L1 now so that its load does not wait on L2 then
-      if (u > 0 && !pd.first && pd.it * kTile + r < a.L)
-        prefetch_l1(a.dq_scr + (static_cast<size_t>(blockIdx.x) * a.L + pd.it * kTile + r) * DP + hc * (DP / 2));
+      // the fp32 dQ rows this thread adds to at the end of the step (the previous step's),
+      // loaded now so that their latency overlaps the step's work
+      float4 prev_acc[DP / 8];
+#pragma unroll
+      for (int e = 0; e < DP / 8; ++e) prev_acc[e] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      if (u > 0 && !pd.first && pd.it * kTile + r < a.L) {
+        const float4* src = reinterpret_cast<const float4*>(
+            a.dq_scr + (static_cast<size_t>(blockIdx.x) * a.L + pd.it * kTile + r) * DP + hc * (DP / 2));
+#pragma unroll
+        for (int e = 0; e < DP / 8; ++e) prev_acc[e] = src[e];
+      }
       if (!mbar_wait_warp(smem_u32(&bars->q_full[s]), ph, g)) { ok = false; break; }
       const float* ld = reinterpret_cast<const float*>(base + lay.ld[s]);
       const float lse2 = ld[r], dlt = ld[128 + r];
@@ -827,7 +835,7 @@ __device__ __forceinline__ void main_compute(const BwdArgs& a, uint8_t* base, co
         if (it == QT - 1) mbar_arrive(smem_u32(&bars->kv_empty[kb]));
       }
       if (u > 0) {
-        if (!main_consume_dq<DP, BF16>(a, pd, u - 1, bars, trow, r, hc, lane, g)) { ok = false; break; }
+        if (!main_consume_dq<DP, BF16>(a, pd, u - 1, bars, trow, r, hc, lane, g, prev_acc)) { ok = false; break; }
         if (it == 0 && !main_write_dkdv<DP, BF16>(a, pk, item_ctr - 1, bars, trow, r, hc, lane, g)) {
           ok = false;
           break;
@@ -842,7 +850,16 @@ __device__ __forceinline__ void main_compute(const BwdArgs& a, uint8_t* base, co
     pk = KvItem{cur.b, cur.n, cur.h, cur.jt};
   }
   if (ok && u > 0) {
-    if (main_consume_dq<DP, BF16>(a, pd, u - 1, bars, trow, r, hc, lane, g))
+    float4 prev_acc[DP / 8];
+#pragma unroll
+    for (int e = 0; e < DP / 8; ++e) prev_acc[e] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    if (!pd.first && pd.it * kTile + r < a.L) {
+      const float4* src = reinterpret_cast<const float4*>(
+          a.dq_scr + (static_cast<size_t>(blockIdx.x) * a.L + pd.it * kTile + r) * DP + hc * (DP / 2));
+#pragma unroll
+      for (int e = 0; e < DP / 8; ++e) prev_acc[e] = src[e];
+    }
+    if (main_consume_dq<DP, BF16>(a, pd, u - 1, bars, trow, r, hc, lane, g, prev_acc))
       main_write_dkdv<DP, BF16>(a, pk, item_ctr - 1, bars, trow, r, hc, lane, g);
   }
 }

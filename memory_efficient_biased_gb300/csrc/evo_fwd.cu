@@ -43,17 +43,31 @@ namespace {
 
 constexpr int kMaxStages = 4;
 constexpr int kSoftmaxWarps = 8;
-constexpr int kThreads = (kSoftmaxWarps + 2) * 32;
+// Three warpgroups: two of softmax warps, and one holding the producer and MMA warps
+// (its other two warps idle).  Launched at 168 registers a thread (three warps share
+// each scheduler's 16K registers); the third warpgroup then gives registers back so
+// that the softmax warps can hold a whole row of scores:
+// 128 x 104 + 256 x 200 = 384 x 168.
+constexpr int kThreads = (kSoftmaxWarps + 4) * 32;
 constexpr int kProducerWarp = kSoftmaxWarps, kMmaWarp = kSoftmaxWarps + 1;
+constexpr uint32_t kRegsLaunch = 168, kRegsSoftmax = 200, kRegsOther = 104;
+static_assert(128 * kRegsOther + 256 * kRegsSoftmax <= kThreads * kRegsLaunch, "register split exceeds the launch");
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.0f;     // the reference max moves only past this margin
 
 // TMEM columns of query tile g: S (128 fp32), P (64 columns of packed pairs; keys
-// 2c, 2c+1 in column c), O (DP fp32).
+// 2c, 2c+1 in column c), O (DP fp32, then, for DP <= 32, 16 columns that each hold
+// the row sum of P: the P·V MMA multiplies P by V with 16 columns of ones appended,
+// which costs nothing at these widths, as an MMA with N <= 64 takes as long as one
+// with N = 16).
 __device__ __forceinline__ uint32_t col_s(uint32_t g) { return g * 256u; }
 __device__ __forceinline__ uint32_t col_p(uint32_t g) { return g * 256u + 128u; }
 __device__ __forceinline__ uint32_t col_o(uint32_t g) { return g * 256u + 192u; }
+template <int DP>
+constexpr bool kOnes = DP <= 32;
+template <int DP>
+constexpr int kOCols = kOnes<DP> ? DP + 16 : DP;
 
 // Pair-bias handling: none, resident per (b, h, pair) group, or streamed per key tile.
 enum B2Kind : int { kB2None = 0, kB2Resident = 1, kB2Stream = 2 };
@@ -83,7 +97,7 @@ template <int DP>
 struct FwdLayout {
   static constexpr uint32_t kTB = kTile * DP * 2;
   Ring q, k, v, b1, b2s;
-  uint32_t b2r, stg, bars, total;
+  uint32_t b2r, stg, ones, bars, total;
   // q[2 * buffer + g]; b2s[stage] + g * 32768; b2r + (g * KT + jt) * 32768
   __host__ __device__ FwdLayout(int b2kind, int stages, int KT) {
     uint32_t off = 0;
@@ -98,6 +112,9 @@ struct FwdLayout {
     off += stages * 2 * kTB;
     stg = off;  // O staging: per softmax warp [32 rows][DP] (row swizzle = 2 DP bytes)
     off += kSoftmaxWarps * 32u * DP * 2u;
+    off = (off + 1023u) & ~1023u;
+    ones = off;  // 128 rows of ones, read as V's extra columns by the P·V MMA
+    if (kOnes<DP>) off += kTile * DP * 2u;
     b1 = Ring{off, 512u};
     off += stages * 512u;
     bars = off;
@@ -149,7 +166,7 @@ struct ItemIter {
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns, int* status) {
   volatile int never = 0;
   WaitGuard g{limit_ns, status, &never};
-  mbar_wait(bar, parity, g);
+  mbar_wait_inl(bar, parity, g);
 }
 
 // Pair-bias tile (query rows i0.., key columns j0..) by plain loads into the
@@ -207,7 +224,7 @@ __device__ __forceinline__ void fwd_producer(const FwdArgs& a, uint8_t* base, co
     nc.next(a);
     if (B2 == kB2Resident && (item == i0 || c.n == 0)) {
       // every softmax warp is done with the previous group's tiles
-      if (!mbar_wait_warp(smem_u32(&bars->b2_empty), (grp_it & 1) ^ 1, g)) { ok = false; break; }
+      if (!mbar_wait_warp_inl(smem_u32(&bars->b2_empty), (grp_it & 1) ^ 1, g)) { ok = false; break; }
       const uint32_t full = smem_u32(&bars->b2_full);
       for (int gq = 0; gq < 2; ++gq) {
         const int qt = 2 * c.p + gq;
@@ -230,7 +247,7 @@ __device__ __forceinline__ void fwd_producer(const FwdArgs& a, uint8_t* base, co
       ++grp_it;
     }
     const uint32_t qb = q_it & 1;
-    if (!mbar_wait_warp(smem_u32(&bars->q_empty[qb]), ((q_it >> 1) & 1) ^ 1, g)) { ok = false; break; }
+    if (!mbar_wait_warp_inl(smem_u32(&bars->q_empty[qb]), ((q_it >> 1) & 1) ^ 1, g)) { ok = false; break; }
     if (lane == 0) {
       const uint32_t full = smem_u32(&bars->q_full[qb]);
       mbar_arrive_expect_tx(full, 2 * kTB);
@@ -248,7 +265,7 @@ __device__ __forceinline__ void fwd_producer(const FwdArgs& a, uint8_t* base, co
     const int jt0 = next_tile(act, -1, KT);
     for (int jt = jt0; jt < KT; ++u) {
       const int jn = next_tile(act, jt, KT);
-      if (!mbar_wait_warp(smem_u32(&bars->kv_empty[s]), ph ^ 1, g)) { ok = false; break; }
+      if (!mbar_wait_warp_inl(smem_u32(&bars->kv_empty[s]), ph ^ 1, g)) { ok = false; break; }
       const uint32_t full = smem_u32(&bars->kv_full[s]);
       if (lane == 0) {  // copies first: the key-mask conversion below must not delay them
         bars->tile_meta[s] = static_cast<uint32_t>(jt) | (jt == jt0 ? kTileFirst : 0u) | (jn >= KT ? kTileLast : 0u);
@@ -305,20 +322,24 @@ __device__ __forceinline__ void fwd_producer(const FwdArgs& a, uint8_t* base, co
 }
 
 // ------------------------------------------------------------ MMA issuer (one thread)
-// O_g (+)= P_g · V (K = 128 keys, P from TMEM) for key tile number v (across items),
-// stage sv, tag meta; first tile of an item: wait for the epilogue to have read O_g.
+// O_g (+)= P_g · [V | 1] (K = 128 keys, P from TMEM) for key tile number v (across
+// items), stage sv, tag meta; first tile of an item: wait for the epilogue to have
+// read O_g.  V is MN-major: its DP columns are one swizzle atom, and the ones block
+// stands in as the next atom (leading byte offset = its distance from the stage).
 template <int DP, bool BF16>
 __device__ __forceinline__ bool fwd_issue_pv(uint32_t g, uint32_t v, uint32_t sv, uint32_t meta, uint32_t item_ord,
                                              uint8_t* base, const FwdLayout<DP>& lay, FwdBars* bars, uint32_t tmem,
                                              const WaitGuard& gd) {
   constexpr uint32_t RB = DP * 2;
   constexpr uint32_t SWZ = swizzle_for_row(RB);
-  constexpr uint32_t id_o = idesc_f16(128, DP, BF16, false, true);
-  if (!mbar_wait(smem_u32(&bars->p_full[g]), v & 1, gd)) return false;
+  constexpr uint32_t id_o = idesc_f16(128, kOCols<DP>, BF16, false, true);
+  if (!mbar_wait_inl(smem_u32(&bars->p_full[g]), v & 1, gd)) return false;
   const bool first = (meta & kTileFirst) != 0;
-  if (first && !mbar_wait(smem_u32(&bars->o_free[g]), (item_ord & 1) ^ 1, gd)) return false;
+  if (first && !mbar_wait_inl(smem_u32(&bars->o_free[g]), (item_ord & 1) ^ 1, gd)) return false;
   tc_fence_after();
-  const uint64_t vd = smem_desc(smem_u32(base + lay.v[sv]), kTile * RB, 8 * RB, SWZ);
+  const uint32_t va = smem_u32(base + lay.v[sv]);
+  const uint32_t lbo = kOnes<DP> ? smem_u32(base + lay.ones) - va : kTile * RB;
+  const uint64_t vd = smem_desc(va, lbo, 8 * RB, SWZ);
 #pragma unroll
   for (int k = 0; k < 8; ++k)  // 128 keys in steps of 16 (8 TMEM columns of packed pairs)
     umma_ts(tmem + col_o(g), tmem + col_p(g) + k * 8, vd + k * 16 * RB / 16, id_o, (!first || k > 0) ? 1u : 0u);
@@ -326,6 +347,8 @@ __device__ __forceinline__ bool fwd_issue_pv(uint32_t g, uint32_t v, uint32_t sv
   return true;
 }
 
+// Per key tile: S of both query tiles as soon as each group has loaded its previous
+// S (s_free), then both groups' P·V of the previous key tile as their P arrives.
 template <int DP, bool BF16, bool SKIP>
 __device__ __forceinline__ void fwd_mma(const FwdArgs& a, uint8_t* base, const FwdLayout<DP>& lay, FwdBars* bars,
                                         uint32_t tmem, const WaitGuard& g, long long i0, long long i1) {
@@ -338,29 +361,28 @@ __device__ __forceinline__ void fwd_mma(const FwdArgs& a, uint8_t* base, const F
   bool ok = true;
   for (long long item = i0; ok && item < i1; ++item, ++item_ord) {
     const uint32_t qb = q_it & 1;
-    if (!mbar_wait(smem_u32(&bars->q_full[qb]), (q_it >> 1) & 1, g)) { ok = false; break; }
+    if (!mbar_wait_inl(smem_u32(&bars->q_full[qb]), (q_it >> 1) & 1, g)) { ok = false; break; }
     ++q_it;
     tc_fence_after();
     for (int x = 0; SKIP || x < KT; ++x) {  // with SKIP, up to the tile tagged last
-      if (!mbar_wait(smem_u32(&bars->kv_full[s]), ph, g)) { ok = false; break; }
+      if (!mbar_wait_inl(smem_u32(&bars->kv_full[s]), ph, g)) { ok = false; break; }
       const uint32_t meta = SKIP ? bars->tile_meta[s] : tile_meta_all(x, KT);
       const bool last = (meta & kTileLast) != 0;
       const uint64_t kd = smem_desc(smem_u32(base + lay.k[s]), 16, 8 * RB, SWZ);
       for (uint32_t gq = 0; gq < 2; ++gq) {
-        // S_g of this tile once the group has decided its previous tile
-        if (!mbar_wait(smem_u32(&bars->s_free[gq]), (u & 1) ^ 1, g)) { ok = false; break; }
+        // S_g of this tile once the group has loaded its previous S
+        if (!mbar_wait_inl(smem_u32(&bars->s_free[gq]), (u & 1) ^ 1, g)) { ok = false; break; }
         tc_fence_after();
         const uint64_t qd = smem_desc(smem_u32(base + lay.q[2 * qb + gq]), 16, 8 * RB, SWZ);
 #pragma unroll
         for (int k = 0; k < DP / 16; ++k) umma_ss(tmem + col_s(gq), qd + k * 2, kd + k * 2, id_s, k > 0);
         umma_commit(smem_u32(&bars->s_full[gq]));
-        if (gq == 1 && last) umma_commit(smem_u32(&bars->q_empty[qb]));
-        // the group's P·V of the previous key tile
-        if (u > 0 && !fwd_issue_pv<DP, BF16>(gq, u - 1, prev_stage, prev_meta, prev_item, base, lay, bars, tmem, g)) {
-          ok = false;
-          break;
-        }
       }
+      if (!ok) break;
+      if (last) umma_commit(smem_u32(&bars->q_empty[qb]));
+      // both groups' P·V of the previous key tile
+      for (uint32_t gq = 0; ok && u > 0 && gq < 2; ++gq)
+        ok = fwd_issue_pv<DP, BF16>(gq, u - 1, prev_stage, prev_meta, prev_item, base, lay, bars, tmem, g);
       if (!ok) break;
       if (u > 0) umma_commit(smem_u32(&bars->kv_empty[prev_stage]));
       prev_stage = s;
@@ -416,62 +438,34 @@ __device__ __forceinline__ void chunk_scores(uint32_t (&sr)[32], const float* b1
   mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
 }
 
-// P = 2^(y - m) for one chunk (y as fp32 bits), packed into pp[0..15]; row sum into rs.
-template <bool BF16>
-__device__ __forceinline__ void chunk_probs(const uint32_t (&y)[32], float m, uint32_t* pp, float2& rs0, float2& rs1) {
+// P = 2^(y - m) for one chunk (y as fp32 bits), packed into pp[0..15]; with ROWSUM,
+// also the row sum into rs (otherwise the P·V MMA forms it).
+template <bool BF16, bool ROWSUM>
+__device__ __forceinline__ void chunk_probs(const uint32_t (&y)[32], float m, uint32_t (&pp)[16], float2& rs) {
   const float2 nm2 = make_float2(-m, -m);
 #pragma unroll
-  for (int x = 0; x < 32; x += 4) {
-    const float2 t0 = add2(make_float2(__uint_as_float(y[x]), __uint_as_float(y[x + 1])), nm2);
-    const float2 t1 = add2(make_float2(__uint_as_float(y[x + 2]), __uint_as_float(y[x + 3])), nm2);
-    const float p0 = ex2(t0.x), p1 = ex2(t0.y), p2 = ex2(t1.x), p3 = ex2(t1.y);
-    rs0 = add2(rs0, make_float2(p0, p1));
-    rs1 = add2(rs1, make_float2(p2, p3));
+  for (int x = 0; x < 32; x += 2) {
+    const float2 t = add2(make_float2(__uint_as_float(y[x]), __uint_as_float(y[x + 1])), nm2);
+    const float p0 = ex2(t.x), p1 = ex2(t.y);
+    if (ROWSUM) rs = add2(rs, make_float2(p0, p1));
     pp[x >> 1] = pack2<BF16>(p0, p1);
-    pp[(x >> 1) + 1] = pack2<BF16>(p2, p3);
   }
 }
 
-// The whole tile (128 keys) of this thread's row from S in TMEM, and the tile's max into
-// mt.  With `use_m`, also P against reference m, written to the group's P columns of TMEM
-// every two chunks (the caller has waited until the previous tile's P·V read them), and
-// the row sum into rs.  The TMEM accesses are warp-collective: use_m must be the same in
-// every lane.
-template <bool BF16, bool HAS_B2>
-__device__ __forceinline__ void tile_pass(uint32_t scol, uint32_t pcol, const float* b1, const uint8_t* b2t, int r,
-                                          float2 sl2, float m, bool use_m, float& mt, float& rs) {
-  float2 rs0 = make_float2(0.0f, 0.0f), rs1 = make_float2(0.0f, 0.0f);
-  // Chunk c+1's TMEM load is in flight while chunk c is computed (one load outstanding
-  // at a time, so each wait covers exactly the chunk about to be used).
-  uint32_t sa[32], sb[32], pp[32];
-  auto chunk = [&](uint32_t (&sr)[32], int c) {
-    chunk_scores<BF16, HAS_B2>(sr, b1 + c * 32, b2t + (c >> 1) * 16384, (c & 1) * 4, r, sl2, mt);
-    if (use_m) chunk_probs<BF16>(sr, m, pp + (c & 1) * 16, rs0, rs1);
-  };
-  tmem_ld32(scol, sa);
-  tmem_wait_ld(sa);
-  tmem_ld32(scol + 32, sb);
-  chunk(sa, 0);
-  tmem_wait_ld(sb);
-  tmem_ld32(scol + 64, sa);
-  chunk(sb, 1);
-  if (use_m) tmem_st32(pcol, pp);
-  tmem_wait_ld(sa);
-  tmem_ld32(scol + 96, sb);
-  chunk(sa, 2);
-  tmem_wait_ld(sb);
-  chunk(sb, 3);
-  if (use_m) tmem_st32(pcol + 32, pp);
-  rs = (rs0.x + rs0.y) + (rs1.x + rs1.y);
-}
-
 // O = acc / l and lse for a finished item: this warp's 32 rows of query tile g through
-// shared memory with one TMA tile store.  (m: reference max in log2 units; l: row sum.)
+// shared memory with one TMA tile store.  (m: reference max in log2 units; l: row sum,
+// read from the ones columns of the accumulator where the MMA forms it.)
 template <int DP, bool BF16>
 __device__ __forceinline__ void fwd_epilogue(const FwdArgs& a, const ItemIter& c, uint32_t g, float m, float l,
                                              uint8_t* base, const FwdLayout<DP>& lay, FwdBars* bars, uint32_t trow,
                                              int wq, int r, int lane) {
   constexpr int PC = DP < 32 ? DP : 32;  // columns per TMEM load
+  if constexpr (kOnes<DP>) {
+    uint32_t x[16];
+    tmem_ld16(trow + col_o(g) + DP, x);
+    tmem_wait_ld(x);
+    l = __uint_as_float(x[0]);
+  }
   const float inv = l > 0.0f ? 1.0f / l : 0.0f;
   uint8_t* blk = base + lay.stg + (g * 4 + wq) * 32 * DP * 2;
   if (lane == 0) bulk_wait_read_all();  // this warp's previous store has read the staging block
@@ -511,20 +505,40 @@ __device__ __forceinline__ void fwd_epilogue(const FwdArgs& a, const ItemIter& c
   if (i < a.L) a.lse[(bn * a.H + c.h) * a.L + i] = l > 0.0f ? (m + lg2(l)) * kLn2 : -INFINITY;
 }
 
+// Scales this thread's row of the O accumulator (with its row-sum columns) by alpha.
+// Warp-collective.
+template <int DP>
+__device__ __forceinline__ void rescale_o(uint32_t ocol, float alpha) {
+#pragma unroll 1
+  for (int c = 0; c < kOCols<DP> / 16; ++c) {
+    uint32_t xo[16];
+    tmem_ld16(ocol + c * 16, xo);
+    tmem_wait_ld(xo);
+#pragma unroll
+    for (int e = 0; e < 16; ++e) xo[e] = __float_as_uint(__uint_as_float(xo[e]) * alpha);
+    tmem_st16(ocol + c * 16, xo);
+  }
+}
+
+// Per key tile: load the row's 128 scores from TMEM into registers (S is then free
+// for the next tile's scores), apply scale and biases, take the tile max, move the
+// reference if needed, and write P = 2^(y - m) to TMEM for the P·V MMA.
 template <int DP, bool BF16, int B2, bool SKIP>
 __device__ __forceinline__ void fwd_softmax(const FwdArgs& a, uint8_t* base, const FwdLayout<DP>& lay,
                                             FwdBars* bars, uint32_t tmem, const WaitGuard& g, long long i0,
                                             long long i1) {
   constexpr bool kHasB2 = B2 != kB2None;
+  constexpr bool kRowSum = !kOnes<DP>;
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t grp = static_cast<uint32_t>(w >> 2);  // query tile of the item
   const int wq = w & 3;                                 // TMEM lane quadrant
   const int r = wq * 32 + lane;                         // query row within the tile == TMEM lane
   const uint32_t trow = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+  const uint32_t scol = trow + col_s(grp), pcol = trow + col_p(grp), ocol = trow + col_o(grp);
   const float2 sl2 = make_float2(a.scale_log2, a.scale_log2);
   const int S = a.stages, KT = a.QT;
   uint32_t u = 0, grp_it = 0, s = 0, ph = 0;
-  float m = 0.0f, l = 0.0f;  // reference max (log2 units) and row sum
+  float m = 0.0f, l = 0.0f;  // reference max (log2 units); row sum (kept here only without ones columns)
   bool have = false;         // a finite reference exists (until then every P is 0)
   ItemIter cur, prev;
   cur.init(i0, a);
@@ -537,7 +551,7 @@ __device__ __forceinline__ void fwd_softmax(const FwdArgs& a, uint8_t* base, con
     }
     const bool grp_last = item + 1 == i1 || cur.n == a.N - 1;
     if (B2 == kB2Resident && (item == i0 || cur.n == 0)) {
-      if (!mbar_wait_warp(smem_u32(&bars->b2_full), grp_it & 1, g)) { ok = false; break; }
+      if (!mbar_wait_warp_inl(smem_u32(&bars->b2_full), grp_it & 1, g)) { ok = false; break; }
       ++grp_it;
     }
     float m_fin = 0.0f, l_fin = 0.0f;  // the previous item's statistics, for its epilogue
@@ -547,84 +561,78 @@ __device__ __forceinline__ void fwd_softmax(const FwdArgs& a, uint8_t* base, con
         m_fin = have ? m : 0.0f;
         l_fin = l;
         have = false;
+        m = 0.0f;
         l = 0.0f;
       }
-      if (!mbar_wait_warp(smem_u32(&bars->kv_full[s]), ph, g)) { ok = false; break; }
+      if (!mbar_wait_warp_inl(smem_u32(&bars->kv_full[s]), ph, g)) { ok = false; break; }
       const uint32_t meta = SKIP ? bars->tile_meta[s] : tile_meta_all(x, KT);
       const int jt = static_cast<int>(meta & 0xffffu);
       const bool last = (meta & kTileLast) != 0;
-      if (!mbar_wait_warp(smem_u32(&bars->s_full[grp]), u & 1, g)) { ok = false; break; }
+      if (!mbar_wait_warp_inl(smem_u32(&bars->s_full[grp]), u & 1, g)) { ok = false; break; }
       tc_fence_after();
       const float* b1 = reinterpret_cast<const float*>(base + lay.b1[s]);
       const uint8_t* b2t =
           base + (B2 == kB2Resident ? lay.b2r + (grp * KT + jt) * 32768u : lay.b2s[s] + grp * 32768u);
-      const uint32_t scol = trow + col_s(grp), pcol = trow + col_p(grp);
-      const uint32_t pe_bar = smem_u32(&bars->p_empty[grp]), pe = (u & 1) ^ 1;  // previous P·V done
-      // First pass over the tile against the current reference (a row without one yet
-      // only takes the tile max).  The whole warp writes P when any row has a reference.
-      // Rare second pass (but always for the first tile of an item): where a row has no
-      // reference yet, or its tile max passes the margin, the whole warp recomputes the
-      // tile from S (still in TMEM) with each row's new reference (rows that need nothing
-      // keep theirs and write the same P again); the accumulator of the previous tiles is
-      // rescaled once their P·V is done.
-      float mt = -INFINITY, rs = 0.0f, mref = have ? m : 0.0f, alpha = 1.0f;
-      bool use_m = __any_sync(0xffffffffu, have), waited = false, need = false, fresh = false;
-#pragma unroll 1
-      for (int pass = 0; pass < 2; ++pass) {
-        if (use_m && !waited) {  // P goes to TMEM once the previous tile's P·V has read it
-          if (!mbar_wait_warp(pe_bar, pe, g)) { ok = false; break; }
-          tc_fence_after();
-          waited = true;
-        }
-        float mp = -INFINITY, rp = 0.0f;
-        tile_pass<BF16, kHasB2>(scol, pcol, b1, b2t, r, sl2, mref, use_m, mp, rp);
-        if (pass == 1) {
-          rs = rp;
-          break;
-        }
-        mt = mp;
-        rs = have ? rp : 0.0f;
-        need = !have || mt > m + kRescaleLog2;
-        if (!__any_sync(0xffffffffu, need)) break;
-        fresh = !have;  // nothing accumulated for this row yet
-        mref = need ? (mt == -INFINITY ? (fresh ? 0.0f : m) : mt) : m;
-        alpha = (need && !fresh) ? ex2(m - mref) : 1.0f;
-        use_m = true;
-      }
-      if (!ok) break;
-      // every lane votes (a warp-collective vote must not be skipped by any lane)
-      const bool any_need = __any_sync(0xffffffffu, need);
-      if (any_need) {
-        if (!first && __any_sync(0xffffffffu, need && !fresh)) {
-          // p_empty (the previous P·V done) was waited for before the second pass
-#pragma unroll 1
-          for (int c = 0; c < DP / 16; ++c) {
-            uint32_t xo[16];
-            tmem_ld16(trow + col_o(grp) + c * 16, xo);
-            tmem_wait_ld(xo);
-#pragma unroll
-            for (int e = 0; e < 16; ++e) xo[e] = __float_as_uint(__uint_as_float(xo[e]) * alpha);
-            tmem_st16(trow + col_o(grp) + c * 16, xo);
-          }
-        }
-        if (need) {
-          l *= fresh ? 0.0f : alpha;
-          m = mref;
-          have = have || mt != -INFINITY;
-        }
-      }
-      l += rs;
-      tmem_wait_st();
-      // S of this tile and the stage's bias data are no longer read by this warp; P is in TMEM
+      // S: two chunks, then the other two in flight while the first two are scored
+      uint32_t y0[32], y1[32], y2[32], y3[32];
+      float mt = -INFINITY;
+      tmem_ld32(scol, y0);
+      tmem_ld32(scol + 32, y1);
+      tmem_wait_ld(y0);
+      tmem_wait_ld(y1);
+      tmem_ld32(scol + 64, y2);
+      tmem_ld32(scol + 96, y3);
+      chunk_scores<BF16, kHasB2>(y0, b1, b2t, 0, r, sl2, mt);
+      chunk_scores<BF16, kHasB2>(y1, b1 + 32, b2t, 4, r, sl2, mt);
+      tmem_wait_ld(y2);
+      tmem_wait_ld(y3);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(smem_u32(&bars->s_free[grp]));
+      if (lane == 0) mbar_arrive(smem_u32(&bars->s_free[grp]));  // S may be overwritten
+      chunk_scores<BF16, kHasB2>(y2, b1 + 64, b2t + 16384, 0, r, sl2, mt);
+      chunk_scores<BF16, kHasB2>(y3, b1 + 96, b2t + 16384, 4, r, sl2, mt);
+      __syncwarp();
+      if (lane == 0) {  // the stage's bias data are no longer read by this warp
         mbar_arrive(smem_u32(&bars->kv_empty[s]));
         if (B2 == kB2Resident && grp_last && last) mbar_arrive(smem_u32(&bars->b2_empty));
-        mbar_arrive(smem_u32(&bars->p_full[grp]));
       }
-      // the previous item's epilogue: its last P·V is done (p_empty above)
+      // The reference moves to the tile max where the row has none yet, or where the
+      // tile max passes it by more than the margin (P then stays below 2^8).
+      bool resc = false;
+      float alpha = 1.0f;
+      if (mt != -INFINITY && (!have || mt > m + kRescaleLog2)) {
+        resc = have;
+        alpha = have ? ex2(m - mt) : 1.0f;
+        m = mt;
+        have = true;
+      }
+      // P goes to TMEM once the previous tile's P·V has read it (and, on the first tile
+      // of an item, the previous item's O is complete)
+      if (!mbar_wait_warp_inl(smem_u32(&bars->p_empty[grp]), (u & 1) ^ 1, g)) { ok = false; break; }
+      tc_fence_after();
+      float2 rs = make_float2(0.0f, 0.0f);
+      uint32_t pp[16];
+      chunk_probs<BF16, kRowSum>(y0, m, pp, rs);
+      tmem_st16(pcol, pp);
+      chunk_probs<BF16, kRowSum>(y1, m, pp, rs);
+      tmem_st16(pcol + 16, pp);
+      chunk_probs<BF16, kRowSum>(y2, m, pp, rs);
+      tmem_st16(pcol + 32, pp);
+      chunk_probs<BF16, kRowSum>(y3, m, pp, rs);
+      tmem_st16(pcol + 48, pp);
+      // The accumulator of the previous tiles (complete: p_empty) is rescaled before this
+      // tile's P·V adds to it (that P·V waits for p_full below).
+      if (!first && __any_sync(0xffffffffu, resc)) {
+        rescale_o<DP>(ocol, alpha);
+        l *= alpha;
+      }
+      if (kRowSum) l += rs.x + rs.y;
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bars->p_full[grp]));
+      // The previous item's O is complete (p_empty above); this item's first P·V, which
+      // overwrites it, waits for the epilogue (o_free).
       if (first && item > i0) fwd_epilogue<DP, BF16>(a, prev, grp, m_fin, l_fin, base, lay, bars, trow, wq, r, lane);
       ++u;
       if (++s == static_cast<uint32_t>(S)) {
@@ -636,7 +644,7 @@ __device__ __forceinline__ void fwd_softmax(const FwdArgs& a, uint8_t* base, con
   }
   if (ok && u > 0) {
     // the last item: its last P·V
-    if (mbar_wait_warp(smem_u32(&bars->p_empty[grp]), ((u - 1) & 1), g)) {
+    if (mbar_wait_warp_inl(smem_u32(&bars->p_empty[grp]), ((u - 1) & 1), g)) {
       tc_fence_after();
       fwd_epilogue<DP, BF16>(a, cur, grp, have ? m : 0.0f, l, base, lay, bars, trow, wq, r, lane);
     }
@@ -684,17 +692,27 @@ __global__ void __launch_bounds__(kThreads, 1) evo_fwd_kernel(const __grid_const
     tmem_alloc(smem_u32(&bars->tmem_slot), 512);
     tmem_relinquish();
   }
+  if constexpr (kOnes<DP>) {  // the row-sum columns' operand: every element 1.0
+    const uint32_t one2 = BF16 ? 0x3F803F80u : 0x3C003C00u;
+    uint4* ones = reinterpret_cast<uint4*>(base + lay.ones);
+    for (int e = threadIdx.x; e < kTile * DP * 2 / 16; e += kThreads) ones[e] = make_uint4(one2, one2, one2, one2);
+    fence_proxy_async_smem();  // seen by the tensor core's reads
+  }
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_slot;
   const WaitGuard g{a.wait_ns, a.status, &bars->abort};
 
-  if (warp == kProducerWarp) {
-    fwd_producer<DP, BF16, B2, SKIP>(a, base, lay, bars, g, lane, i0, i1);
-  } else if (warp == kMmaWarp) {
-    if (lane == 0) fwd_mma<DP, BF16, SKIP>(a, base, lay, bars, tmem, g, i0, i1);
-    __syncwarp();
+  if (warp >= kSoftmaxWarps) {
+    setmaxnreg_dec<kRegsOther>();
+    if (warp == kProducerWarp) {
+      fwd_producer<DP, BF16, B2, SKIP>(a, base, lay, bars, g, lane, i0, i1);
+    } else if (warp == kMmaWarp) {
+      if (lane == 0) fwd_mma<DP, BF16, SKIP>(a, base, lay, bars, tmem, g, i0, i1);
+      __syncwarp();
+    }
   } else {
+    setmaxnreg_inc<kRegsSoftmax>();
     fwd_softmax<DP, BF16, B2, SKIP>(a, base, lay, bars, tmem, g, i0, i1);
   }
 

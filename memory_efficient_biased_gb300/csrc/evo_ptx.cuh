@@ -71,8 +71,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // gives up after g.limit_ns (recording a timeout in the status word and the
 // CTA's abort flag), or at once when another thread of the CTA already gave
 // up.  Returns false when it gave up.
-static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, uint64_t limit_ns, int* status,
-                                            volatile int* abort) {
+__device__ __forceinline__ bool mbar_poll(uint32_t bar, uint32_t parity, uint64_t limit_ns, int* status,
+                                          volatile int* abort) {
   const uint64_t t0 = globaltimer_ns();
   while (true) {
 #pragma unroll 1
@@ -86,9 +86,20 @@ static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity
     }
   }
 }
+// The polling loop as a call, which keeps it out of unrolled code ...
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, uint64_t limit_ns, int* status,
+                                                   volatile int* abort) {
+  return mbar_poll(bar, parity, limit_ns, status, abort);
+}
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitGuard& g) {
   if (mbar_try_wait(bar, parity)) return true;
   return mbar_wait_slow(bar, parity, g.limit_ns, g.status, g.abort);
+}
+// ... or inline, for kernels that must make no calls (a call saves every live
+// register around it, and per-warpgroup register budgets rule calls out).
+__device__ __forceinline__ bool mbar_wait_inl(uint32_t bar, uint32_t parity, const WaitGuard& g) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_poll(bar, parity, g.limit_ns, g.status, g.abort);
 }
 // mbar_wait for code that a whole warp runs: every lane gets the same answer (false if
 // any lane gave up), so that no lane leaves for the error path while the others go on
@@ -96,10 +107,23 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, const WaitGuard& g) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, g));
 }
+__device__ __forceinline__ bool mbar_wait_warp_inl(uint32_t bar, uint32_t parity, const WaitGuard& g) {
+  return __all_sync(0xffffffffu, mbar_wait_inl(bar, parity, g));
+}
 
 // ---------------------------------------------------------------- fences
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// Per-thread register budget of the executing warpgroup (all four warps execute it):
+// dec returns registers to the CTA's pool, inc takes them from it.
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");

@@ -246,6 +246,188 @@ __global__ void __launch_bounds__(128, 1) micro_tmem_ld(long long* cyc, int reps
   }
 }
 
+// The operand forms of the attention kernels' small-N MMAs (M = 128, N = 32, K = 16),
+// 16 per round into one accumulator, from one thread:
+//   FORM 0  A from TMEM, B MN-major 64B swizzle (rows of 32 bf16)   — forward O += P V
+//   FORM 1  A MN-major 128B swizzle, B MN-major 64B swizzle           — backward dV, dK
+//   FORM 2  A K-major 128B swizzle, B MN-major 64B swizzle            — backward dQ
+//   FORM 3  A K-major 64B swizzle, B K-major 64B swizzle              — reference (both K-major)
+struct FormSmem {
+  alignas(1024) uint8_t a[128 * 256];  // a 128 x 128 bf16 tile (two 64-column halves of 128B rows)
+  alignas(1024) uint8_t b[128 * 64];   // a 128 x 32 bf16 tile (rows of 64 bytes)
+  uint64_t done;
+  uint32_t tmem_slot;
+  int abort;
+};
+template <int FORM>
+__global__ void __launch_bounds__(128, 1) micro_form(long long* cyc, int reps, int* status) {
+  extern __shared__ uint8_t dyn[];
+  FormSmem& sm = *reinterpret_cast<FormSmem*>((reinterpret_cast<uintptr_t>(dyn) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) {
+    sm.abort = 0;
+    mbar_init(smem_u32(&sm.done), 1);
+    fence_barrier_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(&sm.tmem_slot), 512);
+    tmem_relinquish();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_slot;
+  if (threadIdx.x == 0) {
+    constexpr uint32_t RB = 64, kTile = 128;
+    constexpr uint32_t id = FORM == 0 ? idesc_f16(128, 32, true, false, true)
+                          : FORM == 1 ? idesc_f16(128, 32, true, true, true)
+                          : FORM == 2 ? idesc_f16(128, 32, true, false, true)
+                                      : idesc_f16(128, 32, true, false, false);
+    const uint32_t a_addr = smem_u32(sm.a), b_addr = smem_u32(sm.b);
+    const long long t0 = clock64();
+#pragma unroll 1
+    for (int r = 0; r < reps; r += 16) {
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const int kk = k & 7;
+        const uint32_t acc = (r > 0 || k > 0) ? 1u : 0u;
+        if (FORM == 0) {
+          const uint64_t bd = smem_desc(b_addr, kTile * RB, 8 * RB, kSwizzle64B) + kk * 16 * RB / 16;
+          umma_ts(tmem, tmem + 256 + kk * 8, bd, id, acc);
+        } else if (FORM == 1) {
+          const uint64_t ad = smem_desc(a_addr + kk * 16 * 128, 16384, 1024, kSwizzle128B);
+          const uint64_t bd = smem_desc(b_addr + kk * 16 * RB, kTile * RB, 8 * RB, kSwizzle64B);
+          umma_ss(tmem, ad, bd, id, acc);
+        } else if (FORM == 2) {
+          const uint64_t ad = smem_desc(a_addr + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024, kSwizzle128B);
+          const uint64_t bd = smem_desc(b_addr + kk * 16 * RB, kTile * RB, 8 * RB, kSwizzle64B);
+          umma_ss(tmem, ad, bd, id, acc);
+        } else {
+          const uint64_t ad = smem_desc(a_addr, 16, 8 * 64, kSwizzle64B) + (k & 1) * 2;
+          const uint64_t bd = smem_desc(b_addr, 16, 8 * 64, kSwizzle64B) + (k & 1) * 2;
+          umma_ss(tmem, ad, bd, id, acc);
+        }
+      }
+    }
+    umma_commit(smem_u32(&sm.done));
+    WaitGuard g{kWaitNs, status, &sm.abort};
+    mbar_wait(smem_u32(&sm.done), 0, g);
+    cyc[blockIdx.x] = clock64() - t0;
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// The forward's P·V MMA form (A = P from TMEM, B = V MN-major 64B, N = 32, or 48 with
+// a second B atom standing for the ones columns) issued by one thread while eight
+// other warps load from / store to TMEM, or use shared memory, or the MUFU, as the
+// softmax warps do: how much each kind of traffic slows the MMAs.
+// MODE: 0 none, 1 TMEM loads (4 x32 per wait), 2 TMEM stores (4 x16 per wait),
+// 3 loads then stores, 4 shared-memory loads and stores, 5 ex2 chains.
+struct ContendSmem {
+  alignas(1024) uint8_t a[128 * 256];
+  alignas(1024) uint8_t b[128 * 64];
+  alignas(1024) uint8_t ones[128 * 64];
+  uint64_t done;
+  uint32_t tmem_slot;
+  int abort;
+};
+
+template <int MODE, int N>
+__global__ void __launch_bounds__(384, 1) micro_contend(long long* cyc, int reps, int creps, float* sink,
+                                                        int* status) {
+  extern __shared__ uint8_t dyn[];
+  ContendSmem& sm = *reinterpret_cast<ContendSmem*>((reinterpret_cast<uintptr_t>(dyn) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    sm.abort = 0;
+    mbar_init(smem_u32(&sm.done), 1);
+    fence_barrier_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(&sm.tmem_slot), 512);
+    tmem_relinquish();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_slot;
+  if (threadIdx.x == 0) {
+    constexpr uint32_t RB = 64, kTile = 128;
+    constexpr uint32_t id = idesc_f16(128, N, true, false, true);
+    const uint32_t b_addr = smem_u32(sm.b);
+    const uint32_t lbo = N > 32 ? smem_u32(sm.ones) - b_addr : kTile * RB;
+    const long long t0 = clock64();
+#pragma unroll 1
+    for (int r = 0; r < reps; r += 16) {
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const int kk = k & 7;
+        const uint64_t bd = smem_desc(b_addr, lbo, 8 * RB, kSwizzle64B) + kk * 16 * RB / 16;
+        umma_ts(tmem, tmem + 256 + kk * 8, bd, id, (r > 0 || k > 0) ? 1u : 0u);
+      }
+    }
+    umma_commit(smem_u32(&sm.done));
+    WaitGuard g{kWaitNs, status, &sm.abort};
+    mbar_wait(smem_u32(&sm.done), 0, g);
+    cyc[blockIdx.x] = clock64() - t0;
+  } else if (warp >= 4 && MODE != 0) {
+    const uint32_t trow = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    const uint32_t half = static_cast<uint32_t>((warp >> 3) & 1);  // two warps per lane quadrant
+    float acc = 0.0f;
+#pragma unroll 1
+    for (int it = 0; it < creps; ++it) {
+      if (MODE == 1 || MODE == 3) {
+        uint32_t x0[32], x1[32], x2[32], x3[32];
+        const uint32_t c = trow + 64 + half * 64;  // columns 64..191 (D uses 0..N-1 <= 63)
+        tmem_ld32(c, x0);
+        tmem_ld32(c + 32, x1);
+        tmem_ld32(c, x2);
+        tmem_ld32(c + 32, x3);
+        tmem_wait_ld(x0);
+        tmem_wait_ld(x1);
+        tmem_wait_ld(x2);
+        tmem_wait_ld(x3);
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+          acc += __uint_as_float(x0[e]) + __uint_as_float(x1[e]) + __uint_as_float(x2[e]) + __uint_as_float(x3[e]);
+      }
+      if (MODE == 2 || MODE == 3) {
+        uint32_t y[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) y[e] = static_cast<uint32_t>(it + e);
+        const uint32_t c = trow + 384 + half * 64;  // columns 384..511
+#pragma unroll
+        for (int q = 0; q < 4; ++q) tmem_st16(c + q * 16, y);
+        tmem_wait_st();
+      }
+      if (MODE == 4) {
+        const uint32_t* src = reinterpret_cast<const uint32_t*>(sm.a);
+        uint32_t* dst = reinterpret_cast<uint32_t*>(sm.a) + 4096;
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          const uint4 v = reinterpret_cast<const uint4*>(src)[(q * 32 + lane + it) & 1023];
+          acc += __uint_as_float(v.x ^ v.y ^ v.z ^ v.w);
+          reinterpret_cast<uint4*>(dst)[(q * 32 + lane) & 1023] = v;
+        }
+      }
+      if (MODE == 5) {
+#pragma unroll
+        for (int q = 0; q < 64; ++q) acc = ex2(acc * -0.5f);
+      }
+    }
+    if (acc == 1234.5f) sink[threadIdx.x] = acc;  // keeps the traffic from being removed
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
 template <int K>
 cudaError_t run_exp(int blocks, int iters, float* sink, long long* cyc, cudaStream_t st) {
   micro_exp<K><<<blocks, 512, 0, st>>>(sink, cyc, iters);
@@ -298,6 +480,59 @@ EVO_MICRO_API int evo_micro_exp(int kind, int blocks, int iters, void* sink, voi
     case kMix31: return run_exp<kMix31>(blocks, iters, s, c, st);
     default: return cudaErrorInvalidValue;
   }
+}
+
+// Small-N MMA operand forms (FORM 0..3 above): `blocks` blocks, `reps` MMAs each
+// (a multiple of 16); cycles: device int64[blocks]; status as evo_micro_mma.
+EVO_MICRO_API int evo_micro_mma_form(int form, int blocks, int reps, void* cycles, void* status, void* stream) {
+  long long* c = static_cast<long long*>(cycles);
+  int* s = static_cast<int*>(status);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (blocks <= 0 || reps <= 0 || reps % 16 != 0 || !cycles || !status) return cudaErrorInvalidValue;
+  const size_t smem = sizeof(FormSmem) + 1024;
+  switch (form) {
+#define EVO_FORM(F)                                                                              \
+  case F: {                                                                                      \
+    cudaError_t e = cudaFuncSetAttribute(micro_form<F>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                                         static_cast<int>(smem));                                \
+    if (e != cudaSuccess) return e;                                                              \
+    micro_form<F><<<blocks, 128, smem, st>>>(c, reps, s);                                        \
+    break;                                                                                       \
+  }
+    EVO_FORM(0)
+    EVO_FORM(1)
+    EVO_FORM(2)
+    EVO_FORM(3)
+#undef EVO_FORM
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+// P·V MMAs under other warps' traffic (micro_contend): mode 0..5, n 32 or 48; `reps`
+// MMAs (a multiple of 16) while the eight other warps run `creps` rounds of traffic.
+EVO_MICRO_API int evo_micro_contend(int mode, int n, int blocks, int reps, int creps, void* cycles, void* sink,
+                                    void* status, void* stream) {
+  long long* c = static_cast<long long*>(cycles);
+  float* sk = static_cast<float*>(sink);
+  int* s = static_cast<int*>(status);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (blocks <= 0 || reps <= 0 || reps % 16 != 0 || creps < 0 || !cycles || !sink || !status ||
+      (n != 32 && n != 48) || mode < 0 || mode > 5)
+    return cudaErrorInvalidValue;
+  const size_t smem = sizeof(ContendSmem) + 1024;
+#define EVO_CONT(M, NN)                                                                                   \
+  if (mode == M && n == NN) {                                                                              \
+    cudaError_t e = cudaFuncSetAttribute(micro_contend<M, NN>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                                         static_cast<int>(smem));                                         \
+    if (e != cudaSuccess) return e;                                                                       \
+    micro_contend<M, NN><<<blocks, 384, smem, st>>>(c, reps, creps, sk, s);                               \
+    return cudaGetLastError();                                                                            \
+  }
+  EVO_CONT(0, 32) EVO_CONT(1, 32) EVO_CONT(2, 32) EVO_CONT(3, 32) EVO_CONT(4, 32) EVO_CONT(5, 32)
+  EVO_CONT(0, 48) EVO_CONT(1, 48) EVO_CONT(2, 48) EVO_CONT(3, 48) EVO_CONT(4, 48) EVO_CONT(5, 48)
+#undef EVO_CONT
+  return cudaErrorInvalidValue;
 }
 
 // tcgen05.ld cost: `blocks` blocks (one per SM) of four warps, each round `per_wait`
