@@ -724,22 +724,34 @@ def run_micro(args):
         print(json.dumps({"micro": "tmem_ld", "loads_per_wait": pw, "columns_per_load": 32,
                           "cycles_per_round": min(vals[1:])}), flush=True)
     modes = ["none", "TMEM loads (4 x32 per wait)", "TMEM stores (4 x16 per wait)", "TMEM loads then stores",
-             "shared-memory loads and stores", "ex2 chains"]
-    creps = [0, 3000, 3000, 2000, 3000, 600]
+             "shared-memory loads and stores", "ex2 chains", "TMEM loads (2 x64 per wait)",
+             "TMEM loads (8 x16 per wait)"]
+    creps = [0, 3000, 3000, 2000, 3000, 600, 3000, 3000]
+    tmem_bytes = [0, 16384, 8192, 24576, 0, 0, 16384, 16384]  # per traffic warp and round
+    ccyc = torch.zeros(sms, dtype=torch.int64, device="cuda")
     csink = torch.zeros(384, dtype=torch.float32, device="cuda")
-    for n in (32, 48):
-        for mode, what in enumerate(modes):
-            vals = []
-            for rep in range(3):
-                rc = lib.evo_micro_contend(mode, n, sms, 4096, creps[mode], ctypes.c_void_p(mcyc.data_ptr()),
-                                           ctypes.c_void_p(csink.data_ptr()), ctypes.c_void_p(status.data_ptr()),
-                                           stream)
-                torch.cuda.synchronize()
-                if rc != 0 or int(status.item()) != 0:
-                    raise RuntimeError(f"micro_contend {mode} N={n}: rc {rc} status {int(status.item())}")
-                vals.append(statistics.median(mcyc.cpu().tolist()) / 4096)
-            print(json.dumps({"micro": "mma_contend", "form": "A from TMEM, B MN-major 64B", "N": n,
-                              "other_warps": what, "cycles_per_mma": min(vals[1:])}), flush=True)
+    for ss in (0, 1):
+        for n in (32, 48):
+            for mode, what in enumerate(modes):
+                if ss and n == 48:
+                    continue
+                vals, tcyc = [], []
+                for rep in range(3):
+                    rc = lib.evo_micro_contend(mode, n, ss, sms, 4096, creps[mode], ctypes.c_void_p(mcyc.data_ptr()),
+                                               ctypes.c_void_p(ccyc.data_ptr()), ctypes.c_void_p(csink.data_ptr()),
+                                               ctypes.c_void_p(status.data_ptr()), stream)
+                    torch.cuda.synchronize()
+                    if rc != 0 or int(status.item()) != 0:
+                        raise RuntimeError(f"micro_contend {mode} N={n}: rc {rc} status {int(status.item())}")
+                    vals.append(statistics.median(mcyc.cpu().tolist()) / 4096)
+                    tcyc.append(statistics.median(ccyc.cpu().tolist()))
+                form = "A K-major 128B in smem" if ss else "A from TMEM"
+                rec = {"micro": "mma_contend", "form": form + ", B MN-major 64B", "N": n, "other_warps": what,
+                       "cycles_per_mma": min(vals[1:])}
+                if tmem_bytes[mode] and mode != 0:
+                    rec["traffic_tmem_bytes_per_clock"] = 8 * tmem_bytes[mode] * creps[mode] / max(tcyc[1:])
+                    rec["traffic_cycles_per_round"] = max(tcyc[1:]) / creps[mode]
+                print(json.dumps(rec), flush=True)
     rows = sampler.stop()
     print(json.dumps({"micro": "clocks", **summarize_clocks(rows, 0, 1e18, sampler.source)}), flush=True)
     return 0

@@ -264,12 +264,15 @@ __global__ void __launch_bounds__(256) evo_bwd_db2_sum(const BwdArgs a) {
 //   dQ_tile = dS K (issued first, so its consumer starts early), dV += Pᵀ dO and
 //   dK += dSᵀ Q (the same tiles as MN-major A operands; dK, dV double-buffered across
 //   key tiles where TMEM allows).
-// dQ of a slice accumulates in the CTA's own fp32 rows of the workspace: the first key
-// tile of the slice stores its tile, later ones add to it, and the last one adds, scales
-// and writes dQ in the dtype.  Each compute thread owns the same (query row, column
-// half) at every step, so its own program order orders these plain loads and stores;
-// the sum runs over the key tiles in a fixed order, so dQ is bitwise reproducible, and
-// the fp32 rows of one CTA (L × DP floats) stay in L2.
+// dQ of a slice accumulates in the CTA's own fp32 blocks of the workspace (one block of
+// 32 rows × DP/2 columns per compute warp and query tile): each compute warp stages its
+// dQ_tile block in shared memory and hands it to the bulk-copy engine, which stores it
+// (first key tile of the slice) or adds it in L2 (later key tiles); the last key tile
+// reads the sum back, adds its own tile, scales and writes dQ in the dtype.  Successive
+// additions to one block are a query-tile sweep apart, and each is issued only once every
+// bulk operation of the warp but the newest is complete, so they run one after another
+// in key-tile order: dQ is bitwise reproducible.  The blocks of one CTA (L × DP floats)
+// stay in L2.
 __device__ __forceinline__ uint32_t col_s() { return 0u; }
 __device__ __forceinline__ uint32_t col_dp() { return 128u; }
 template <int DP>
@@ -301,7 +304,10 @@ struct MainBars {
 template <int DP>
 struct MainLayout {
   static constexpr uint32_t kTB = kTile * DP * 2;
-  Ring p, ds, k, v, q, d_o, b2s, b1, ld;
+  static constexpr uint32_t kDqBlk = 32u * (DP / 2) * 4u;  // a compute warp's fp32 dQ block
+  // staged (and sent) 1 KB at a time: small enough to leave room for a third Q/dO stage
+  static constexpr uint32_t kDqStg = kDqBlk < 1024u ? kDqBlk : 1024u;
+  Ring p, ds, k, v, q, d_o, b2s, b1, ld, dqs;
   uint32_t bars, total;
   __host__ __device__ MainLayout(bool has_b2, int qs, int pds) {
     uint32_t off = 0;
@@ -321,6 +327,8 @@ struct MainLayout {
     off += 1024u;
     ld = Ring{off, 1024u};
     off += qs * 1024u;
+    dqs = Ring{off, kDqStg};  // per compute warp: its dQ block on the way to the workspace
+    off += kComputeWarps * kDqStg;
     bars = off;
     off += (sizeof(MainBars) + 127) & ~127u;
     total = off;
@@ -576,14 +584,18 @@ struct DqStep {
   bool first, last;  // first / last (kept) key tile of its slice
 };
 
-// dQ tile of a step (TMEM lanes = queries of tile it): this warp's DP/2 columns, into
-// the CTA's fp32 rows (first key tile: store; later: add), and at the slice's last key
-// tile × s into dQ in the dtype.
+// dQ tile of a step (TMEM lanes = queries of tile it): this warp's DP/2 columns, to
+// its fp32 block of the workspace (a bulk store on the slice's first key tile, a bulk
+// add on later ones), or, on the slice's last key tile, added to the block's sum, scaled
+// and written as dQ in the dtype.  The block is chunk-major ([DP/8][32 rows][4 floats])
+// in both places, so that the staging writes and the read-back are conflict-free.
 template <int DP, bool BF16>
 __device__ __forceinline__ bool main_consume_dq(const BwdArgs& a, const DqStep& d, uint32_t u, MainBars* bars,
-                                                uint32_t trow, int r, int hc, int lane, const WaitGuard& g,
-                                                const float4 (&prev)[DP / 8]) {
+                                                uint32_t trow, int r, int w, int hc, int lane, uint8_t* stg,
+                                                const WaitGuard& g) {
   constexpr int HD = DP / 2;
+  constexpr uint32_t kBlk = MainLayout<DP>::kDqBlk, kStg = MainLayout<DP>::kDqStg;
+  constexpr int kPieces = static_cast<int>(kBlk / kStg), kChunks = static_cast<int>(kStg / 512);  // 512 B: 32 rows x 4 floats
   const uint32_t qb = u & 1;
   if (!mbar_wait_warp(smem_u32(&bars->dq_full[qb]), (u >> 1) & 1, g)) return false;
   tc_fence_after();
@@ -609,24 +621,51 @@ __device__ __forceinline__ bool main_consume_dq(const BwdArgs& a, const DqStep& 
   tc_fence_before();
   __syncwarp();
   if (lane == 0) mbar_arrive(smem_u32(&bars->dq_free[qb]));
-  const int i = d.it * kTile + r;
-  if (i >= a.L) return true;
-  float4* acc = reinterpret_cast<float4*>(a.dq_scr + (static_cast<size_t>(blockIdx.x) * a.L + i) * DP + hc * HD);
-  if (!d.first) {  // the rows' earlier sum, loaded at the start of the step
-#pragma unroll
-    for (int e = 0; e < HD; e += 4) {
-      const float4 o = prev[e >> 2];
-      v[e] += o.x;
-      v[e + 1] += o.y;
-      v[e + 2] += o.z;
-      v[e + 3] += o.w;
-    }
-  }
+  float* blk = a.dq_scr + ((static_cast<size_t>(blockIdx.x) * a.QT + d.it) * kComputeWarps + w) * (kBlk / 4);
   if (!d.last) {
 #pragma unroll
-    for (int e = 0; e < HD; e += 4) acc[e >> 2] = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+    for (int pc = 0; pc < kPieces; ++pc) {
+      if (lane == 0) bulk_wait_read_all();  // the previous bulk operation has read the staging block
+      __syncwarp();
+      float4* sp = reinterpret_cast<float4*>(stg);
+#pragma unroll
+      for (int q = 0; q < kChunks; ++q) {
+        const int c = pc * kChunks + q;
+        sp[q * 32 + lane] = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        float* dst = blk + pc * (kStg / 4);
+        if (d.first) {
+          bulk_store_s2g(dst, smem_u32(stg), kStg);
+        } else {
+          bulk_wait_all_but_newest();  // the piece's previous store or add (a sweep ago) is complete
+          bulk_reduce_add_f32(dst, smem_u32(stg), kStg);
+        }
+        bulk_commit_group();
+      }
+    }
     return true;
   }
+  if (!d.first) {  // the sum of the slice's earlier key tiles
+    if (lane == 0) {
+      bulk_wait_all_but_newest();
+      fence_proxy_async_global();
+    }
+    __syncwarp();
+    const float4* sp = reinterpret_cast<const float4*>(blk);
+#pragma unroll
+    for (int q = 0; q < HD / 4; ++q) {
+      const float4 o = sp[q * 32 + lane];
+      v[4 * q] += o.x;
+      v[4 * q + 1] += o.y;
+      v[4 * q + 2] += o.z;
+      v[4 * q + 3] += o.w;
+    }
+  }
+  const int i = d.it * kTile + r;
+  if (i >= a.L) return true;
   const long long bn = static_cast<long long>(d.b) * a.N + d.n;
   uint16_t* dq = a.dq + bn * a.r_dq.bn + static_cast<long long>(i) * a.r_dq.l + d.h * a.D + hc * HD;
 #pragma unroll
@@ -763,6 +802,7 @@ __device__ __forceinline__ void main_compute(const BwdArgs& a, uint8_t* base, co
   const float2 sl2 = make_float2(a.scale_log2, a.scale_log2);
   const int QS = a.q_stages, QT = a.QT;
   const uint32_t pds = static_cast<uint32_t>(a.pds_bufs);
+  uint8_t* dq_stg = base + lay.dqs[w];
   uint32_t u = 0, item_ctr = 0, s = 0, ph = 0;
   MainWalk cur;
   cur.init(s0, a);
@@ -775,17 +815,6 @@ __device__ __forceinline__ void main_compute(const BwdArgs& a, uint8_t* base, co
     if (!mbar_wait_warp(smem_u32(&bars->kv_full[kb]), (item_ctr >> 1) & 1, g)) { ok = false; break; }
     const float* b1 = reinterpret_cast<const float*>(base + lay.b1[kb]) + hc * 64;
     for (int it = 0; it < QT; ++it, ++u) {
-      // the fp32 dQ rows this thread adds to at the end of the step (the previous step's),
-      // loaded now so that their latency overlaps the step's work
-      float4 prev_acc[DP / 8];
-#pragma unroll
-      for (int e = 0; e < DP / 8; ++e) prev_acc[e] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-      if (u > 0 && !pd.first && pd.it * kTile + r < a.L) {
-        const float4* src = reinterpret_cast<const float4*>(
-            a.dq_scr + (static_cast<size_t>(blockIdx.x) * a.L + pd.it * kTile + r) * DP + hc * (DP / 2));
-#pragma unroll
-        for (int e = 0; e < DP / 8; ++e) prev_acc[e] = src[e];
-      }
       if (!mbar_wait_warp(smem_u32(&bars->q_full[s]), ph, g)) { ok = false; break; }
       const float* ld = reinterpret_cast<const float*>(base + lay.ld[s]);
       const float lse2 = ld[r], dlt = ld[128 + r];
@@ -835,7 +864,7 @@ __device__ __forceinline__ void main_compute(const BwdArgs& a, uint8_t* base, co
         if (it == QT - 1) mbar_arrive(smem_u32(&bars->kv_empty[kb]));
       }
       if (u > 0) {
-        if (!main_consume_dq<DP, BF16>(a, pd, u - 1, bars, trow, r, hc, lane, g, prev_acc)) { ok = false; break; }
+        if (!main_consume_dq<DP, BF16>(a, pd, u - 1, bars, trow, r, w, hc, lane, dq_stg, g)) { ok = false; break; }
         if (it == 0 && !main_write_dkdv<DP, BF16>(a, pk, item_ctr - 1, bars, trow, r, hc, lane, g)) {
           ok = false;
           break;
@@ -850,18 +879,10 @@ __device__ __forceinline__ void main_compute(const BwdArgs& a, uint8_t* base, co
     pk = KvItem{cur.b, cur.n, cur.h, cur.jt};
   }
   if (ok && u > 0) {
-    float4 prev_acc[DP / 8];
-#pragma unroll
-    for (int e = 0; e < DP / 8; ++e) prev_acc[e] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-    if (!pd.first && pd.it * kTile + r < a.L) {
-      const float4* src = reinterpret_cast<const float4*>(
-          a.dq_scr + (static_cast<size_t>(blockIdx.x) * a.L + pd.it * kTile + r) * DP + hc * (DP / 2));
-#pragma unroll
-      for (int e = 0; e < DP / 8; ++e) prev_acc[e] = src[e];
-    }
-    if (main_consume_dq<DP, BF16>(a, pd, u - 1, bars, trow, r, hc, lane, g, prev_acc))
+    if (main_consume_dq<DP, BF16>(a, pd, u - 1, bars, trow, r, w, hc, lane, dq_stg, g))
       main_write_dkdv<DP, BF16>(a, pk, item_ctr - 1, bars, trow, r, hc, lane, g);
   }
+  if (lane == 0) bulk_wait_all();  // the dQ bulk operations are done with the staging block
 }
 
 template <int DP, bool BF16, bool HAS_B2>
@@ -1816,8 +1837,8 @@ cudaError_t launch_main(BwdArgs a, cudaStream_t st) {
   static bool limit_set[64] = {};
   cudaError_t e = ensure_smem_limit(kern, kMaxSmem, limit_set);
   if (e != cudaSuccess) return e;
-  // whole slices per CTA; at most kMainMaxCtas CTAs (the workspace holds L × DP fp32 dQ
-  // rows for each)
+  // whole slices per CTA; at most kMainMaxCtas CTAs (the workspace holds QT × 128 × DP
+  // fp32 dQ values for each)
   a.items = static_cast<long long>(a.B) * a.H * a.N;
   long long ctas = num_sms();
   if (ctas > kMainMaxCtas) ctas = kMainMaxCtas;

@@ -348,7 +348,7 @@ WsLayout ws_layout(const evo_shape_t& s, bool has_bias2, bool has_db1 = false, b
   if (w.plan.mode == kBwdMain) {
     const int64_t slices = s.B * s.H * s.N;
     const int64_t ctas = slices < kMainMaxCtas ? slices : kMainMaxCtas;
-    off += round256(size_t(ctas) * s.L * padded_dim(s.D) * 4);
+    off += round256(size_t(ctas) * ((s.L + kTile - 1) / kTile) * kTile * padded_dim(s.D) * 4);
   }
   w.b2t = off;
   if ((w.plan.mode == kBwdKeyMajor || has_db1) && has_bias2)

@@ -66,7 +66,7 @@ struct BwdArgs {
   Rows r_dq, r_dk, r_dv;    // row strides of the plain writes of dQ, dK, dV
   int packed;               // all five of the above are packed [B*N][L][H*D]
   float* delta;             // workspace [B,N,H,L]
-  float* dq_scr;            // workspace: per-key-tile kernel, L × DP fp32 dQ rows per CTA
+  float* dq_scr;            // workspace: per-key-tile kernel, QT × 128 × DP fp32 dQ values per CTA
   float* db2_part;          // workspace [G][B,H,L,L]
   uint16_t* dbias1;         // [B,N,L] or nullptr
   float* db1p;              // workspace [B*N*H][2][L]: key-mask gradient partials (per key half of the queries)

@@ -321,12 +321,24 @@ __global__ void __launch_bounds__(128, 1) micro_form(long long* cyc, int reps, i
   }
 }
 
+// 32 lanes x 64 columns in one load, and its wait tied to the 64 registers.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+               : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld64(uint32_t (&r)[64]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31]), "+r"(r[32]), "+r"(r[33]), "+r"(r[34]), "+r"(r[35]), "+r"(r[36]), "+r"(r[37]), "+r"(r[38]), "+r"(r[39]), "+r"(r[40]), "+r"(r[41]), "+r"(r[42]), "+r"(r[43]), "+r"(r[44]), "+r"(r[45]), "+r"(r[46]), "+r"(r[47]), "+r"(r[48]), "+r"(r[49]), "+r"(r[50]), "+r"(r[51]), "+r"(r[52]), "+r"(r[53]), "+r"(r[54]), "+r"(r[55]), "+r"(r[56]), "+r"(r[57]), "+r"(r[58]), "+r"(r[59]), "+r"(r[60]), "+r"(r[61]), "+r"(r[62]), "+r"(r[63]) : : "memory");
+}
+
 // The forward's P·V MMA form (A = P from TMEM, B = V MN-major 64B, N = 32, or 48 with
 // a second B atom standing for the ones columns) issued by one thread while eight
 // other warps load from / store to TMEM, or use shared memory, or the MUFU, as the
 // softmax warps do: how much each kind of traffic slows the MMAs.
 // MODE: 0 none, 1 TMEM loads (4 x32 per wait), 2 TMEM stores (4 x16 per wait),
-// 3 loads then stores, 4 shared-memory loads and stores, 5 ex2 chains.
+// 3 loads then stores, 4 shared-memory loads and stores, 5 ex2 chains, 6 TMEM loads
+// (2 x64 per wait), 7 TMEM loads (8 x16 per wait).  ccyc: the first traffic warp's
+// own loop time.
 struct ContendSmem {
   alignas(1024) uint8_t a[128 * 256];
   alignas(1024) uint8_t b[128 * 64];
@@ -336,9 +348,9 @@ struct ContendSmem {
   int abort;
 };
 
-template <int MODE, int N>
-__global__ void __launch_bounds__(384, 1) micro_contend(long long* cyc, int reps, int creps, float* sink,
-                                                        int* status) {
+template <int MODE, int N, bool SS>
+__global__ void __launch_bounds__(384, 1) micro_contend(long long* cyc, long long* ccyc, int reps, int creps,
+                                                        float* sink, int* status) {
   extern __shared__ uint8_t dyn[];
   ContendSmem& sm = *reinterpret_cast<ContendSmem*>((reinterpret_cast<uintptr_t>(dyn) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -357,7 +369,7 @@ __global__ void __launch_bounds__(384, 1) micro_contend(long long* cyc, int reps
   if (threadIdx.x == 0) {
     constexpr uint32_t RB = 64, kTile = 128;
     constexpr uint32_t id = idesc_f16(128, N, true, false, true);
-    const uint32_t b_addr = smem_u32(sm.b);
+    const uint32_t a_addr = smem_u32(sm.a), b_addr = smem_u32(sm.b);
     const uint32_t lbo = N > 32 ? smem_u32(sm.ones) - b_addr : kTile * RB;
     const long long t0 = clock64();
 #pragma unroll 1
@@ -366,7 +378,12 @@ __global__ void __launch_bounds__(384, 1) micro_contend(long long* cyc, int reps
       for (int k = 0; k < 16; ++k) {
         const int kk = k & 7;
         const uint64_t bd = smem_desc(b_addr, lbo, 8 * RB, kSwizzle64B) + kk * 16 * RB / 16;
-        umma_ts(tmem, tmem + 256 + kk * 8, bd, id, (r > 0 || k > 0) ? 1u : 0u);
+        if (SS) {  // A = a 128 x 128 K-major tile, 128B swizzle (two 64-key halves)
+          const uint64_t ad = smem_desc(a_addr + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024, kSwizzle128B);
+          umma_ss(tmem, ad, bd, id, (r > 0 || k > 0) ? 1u : 0u);
+        } else {
+          umma_ts(tmem, tmem + 256 + kk * 8, bd, id, (r > 0 || k > 0) ? 1u : 0u);
+        }
       }
     }
     umma_commit(smem_u32(&sm.done));
@@ -377,8 +394,37 @@ __global__ void __launch_bounds__(384, 1) micro_contend(long long* cyc, int reps
     const uint32_t trow = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     const uint32_t half = static_cast<uint32_t>((warp >> 3) & 1);  // two warps per lane quadrant
     float acc = 0.0f;
+    const long long c0 = clock64();
 #pragma unroll 1
     for (int it = 0; it < creps; ++it) {
+      if (MODE == 6) {
+        uint32_t x0[64], x1[64];
+        const uint32_t c = trow + 64 + half * 64;
+        tmem_ld64(c, x0);
+        tmem_ld64(c, x1);
+        tmem_wait_ld64(x0);
+        tmem_wait_ld64(x1);
+#pragma unroll
+        for (int e = 0; e < 64; ++e) acc += __uint_as_float(x0[e]) + __uint_as_float(x1[e]);
+      }
+      if (MODE == 7) {
+        const uint32_t c = trow + 64 + half * 64;
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          uint32_t x0[16], x1[16], x2[16], x3[16];
+          tmem_ld16(c + q * 32, x0);
+          tmem_ld16(c + q * 32 + 16, x1);
+          tmem_ld16(c + q * 32, x2);
+          tmem_ld16(c + q * 32 + 16, x3);
+          tmem_wait_ld(x0);
+          tmem_wait_ld(x1);
+          tmem_wait_ld(x2);
+          tmem_wait_ld(x3);
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            acc += __uint_as_float(x0[e]) + __uint_as_float(x1[e]) + __uint_as_float(x2[e]) + __uint_as_float(x3[e]);
+        }
+      }
       if (MODE == 1 || MODE == 3) {
         uint32_t x0[32], x1[32], x2[32], x3[32];
         const uint32_t c = trow + 64 + half * 64;  // columns 64..191 (D uses 0..N-1 <= 63)
@@ -418,6 +464,7 @@ __global__ void __launch_bounds__(384, 1) micro_contend(long long* cyc, int reps
         for (int q = 0; q < 64; ++q) acc = ex2(acc * -0.5f);
       }
     }
+    if (warp == 4 && lane == 0) ccyc[blockIdx.x] = clock64() - c0;
     if (acc == 1234.5f) sink[threadIdx.x] = acc;  // keeps the traffic from being removed
   }
   tc_fence_before();
@@ -511,26 +558,30 @@ EVO_MICRO_API int evo_micro_mma_form(int form, int blocks, int reps, void* cycle
 
 // P·V MMAs under other warps' traffic (micro_contend): mode 0..5, n 32 or 48; `reps`
 // MMAs (a multiple of 16) while the eight other warps run `creps` rounds of traffic.
-EVO_MICRO_API int evo_micro_contend(int mode, int n, int blocks, int reps, int creps, void* cycles, void* sink,
-                                    void* status, void* stream) {
+EVO_MICRO_API int evo_micro_contend(int mode, int n, int ss, int blocks, int reps, int creps, void* cycles,
+                                    void* ccycles, void* sink, void* status, void* stream) {
   long long* c = static_cast<long long*>(cycles);
+  long long* cc = static_cast<long long*>(ccycles);
   float* sk = static_cast<float*>(sink);
   int* s = static_cast<int*>(status);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (blocks <= 0 || reps <= 0 || reps % 16 != 0 || creps < 0 || !cycles || !sink || !status ||
-      (n != 32 && n != 48) || mode < 0 || mode > 5)
+      !ccycles || (n != 32 && n != 48) || mode < 0 || mode > 7)
     return cudaErrorInvalidValue;
   const size_t smem = sizeof(ContendSmem) + 1024;
-#define EVO_CONT(M, NN)                                                                                   \
-  if (mode == M && n == NN) {                                                                              \
-    cudaError_t e = cudaFuncSetAttribute(micro_contend<M, NN>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
-                                         static_cast<int>(smem));                                         \
-    if (e != cudaSuccess) return e;                                                                       \
-    micro_contend<M, NN><<<blocks, 384, smem, st>>>(c, reps, creps, sk, s);                               \
-    return cudaGetLastError();                                                                            \
+#define EVO_CONT(M, NN, SSF)                                                                      \
+  if (mode == M && n == NN && (ss != 0) == SSF) {                                                  \
+    auto kern = micro_contend<M, NN, SSF>;                                                         \
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,        \
+                                         static_cast<int>(smem));                                  \
+    if (e != cudaSuccess) return e;                                                                \
+    kern<<<blocks, 384, smem, st>>>(c, cc, reps, creps, sk, s);                                    \
+    return cudaGetLastError();                                                                     \
   }
-  EVO_CONT(0, 32) EVO_CONT(1, 32) EVO_CONT(2, 32) EVO_CONT(3, 32) EVO_CONT(4, 32) EVO_CONT(5, 32)
-  EVO_CONT(0, 48) EVO_CONT(1, 48) EVO_CONT(2, 48) EVO_CONT(3, 48) EVO_CONT(4, 48) EVO_CONT(5, 48)
+#define EVO_CONT_N(M) EVO_CONT(M, 32, false) EVO_CONT(M, 48, false) EVO_CONT(M, 32, true) EVO_CONT(M, 48, true)
+  EVO_CONT_N(0) EVO_CONT_N(1) EVO_CONT_N(2) EVO_CONT_N(3) EVO_CONT_N(4) EVO_CONT_N(5) EVO_CONT_N(6)
+  EVO_CONT_N(7)
+#undef EVO_CONT_N
 #undef EVO_CONT
   return cudaErrorInvalidValue;
 }
