@@ -15,23 +15,27 @@
 //               key-mask chunk per key tile into a ring of stages; pair-bias tiles
 //               either resident per (b, h, pair) group across n, or streamed with
 //               each key tile.
-//   warp 9      MMA issuer (one thread): per key tile and query tile g,
-//               S_g = Q_g K_jᵀ into TMEM, and the previous key tile's
-//               O_g += P_g V_{j-1} (P read from TMEM).
+//   warps 9, 10 MMA issuers (one thread each, one per query tile g): per key
+//               tile, S_g = Q_g K_jᵀ into TMEM, and the previous key tile's
+//               O_g += P_g [V_{j-1} | 1] (P read from TMEM; the ones columns make
+//               the MMA form the row sums of P too).  Neither waits on the other.
 //   warps 0..3  softmax of query tile 0, warps 4..7 of query tile 1: one thread
-//   and 4..7    per query row, all 128 keys of a tile, in four chunks of 32.  The
-//               two groups work on different query tiles, so one group's
-//               exponentials overlap the other's wait for its scores (ping-pong).
+//   and 4..7    per query row.  Each key tile's 128 scores are loaded into
+//               registers in two 64-column loads, and S is released at once, so
+//               the next tile's scores are computed while this one is worked on.
+//               The two groups take turns for the exponentials (a bounded
+//               mbarrier hand-off), so one group's exponentials overlap the other's
+//               scoring and waits.
+//   warp 11     idle (the three warpgroups share the register file: the third
+//               gives registers back, the softmax warpgroups take them).
 // Online softmax with a lazily moved reference: a row's reference max m moves
 // only when a key tile's max exceeds it by more than 2^8 (P then stays below
-// 256, exact enough in fp16/bf16); the tile's P is then rescaled in registers
-// (or, for larger jumps and for the first key tile of a row, recomputed from
-// S, which stays in TMEM until the row's tile is decided), and the O
-// accumulator in TMEM is rescaled once the previous P·V is done.  Scale and
-// biases are applied in the log2 domain with packed f32x2 arithmetic.  P is
-// held in registers (64 packed pairs) until the tile is decided, then written
-// to TMEM for the P·V MMA.  The epilogue divides O by the row sum and writes O
-// through shared memory with one TMA tile store per warp, and lse.
+// 256, exact enough in fp16/bf16); the O accumulator (with its row-sum columns)
+// is then rescaled in TMEM once the previous P·V is done.  The tile max is taken
+// before P is formed, so each tile is exponentiated once.  Scale and biases are
+// applied in the log2 domain with packed f32x2 arithmetic.  The epilogue divides
+// O by the row sum and writes O through shared memory with one TMA tile store per
+// warp, and lse.
 // Key columns past L carry a -inf key-mask entry, so no other masking is
 // needed; query rows past L (a partial or absent second query tile) are
 // computed and not stored.
@@ -49,7 +53,7 @@ constexpr int kSoftmaxWarps = 8;
 // that the softmax warps can hold a whole row of scores:
 // 128 x 104 + 256 x 200 = 384 x 168.
 constexpr int kThreads = (kSoftmaxWarps + 4) * 32;
-constexpr int kProducerWarp = kSoftmaxWarps, kMmaWarp = kSoftmaxWarps + 1;
+constexpr int kProducerWarp = kSoftmaxWarps, kMmaWarp = kSoftmaxWarps + 1;  // MMA warps: kMmaWarp + g
 constexpr uint32_t kRegsLaunch = 168, kRegsSoftmax = 200, kRegsOther = 104;
 static_assert(128 * kRegsOther + 256 * kRegsSoftmax <= kThreads * kRegsLaunch, "register split exceeds the launch");
 constexpr float kLog2e = 1.4426950408889634f;
@@ -79,7 +83,8 @@ struct FwdBars {
   uint64_t s_full[2], s_free[2];    // per query tile: S written / read and decided
   uint64_t p_full[2], p_empty[2];   // per query tile: P written / its P·V done
   uint64_t o_free[2];               // per query tile: the epilogue has read O
-  uint64_t drain;
+  uint64_t turn[2];
+  uint64_t drain[2];
   uint32_t tmem_slot;
   int abort;
   // per K/V stage, written by the producer before it arrives on kv_full: the key tile
@@ -347,11 +352,12 @@ __device__ __forceinline__ bool fwd_issue_pv(uint32_t g, uint32_t v, uint32_t sv
   return true;
 }
 
-// Per key tile: S of both query tiles as soon as each group has loaded its previous
-// S (s_free), then both groups' P·V of the previous key tile as their P arrives.
+// One issuing thread per query tile g: per key tile, S_g as soon as the group has loaded
+// its previous S (s_free), then the group's P·V of the previous key tile as its P
+// arrives.  The two threads share the tensor core but never wait on each other.
 template <int DP, bool BF16, bool SKIP>
 __device__ __forceinline__ void fwd_mma(const FwdArgs& a, uint8_t* base, const FwdLayout<DP>& lay, FwdBars* bars,
-                                        uint32_t tmem, const WaitGuard& g, long long i0, long long i1) {
+                                        uint32_t tmem, uint32_t gq, const WaitGuard& g, long long i0, long long i1) {
   constexpr uint32_t RB = DP * 2;
   constexpr uint32_t SWZ = swizzle_for_row(RB);
   constexpr uint32_t id_s = idesc_f16(128, 128, BF16, false, false);
@@ -368,23 +374,23 @@ __device__ __forceinline__ void fwd_mma(const FwdArgs& a, uint8_t* base, const F
       if (!mbar_wait_inl(smem_u32(&bars->kv_full[s]), ph, g)) { ok = false; break; }
       const uint32_t meta = SKIP ? bars->tile_meta[s] : tile_meta_all(x, KT);
       const bool last = (meta & kTileLast) != 0;
+      // S_g of this tile once the group has loaded its previous S
+      if (!mbar_wait_inl(smem_u32(&bars->s_free[gq]), (u & 1) ^ 1, g)) { ok = false; break; }
+      tc_fence_after();
       const uint64_t kd = smem_desc(smem_u32(base + lay.k[s]), 16, 8 * RB, SWZ);
-      for (uint32_t gq = 0; gq < 2; ++gq) {
-        // S_g of this tile once the group has loaded its previous S
-        if (!mbar_wait_inl(smem_u32(&bars->s_free[gq]), (u & 1) ^ 1, g)) { ok = false; break; }
-        tc_fence_after();
-        const uint64_t qd = smem_desc(smem_u32(base + lay.q[2 * qb + gq]), 16, 8 * RB, SWZ);
+      const uint64_t qd = smem_desc(smem_u32(base + lay.q[2 * qb + gq]), 16, 8 * RB, SWZ);
 #pragma unroll
-        for (int k = 0; k < DP / 16; ++k) umma_ss(tmem + col_s(gq), qd + k * 2, kd + k * 2, id_s, k > 0);
-        umma_commit(smem_u32(&bars->s_full[gq]));
-      }
-      if (!ok) break;
+      for (int k = 0; k < DP / 16; ++k) umma_ss(tmem + col_s(gq), qd + k * 2, kd + k * 2, id_s, k > 0);
+      umma_commit(smem_u32(&bars->s_full[gq]));
       if (last) umma_commit(smem_u32(&bars->q_empty[qb]));
-      // both groups' P·V of the previous key tile
-      for (uint32_t gq = 0; ok && u > 0 && gq < 2; ++gq)
-        ok = fwd_issue_pv<DP, BF16>(gq, u - 1, prev_stage, prev_meta, prev_item, base, lay, bars, tmem, g);
-      if (!ok) break;
-      if (u > 0) umma_commit(smem_u32(&bars->kv_empty[prev_stage]));
+      // the group's P·V of the previous key tile
+      if (u > 0) {
+        if (!fwd_issue_pv<DP, BF16>(gq, u - 1, prev_stage, prev_meta, prev_item, base, lay, bars, tmem, g)) {
+          ok = false;
+          break;
+        }
+        umma_commit(smem_u32(&bars->kv_empty[prev_stage]));
+      }
       prev_stage = s;
       prev_meta = meta;
       prev_item = item_ord;
@@ -396,14 +402,11 @@ __device__ __forceinline__ void fwd_mma(const FwdArgs& a, uint8_t* base, const F
       if (SKIP && last) break;
     }
   }
-  if (ok && u > 0) {
-    for (uint32_t gq = 0; ok && gq < 2; ++gq)
-      ok = fwd_issue_pv<DP, BF16>(gq, u - 1, prev_stage, prev_meta, prev_item, base, lay, bars, tmem, g);
-    if (ok) umma_commit(smem_u32(&bars->kv_empty[prev_stage]));
-  }
+  if (ok && u > 0 && fwd_issue_pv<DP, BF16>(gq, u - 1, prev_stage, prev_meta, prev_item, base, lay, bars, tmem, g))
+    umma_commit(smem_u32(&bars->kv_empty[prev_stage]));
   // Drain: all MMAs this thread issued are complete before TMEM is freed.
-  umma_commit(smem_u32(&bars->drain));
-  drain_wait(smem_u32(&bars->drain), 0, a.wait_ns, a.status);
+  umma_commit(smem_u32(&bars->drain[gq]));
+  drain_wait(smem_u32(&bars->drain[gq]), 0, a.wait_ns, a.status);
 }
 
 // ------------------------------------------------------------ softmax (warps 0..7)
@@ -544,6 +547,7 @@ __device__ __forceinline__ void fwd_softmax(const FwdArgs& a, uint8_t* base, con
   cur.init(i0, a);
   prev = cur;
   bool ok = true;
+  if (grp == 1 && lane == 0) mbar_arrive(smem_u32(&bars->turn[0]));  // query tile 0 goes first
   for (long long item = i0; ok && item < i1; ++item) {
     if (item > i0) {
       prev = cur;
@@ -573,19 +577,19 @@ __device__ __forceinline__ void fwd_softmax(const FwdArgs& a, uint8_t* base, con
       const float* b1 = reinterpret_cast<const float*>(base + lay.b1[s]);
       const uint8_t* b2t =
           base + (B2 == kB2Resident ? lay.b2r + (grp * KT + jt) * 32768u : lay.b2s[s] + grp * 32768u);
-      // S: two chunks, then the other two in flight while the first two are scored
-      uint32_t y0[32], y1[32], y2[32], y3[32];
+      // S in two 64-column loads: the second is in flight while the first half is scored
+      uint32_t ya[64], yb[64];
+      uint32_t(&y0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&ya[0]);
+      uint32_t(&y1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&ya[32]);
+      uint32_t(&y2)[32] = *reinterpret_cast<uint32_t(*)[32]>(&yb[0]);
+      uint32_t(&y3)[32] = *reinterpret_cast<uint32_t(*)[32]>(&yb[32]);
       float mt = -INFINITY;
-      tmem_ld32(scol, y0);
-      tmem_ld32(scol + 32, y1);
-      tmem_wait_ld(y0);
-      tmem_wait_ld(y1);
-      tmem_ld32(scol + 64, y2);
-      tmem_ld32(scol + 96, y3);
+      tmem_ld64(scol, ya);
+      tmem_wait_ld(ya);
+      tmem_ld64(scol + 64, yb);
       chunk_scores<BF16, kHasB2>(y0, b1, b2t, 0, r, sl2, mt);
       chunk_scores<BF16, kHasB2>(y1, b1 + 32, b2t, 4, r, sl2, mt);
-      tmem_wait_ld(y2);
-      tmem_wait_ld(y3);
+      tmem_wait_ld(yb);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&bars->s_free[grp]));  // S may be overwritten
@@ -610,16 +614,21 @@ __device__ __forceinline__ void fwd_softmax(const FwdArgs& a, uint8_t* base, con
       // of an item, the previous item's O is complete)
       if (!mbar_wait_warp_inl(smem_u32(&bars->p_empty[grp]), (u & 1) ^ 1, g)) { ok = false; break; }
       tc_fence_after();
+      if (!mbar_wait_warp_inl(smem_u32(&bars->turn[grp]), u & 1, g)) { ok = false; break; }
       float2 rs = make_float2(0.0f, 0.0f);
-      uint32_t pp[16];
-      chunk_probs<BF16, kRowSum>(y0, m, pp, rs);
-      tmem_st16(pcol, pp);
-      chunk_probs<BF16, kRowSum>(y1, m, pp, rs);
-      tmem_st16(pcol + 16, pp);
-      chunk_probs<BF16, kRowSum>(y2, m, pp, rs);
-      tmem_st16(pcol + 32, pp);
-      chunk_probs<BF16, kRowSum>(y3, m, pp, rs);
-      tmem_st16(pcol + 48, pp);
+      {  // P in two 32-column stores
+        uint32_t pp[32];
+        uint32_t(&p0)[16] = *reinterpret_cast<uint32_t(*)[16]>(&pp[0]);
+        uint32_t(&p1)[16] = *reinterpret_cast<uint32_t(*)[16]>(&pp[16]);
+        chunk_probs<BF16, kRowSum>(y0, m, p0, rs);
+        chunk_probs<BF16, kRowSum>(y1, m, p1, rs);
+        tmem_st32(pcol, pp);
+        chunk_probs<BF16, kRowSum>(y2, m, p0, rs);
+        chunk_probs<BF16, kRowSum>(y3, m, p1, rs);
+        tmem_st32(pcol + 32, pp);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bars->turn[grp ^ 1]));
       // The accumulator of the previous tiles (complete: p_empty) is rescaled before this
       // tile's P·V adds to it (that P·V waits for p_full below).
       if (!first && __any_sync(0xffffffffu, resc)) {
@@ -665,20 +674,21 @@ __global__ void __launch_bounds__(kThreads, 1) evo_fwd_kernel(const __grid_const
     bars->abort = 0;
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(&bars->q_full[s]), 1);
-      mbar_init(smem_u32(&bars->q_empty[s]), 1);
+      mbar_init(smem_u32(&bars->q_empty[s]), 2);  // both MMA threads
+      mbar_init(smem_u32(&bars->drain[s]), 1);
       mbar_init(smem_u32(&bars->s_full[s]), 1);
       mbar_init(smem_u32(&bars->s_free[s]), 4);
       mbar_init(smem_u32(&bars->p_full[s]), 4);
       mbar_init(smem_u32(&bars->p_empty[s]), 1);
       mbar_init(smem_u32(&bars->o_free[s]), 4);
+      mbar_init(smem_u32(&bars->turn[s]), 4);
     }
     for (int s = 0; s < kMaxStages; ++s) {
       mbar_init(smem_u32(&bars->kv_full[s]), 32);
-      mbar_init(smem_u32(&bars->kv_empty[s]), 1 + kSoftmaxWarps);
+      mbar_init(smem_u32(&bars->kv_empty[s]), 2 + kSoftmaxWarps);  // both MMA threads, every softmax warp
     }
     mbar_init(smem_u32(&bars->b2_full), 32);
     mbar_init(smem_u32(&bars->b2_empty), kSoftmaxWarps);
-    mbar_init(smem_u32(&bars->drain), 1);
     fence_barrier_init();
   }
   if (warp == kProducerWarp && lane == 0) {
@@ -707,8 +717,8 @@ __global__ void __launch_bounds__(kThreads, 1) evo_fwd_kernel(const __grid_const
     setmaxnreg_dec<kRegsOther>();
     if (warp == kProducerWarp) {
       fwd_producer<DP, BF16, B2, SKIP>(a, base, lay, bars, g, lane, i0, i1);
-    } else if (warp == kMmaWarp) {
-      if (lane == 0) fwd_mma<DP, BF16, SKIP>(a, base, lay, bars, tmem, g, i0, i1);
+    } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
+      if (lane == 0) fwd_mma<DP, BF16, SKIP>(a, base, lay, bars, tmem, static_cast<uint32_t>(warp - kMmaWarp), g, i0, i1);
       __syncwarp();
     }
   } else {
