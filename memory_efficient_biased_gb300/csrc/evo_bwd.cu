@@ -309,7 +309,8 @@ struct MainLayout {
   static constexpr uint32_t kDqStg = kDqBlk < 1024u ? kDqBlk : 1024u;
   Ring p, ds, k, v, q, d_o, b2s, b1, ld, dqs;
   uint32_t bars, total;
-  __host__ __device__ MainLayout(bool has_b2, int qs, int pds) {
+  int kvb;  // K/V buffers
+  __host__ __device__ MainLayout(bool has_b2, int qs, int pds, int kv_bufs) : kvb(kv_bufs) {
     uint32_t off = 0;
     p = Ring{off, 32768u};
     off += pds * 32768u;
@@ -317,7 +318,7 @@ struct MainLayout {
     off += pds * 32768u;
     k = Ring{off, 2 * kTB};
     v = Ring{off + kTB, 2 * kTB};
-    off += 4 * kTB;
+    off += kvb * 2 * kTB;
     q = Ring{off, 2 * kTB};
     d_o = Ring{off + kTB, 2 * kTB};
     off += qs * 2 * kTB;
@@ -334,6 +335,11 @@ struct MainLayout {
     total = off;
   }
 };
+
+// K/V buffer of item number c (items alternate between two buffers, or share one) and
+// the parity of that buffer's c-th use.
+__device__ __forceinline__ uint32_t kv_buf(uint32_t c, int kvb) { return kvb == 2 ? (c & 1) : 0u; }
+__device__ __forceinline__ uint32_t kv_par(uint32_t c, int kvb) { return kvb == 2 ? ((c >> 1) & 1) : (c & 1); }
 
 // The walk of one CTA over its steps: slices s0 <= s < s1 (order b, h, n), the kept key
 // tiles of each (all, or those not in the row's skip bits), the QT query tiles of each.
@@ -397,8 +403,8 @@ __device__ __forceinline__ void main_producer(const BwdArgs& a, uint8_t* base, c
   for (; ok && w.s < s1; ++item_ctr, w.next_item(a)) {
     const int bn = w.b * a.N + w.n, bh = w.b * a.H + w.h;
     const size_t bnh = static_cast<size_t>(bn) * a.H + w.h;
-    const uint32_t kb = item_ctr & 1;
-    if (!mbar_wait_warp(smem_u32(&bars->kv_empty[kb]), ((item_ctr >> 1) & 1) ^ 1, g)) { ok = false; break; }
+    const uint32_t kb = kv_buf(item_ctr, lay.kvb);
+    if (!mbar_wait_warp(smem_u32(&bars->kv_empty[kb]), kv_par(item_ctr, lay.kvb) ^ 1, g)) { ok = false; break; }
     {
       const uint32_t full = smem_u32(&bars->kv_full[kb]);
       if (lane == 0) {
@@ -434,8 +440,8 @@ __device__ __forceinline__ void main_producer(const BwdArgs& a, uint8_t* base, c
     }
   }
   // Drain: every copy this warp started has landed before the CTA may exit.
-  for (uint32_t b = 0; b < 2; ++b) {
-    const uint32_t issued = (item_ctr + 1 - b) / 2;
+  for (uint32_t b = 0; b < static_cast<uint32_t>(lay.kvb); ++b) {
+    const uint32_t issued = lay.kvb == 2 ? (item_ctr + 1 - b) / 2 : item_ctr;
     if (issued > 0) drain_wait(smem_u32(&bars->kv_full[b]), (issued - 1) & 1, a.wait_ns, a.status);
   }
   for (uint32_t st = 0; st < static_cast<uint32_t>(QS); ++st) {
@@ -457,8 +463,8 @@ __device__ __forceinline__ bool main_issue_sdp(const Step& st, uint8_t* base, co
   constexpr uint32_t RB = DP * 2;
   constexpr uint32_t SWZ = swizzle_for_row(RB);
   constexpr uint32_t id_s = idesc_f16(128, 128, BF16, false, false);  // K-major A and B
-  const uint32_t kb = st.item_ctr & 1;
-  if (st.it == 0 && !mbar_wait(smem_u32(&bars->kv_full[kb]), (st.item_ctr >> 1) & 1, g)) return false;
+  const uint32_t kb = kv_buf(st.item_ctr, lay.kvb);
+  if (st.it == 0 && !mbar_wait(smem_u32(&bars->kv_full[kb]), kv_par(st.item_ctr, lay.kvb), g)) return false;
   if (!mbar_wait(smem_u32(&bars->q_full[st.qs]), st.qph, g)) return false;
   if (!mbar_wait(smem_u32(&bars->st_free), (st.u & 1) ^ 1, g)) return false;
   tc_fence_after();
@@ -485,7 +491,7 @@ __device__ __forceinline__ bool main_issue_grads(const Step& st, int QT, int pds
   constexpr uint32_t id_kv = idesc_f16(128, DP, BF16, true, true);  // dV, dK: MN-major A and B
   constexpr uint32_t id_q = idesc_f16(128, DP, BF16, false, true);  // dQ: K-major A, MN-major B
   constexpr int NB = kv_acc_buffers<DP>();
-  const uint32_t kb = st.item_ctr & 1;
+  const uint32_t kb = kv_buf(st.item_ctr, lay.kvb);
   const uint32_t db = st.item_ctr % NB, dph = (st.item_ctr / NB) & 1;
   const uint32_t qb = st.u & 1;
   const uint32_t pb = st.u % pds, pph = (st.u / pds) & 1;
@@ -552,6 +558,8 @@ __device__ __forceinline__ void main_mma(const BwdArgs& a, uint8_t* base, const 
     // S/dP of step u+1 go ahead of step u's gradient MMAs, so the compute warps
     // can start on u+1 while the tensor core finishes u.  (Needs a second
     // Q/dO stage: step u's stage is released by its gradient MMAs.)
+    // With one K/V buffer, a step that starts a new key tile needs the buffer the
+    // previous step's gradient MMAs release: those go first there.
     if (ok) ok = main_issue_sdp<DP, BF16>(cur, base, lay, bars, tmem, g);
     while (ok) {
       Step nxt = cur;
@@ -559,8 +567,10 @@ __device__ __forceinline__ void main_mma(const BwdArgs& a, uint8_t* base, const 
       advance_walk(wn, cur);
       step_of(nxt);
       const bool more = wn.s < s1;
-      if (more && !main_issue_sdp<DP, BF16>(nxt, base, lay, bars, tmem, g)) { ok = false; break; }
+      const bool grads_first = lay.kvb == 1 && nxt.it == 0;
+      if (more && !grads_first && !main_issue_sdp<DP, BF16>(nxt, base, lay, bars, tmem, g)) { ok = false; break; }
       if (!main_issue_grads<DP, BF16>(cur, QT, pds, base, lay, bars, tmem, g)) { ok = false; break; }
+      if (more && grads_first && !main_issue_sdp<DP, BF16>(nxt, base, lay, bars, tmem, g)) { ok = false; break; }
       if (!more) break;
       cur = nxt;
       w = wn;
@@ -810,9 +820,9 @@ __device__ __forceinline__ void main_compute(const BwdArgs& a, uint8_t* base, co
   KvItem pk{0, 0, 0, 0};
   bool ok = true;
   for (; ok && cur.s < s1; ++item_ctr, cur.next_item(a)) {
-    const uint32_t kb = item_ctr & 1;
+    const uint32_t kb = kv_buf(item_ctr, lay.kvb);
     const bool first = cur.first_tile(a), last = cur.last_tile(a);
-    if (!mbar_wait_warp(smem_u32(&bars->kv_full[kb]), (item_ctr >> 1) & 1, g)) { ok = false; break; }
+    if (!mbar_wait_warp(smem_u32(&bars->kv_full[kb]), kv_par(item_ctr, lay.kvb), g)) { ok = false; break; }
     const float* b1 = reinterpret_cast<const float*>(base + lay.b1[kb]) + hc * 64;
     for (int it = 0; it < QT; ++it, ++u) {
       if (!mbar_wait_warp(smem_u32(&bars->q_full[s]), ph, g)) { ok = false; break; }
@@ -889,7 +899,7 @@ template <int DP, bool BF16, bool HAS_B2>
 __global__ void __launch_bounds__(kThreads, 1) evo_bwd_main(const __grid_constant__ BwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const MainLayout<DP> lay(HAS_B2, a.q_stages, a.pds_bufs);
+  const MainLayout<DP> lay(HAS_B2, a.q_stages, a.pds_bufs, a.kv_bufs);
   MainBars* bars = reinterpret_cast<MainBars*>(base + lay.bars);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // the CTA's contiguous range of whole slices
@@ -1831,7 +1841,7 @@ unsigned grid_for(long long work, long long per_block) {
 
 template <int DP, bool BF16, bool HAS_B2>
 cudaError_t launch_main(BwdArgs a, cudaStream_t st) {
-  const MainLayout<DP> lay(HAS_B2, a.q_stages, a.pds_bufs);
+  const MainLayout<DP> lay(HAS_B2, a.q_stages, a.pds_bufs, a.kv_bufs);
   const size_t smem = one_cta_per_sm(lay.total + 1024);
   auto kern = evo_bwd_main<DP, BF16, HAS_B2>;
   static bool limit_set[64] = {};
@@ -1901,7 +1911,7 @@ cudaError_t launch_bwd_d(BwdArgs a, cudaStream_t st, const ProfileEvents* prof) 
 
   // per-key-tile kernel: double P/dS buffers with the deepest Q/dO ring (at least two
   // stages) that fits; otherwise single buffers
-  auto fits = [&](int qs, int pds) { return MainLayout<DP>(has_b2, qs, pds).total + 1024 <= kMaxSmem; };
+  auto fits = [&](int qs, int pds) { return MainLayout<DP>(has_b2, qs, pds, 2).total + 1024 <= kMaxSmem; };
   int qs = 1, pds = 1;
   for (int q = 4; q >= 2 && pds == 1; --q)
     if (fits(q, 2)) {
@@ -1916,6 +1926,7 @@ cudaError_t launch_bwd_d(BwdArgs a, cudaStream_t st, const ProfileEvents* prof) 
       }
   a.q_stages = qs;
   a.pds_bufs = pds;
+  a.kv_bufs = 2;
   if (a.tile_skip) {  // masked key tiles: skip bits, and zeros for dK/dV of the skipped tiles
     evo_bwd_tile_mask<BF16><<<grid_for(static_cast<long long>(a.B) * a.N * 32, 256), 256, 0, st>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;

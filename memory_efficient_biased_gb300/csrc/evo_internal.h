@@ -80,6 +80,7 @@ struct BwdArgs {
   long long chunk;          // main kernel: consecutive slices per CTA
   int q_stages;             // main kernel: depth of the Q/dO ring
   int pds_bufs;             // main kernel: P and dS shared-memory buffers (1 or 2)
+  int kv_bufs;              // main kernel: K/V buffers (2: the next key tile loads ahead; 1)
   int part_stages;          // pair-bias partial kernel: depth of its ring
   int db2p_tma;             // pair-bias partial kernel: tile stores through tdb2p (L % 4 == 0)
   // Masked key-tile skipping in the per-key-tile kernel (tile_skip; QT <= 64): it skips
