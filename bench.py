@@ -314,12 +314,14 @@ def bias2_groups(w) -> int:
     return -(-w.N // gs)
 
 
-def bwd_mode(w) -> str:
+def bwd_mode(w, skip=False) -> str:
     """Which backward kernel the library runs for this shape (its TMEM-fit rule)."""
     dp = 16 if w.D <= 16 else (32 if w.D <= 32 else 64)
     qt = -(-w.L // 128)
     if dp <= 32 and 384 + 2 * dp + qt * dp <= 512:
         return "key-major"
+    if dp <= 32:  # the streamed key-major kernel; with masked-tile skipping, the per-key-tile one
+        return "main" if skip else "key-major, dQ streamed"
     if 320 + 2 * dp + qt * dp <= 512:
         return "slice"
     return "main"
@@ -503,7 +505,7 @@ def run_ours(args):
     if not status_ok():
         raise RuntimeError("device wait timed out during the instrumented replays")
     # the slots of the kernels that launch (no dQ cast kernel: every schedule writes dQ itself)
-    mode = bwd_mode(w)
+    mode = bwd_mode(w, args.skip_masked_tiles)
     names = ["fwd", "bwd_pre", "bwd_main"] + (["bwd_db2_part", "bwd_db2_sum"] if has_b2 else [])
     pairs = [(0, 1), (2, 3), (3, 4)] + ([(5, 6), (6, 7)] if has_b2 else [])
     kern_ms = {n: statistics.mean(evs[r][a].elapsed_time(evs[r][b]) for r in range(R))
@@ -525,7 +527,7 @@ def run_ours(args):
         "bwd_main": ("tensor", F["bwd"]),
         "bwd_db2_part": ("tensor", 4.0 * E_el * w.D),
         # O, dO read, delta written; plus the transposed pair-bias copy (key-major mode)
-        "bwd_pre": ("hbm", 2 * qkv + bnhl * 4 + (2 * b2b if mode == "key-major" else 0)),
+        "bwd_pre": ("hbm", 2 * qkv + bnhl * 4 + (2 * b2b if mode.startswith("key-major") else 0)),
         "bwd_db2_sum": ("hbm", bias2_groups(w) * w.B * w.H * w.L * w.L * 4 + b2b if has_b2 else 0),
     }
     # The kernels are timed in windows far shorter than the seconds-long loop of the

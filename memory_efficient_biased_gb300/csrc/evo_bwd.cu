@@ -304,9 +304,7 @@ struct MainBars {
 template <int DP>
 struct MainLayout {
   static constexpr uint32_t kTB = kTile * DP * 2;
-  static constexpr uint32_t kDqBlk = 32u * (DP / 2) * 4u;  // a compute warp's fp32 dQ block
-  // staged (and sent) 1 KB at a time: small enough to leave room for a third Q/dO stage
-  static constexpr uint32_t kDqStg = kDqBlk < 1024u ? kDqBlk : 1024u;
+  static constexpr uint32_t kDqStg = DqScr<DP>::kStg;
   Ring p, ds, k, v, q, d_o, b2s, b1, ld, dqs;
   uint32_t bars, total;
   int kvb;  // K/V buffers
@@ -588,107 +586,15 @@ __device__ __forceinline__ void main_mma(const BwdArgs& a, uint8_t* base, const 
   drain_wait(smem_u32(&bars->drain), 0, a.wait_ns, a.status);
 }
 
-// What the compute warps remember of a step until they consume its dQ tile.
-struct DqStep {
-  int b, n, h, it;
-  bool first, last;  // first / last (kept) key tile of its slice
-};
-
-// dQ tile of a step (TMEM lanes = queries of tile it): this warp's DP/2 columns, to
-// its fp32 block of the workspace (a bulk store on the slice's first key tile, a bulk
-// add on later ones), or, on the slice's last key tile, added to the block's sum, scaled
-// and written as dQ in the dtype.  The block is chunk-major ([DP/8][32 rows][4 floats])
-// in both places, so that the staging writes and the read-back are conflict-free.
+// dQ tile of step u (double-buffered in TMEM by step parity): this warp's DP/2 columns
+// into the CTA's fp32 dQ blocks (consume_dq_tile).
 template <int DP, bool BF16>
 __device__ __forceinline__ bool main_consume_dq(const BwdArgs& a, const DqStep& d, uint32_t u, MainBars* bars,
                                                 uint32_t trow, int r, int w, int hc, int lane, uint8_t* stg,
                                                 const WaitGuard& g) {
-  constexpr int HD = DP / 2;
-  constexpr uint32_t kBlk = MainLayout<DP>::kDqBlk, kStg = MainLayout<DP>::kDqStg;
-  constexpr int kPieces = static_cast<int>(kBlk / kStg), kChunks = static_cast<int>(kStg / 512);  // 512 B: 32 rows x 4 floats
   const uint32_t qb = u & 1;
-  if (!mbar_wait_warp(smem_u32(&bars->dq_full[qb]), (u >> 1) & 1, g)) return false;
-  tc_fence_after();
-  float v[HD];
-  const uint32_t col = trow + col_dq<DP>(qb) + hc * HD;
-  if constexpr (HD == 8) {
-    uint32_t x[8];
-    tmem_ld8(col, x);
-    tmem_wait_ld(x);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) v[e] = __uint_as_float(x[e]);
-  } else {
-    uint32_t x[HD / 16][16];
-#pragma unroll
-    for (int q = 0; q < HD / 16; ++q) tmem_ld16(col + q * 16, x[q]);
-#pragma unroll
-    for (int q = 0; q < HD / 16; ++q) tmem_wait_ld(x[q]);
-#pragma unroll
-    for (int q = 0; q < HD / 16; ++q)
-#pragma unroll
-      for (int e = 0; e < 16; ++e) v[q * 16 + e] = __uint_as_float(x[q][e]);
-  }
-  tc_fence_before();
-  __syncwarp();
-  if (lane == 0) mbar_arrive(smem_u32(&bars->dq_free[qb]));
-  float* blk = a.dq_scr + ((static_cast<size_t>(blockIdx.x) * a.QT + d.it) * kComputeWarps + w) * (kBlk / 4);
-  if (!d.last) {
-#pragma unroll
-    for (int pc = 0; pc < kPieces; ++pc) {
-      if (lane == 0) bulk_wait_read_all();  // the previous bulk operation has read the staging block
-      __syncwarp();
-      float4* sp = reinterpret_cast<float4*>(stg);
-#pragma unroll
-      for (int q = 0; q < kChunks; ++q) {
-        const int c = pc * kChunks + q;
-        sp[q * 32 + lane] = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        float* dst = blk + pc * (kStg / 4);
-        if (d.first) {
-          bulk_store_s2g(dst, smem_u32(stg), kStg);
-        } else {
-          bulk_wait_all_but_newest();  // the piece's previous store or add (a sweep ago) is complete
-          bulk_reduce_add_f32(dst, smem_u32(stg), kStg);
-        }
-        bulk_commit_group();
-      }
-    }
-    return true;
-  }
-  if (!d.first) {  // the sum of the slice's earlier key tiles
-    if (lane == 0) {
-      bulk_wait_all_but_newest();
-      fence_proxy_async_global();
-    }
-    __syncwarp();
-    const float4* sp = reinterpret_cast<const float4*>(blk);
-#pragma unroll
-    for (int q = 0; q < HD / 4; ++q) {
-      const float4 o = sp[q * 32 + lane];
-      v[4 * q] += o.x;
-      v[4 * q + 1] += o.y;
-      v[4 * q + 2] += o.z;
-      v[4 * q + 3] += o.w;
-    }
-  }
-  const int i = d.it * kTile + r;
-  if (i >= a.L) return true;
-  const long long bn = static_cast<long long>(d.b) * a.N + d.n;
-  uint16_t* dq = a.dq + bn * a.r_dq.bn + static_cast<long long>(i) * a.r_dq.l + d.h * a.D + hc * HD;
-#pragma unroll
-  for (int e = 0; e < HD; e += 8)
-    if (hc * HD + e < a.D) {
-      uint4 pk;
-      pk.x = pack2<BF16>(v[e + 0] * a.scale, v[e + 1] * a.scale);
-      pk.y = pack2<BF16>(v[e + 2] * a.scale, v[e + 3] * a.scale);
-      pk.z = pack2<BF16>(v[e + 4] * a.scale, v[e + 5] * a.scale);
-      pk.w = pack2<BF16>(v[e + 6] * a.scale, v[e + 7] * a.scale);
-      *reinterpret_cast<uint4*>(dq + e) = pk;
-    }
-  return true;
+  return consume_dq_tile<DP, BF16>(a, d, smem_u32(&bars->dq_full[qb]), smem_u32(&bars->dq_free[qb]), (u >> 1) & 1,
+                                   trow + col_dq<DP>(qb) + hc * (DP / 2), r, w, hc, lane, stg, g);
 }
 
 // What the compute warps remember of an item until they write its dK and dV.
@@ -1890,17 +1796,26 @@ cudaError_t launch_bwd_d(BwdArgs a, cudaStream_t st, const ProfileEvents* prof) 
   a.items = static_cast<long long>(a.B) * a.H * a.QT * a.N;
   const BwdPlan plan = bwd_plan(DP, a.QT, has_b2);
   const int slice_qs = plan.mode == kBwdSlice ? plan.q_stages : 0;
-  if (plan.mode != kBwdKeyMajor && !a.db1p) a.b2t = nullptr;
+  // the streamed key-major kernel does not skip masked tiles: with skipping asked for, the
+  // per-key-tile kernel runs instead (the workspace covers both)
+  const bool km_stream = plan.mode == kBwdKeyMajorStream && !a.tile_skip;
+  const bool km_any = plan.mode == kBwdKeyMajor || km_stream;
+  if (!km_any && !a.db1p) a.b2t = nullptr;
   prof_record(prof, 2, st);
   evo_bwd_pre<DP, BF16><<<grid_for(rows, 256), 256, 0, st>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   prof_record(prof, 3, st);
-  if (plan.mode == kBwdKeyMajor) {
-    a.q_stages = plan.q_stages;
-    if ((e = launch_bwd_kmajor(a, DP, BF16, has_b2, st)) != cudaSuccess) return e;
+  if (km_any) {
+    // The streamed kernel leaves the key-mask gradient to the separate pass, as the
+    // per-key-tile kernel does, so that a call gives the same bytes with or without
+    // masked-tile skipping.
+    BwdArgs ak = a;
+    ak.q_stages = plan.q_stages;
+    if (km_stream) ak.db1p = nullptr;
+    if ((e = launch_bwd_kmajor(ak, DP, BF16, has_b2, km_stream, st)) != cudaSuccess) return e;
     prof_record(prof, 4, st);
-    prof_record(prof, 5, st);  // no dQ cast: dQ stays in TMEM
+    prof_record(prof, 5, st);  // no dQ cast: dQ stays in TMEM or leaves through the workspace
   } else if (slice_qs > 0) {
     a.q_stages = slice_qs;
     e = has_b2 ? launch_slice<DP, BF16, true>(a, st) : launch_slice<DP, BF16, false>(a, st);
@@ -1969,6 +1884,8 @@ template <int DP>
 BwdPlan plan_d(int QT, bool has_b2) {
   const int km = kmajor_q_stages(DP, QT, has_b2);
   if (km > 0) return {kBwdKeyMajor, km};
+  const int kms = kmajor_stream_q_stages(DP, has_b2);
+  if (kms > 0) return {kBwdKeyMajorStream, kms};
   const int sl = slice_q_stages<DP>(QT, has_b2);
   if (sl > 0) return {kBwdSlice, sl};
   return {kBwdMain, 0};

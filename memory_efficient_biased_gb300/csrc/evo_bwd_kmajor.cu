@@ -36,18 +36,26 @@ __device__ __forceinline__ uint32_t km_col_p(uint32_t b) { return kKmP + b * 64u
 
 __host__ __device__ constexpr bool km_tmem_fits(int DP, int QT) { return 384 + 2 * DP + QT * DP <= 512; }
 __host__ __device__ constexpr int km_kv_bufs(int DP, int QT) { return 384 + 4 * DP + QT * DP <= 512 ? 2 : 1; }
+// Streamed dQ (long L): two dQ tile buffers instead of one per query tile.
+__host__ __device__ constexpr bool km_stream_fits(int DP) { return 384 + 2 * DP + 2 * DP <= 512; }
+__host__ __device__ constexpr int km_stream_kv_bufs(int DP) { return 384 + 4 * DP + 2 * DP <= 512 ? 2 : 1; }
+__host__ __device__ constexpr int km_nb(int DP, int QT, bool dqs) { return dqs ? km_stream_kv_bufs(DP) : km_kv_bufs(DP, QT); }
 template <int DP>
 __device__ __forceinline__ uint32_t km_col_dk(uint32_t b) { return kKmAcc + b * 2 * DP; }
 template <int DP>
 __device__ __forceinline__ uint32_t km_col_dv(uint32_t b) { return kKmAcc + b * 2 * DP + DP; }
 template <int DP>
 __device__ __forceinline__ uint32_t km_col_dq(int it, int nb) { return kKmAcc + nb * 2 * DP + it * DP; }
+// streamed dQ: the tile of step u in buffer u & 1
+template <int DP>
+__device__ __forceinline__ uint32_t km_col_dqs(uint32_t b, int nb) { return kKmAcc + nb * 2 * DP + b * DP; }
 
 struct KmBars {
   uint64_t kv_full[2], kv_empty[2];
   uint64_t q_full[kKmMaxQS], q_empty[kKmMaxQS];
   uint64_t st_full, st_free, pds_full, buf_free[2];
   uint64_t dkdv_full[2], dkdv_free[2], dq_full, dq_free;
+  uint64_t dqb_full[2], dqb_free[2];  // streamed dQ: per tile buffer
   uint64_t sd_full[2], sd_free[2];  // key-mask gradient pass: Sᵀ / dPᵀ double buffer
   uint64_t drain;
   uint32_t tmem_slot;
@@ -57,11 +65,12 @@ struct KmBars {
 template <int DP>
 struct KmLayout {
   static constexpr uint32_t kTB = kTile * DP * 2;
-  Ring ds, stg, b2t, k, v, q, d_o, b1, ld;
+  Ring ds, stg, b2t, k, v, q, d_o, b1, ld, dqs;
   uint32_t bars, total;
   // grads: the full backward (dS tiles and output staging); without, the key-mask
-  // gradient pass that only recomputes dS
-  __host__ __device__ KmLayout(bool has_b2, int qs, bool grads = true) {
+  // gradient pass that only recomputes dS.  dq_stream: staging of the streamed dQ
+  // blocks (one per compute warp).
+  __host__ __device__ KmLayout(bool has_b2, int qs, bool grads = true, bool dq_stream = false) {
     uint32_t off = 0;
     ds = Ring{off, 32768u};  // 128B-swizzled tiles first (1024-byte aligned)
     if (grads) off += 2 * 32768u;
@@ -79,6 +88,8 @@ struct KmLayout {
     off += 1024u;
     ld = Ring{off, 1024u};
     off += qs * 1024u;
+    dqs = Ring{off, DqScr<DP>::kStg};
+    if (dq_stream) off += kComputeWarps * DqScr<DP>::kStg;
     bars = off;
     off += (sizeof(KmBars) + 127) & ~127u;
     total = off;
@@ -249,7 +260,7 @@ __device__ __forceinline__ bool km_issue_sdp(const KmStep& st, uint8_t* base, co
 
 // dV += Pᵀ dO (A = Pᵀ in TMEM), dK += dSᵀ Q (A = the dS tile, K-major), then
 // dQ_it += dS K (A = the same tile, MN-major).
-template <int DP, bool BF16>
+template <int DP, bool BF16, bool DQS>
 __device__ __forceinline__ bool km_issue_grads(const KmStep& st, int QT, uint8_t* base, const KmLayout<DP>& lay,
                                                KmBars* bars, uint32_t tmem, const WaitGuard& g) {
   constexpr uint32_t RB = DP * 2;
@@ -258,7 +269,7 @@ __device__ __forceinline__ bool km_issue_grads(const KmStep& st, int QT, uint8_t
   constexpr uint32_t id_k = idesc_f16(128, DP, BF16, false, true);   // K-major A (smem), MN-major B
   constexpr uint32_t id_q = idesc_f16(128, DP, BF16, true, true);    // MN-major A, MN-major B
   const uint32_t kb = st.grp & 1;
-  const int nb = km_kv_bufs(DP, QT);
+  const int nb = km_nb(DP, QT, DQS);
   const uint32_t db = st.grp % nb, dph = (st.grp / nb) & 1;
   const uint32_t b = st.u & 1;
   if (!mbar_wait(smem_u32(&bars->pds_full), st.u & 1, g)) return false;
@@ -282,6 +293,17 @@ __device__ __forceinline__ bool km_issue_grads(const KmStep& st, int QT, uint8_t
             (acc_v | k) ? 1u : 0u);
   umma_commit(smem_u32(&bars->q_empty[st.qs]));
   if (st.it == QT - 1) umma_commit(smem_u32(&bars->dkdv_full[db]));
+  if (DQS) {  // this step's dQ tile, into the buffer its consumer has emptied
+    if (!mbar_wait(smem_u32(&bars->dqb_free[b]), ((st.u >> 1) & 1) ^ 1, g)) return false;
+    tc_fence_after();
+#pragma unroll
+    for (int k = 0; k < 8; ++k)  // dQ tile = dS K_jt   (K = 128 keys)
+      umma_ss(tmem + km_col_dqs<DP>(b, nb), dsmd + k * 128, kd + k * RB, id_q, k > 0 ? 1u : 0u);
+    umma_commit(smem_u32(&bars->dqb_full[b]));
+    umma_commit(smem_u32(&bars->buf_free[b]));
+    if (st.it == QT - 1) umma_commit(smem_u32(&bars->kv_empty[kb]));
+    return true;
+  }
   if (st.it == 0 && st.jt == 0 && !mbar_wait(smem_u32(&bars->dq_free), (st.slice & 1) ^ 1, g)) return false;
   tc_fence_after();
   const uint32_t acc_q = (st.jt > 0) ? 1u : 0u;
@@ -296,7 +318,7 @@ __device__ __forceinline__ bool km_issue_grads(const KmStep& st, int QT, uint8_t
   return true;
 }
 
-template <int DP, bool BF16>
+template <int DP, bool BF16, bool DQS>
 __device__ __forceinline__ void km_mma(const BwdArgs& a, uint8_t* base, const KmLayout<DP>& lay, KmBars* bars,
                                        uint32_t tmem, const WaitGuard& g, long long i0, long long i1) {
   const int QS = a.q_stages, QT = a.QT;
@@ -324,7 +346,7 @@ __device__ __forceinline__ void km_mma(const BwdArgs& a, uint8_t* base, const Km
     KmStep nxt = cur;
     advance(nxt);
     if (u + 1 < total && !km_issue_sdp<DP, BF16>(nxt, base, lay, bars, tmem, g)) break;
-    if (!km_issue_grads<DP, BF16>(cur, QT, base, lay, bars, tmem, g)) break;
+    if (!km_issue_grads<DP, BF16, DQS>(cur, QT, base, lay, bars, tmem, g)) break;
     cur = nxt;
   }
   umma_commit(smem_u32(&bars->drain));
@@ -468,12 +490,12 @@ __device__ __forceinline__ void km_stage_close() {
 }
 
 // dK (× s) and dV of key tile jt of slice c.
-template <int DP, bool BF16>
+template <int DP, bool BF16, bool DQS>
 __device__ __forceinline__ bool km_write_dkdv(const BwdArgs& a, const SlIter& c, int jt, uint32_t grp, uint8_t* base,
                                               const KmLayout<DP>& lay, KmBars* bars, uint32_t trow, int w, int hc,
                                               int lane, const WaitGuard& g) {
   constexpr int HD = DP / 2;
-  const int nb = km_kv_bufs(DP, a.QT);
+  const int nb = km_nb(DP, a.QT, DQS);
   const uint32_t db = grp % nb;
   if (!mbar_wait_warp(smem_u32(&bars->dkdv_full[db]), (grp / nb) & 1, g)) return false;
   tc_fence_after();
@@ -540,7 +562,7 @@ __device__ __forceinline__ void km_store_db1(const BwdArgs& a, const SlIter& c, 
     a.db1p[((static_cast<size_t>(c.b * a.N + c.n) * a.H + c.h) * 2 + hc) * a.L + j] = v;
 }
 
-template <int DP, bool BF16, bool HAS_B2, bool DB1>
+template <int DP, bool BF16, bool HAS_B2, bool DB1, bool DQS>
 __device__ __forceinline__ void km_compute(const BwdArgs& a, uint8_t* base, const KmLayout<DP>& lay, KmBars* bars,
                                            uint32_t tmem, const WaitGuard& g, long long i0, long long i1) {
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -555,6 +577,16 @@ __device__ __forceinline__ void km_compute(const BwdArgs& a, uint8_t* base, cons
   prev = cur;
   float b1j = 0.0f;
   float2 dsum = make_float2(0.0f, 0.0f);  // DB1: Σ over the key tile's queries of this key's dS
+  // DQS: the previous step's dQ tile is consumed one step late (its MMAs are done by then)
+  const int nbq = km_nb(DP, QT, DQS);
+  uint8_t* dq_stg = base + lay.dqs[w];
+  DqStep pd{0, 0, 0, 0, false, false};
+  auto consume = [&](uint32_t v) {
+    const uint32_t qb = v & 1;
+    return consume_dq_tile<DP, BF16>(a, pd, smem_u32(&bars->dqb_full[qb]), smem_u32(&bars->dqb_free[qb]),
+                                     (v >> 1) & 1, trow + km_col_dqs<DP>(qb, nbq) + hc * (DP / 2), r, w, hc, lane,
+                                     dq_stg, g);
+  };
   bool ok = true;
   for (long long item = i0; ok && item < i1; ++item, ++slice) {
     if (item > i0) {
@@ -624,6 +656,10 @@ __device__ __forceinline__ void km_compute(const BwdArgs& a, uint8_t* base, cons
           s = 0;
           ph ^= 1;
         }
+        if (DQS) {
+          if (u > 0 && !consume(u - 1)) { ok = false; break; }
+          pd = DqStep{cur.b, cur.n, cur.h, it, jt == 0, jt == QT - 1};
+        }
         if (DB1 && it == QT - 1) {  // this key's share over the slice's queries, per query half
           km_store_db1(a, cur, hc, jt * kTile + r, dsum.x + dsum.y);
           dsum = make_float2(0.0f, 0.0f);
@@ -631,12 +667,12 @@ __device__ __forceinline__ void km_compute(const BwdArgs& a, uint8_t* base, cons
         // one step late (their MMAs are done by now): dK/dV of the previous key tile and,
         // at a slice boundary, the previous slice's dQ
         if (it == 0 && grp > 0 &&
-            !km_write_dkdv<DP, BF16>(a, jt > 0 ? cur : prev, jt > 0 ? jt - 1 : QT - 1, grp - 1, base, lay, bars,
-                                     trow, w, hc, lane, g)) {
+            !km_write_dkdv<DP, BF16, DQS>(a, jt > 0 ? cur : prev, jt > 0 ? jt - 1 : QT - 1, grp - 1, base, lay,
+                                          bars, trow, w, hc, lane, g)) {
           ok = false;
           break;
         }
-        if (it == 0 && jt == 0 && slice > 0 &&
+        if (!DQS && it == 0 && jt == 0 && slice > 0 &&
             !km_write_dq<DP, BF16>(a, prev, slice - 1, base, lay, bars, trow, w, hc, lane, g)) {
           ok = false;
           break;
@@ -645,17 +681,20 @@ __device__ __forceinline__ void km_compute(const BwdArgs& a, uint8_t* base, cons
     }
   }
   if (ok && grp > 0) {
-    if (km_write_dkdv<DP, BF16>(a, cur, QT - 1, grp - 1, base, lay, bars, trow, w, hc, lane, g))
+    if (DQS) {
+      if (consume(u - 1)) km_write_dkdv<DP, BF16, DQS>(a, cur, QT - 1, grp - 1, base, lay, bars, trow, w, hc, lane, g);
+    } else if (km_write_dkdv<DP, BF16, DQS>(a, cur, QT - 1, grp - 1, base, lay, bars, trow, w, hc, lane, g)) {
       km_write_dq<DP, BF16>(a, cur, slice - 1, base, lay, bars, trow, w, hc, lane, g);
+    }
   }
   if (lane == 0) bulk_wait_all();  // this warp's tile stores complete before the CTA's smem goes away
 }
 
-template <int DP, bool BF16, bool HAS_B2, bool DB1>
+template <int DP, bool BF16, bool HAS_B2, bool DB1, bool DQS>
 __global__ void __launch_bounds__(kThreads, 1) evo_bwd_kmajor(const __grid_constant__ BwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const KmLayout<DP> lay(HAS_B2, a.q_stages);
+  const KmLayout<DP> lay(HAS_B2, a.q_stages, true, DQS);
   KmBars* bars = reinterpret_cast<KmBars*>(base + lay.bars);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long i0 = static_cast<long long>(blockIdx.x) * a.chunk;
@@ -668,6 +707,8 @@ __global__ void __launch_bounds__(kThreads, 1) evo_bwd_kmajor(const __grid_const
       mbar_init(smem_u32(&bars->buf_free[s]), 1);
       mbar_init(smem_u32(&bars->dkdv_full[s]), 1);
       mbar_init(smem_u32(&bars->dkdv_free[s]), kComputeWarps);
+      mbar_init(smem_u32(&bars->dqb_full[s]), 1);
+      mbar_init(smem_u32(&bars->dqb_free[s]), kComputeWarps);
     }
     for (int s = 0; s < kKmMaxQS; ++s) {
       mbar_init(smem_u32(&bars->q_full[s]), 32);
@@ -702,10 +743,10 @@ __global__ void __launch_bounds__(kThreads, 1) evo_bwd_kmajor(const __grid_const
   if (warp == kProducerWarp) {
     km_producer<DP, BF16, HAS_B2>(a, base, lay, bars, g, lane, i0, i1);
   } else if (warp == kMmaWarp) {
-    if (lane == 0) km_mma<DP, BF16>(a, base, lay, bars, tmem, g, i0, i1);
+    if (lane == 0) km_mma<DP, BF16, DQS>(a, base, lay, bars, tmem, g, i0, i1);
     __syncwarp();
   } else {
-    km_compute<DP, BF16, HAS_B2, DB1>(a, base, lay, bars, tmem, g, i0, i1);
+    km_compute<DP, BF16, HAS_B2, DB1, DQS>(a, base, lay, bars, tmem, g, i0, i1);
   }
   tc_fence_before();
   __syncthreads();
@@ -962,12 +1003,20 @@ int km_stages(int QT, bool has_b2) {
     if (KmLayout<DP>(has_b2, qs).total + 1024 <= kMaxSmem) return qs;
   return 0;
 }
+// Streamed dQ: any number of query tiles (their dQ leaves through the workspace each step).
+template <int DP>
+int km_stream_stages(bool has_b2) {
+  if (!km_stream_fits(DP)) return 0;
+  for (int qs = kKmMaxQS; qs >= 2; --qs)
+    if (KmLayout<DP>(has_b2, qs, true, true).total + 1024 <= kMaxSmem) return qs;
+  return 0;
+}
 
-template <int DP, bool BF16, bool HAS_B2, bool DB1>
+template <int DP, bool BF16, bool HAS_B2, bool DB1, bool DQS>
 cudaError_t launch_km(BwdArgs a, cudaStream_t st) {
-  const KmLayout<DP> lay(HAS_B2, a.q_stages);
+  const KmLayout<DP> lay(HAS_B2, a.q_stages, true, DQS);
   const size_t smem = one_cta_per_sm(lay.total + 1024);
-  auto kern = evo_bwd_kmajor<DP, BF16, HAS_B2, DB1>;
+  auto kern = evo_bwd_kmajor<DP, BF16, HAS_B2, DB1, DQS>;
   static bool limit_set[64] = {};
   cudaError_t e = ensure_smem_limit(kern, kMaxSmem, limit_set);
   if (e != cudaSuccess) return e;
@@ -979,15 +1028,17 @@ cudaError_t launch_km(BwdArgs a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-template <int DP, bool BF16>
+template <int DP, bool BF16, bool DQS>
 cudaError_t launch_km_b(const BwdArgs& a, bool has_b2, cudaStream_t st) {
-  if (a.db1p) return has_b2 ? launch_km<DP, BF16, true, true>(a, st) : launch_km<DP, BF16, false, true>(a, st);
-  return has_b2 ? launch_km<DP, BF16, true, false>(a, st) : launch_km<DP, BF16, false, false>(a, st);
+  if (a.db1p)
+    return has_b2 ? launch_km<DP, BF16, true, true, DQS>(a, st) : launch_km<DP, BF16, false, true, DQS>(a, st);
+  return has_b2 ? launch_km<DP, BF16, true, false, DQS>(a, st) : launch_km<DP, BF16, false, false, DQS>(a, st);
 }
 
 template <int DP>
-cudaError_t launch_km_d(const BwdArgs& a, bool bf16, bool has_b2, cudaStream_t st) {
-  return bf16 ? launch_km_b<DP, true>(a, has_b2, st) : launch_km_b<DP, false>(a, has_b2, st);
+cudaError_t launch_km_d(const BwdArgs& a, bool bf16, bool has_b2, bool dqs, cudaStream_t st) {
+  if (dqs) return bf16 ? launch_km_b<DP, true, true>(a, has_b2, st) : launch_km_b<DP, false, true>(a, has_b2, st);
+  return bf16 ? launch_km_b<DP, true, false>(a, has_b2, st) : launch_km_b<DP, false, false>(a, has_b2, st);
 }
 
 }  // namespace
@@ -996,6 +1047,13 @@ int kmajor_q_stages(int DP, int QT, bool has_b2) {
   switch (DP) {
     case 16: return km_stages<16>(QT, has_b2);
     case 32: return km_stages<32>(QT, has_b2);
+    default: return 0;
+  }
+}
+int kmajor_stream_q_stages(int DP, bool has_b2) {
+  switch (DP) {
+    case 16: return km_stream_stages<16>(has_b2);
+    case 32: return km_stream_stages<32>(has_b2);
     default: return 0;
   }
 }
@@ -1021,10 +1079,10 @@ cudaError_t launch_bwd_db1_sum(const BwdArgs& a, bool bf16, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_kmajor(const BwdArgs& a, int DP, bool bf16, bool has_b2, cudaStream_t st) {
+cudaError_t launch_bwd_kmajor(const BwdArgs& a, int DP, bool bf16, bool has_b2, bool dq_stream, cudaStream_t st) {
   switch (DP) {
-    case 16: return launch_km_d<16>(a, bf16, has_b2, st);
-    case 32: return launch_km_d<32>(a, bf16, has_b2, st);
+    case 16: return launch_km_d<16>(a, bf16, has_b2, dq_stream, st);
+    case 32: return launch_km_d<32>(a, bf16, has_b2, dq_stream, st);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -345,13 +345,13 @@ WsLayout ws_layout(const evo_shape_t& s, bool has_bias2, bool has_db1 = false, b
   w.delta = off;
   off += round256(size_t(s.B) * s.N * s.H * s.L * 4);
   w.dq_scr = off;
-  if (w.plan.mode == kBwdMain) {
+  if (w.plan.mode == kBwdMain || w.plan.mode == kBwdKeyMajorStream) {
     const int64_t slices = s.B * s.H * s.N;
     const int64_t ctas = slices < kMainMaxCtas ? slices : kMainMaxCtas;
     off += round256(size_t(ctas) * ((s.L + kTile - 1) / kTile) * kTile * padded_dim(s.D) * 4);
   }
   w.b2t = off;
-  if ((w.plan.mode == kBwdKeyMajor || has_db1) && has_bias2)
+  if ((w.plan.mode == kBwdKeyMajor || w.plan.mode == kBwdKeyMajorStream || has_db1) && has_bias2)
     off += round256(size_t(s.B) * s.H * s.L * b2t_pitch(s) * 2);
   w.db1p = off;
   if (has_db1) off += round256(size_t(s.B) * s.N * s.H * 2 * s.L * 4);
@@ -364,7 +364,7 @@ WsLayout ws_layout(const evo_shape_t& s, bool has_bias2, bool has_db1 = false, b
   // masked-tile skipping of the per-key-tile kernel: skip bits [B*N] u64
   const int64_t QT = (s.L + kTile - 1) / kTile;
   w.skip = off;
-  w.can_skip = w.plan.mode == kBwdMain && QT <= 64;
+  w.can_skip = (w.plan.mode == kBwdMain || w.plan.mode == kBwdKeyMajorStream) && QT <= 64;
   if (w.can_skip) off += round256(size_t(s.B) * s.N * 8);
   w.total = off;
   return w;
@@ -699,7 +699,7 @@ evo_status_t bwd_impl(const void* q, const void* k, const void* v, const void* b
       a.dbias1 = static_cast<uint16_t*>(dbias1) + b1_off;
       a.db1p = reinterpret_cast<float*>(ws + w.db1p);
     }
-    if (bias2 && (w.plan.mode == kBwdKeyMajor || dbias1)) {
+    if (bias2 && (w.plan.mode == kBwdKeyMajor || w.plan.mode == kBwdKeyMajorStream || dbias1)) {
       a.b2t = reinterpret_cast<uint16_t*>(ws + w.b2t);
       a.b2t_pitch = b2t_pitch(sub);
       if (!map_b2t(&a.tb2t, a.b2t, sub, bf16, a.b2t_pitch)) return EVO_ERR_CUDA;

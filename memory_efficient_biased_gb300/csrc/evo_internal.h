@@ -136,14 +136,15 @@ cudaError_t ensure_smem_limit(Kernel kern, size_t bytes, bool (&done)[64]) {
 // Which backward kernel runs for a shape (shared by workspace sizing and launch):
 // key-major slice kernel, query-major slice kernel (both keep dQ in TMEM), or the
 // per-key-tile kernel with an fp32 dQ accumulator in the workspace.
-enum BwdMode : int { kBwdKeyMajor = 0, kBwdSlice = 1, kBwdMain = 2 };
+enum BwdMode : int { kBwdKeyMajor = 0, kBwdSlice = 1, kBwdMain = 2, kBwdKeyMajorStream = 3 };
 struct BwdPlan {
   int mode;
   int q_stages;
 };
 BwdPlan bwd_plan(int DP, int QT, bool has_b2);
 int kmajor_q_stages(int DP, int QT, bool has_b2);
-cudaError_t launch_bwd_kmajor(const BwdArgs& a, int DP, bool bf16, bool has_b2, cudaStream_t st);
+int kmajor_stream_q_stages(int DP, bool has_b2);
+cudaError_t launch_bwd_kmajor(const BwdArgs& a, int DP, bool bf16, bool has_b2, bool dq_stream, cudaStream_t st);
 // Key-mask gradient partials (a.db1p) by the key-major score recompute alone, for the
 // schedules whose main kernel does not produce them; then the fixed-order sum into a.dbias1.
 cudaError_t launch_bwd_db1_partials(const BwdArgs& a, int DP, bool bf16, bool has_b2, cudaStream_t st);
