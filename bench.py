@@ -305,13 +305,24 @@ def memory_versus_dense(d):
 
 
 def bias2_groups(w) -> int:
-    """n-groups of the two-stage pair-bias gradient: the library's rule (enough
-    (b, h, query tile, key tile, group) blocks for two waves on 152 SMs)."""
+    """n-groups of the two-stage pair-bias gradient: the library's rule (at least two
+    waves of 152 (b, h, query tile, key tile, group) blocks; among up to four times as
+    many groups, the fewest that fill the last wave to 95 %, else the fullest)."""
     qt = -(-w.L // 128)
     tiles = w.B * w.H * qt * qt
-    g = max(1, min(w.N, -(-304 // tiles)))
-    gs = -(-w.N // g)
-    return -(-w.N // gs)
+    n = max(1, w.N)
+    g0 = max(1, min(n, -(-304 // tiles)))
+    best, best_eff = 0, -1.0
+    for g in range(g0, min(4 * g0, n) + 1):
+        gs = -(-n // g)
+        ge = -(-n // gs)
+        ctas = tiles * ge
+        eff = ctas / (-(-ctas // 152) * 152)
+        if eff > best_eff + 1e-9:
+            best, best_eff = ge, eff
+        if eff >= 0.95:
+            break
+    return best
 
 
 def bwd_mode(w, skip=False) -> str:

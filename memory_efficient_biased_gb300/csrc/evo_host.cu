@@ -310,16 +310,33 @@ size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // n-groups of the deterministic two-stage pair-bias gradient: enough
 // (b, h, q-tile, k-tile, group) blocks for two waves over 152 SMs.
+// n-groups of the pair-bias partial kernel (one CTA per (b, h, query tile, key tile,
+// group)): at least two waves of 152 CTAs, and, among up to four times that many
+// groups, the fewest whose CTAs fill the last wave to 95 % (else the fullest last wave),
+// so that no SM idles through a nearly empty last wave.
 void bwd_groups(const evo_shape_t& s, int* groups, int* group_size) {
+  constexpr int64_t kWave = 152;
   const int64_t QT = (s.L + kTile - 1) / kTile;
   const int64_t tiles = s.B * s.H * QT * QT;
-  int64_t g = (304 + tiles - 1) / tiles;
-  if (g < 1) g = 1;
-  if (g > s.N) g = s.N;
-  int64_t gs = (s.N + g - 1) / g;
-  g = (s.N + gs - 1) / gs;
-  *groups = static_cast<int>(g);
-  *group_size = static_cast<int>(gs);
+  const int64_t n = s.N > 0 ? s.N : 1;
+  int64_t g0 = (2 * kWave + tiles - 1) / tiles;
+  if (g0 < 1) g0 = 1;
+  if (g0 > n) g0 = n;
+  int64_t best_g = 0, best_gs = 0;
+  double best_eff = -1.0;
+  for (int64_t g = g0; g <= 4 * g0 && g <= n; ++g) {
+    const int64_t gs = (n + g - 1) / g, ge = (n + gs - 1) / gs;  // groups after rounding the size
+    const int64_t ctas = tiles * ge, waves = (ctas + kWave - 1) / kWave;
+    const double eff = static_cast<double>(ctas) / static_cast<double>(waves * kWave);
+    if (eff > best_eff + 1e-9) {
+      best_eff = eff;
+      best_g = ge;
+      best_gs = gs;
+    }
+    if (eff >= 0.95) break;
+  }
+  *groups = static_cast<int>(best_g);
+  *group_size = static_cast<int>(best_gs);
 }
 
 int b2t_pitch(const evo_shape_t& s) { return static_cast<int>((s.L + 7) / 8 * 8); }
