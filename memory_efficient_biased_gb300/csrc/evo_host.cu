@@ -836,9 +836,12 @@ evo_status_t evo_attn_step_host(const void* q, const void* k, const void* v, con
   // and chunk c-1's results travel back (stream co).  Without a pair bias the backward
   // runs chunk by chunk too; with one it runs once over all rows (its gradient sums
   // over every n), and dQ, dK, dV start back as soon as its main kernel is done.
+  // With a pair bias only the forward runs in chunks, and smaller forward launches cost
+  // more than the overlap gains past two chunks (measured on triangle, many_head, msa_row).
   const int64_t slices = shape.B * shape.N * shape.H;
   int64_t target = slices / (2 * static_cast<int64_t>(dev->sms > 0 ? dev->sms : 148));
   target = target < 1 ? 1 : (target > 8 ? 8 : target);
+  if (bias2 != nullptr && target > 2) target = 2;
   int64_t per_b = (target + shape.B - 1) / shape.B;
   if (per_b > shape.N) per_b = shape.N;
   const int64_t nc = (shape.N + per_b - 1) / per_b;  // rows per chunk
