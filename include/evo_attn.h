@@ -373,7 +373,8 @@ EVO_API evo_status_t evo_attn_selftest_wait_timeout(uint64_t limit_ns, int* stat
 
 /*
  * Bytes of device arena evo_attn_step_host needs for this problem (0 on a bad
- * shape or dtype): room for the inputs, outputs, lse and backward workspace.
+ * shape or dtype): room for the inputs, outputs, lse and backward workspace
+ * (and, with a pair bias and B = 1, the fp32 partial planes of its gradient).
  */
 EVO_API size_t evo_attn_step_host_arena_bytes(evo_shape_t shape, evo_dtype_t dtype, int has_bias1,
                                               int has_bias2);
@@ -384,9 +385,13 @@ EVO_API size_t evo_attn_step_host_arena_bytes(evo_shape_t shape, evo_dtype_t dty
  * the caller's device arena (one cudaMemcpyAsync per tensor), runs
  * evo_attn_fwd and evo_attn_bwd there, and copies out, dq, dk, dv, dbias2
  * (required iff bias2 != NULL) and, when lse != NULL, lse back to host
- * buffers.  Host buffers should be page-locked for the copies to be
- * asynchronous; all work is queued on `stream`, so synchronise it before
- * reading the outputs.  arena: device memory of at least
+ * buffers.  The work runs in chunks of rows (b, n), so that the copies of one
+ * chunk overlap another's compute; with a pair bias and B = 1 each chunk's
+ * backward writes the partial sums of its own n-groups of the pair-bias
+ * gradient and one fixed-order sum follows, so every output is the same bytes
+ * as evo_attn_fwd + evo_attn_bwd on device buffers give.  Host buffers should
+ * be page-locked for the copies to be asynchronous; all work is queued on
+ * `stream`, so synchronise it before reading the outputs.  arena: device memory of at least
  * evo_attn_step_host_arena_bytes(...) bytes, 256-byte aligned, caller-owned.
  * Host pointers have no alignment rule.  Validation as in evo_attn_fwd/bwd.
  */

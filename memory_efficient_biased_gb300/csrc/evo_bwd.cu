@@ -1872,9 +1872,11 @@ cudaError_t launch_bwd_d(BwdArgs a, cudaStream_t st, const ProfileEvents* prof) 
     kern<<<static_cast<unsigned>(blocks), kThreads, smem, st>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     prof_record(prof, 6, st);
-    const long long plane = static_cast<long long>(a.B) * a.H * a.L * a.L;
-    evo_bwd_db2_sum<BF16><<<grid_for(plane, 256), 256, 0, st>>>(a);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (!a.db2_no_sum) {
+      const long long plane = static_cast<long long>(a.B) * a.H * a.L * a.L;
+      evo_bwd_db2_sum<BF16><<<grid_for(plane, 256), 256, 0, st>>>(a);
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
     prof_record(prof, 7, st);
   }
   return cudaSuccess;
@@ -1899,6 +1901,16 @@ BwdPlan bwd_plan(int DP, int QT, bool has_b2) {
     case 32: return plan_d<32>(QT, has_b2);
     default: return plan_d<64>(QT, has_b2);
   }
+}
+
+cudaError_t launch_bwd_db2_sum(const BwdArgs& a, bool bf16, cudaStream_t st) {
+  const long long plane = static_cast<long long>(a.B) * a.H * a.L * a.L;
+  if (plane <= 0 || a.groups <= 0) return cudaSuccess;
+  if (bf16)
+    evo_bwd_db2_sum<true><<<grid_for(plane, 256), 256, 0, st>>>(a);
+  else
+    evo_bwd_db2_sum<false><<<grid_for(plane, 256), 256, 0, st>>>(a);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_bwd(const BwdArgs& a, int DP, bool bf16, cudaStream_t st, const ProfileEvents* p) {

@@ -73,6 +73,11 @@ struct CallOpts {
   int* status = nullptr;  // where kernels record a timeout; nullptr = the call's default location
   bool no_db2 = false;
   ProfileEvents prof{{nullptr}, 0};
+  // internal (the host-buffer step's row chunks): the pair-bias gradient's n-group size
+  // (0: the shape's own rule), the partial planes written to db2_planes (one per group
+  // of this call, H planes of L x L each) and not summed
+  int db2_group_size = 0;
+  float* db2_planes = nullptr;
 };
 
 // Reads *o into c; false when the struct is malformed.
@@ -642,7 +647,8 @@ evo_status_t bwd_impl(const void* q, const void* k, const void* v, const void* b
   for (const evo_strides_t& x : t) whole = whole && merges(x, shape);
   evo_shape_t sub = shape;
   sub.B = whole ? shape.B : 1;
-  const WsLayout w = ws_layout(sub, bias2 != nullptr, dbias1 != nullptr, dbias2 != nullptr);
+  // (partial planes written elsewhere take no room in the workspace)
+  const WsLayout w = ws_layout(sub, bias2 != nullptr, dbias1 != nullptr, dbias2 != nullptr && !co.db2_planes);
   if (workspace_bytes < w.total) return EVO_ERR_WORKSPACE_TOO_SMALL;
   const Range ins[8] = {{q, span_bytes(t[Q], shape)},      {k, span_bytes(t[K], shape)},
                         {v, span_bytes(t[V], shape)},      {bias1, bias1 ? bias1_bytes(shape) : 0},
@@ -728,6 +734,14 @@ evo_status_t bwd_impl(const void* q, const void* k, const void* v, const void* b
     a.D = static_cast<int>(shape.D);
     a.QT = static_cast<int>((shape.L + kTile - 1) / kTile);
     bwd_groups(sub, &a.groups, &a.group_size);
+    if (co.db2_group_size > 0) {
+      a.group_size = co.db2_group_size;
+      a.groups = static_cast<int>((sub.N + a.group_size - 1) / a.group_size);
+    }
+    if (co.db2_planes && dbias2) {
+      a.db2_part = co.db2_planes;
+      a.db2_no_sum = 1;
+    }
     if (dbias2 && shape.L % 4 == 0) {
       if (!map_db2_part(&a.tdb2p, a.db2_part, sub, a.groups)) return EVO_ERR_CUDA;
       a.db2p_tma = 1;
@@ -782,8 +796,13 @@ evo_status_t evo_attn_selftest_wait_timeout(uint64_t limit_ns, int* status, void
 
 namespace {
 struct ArenaLayout {
-  size_t q, k, v, dout, out, dq, dk, dv, b1, b2, db2, lse, ws, total;
+  size_t q, k, v, dout, out, dq, dk, dv, b1, b2, db2, db2p, lse, ws, total;
 };
+// The host-buffer step runs the backward chunk by chunk with a pair bias too when B = 1:
+// each chunk writes the pair-bias partial planes of its n-groups (the whole call's
+// groups, so that the chunk boundaries fall on group boundaries) into one buffer, summed
+// once at the end in the same fixed order as an unchunked call.
+bool chunked_db2(const evo_shape_t& s, bool has_b2) { return has_b2 && s.B == 1; }
 ArenaLayout arena_layout(const evo_shape_t& s, bool has_b1, bool has_b2) {
   ArenaLayout a{};
   size_t off = 0;
@@ -799,6 +818,12 @@ ArenaLayout arena_layout(const evo_shape_t& s, bool has_b1, bool has_b2) {
   if (has_b2) off += round256(bias2_bytes(s));
   a.db2 = off;
   if (has_b2) off += round256(bias2_bytes(s));
+  a.db2p = off;
+  if (chunked_db2(s, has_b2)) {
+    int g = 0, gs = 0;
+    bwd_groups(s, &g, &gs);
+    off += round256(size_t(g) * s.H * s.L * s.L * 4);
+  }
   a.lse = off;
   off += round256(lse_bytes(s));
   a.ws = off;
@@ -836,19 +861,33 @@ evo_status_t evo_attn_step_host(const void* q, const void* k, const void* v, con
   // and chunk c-1's results travel back (stream co).  Without a pair bias the backward
   // runs chunk by chunk too; with one it runs once over all rows (its gradient sums
   // over every n), and dQ, dK, dV start back as soon as its main kernel is done.
-  // With a pair bias only the forward runs in chunks, and smaller forward launches cost
-  // more than the overlap gains past two chunks (measured on triangle, many_head, msa_row).
+  // With a pair bias and B = 1 the backward runs in chunks too (whole n-groups of the
+  // pair-bias gradient per chunk): four chunks measured best on triangle, many_head and
+  // msa_row.  With a pair bias and B > 1 only the forward runs in chunks, and smaller
+  // forward launches cost more than the overlap gains past two.
+  const bool db2_chunks = chunked_db2(shape, bias2 != nullptr);
+  const int64_t sms = dev->sms > 0 ? dev->sms : 148;
   const int64_t slices = shape.B * shape.N * shape.H;
-  int64_t target = slices / (2 * static_cast<int64_t>(dev->sms > 0 ? dev->sms : 148));
+  int64_t target = slices / (2 * sms);
   target = target < 1 ? 1 : (target > 8 ? 8 : target);
-  if (bias2 != nullptr && target > 2) target = 2;
+  if (db2_chunks && slices >= 4 * sms) target = 4;
+  if (bias2 != nullptr && !db2_chunks && target > 2) target = 2;
   int64_t per_b = (target + shape.B - 1) / shape.B;
   if (per_b > shape.N) per_b = shape.N;
   const int64_t nc = (shape.N + per_b - 1) / per_b;  // rows per chunk
   const int64_t chunks_per_b = (shape.N + nc - 1) / nc;
-  const int64_t chunks = shape.B * chunks_per_b;
+  int64_t chunks = shape.B * chunks_per_b;
   if (chunks > 64) return EVO_ERR_BAD_SHAPE;  // cannot happen: target <= 8 and B * ceil(8 / B) <= 8 + B
-  const bool chunk_bwd = bias2 == nullptr;
+  const bool chunk_bwd = bias2 == nullptr || db2_chunks;
+  int db2_groups = 0, db2_gs = 0;
+  int64_t nc_rows = nc;  // rows per chunk
+  if (db2_chunks) {  // whole pair-bias n-groups per chunk
+    bwd_groups(shape, &db2_groups, &db2_gs);
+    const int64_t gpc = (db2_groups + target - 1) / target;
+    nc_rows = gpc * db2_gs;
+    if (nc_rows > shape.N) nc_rows = shape.N;
+    chunks = (shape.N + nc_rows - 1) / nc_rows;
+  }
 
   struct Res {
     cudaStream_t ci = nullptr, co = nullptr;
@@ -892,10 +931,17 @@ evo_status_t evo_attn_step_host(const void* q, const void* k, const void* v, con
   };
   const auto hp = [](const void* p, size_t off) { return static_cast<const uint8_t*>(p) + off; };
   const auto hw = [](void* p, size_t off) { return static_cast<uint8_t*>(p) + off; };
+  // chunk c: batch b, rows n0 .. n0 + nn
+  const int64_t cpb = db2_chunks ? chunks : chunks_per_b, rpc = db2_chunks ? nc_rows : nc;
+  auto chunk_rows = [&](int64_t c, int64_t* b, int64_t* n0, int64_t* nn) {
+    *b = c / cpb;
+    *n0 = (c % cpb) * rpc;
+    *nn = shape.N - *n0 < rpc ? shape.N - *n0 : rpc;
+  };
   if (bias2) h2d(L.b2, bias2, bias2_bytes(shape));
   for (int64_t c = 0; c < chunks; ++c) {
-    const int64_t b = c / chunks_per_b, n0 = (c % chunks_per_b) * nc;
-    const int64_t nn = shape.N - n0 < nc ? shape.N - n0 : nc;
+    int64_t b, n0, nn;
+    chunk_rows(c, &b, &n0, &nn);
     const size_t row0 = size_t(b * shape.N + n0), rows = size_t(nn);
     h2d(L.q + row0 * row_qkv, hp(q, row0 * row_qkv), rows * row_qkv);
     h2d(L.k + row0 * row_qkv, hp(k, row0 * row_qkv), rows * row_qkv);
@@ -905,8 +951,8 @@ evo_status_t evo_attn_step_host(const void* q, const void* k, const void* v, con
     ok(cudaEventRecord(ev_in(c), r.ci));
   }
   for (int64_t c = 0; c < chunks && e == cudaSuccess && st == EVO_OK; ++c) {
-    const int64_t b = c / chunks_per_b, n0 = (c % chunks_per_b) * nc;
-    const int64_t nn = shape.N - n0 < nc ? shape.N - n0 : nc;
+    int64_t b, n0, nn;
+    chunk_rows(c, &b, &n0, &nn);
     const size_t row0 = size_t(b * shape.N + n0), rows = size_t(nn);
     const evo_shape_t sub{1, nn, shape.L, shape.H, shape.D};
     uint8_t* cq = A + L.q + row0 * row_qkv;
@@ -921,10 +967,19 @@ evo_status_t evo_attn_step_host(const void* q, const void* k, const void* v, con
     st = evo_attn_fwd(cq, ck, cv, cb1, cb2, cout, clse, sub, dtype, stream);
     if (st != EVO_OK) break;
     ok(cudaEventRecord(ev_fwd(c), s));
-    if (chunk_bwd) {
+    if (chunk_bwd && !db2_chunks) {
       st = evo_attn_bwd(cq, ck, cv, cb1, nullptr, cout, clse, cdo, A + L.dq + row0 * row_qkv,
                         A + L.dk + row0 * row_qkv, A + L.dv + row0 * row_qkv, nullptr, A + L.ws, arena_bytes - L.ws,
                         sub, dtype, stream);
+      if (st != EVO_OK) break;
+      ok(cudaEventRecord(ev_bwd(c), s));
+    } else if (db2_chunks) {  // this chunk's n-groups of pair-bias partials, summed after the last chunk
+      CallOpts co;
+      co.db2_group_size = db2_gs;
+      co.db2_planes = reinterpret_cast<float*>(A + L.db2p) + size_t(n0 / db2_gs) * shape.H * shape.L * shape.L;
+      st = bwd_impl(cq, ck, cv, cb1, cb2, cout, clse, cdo, A + L.dq + row0 * row_qkv, A + L.dk + row0 * row_qkv,
+                    A + L.dv + row0 * row_qkv, nullptr, A + L.db2, A + L.ws, arena_bytes - L.ws, sub, dtype, nullptr,
+                    co, true, stream);
       if (st != EVO_OK) break;
       ok(cudaEventRecord(ev_bwd(c), s));
     }
@@ -937,6 +992,21 @@ evo_status_t evo_attn_step_host(const void* q, const void* k, const void* v, con
       d2h(hw(dk, row0 * row_qkv), L.dk + row0 * row_qkv, rows * row_qkv);
       d2h(hw(dv, row0 * row_qkv), L.dv + row0 * row_qkv, rows * row_qkv);
     }
+  }
+  if (db2_chunks && e == cudaSuccess && st == EVO_OK) {  // the pair-bias gradient: every group's planes
+    BwdArgs sa;
+    std::memset(&sa, 0, sizeof(sa));
+    sa.B = 1;
+    sa.N = static_cast<int>(shape.N);
+    sa.H = static_cast<int>(shape.H);
+    sa.L = static_cast<int>(shape.L);
+    sa.groups = db2_groups;
+    sa.db2_part = reinterpret_cast<float*>(A + L.db2p);
+    sa.dbias2 = reinterpret_cast<uint16_t*>(A + L.db2);
+    ok(launch_bwd_db2_sum(sa, dtype == EVO_BF16, s));
+    ok(cudaEventRecord(ev_mid, s));
+    ok(cudaStreamWaitEvent(r.co, ev_mid, 0));
+    d2h(dbias2, L.db2, bias2_bytes(shape));
   }
   if (!chunk_bwd && e == cudaSuccess && st == EVO_OK) {
     CallOpts co;

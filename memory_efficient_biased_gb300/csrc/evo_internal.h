@@ -83,6 +83,7 @@ struct BwdArgs {
   int kv_bufs;              // main kernel: K/V buffers (2: the next key tile loads ahead; 1)
   int part_stages;          // pair-bias partial kernel: depth of its ring
   int db2p_tma;             // pair-bias partial kernel: tile stores through tdb2p (L % 4 == 0)
+  int db2_no_sum;           // pair-bias gradient: write the partial planes only (the caller sums them)
   // Masked key-tile skipping in the per-key-tile kernel (tile_skip; QT <= 64): it skips
   // the key tiles of each slice whose every key mask is <= skip_at (rows with no kept key
   // skip nothing); dK and dV of the skipped key tiles are written as zeros beforehand.
@@ -145,6 +146,8 @@ BwdPlan bwd_plan(int DP, int QT, bool has_b2);
 int kmajor_q_stages(int DP, int QT, bool has_b2);
 int kmajor_stream_q_stages(int DP, bool has_b2);
 cudaError_t launch_bwd_kmajor(const BwdArgs& a, int DP, bool bf16, bool has_b2, bool dq_stream, cudaStream_t st);
+// The pair-bias gradient's fixed-order sum over a.groups partial planes at a.db2_part.
+cudaError_t launch_bwd_db2_sum(const BwdArgs& a, bool bf16, cudaStream_t st);
 // Key-mask gradient partials (a.db1p) by the key-major score recompute alone, for the
 // schedules whose main kernel does not produce them; then the fixed-order sum into a.dbias1.
 cudaError_t launch_bwd_db1_partials(const BwdArgs& a, int DP, bool bf16, bool has_b2, cudaStream_t st);

@@ -18,7 +18,9 @@ CASES = [
     (1, 4, 200, 3, 8, "fp16", ("random", 0.10), 0.5),   # key-major, D = 8
     (2, 3, 256, 2, 32, "bf16", ("random", 0.05), 1.0),  # key-major, L = 256
     (1, 3, 131, 2, 24, "bf16", ("tail", 0.05), None),   # key-major, no pair bias, odd L
-    (1, 2, 300, 2, 32, "fp16", ("random", 0.05), 1.0),  # query-major slice (3 key tiles)
+    (1, 2, 300, 2, 32, "fp16", ("random", 0.05), 1.0),  # key-major, dQ streamed (3 key tiles)
+    (1, 2, 600, 1, 16, "bf16", ("random", 0.05), None), # key-major, dQ streamed, D = 16 (5 key tiles)
+    (1, 3, 100, 2, 64, "bf16", ("random", 0.05), 1.0),  # query-major slice (D = 64, one key tile)
     (1, 2, 257, 1, 64, "bf16", ("random", 0.05), 1.0),  # per key tile
     (1, 2, 384, 1, 56, "fp16", ("tail", 0.03), None),   # per key tile, no pair bias
 ]

@@ -114,6 +114,30 @@ def test_step_host_matches_device_path():
     assert torch.equal(h["dq"], dq.cpu())
 
 
+def test_step_host_row_chunks_match_device_path():
+    """Enough rows for the host-buffer step to run in two row chunks with a pair bias: each
+    chunk's backward writes the partial planes of its own n-groups and one sum follows, in
+    the order an unchunked call uses, so every output (dbias2 included) is the same bytes."""
+    inp = make_inputs(1, 160, 128, 4, 16, dtype="bf16", mask=("random", 0.05), seed=23)
+    d = to_dev(inp)
+    out, lse = run_fwd(d)
+    dq, dk, dv, db2 = run_bwd(d, out, lse)
+    pin = {k: v.pin_memory() for k, v in inp.items()}
+    h = {k: torch.empty_like(pin["q"]).pin_memory() for k in ("out", "dq", "dk", "dv")}
+    hdb2 = torch.empty_like(pin["bias2"]).pin_memory()
+    hlse = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+    arena = torch.empty(E.evo_attn_step_host_arena_bytes(tuple(inp["q"].shape), torch.bfloat16, True, True),
+                        dtype=torch.uint8, device="cuda")
+    for _ in range(2):  # the second call reuses the arena
+        E.evo_attn_step_host(pin["q"], pin["k"], pin["v"], pin["bias1"], pin["bias2"], pin["do"], h["out"], hlse,
+                             h["dq"], h["dk"], h["dv"], hdb2, arena)
+        torch.cuda.synchronize()
+        assert E.evo_attn_device_status() == 0
+        assert torch.equal(h["out"], out.cpu()) and torch.equal(hlse, lse.cpu())
+        assert torch.equal(h["dq"], dq.cpu()) and torch.equal(h["dk"], dk.cpu()) and torch.equal(h["dv"], dv.cpu())
+        assert torch.equal(hdb2, db2.cpu())
+
+
 def test_cuda_graph_capture_replays_identically():
     inp = _inputs()
     d = to_dev(inp)

@@ -23,6 +23,8 @@ SMALL = [
     (1, 2, 128, 2, 48, "fp16", ("tail", 0.5), None, False),
     (1, 2, 384, 1, 56, "bf16", ("tail", 0.03), 1.0, True),
     (1, 5, 33, 1, 32, "fp16", ("random", 0.3), 1.0, True),
+    (1, 3, 700, 2, 16, "fp16", ("random", 0.05), 1.0, True),   # key-major, dQ streamed, D = 16 (6 key tiles)
+    (2, 3, 450, 1, 32, "bf16", ("tail", 0.10), None, True),    # key-major, dQ streamed, ragged L, two batches
 ]
 
 

@@ -60,11 +60,12 @@ def outside_untouched(buf, view):
 CASES = [
     (1, 4, 200, 3, 8, "fp16", ("random", 0.10), 0.5, "transposed"),   # key-major
     (2, 3, 256, 2, 32, "bf16", ("random", 0.05), 1.0, "transposed"),   # key-major, batch by batch
-    (1, 2, 300, 2, 32, "fp16", ("random", 0.05), 1.0, "transposed"),   # query-major slice
-    (1, 2, 257, 1, 64, "bf16", ("random", 0.05), 1.0, "transposed"),   # per key tile (dQ cast)
+    (1, 2, 300, 2, 32, "fp16", ("random", 0.05), 1.0, "transposed"),   # key-major, dQ streamed
+    (1, 2, 257, 1, 64, "bf16", ("random", 0.05), 1.0, "transposed"),   # per key tile
     (2, 2, 200, 1, 64, "fp16", ("tail", 0.05), 1.0, "transposed"),     # per key tile, batch by batch
     (1, 3, 131, 2, 24, "bf16", ("tail", 0.05), None, "padded"),        # odd D and L, no pair bias
-    (2, 2, 384, 2, 16, "fp16", ("random", 0.05), 1.0, "padded"),       # slice/key-major, padded rows
+    (2, 2, 384, 2, 16, "fp16", ("random", 0.05), 1.0, "padded"),       # key-major (D = 16), padded rows
+    (2, 2, 640, 1, 16, "bf16", ("random", 0.05), None, "transposed"),  # key-major, dQ streamed, batch by batch
 ]
 
 
