@@ -765,9 +765,70 @@ def run_micro(args):
                     rec["traffic_tmem_bytes_per_clock"] = 8 * tmem_bytes[mode] * creps[mode] / max(tcyc[1:])
                     rec["traffic_cycles_per_round"] = max(tcyc[1:]) / creps[mode]
                 print(json.dumps(rec), flush=True)
+    micro_host_link(lib, sms)
     rows = sampler.stop()
     print(json.dumps({"micro": "clocks", **summarize_clocks(rows, 0, 1e18, sampler.source)}), flush=True)
     return 0
+
+
+def micro_host_link(lib, sms, nbytes=512 << 20):
+    """Host <-> device bandwidth between pinned host memory and HBM: the copy engines one
+    direction at a time and both at once, and copies by the SMs through mapped pinned
+    memory.  These rates bound the host-buffer step (its e2e number)."""
+    import ctypes
+    import torch
+    h_in = torch.ones(nbytes, dtype=torch.uint8).pin_memory()
+    h_out = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    d_a = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    d_b = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+    s_up, s_down = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def timed(fn, reps=5):
+        fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e-3 / reps
+
+    def duplex():
+        cur = torch.cuda.current_stream()
+        for st in (s_up, s_down):
+            st.wait_stream(cur)
+        with torch.cuda.stream(s_up):
+            d_a.copy_(h_in, non_blocking=True)
+        with torch.cuda.stream(s_down):
+            h_out.copy_(d_b, non_blocking=True)
+        for st in (s_up, s_down):
+            cur.wait_stream(st)
+
+    rec = {"micro": "host_link", "bytes": nbytes,
+           "copy_engine_h2d_gbs": nbytes / timed(lambda: d_a.copy_(h_in, non_blocking=True)) / 1e9,
+           "copy_engine_d2h_gbs": nbytes / timed(lambda: h_out.copy_(d_b, non_blocking=True)) / 1e9,
+           "copy_engine_both_directions_gbs": 2 * nbytes / timed(duplex) / 1e9}
+    lib.evo_micro_host_ptr.argtypes = [ctypes.c_void_p, ctypes.POINTER(ctypes.c_void_p)]
+    lib.evo_micro_copy.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_void_p]
+    p_in, p_out = ctypes.c_void_p(), ctypes.c_void_p()
+    r_in = lib.evo_micro_host_ptr(ctypes.c_void_p(h_in.data_ptr()), ctypes.byref(p_in))
+    r_out = lib.evo_micro_host_ptr(ctypes.c_void_p(h_out.data_ptr()), ctypes.byref(p_out))
+    if r_in == 0 and r_out == 0 and p_in.value and p_out.value:  # SM copies only through mapped memory
+        st = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+        def sm_copy(src, dst):
+            rc = lib.evo_micro_copy(src, dst, nbytes, 2 * sms, st)
+            if rc != 0:
+                raise RuntimeError(f"micro_copy: cuda error {rc}")
+
+        rec["sm_copy_h2d_gbs"] = nbytes / timed(lambda: sm_copy(p_in, ctypes.c_void_p(d_a.data_ptr()))) / 1e9
+        rec["sm_copy_d2h_gbs"] = nbytes / timed(lambda: sm_copy(ctypes.c_void_p(d_b.data_ptr()), p_out)) / 1e9
+        if not torch.equal(d_a[:4096].cpu(), h_in[:4096]):
+            raise RuntimeError("micro_copy: wrong bytes")
+    else:
+        rec["sm_copy"] = "pinned memory not mapped into the device address space"
+    print(json.dumps(rec), flush=True)
 
 
 def main():

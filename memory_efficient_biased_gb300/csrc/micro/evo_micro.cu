@@ -621,3 +621,31 @@ EVO_MICRO_API int evo_micro_mma(int n, int ts, int accs, int blocks, int reps, v
     default: return cudaErrorInvalidValue;
   }
 }
+
+// ---------------------------------------------------------------- host link
+// Copies driven by the SMs: a grid-stride loop of 16-byte loads and stores, for host ↔
+// device copies through mapped pinned host memory (against the copy engines' rate).
+__global__ void micro_copy16(const uint4* __restrict__ src, uint4* __restrict__ dst, size_t n) {
+  const size_t step = static_cast<size_t>(gridDim.x) * blockDim.x;
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n; i += step) dst[i] = src[i];
+}
+
+// dst[0 .. bytes) = src[0 .. bytes); both 16-byte aligned device-accessible pointers (device
+// memory, or the device pointer of mapped pinned host memory), bytes a multiple of 16.
+EVO_MICRO_API int evo_micro_copy(const void* src, void* dst, size_t bytes, int blocks, void* stream) {
+  if (!src || !dst || blocks <= 0 || bytes % 16 != 0 || (reinterpret_cast<uintptr_t>(src) & 15) != 0 ||
+      (reinterpret_cast<uintptr_t>(dst) & 15) != 0)
+    return cudaErrorInvalidValue;
+  micro_copy16<<<blocks, 512, 0, static_cast<cudaStream_t>(stream)>>>(static_cast<const uint4*>(src),
+                                                                     static_cast<uint4*>(dst), bytes / 16);
+  return cudaGetLastError();
+}
+
+// The device pointer of pinned host memory (cudaHostGetDevicePointer); *dev = nullptr and an
+// error when the memory is not mapped.
+EVO_MICRO_API int evo_micro_host_ptr(void* host, void** dev) {
+  *dev = nullptr;
+  const cudaError_t e = cudaHostGetDevicePointer(dev, host, 0);
+  if (e != cudaSuccess) *dev = nullptr;
+  return static_cast<int>(e);
+}
