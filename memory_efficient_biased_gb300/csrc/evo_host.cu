@@ -891,7 +891,7 @@ evo_status_t evo_attn_step_host(const void* q, const void* k, const void* v, con
 
   struct Res {
     cudaStream_t ci = nullptr, co = nullptr;
-    cudaEvent_t ev[3 * 64 + 3] = {};
+    cudaEvent_t ev[4 * 64 + 3] = {};
     int nev = 0;
     ~Res() {  // released once their pending work is done
       for (int i = 0; i < nev; ++i)
@@ -902,16 +902,17 @@ evo_status_t evo_attn_step_host(const void* q, const void* k, const void* v, con
   } r;
   cudaError_t e = cudaStreamCreateWithFlags(&r.ci, cudaStreamNonBlocking);
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&r.co, cudaStreamNonBlocking);
-  const int nev = static_cast<int>(3 * chunks + 3);
+  const int nev = static_cast<int>(4 * chunks + 3);
   for (int i = 0; e == cudaSuccess && i < nev; ++i) {
     e = cudaEventCreateWithFlags(&r.ev[i], cudaEventDisableTiming);
     r.nev = i + 1;
   }
   if (e != cudaSuccess) return cuda_fail("host step: streams and events", e);
   cudaEvent_t ev_start = r.ev[0], ev_mid = r.ev[1], ev_done = r.ev[2];
-  auto ev_in = [&](int64_t c) { return r.ev[3 + 3 * c]; };
-  auto ev_fwd = [&](int64_t c) { return r.ev[3 + 3 * c + 1]; };
-  auto ev_bwd = [&](int64_t c) { return r.ev[3 + 3 * c + 2]; };
+  auto ev_in = [&](int64_t c) { return r.ev[3 + 4 * c]; };       // all of the chunk's inputs are up
+  auto ev_fwd = [&](int64_t c) { return r.ev[3 + 4 * c + 1]; };
+  auto ev_bwd = [&](int64_t c) { return r.ev[3 + 4 * c + 2]; };
+  auto ev_fwd_in = [&](int64_t c) { return r.ev[3 + 4 * c + 3]; };  // the forward's inputs are up
   auto ok = [&](cudaError_t x) {
     if (x != cudaSuccess && e == cudaSuccess) e = x;
     return x == cudaSuccess;
@@ -947,6 +948,7 @@ evo_status_t evo_attn_step_host(const void* q, const void* k, const void* v, con
     h2d(L.k + row0 * row_qkv, hp(k, row0 * row_qkv), rows * row_qkv);
     h2d(L.v + row0 * row_qkv, hp(v, row0 * row_qkv), rows * row_qkv);
     if (bias1) h2d(L.b1 + row0 * row_b1, hp(bias1, row0 * row_b1), rows * row_b1);
+    ok(cudaEventRecord(ev_fwd_in(c), r.ci));  // the forward need not wait for dO
     h2d(L.dout + row0 * row_qkv, hp(dout, row0 * row_qkv), rows * row_qkv);
     ok(cudaEventRecord(ev_in(c), r.ci));
   }
@@ -963,10 +965,11 @@ evo_status_t evo_attn_step_host(const void* q, const void* k, const void* v, con
     const void* cb1 = bias1 ? A + L.b1 + row0 * row_b1 : nullptr;
     const void* cb2 = bias2 ? A + L.b2 + size_t(b) * shape.H * shape.L * shape.L * 2 : nullptr;
     float* clse = reinterpret_cast<float*>(A + L.lse + row0 * row_lse);
-    ok(cudaStreamWaitEvent(s, ev_in(c), 0));
+    ok(cudaStreamWaitEvent(s, ev_fwd_in(c), 0));
     st = evo_attn_fwd(cq, ck, cv, cb1, cb2, cout, clse, sub, dtype, stream);
     if (st != EVO_OK) break;
     ok(cudaEventRecord(ev_fwd(c), s));
+    if (chunk_bwd) ok(cudaStreamWaitEvent(s, ev_in(c), 0));  // dO of this chunk
     if (chunk_bwd && !db2_chunks) {
       st = evo_attn_bwd(cq, ck, cv, cb1, nullptr, cout, clse, cdo, A + L.dq + row0 * row_qkv,
                         A + L.dk + row0 * row_qkv, A + L.dv + row0 * row_qkv, nullptr, A + L.ws, arena_bytes - L.ws,
@@ -1009,6 +1012,7 @@ evo_status_t evo_attn_step_host(const void* q, const void* k, const void* v, con
     d2h(dbias2, L.db2, bias2_bytes(shape));
   }
   if (!chunk_bwd && e == cudaSuccess && st == EVO_OK) {
+    ok(cudaStreamWaitEvent(s, ev_in(chunks - 1), 0));  // every chunk's dO (the copies run in order)
     CallOpts co;
     co.prof.count = 6;
     co.prof.ev[5] = ev_mid;  // recorded once the main backward kernel is done
