@@ -12,11 +12,14 @@
 // an item is a pair of 128-row query tiles (2p, 2p + 1) of one (b, n, h) slice,
 // which share its K and V tiles.
 //   warp 8      TMA producer: both Q tiles of an item (two buffers); K, V and the
-//               key-mask chunk per key tile into a ring of stages; pair-bias tiles
+//               key mask (extension rows of the score MMA, or fp32 with a pair bias)
+//               per key tile into a ring of stages; pair-bias tiles
 //               either resident per (b, h, pair) group across n, or streamed with
 //               each key tile.
 //   warps 9, 10 MMA issuers (one thread each, one per query tile g): per key
-//               tile, S_g = Q_g K_jᵀ into TMEM, and the previous key tile's
+//               tile, S_g = Q_g K_jᵀ into TMEM (without a pair bias + mask_j·D^1/2,
+//               as one more K = 16 step: a ones column block against the mask split
+//               into three bf16 parts, which hold all 24 bits of the fp32 value), and the previous key tile's
 //               O_g += P_g [V_{j-1} | 1] (P read from TMEM; the ones columns make
 //               the MMA form the row sums of P too).  Neither waits on the other.
 //   warps 0..3  softmax of query tile 0, warps 4..7 of query tile 1: one thread
@@ -32,12 +35,12 @@
 // only when a key tile's max exceeds it by more than 2^8 (P then stays below
 // 256, exact enough in fp16/bf16); the O accumulator (with its row-sum columns)
 // is then rescaled in TMEM once the previous P·V is done.  The tile max is taken
-// before P is formed, so each tile is exponentiated once.  Scale and biases are
-// applied in the log2 domain with packed f32x2 arithmetic.  The epilogue divides
+// before P is formed, so each tile is exponentiated once.  Without a pair bias
+// P = 2^(S'·D^-1/2·log2 e − m) is one packed f32x2 multiply-add and an exponential
+// per score; with one, scale and biases are applied in the log2 domain first.  The epilogue divides
 // O by the row sum and writes O through shared memory with one TMA tile store per
 // warp, and lse.
-// Key columns past L carry a -inf key-mask entry, so no other masking is
-// needed; query rows past L (a partial or absent second query tile) are
+// Key columns past L carry a -inf mask entry, so no other masking is needed; query rows past L (a partial or absent second query tile) are
 // computed and not stored.
 #include "evo_internal.h"
 #include "evo_ptx.cuh"
@@ -101,8 +104,8 @@ __device__ __forceinline__ uint32_t tile_meta_all(int x, int KT) {
 template <int DP>
 struct FwdLayout {
   static constexpr uint32_t kTB = kTile * DP * 2;
-  Ring q, k, v, b1, b2s;
-  uint32_t b2r, stg, ones, bars, total;
+  Ring q, k, v, kx, b1, b2s;
+  uint32_t b2r, stg, ones, qx, bars, total;
   // q[2 * buffer + g]; b2s[stage] + g * 32768; b2r + (g * KT + jt) * 32768
   __host__ __device__ FwdLayout(int b2kind, int stages, int KT) {
     uint32_t off = 0;
@@ -120,8 +123,22 @@ struct FwdLayout {
     off = (off + 1023u) & ~1023u;
     ones = off;  // 128 rows of ones, read as V's extra columns by the P·V MMA
     if (kOnes<DP>) off += kTile * DP * 2u;
-    b1 = Ring{off, 512u};
-    off += stages * 512u;
+    qx = 0;
+    kx = Ring{0, 0};
+    b1 = Ring{0, 0};
+    if (b2kind == kB2None) {
+      // without a pair bias the key mask enters S through one more K = 16 step of the score
+      // MMA: the Q side is a constant [128][16] bf16 tile (columns 0..2 one), the K side per
+      // stage holds each key's mask·D^1/2 split into three bf16 parts (columns 0..2); rows of
+      // 32 bytes, 32-byte swizzle
+      qx = off;
+      off += kTile * 32u;
+      kx = Ring{off, kTile * 32u};
+      off += stages * kTile * 32u;
+    } else {  // with one, the softmax warps add the mask: fp32 × log2 e per key and stage
+      b1 = Ring{off, 512u};
+      off += stages * 512u;
+    }
     bars = off;
     off += (sizeof(FwdBars) + 127) & ~127u;
     total = off;
@@ -220,6 +237,17 @@ __device__ __forceinline__ void fwd_producer(const FwdArgs& a, uint8_t* base, co
   };
   RowScan nscan;
   const bool scan_ahead = SKIP && a.bias1 && row_scan_fits(a.bias1, a.L);
+  const float inv_scale = kLog2e / a.scale_log2;  // the mask in units of Q·Kᵀ
+  // the constant parts of the mask extension: the Q side's ones, and columns 8..15 (zero) of
+  // every stage's K side; written before this warp's first arrival on a stage
+#pragma unroll 1
+  for (int row = lane; B2 == kB2None && row < kTile; row += 32) {
+    *reinterpret_cast<uint4*>(base + lay.qx + swz_offset(row, 0, 32)) =
+        make_uint4(kBf16One | kBf16One << 16, kBf16One, 0u, 0u);
+    *reinterpret_cast<uint4*>(base + lay.qx + swz_offset(row, 1, 32)) = make_uint4(0u, 0u, 0u, 0u);
+    for (int st = 0; st < S; ++st)
+      *reinterpret_cast<uint4*>(base + lay.kx[st] + swz_offset(row, 1, 32)) = make_uint4(0u, 0u, 0u, 0u);
+  }
   uint64_t act = tiles_of(c);
   b1_prefetch(c, next_tile(act, -1, KT));
   bool ok = true;
@@ -289,7 +317,7 @@ __device__ __forceinline__ void fwd_producer(const FwdArgs& a, uint8_t* base, co
         for (int gq = 0; gq < 2; ++gq)
           fill_b2_loads(base + lay.b2s[s] + gq * 32768u, a.bias2 + static_cast<size_t>(bh) * a.L * a.L, a.L,
                         (2 * c.p + gq) * kTile, jt * kTile, lane);
-      {  // key-mask chunk, fp32 in the log2 domain; -inf past L
+      if constexpr (B2 != kB2None) {  // key-mask chunk, fp32 in the log2 domain; -inf past L
         float4 m4;
         float* mv = reinterpret_cast<float*>(&m4);
 #pragma unroll
@@ -298,6 +326,17 @@ __device__ __forceinline__ void fwd_producer(const FwdArgs& a, uint8_t* base, co
           mv[e] = j < a.L ? (a.bias1 ? to_f32<BF16>(b1raw[e]) * kLog2e : 0.0f) : -INFINITY;
         }
         *reinterpret_cast<float4*>(base + lay.b1[s] + lane * 16) = m4;
+      } else {  // this lane's four keys of the mask extension: mask·D^1/2 in three bf16 parts; -inf past L
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int j = jt * kTile + lane * 4 + e;
+          const float mk = j < a.L ? (a.bias1 ? to_f32<BF16>(b1raw[e]) * inv_scale : 0.0f) : -INFINITY;
+          uint32_t h, m, l;
+          split3_bf16(mk, h, m, l);
+          *reinterpret_cast<uint4*>(base + lay.kx[s] + swz_offset(lane * 4 + e, 0, 32)) =
+              make_uint4(h | m << 16, l, 0u, 0u);
+        }
+        fence_proxy_async_smem();  // read by the tensor cores
       }
       mbar_arrive(full);
       if (jn < KT) {
@@ -355,12 +394,14 @@ __device__ __forceinline__ bool fwd_issue_pv(uint32_t g, uint32_t v, uint32_t sv
 // One issuing thread per query tile g: per key tile, S_g as soon as the group has loaded
 // its previous S (s_free), then the group's P·V of the previous key tile as its P
 // arrives.  The two threads share the tensor core but never wait on each other.
-template <int DP, bool BF16, bool SKIP>
+template <int DP, bool BF16, int B2, bool SKIP>
 __device__ __forceinline__ void fwd_mma(const FwdArgs& a, uint8_t* base, const FwdLayout<DP>& lay, FwdBars* bars,
                                         uint32_t tmem, uint32_t gq, const WaitGuard& g, long long i0, long long i1) {
   constexpr uint32_t RB = DP * 2;
   constexpr uint32_t SWZ = swizzle_for_row(RB);
   constexpr uint32_t id_s = idesc_f16(128, 128, BF16, false, false);
+  constexpr uint32_t id_x = idesc_f16(128, 128, true, false, false);  // the mask step: bf16 whatever the inputs
+  const uint64_t qxd = B2 == kB2None ? smem_desc(smem_u32(base + lay.qx), 16, 8 * 32, kSwizzle32B) : 0ull;
   const int S = a.stages, KT = a.QT;
   uint32_t u = 0, q_it = 0, s = 0, ph = 0, item_ord = 0;
   uint32_t prev_stage = 0, prev_meta = 0, prev_item = 0;
@@ -381,6 +422,8 @@ __device__ __forceinline__ void fwd_mma(const FwdArgs& a, uint8_t* base, const F
       const uint64_t qd = smem_desc(smem_u32(base + lay.q[2 * qb + gq]), 16, 8 * RB, SWZ);
 #pragma unroll
       for (int k = 0; k < DP / 16; ++k) umma_ss(tmem + col_s(gq), qd + k * 2, kd + k * 2, id_s, k > 0);
+      if (B2 == kB2None)  // the key mask
+        umma_ss(tmem + col_s(gq), qxd, smem_desc(smem_u32(base + lay.kx[s]), 16, 8 * 32, kSwizzle32B), id_x, 1u);
       umma_commit(smem_u32(&bars->s_full[gq]));
       if (last) umma_commit(smem_u32(&bars->q_empty[qb]));
       // the group's P·V of the previous key tile
@@ -410,10 +453,12 @@ __device__ __forceinline__ void fwd_mma(const FwdArgs& a, uint8_t* base, const F
 }
 
 // ------------------------------------------------------------ softmax (warps 0..7)
-// One 32-key chunk of this thread's row, in place: sr holds S (fp32 bits) on entry and
-// y = S·s·log2e + bias1·log2e (+ bias2·log2e) on return; the chunk's max goes into mt.
-// (b2h: the 64-key half of the pair-bias tile holding the chunk; c0: the chunk's first
-// 16-byte column within that half's 128-byte rows.)
+// One 32-key chunk of this thread's row, in place; the chunk's max goes into mt.
+//   Without a pair bias (HAS_B2 false) sr holds S' = Q·Kᵀ + mask·D^1/2 (fp32 bits; the score
+//   MMA adds the mask) and stays as it is: y = S', in units of Q·Kᵀ.
+//   With one, sr holds S and becomes y = S·s + mask·log2 e + bias2·log2 e, in log2 units
+//   (b1c: the chunk's mask × log2 e; b2h: the 64-key half of the pair-bias tile holding the
+//   chunk; c0: the chunk's first 16-byte column within that half's 128-byte rows).
 template <bool BF16, bool HAS_B2>
 __device__ __forceinline__ void chunk_scores(uint32_t (&sr)[32], const float* b1c, const uint8_t* b2h, int c0, int r,
                                              float2 sl2, float& mt) {
@@ -421,34 +466,44 @@ __device__ __forceinline__ void chunk_scores(uint32_t (&sr)[32], const float* b1
   float mx[4] = {mt, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
   for (int q = 0; q < 4; ++q) {  // 8 keys per q
-    const float4 m0 = *reinterpret_cast<const float4*>(b1c + q * 8);
-    const float4 m1 = *reinterpret_cast<const float4*>(b1c + q * 8 + 4);
-    const float2 mk[4] = {make_float2(m0.x, m0.y), make_float2(m0.z, m0.w), make_float2(m1.x, m1.y),
-                          make_float2(m1.z, m1.w)};
-    uint4 pb = make_uint4(0u, 0u, 0u, 0u);
-    if (HAS_B2) pb = *reinterpret_cast<const uint4*>(b2h + swz_offset(r, c0 + q, 128));
-    const uint32_t pw[4] = {pb.x, pb.y, pb.z, pb.w};
+    if constexpr (HAS_B2) {
+      const float4 m0 = *reinterpret_cast<const float4*>(b1c + q * 8);
+      const float4 m1 = *reinterpret_cast<const float4*>(b1c + q * 8 + 4);
+      const float2 mk[4] = {make_float2(m0.x, m0.y), make_float2(m0.z, m0.w), make_float2(m1.x, m1.y),
+                            make_float2(m1.z, m1.w)};
+      const uint4 pb = *reinterpret_cast<const uint4*>(b2h + swz_offset(r, c0 + q, 128));
+      const uint32_t pw[4] = {pb.x, pb.y, pb.z, pb.w};
 #pragma unroll
-    for (int e2 = 0; e2 < 4; ++e2) {
-      const int x = q * 8 + e2 * 2;
-      float2 t = fma2(make_float2(__uint_as_float(sr[x]), __uint_as_float(sr[x + 1])), sl2, mk[e2]);
-      if (HAS_B2) t = fma2(unpack2<BF16>(pw[e2]), l2e2, t);
-      sr[x] = __float_as_uint(t.x);
-      sr[x + 1] = __float_as_uint(t.y);
-      mx[e2] = max3(mx[e2], t.x, t.y);
+      for (int e2 = 0; e2 < 4; ++e2) {
+        const int x = q * 8 + e2 * 2;
+        float2 t = fma2(make_float2(__uint_as_float(sr[x]), __uint_as_float(sr[x + 1])), sl2, mk[e2]);
+        t = fma2(unpack2<BF16>(pw[e2]), l2e2, t);
+        sr[x] = __float_as_uint(t.x);
+        sr[x + 1] = __float_as_uint(t.y);
+        mx[e2] = max3(mx[e2], t.x, t.y);
+      }
+    } else {
+#pragma unroll
+      for (int e2 = 0; e2 < 4; ++e2) {
+        const int x = q * 8 + e2 * 2;
+        mx[e2] = max3(mx[e2], __uint_as_float(sr[x]), __uint_as_float(sr[x + 1]));
+      }
     }
   }
   mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
 }
 
-// P = 2^(y - m) for one chunk (y as fp32 bits), packed into pp[0..15]; with ROWSUM,
-// also the row sum into rs (otherwise the P·V MMA forms it).
-template <bool BF16, bool ROWSUM>
-__device__ __forceinline__ void chunk_probs(const uint32_t (&y)[32], float m, uint32_t (&pp)[16], float2& rs) {
+// P = 2^(y·s - m) for one chunk (y in units of Q·Kᵀ, SCALED) or 2^(y - m) (y in log2
+// units), y as fp32 bits, packed into pp[0..15]; with ROWSUM, also the row sum into rs
+// (otherwise the P·V MMA forms it).
+template <bool BF16, bool ROWSUM, bool SCALED>
+__device__ __forceinline__ void chunk_probs(const uint32_t (&y)[32], float2 sl2, float m, uint32_t (&pp)[16],
+                                            float2& rs) {
   const float2 nm2 = make_float2(-m, -m);
 #pragma unroll
   for (int x = 0; x < 32; x += 2) {
-    const float2 t = add2(make_float2(__uint_as_float(y[x]), __uint_as_float(y[x + 1])), nm2);
+    const float2 yy = make_float2(__uint_as_float(y[x]), __uint_as_float(y[x + 1]));
+    const float2 t = SCALED ? fma2(yy, sl2, nm2) : add2(yy, nm2);
     const float p0 = ex2(t.x), p1 = ex2(t.y);
     if (ROWSUM) rs = add2(rs, make_float2(p0, p1));
     pp[x >> 1] = pack2<BF16>(p0, p1);
@@ -574,7 +629,7 @@ __device__ __forceinline__ void fwd_softmax(const FwdArgs& a, uint8_t* base, con
       const bool last = (meta & kTileLast) != 0;
       if (!mbar_wait_warp_inl(smem_u32(&bars->s_full[grp]), u & 1, g)) { ok = false; break; }
       tc_fence_after();
-      const float* b1 = reinterpret_cast<const float*>(base + lay.b1[s]);
+      const float* b1 = reinterpret_cast<const float*>(base + lay.b1[s]);  // (with a pair bias)
       const uint8_t* b2t =
           base + (B2 == kB2Resident ? lay.b2r + (grp * KT + jt) * 32768u : lay.b2s[s] + grp * 32768u);
       // S in two 64-column loads: the second is in flight while the first half is scored
@@ -595,6 +650,7 @@ __device__ __forceinline__ void fwd_softmax(const FwdArgs& a, uint8_t* base, con
       if (lane == 0) mbar_arrive(smem_u32(&bars->s_free[grp]));  // S may be overwritten
       chunk_scores<BF16, kHasB2>(y2, b1 + 64, b2t + 16384, 0, r, sl2, mt);
       chunk_scores<BF16, kHasB2>(y3, b1 + 96, b2t + 16384, 4, r, sl2, mt);
+      if (!kHasB2) mt *= a.scale_log2;  // to the log2 units of the reference max (a positive factor keeps the max)
       __syncwarp();
       if (lane == 0) {  // the stage's bias data are no longer read by this warp
         mbar_arrive(smem_u32(&bars->kv_empty[s]));
@@ -620,11 +676,11 @@ __device__ __forceinline__ void fwd_softmax(const FwdArgs& a, uint8_t* base, con
         uint32_t pp[32];
         uint32_t(&p0)[16] = *reinterpret_cast<uint32_t(*)[16]>(&pp[0]);
         uint32_t(&p1)[16] = *reinterpret_cast<uint32_t(*)[16]>(&pp[16]);
-        chunk_probs<BF16, kRowSum>(y0, m, p0, rs);
-        chunk_probs<BF16, kRowSum>(y1, m, p1, rs);
+        chunk_probs<BF16, kRowSum, !kHasB2>(y0, sl2, m, p0, rs);
+        chunk_probs<BF16, kRowSum, !kHasB2>(y1, sl2, m, p1, rs);
         tmem_st32(pcol, pp);
-        chunk_probs<BF16, kRowSum>(y2, m, p0, rs);
-        chunk_probs<BF16, kRowSum>(y3, m, p1, rs);
+        chunk_probs<BF16, kRowSum, !kHasB2>(y2, sl2, m, p0, rs);
+        chunk_probs<BF16, kRowSum, !kHasB2>(y3, sl2, m, p1, rs);
         tmem_st32(pcol + 32, pp);
       }
       __syncwarp();
@@ -718,7 +774,7 @@ __global__ void __launch_bounds__(kThreads, 1) evo_fwd_kernel(const __grid_const
     if (warp == kProducerWarp) {
       fwd_producer<DP, BF16, B2, SKIP>(a, base, lay, bars, g, lane, i0, i1);
     } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
-      if (lane == 0) fwd_mma<DP, BF16, SKIP>(a, base, lay, bars, tmem, static_cast<uint32_t>(warp - kMmaWarp), g, i0, i1);
+      if (lane == 0) fwd_mma<DP, BF16, B2, SKIP>(a, base, lay, bars, tmem, static_cast<uint32_t>(warp - kMmaWarp), g, i0, i1);
       __syncwarp();
     }
   } else {

@@ -389,6 +389,23 @@ __device__ __forceinline__ uint32_t swz_offset(uint32_t row, uint32_t chunk, uin
 }
 
 // ---------------------------------------------------------------- math
+// x ≈ h + m + l, each rounded to bf16 in turn (the remainders are exact in fp32, so the three
+// parts carry all 24 bits of x); an infinity, or a value past the bf16 range, stays in h with
+// m = l = 0.  Returned as bf16 bit patterns.
+__device__ __forceinline__ void split3_bf16(float x, uint32_t& h, uint32_t& m, uint32_t& l) {
+  uint16_t hb, mb, lb;
+  asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(hb) : "f"(x));
+  const float hf = __uint_as_float(static_cast<uint32_t>(hb) << 16);
+  const float r1 = fabsf(hf) < INFINITY ? x - hf : 0.0f;
+  asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(mb) : "f"(r1));
+  const float r2 = r1 - __uint_as_float(static_cast<uint32_t>(mb) << 16);
+  asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(lb) : "f"(r2));
+  h = hb;
+  m = mb;
+  l = lb;
+}
+constexpr uint32_t kBf16One = 0x3F80u;
+
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
