@@ -835,7 +835,10 @@ cudaError_t launch_fwd_d(FwdArgs a, cudaStream_t st) {
       return launch_fwd_t<DP, BF16, kB2Resident>(a, st);
     }
   }
-  if (!fits(kB2Stream, 2)) return launch_fwd_single(a, BF16, st);  // D > 32 with a long pair bias
+  // D > 32 with a long pair bias: the single-tile kernel, built for 64 columns only (its tile
+  // loads would not fill its stages for another width); with D <= 32 the streamed layout
+  // always fits, so anything else is a layout error
+  if (!fits(kB2Stream, 2)) return DP == 64 ? launch_fwd_single(a, BF16, st) : cudaErrorInvalidValue;
   a.stages = 2;
   a.b2_resident = 0;
   a.qt_fast = 1;
