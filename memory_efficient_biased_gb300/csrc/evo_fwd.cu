@@ -12,14 +12,15 @@
 // an item is a pair of 128-row query tiles (2p, 2p + 1) of one (b, n, h) slice,
 // which share its K and V tiles.
 //   warp 8      TMA producer: both Q tiles of an item (two buffers); K, V and the
-//               key mask (extension rows of the score MMA, or fp32 with a pair bias)
+//               key mask (extension rows of the score MMA, or fp32 for the softmax)
 //               per key tile into a ring of stages; pair-bias tiles
 //               either resident per (b, h, pair) group across n, or streamed with
 //               each key tile.
 //   warps 9, 10 MMA issuers (one thread each, one per query tile g): per key
-//               tile, S_g = Q_g K_jᵀ into TMEM (without a pair bias + mask_j·D^1/2,
-//               as one more K = 16 step: a ones column block against the mask split
-//               into three bf16 parts, which hold all 24 bits of the fp32 value), and the previous key tile's
+//               tile, S_g = Q_g K_jᵀ into TMEM (+ mask_j·D^1/2 without a pair bias,
+//               and with one for bf16 at D <= 32: one more K = 16 step, a ones block
+//               against the mask split into three bf16 parts, which hold all 24 bits
+//               of the fp32 value), and the previous key tile's
 //               O_g += P_g [V_{j-1} | 1] (P read from TMEM; the ones columns make
 //               the MMA form the row sums of P too).  Neither waits on the other.
 //   warps 0..3  softmax of query tile 0, warps 4..7 of query tile 1: one thread
@@ -35,9 +36,10 @@
 // only when a key tile's max exceeds it by more than 2^8 (P then stays below
 // 256, exact enough in fp16/bf16); the O accumulator (with its row-sum columns)
 // is then rescaled in TMEM once the previous P·V is done.  The tile max is taken
-// before P is formed, so each tile is exponentiated once.  Without a pair bias
-// P = 2^(S'·D^-1/2·log2 e − m) is one packed f32x2 multiply-add and an exponential
-// per score; with one, scale and biases are applied in the log2 domain first.  The epilogue divides
+// before P is formed, so each tile is exponentiated once.  Where the score MMA adds
+// the mask, P = 2^((S' + bias2·D^1/2)·D^-1/2·log2 e − m) costs a packed f32x2
+// multiply-add (two with a pair bias) and an exponential per score; otherwise scale
+// and biases are applied in the log2 domain first.  The epilogue divides
 // O by the row sum and writes O through shared memory with one TMA tile store per
 // warp, and lse.
 // Key columns past L carry a -inf mask entry, so no other masking is needed; query rows past L (a partial or absent second query tile) are
@@ -78,6 +80,13 @@ constexpr int kOCols = kOnes<DP> ? DP + 16 : DP;
 
 // Pair-bias handling: none, resident per (b, h, pair) group, or streamed per key tile.
 enum B2Kind : int { kB2None = 0, kB2Resident = 1, kB2Stream = 2 };
+// The key mask is added by the score MMA (one more K = 16 step against a block of ones) without
+// a pair bias (a ones tile of its own), and with one for bf16 inputs at D <= 32, where the P·V
+// MMA's ones block serves (every element 1.0 in bf16; the K side is zero past its three
+// columns); otherwise the softmax warps add it.
+__host__ __device__ constexpr bool mask_in_s(int DP, bool bf16, int b2kind) {
+  return b2kind == kB2None || (bf16 && DP <= 32);
+}
 
 struct FwdBars {
   uint64_t q_full[2], q_empty[2];
@@ -107,7 +116,7 @@ struct FwdLayout {
   Ring q, k, v, kx, b1, b2s;
   uint32_t b2r, stg, ones, qx, bars, total;
   // q[2 * buffer + g]; b2s[stage] + g * 32768; b2r + (g * KT + jt) * 32768
-  __host__ __device__ FwdLayout(int b2kind, int stages, int KT) {
+  __host__ __device__ FwdLayout(int b2kind, int stages, int KT, bool bf16) {
     uint32_t off = 0;
     b2s = Ring{off, 65536u};
     if (b2kind == kB2Stream) off += stages * 65536u;
@@ -126,16 +135,20 @@ struct FwdLayout {
     qx = 0;
     kx = Ring{0, 0};
     b1 = Ring{0, 0};
-    if (b2kind == kB2None) {
-      // without a pair bias the key mask enters S through one more K = 16 step of the score
-      // MMA: the Q side is a constant [128][16] bf16 tile (columns 0..2 one), the K side per
-      // stage holds each key's mask·D^1/2 split into three bf16 parts (columns 0..2); rows of
-      // 32 bytes, 32-byte swizzle
-      qx = off;
-      off += kTile * 32u;
+    if (mask_in_s(DP, bf16, b2kind)) {
+      // the key mask enters S through one more K = 16 step of the score MMA: the Q side is a
+      // constant [128][16] bf16 tile (columns 0..2 one; with a pair bias the ones block), the K
+      // side per stage holds each key's mask·D^1/2 split into three bf16 parts (columns 0..2);
+      // rows of 32 bytes, 32-byte swizzle
+      if (b2kind == kB2None) {
+        qx = off;
+        off += kTile * 32u;
+      } else {
+        qx = ones;
+      }
       kx = Ring{off, kTile * 32u};
       off += stages * kTile * 32u;
-    } else {  // with one, the softmax warps add the mask: fp32 × log2 e per key and stage
+    } else {  // otherwise the softmax warps add the mask: fp32 × log2 e per key and stage
       b1 = Ring{off, 512u};
       off += stages * 512u;
     }
@@ -241,10 +254,12 @@ __device__ __forceinline__ void fwd_producer(const FwdArgs& a, uint8_t* base, co
   // the constant parts of the mask extension: the Q side's ones, and columns 8..15 (zero) of
   // every stage's K side; written before this warp's first arrival on a stage
 #pragma unroll 1
-  for (int row = lane; B2 == kB2None && row < kTile; row += 32) {
-    *reinterpret_cast<uint4*>(base + lay.qx + swz_offset(row, 0, 32)) =
-        make_uint4(kBf16One | kBf16One << 16, kBf16One, 0u, 0u);
-    *reinterpret_cast<uint4*>(base + lay.qx + swz_offset(row, 1, 32)) = make_uint4(0u, 0u, 0u, 0u);
+  for (int row = lane; mask_in_s(DP, BF16, B2) && row < kTile; row += 32) {
+    if (B2 == kB2None) {  // (with a pair bias the ones block serves)
+      *reinterpret_cast<uint4*>(base + lay.qx + swz_offset(row, 0, 32)) =
+          make_uint4(kBf16One | kBf16One << 16, kBf16One, 0u, 0u);
+      *reinterpret_cast<uint4*>(base + lay.qx + swz_offset(row, 1, 32)) = make_uint4(0u, 0u, 0u, 0u);
+    }
     for (int st = 0; st < S; ++st)
       *reinterpret_cast<uint4*>(base + lay.kx[st] + swz_offset(row, 1, 32)) = make_uint4(0u, 0u, 0u, 0u);
   }
@@ -317,7 +332,7 @@ __device__ __forceinline__ void fwd_producer(const FwdArgs& a, uint8_t* base, co
         for (int gq = 0; gq < 2; ++gq)
           fill_b2_loads(base + lay.b2s[s] + gq * 32768u, a.bias2 + static_cast<size_t>(bh) * a.L * a.L, a.L,
                         (2 * c.p + gq) * kTile, jt * kTile, lane);
-      if constexpr (B2 != kB2None) {  // key-mask chunk, fp32 in the log2 domain; -inf past L
+      if constexpr (!mask_in_s(DP, BF16, B2)) {  // key-mask chunk, fp32 in the log2 domain; -inf past L
         float4 m4;
         float* mv = reinterpret_cast<float*>(&m4);
 #pragma unroll
@@ -401,7 +416,8 @@ __device__ __forceinline__ void fwd_mma(const FwdArgs& a, uint8_t* base, const F
   constexpr uint32_t SWZ = swizzle_for_row(RB);
   constexpr uint32_t id_s = idesc_f16(128, 128, BF16, false, false);
   constexpr uint32_t id_x = idesc_f16(128, 128, true, false, false);  // the mask step: bf16 whatever the inputs
-  const uint64_t qxd = B2 == kB2None ? smem_desc(smem_u32(base + lay.qx), 16, 8 * 32, kSwizzle32B) : 0ull;
+  constexpr bool kMaskInS = mask_in_s(DP, BF16, B2);
+  const uint64_t qxd = kMaskInS ? smem_desc(smem_u32(base + lay.qx), 16, 8 * 32, kSwizzle32B) : 0ull;
   const int S = a.stages, KT = a.QT;
   uint32_t u = 0, q_it = 0, s = 0, ph = 0, item_ord = 0;
   uint32_t prev_stage = 0, prev_meta = 0, prev_item = 0;
@@ -422,7 +438,7 @@ __device__ __forceinline__ void fwd_mma(const FwdArgs& a, uint8_t* base, const F
       const uint64_t qd = smem_desc(smem_u32(base + lay.q[2 * qb + gq]), 16, 8 * RB, SWZ);
 #pragma unroll
       for (int k = 0; k < DP / 16; ++k) umma_ss(tmem + col_s(gq), qd + k * 2, kd + k * 2, id_s, k > 0);
-      if (B2 == kB2None)  // the key mask
+      if (kMaskInS)  // the key mask
         umma_ss(tmem + col_s(gq), qxd, smem_desc(smem_u32(base + lay.kx[s]), 16, 8 * 32, kSwizzle32B), id_x, 1u);
       umma_commit(smem_u32(&bars->s_full[gq]));
       if (last) umma_commit(smem_u32(&bars->q_empty[qb]));
@@ -454,40 +470,44 @@ __device__ __forceinline__ void fwd_mma(const FwdArgs& a, uint8_t* base, const F
 
 // ------------------------------------------------------------ softmax (warps 0..7)
 // One 32-key chunk of this thread's row, in place; the chunk's max goes into mt.
-//   Without a pair bias (HAS_B2 false) sr holds S' = Q·Kᵀ + mask·D^1/2 (fp32 bits; the score
-//   MMA adds the mask) and stays as it is: y = S', in units of Q·Kᵀ.
-//   With one, sr holds S and becomes y = S·s + mask·log2 e + bias2·log2 e, in log2 units
-//   (b1c: the chunk's mask × log2 e; b2h: the 64-key half of the pair-bias tile holding the
-//   chunk; c0: the chunk's first 16-byte column within that half's 128-byte rows).
-template <bool BF16, bool HAS_B2>
+//   FOLD (the score MMA added the mask): sr holds S' = Q·Kᵀ + mask·D^1/2 (fp32 bits) and
+//   becomes y = S' (+ bias2·D^1/2), in units of Q·Kᵀ (bs2: D^1/2 in both lanes).
+//   Otherwise sr holds S and becomes y = S·s + mask·log2 e (+ bias2·log2 e), in log2 units
+//   (b1c: the chunk's mask × log2 e).
+//   (b2h: the 64-key half of the pair-bias tile holding the chunk; c0: the chunk's first
+//   16-byte column within that half's 128-byte rows.)
+template <bool BF16, bool HAS_B2, bool FOLD>
 __device__ __forceinline__ void chunk_scores(uint32_t (&sr)[32], const float* b1c, const uint8_t* b2h, int c0, int r,
-                                             float2 sl2, float& mt) {
+                                             float2 sl2, float2 bs2, float& mt) {
   const float2 l2e2 = make_float2(kLog2e, kLog2e);
   float mx[4] = {mt, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
   for (int q = 0; q < 4; ++q) {  // 8 keys per q
-    if constexpr (HAS_B2) {
+    float2 mk[4];
+    if constexpr (!FOLD) {
       const float4 m0 = *reinterpret_cast<const float4*>(b1c + q * 8);
       const float4 m1 = *reinterpret_cast<const float4*>(b1c + q * 8 + 4);
-      const float2 mk[4] = {make_float2(m0.x, m0.y), make_float2(m0.z, m0.w), make_float2(m1.x, m1.y),
-                            make_float2(m1.z, m1.w)};
-      const uint4 pb = *reinterpret_cast<const uint4*>(b2h + swz_offset(r, c0 + q, 128));
-      const uint32_t pw[4] = {pb.x, pb.y, pb.z, pb.w};
+      mk[0] = make_float2(m0.x, m0.y), mk[1] = make_float2(m0.z, m0.w);
+      mk[2] = make_float2(m1.x, m1.y), mk[3] = make_float2(m1.z, m1.w);
+    }
+    uint4 pb = make_uint4(0u, 0u, 0u, 0u);
+    if (HAS_B2) pb = *reinterpret_cast<const uint4*>(b2h + swz_offset(r, c0 + q, 128));
+    const uint32_t pw[4] = {pb.x, pb.y, pb.z, pb.w};
 #pragma unroll
-      for (int e2 = 0; e2 < 4; ++e2) {
-        const int x = q * 8 + e2 * 2;
-        float2 t = fma2(make_float2(__uint_as_float(sr[x]), __uint_as_float(sr[x + 1])), sl2, mk[e2]);
-        t = fma2(unpack2<BF16>(pw[e2]), l2e2, t);
+    for (int e2 = 0; e2 < 4; ++e2) {
+      const int x = q * 8 + e2 * 2;
+      float2 t = make_float2(__uint_as_float(sr[x]), __uint_as_float(sr[x + 1]));
+      if constexpr (FOLD) {
+        if (HAS_B2) t = fma2(unpack2<BF16>(pw[e2]), bs2, t);
+      } else {
+        t = fma2(t, sl2, mk[e2]);
+        if (HAS_B2) t = fma2(unpack2<BF16>(pw[e2]), l2e2, t);
+      }
+      if (HAS_B2 || !FOLD) {
         sr[x] = __float_as_uint(t.x);
         sr[x + 1] = __float_as_uint(t.y);
-        mx[e2] = max3(mx[e2], t.x, t.y);
       }
-    } else {
-#pragma unroll
-      for (int e2 = 0; e2 < 4; ++e2) {
-        const int x = q * 8 + e2 * 2;
-        mx[e2] = max3(mx[e2], __uint_as_float(sr[x]), __uint_as_float(sr[x + 1]));
-      }
+      mx[e2] = max3(mx[e2], t.x, t.y);
     }
   }
   mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
@@ -586,6 +606,7 @@ __device__ __forceinline__ void fwd_softmax(const FwdArgs& a, uint8_t* base, con
                                             FwdBars* bars, uint32_t tmem, const WaitGuard& g, long long i0,
                                             long long i1) {
   constexpr bool kHasB2 = B2 != kB2None;
+  constexpr bool kFold = mask_in_s(DP, BF16, B2);  // the score MMA added the mask
   constexpr bool kRowSum = !kOnes<DP>;
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t grp = static_cast<uint32_t>(w >> 2);  // query tile of the item
@@ -594,6 +615,8 @@ __device__ __forceinline__ void fwd_softmax(const FwdArgs& a, uint8_t* base, con
   const uint32_t trow = tmem + (static_cast<uint32_t>(wq * 32) << 16);
   const uint32_t scol = trow + col_s(grp), pcol = trow + col_p(grp), ocol = trow + col_o(grp);
   const float2 sl2 = make_float2(a.scale_log2, a.scale_log2);
+  const float inv_scale = kLog2e / a.scale_log2;  // D^1/2: the pair bias in units of Q·Kᵀ
+  const float2 bs2 = make_float2(inv_scale, inv_scale);
   const int S = a.stages, KT = a.QT;
   uint32_t u = 0, grp_it = 0, s = 0, ph = 0;
   float m = 0.0f, l = 0.0f;  // reference max (log2 units); row sum (kept here only without ones columns)
@@ -629,7 +652,7 @@ __device__ __forceinline__ void fwd_softmax(const FwdArgs& a, uint8_t* base, con
       const bool last = (meta & kTileLast) != 0;
       if (!mbar_wait_warp_inl(smem_u32(&bars->s_full[grp]), u & 1, g)) { ok = false; break; }
       tc_fence_after();
-      const float* b1 = reinterpret_cast<const float*>(base + lay.b1[s]);  // (with a pair bias)
+      const float* b1 = reinterpret_cast<const float*>(base + lay.b1[s]);  // (where the softmax adds the mask)
       const uint8_t* b2t =
           base + (B2 == kB2Resident ? lay.b2r + (grp * KT + jt) * 32768u : lay.b2s[s] + grp * 32768u);
       // S in two 64-column loads: the second is in flight while the first half is scored
@@ -642,15 +665,15 @@ __device__ __forceinline__ void fwd_softmax(const FwdArgs& a, uint8_t* base, con
       tmem_ld64(scol, ya);
       tmem_wait_ld(ya);
       tmem_ld64(scol + 64, yb);
-      chunk_scores<BF16, kHasB2>(y0, b1, b2t, 0, r, sl2, mt);
-      chunk_scores<BF16, kHasB2>(y1, b1 + 32, b2t, 4, r, sl2, mt);
+      chunk_scores<BF16, kHasB2, kFold>(y0, b1, b2t, 0, r, sl2, bs2, mt);
+      chunk_scores<BF16, kHasB2, kFold>(y1, b1 + 32, b2t, 4, r, sl2, bs2, mt);
       tmem_wait_ld(yb);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&bars->s_free[grp]));  // S may be overwritten
-      chunk_scores<BF16, kHasB2>(y2, b1 + 64, b2t + 16384, 0, r, sl2, mt);
-      chunk_scores<BF16, kHasB2>(y3, b1 + 96, b2t + 16384, 4, r, sl2, mt);
-      if (!kHasB2) mt *= a.scale_log2;  // to the log2 units of the reference max (a positive factor keeps the max)
+      chunk_scores<BF16, kHasB2, kFold>(y2, b1 + 64, b2t + 16384, 0, r, sl2, bs2, mt);
+      chunk_scores<BF16, kHasB2, kFold>(y3, b1 + 96, b2t + 16384, 4, r, sl2, bs2, mt);
+      if (kFold) mt *= a.scale_log2;  // to the log2 units of the reference max (a positive factor keeps the max)
       __syncwarp();
       if (lane == 0) {  // the stage's bias data are no longer read by this warp
         mbar_arrive(smem_u32(&bars->kv_empty[s]));
@@ -676,11 +699,11 @@ __device__ __forceinline__ void fwd_softmax(const FwdArgs& a, uint8_t* base, con
         uint32_t pp[32];
         uint32_t(&p0)[16] = *reinterpret_cast<uint32_t(*)[16]>(&pp[0]);
         uint32_t(&p1)[16] = *reinterpret_cast<uint32_t(*)[16]>(&pp[16]);
-        chunk_probs<BF16, kRowSum, !kHasB2>(y0, sl2, m, p0, rs);
-        chunk_probs<BF16, kRowSum, !kHasB2>(y1, sl2, m, p1, rs);
+        chunk_probs<BF16, kRowSum, kFold>(y0, sl2, m, p0, rs);
+        chunk_probs<BF16, kRowSum, kFold>(y1, sl2, m, p1, rs);
         tmem_st32(pcol, pp);
-        chunk_probs<BF16, kRowSum, !kHasB2>(y2, sl2, m, p0, rs);
-        chunk_probs<BF16, kRowSum, !kHasB2>(y3, sl2, m, p1, rs);
+        chunk_probs<BF16, kRowSum, kFold>(y2, sl2, m, p0, rs);
+        chunk_probs<BF16, kRowSum, kFold>(y3, sl2, m, p1, rs);
         tmem_st32(pcol + 32, pp);
       }
       __syncwarp();
@@ -721,7 +744,7 @@ template <int DP, bool BF16, int B2, bool SKIP>
 __global__ void __launch_bounds__(kThreads, 1) evo_fwd_kernel(const __grid_constant__ FwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const FwdLayout<DP> lay(B2, a.stages, a.QT);
+  const FwdLayout<DP> lay(B2, a.stages, a.QT, BF16);
   FwdBars* bars = reinterpret_cast<FwdBars*>(base + lay.bars);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long i0 = static_cast<long long>(blockIdx.x) * a.chunk;
@@ -794,7 +817,7 @@ constexpr size_t kMaxSmem = 232448;  // 227 KB opt-in limit per block
 
 template <int DP, bool BF16, int B2, bool SKIP>
 cudaError_t launch_fwd_s(FwdArgs a, cudaStream_t st) {
-  const FwdLayout<DP> lay(B2, a.stages, a.QT);
+  const FwdLayout<DP> lay(B2, a.stages, a.QT, BF16);
   // At least 116 KB so that two CTAs never share an SM: each allocates all 512
   // TMEM columns, and a second resident CTA would stall in tcgen05.alloc.
   const size_t smem = (lay.total + 1024 > 116u * 1024u) ? lay.total + 1024 : 116u * 1024u;
@@ -819,7 +842,7 @@ cudaError_t launch_fwd_t(FwdArgs a, cudaStream_t st) {
 // query tiles' pair-bias tiles do not fit (D = 64), the single-tile kernel runs.
 template <int DP, bool BF16>
 cudaError_t launch_fwd_d(FwdArgs a, cudaStream_t st) {
-  auto fits = [&](int kind, int stages) { return FwdLayout<DP>(kind, stages, a.QT).total + 1024 <= kMaxSmem; };
+  auto fits = [&](int kind, int stages) { return FwdLayout<DP>(kind, stages, a.QT, BF16).total + 1024 <= kMaxSmem; };
   a.NP = (a.QT + 1) / 2;
   a.items = static_cast<long long>(a.B) * a.H * a.N * a.NP;
   if (a.bias2_mode == kBias2None) {
