@@ -703,11 +703,13 @@ __device__ __forceinline__ void fwd_softmax(const FwdArgs& a, uint8_t* base, con
         chunk_probs<BF16, kRowSum, kFold>(y1, sl2, m, p1, rs);
         tmem_st32(pcol, pp);
         chunk_probs<BF16, kRowSum, kFold>(y2, sl2, m, p0, rs);
+        // the other group's turn begins with this tile's last quarter (the turns only share
+        // out the exponential unit; nothing in either group's data depends on them)
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bars->turn[grp ^ 1]));
         chunk_probs<BF16, kRowSum, kFold>(y3, sl2, m, p1, rs);
         tmem_st32(pcol + 32, pp);
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&bars->turn[grp ^ 1]));
       // The accumulator of the previous tiles (complete: p_empty) is rescaled before this
       // tile's P·V adds to it (that P·V waits for p_full below).
       if (!first && __any_sync(0xffffffffu, resc)) {
