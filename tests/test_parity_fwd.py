@@ -90,6 +90,35 @@ def test_fully_masked_rows_bf16_no_nan():
     assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("pair", [False, True], ids=["no_pair_bias", "pair_bias"])
+@pytest.mark.parametrize("D", [16, 32, 64])
+def test_real_valued_key_bias(dtype, pair, D):
+    """bias1 as a general additive bias (page §3.5: any bias broadcast over heads and queries),
+    not only 0 or masked: real values of a few tens next to masked keys.  Where the score MMA
+    adds the key bias it carries the bias in three bf16 parts, which together hold the full
+    fp32 value; one part alone would be off by ~2^-9 of the bias, several percent of P here."""
+    inp = make_inputs(1, 3, 200, 2, D, dtype=dtype, mask=("random", 0.1), bias2_sigma=1.0 if pair else None,
+                      seed=21)
+    b1 = inp["bias1"].float()
+    gen = torch.Generator().manual_seed(5)
+    cont = torch.randn(b1.shape, generator=gen) * 12.0
+    inp["bias1"] = torch.where(b1 == 0, cont, b1).to(inp["q"].dtype)  # masked keys stay masked
+    tdt = torch.float16 if dtype == "fp16" else torch.bfloat16
+    _compare(inp, tdt)
+    # and the backward, which adds the key bias itself
+    from memory_efficient_biased_gb300 import evo_attn as E
+    from tests.parity_util import GRAD_TOL, rel_l2
+    d = to_dev(inp)
+    out, lse = E.evo_attn_fwd(d["q"], d["k"], d["v"], d["bias1"], d["bias2"])
+    dq, dk, dv, _ = E.evo_attn_bwd(d["q"], d["k"], d["v"], d["bias1"], d["bias2"], out, lse, d["do"])
+    assert E.evo_attn_device_status() == 0
+    a = {k: np64(v) for k, v in inp.items()}
+    g = O.backward(a["q"], a["k"], a["v"], a["bias1"], a["bias2"], a["do"])
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        assert rel_l2(np64(t), g[name]) <= GRAD_TOL[tdt], name
+
+
 @pytest.mark.parametrize("name,dtype", [("tiny", "fp16"), ("msa_row", "fp16"), ("msa_row", "bf16"),
                                         ("many_head", "bf16")])
 def test_workload_full(name, dtype):
